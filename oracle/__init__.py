@@ -1,0 +1,177 @@
+"""FP64 CPU oracle for the SAMU mixer and the RG-LRU scan (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline leg may import this package; the product path never does.  The C
+source ``oracle.c`` is the plain sequential definition of the equations on the
+SAMU GPU page (section 05 for SAMU, section 04 for RG-LRU) and shares no code
+with the CUDA library.
+
+Every function takes float64 numpy arrays in the layouts documented in
+``oracle.c`` and returns float64 results.  Parity status: every function here
+is pinned by ``tests/test_oracle_pins.py`` (closed forms, special cases,
+invariants, finite differences, the pages' printed parameter counts).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    ):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+             "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            i = ctypes.c_int
+            d = ctypes.c_double
+            lib.oracle_samu_forward.argtypes = [i, i, i, dp, dp, dp, u8p, dp, dp, dp, dp, d, d, dp, dp, dp]
+            lib.oracle_samu_forward.restype = None
+            lib.oracle_samu_backward.argtypes = [i, i, i, dp, dp, dp, u8p, dp, dp, dp, dp, d, d,
+                                                 dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_samu_backward.restype = None
+            lib.oracle_rglru_forward.argtypes = [i, i, i, dp, dp, dp, dp, dp, u8p, dp, dp]
+            lib.oracle_rglru_forward.restype = None
+            lib.oracle_rglru_backward.argtypes = [i, i, i, dp, dp, dp, dp, dp, u8p, dp, dp,
+                                                  dp, dp, dp, dp, dp]
+            lib.oracle_rglru_backward.restype = None
+            lib.oracle_bf16_rne_array.argtypes = [dp, ctypes.POINTER(ctypes.c_uint16), ctypes.c_long]
+            lib.oracle_bf16_rne_array.restype = None
+            _lib = lib
+    return _lib
+
+
+def _dptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _u8(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _u8ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def bf16_rne(v) -> np.ndarray:
+    """Round float64 values to bfloat16 (ties to even) directly; returns uint16 bit patterns."""
+    lib = _load()
+    v = _f64(v)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib.oracle_bf16_rne_array(_dptr(v), out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), v.size)
+    return out
+
+
+def samu_forward(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r):
+    """SAMU mixer forward.  x_sel, w: [B,L,D]; h0: [B,M,2] or None; reset: [B,L] or None.
+
+    Returns dict(y=[B,L,D], hT=[B,M,2], ctrl=[B,L,5] with columns p, r, E, C, S).
+    """
+    lib = _load()
+    x_sel, w = _f64(x_sel), _f64(w)
+    B, L, D = x_sel.shape
+    M = D // 2
+    h0, reset = _f64(h0), _u8(reset)
+    nu, theta, w_phi, w_r = _f64(nu), _f64(theta), _f64(w_phi), _f64(w_r)
+    y = np.empty((B, L, D))
+    hT = np.empty((B, M, 2))
+    ctrl = np.empty((B, L, 5))
+    lib.oracle_samu_forward(B, L, D, _dptr(x_sel), _dptr(w), _dptr(h0), _u8ptr(reset),
+                            _dptr(nu), _dptr(theta), _dptr(w_phi), _dptr(w_r),
+                            float(a_phi), float(a_r), _dptr(y), _dptr(hT), _dptr(ctrl))
+    return {"y": y, "hT": hT, "ctrl": ctrl}
+
+
+def samu_backward(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r, dy, dhT):
+    """SAMU mixer backward (hand-derived adjoint).  dhT may be None (zero).
+
+    Returns dict(dx_sel, dw, dh0, dnu, dtheta, dw_phi, dw_r, da_phi, da_r).
+    """
+    lib = _load()
+    x_sel, w, dy = _f64(x_sel), _f64(w), _f64(dy)
+    B, L, D = x_sel.shape
+    M = D // 2
+    h0, reset, dhT = _f64(h0), _u8(reset), _f64(dhT)
+    nu, theta, w_phi, w_r = _f64(nu), _f64(theta), _f64(w_phi), _f64(w_r)
+    out = {
+        "dx_sel": np.empty((B, L, D)), "dw": np.empty((B, L, D)), "dh0": np.empty((B, M, 2)),
+        "dnu": np.empty(M), "dtheta": np.empty(M), "dw_phi": np.empty(D + 1), "dw_r": np.empty(D + 1),
+    }
+    da_phi = ctypes.c_double(0.0)
+    da_r = ctypes.c_double(0.0)
+    lib.oracle_samu_backward(B, L, D, _dptr(x_sel), _dptr(w), _dptr(h0), _u8ptr(reset),
+                             _dptr(nu), _dptr(theta), _dptr(w_phi), _dptr(w_r),
+                             float(a_phi), float(a_r), _dptr(dy), _dptr(dhT),
+                             _dptr(out["dx_sel"]), _dptr(out["dw"]), _dptr(out["dh0"]),
+                             _dptr(out["dnu"]), _dptr(out["dtheta"]),
+                             _dptr(out["dw_phi"]), _dptr(out["dw_r"]),
+                             ctypes.byref(da_phi), ctypes.byref(da_r))
+    out["da_phi"] = da_phi.value
+    out["da_r"] = da_r.value
+    return out
+
+
+def rglru_forward(x, lx, la, alpha, h0, reset):
+    """RG-LRU forward.  x, lx, la: [B,L,D]; alpha: [D]; h0: [B,D] or None.  Returns dict(y, hT)."""
+    lib = _load()
+    x, lx, la = _f64(x), _f64(lx), _f64(la)
+    B, L, D = x.shape
+    alpha, h0, reset = _f64(alpha), _f64(h0), _u8(reset)
+    y = np.empty((B, L, D))
+    hT = np.empty((B, D))
+    lib.oracle_rglru_forward(B, L, D, _dptr(x), _dptr(lx), _dptr(la), _dptr(alpha), _dptr(h0),
+                             _u8ptr(reset), _dptr(y), _dptr(hT))
+    return {"y": y, "hT": hT}
+
+
+def rglru_backward(x, lx, la, alpha, h0, reset, dy, dhT):
+    """RG-LRU backward.  Returns dict(dx, dlx, dla, dalpha, dh0)."""
+    lib = _load()
+    x, lx, la, dy = _f64(x), _f64(lx), _f64(la), _f64(dy)
+    B, L, D = x.shape
+    alpha, h0, reset, dhT = _f64(alpha), _f64(h0), _u8(reset), _f64(dhT)
+    out = {"dx": np.empty((B, L, D)), "dlx": np.empty((B, L, D)), "dla": np.empty((B, L, D)),
+           "dalpha": np.empty(D), "dh0": np.empty((B, D))}
+    lib.oracle_rglru_backward(B, L, D, _dptr(x), _dptr(lx), _dptr(la), _dptr(alpha), _dptr(h0),
+                              _u8ptr(reset), _dptr(dy), _dptr(dhT),
+                              _dptr(out["dx"]), _dptr(out["dlx"]), _dptr(out["dla"]),
+                              _dptr(out["dalpha"]), _dptr(out["dh0"]))
+    return out

@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""SAMU mixer forward+backward benchmark on GB300 (one JSON line on rank 0).
+
+One step = samu_forward + samu_backward (BF16 gradients) through the C ABI on
+the B=1, L=32768, D=2048 workload (the metric's configuration), inputs
+resident in HBM.  L2 is flushed (256 MiB memset) before every timed step and
+each step is timed with its own CUDA events; the memset is outside the timed
+events.  Alongside the device-timed value the line carries:
+  e2e          the same metric through the public Python API with host (pinned)
+               inputs copied in and results copied out inside the timed region;
+  roofline     the dominant kernel's algorithmic bytes / its average CUDA-event
+               duration (events recorded by the library on the launching stream)
+               against the measured HBM copy bandwidth;
+  cpu_baseline the FP64 oracle timed on the host (rank 0, N=1) on a bounded sample;
+  clocks       nvidia-smi samples taken during the timed region.
+
+--impl reference times the oracle itself (CPU) on the same metric.
+Multi-GPU (torchrun): every rank runs its own independent batch (weak scaling,
+no collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SAMU mixer F+B ms & Mtok/s (B1,L32K,D2048); achieved HBM GB/s vs GB300 peak"
+UNIT = "Mtok/s"
+DEFAULT_WORKLOAD = "width_2048"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+# Algorithmic bytes per launch, in units of B*L*D (one BF16 [B,L,D] tensor = 2 units):
+#   controller forward: read x_sel (2)            scan forward: read w, write y (4)
+#   scan backward: read dy, w, write dw (6)       controller backward: read x_sel, write dx_sel (4)
+KERNEL_BYTES_PER_BLD = {
+    "samu_ctrl_fwd_kernel": 2.0, "samu_scan_fwd_kernel": 4.0,
+    "samu_scan_bwd_kernel": 6.0, "samu_ctrl_bwd_kernel": 4.0,
+}
+STEP_BYTES_PER_BLD = 16.0
+LAUNCHES_PER_RECORD = {"samu_params_kernels": 3, "rglru_alpha_kernels": 2}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own independent batch (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (timing); identity on a single process."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_recurrence_sequence_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_traffic(kernel: str, bld: int):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel sources
+    are unchanged since it was taken; scaled by the units processed."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_sha") != source_hash():
+        return None
+    return float(rec["dram_bytes_per_bld"]) * bld
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index_or_uuid):
+        self.sel = device_index_or_uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(self.sel)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_selector(device):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(device).uuid
+        return "GPU-" + str(u)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        first = vis.split(",")[0] if vis else "0"
+        return first if first.isdigit() else 0
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample_time(B, L, D, seed=0):
+    """Seconds for one FP64 oracle forward+backward on a [B, L, D] SAMU sample."""
+    import oracle
+    from linear_recurrence_sequence_gb300 import synth
+    inp = synth.samu_inputs(B, L, D, seed, h0=False)
+    f64 = synth.bf16_bits_to_f64
+    x, w, dy = f64(inp["x_sel"]), f64(inp["w"]), f64(inp["dy"])
+    args = (x, w, inp["h0"], inp["reset"], inp["nu"], inp["theta"], inp["w_phi"], inp["w_r"],
+            float(inp["a_phi"]), float(inp["a_r"]))
+    t0 = time.perf_counter()
+    oracle.samu_forward(*args)
+    oracle.samu_backward(*args, dy, inp["dhT"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(D, target_s=12.0):
+    """The oracle as it stands (single thread), on a bounded sample of the
+    workload: B=1, D of the workload, L sized for roughly target_s seconds."""
+    t_small = oracle_sample_time(1, 256, D)
+    per_tok = t_small / 256
+    L = int(min(32768, max(512, target_s / max(per_tok, 1e-9))))
+    L = max(512, (L // 256) * 256)
+    t = oracle_sample_time(1, L, D, seed=1)
+    return {"value": L / t / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one FP64 forward+backward at B=1, L={L}, D={D} (single thread), {t:.1f} s"}
+
+
+def run_reference(args):
+    """Times the oracle itself: each step is one bounded sample of the workload."""
+    from linear_recurrence_sequence_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    D = wl.D
+    per_step_budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    t_small = oracle_sample_time(1, 128, D)
+    L = int(max(64, min(wl.L, per_step_budget / max(t_small / 128, 1e-9))))
+    L = max(64, (L // 64) * 64)
+    for _ in range(args.warmup):
+        oracle_sample_time(1, L, D)
+    times = [oracle_sample_time(1, L, D, seed=s) for s in range(args.steps)]
+    total = sum(times)
+    value = args.steps * L / total / 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"samu_fb_B{wl.B}_L{wl.L}_D{wl.D}", "B": wl.B, "L": wl.L, "D": wl.D,
+                   "sample_per_step": f"B=1, L={L}, D={D}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step one FP64 forward+backward at B=1, L={L}, D={D}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from linear_recurrence_sequence_gb300 import api, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    if wl.kind != "samu":
+        raise SystemExit("bench.py times the SAMU mixer workloads")
+    B, L, D = wl.B, wl.L, wl.D
+    M = D // 2
+    BLD = B * L * D
+    inp = wl.make(shard_seed(wl.seeds[0], rank))
+    t = api.samu_tensors_from_numpy(inp, dev)
+    nsaved, nscratch = api.samu_workspace_bytes(B, L, D)
+    saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    fo = {"y": torch.empty((B, L, D), dtype=torch.bfloat16, device=dev),
+          "hT": torch.empty((B, M, 2), dtype=torch.float32, device=dev)}
+    go = {k: None for k in ("dx_sel", "dw", "dh0", "dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r")}
+    go["dx_sel"] = torch.empty((B, L, D), dtype=torch.bfloat16, device=dev)
+    go["dw"] = torch.empty((B, L, D), dtype=torch.bfloat16, device=dev)
+
+    def step(x_sel, w, dy):
+        api.samu_forward(x_sel, w, t["h0"], t["reset"], t["nu"], t["theta"], t["w_phi"], t["w_r"],
+                         t["a_phi"], t["a_r"], out=fo, saved=saved, scratch=scratch)
+        return api.samu_backward(dy, t["dhT"], x_sel, w, t["h0"], t["reset"], t["nu"], t["theta"],
+                                 t["w_phi"], t["w_r"], t["a_phi"], t["a_r"], saved, out=go,
+                                 scratch=scratch)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(t["x_sel"], t["w"], t["dy"])
+    torch.cuda.synchronize(dev)
+    if api.device_status(scratch) != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_selector(dev))
+    sampler.start()
+    time.sleep(0.1)
+    cap = K * 8
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    api.profile_begin(cap)
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record()
+        step(t["x_sel"], t["w"], t["dy"])
+        ev1[i].record()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    records, n_launch_records = api.profile_end(cap)
+    clocks = sampler.stop()
+    if api.device_status(scratch) != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+    total_ms = reduce_max(sum(step_ms), world, dev)
+    ms_per_step = total_ms / K
+    value = world * B * L * K / (total_ms / 1e3) / 1e6
+
+    # per-kernel averages and the dominant kernel's roofline
+    per = {}
+    launches = 0
+    for name, ms in records:
+        per.setdefault(name, []).append(ms)
+        launches += LAUNCHES_PER_RECORD.get(name, 1)
+    avg = {k: sum(v) / len(v) for k, v in per.items()}
+    dom = max((k for k in avg if k in KERNEL_BYTES_PER_BLD), key=lambda k: avg[k] * len(per[k]))
+    peak, peak_src = load_peak()
+    alg = KERNEL_BYTES_PER_BLD[dom] * BLD
+    achieved = alg / (avg[dom] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": load_traffic(dom, BLD), "algorithmic_bytes": alg,
+                "avg_launch_ms": round(avg[dom], 5)}
+
+    # end to end through the public API with pinned host buffers
+    K2 = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 50))
+    hx = t["x_sel"].cpu().pin_memory()
+    hw = t["w"].cpu().pin_memory()
+    hdy = t["dy"].cpu().pin_memory()
+    dx_, dw_, ddy_ = torch.empty_like(t["x_sel"]), torch.empty_like(t["w"]), torch.empty_like(t["dy"])
+    hy = torch.empty((B, L, D), dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty((B, L, D), dtype=torch.bfloat16).pin_memory()
+    hdw = torch.empty((B, L, D), dtype=torch.bfloat16).pin_memory()
+    small_keys = ("dh0", "dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r")
+    hsmall = {}
+    h2d = 3 * BLD * 2
+    d2h = 3 * BLD * 2 + 4 * (B * M * 2)
+    e2e_ms = 0.0
+    for i in range(K2 + 1):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dx_.copy_(hx, non_blocking=True)
+        dw_.copy_(hw, non_blocking=True)
+        ddy_.copy_(hdy, non_blocking=True)
+        g = step(dx_, dw_, ddy_)
+        hy.copy_(fo["y"], non_blocking=True)
+        hdx.copy_(g["dx_sel"], non_blocking=True)
+        hdw.copy_(g["dw"], non_blocking=True)
+        for k in small_keys:
+            hsmall[k] = g[k].to("cpu", non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i > 0:                     # the first pass pins/warms the copy path
+            e2e_ms += e0.elapsed_time(e1)
+    d2h += sum(v.numel() * 4 for k, v in hsmall.items() if k != "dh0")
+    e2e_ms = reduce_max(e2e_ms, world, dev)
+    e2e_value = world * B * L * K2 / (e2e_ms / 1e3) / 1e6
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"samu_fb_B{B}_L{L}_D{D}", "B": B, "L": L, "D": D, "grad_dtype": "bf16",
+                   "h0": wl.h0, "reset_p": wl.reset_p, "seed": shard_seed(wl.seeds[0], rank),
+                   "l2": "flushed before every timed step (256 MiB memset outside the step events)",
+                   "per_gpu_batch": B},
+        "achieved_step_gbs": round(STEP_BYTES_PER_BLD * BLD / (ms_per_step / 1e3) / 1e9, 1),
+        "roofline": roofline,
+        "kernels_avg_ms": {k: round(v, 5) for k, v in sorted(avg.items())},
+        "gpu_launches": launches,
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K2},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(D)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        run_reference(args)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

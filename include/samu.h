@@ -1,0 +1,204 @@
+/*
+ * samu.h — C ABI of the GB300 (sm_103a) chunked affine scan library for the
+ * SAMU recurrent mixer and the real RG-LRU scan.
+ *
+ * Sources (cited by page title and section):
+ *   [SAMU page]  "SAMU 与 RG-LRU 的 H800 训练性能对比" (SAMU_GPU index page):
+ *                section 05 "SAMU 在 GPU 上如何运行" — controller, transition
+ *                lambda_{t,m}, complex recurrence, affine composition, forward
+ *                and reverse (conjugate) passes, shared-control reduction;
+ *                section 04 "RG-LRU 在 GPU 上如何运行" — gates, recurrence,
+ *                reset rule, backward; section 02 glossary — "前向+反向" scope
+ *                (backward returns the input, initial-state and all parameter
+ *                gradients from a dense output cotangent).
+ *   [Protocol]   "Griffin 第 4、5 节 H800 对照协议", "SAMU 的固定方程" (M complex
+ *                modes = 2M real states, wide branch split into real and
+ *                imaginary parts) and "RG-LRU 的固定方程" (segment start cuts
+ *                the old state and cancels the normaliser).
+ *   [Report]     "SAMU strengthened-baseline H800 report", "Reverse complex
+ *                backward" (two shared controller-gradient partials per token,
+ *                deterministic FP32 second stage).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA
+ *    storage), row-major, contiguous, at least 16-byte aligned.
+ *  - Shapes: B batch, L sequence length, D real state width, M = D / 2 complex
+ *    modes.  [B,L,D] tensors put the real part of mode m in channel m and its
+ *    imaginary part in channel M + m ("halves" layout).
+ *  - BF16 tensors are passed as `const void*` / `void*` (IEEE bfloat16 bits).
+ *    Complex FP32 states ([B,M,2]) are interleaved (re, im).
+ *  - Ownership: the caller allocates every buffer, including `saved` (written
+ *    by the forward, read by the backward) and `scratch`; sizes come from the
+ *    *_workspace_bytes query.  The library never allocates, never frees and
+ *    never synchronises the stream.
+ *  - Every call is asynchronous on `stream`; outputs are overwritten, never
+ *    accumulated.  A scratch buffer must not be used by two calls that may
+ *    run concurrently.  `saved` must come from a forward with the same inputs.
+ *  - Errors: the return value is a status code (LRS_OK = 0).  Argument checks
+ *    happen on the host before anything is launched.  A device-side bounded
+ *    wait that gives up is recorded in the scratch status word and reported by
+ *    lrs_device_status() (LRS_ERR_TIMEOUT); the affected outputs are then
+ *    undefined.  No C++ exception crosses this ABI.
+ *  - Supported shapes: B >= 1, L >= 1.  SAMU: D % 16 == 0 and D <= 4096;
+ *    RG-LRU: D % 8 == 0 (every measured width satisfies both).  Other even D
+ *    return LRS_ERR_UNSUPPORTED: the tiles are fetched by TMA, whose innermost
+ *    box coordinate must fall on a 16-byte boundary.
+ */
+#ifndef LRS_SAMU_H
+#define LRS_SAMU_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define LRS_OK 0
+#define LRS_ERR_ARG 1          /* null pointer, bad shape, misaligned pointer */
+#define LRS_ERR_UNSUPPORTED 2  /* valid but unsupported shape (see "Supported shapes") */
+#define LRS_ERR_CUDA 3         /* a kernel launch or memset failed */
+#define LRS_ERR_TIMEOUT 4      /* a bounded device-side wait gave up */
+
+/* Gradient output dtype selector for the backward calls. */
+#define LRS_GRAD_BF16 0
+#define LRS_GRAD_FP32 1
+
+/* Human-readable text for a status code (static storage). */
+const char* lrs_status_string(int status);
+
+/* ABI version (major * 100 + minor). */
+int lrs_version(void);
+
+/* Reads the device status word kept in `scratch` (a buffer last used by one
+ * of the calls below; every call clears the word when it starts, so it covers
+ * the most recent call).  SYNCHRONISES `stream`.  *status receives LRS_OK or
+ * LRS_ERR_TIMEOUT.  Returns LRS_ERR_ARG / LRS_ERR_CUDA on failure. */
+int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
+
+/* Opt-in per-kernel timing for benchmarks (not needed for computing).
+ * lrs_profile_begin creates (once) `capacity` pairs of CUDA events and, until
+ * lrs_profile_end, records one pair on the launching stream around every
+ * kernel that the calls below launch (at most `capacity`).  lrs_profile_end
+ * waits for the recorded events and writes, for the first min(count,
+ * capacity) kernels, their id (1 prep, 2 controller forward, 3 SAMU scan
+ * forward, 4 SAMU scan backward, 5 controller backward, 6 SAMU parameter
+ * reductions, 7 RG-LRU scan forward, 8 RG-LRU scan backward, 9 RG-LRU alpha
+ * reduction) and duration in milliseconds; *count receives the number of
+ * kernels launched while profiling was on.  Not thread-safe: one profiling
+ * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),
+ * LRS_ERR_CUDA. */
+int lrs_profile_begin(int capacity);
+int lrs_profile_end(int* kernel_ids, float* ms, int capacity, int* count);
+
+/* ======================================================================== */
+/* SAMU mixer                                                                */
+/* ======================================================================== */
+
+/* Bytes of the caller-owned `saved` buffer (forward -> backward) and of the
+ * `scratch` buffer for problems of shape (B, L, D).  Either output pointer may
+ * be NULL.  Pure host function. */
+int samu_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes);
+
+/* SAMU mixer forward ([SAMU page] section 05, forward):
+ *   x~_t = [x_sel_t; 1]; w^_phi = w_phi/||w_phi||, w^_r = w_r/||w_r|| (norms over
+ *   all D+1 entries); p_t = tanh(x~_t . w^_phi), r_t = tanh(x~_t . w^_r);
+ *   d_t = tanh(a_phi)/sqrt(M) p_t; c_t = tanh(a_r)/sqrt(M) r_t/(1+r_t^2);
+ *   E_t = e^{c_t}, C_t = cos d_t, S_t = sin d_t (once per token);
+ *   lambda_{t,m} = e^{-nu_m E_t} [(cos th_m C_t - sin th_m S_t) + i(sin th_m C_t + cos th_m S_t)]
+ *   (lambda = 0 where reset[b,t] != 0);
+ *   z_{t,m} = lambda_{t,m} z_{t-1,m} + b_{t,m},  b_{t,m} = w[t,m] + i w[t,M+m],  z_{-1} = h0;
+ *   y_t = z_t in the halves layout;  hT = z_{L-1}.
+ *
+ *   x_sel, w   [B,L,D] BF16 (in)
+ *   h0         [B,M,2] FP32 (in) or NULL for zero
+ *   reset      [B,L] uint8, nonzero = segment start (in) or NULL for none
+ *   nu, theta  [M] FP32 (in);  w_phi, w_r [D+1] FP32 (in; last entry = bias)
+ *   a_phi, a_r device pointers to one FP32 each (in)
+ *   y          [B,L,D] BF16 (out, round to nearest even from the FP32 state)
+ *   y32        [B,L,D] FP32 (out, optional: the pre-rounding value) or NULL
+ *   hT         [B,M,2] FP32 (out)
+ *   saved      samu_workspace_bytes().saved bytes (out: controller cache p, r,
+ *              E/C/S, normalised directions and chunk entry states)
+ *   scratch    samu_workspace_bytes().scratch bytes (temporary)
+ * Errors: LRS_ERR_ARG for a NULL required pointer, non-positive shape, odd D,
+ * or a tensor pointer not 16-byte aligned; LRS_ERR_UNSUPPORTED for
+ * D % 16 != 0 or D > 4096; LRS_ERR_CUDA if a launch fails. */
+int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_t* reset,
+                 const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                 const float* a_phi, const float* a_r, int B, int L, int D,
+                 void* y, float* y32, float* hT, void* saved, void* scratch,
+                 cudaStream_t stream);
+
+/* SAMU mixer backward ([SAMU page] section 05, backward; [Report] "Reverse
+ * complex backward"): the conjugate reverse scan zbar_{t-1} += conj(lambda_t)
+ * zbar_t with bbar_t = zbar_t, the per-token shared-control gradients
+ * cbar_t = sum_m cbar_{t,m}, dbar_t = sum_m dbar_{t,m} (two FP32 partials per
+ * mode slice, reduced in a fixed order), and the controller chain rule down to
+ * x_sel and the parameters.
+ *
+ *   dy          [B,L,D] BF16 dense output cotangent (in)
+ *   dhT         [B,M,2] FP32 cotangent of hT (in) or NULL for zero
+ *   x_sel ... a_r, B, L, D: exactly the forward's inputs (in)
+ *   saved       the forward's saved buffer (in)
+ *   dx_sel, dw  [B,L,D] (out) in BF16 (grad_dtype = LRS_GRAD_BF16) or FP32
+ *   dh0         [B,M,2] FP32 (out)
+ *   dnu, dtheta [M] FP32 (out);  dw_phi, dw_r [D+1] FP32 (out)
+ *   da_phi, da_r device pointers to one FP32 each (out)
+ *   scratch     as for the forward (temporary)
+ * Parameter gradients are deterministic (fixed reduction order).
+ * Errors: as samu_forward, plus LRS_ERR_ARG for an unknown grad_dtype. */
+int samu_backward(const void* dy, const float* dhT,
+                  const void* x_sel, const void* w, const float* h0, const uint8_t* reset,
+                  const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                  const float* a_phi, const float* a_r, int B, int L, int D,
+                  const void* saved, void* dx_sel, void* dw, int grad_dtype,
+                  float* dh0, float* dnu, float* dtheta, float* dw_phi, float* dw_r,
+                  float* da_phi, float* da_r, void* scratch, cudaStream_t stream);
+
+/* ======================================================================== */
+/* RG-LRU (comparison path on the same engine)                               */
+/* ======================================================================== */
+
+int rglru_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes);
+
+/* RG-LRU forward ([SAMU page] section 04; [Protocol] "RG-LRU 的固定方程"):
+ *   g^x = sigmoid(lx), g^a = sigmoid(la), a_t = exp(-8 g^a softplus(alpha)),
+ *   b_t = x_t g^x sqrt(max(1 - a_t^2, 0)); at a segment start a_t = 0 and the
+ *   normaliser is 1; h_t = a_t h_{t-1} + b_t, h_{-1} = h0; y_t = h_t; hT = h_{L-1}.
+ *
+ *   x, lx, la  [B,L,D] BF16 (in);  alpha [D] FP32 (in)
+ *   h0         [B,D] FP32 (in) or NULL;  reset [B,L] uint8 (in) or NULL
+ *   y          [B,L,D] BF16 (out);  y32 [B,L,D] FP32 (out, optional) or NULL
+ *   hT         [B,D] FP32 (out);  saved, scratch: rglru_workspace_bytes()
+ * Errors: as samu_forward. */
+int rglru_forward(const void* x, const void* lx, const void* la, const float* alpha,
+                  const float* h0, const uint8_t* reset, int B, int L, int D,
+                  void* y, float* y32, float* hT, void* saved, void* scratch,
+                  cudaStream_t stream);
+
+/* RG-LRU backward ([SAMU page] section 04, backward): reverse real affine scan,
+ * gates recomputed, square-root derivative bounded at 1000 (the clipped
+ * derivative of the canonical reference), dalpha reduced over batch and chunks
+ * to [D] in a fixed order.
+ *
+ *   dy [B,L,D] BF16 (in);  dhT [B,D] FP32 (in) or NULL
+ *   x, lx, la, alpha, h0, reset, B, L, D: the forward's inputs (in)
+ *   saved: the forward's saved buffer (in)
+ *   dx, dlx, dla [B,L,D] BF16 or FP32 by grad_dtype (out)
+ *   dalpha [D] FP32 (out);  dh0 [B,D] FP32 (out)
+ * Errors: as samu_backward. */
+int rglru_backward(const void* dy, const float* dhT, const void* x, const void* lx,
+                   const void* la, const float* alpha, const float* h0, const uint8_t* reset,
+                   int B, int L, int D, const void* saved, void* dx, void* dlx, void* dla,
+                   int grad_dtype, float* dalpha, float* dh0, void* scratch,
+                   cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRS_SAMU_H */

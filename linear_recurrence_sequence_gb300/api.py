@@ -1,0 +1,316 @@
+"""Thin Python binding over the C ABI in ``include/samu.h``.
+
+Argument marshalling only: tensors are checked for dtype, device and
+contiguity, their ``data_ptr()`` and the current CUDA stream are handed to the
+shared library, and every step of the computation runs in its CUDA kernels.
+There is no fallback: if ``liblrs_gb300.so`` is missing or fails to load, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "liblrs_gb300.so"
+_lock = threading.Lock()
+_lib = None
+
+LRS_GRAD_BF16 = 0
+LRS_GRAD_FP32 = 1
+
+# names and argument kinds of every exported symbol (checked by the tests)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZP = ctypes.POINTER(ctypes.c_size_t)
+_SIGNATURES = {
+    "lrs_status_string": ([_I], ctypes.c_char_p),
+    "lrs_version": ([], _I),
+    "lrs_device_status": ([_P, ctypes.POINTER(_I), _P], _I),
+    "lrs_profile_begin": ([_I], _I),
+    "lrs_profile_end": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
+    "samu_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
+    "samu_forward": ([_P] * 10 + [_I, _I, _I] + [_P] * 6, _I),
+    "samu_backward": ([_P] * 12 + [_I, _I, _I] + [_P, _P, _P, _I] + [_P] * 9, _I),
+    "rglru_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
+    "rglru_forward": ([_P] * 6 + [_I, _I, _I] + [_P] * 6, _I),
+    "rglru_backward": ([_P] * 8 + [_I, _I, _I] + [_P] * 4 + [_I] + [_P] * 4, _I),
+}
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{_LIB_NAME} is not built ({path}); run __graft_entry__.build() first")
+            lib = ctypes.CDLL(path)
+            for name, (argtypes, restype) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = lib
+    return _lib
+
+
+class LrsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _load().lrs_status_string(status).decode()
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise LrsError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, device, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _opt(t, name, dtype, device, shape=None):
+    return None if t is None else _need(t, name, dtype, device, shape)
+
+
+def _empty(shape, dtype, device, out, key):
+    if out is not None and key in out and out[key] is not None:
+        return _need(out[key], key, dtype, device, shape)
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+# ---------------------------------------------------------------------------
+# SAMU
+# ---------------------------------------------------------------------------
+def samu_workspace_bytes(B: int, L: int, D: int):
+    lib = _load()
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    _check("samu_workspace_bytes", lib.samu_workspace_bytes(B, L, D, ctypes.byref(s), ctypes.byref(c)))
+    return int(s.value), int(c.value)
+
+
+def samu_forward(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r, *, want_y32=False,
+                 out=None, saved=None, scratch=None):
+    """SAMU mixer forward through ``samu_forward``.  Returns dict(y, y32, hT, saved, scratch)."""
+    dev = x_sel.device
+    B, L, D = x_sel.shape
+    M = D // 2
+    _need(x_sel, "x_sel", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev, (B, L, D))
+    _opt(h0, "h0", torch.float32, dev, (B, M, 2))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    _need(nu, "nu", torch.float32, dev, (M,))
+    _need(theta, "theta", torch.float32, dev, (M,))
+    _need(w_phi, "w_phi", torch.float32, dev, (D + 1,))
+    _need(w_r, "w_r", torch.float32, dev, (D + 1,))
+    _need(a_phi, "a_phi", torch.float32, dev, (1,))
+    _need(a_r, "a_r", torch.float32, dev, (1,))
+    nsaved, nscratch = samu_workspace_bytes(B, L, D)
+    y = _empty((B, L, D), torch.bfloat16, dev, out, "y")
+    y32 = _empty((B, L, D), torch.float32, dev, out, "y32") if want_y32 else None
+    hT = _empty((B, M, 2), torch.float32, dev, out, "hT")
+    if saved is None:
+        saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    if saved.numel() < nsaved or scratch.numel() < nscratch:
+        raise ValueError("saved/scratch buffers are too small")
+    st = _load().samu_forward(_ptr(x_sel), _ptr(w), _ptr(h0), _ptr(reset), _ptr(nu), _ptr(theta),
+                              _ptr(w_phi), _ptr(w_r), _ptr(a_phi), _ptr(a_r), B, L, D,
+                              _ptr(y), _ptr(y32), _ptr(hT), _ptr(saved), _ptr(scratch), _stream(dev))
+    _check("samu_forward", st)
+    return {"y": y, "y32": y32, "hT": hT, "saved": saved, "scratch": scratch}
+
+
+def samu_backward(dy, dhT, x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r, saved, *,
+                  grad_fp32=False, out=None, scratch=None):
+    """SAMU mixer backward through ``samu_backward``.
+
+    Returns dict(dx_sel, dw, dh0, dnu, dtheta, dw_phi, dw_r, da_phi, da_r, scratch).
+    """
+    dev = x_sel.device
+    B, L, D = x_sel.shape
+    M = D // 2
+    _need(dy, "dy", torch.bfloat16, dev, (B, L, D))
+    _opt(dhT, "dhT", torch.float32, dev, (B, M, 2))
+    _need(x_sel, "x_sel", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev, (B, L, D))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    nsaved, nscratch = samu_workspace_bytes(B, L, D)
+    if saved is None or saved.numel() < nsaved:
+        raise ValueError("saved must be the forward's saved buffer")
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    gdt = torch.float32 if grad_fp32 else torch.bfloat16
+    o = {
+        "dx_sel": _empty((B, L, D), gdt, dev, out, "dx_sel"),
+        "dw": _empty((B, L, D), gdt, dev, out, "dw"),
+        "dh0": _empty((B, M, 2), torch.float32, dev, out, "dh0"),
+        "dnu": _empty((M,), torch.float32, dev, out, "dnu"),
+        "dtheta": _empty((M,), torch.float32, dev, out, "dtheta"),
+        "dw_phi": _empty((D + 1,), torch.float32, dev, out, "dw_phi"),
+        "dw_r": _empty((D + 1,), torch.float32, dev, out, "dw_r"),
+        "da_phi": _empty((1,), torch.float32, dev, out, "da_phi"),
+        "da_r": _empty((1,), torch.float32, dev, out, "da_r"),
+    }
+    st = _load().samu_backward(_ptr(dy), _ptr(dhT), _ptr(x_sel), _ptr(w), _ptr(h0), _ptr(reset), _ptr(nu),
+                               _ptr(theta), _ptr(w_phi), _ptr(w_r), _ptr(a_phi), _ptr(a_r), B, L, D,
+                               _ptr(saved), _ptr(o["dx_sel"]), _ptr(o["dw"]),
+                               LRS_GRAD_FP32 if grad_fp32 else LRS_GRAD_BF16,
+                               _ptr(o["dh0"]), _ptr(o["dnu"]), _ptr(o["dtheta"]), _ptr(o["dw_phi"]),
+                               _ptr(o["dw_r"]), _ptr(o["da_phi"]), _ptr(o["da_r"]), _ptr(scratch), _stream(dev))
+    _check("samu_backward", st)
+    o["scratch"] = scratch
+    return o
+
+
+# ---------------------------------------------------------------------------
+# RG-LRU
+# ---------------------------------------------------------------------------
+def rglru_workspace_bytes(B: int, L: int, D: int):
+    lib = _load()
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    _check("rglru_workspace_bytes", lib.rglru_workspace_bytes(B, L, D, ctypes.byref(s), ctypes.byref(c)))
+    return int(s.value), int(c.value)
+
+
+def rglru_forward(x, lx, la, alpha, h0, reset, *, want_y32=False, out=None, saved=None, scratch=None):
+    """RG-LRU forward through ``rglru_forward``.  Returns dict(y, y32, hT, saved, scratch)."""
+    dev = x.device
+    B, L, D = x.shape
+    _need(x, "x", torch.bfloat16, dev)
+    _need(lx, "lx", torch.bfloat16, dev, (B, L, D))
+    _need(la, "la", torch.bfloat16, dev, (B, L, D))
+    _need(alpha, "alpha", torch.float32, dev, (D,))
+    _opt(h0, "h0", torch.float32, dev, (B, D))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    nsaved, nscratch = rglru_workspace_bytes(B, L, D)
+    y = _empty((B, L, D), torch.bfloat16, dev, out, "y")
+    y32 = _empty((B, L, D), torch.float32, dev, out, "y32") if want_y32 else None
+    hT = _empty((B, D), torch.float32, dev, out, "hT")
+    if saved is None:
+        saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    st = _load().rglru_forward(_ptr(x), _ptr(lx), _ptr(la), _ptr(alpha), _ptr(h0), _ptr(reset), B, L, D,
+                               _ptr(y), _ptr(y32), _ptr(hT), _ptr(saved), _ptr(scratch), _stream(dev))
+    _check("rglru_forward", st)
+    return {"y": y, "y32": y32, "hT": hT, "saved": saved, "scratch": scratch}
+
+
+def rglru_backward(dy, dhT, x, lx, la, alpha, h0, reset, saved, *, grad_fp32=False, out=None, scratch=None):
+    """RG-LRU backward through ``rglru_backward``.  Returns dict(dx, dlx, dla, dalpha, dh0, scratch)."""
+    dev = x.device
+    B, L, D = x.shape
+    _need(dy, "dy", torch.bfloat16, dev, (B, L, D))
+    _opt(dhT, "dhT", torch.float32, dev, (B, D))
+    nsaved, nscratch = rglru_workspace_bytes(B, L, D)
+    if saved is None or saved.numel() < nsaved:
+        raise ValueError("saved must be the forward's saved buffer")
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    gdt = torch.float32 if grad_fp32 else torch.bfloat16
+    o = {
+        "dx": _empty((B, L, D), gdt, dev, out, "dx"),
+        "dlx": _empty((B, L, D), gdt, dev, out, "dlx"),
+        "dla": _empty((B, L, D), gdt, dev, out, "dla"),
+        "dalpha": _empty((D,), torch.float32, dev, out, "dalpha"),
+        "dh0": _empty((B, D), torch.float32, dev, out, "dh0"),
+    }
+    st = _load().rglru_backward(_ptr(dy), _ptr(dhT), _ptr(x), _ptr(lx), _ptr(la), _ptr(alpha), _ptr(h0),
+                                _ptr(reset), B, L, D, _ptr(saved), _ptr(o["dx"]), _ptr(o["dlx"]), _ptr(o["dla"]),
+                                LRS_GRAD_FP32 if grad_fp32 else LRS_GRAD_BF16,
+                                _ptr(o["dalpha"]), _ptr(o["dh0"]), _ptr(scratch), _stream(dev))
+    _check("rglru_backward", st)
+    o["scratch"] = scratch
+    return o
+
+
+def device_status(scratch, device=None) -> int:
+    """Status word of the most recent call that used ``scratch`` (synchronises the stream)."""
+    dev = scratch.device if device is None else device
+    v = ctypes.c_int(0)
+    _check("lrs_device_status", _load().lrs_device_status(_ptr(scratch), ctypes.byref(v), _stream(dev)))
+    return int(v.value)
+
+
+KERNEL_NAMES = {
+    1: "samu_prep_kernel", 2: "samu_ctrl_fwd_kernel", 3: "samu_scan_fwd_kernel",
+    4: "samu_scan_bwd_kernel", 5: "samu_ctrl_bwd_kernel", 6: "samu_params_kernels",
+    7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
+}
+
+
+def profile_begin(capacity: int) -> None:
+    """Record CUDA events around every library kernel launched until profile_end()."""
+    _check("lrs_profile_begin", _load().lrs_profile_begin(int(capacity)))
+
+
+def profile_end(capacity: int):
+    """Returns (list of (kernel name, ms) for the recorded launches, total launches seen)."""
+    ids = (ctypes.c_int * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = ctypes.c_int(0)
+    _check("lrs_profile_end", _load().lrs_profile_end(ids, ms, capacity, ctypes.byref(n)))
+    k = min(n.value, capacity)
+    return [(KERNEL_NAMES.get(ids[i], str(ids[i])), float(ms[i])) for i in range(k)], int(n.value)
+
+
+# ---------------------------------------------------------------------------
+# numpy (seeded generator output) -> device tensors
+# ---------------------------------------------------------------------------
+def _bf16(bits: np.ndarray, device):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def _f32(a, device):
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32).reshape(np.shape(a) or (1,))).to(device)
+
+
+def samu_tensors_from_numpy(inp: dict, device) -> dict:
+    out = {k: _bf16(inp[k], device) for k in ("x_sel", "w", "dy")}
+    for k in ("nu", "theta", "w_phi", "w_r", "a_phi", "a_r", "h0", "dhT"):
+        out[k] = _f32(inp[k], device)
+    out["reset"] = None if inp["reset"] is None else torch.from_numpy(inp["reset"]).to(device)
+    return out
+
+
+def rglru_tensors_from_numpy(inp: dict, device) -> dict:
+    out = {k: _bf16(inp[k], device) for k in ("x", "lx", "la", "dy")}
+    for k in ("alpha", "h0", "dhT"):
+        out[k] = _f32(inp[k], device)
+    out["reset"] = None if inp["reset"] is None else torch.from_numpy(inp["reset"]).to(device)
+    return out

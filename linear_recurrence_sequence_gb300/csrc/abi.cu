@@ -1,0 +1,423 @@
+// extern "C" entry points declared in include/samu.h: argument checks,
+// workspace carving and kernel launches.  No allocation, no synchronisation
+// (except lrs_device_status, which documents that it synchronises).
+#include <cstdint>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+
+using namespace lrs;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int L, int D) {
+    if (B < 1 || L < 1 || D < 2 || (D & 1)) return LRS_ERR_ARG;
+    const long long BL = (long long)B * L;
+    if (BL * (long long)D > (1LL << 40)) return LRS_ERR_UNSUPPORTED;
+    return LRS_OK;
+}
+
+int check_samu_shape(int B, int L, int D) {
+    int st = check_common(B, L, D);
+    if (st != LRS_OK) return st;
+    if (D % 16 != 0 || D > 4096) return LRS_ERR_UNSUPPORTED;
+    const ScanGeom g = make_geom(B, L, D / 2);
+    if (g.n_tiles > 0x7fffffffLL) return LRS_ERR_UNSUPPORTED;
+    return LRS_OK;
+}
+
+int check_rglru_shape(int B, int L, int D) {
+    int st = check_common(B, L, D);
+    if (st != LRS_OK) return st;
+    if (D % 8 != 0) return LRS_ERR_UNSUPPORTED;
+    const ScanGeom g = make_geom(B, L, D);
+    if (g.n_tiles > 0x7fffffffLL) return LRS_ERR_UNSUPPORTED;
+    return LRS_OK;
+}
+
+// Required pointer: non-null and 16-byte aligned.
+bool req(const void* p) { return p != nullptr && aligned16(p); }
+// Optional pointer: null, or 16-byte aligned.
+bool opt(const void* p) { return p == nullptr || aligned16(p); }
+
+// Opt-in per-kernel event timing (lrs_profile_*): a fixed pool of CUDA event
+// pairs recorded on the launching stream around each kernel.
+struct Profiler {
+    bool on = false;
+    int cap = 0;
+    int n = 0;
+    cudaEvent_t* ev = nullptr;   // 2 * cap events
+    int* ids = nullptr;
+} g_prof;
+
+void prof_begin(int id, cudaStream_t s) {
+    if (!g_prof.on || g_prof.n >= g_prof.cap) return;
+    g_prof.ids[g_prof.n] = id;
+    cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
+}
+
+void prof_end(cudaStream_t s) {
+    if (!g_prof.on || g_prof.n >= g_prof.cap) return;
+    cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
+    ++g_prof.n;
+}
+
+// Kernel ids reported by lrs_profile_end.
+enum {
+    KID_SAMU_PREP = 1, KID_SAMU_CTRL_FWD, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
+    KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA
+};
+
+#define LRS_LAUNCH(id, stream, expr)            \
+    do {                                        \
+        prof_begin((id), (stream));             \
+        cudaError_t e_ = (expr);                \
+        prof_end(stream);                       \
+        if (e_ != cudaSuccess) return LRS_ERR_CUDA; \
+    } while (0)
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 3-D tensor map over a contiguous [B, L, D] BF16 tensor with a box of
+// kTile tokens x kGroup channels (rows past L read as zero).
+bool make_bf16_map(CUtensorMap* map, const void* ptr, int B, int L, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * (cuuint64_t)D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kGroup, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <typename T>
+const T* at(const void* base, size_t off) {
+    return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lrs_status_string(int status) {
+    switch (status) {
+        case LRS_OK: return "ok";
+        case LRS_ERR_ARG: return "invalid argument (null or misaligned pointer, bad shape)";
+        case LRS_ERR_UNSUPPORTED: return "unsupported shape";
+        case LRS_ERR_CUDA: return "CUDA launch failed";
+        case LRS_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+        default: return "unknown status";
+    }
+}
+
+int lrs_version(void) { return 100; }
+
+int lrs_profile_begin(int capacity) {
+    if (capacity < 1) return LRS_ERR_ARG;
+    if (g_prof.cap < capacity) {
+        for (int i = 0; i < 2 * g_prof.cap; ++i) cudaEventDestroy(g_prof.ev[i]);
+        delete[] g_prof.ev;
+        delete[] g_prof.ids;
+        g_prof.ev = new cudaEvent_t[2 * capacity];
+        g_prof.ids = new int[capacity];
+        for (int i = 0; i < 2 * capacity; ++i) {
+            if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+                g_prof.cap = 0;
+                return LRS_ERR_CUDA;
+            }
+        }
+        g_prof.cap = capacity;
+    }
+    g_prof.n = 0;
+    g_prof.on = true;
+    return LRS_OK;
+}
+
+int lrs_profile_end(int* kernel_ids, float* ms, int capacity, int* count) {
+    if (count == nullptr) return LRS_ERR_ARG;
+    g_prof.on = false;
+    const int n = g_prof.n < capacity ? g_prof.n : capacity;
+    for (int i = 0; i < n; ++i) {
+        if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) return LRS_ERR_CUDA;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) return LRS_ERR_CUDA;
+        if (kernel_ids) kernel_ids[i] = g_prof.ids[i];
+        if (ms) ms[i] = t;
+    }
+    *count = g_prof.n;
+    return LRS_OK;
+}
+
+int lrs_device_status(void* scratch, int* status, cudaStream_t stream) {
+    if (scratch == nullptr || status == nullptr) return LRS_ERR_ARG;
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return LRS_ERR_CUDA;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return LRS_ERR_CUDA;
+    *status = (v & (kStatusTimeout | kStatusUpstream)) ? LRS_ERR_TIMEOUT : LRS_OK;
+    return LRS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// SAMU
+// ---------------------------------------------------------------------------
+int samu_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes) {
+    const int st = check_samu_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (saved_bytes) *saved_bytes = samu_saved_layout(B, L, D).total;
+    if (scratch_bytes) *scratch_bytes = samu_scratch_layout(B, L, D).total;
+    return LRS_OK;
+}
+
+int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_t* reset,
+                 const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                 const float* a_phi, const float* a_r, int B, int L, int D,
+                 void* y, float* y32, float* hT, void* saved, void* scratch,
+                 cudaStream_t stream) {
+    const int st = check_samu_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (!req(x_sel) || !req(w) || !opt(h0) || !req(nu) || !req(theta) || !req(w_phi) ||
+        !req(w_r) || a_phi == nullptr || a_r == nullptr || !req(y) || !opt(y32) || !req(hT) ||
+        !req(saved) || !req(scratch))
+        return LRS_ERR_ARG;
+    const int M = D / 2;
+    const SamuSaved sv = samu_saved_layout(B, L, D);
+    const SamuScratch sc = samu_scratch_layout(B, L, D);
+    const long long BL = (long long)B * L;
+
+    float* wh = at<float>(saved, sv.wh);
+    float* misc = at<float>(saved, sv.misc);
+    float* p = at<float>(saved, sv.p);
+    float* r = at<float>(saved, sv.r);
+    float4* ctrl = at<float4>(saved, sv.ctrl);
+
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
+    if (e != cudaSuccess) return LRS_ERR_CUDA;
+    float4* modes = at<float4>(saved, sv.modes);
+    LRS_LAUNCH(KID_SAMU_PREP, stream,
+               launch_samu_prep(w_phi, w_r, a_phi, a_r, nu, theta, D, wh, misc, modes, stream));
+    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(x_sel, reset, wh, misc, BL, D, p, r, ctrl, stream));
+
+    CUtensorMap tm_w;
+    if (!make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;
+    SamuScanFwdArgs a;
+    a.g = make_geom(B, L, M);
+    a.ctrl = ctrl;
+    a.modes = modes;
+    a.nu = nu;
+    a.h0 = h0;
+    a.y = static_cast<uint32_t*>(y);
+    a.y32 = y32;
+    a.hT = hT;
+    a.hsub = at<float2>(saved, sv.hsub);
+    a.agg = at<float4>(scratch, sc.agg);
+    a.flags = at<uint32_t>(scratch, sc.flags);
+    a.counter = at<uint32_t>(scratch, sc.status + 4);
+    a.status = at<uint32_t>(scratch, sc.status);
+    LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_scan_fwd(tm_w, a, stream));
+    return LRS_OK;
+}
+
+int samu_backward(const void* dy, const float* dhT,
+                  const void* x_sel, const void* w, const float* h0, const uint8_t* reset,
+                  const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                  const float* a_phi, const float* a_r, int B, int L, int D,
+                  const void* saved, void* dx_sel, void* dw, int grad_dtype,
+                  float* dh0, float* dnu, float* dtheta, float* dw_phi, float* dw_r,
+                  float* da_phi, float* da_r, void* scratch, cudaStream_t stream) {
+    (void)h0;
+    (void)w_phi;
+    (void)w_r;
+    (void)a_phi;
+    (void)a_r;
+    const int st = check_samu_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (grad_dtype != LRS_GRAD_BF16 && grad_dtype != LRS_GRAD_FP32) return LRS_ERR_ARG;
+    if (!req(dy) || !opt(dhT) || !req(x_sel) || !req(w) || !req(nu) || !req(theta) ||
+        !req(saved) || !req(dx_sel) || !req(dw) || !req(dh0) || !req(dnu) || !req(dtheta) ||
+        !req(dw_phi) || !req(dw_r) || da_phi == nullptr || da_r == nullptr || !req(scratch))
+        return LRS_ERR_ARG;
+    const int M = D / 2;
+    const SamuSaved sv = samu_saved_layout(B, L, D);
+    const SamuScratch sc = samu_scratch_layout(B, L, D);
+    const ScanGeom g = make_geom(B, L, M);
+    const int fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
+
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
+    if (e != cudaSuccess) return LRS_ERR_CUDA;
+
+    CUtensorMap tm_dy, tm_w;
+    if (!make_bf16_map(&tm_dy, dy, B, L, D) || !make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;
+    SamuScanBwdArgs s;
+    s.g = g;
+    s.ctrl = at<float4>(saved, sv.ctrl);
+    s.modes = at<float4>(saved, sv.modes);
+    s.nu = nu;
+    s.dhT = dhT;
+    s.hsub = at<float2>(saved, sv.hsub);
+    s.dw = dw;
+    s.grad_fp32 = fp32;
+    s.dh0 = dh0;
+    s.agg = at<float4>(scratch, sc.agg);
+    s.rin = at<float2>(scratch, sc.rin);
+    s.kpart = at<float2>(scratch, sc.kpart);
+    s.numod = at<float2>(scratch, sc.numod);
+    s.flags = at<uint32_t>(scratch, sc.flags);
+    s.counter = at<uint32_t>(scratch, sc.status + 4);
+    s.status = at<uint32_t>(scratch, sc.status);
+    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_scan_bwd(tm_dy, tm_w, s, stream));
+
+    SamuCtrlBwdArgs cb;
+    cb.B = B;
+    cb.L = L;
+    cb.D = D;
+    cb.n_groups = g.n_groups;
+    cb.x = static_cast<const uint4*>(x_sel);
+    cb.kpart = s.kpart;
+    cb.p = at<float>(saved, sv.p);
+    cb.r = at<float>(saved, sv.r);
+    cb.ctrl = s.ctrl;
+    cb.wh = at<float>(saved, sv.wh);
+    cb.misc = at<float>(saved, sv.misc);
+    cb.dx = dx_sel;
+    cb.grad_fp32 = fp32;
+    cb.dwh_part = at<float>(scratch, sc.dwh_part);
+    cb.amp_part = at<float2>(scratch, sc.amp_part);
+    LRS_LAUNCH(KID_SAMU_CTRL_BWD, stream, launch_samu_ctrl_bwd(cb, stream));
+
+    SamuParamArgs pa;
+    pa.B = B;
+    pa.L = L;
+    pa.D = D;
+    pa.CT = g.CT;
+    pa.numod = at<float2>(scratch, sc.numod);
+    pa.numod2 = at<float2>(scratch, sc.numod2);
+    pa.dwh_part = cb.dwh_part;
+    pa.amp_part = cb.amp_part;
+    pa.dwh = at<float>(scratch, sc.dwh);
+    pa.wh = cb.wh;
+    pa.misc = cb.misc;
+    pa.dnu = dnu;
+    pa.dtheta = dtheta;
+    pa.dw_phi = dw_phi;
+    pa.dw_r = dw_r;
+    pa.da_phi = da_phi;
+    pa.da_r = da_r;
+    LRS_LAUNCH(KID_SAMU_PARAMS, stream, launch_samu_params(pa, stream));
+    return LRS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// RG-LRU
+// ---------------------------------------------------------------------------
+int rglru_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes) {
+    const int st = check_rglru_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (saved_bytes) *saved_bytes = rglru_saved_layout(B, L, D).total;
+    if (scratch_bytes) *scratch_bytes = rglru_scratch_layout(B, L, D).total;
+    return LRS_OK;
+}
+
+int rglru_forward(const void* x, const void* lx, const void* la, const float* alpha,
+                  const float* h0, const uint8_t* reset, int B, int L, int D,
+                  void* y, float* y32, float* hT, void* saved, void* scratch,
+                  cudaStream_t stream) {
+    const int st = check_rglru_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (!req(x) || !req(lx) || !req(la) || !req(alpha) || !opt(h0) || !req(y) || !opt(y32) ||
+        !req(hT) || !req(saved) || !req(scratch))
+        return LRS_ERR_ARG;
+    const RglruSaved sv = rglru_saved_layout(B, L, D);
+    const RglruScratch sc = rglru_scratch_layout(B, L, D);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
+    if (e != cudaSuccess) return LRS_ERR_CUDA;
+    CUtensorMap tm_x, tm_lx, tm_la;
+    if (!make_bf16_map(&tm_x, x, B, L, D) || !make_bf16_map(&tm_lx, lx, B, L, D) ||
+        !make_bf16_map(&tm_la, la, B, L, D))
+        return LRS_ERR_CUDA;
+    RglruScanFwdArgs a;
+    a.g = make_geom(B, L, D);
+    a.alpha = alpha;
+    a.reset = reset;
+    a.h0 = h0;
+    a.y = static_cast<uint32_t*>(y);
+    a.y32 = y32;
+    a.hT = hT;
+    a.hsub = at<float>(saved, sv.hsub);
+    a.agg = at<float2>(scratch, sc.agg);
+    a.flags = at<uint32_t>(scratch, sc.flags);
+    a.counter = at<uint32_t>(scratch, sc.status + 4);
+    a.status = at<uint32_t>(scratch, sc.status);
+    LRS_LAUNCH(KID_RGLRU_SCAN_FWD, stream, launch_rglru_scan_fwd(tm_x, tm_lx, tm_la, a, stream));
+    return LRS_OK;
+}
+
+int rglru_backward(const void* dy, const float* dhT, const void* x, const void* lx,
+                   const void* la, const float* alpha, const float* h0, const uint8_t* reset,
+                   int B, int L, int D, const void* saved, void* dx, void* dlx, void* dla,
+                   int grad_dtype, float* dalpha, float* dh0, void* scratch,
+                   cudaStream_t stream) {
+    (void)h0;
+    const int st = check_rglru_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (grad_dtype != LRS_GRAD_BF16 && grad_dtype != LRS_GRAD_FP32) return LRS_ERR_ARG;
+    if (!req(dy) || !opt(dhT) || !req(x) || !req(lx) || !req(la) || !req(alpha) || !req(saved) ||
+        !req(dx) || !req(dlx) || !req(dla) || !req(dalpha) || !req(dh0) || !req(scratch))
+        return LRS_ERR_ARG;
+    const RglruSaved sv = rglru_saved_layout(B, L, D);
+    const RglruScratch sc = rglru_scratch_layout(B, L, D);
+    const ScanGeom g = make_geom(B, L, D);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
+    if (e != cudaSuccess) return LRS_ERR_CUDA;
+    CUtensorMap tm_dy, tm_x, tm_lx, tm_la;
+    if (!make_bf16_map(&tm_dy, dy, B, L, D) || !make_bf16_map(&tm_x, x, B, L, D) ||
+        !make_bf16_map(&tm_lx, lx, B, L, D) || !make_bf16_map(&tm_la, la, B, L, D))
+        return LRS_ERR_CUDA;
+    RglruScanBwdArgs a;
+    a.g = g;
+    a.alpha = alpha;
+    a.reset = reset;
+    a.dhT = dhT;
+    a.hsub = at<float>(saved, sv.hsub);
+    a.dx = dx;
+    a.dlx = dlx;
+    a.dla = dla;
+    a.grad_fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
+    a.dh0 = dh0;
+    a.agg = at<float2>(scratch, sc.agg);
+    a.rin = at<float>(scratch, sc.rin);
+    a.apart = at<float>(scratch, sc.apart);
+    a.flags = at<uint32_t>(scratch, sc.flags);
+    a.counter = at<uint32_t>(scratch, sc.status + 4);
+    a.status = at<uint32_t>(scratch, sc.status);
+    LRS_LAUNCH(KID_RGLRU_SCAN_BWD, stream, launch_rglru_scan_bwd(tm_dy, tm_x, tm_lx, tm_la, a, stream));
+    LRS_LAUNCH(KID_RGLRU_ALPHA, stream,
+               launch_rglru_alpha(a.apart, at<float>(scratch, sc.apart2), dalpha, B * g.CT, D, stream));
+    return LRS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,236 @@
+// Device helpers shared by the SAMU and RG-LRU scan kernels (sm_103a).
+//
+// Nothing here is shared with the FP64 oracle: this is the CUDA side only.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>            // CUtensorMap (type only)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/samu.h"
+
+namespace lrs {
+
+// ---------------------------------------------------------------------------
+// Tiling.  A chain is one (batch row, group of 64 modes or channels); each
+// lane of a warp owns two adjacent modes, so a warp covers a group and reads
+// 128 contiguous bytes of each BF16 half per token.  A tile is 128 tokens of
+// one chain, split over 8 warps of 16 tokens each (sub-chunks).
+// ---------------------------------------------------------------------------
+constexpr int kGroup = 64;           // modes (SAMU) or channels (RG-LRU) per chain
+constexpr int kSub = 16;             // tokens per warp sub-chunk
+constexpr int kScanWarps = 8;        // sub-chunks per tile
+constexpr int kTile = kSub * kScanWarps;   // tokens per tile (128)
+constexpr int kScanThreads = kScanWarps * 32;
+constexpr int kBoxBytes = kTile * kGroup * 2;   // one BF16 [128 x 64] box (16 KB)
+
+// Look-back status values stored per (chain, chunk).
+constexpr uint32_t kFlagEmpty = 0u;
+constexpr uint32_t kFlagAgg = 1u;    // the tile's own affine map is published
+constexpr uint32_t kFlagIncl = 2u;   // the state after the tile is published
+constexpr uint32_t kFlagErr = 3u;    // the tile gave up; waiters abort
+
+// Bounded spin: polls before a waiter records LRS_ERR_TIMEOUT and returns.
+// With the nanosleep back-off this is well under a second per wait.
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// Device status word bits (OR-ed together by failing CTAs).
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusUpstream = 2u;
+
+// ---------------------------------------------------------------------------
+// Memory-model primitives (PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// L2-only loads (never served from a possibly stale L1 line).
+__device__ __forceinline__ float4 ldcg4(const float4* p) { return __ldcg(p); }
+__device__ __forceinline__ float2 ldcg2(const float2* p) { return __ldcg(p); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory barriers and TMA (cp.async.bulk.tensor) loads.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the barrier phase; false if kSpinLimit polls pass first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    for (uint32_t n = 0; n < kSpinLimit; ++n) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (n > 16) __nanosleep(32);
+    }
+    return false;
+}
+
+// 3-D tiled tensor load of one box into shared memory, completing on `bar`.
+// The innermost coordinate x must be a multiple of 8 elements (16 bytes).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Warp-level chain search for the decoupled look-back (see lookback_find);
+// executed by one full warp, returns the same value in every lane.
+__device__ __forceinline__ int lookback_find_warp(const uint32_t* flags, int c, int C, int dir) {
+    const int lane = threadIdx.x & 31;
+    int base = c + dir;
+    uint32_t polls = 0;
+    for (;;) {
+        const int idx = base + dir * lane;
+        const bool valid = idx >= 0 && idx < C;
+        const uint32_t f = valid ? ld_acquire_gpu(flags + idx) : kFlagAgg;
+        const unsigned incl = __ballot_sync(0xffffffffu, f == kFlagIncl);
+        const unsigned empty = __ballot_sync(0xffffffffu, f == kFlagEmpty);
+        const unsigned bad = __ballot_sync(0xffffffffu, f == kFlagErr);
+        const int first = incl ? (__ffs(incl) - 1) : 32;
+        const unsigned upto = first >= 31 ? 0xffffffffu : ((2u << first) - 1u);
+        const unsigned before = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
+        if (bad & upto) return -1;
+        if (empty & before) {
+            if (++polls > kSpinLimit) return -1;
+            if (polls > 8) __nanosleep(64);
+            continue;
+        }
+        if (first < 32) return base + dir * first;
+        base += 32 * dir;
+    }
+}
+
+// Decoupled look-back, chain search.  For tile c of one chain, find the
+// nearest predecessor (walking in direction dir: -1 towards chunk 0, +1
+// towards chunk C-1) whose state after the chunk (kFlagIncl) is published,
+// while every closer predecessor has at least published its map (kFlagAgg).
+// Warp 0 inspects 32 predecessors per poll (one per lane, acquire loads) and
+// the answer is broadcast through *s_j after a CTA barrier; -1 means a
+// predecessor failed or the bounded wait ran out.  Must be called by every
+// thread of the CTA.
+__device__ __forceinline__ int lookback_find(const uint32_t* flags, int c, int C, int dir, int* s_j) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int base = c + dir;
+        int result = -1;
+        uint32_t polls = 0;
+        for (;;) {
+            const int idx = base + dir * lane;
+            const bool valid = idx >= 0 && idx < C;
+            const uint32_t f = valid ? ld_acquire_gpu(flags + idx) : kFlagAgg;
+            const unsigned incl = __ballot_sync(0xffffffffu, f == kFlagIncl);
+            const unsigned empty = __ballot_sync(0xffffffffu, f == kFlagEmpty);
+            const unsigned bad = __ballot_sync(0xffffffffu, f == kFlagErr);
+            const int first = incl ? (__ffs(incl) - 1) : 32;
+            const unsigned upto = first >= 31 ? 0xffffffffu : ((2u << first) - 1u);
+            const unsigned before = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
+            if (bad & upto) break;
+            if (empty & before) {
+                if (++polls > kSpinLimit) break;
+                if (polls > 8) __nanosleep(64);
+                continue;
+            }
+            if (first < 32) {
+                result = base + dir * first;
+                break;
+            }
+            base += 32 * dir;
+        }
+        if (lane == 0) *s_j = result;
+    }
+    __syncthreads();
+    return *s_j;
+}
+
+// 2^x on the SFU (PTX ex2.approx, documented relative error ~2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------
+// BF16 pairs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+    return __bfloat1622float2(h);
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// Complex affine maps T(h) = lam h + beta, stored as float4 {lam.re, lam.im,
+// beta.re, beta.im}.  apply() is the single place where a map meets a state,
+// so a state rebuilt during look-back is bitwise the state the owning tile
+// published (explicit fmaf: no contraction choices left to the compiler).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 capply(float4 T, float2 h) {
+    float re = __fmaf_rn(T.x, h.x, __fmaf_rn(-T.y, h.y, T.z));
+    float im = __fmaf_rn(T.x, h.y, __fmaf_rn(T.y, h.x, T.w));
+    return make_float2(re, im);
+}
+
+// lam * z (complex)
+__device__ __forceinline__ float2 cmul(float2 a, float2 z) {
+    return make_float2(__fmaf_rn(a.x, z.x, -__fmul_rn(a.y, z.y)),
+                       __fmaf_rn(a.x, z.y, __fmul_rn(a.y, z.x)));
+}
+
+// conj(a) * z
+__device__ __forceinline__ float2 cmulc(float2 a, float2 z) {
+    return make_float2(__fmaf_rn(a.x, z.x, __fmul_rn(a.y, z.y)),
+                       __fmaf_rn(a.x, z.y, -__fmul_rn(a.y, z.x)));
+}
+
+// T2 o T1 (T1 first): (l2 l1, l2 b1 + b2).
+__device__ __forceinline__ float4 compose_maps(float4 T2, float4 T1) {
+    const float2 L = cmul(make_float2(T2.x, T2.y), make_float2(T1.x, T1.y));
+    const float2 Bv = capply(T2, make_float2(T1.z, T1.w));
+    return make_float4(L.x, L.y, Bv.x, Bv.y);
+}
+
+// Real affine maps {a, b} for the RG-LRU chain.
+__device__ __forceinline__ float rapply(float2 T, float h) { return __fmaf_rn(T.x, h, T.y); }
+
+// T2 o T1 for real maps.
+__device__ __forceinline__ float2 rcompose(float2 T2, float2 T1) {
+    return make_float2(__fmul_rn(T2.x, T1.x), __fmaf_rn(T2.x, T1.y, T2.y));
+}
+
+}  // namespace lrs

@@ -1,0 +1,194 @@
+// Kernel argument blocks, shared per-step device functions and launcher
+// declarations of the CUDA library.
+#pragma once
+
+#include "common.cuh"
+#include "layout.cuh"
+
+namespace lrs {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Per-mode constants of the transition.  lambda_{t,m} = e^{-nu_m E_t} e^{i(theta_m + d_t)}
+// (SAMU GPU page, section 05, transition equation) is evaluated as
+//   lambda_{t,m} = lbar_m * delta_{t,m},  lbar_m = e^{-nu_m} e^{i theta_m},
+//   delta_{t,m} = e^{-nu_m (E_t - 1)} (C_t + i S_t),
+// which is the same number.  lbar_m is held as a double-float (hi + lo, formed
+// once in FP64), so no per-mode rounding of e^{-nu}, cos theta or sin theta
+// biases every step of a long chain; delta is close to 1 and formed per step
+// in FP32 from E_t - 1 = expm1(c_t) and the shared C_t, S_t.
+struct ModeConst {
+    float hr, hi, lr, li;   // lbar: hi part (re, im), lo part (re, im)
+    float nu;
+};
+
+__device__ __forceinline__ ModeConst load_mode(const float4* __restrict__ modes,
+                                               const float* __restrict__ nu, int m) {
+    const float4 v = modes[m];
+    ModeConst k;
+    k.hr = v.x;
+    k.hi = v.y;
+    k.lr = v.z;
+    k.li = v.w;
+    k.nu = nu[m];
+    return k;
+}
+
+// ctl = {E - 1, C, S, reset}.  0 at a reset position.  Every pass that needs
+// lambda calls this, so the forward and the backward rebuild the same bits.
+__device__ __forceinline__ float2 samu_lambda(const ModeConst& k, float4 ctl) {
+    const float x = __fmul_rn(k.nu, ctl.x);                 // nu (E - 1)
+    float q;                                                 // e^{-x}
+    if (fabsf(x) < 0.03125f) {
+        // degree-4 Taylor polynomial: truncation below 3e-10 relative
+        q = __fmaf_rn(x, __fmaf_rn(x, __fmaf_rn(x, __fmaf_rn(x, 1.0f / 24.0f, -1.0f / 6.0f), 0.5f), -1.0f), 1.0f);
+    } else {
+        q = expf(-x);
+    }
+    const float dr = __fmul_rn(q, ctl.y);
+    const float di = __fmul_rn(q, ctl.z);
+    const float lr = __fmaf_rn(k.hr, dr, __fmaf_rn(-k.hi, di, k.lr));
+    const float li = __fmaf_rn(k.hr, di, __fmaf_rn(k.hi, dr, k.li));
+    const bool rs = ctl.w != 0.f;
+    return make_float2(rs ? 0.f : lr, rs ? 0.f : li);
+}
+
+// One state step z' = lambda z + b, formed as u = lambda z then u + b.  The
+// backward keeps u = lambda z_{t-1} for kappa, so both directions use this form.
+__device__ __forceinline__ float2 step_state(float2 l, float2 bb, float2 z, float2* u_out = nullptr) {
+    const float2 u = cmul(l, z);
+    if (u_out) *u_out = u;
+    return make_float2(__fadd_rn(u.x, bb.x), __fadd_rn(u.y, bb.y));
+}
+
+// S <- T_t o S for T_t(h) = l h + bb, S = {Lambda, beta}.
+__device__ __forceinline__ float4 compose_step(float2 l, float2 bb, float4 S) {
+    const float2 L = cmul(l, make_float2(S.x, S.y));
+    const float2 Bv = capply(make_float4(l.x, l.y, bb.x, bb.y), make_float2(S.z, S.w));
+    return make_float4(L.x, L.y, Bv.x, Bv.y);
+}
+
+struct SamuScanFwdArgs {
+    ScanGeom g;
+    const float4* ctrl;     // [B*L] {E - 1, C, S, reset}
+    const float4* modes;    // [M] lbar hi/lo
+    const float* nu;
+    const float* h0;        // [B,M,2] or null
+    uint32_t* y;            // BF16 pairs of y
+    float* y32;             // optional
+    float* hT;              // [B,M,2]
+    float2* hsub;           // [B][CS][M] sub-chunk entry states
+    float4* agg;            // [B][CT][M] tile maps
+    uint32_t* flags;        // [n_chains][CT]
+    uint32_t* counter;
+    uint32_t* status;
+};
+
+struct SamuScanBwdArgs {
+    ScanGeom g;
+    const float4* ctrl;
+    const float4* modes;
+    const float* nu;
+    const float* dhT;       // [B,M,2] or null
+    const float2* hsub;     // [B][CS][M] (the forward's sub-chunk entry states)
+    void* dw;               // BF16 pairs or FP32
+    int grad_fp32;
+    float* dh0;             // [B,M,2]
+    float4* agg;            // [B][CT][M] reverse tile maps
+    float2* rin;            // [B][CT][M] adjoint leaving each tile towards the past
+    float2* kpart;          // [B*L][n_groups] {sum Im kappa, sum -nu Re kappa}
+    float2* numod;          // [B][CT][M] {dnu, dtheta} per tile
+    uint32_t* flags;
+    uint32_t* counter;
+    uint32_t* status;
+};
+
+struct SamuCtrlBwdArgs {
+    int B, L, D, n_groups;
+    const uint4* x;         // BF16 x_sel as 16-byte vectors
+    const float2* kpart;
+    const float* p;
+    const float* r;
+    const float4* ctrl;
+    const float* wh;        // [2][D+1]
+    const float* misc;
+    void* dx;               // BF16 or FP32
+    int grad_fp32;
+    float* dwh_part;        // [kCtrlBwdCtas * 2 halves][2][D+1]
+    float2* amp_part;       // [kCtrlBwdCtas]
+};
+
+struct SamuParamArgs {
+    int B, L, D, CT;
+    const float2* numod;    // [B*CT][M]
+    float2* numod2;         // [kReduceGroups][M]
+    const float* dwh_part;  // [kCtrlBwdCtas * 2 halves][2][D+1]
+    const float2* amp_part;
+    float* dwh;             // [2][D+1] column sums of dwh_part
+    const float* wh;
+    const float* misc;
+    float* dnu;
+    float* dtheta;
+    float* dw_phi;
+    float* dw_r;
+    float* da_phi;
+    float* da_r;
+};
+
+cudaError_t launch_samu_prep(const float* w_phi, const float* w_r, const float* a_phi,
+                             const float* a_r, const float* nu, const float* theta, int D,
+                             float* wh, float* misc, float4* modes, cudaStream_t s);
+cudaError_t launch_samu_ctrl_fwd(const void* x, const uint8_t* reset, const float* wh,
+                                 const float* misc, long long BL, int D, float* p, float* r,
+                                 float4* ctrl, cudaStream_t s);
+cudaError_t launch_samu_scan_fwd(const CUtensorMap& tm_w, const SamuScanFwdArgs& args, cudaStream_t s);
+cudaError_t launch_samu_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_w,
+                                 const SamuScanBwdArgs& args, cudaStream_t s);
+cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s);
+cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// RG-LRU
+// ---------------------------------------------------------------------------
+struct RglruScanFwdArgs {
+    ScanGeom g;
+    const float* alpha;
+    const uint8_t* reset;
+    const float* h0;        // [B,D] or null
+    uint32_t* y;
+    float* y32;
+    float* hT;
+    float* hsub;            // [B][CS][D]
+    float2* agg;            // [B][CT][D] {a, b}
+    uint32_t* flags;
+    uint32_t* counter;
+    uint32_t* status;
+};
+
+struct RglruScanBwdArgs {
+    ScanGeom g;
+    const float* alpha;
+    const uint8_t* reset;
+    const float* dhT;
+    const float* hsub;
+    void* dx;
+    void* dlx;
+    void* dla;
+    int grad_fp32;
+    float* dh0;
+    float2* agg;
+    float* rin;
+    float* apart;           // [B*CT][D]
+    uint32_t* flags;
+    uint32_t* counter;
+    uint32_t* status;
+};
+
+cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
+                                  const RglruScanFwdArgs& args, cudaStream_t s);
+cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
+                                  const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s);
+cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,
+                               cudaStream_t s);
+
+}  // namespace lrs

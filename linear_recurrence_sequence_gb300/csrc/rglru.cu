@@ -1,0 +1,530 @@
+// RG-LRU real scan on the same tiled look-back engine (comparison path).
+//
+// Equations: SAMU GPU page ("SAMU 与 RG-LRU 的 H800 训练性能对比"), section 04:
+// g^x = sigmoid(l^x), g^a = sigmoid(l^a), a_t = exp(-8 g^a softplus(alpha)),
+// b_t = x_t g^x sqrt(max(1 - a_t^2, 0)), h_t = a_t h_{t-1} + b_t, with the gate
+// preparation fused into the scan (no materialised a/b tensors) and, at a
+// segment start, a_t = 0 and a unit normaliser ("Griffin 第 4、5 节 H800 对照
+// 协议", "RG-LRU 的固定方程").  1 - a^2 is evaluated as -expm1(2 log a) so the
+// normaliser keeps full FP32 relative accuracy when a is close to 1.
+//
+// Tiling as in the SAMU scan: a chain is (batch row, 64 channels), a CTA owns
+// a 128-token tile (x, l^x, l^a and, backward, dy staged by TMA), 8 warps of
+// 16-token sub-chunks, lane l owns channels 2l, 2l+1, decoupled look-back
+// between tiles.
+#include "kernels.cuh"
+
+namespace lrs {
+
+struct RgGate {
+    float a;    // retention (0 at a segment start)
+    float n;    // write normaliser sqrt(1 - a^2) (1 at a segment start)
+    float u;    // 1 - a^2
+    float gx;   // sigmoid(l^x)
+    float ga;   // sigmoid(l^a)
+};
+
+__device__ __forceinline__ float sigmoid_f(float v) {
+    return __frcp_rn(1.0f + ex2_approx(-v * kLog2e));
+}
+
+// nsp = -8 softplus(alpha) for this channel
+__device__ __forceinline__ RgGate rg_gate(float lx, float la, float nsp, bool is_reset) {
+    RgGate gt;
+    gt.gx = sigmoid_f(lx);
+    gt.ga = sigmoid_f(la);
+    const float lg = gt.ga * nsp;                 // log a
+    gt.a = ex2_approx(lg * kLog2e);
+    gt.u = -expm1f(2.0f * lg);
+    gt.n = sqrtf(fmaxf(gt.u, 0.0f));
+    if (is_reset) {
+        gt.a = 0.0f;
+        gt.n = 1.0f;
+    }
+    return gt;
+}
+
+__device__ __forceinline__ float softplus_f(float v) {
+    return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
+}
+
+// ---------------------------------------------------------------------------
+// Forward
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanThreads, 2)
+    rglru_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_lx,
+                          const __grid_constant__ CUtensorMap tm_la, RglruScanFwdArgs a) {
+    extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: x, l^x, l^a
+    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
+    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kBoxBytes);
+    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kBoxBytes);
+    __shared__ uint8_t s_rst[kTile];
+    __shared__ float4 s_map[kScanWarps][32];
+    __shared__ float2 s_ent[kScanWarps][32];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ uint32_t s_tile;
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    if (tid == 0) {
+        s_tile = atomicAdd(a.counter, 1u);
+        mbar_init(&s_bar, 1);
+    }
+    __syncthreads();
+    const ScanGeom& g = a.g;
+    const long long tile = s_tile;
+    const int chain = (int)(tile % g.n_chains);
+    const int c = (int)(tile / g.n_chains);
+    const int b = chain / g.n_groups;
+    const int grp = chain % g.n_groups;
+    const int D = g.lanes;
+    const int L = g.L;
+    const int CT = g.CT;
+    const int t0 = c * kTile;
+    const int d = grp * kGroup + 2 * lane;
+    const bool active = d < D;
+    uint32_t* fl = a.flags + (size_t)chain * CT;
+    const size_t hb = (size_t)b * g.CS;
+
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&s_bar, 3 * kBoxBytes);
+        tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(&s_lx[0][0], &tm_lx, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(&s_la[0][0], &tm_la, grp * kGroup, t0, b, &s_bar);
+    }
+    if (tid < kTile) {
+        const int t = t0 + tid;
+        s_rst[tid] = (t < L && a.reset != nullptr && a.reset[(size_t)b * L + t] != 0) ? 1 : 0;
+    }
+    float nsp0 = 0.f, nsp1 = 0.f;
+    if (active) {
+        nsp0 = -8.0f * softplus_f(a.alpha[d]);
+        nsp1 = -8.0f * softplus_f(a.alpha[d + 1]);
+    }
+    const int r0 = warp * kSub;
+    const int nsub = max(0, min(kSub, L - t0 - r0));
+    const bool landed = mbar_wait_bounded(&s_bar, 0);
+    if (!__syncthreads_and(landed)) {
+        if (tid == 0) {
+            st_release_gpu(fl + c, kFlagErr);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        mbar_wait_bounded(&s_bar, 0);
+        return;
+    }
+
+    float4 ab[kSub];   // {a_d, b_d, a_d+1, b_d+1}
+    float2 S0 = make_float2(1.f, 0.f), S1 = S0;
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        ab[i] = make_float4(1.f, 0.f, 1.f, 0.f);
+        if (i < nsub) {
+            const bool rs = s_rst[r0 + i] != 0;
+            const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
+            const float2 gl = bf2_to_f2(s_lx[r0 + i][lane]);
+            const float2 al = bf2_to_f2(s_la[r0 + i][lane]);
+            const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
+            const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
+            ab[i] = make_float4(g0.a, xx.x * g0.gx * g0.n, g1.a, xx.y * g1.gx * g1.n);
+            S0 = rcompose(make_float2(ab[i].x, ab[i].y), S0);
+            S1 = rcompose(make_float2(ab[i].z, ab[i].w), S1);
+        }
+    }
+    s_map[warp][lane] = make_float4(S0.x, S0.y, S1.x, S1.y);
+    __syncthreads();
+
+    if (warp == 0) {
+        float4 A = s_map[0][lane];
+#pragma unroll
+        for (int w = 1; w < kScanWarps; ++w) {
+            const float4 Sw = s_map[w][lane];
+            const float2 t0v = rcompose(make_float2(Sw.x, Sw.y), make_float2(A.x, A.y));
+            const float2 t1v = rcompose(make_float2(Sw.z, Sw.w), make_float2(A.z, A.w));
+            A = make_float4(t0v.x, t0v.y, t1v.x, t1v.y);
+        }
+        float h0v = 0.f, h1v = 0.f;
+        bool err = false;
+        if (c == 0) {
+            if (active && a.h0 != nullptr) {
+                const float2 hv = *reinterpret_cast<const float2*>(a.h0 + (size_t)b * D + d);
+                h0v = hv.x;
+                h1v = hv.y;
+            }
+        } else {
+            if (active)
+                *reinterpret_cast<float4*>(a.agg + ((size_t)b * CT + c) * D + d) = A;
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
+            const int j = lookback_find_warp(fl, c, CT, -1);
+            if (j < 0) {
+                err = true;
+            } else if (active) {
+                const float2 hv = __ldcg(reinterpret_cast<const float2*>(
+                    a.hsub + (hb + (size_t)(j + 1) * kScanWarps) * D + d));
+                h0v = hv.x;
+                h1v = hv.y;
+                for (int i = j + 1; i < c; i += 4) {
+                    float4 T[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (i + q < c)
+                            T[q] = ldcg4(reinterpret_cast<const float4*>(a.agg + ((size_t)b * CT + i + q) * D + d));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (i + q < c) {
+                            h0v = rapply(make_float2(T[q].x, T[q].y), h0v);
+                            h1v = rapply(make_float2(T[q].z, T[q].w), h1v);
+                        }
+                    }
+                }
+            }
+        }
+        if (!err) {
+            float e0 = h0v, e1 = h1v;
+#pragma unroll
+            for (int w = 0; w < kScanWarps; ++w) {
+                s_ent[w][lane] = make_float2(e0, e1);
+                if (active && (w > 0 || c == 0))
+                    *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)c * kScanWarps + w) * D + d) = make_float2(e0, e1);
+                const float4 Sw = s_map[w][lane];
+                e0 = rapply(make_float2(Sw.x, Sw.y), e0);
+                e1 = rapply(make_float2(Sw.z, Sw.w), e1);
+            }
+            if (active)
+                *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)(c + 1) * kScanWarps) * D + d) =
+                    make_float2(rapply(make_float2(A.x, A.y), h0v), rapply(make_float2(A.z, A.w), h1v));
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
+        } else if (lane == 0) {
+            st_release_gpu(fl + c, kFlagErr);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        if (lane == 0) s_err = err ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_err) return;
+
+    const float2 e = s_ent[warp][lane];
+    float z0 = e.x, z1 = e.y;
+    const size_t row = (((size_t)b * L + t0 + r0) * D + d) / 2;
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        if (i < nsub) {
+            z0 = __fmaf_rn(ab[i].x, z0, ab[i].y);
+            z1 = __fmaf_rn(ab[i].z, z1, ab[i].w);
+            if (active) {
+                const size_t o = row + (size_t)i * (D / 2);
+                __stcs(a.y + o, f2_to_bf2(z0, z1));
+                if (a.y32 != nullptr) *reinterpret_cast<float2*>(a.y32 + 2 * o) = make_float2(z0, z1);
+            }
+        }
+    }
+    if (active && nsub > 0 && t0 + r0 + nsub == L)
+        *reinterpret_cast<float2*>(a.hT + (size_t)b * D + d) = make_float2(z0, z1);
+}
+
+// ---------------------------------------------------------------------------
+// Backward.  Forward sweep from the saved sub-chunk entry: h_{t-1} (kept in
+// registers), the prefix product P_t = a_s..a_t and q = sum_t P_t dy_t; the
+// sub-chunk maps an adjoint R arriving at its last token to R' = P_e R + q.
+// Warp 0 composes, looks back over later tiles and hands out incoming
+// adjoints.  Reverse sweep with the gate derivatives:
+//   H_t = dy_t + a_{t+1} H_{t+1};  dx = H g^x n;  dl^x = H x n g^x (1 - g^x);
+//   abar = H h_{t-1} + H x g^x (-2 a) / sqrt(max(4 (1 - a^2), 1e-6));
+//   dl^a = abar (-8 softplus(alpha)) a g^a (1 - g^a);
+//   dalpha += abar (-8 g^a) sigmoid(alpha) a.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanThreads, 2)
+    rglru_scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_lx, const __grid_constant__ CUtensorMap tm_la,
+                          RglruScanBwdArgs a) {
+    extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: dy, x, l^x, l^a
+    uint32_t (*s_g)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
+    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kBoxBytes);
+    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kBoxBytes);
+    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 3 * kBoxBytes);
+    __shared__ uint8_t s_rst[kTile];
+    __shared__ float4 s_map[kScanWarps][32];
+    __shared__ float2 s_ent[kScanWarps][32];
+    __shared__ float2 s_acc[kScanWarps][32];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ uint32_t s_tile;
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    if (tid == 0) {
+        s_tile = atomicAdd(a.counter, 1u);
+        mbar_init(&s_bar, 1);
+    }
+    __syncthreads();
+    const ScanGeom& g = a.g;
+    const long long tile = s_tile;
+    const int chain = (int)(tile % g.n_chains);
+    const int CT = g.CT;
+    const int c = CT - 1 - (int)(tile / g.n_chains);
+    const int b = chain / g.n_groups;
+    const int grp = chain % g.n_groups;
+    const int D = g.lanes;
+    const int L = g.L;
+    const int t0 = c * kTile;
+    const int d = grp * kGroup + 2 * lane;
+    const bool active = d < D;
+    uint32_t* fl = a.flags + (size_t)chain * CT;
+    const size_t hb = (size_t)b * g.CS;
+
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&s_bar, 4 * kBoxBytes);
+        tma_load_3d(&s_g[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(&s_lx[0][0], &tm_lx, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(&s_la[0][0], &tm_la, grp * kGroup, t0, b, &s_bar);
+    }
+    if (tid < kTile) {
+        const int t = t0 + tid;
+        s_rst[tid] = (t < L && a.reset != nullptr && a.reset[(size_t)b * L + t] != 0) ? 1 : 0;
+    }
+    const int r0 = warp * kSub;
+    const int nsub = max(0, min(kSub, L - t0 - r0));
+    float nsp0 = 0.f, nsp1 = 0.f, sa0 = 0.f, sa1 = 0.f;
+    float h0v = 0.f, h1v = 0.f;
+    if (active) {
+        const float al0 = a.alpha[d], al1 = a.alpha[d + 1];
+        nsp0 = -8.0f * softplus_f(al0);
+        nsp1 = -8.0f * softplus_f(al1);
+        sa0 = 1.0f / (1.0f + expf(-al0));
+        sa1 = 1.0f / (1.0f + expf(-al1));
+        if (nsub > 0) {
+            const float2 hv = __ldcg(reinterpret_cast<const float2*>(
+                a.hsub + (hb + (size_t)c * kScanWarps + warp) * D + d));
+            h0v = hv.x;
+            h1v = hv.y;
+        }
+    }
+    const bool landed = mbar_wait_bounded(&s_bar, 0);
+    if (!__syncthreads_and(landed)) {
+        if (tid == 0) {
+            st_release_gpu(fl + c, kFlagErr);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        mbar_wait_bounded(&s_bar, 0);
+        return;
+    }
+
+    float2 hp[kSub];   // h_{t-1} per token
+    float P0 = 1.f, P1 = 1.f, q0 = 0.f, q1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        hp[i] = make_float2(0.f, 0.f);
+        if (i < nsub) {
+            const bool rs = s_rst[r0 + i] != 0;
+            const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
+            const float2 gl = bf2_to_f2(s_lx[r0 + i][lane]);
+            const float2 al = bf2_to_f2(s_la[r0 + i][lane]);
+            const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
+            const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
+            const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
+            hp[i] = make_float2(h0v, h1v);
+            h0v = __fmaf_rn(g0.a, h0v, xx.x * g0.gx * g0.n);
+            h1v = __fmaf_rn(g1.a, h1v, xx.y * g1.gx * g1.n);
+            P0 *= g0.a;
+            P1 *= g1.a;
+            q0 = fmaf(P0, gg.x, q0);
+            q1 = fmaf(P1, gg.y, q1);
+        }
+    }
+    s_map[warp][lane] = make_float4(P0, q0, P1, q1);
+    __syncthreads();
+
+    if (warp == 0) {
+        float4 A = s_map[kScanWarps - 1][lane];
+#pragma unroll
+        for (int w = kScanWarps - 2; w >= 0; --w) {
+            const float4 Fw = s_map[w][lane];
+            const float2 t0v = rcompose(make_float2(Fw.x, Fw.y), make_float2(A.x, A.y));
+            const float2 t1v = rcompose(make_float2(Fw.z, Fw.w), make_float2(A.z, A.w));
+            A = make_float4(t0v.x, t0v.y, t1v.x, t1v.y);
+        }
+        float R0 = 0.f, R1 = 0.f;
+        bool err = false;
+        if (c == CT - 1) {
+            if (active && a.dhT != nullptr) {
+                const float2 v = *reinterpret_cast<const float2*>(a.dhT + (size_t)b * D + d);
+                R0 = v.x;
+                R1 = v.y;
+            }
+        } else {
+            if (active)
+                *reinterpret_cast<float4*>(a.agg + ((size_t)b * CT + c) * D + d) = A;
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
+            const int j = lookback_find_warp(fl, c, CT, +1);
+            if (j < 0) {
+                err = true;
+            } else if (active) {
+                const float2 rv = __ldcg(reinterpret_cast<const float2*>(a.rin + ((size_t)b * CT + j) * D + d));
+                R0 = rv.x;
+                R1 = rv.y;
+                for (int i = j - 1; i > c; i -= 4) {
+                    float4 T[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (i - q > c)
+                            T[q] = ldcg4(reinterpret_cast<const float4*>(a.agg + ((size_t)b * CT + i - q) * D + d));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (i - q > c) {
+                            R0 = rapply(make_float2(T[q].x, T[q].y), R0);
+                            R1 = rapply(make_float2(T[q].z, T[q].w), R1);
+                        }
+                    }
+                }
+            }
+        }
+        if (!err) {
+            float v0 = R0, v1 = R1;
+#pragma unroll
+            for (int w = kScanWarps - 1; w >= 0; --w) {
+                s_ent[w][lane] = make_float2(v0, v1);
+                const float4 Fw = s_map[w][lane];
+                v0 = rapply(make_float2(Fw.x, Fw.y), v0);
+                v1 = rapply(make_float2(Fw.z, Fw.w), v1);
+            }
+            if (active)
+                *reinterpret_cast<float2*>(a.rin + ((size_t)b * CT + c) * D + d) =
+                    make_float2(rapply(make_float2(A.x, A.y), R0), rapply(make_float2(A.z, A.w), R1));
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
+        } else if (lane == 0) {
+            st_release_gpu(fl + c, kFlagErr);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        if (lane == 0) s_err = err ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_err) return;
+
+    const float2 e = s_ent[warp][lane];
+    float H0 = e.x, H1 = e.y, da0 = 0.f, da1 = 0.f;
+    const size_t row = (((size_t)b * L + t0 + r0) * D + d) / 2;
+#pragma unroll
+    for (int i = kSub - 1; i >= 0; --i) {
+        if (i < nsub) {
+            const bool rs = s_rst[r0 + i] != 0;
+            const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
+            const float2 gl = bf2_to_f2(s_lx[r0 + i][lane]);
+            const float2 al = bf2_to_f2(s_la[r0 + i][lane]);
+            const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
+            const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
+            const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
+            H0 += gg.x;
+            H1 += gg.y;
+            const float dx0 = H0 * g0.gx * g0.n, dx1 = H1 * g1.gx * g1.n;
+            const float dlx0 = H0 * xx.x * g0.n * g0.gx * (1.f - g0.gx);
+            const float dlx1 = H1 * xx.y * g1.n * g1.gx * (1.f - g1.gx);
+            float dla0 = 0.f, dla1 = 0.f;
+            if (!rs) {
+                const float ab0 = fmaf(H0, hp[i].x, H0 * xx.x * g0.gx * (-2.f * g0.a) * rsqrtf(fmaxf(4.f * g0.u, 1e-6f)));
+                const float ab1 = fmaf(H1, hp[i].y, H1 * xx.y * g1.gx * (-2.f * g1.a) * rsqrtf(fmaxf(4.f * g1.u, 1e-6f)));
+                dla0 = ab0 * nsp0 * g0.a * g0.ga * (1.f - g0.ga);
+                dla1 = ab1 * nsp1 * g1.a * g1.ga * (1.f - g1.ga);
+                da0 = fmaf(ab0, -8.f * g0.ga * sa0 * g0.a, da0);
+                da1 = fmaf(ab1, -8.f * g1.ga * sa1 * g1.a, da1);
+            }
+            if (active) {
+                const size_t o = row + (size_t)i * (D / 2);
+                if (a.grad_fp32) {
+                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.dx) + 2 * o) = make_float2(dx0, dx1);
+                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.dlx) + 2 * o) = make_float2(dlx0, dlx1);
+                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.dla) + 2 * o) = make_float2(dla0, dla1);
+                } else {
+                    __stcs(reinterpret_cast<uint32_t*>(a.dx) + o, f2_to_bf2(dx0, dx1));
+                    __stcs(reinterpret_cast<uint32_t*>(a.dlx) + o, f2_to_bf2(dlx0, dlx1));
+                    __stcs(reinterpret_cast<uint32_t*>(a.dla) + o, f2_to_bf2(dla0, dla1));
+                }
+            }
+            H0 *= g0.a;
+            H1 *= g1.a;
+        }
+    }
+    if (c == 0 && warp == 0 && active) *reinterpret_cast<float2*>(a.dh0 + (size_t)b * D + d) = make_float2(H0, H1);
+    s_acc[warp][lane] = make_float2(da0, da1);
+    __syncthreads();
+    if (warp == 0 && active) {
+        float2 s = s_acc[0][lane];
+#pragma unroll
+        for (int w = 1; w < kScanWarps; ++w) {
+            s.x += s_acc[w][lane].x;
+            s.y += s_acc[w][lane].y;
+        }
+        *reinterpret_cast<float2*>(a.apart + ((size_t)b * CT + c) * D + d) = s;
+    }
+}
+
+// dalpha: two fixed-order stages over the per-tile partials [rows][D]
+__global__ void __launch_bounds__(256) rglru_alpha_stage1_kernel(const float* __restrict__ apart,
+                                                                 float* __restrict__ apart2, int rows, int D) {
+    const int d = blockIdx.x * blockDim.x + threadIdx.x;
+    const int gidx = blockIdx.y;
+    if (d >= D) return;
+    const int per = (rows + kReduceGroups - 1) / kReduceGroups;
+    const int r0 = gidx * per;
+    const int r1 = min(rows, r0 + per);
+    float s = 0.f;
+    int r = r0;
+    for (; r + 8 <= r1; r += 8) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __ldcs(apart + (size_t)(r + k) * D + d);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += v[k];
+    }
+    for (; r < r1; ++r) s += __ldcs(apart + (size_t)r * D + d);
+    apart2[(size_t)gidx * D + d] = s;
+}
+
+__global__ void __launch_bounds__(256) rglru_alpha_stage2_kernel(const float* __restrict__ apart2,
+                                                                 float* __restrict__ dalpha, int D) {
+    const int d = blockIdx.x * blockDim.x + threadIdx.x;
+    if (d >= D) return;
+    float s = 0.f;
+    for (int gi = 0; gi < kReduceGroups; ++gi) s += apart2[(size_t)gi * D + d];
+    dalpha[d] = s;
+}
+
+cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
+                                  const RglruScanFwdArgs& args, cudaStream_t s) {
+    const int smem = 3 * kBoxBytes;
+    cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    rglru_scan_fwd_kernel<<<(unsigned)args.g.n_tiles, kScanThreads, smem, s>>>(tm_x, tm_lx, tm_la, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
+                                  const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s) {
+    const int smem = 4 * kBoxBytes;
+    cudaError_t e = cudaFuncSetAttribute(rglru_scan_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    rglru_scan_bwd_kernel<<<(unsigned)args.g.n_tiles, kScanThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,
+                               cudaStream_t s) {
+    dim3 g1((D + 255) / 256, kReduceGroups);
+    rglru_alpha_stage1_kernel<<<g1, 256, 0, s>>>(apart, apart2, rows, D);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    rglru_alpha_stage2_kernel<<<(D + 255) / 256, 256, 0, s>>>(apart2, dalpha, D);
+    return cudaGetLastError();
+}
+
+}  // namespace lrs

@@ -31,10 +31,11 @@ __all__ = [
 def f32_to_bf16_bits(a) -> np.ndarray:
     """Quantise to bfloat16 (round to nearest, ties to even) via float32; returns uint16 bits."""
     f = np.ascontiguousarray(a, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    # ties-to-even rounding of the low 16 bits; NaN inputs are not produced here
-    bias = 0x7FFF + ((u >> 16) & 1)
-    return ((u + bias) >> 16).astype(np.uint16)
+    u = f.view(np.uint32)
+    # ties-to-even rounding of the low 16 bits; finite inputs cannot overflow
+    # 32 bits here (NaN inputs are not produced by these generators)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
 
 
 def bf16_bits_to_f32(bits) -> np.ndarray:

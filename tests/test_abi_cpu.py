@@ -1,0 +1,126 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol that
+include/samu.h declares, and rejects bad arguments on the host before any
+CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "samu.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_recurrence_sequence_gb300 import api
+    if not os.path.exists(api.library_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return api._load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ["samu_forward", "samu_backward", "samu_workspace_bytes", "rglru_forward",
+              "rglru_backward", "rglru_workspace_bytes", "lrs_status_string", "lrs_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from linear_recurrence_sequence_gb300 import api
+    out = subprocess.run(["nm", "-D", "--defined-only", api.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    assert lib.lrs_status_string(0) == b"ok"
+    for s in (1, 2, 3, 4):
+        assert len(lib.lrs_status_string(s)) > 5
+    assert lib.lrs_version() >= 100
+
+
+def _ws(lib, fn, B, L, D):
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    st = getattr(lib, fn)(B, L, D, ctypes.byref(s), ctypes.byref(c))
+    return st, s.value, c.value
+
+
+def test_workspace_sizes(lib):
+    st, saved, scratch = _ws(lib, "samu_workspace_bytes", 1, 32768, 2048)
+    assert st == 0
+    BL, M, S = 32768, 1024, 32768 // 16
+    # controller cache (p, r, E-1/C/S/reset) + one entry state per 16-token sub-chunk at least
+    assert saved >= BL * (4 + 4 + 16) + (S + 1) * M * 8
+    assert saved % 256 == 0 and scratch % 256 == 0
+    # bigger problems need at least as much workspace
+    st2, saved2, scratch2 = _ws(lib, "samu_workspace_bytes", 2, 32768, 2048)
+    assert saved2 > saved and scratch2 > scratch
+    st, saved, scratch = _ws(lib, "rglru_workspace_bytes", 8, 16384, 1024)
+    assert st == 0 and saved >= 8 * (16384 // 16 + 1) * 1024 * 4
+
+
+@pytest.mark.parametrize("B,L,D,expect", [
+    (0, 16, 64, 1), (1, 0, 64, 1), (1, 16, 63, 1), (1, 16, -2, 1),
+    (1, 16, 12, 2), (1, 16, 8, 2), (1, 16, 24, 2), (1, 16, 4112, 2), (1, 16, 16, 0), (1, 1, 4096, 0),
+])
+def test_samu_shape_validation(lib, B, L, D, expect):
+    st, _, _ = _ws(lib, "samu_workspace_bytes", B, L, D)
+    assert st == expect
+
+
+def test_rglru_width_rules(lib):
+    assert _ws(lib, "rglru_workspace_bytes", 1, 5, 8)[0] == 0
+    assert _ws(lib, "rglru_workspace_bytes", 1, 5, 1304)[0] == 0
+    assert _ws(lib, "rglru_workspace_bytes", 1, 5, 6)[0] == 2
+    assert _ws(lib, "rglru_workspace_bytes", 1, 5, 3)[0] == 1
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_forward_rejects_null_and_misaligned_pointers(lib):
+    good = _fake(1 << 20)
+    args = [good] * 10 + [1, 16, 64] + [good] * 5 + [None]
+    # h0 = NULL and reset = NULL are allowed, the rest is checked; misaligned x_sel:
+    bad = list(args)
+    bad[0] = _fake((1 << 20) + 2)
+    assert lib.samu_forward(*bad) == 1
+    bad = list(args)
+    bad[1] = None       # w is required
+    assert lib.samu_forward(*bad) == 1
+    bad = list(args)
+    bad[13] = None      # y is required
+    assert lib.samu_forward(*bad) == 1
+    # odd width is an argument error even with valid pointers
+    bad = list(args)
+    bad[12] = 63
+    assert lib.samu_forward(*bad) == 1
+
+
+def test_backward_rejects_bad_grad_dtype(lib):
+    good = _fake(1 << 20)
+    args = [good] * 12 + [1, 16, 64] + [good, good, good, 7] + [good] * 8 + [None]
+    assert lib.samu_backward(*args) == 1
+    rg = [good] * 8 + [1, 16, 64] + [good] * 4 + [9] + [good] * 3 + [None]
+    assert lib.rglru_backward(*rg) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from linear_recurrence_sequence_gb300 import api
+    monkeypatch.setattr(api, "_lib", None)
+    monkeypatch.setattr(api, "_HERE", str(tmp_path))
+    with pytest.raises(RuntimeError, match="not built"):
+        api._load()

@@ -1,0 +1,107 @@
+"""SAMU mixer: CUDA path (through the C ABI) vs the FP64 oracle, element by element,
+on seeded inputs of every measured workload plus ragged and degenerate shapes."""
+import numpy as np
+import pytest
+
+from linear_recurrence_sequence_gb300 import synth
+from parity import check_samu, run_samu_gpu, run_samu_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    return torch.device("cuda:0")
+
+
+def _case(B, L, D, seed, h0=True, reset_p=0.0):
+    return synth.samu_inputs(B, L, D, seed, h0=h0, reset_p=reset_p)
+
+
+SMALL = {
+    "tiny_B2_L2048_D256": dict(B=2, L=2048, D=256, seed=0, h0=True, reset_p=1 / 512),
+    "ragged_B3_L77_D64": dict(B=3, L=77, D=64, seed=11, h0=True, reset_p=0.05),
+    "single_token_B2_L1_D16": dict(B=2, L=1, D=16, seed=12, h0=True),
+    "one_subchunk_plus_one_L17_D400": dict(B=1, L=17, D=400, seed=13, h0=True, reset_p=0.1),
+    "one_tile_plus_one_L129_D96": dict(B=2, L=129, D=96, seed=20, h0=True, reset_p=0.02),
+    "partial_group_B2_L300_D1552": dict(B=2, L=300, D=1552, seed=14, h0=True, reset_p=0.01),
+    "many_chunks_B1_L5003_D32": dict(B=1, L=5003, D=32, seed=15, h0=True, reset_p=0.002),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_samu_small_cases(name, dev):
+    inp = _case(**SMALL[name])
+    ref_f, ref_b = run_samu_oracle(inp)
+    fwd, bwd = run_samu_gpu(inp, dev, grad_fp32=True)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, grad_fp32=True, label=name)
+
+
+def test_samu_bf16_gradients(dev):
+    inp = _case(**SMALL["tiny_B2_L2048_D256"])
+    ref_f, ref_b = run_samu_oracle(inp)
+    fwd, bwd = run_samu_gpu(inp, dev, grad_fp32=False)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, grad_fp32=False, label="tiny_bf16_grads")
+
+
+def test_samu_resets_at_ends_and_everywhere(dev):
+    inp = _case(B=2, L=64, D=32, seed=16, h0=True)
+    reset = np.zeros((2, 64), np.uint8)
+    reset[0, 0] = 1
+    reset[0, 63] = 1
+    reset[1, :] = 1                     # every token starts a segment: y = w, dh0 = 0
+    inp["reset"] = reset
+    ref_f, ref_b = run_samu_oracle(inp)
+    fwd, bwd = run_samu_gpu(inp, dev)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, label="resets")
+    w32 = synth.bf16_bits_to_f32(inp["w"][1])
+    np.testing.assert_array_equal(fwd["y32"][1].cpu().numpy(), w32)
+    assert float(bwd["dh0"][1].abs().max()) == 0.0
+
+
+def test_samu_no_dhT_no_h0(dev):
+    inp = _case(B=2, L=333, D=64, seed=17, h0=False, reset_p=0.0)
+    inp["dhT"] = None
+    ref_f, ref_b = run_samu_oracle(inp)
+    fwd, bwd = run_samu_gpu(inp, dev, dhT=False)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, label="no_dhT")
+
+
+def test_samu_rtu_degeneration_exact_zeros(dev):
+    """Zero amplitudes: the controller is inert, dx_sel and dw_phi, dw_r are exactly zero."""
+    inp = synth.samu_inputs(1, 500, 64, 18, h0=True, reset_p=0.01, zero_amplitudes=True)
+    ref_f, ref_b = run_samu_oracle(inp)
+    fwd, bwd = run_samu_gpu(inp, dev)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, label="rtu")
+    assert float(bwd["dx_sel"].abs().max()) == 0.0
+    assert float(bwd["dw_phi"].abs().max()) == 0.0
+    assert float(bwd["dw_r"].abs().max()) == 0.0
+
+
+def test_samu_run_to_run_bitwise(dev):
+    """Look-back entry states equal the serial chunk chain bit for bit, and every
+    reduction has a fixed order, so two runs agree exactly."""
+    import torch
+    inp = _case(B=2, L=4096, D=512, seed=19, h0=True, reset_p=1 / 1000)
+    f1, b1 = run_samu_gpu(inp, dev)
+    f2, b2 = run_samu_gpu(inp, dev)
+    for k in ("y", "y32", "hT"):
+        assert torch.equal(f1[k], f2[k]), k
+    for k in ("dx_sel", "dw", "dh0", "dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r"):
+        assert torch.equal(b1[k], b2[k]), k
+
+
+WORKLOADS = ["short", "length_8k", "length_32k", "length_64k", "length_128k",
+             "width_1024", "width_1536", "width_2048", "width_2560", "medium_8k_2560"]
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_samu_workloads(name, dev):
+    wl = synth.WORKLOADS[name]
+    for seed in wl.seeds:
+        inp = wl.make(seed)
+        ref_f, ref_b = run_samu_oracle(inp)
+        fwd, bwd = run_samu_gpu(inp, dev)
+        check_samu(inp, fwd, bwd, ref_f, ref_b, label=f"{name}/seed{seed}")
+        del ref_f, ref_b, fwd, bwd

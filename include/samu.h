@@ -62,6 +62,7 @@ extern "C" {
 #define LRS_ERR_UNSUPPORTED 2  /* valid but unsupported shape (see "Supported shapes") */
 #define LRS_ERR_CUDA 3         /* a kernel launch or memset failed */
 #define LRS_ERR_TIMEOUT 4      /* a bounded device-side wait gave up */
+#define LRS_ERR_TOO_LARGE 5    /* problem does not fit the fixed no-allocation workspace */
 
 /* Gradient output dtype selector for the backward calls. */
 #define LRS_GRAD_BF16 0
@@ -196,6 +197,44 @@ int rglru_backward(const void* dy, const float* dhT, const void* x, const void* 
                    int B, int L, int D, const void* saved, void* dx, void* dlx, void* dla,
                    int grad_dtype, float* dalpha, float* dh0, void* scratch,
                    cudaStream_t stream);
+
+/* ======================================================================== */
+/* SAMU forward without allocation                                           */
+/* ======================================================================== */
+
+/* Size of the fixed device workspace used by samu_forward_noalloc.  Every
+ * GPU that loads this library holds this much device memory for it until the
+ * process exits. */
+#define LRS_NOALLOC_BYTES (32u << 20)
+
+/* samu_forward for callers that cannot allocate device memory and have no
+ * spare buffer to lend as `saved`/`scratch` (for example an application whose
+ * device memory belongs to its own pooled allocator, or a latency-critical
+ * loop that must not take cudaMalloc's implicit synchronisation).  The paper
+ * has no counterpart; it exists for such callers.
+ *
+ * Same computation and same arguments as samu_forward without `saved` and
+ * `scratch`: the caller still passes every input and output (x_sel, w, h0,
+ * reset, nu, theta, w_phi, w_r, a_phi, a_r, y, y32, hT, as documented there).
+ * The intermediates live in one fixed device array of LRS_NOALLOC_BYTES that
+ * the library declares; nothing is allocated or freed (no cudaMalloc,
+ * cudaFree or allocating library routine).  There is no matching backward:
+ * the controller cache and entry states are overwritten by the next call.
+ *
+ * - The first call on each device looks up the array's device address (one
+ *   cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture on the device.
+ * - Every call on a device shares the array and leaves its contents behind;
+ *   each call clears what must start at zero.  Calls whose GPU work overlaps
+ *   (other streams, other host threads) race on the array: serialise them.
+ * - Problems whose intermediates exceed LRS_NOALLOC_BYTES are rejected with
+ *   LRS_ERR_TOO_LARGE before anything is launched (B=1, L=32768, D=2048 uses
+ *   about 22 MiB).
+ * Errors: as samu_forward, plus LRS_ERR_TOO_LARGE. */
+int samu_forward_noalloc(const void* x_sel, const void* w, const float* h0, const uint8_t* reset,
+                         const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                         const float* a_phi, const float* a_r, int B, int L, int D,
+                         void* y, float* y32, float* hT, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -36,6 +36,7 @@ _SIGNATURES = {
     "samu_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
     "samu_forward": ([_P] * 10 + [_I, _I, _I] + [_P] * 6, _I),
     "samu_backward": ([_P] * 12 + [_I, _I, _I] + [_P, _P, _P, _I] + [_P] * 9, _I),
+    "samu_forward_noalloc": ([_P] * 10 + [_I, _I, _I] + [_P] * 4, _I),
     "rglru_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
     "rglru_forward": ([_P] * 6 + [_I, _I, _I] + [_P] * 6, _I),
     "rglru_backward": ([_P] * 8 + [_I, _I, _I] + [_P] * 4 + [_I] + [_P] * 4, _I),
@@ -191,6 +192,36 @@ def samu_backward(dy, dhT, x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_
     _check("samu_backward", st)
     o["scratch"] = scratch
     return o
+
+
+def samu_forward_noalloc(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r, *, want_y32=False,
+                         out=None):
+    """SAMU forward through ``samu_forward_noalloc``: for callers that cannot
+    allocate device memory for the workspace, the library keeps its
+    intermediates in one fixed device array (LRS_NOALLOC_BYTES, shared by all
+    calls on a device; calls that overlap on the GPU race).  Outputs are still
+    caller-provided (``out``) or allocated here by torch.  Returns dict(y, y32, hT)."""
+    dev = x_sel.device
+    B, L, D = x_sel.shape
+    M = D // 2
+    _need(x_sel, "x_sel", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev, (B, L, D))
+    _opt(h0, "h0", torch.float32, dev, (B, M, 2))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    _need(nu, "nu", torch.float32, dev, (M,))
+    _need(theta, "theta", torch.float32, dev, (M,))
+    _need(w_phi, "w_phi", torch.float32, dev, (D + 1,))
+    _need(w_r, "w_r", torch.float32, dev, (D + 1,))
+    _need(a_phi, "a_phi", torch.float32, dev, (1,))
+    _need(a_r, "a_r", torch.float32, dev, (1,))
+    y = _empty((B, L, D), torch.bfloat16, dev, out, "y")
+    y32 = _empty((B, L, D), torch.float32, dev, out, "y32") if want_y32 else None
+    hT = _empty((B, M, 2), torch.float32, dev, out, "hT")
+    st = _load().samu_forward_noalloc(_ptr(x_sel), _ptr(w), _ptr(h0), _ptr(reset), _ptr(nu), _ptr(theta),
+                                      _ptr(w_phi), _ptr(w_r), _ptr(a_phi), _ptr(a_r), B, L, D,
+                                      _ptr(y), _ptr(y32), _ptr(hT), _stream(dev))
+    _check("samu_forward_noalloc", st)
+    return {"y": y, "y32": y32, "hT": hT}
 
 
 # ---------------------------------------------------------------------------

@@ -188,9 +188,24 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
     if (e != cudaSuccess) return LRS_ERR_CUDA;
     float4* modes = at<float4>(saved, sv.modes);
-    LRS_LAUNCH(KID_SAMU_PREP, stream,
-               launch_samu_prep(w_phi, w_r, a_phi, a_r, nu, theta, D, wh, misc, modes, stream));
-    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(x_sel, reset, wh, misc, BL, D, p, r, ctrl, stream));
+    SamuCtrlFwdArgs cf;
+    cf.BL = BL;
+    cf.D = D;
+    cf.x = static_cast<const uint4*>(x_sel);
+    cf.reset = reset;
+    cf.w_phi = w_phi;
+    cf.w_r = w_r;
+    cf.a_phi = a_phi;
+    cf.a_r = a_r;
+    cf.nu = nu;
+    cf.theta = theta;
+    cf.p = p;
+    cf.r = r;
+    cf.ctrl = ctrl;
+    cf.wh = wh;
+    cf.misc = misc;
+    cf.modes = modes;
+    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream));
 
     CUtensorMap tm_w;
     if (!make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;

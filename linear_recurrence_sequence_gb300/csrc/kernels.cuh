@@ -34,23 +34,37 @@ __device__ __forceinline__ ModeConst load_mode(const float4* __restrict__ modes,
     return k;
 }
 
-// ctl = {E - 1, C, S, reset}.  0 at a reset position.  Every pass that needs
-// lambda calls this, so the forward and the backward rebuild the same bits.
+// Per-token control word in shared memory: {E - 1, C, S, kind} with kind
+// kTokNormal, kTokReset (segment start: lambda = 0) or kTokPad (past the end
+// of the sequence: the token is skipped).  kind is the same for every lane,
+// so the branches on it are warp-uniform.
+constexpr float kTokNormal = 0.f;
+constexpr float kTokReset = 1.f;
+constexpr float kTokPad = 2.f;
+
+// Bound on |nu (E - 1)| under which the degree-3 polynomial below is exact to
+// < 2e-11 relative (the truncation term x^4/24), checked once per warp and tile.
+constexpr float kPolyBound = 1.0f / 64.0f;
+
+// lambda_{t,m} for a token that is not a reset: lbar_m * e^{-nu (E-1)} (C + iS).
+// FAST: e^{-x} by its degree-3 Taylor polynomial (valid for |x| < kPolyBound;
+// its rounding errors carry no per-mode bias); otherwise ex2.approx, whose
+// ~1e-7 error matters little for the short-memory modes that need it.
+// Every pass that needs lambda calls this, so the forward and the backward
+// rebuild the same bits.
+template <bool FAST>
 __device__ __forceinline__ float2 samu_lambda(const ModeConst& k, float4 ctl) {
     const float x = __fmul_rn(k.nu, ctl.x);                 // nu (E - 1)
     float q;                                                 // e^{-x}
-    if (fabsf(x) < 0.03125f) {
-        // degree-4 Taylor polynomial: truncation below 3e-10 relative
-        q = __fmaf_rn(x, __fmaf_rn(x, __fmaf_rn(x, __fmaf_rn(x, 1.0f / 24.0f, -1.0f / 6.0f), 0.5f), -1.0f), 1.0f);
+    if (FAST) {
+        q = __fmaf_rn(x, __fmaf_rn(x, __fmaf_rn(x, -1.0f / 6.0f, 0.5f), -1.0f), 1.0f);
     } else {
-        q = expf(-x);
+        q = ex2_approx(__fmul_rn(-x, kLog2e));
     }
     const float dr = __fmul_rn(q, ctl.y);
     const float di = __fmul_rn(q, ctl.z);
-    const float lr = __fmaf_rn(k.hr, dr, __fmaf_rn(-k.hi, di, k.lr));
-    const float li = __fmaf_rn(k.hr, di, __fmaf_rn(k.hi, dr, k.li));
-    const bool rs = ctl.w != 0.f;
-    return make_float2(rs ? 0.f : lr, rs ? 0.f : li);
+    return make_float2(__fmaf_rn(k.hr, dr, __fmaf_rn(-k.hi, di, k.lr)),
+                       __fmaf_rn(k.hr, di, __fmaf_rn(k.hi, dr, k.li)));
 }
 
 // One state step z' = lambda z + b, formed as u = lambda z then u + b.  The
@@ -124,7 +138,7 @@ struct SamuParamArgs {
     float2* numod2;         // [kReduceGroups][M]
     const float* dwh_part;  // [kCtrlBwdCtas * 2 halves][2][D+1]
     const float2* amp_part;
-    float* dwh;             // [2][D+1] column sums of dwh_part
+    float* dwh;             // [8 groups][2][D+1] column sums of dwh_part
     const float* wh;
     const float* misc;
     float* dnu;
@@ -135,12 +149,27 @@ struct SamuParamArgs {
     float* da_r;
 };
 
-cudaError_t launch_samu_prep(const float* w_phi, const float* w_r, const float* a_phi,
-                             const float* a_r, const float* nu, const float* theta, int D,
-                             float* wh, float* misc, float4* modes, cudaStream_t s);
-cudaError_t launch_samu_ctrl_fwd(const void* x, const uint8_t* reset, const float* wh,
-                                 const float* misc, long long BL, int D, float* p, float* r,
-                                 float4* ctrl, cudaStream_t s);
+struct SamuCtrlFwdArgs {
+    long long BL;
+    int D;
+    int n_mode_ctas, n_tok_ctas;   // filled by the launcher
+    const uint4* x;                // BF16 x_sel as 16-byte vectors
+    const uint8_t* reset;
+    const float* w_phi;
+    const float* w_r;
+    const float* a_phi;
+    const float* a_r;
+    const float* nu;
+    const float* theta;
+    float* p;
+    float* r;
+    float4* ctrl;                  // {E - 1, C, S, reset}
+    float* wh;                     // [2][D+1]
+    float* misc;
+    float4* modes;                 // [M] lbar hi/lo
+};
+
+cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s);
 cudaError_t launch_samu_scan_fwd(const CUtensorMap& tm_w, const SamuScanFwdArgs& args, cudaStream_t s);
 cudaError_t launch_samu_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_w,
                                  const SamuScanBwdArgs& args, cudaStream_t s);

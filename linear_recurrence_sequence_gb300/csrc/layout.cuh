@@ -91,7 +91,7 @@ inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     s.numod2 = o;   o = align_up(o + (size_t)kReduceGroups * M * 8);
     s.dwh_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 2 * 2 * (D + 1) * 4);   // (cta, half) rows
     s.amp_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 8);
-    s.dwh = o;      o = align_up(o + (size_t)2 * (D + 1) * 4);
+    s.dwh = o;      o = align_up(o + (size_t)8 * 2 * (D + 1) * 4);             // column-sum groups
     s.total = o;
     return s;
 }

@@ -91,10 +91,24 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     CUtensorMap tm_w;
     if (!make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;
     if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
-    if (launch_samu_prep(w_phi, w_r, a_phi, a_r, nu, theta, D, wh, misc, modes, stream) != cudaSuccess)
-        return LRS_ERR_CUDA;
-    if (launch_samu_ctrl_fwd(x_sel, reset, wh, misc, (long long)B * L, D, p, r, ctrl, stream) != cudaSuccess)
-        return LRS_ERR_CUDA;
+    SamuCtrlFwdArgs cf;
+    cf.BL = (long long)B * L;
+    cf.D = D;
+    cf.x = static_cast<const uint4*>(x_sel);
+    cf.reset = reset;
+    cf.w_phi = w_phi;
+    cf.w_r = w_r;
+    cf.a_phi = a_phi;
+    cf.a_r = a_r;
+    cf.nu = nu;
+    cf.theta = theta;
+    cf.p = p;
+    cf.r = r;
+    cf.ctrl = ctrl;
+    cf.wh = wh;
+    cf.misc = misc;
+    cf.modes = modes;
+    if (launch_samu_ctrl_fwd(cf, stream) != cudaSuccess) return LRS_ERR_CUDA;
 
     SamuScanFwdArgs a;
     a.g = g;

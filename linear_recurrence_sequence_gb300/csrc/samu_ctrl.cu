@@ -15,154 +15,181 @@
 namespace lrs {
 
 // ---------------------------------------------------------------------------
-// Prep (FP64, once per forward).  CTA 0: unit directions w_hat = w / ||w||
-// (norm over all D+1 entries) and the amplitude factors tanh(a)/sqrt(M).
-// CTAs 1..: the per-mode transition constant lbar_m = e^{-nu_m} e^{i theta_m}
-// as a double-float (hi, lo), one mode per thread.  Small CTAs spread the
-// FP64 work over many SMs.
+// Controller forward, with the parameter preparation folded in.
+//
+// Grid = n_mode CTAs followed by controller CTAs.
+//  - Mode CTAs (32 active threads each): the per-mode transition constant
+//    lbar_m = e^{-nu_m} e^{i theta_m} as a double-float (hi, lo) in FP64; they
+//    run alongside the streaming CTAs, off the critical path.
+//  - Controller CTAs: the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
+//    fixed-order tree, recomputed identically by every CTA); each thread then
+//    owns 8 consecutive channels with its 16 unit-direction weights in
+//    registers, and the CTA walks its token range in batches of 8 tokens: one
+//    16-byte load of x_sel per token per thread, 16 partial dot products per
+//    thread, a 16-shuffle reduce-scatter inside each warp, a fixed-order sum
+//    over the warps, and 8 threads evaluate p, r, q(r), d, c and the shared
+//    E - 1 = expm1(c), C = cos d, S = sin d for the 8 tokens in parallel.
+//    The first controller CTA stores w_hat and the amplitude factors for the
+//    backward.
 // ---------------------------------------------------------------------------
-constexpr int kPrepThreads = 32;
+constexpr int kCfTok = 8;              // tokens per batch
+constexpr int kModeThreads = 32;       // active threads of a mode CTA
 
-__global__ void __launch_bounds__(kPrepThreads) samu_prep_kernel(
-    const float* __restrict__ w_phi, const float* __restrict__ w_r, const float* __restrict__ a_phi,
-    const float* __restrict__ a_r, const float* __restrict__ nu, const float* __restrict__ theta, int D,
-    float* __restrict__ wh, float* __restrict__ misc, float4* __restrict__ modes) {
-    const int M = D / 2;
-    const int tid = threadIdx.x;
-    if (blockIdx.x > 0) {
-        const int m = (blockIdx.x - 1) * kPrepThreads + tid;
-        if (m < M) {
-            const double r = exp(-(double)nu[m]);
-            double sn, cs;
-            sincos((double)theta[m], &sn, &cs);
-            const double re = r * cs, im = r * sn;
-            const float hr = (float)re, hi = (float)im;
-            modes[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
-        }
-        return;
-    }
-    __shared__ double s_sum[2][kPrepThreads];
-    const int n = D + 1;
-    double sp = 0.0, sr = 0.0;
-    for (int j = tid; j < n; j += kPrepThreads) {
-        const double x = w_phi[j], y = w_r[j];
-        sp = fma(x, x, sp);
-        sr = fma(y, y, sr);
-    }
-    s_sum[0][tid] = sp;
-    s_sum[1][tid] = sr;
-    __syncwarp();
-    for (int s2 = kPrepThreads / 2; s2 > 0; s2 >>= 1) {
-        if (tid < s2) {
-            s_sum[0][tid] += s_sum[0][tid + s2];
-            s_sum[1][tid] += s_sum[1][tid + s2];
-        }
-        __syncwarp();
-    }
-    const double nphi = sqrt(s_sum[0][0]);
-    const double nr = sqrt(s_sum[1][0]);
-    const double inv_phi = 1.0 / nphi;
-    const double inv_r = 1.0 / nr;
-    for (int j = tid; j < n; j += kPrepThreads) {
-        wh[j] = (float)((double)w_phi[j] * inv_phi);
-        wh[n + j] = (float)((double)w_r[j] * inv_r);
-    }
-    if (tid == 0) {
-        const double inv_sqrt_m = 1.0 / sqrt((double)M);
-        const double ta = tanh((double)a_phi[0]);
-        const double tr = tanh((double)a_r[0]);
-        misc[0] = (float)(ta * inv_sqrt_m);
-        misc[1] = (float)(tr * inv_sqrt_m);
-        misc[2] = (float)nphi;
-        misc[3] = (float)nr;
-        misc[4] = (float)ta;
-        misc[5] = (float)tr;
-        misc[6] = (float)inv_sqrt_m;
-    }
+__device__ __forceinline__ void mode_constants(const float* __restrict__ nu, const float* __restrict__ theta,
+                                               int M, float4* __restrict__ modes, int m) {
+    if (m >= M) return;
+    const double r = exp(-(double)nu[m]);
+    double sn, cs;
+    sincos((double)theta[m], &sn, &cs);
+    const double re = r * cs, im = r * sn;
+    const float hr = (float)re, hi = (float)im;
+    modes[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
 }
 
-// ---------------------------------------------------------------------------
-// Controller forward: one warp per token, grid-stride over tokens.  The row
-// x_sel[t, :] is read once with 16-byte loads (all of a lane's vectors in
-// flight together); both projections accumulate in FP32; the lanes then
-// evaluate tanh, q(r), d, c and the shared special functions E - 1 =
-// expm1(c), C = cos d, S = sin d, and lane 0 stores them.
-// ---------------------------------------------------------------------------
-constexpr int kCtrlWarps = 8;
-
-template <int VPL>
-__global__ void __launch_bounds__(kCtrlWarps * 32) samu_ctrl_fwd_kernel(
-    const uint4* __restrict__ x, const uint8_t* __restrict__ reset, const float* __restrict__ wh,
-    const float* __restrict__ misc, long long BL, int D, float* __restrict__ p_out,
-    float* __restrict__ r_out, float4* __restrict__ ctrl) {
-    extern __shared__ __align__(16) float s_w[];   // [2][stride]: w_hat_phi, w_hat_r
+__global__ void __launch_bounds__(512) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
+    __shared__ float s_red[2][512 / 32];
+    __shared__ float s_part[512 / 32][2 * kCfTok];
+    const int tid = threadIdx.x;
+    const int D = a.D;
+    const int M = D / 2;
+    if ((int)blockIdx.x < a.n_mode_ctas) {
+        if (tid < kModeThreads) mode_constants(a.nu, a.theta, M, a.modes, blockIdx.x * kModeThreads + tid);
+        return;
+    }
+    const int cta = blockIdx.x - a.n_mode_ctas;
     const int n = D + 1;
-    const int stride = (n + 3) & ~3;                 // keeps both rows 16-byte aligned
-    for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        s_w[j] = wh[j];
-        s_w[stride + j] = wh[n + j];
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int nwarps = blockDim.x >> 5;
+
+    // norms (FP32, fixed order: per-thread strided sum, warp tree, warp-order sum)
+    float sp = 0.f, sr = 0.f;
+    for (int j = tid; j < n; j += blockDim.x) {
+        const float x = a.w_phi[j], y = a.w_r[j];
+        sp = fmaf(x, x, sp);
+        sr = fmaf(y, y, sr);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+        sr += __shfl_xor_sync(0xffffffffu, sr, o);
+    }
+    if (lane == 0) {
+        s_red[0][warp] = sp;
+        s_red[1][warp] = sr;
     }
     __syncthreads();
-    const float* s_phi = s_w;
-    const float* s_r = s_w + stride;
-    const float k_phi = misc[0];
-    const float k_r = misc[1];
-    const float bias_phi = s_phi[D];   // x~ carries a constant 1 against the bias weight
-    const float bias_r = s_r[D];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    float tp = 0.f, tr = 0.f;
+    for (int w = 0; w < nwarps; ++w) {
+        tp += s_red[0][w];
+        tr += s_red[1][w];
+    }
+    const float nphi = sqrtf(tp), nr = sqrtf(tr);
+    const float inv_phi = 1.0f / nphi, inv_r = 1.0f / nr;
+    const float ta = tanhf(a.a_phi[0]), tra = tanhf(a.a_r[0]);
+    const float ism = 1.0f / sqrtf((float)M);
+    const float k_phi = ta * ism, k_r = tra * ism;
     const int vecs = D / 8;
-    const long long nwarps = (long long)gridDim.x * kCtrlWarps;
-    for (long long t = (long long)blockIdx.x * kCtrlWarps + warp; t < BL; t += nwarps) {
-        const uint4* row = x + t * vecs;
-        uint4 q[VPL];
+    const bool col_ok = tid < vecs;
+    float wp[8], wr[8];
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int v = lane + 32 * k;
-            q[k] = (v < vecs) ? __ldcs(row + v) : make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < 8; ++k) {
+        wp[k] = col_ok ? a.w_phi[8 * tid + k] * inv_phi : 0.f;
+        wr[k] = col_ok ? a.w_r[8 * tid + k] * inv_r : 0.f;
+    }
+    const float bias_p = a.w_phi[D] * inv_phi, bias_r = a.w_r[D] * inv_r;
+    if (cta == 0) {
+        for (int j = tid; j < n; j += blockDim.x) {
+            a.wh[j] = a.w_phi[j] * inv_phi;
+            a.wh[n + j] = a.w_r[j] * inv_r;
         }
-        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+        if (tid == 0) {
+            a.misc[0] = k_phi;
+            a.misc[1] = k_r;
+            a.misc[2] = nphi;
+            a.misc[3] = nr;
+            a.misc[4] = ta;
+            a.misc[5] = tra;
+            a.misc[6] = ism;
+        }
+    }
+
+    const long long BL = a.BL;
+    const long long per = (BL + a.n_tok_ctas - 1) / a.n_tok_ctas;
+    const long long tb = (long long)cta * per;
+    const long long te = min(BL, tb + per);
+    for (long long t0 = tb; t0 < te; t0 += kCfTok) {
+        uint4 q[kCfTok];
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int v = lane + 32 * k;
-            if (v < vecs) {
-                const float2 x01 = bf2_to_f2(q[k].x), x23 = bf2_to_f2(q[k].y);
-                const float2 x45 = bf2_to_f2(q[k].z), x67 = bf2_to_f2(q[k].w);
-                const float4 p0 = *reinterpret_cast<const float4*>(s_phi + 8 * v);
-                const float4 p1 = *reinterpret_cast<const float4*>(s_phi + 8 * v + 4);
-                const float4 r0 = *reinterpret_cast<const float4*>(s_r + 8 * v);
-                const float4 r1 = *reinterpret_cast<const float4*>(s_r + 8 * v + 4);
-                a0 = fmaf(x01.x, p0.x, a0); a1 = fmaf(x01.y, p0.y, a1);
-                a0 = fmaf(x23.x, p0.z, a0); a1 = fmaf(x23.y, p0.w, a1);
-                a0 = fmaf(x45.x, p1.x, a0); a1 = fmaf(x45.y, p1.y, a1);
-                a0 = fmaf(x67.x, p1.z, a0); a1 = fmaf(x67.y, p1.w, a1);
-                b0 = fmaf(x01.x, r0.x, b0); b1 = fmaf(x01.y, r0.y, b1);
-                b0 = fmaf(x23.x, r0.z, b0); b1 = fmaf(x23.y, r0.w, b1);
-                b0 = fmaf(x45.x, r1.x, b0); b1 = fmaf(x45.y, r1.y, b1);
-                b0 = fmaf(x67.x, r1.z, b0); b1 = fmaf(x67.y, r1.w, b1);
+        for (int u = 0; u < kCfTok; ++u)
+            q[u] = (col_ok && t0 + u < te) ? __ldcs(a.x + (t0 + u) * vecs + tid) : make_uint4(0u, 0u, 0u, 0u);
+        float v[2 * kCfTok];   // v[2u] = phi partial of token u, v[2u+1] = r partial
+#pragma unroll
+        for (int u = 0; u < kCfTok; ++u) {
+            float2 f;
+            float ap = 0.f, ar = 0.f;
+            f = bf2_to_f2(q[u].x); ap = fmaf(f.x, wp[0], ap); ap = fmaf(f.y, wp[1], ap); ar = fmaf(f.x, wr[0], ar); ar = fmaf(f.y, wr[1], ar);
+            f = bf2_to_f2(q[u].y); ap = fmaf(f.x, wp[2], ap); ap = fmaf(f.y, wp[3], ap); ar = fmaf(f.x, wr[2], ar); ar = fmaf(f.y, wr[3], ar);
+            f = bf2_to_f2(q[u].z); ap = fmaf(f.x, wp[4], ap); ap = fmaf(f.y, wp[5], ap); ar = fmaf(f.x, wr[4], ar); ar = fmaf(f.y, wr[5], ar);
+            f = bf2_to_f2(q[u].w); ap = fmaf(f.x, wp[6], ap); ap = fmaf(f.y, wp[7], ap); ar = fmaf(f.x, wr[6], ar); ar = fmaf(f.y, wr[7], ar);
+            v[2 * u] = ap;
+            v[2 * u + 1] = ar;
+        }
+        // reduce-scatter of 16 values over the warp: after it, lanes 2i and
+        // 2i+1 both hold the warp sum of value sel(i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const bool hi = lane & 16;
+            const float send = hi ? v[k] : v[k + 8];
+            const float keep = hi ? v[k + 8] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const bool hi = lane & 8;
+            const float send = hi ? v[k] : v[k + 4];
+            const float keep = hi ? v[k + 4] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const bool hi = lane & 4;
+            const float send = hi ? v[k] : v[k + 2];
+            const float keep = hi ? v[k + 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        {
+            const bool hi = lane & 2;
+            const float send = hi ? v[0] : v[1];
+            const float keep = hi ? v[1] : v[0];
+            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        if ((lane & 1) == 0) {
+            const int sel = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+            s_part[warp][sel] = v[0];
+        }
+        __syncthreads();
+        if (tid < kCfTok && t0 + tid < te) {
+            const long long t = t0 + tid;
+            float s_phi = 0.f, s_r = 0.f;
+            for (int w = 0; w < nwarps; ++w) {
+                s_phi += s_part[w][2 * tid];
+                s_r += s_part[w][2 * tid + 1];
             }
-        }
-        float sphi = a0 + a1;
-        float sr = b0 + b1;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sphi += __shfl_xor_sync(0xffffffffu, sphi, o);
-            sr += __shfl_xor_sync(0xffffffffu, sr, o);
-        }
-        if (lane == 0) {
-            const float p = tanhf(sphi + bias_phi);
-            const float r = tanhf(sr + bias_r);
+            const float p = tanhf(s_phi + bias_p);
+            const float r = tanhf(s_r + bias_r);
             const float qr = r / (1.0f + r * r);
             const float d = k_phi * p;
             const float c = k_r * qr;
             float sn, cs;
             sincosf(d, &sn, &cs);
-            const float em1 = expm1f(c);
-            const float rs = (reset != nullptr && reset[t] != 0) ? 1.0f : 0.0f;
-            p_out[t] = p;
-            r_out[t] = r;
-            ctrl[t] = make_float4(em1, cs, sn, rs);
+            const float rs = (a.reset != nullptr && a.reset[t] != 0) ? 1.0f : 0.0f;
+            a.p[t] = p;
+            a.r[t] = r;
+            a.ctrl[t] = make_float4(expm1f(c), cs, sn, rs);
         }
+        __syncthreads();
     }
 }
 
@@ -180,9 +207,9 @@ __global__ void __launch_bounds__(kCtrlWarps * 32) samu_ctrl_fwd_kernel(
 // amplitude partials sum dbar p and sum cbar q(r).
 // ---------------------------------------------------------------------------
 constexpr int kCbTokBlock = 128;
-constexpr int kCbUnroll = 8;
+constexpr int kCbUnroll = 2;
 
-__global__ void __launch_bounds__(512) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
+__global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     __shared__ float s_sphi[kCbTokBlock];
     __shared__ float s_sr[kCbTokBlock];
     __shared__ float s_red[4][kCbTokBlock];
@@ -357,33 +384,49 @@ __global__ void __launch_bounds__(256) samu_numod_stage1_kernel(const float2* __
     numod2[(size_t)gidx * M + m] = make_float2(sx, sy);
 }
 
-// column sums of the controller-backward partial rows: dwh[which][j].  A CTA
-// takes 32 columns; its 8 warps each sum a strided set of rows, then the 8
-// warp sums are added in a fixed order.
+// stage 2: dnu[m], dtheta[m] = sum over the kReduceGroups first-stage sums
+__global__ void __launch_bounds__(256) samu_numod_stage2_kernel(const float2* __restrict__ numod2,
+                                                                float* __restrict__ dnu,
+                                                                float* __restrict__ dtheta, int M) {
+    const int m = blockIdx.x * blockDim.x + threadIdx.x;
+    if (m >= M) return;
+    float sx = 0.f, sy = 0.f;
+#pragma unroll 16
+    for (int gi = 0; gi < kReduceGroups; ++gi) {
+        const float2 v = numod2[(size_t)gi * M + m];
+        sx += v.x;
+        sy += v.y;
+    }
+    dnu[m] = sx;
+    dtheta[m] = sy;
+}
+
+// column sums of the controller-backward partial rows, first stage: CTA
+// (column block of 32, which in {phi, r}, row group z) -> colpart[z][which][j].
 constexpr int kColRows = 2 * kCtrlBwdCtas;
+constexpr int kColGroups = 8;
+constexpr int kColRowsPerGroup = (kColRows + kColGroups - 1) / kColGroups;
 
 __global__ void __launch_bounds__(256) samu_dwh_colsum_kernel(const float* __restrict__ part,
-                                                              float* __restrict__ dwh, int D) {
+                                                              float* __restrict__ colpart, int D) {
     __shared__ float s_part[8][32];
     const int n = D + 1;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int j = blockIdx.x * 32 + lane;
     const int which = blockIdx.y;
+    const int r0 = blockIdx.z * kColRowsPerGroup;
+    const int r1 = min(kColRows, r0 + kColRowsPerGroup);
     float s = 0.f;
     if (j < n) {
-        int k = warp;
-        for (; k + 8 * 3 < kColRows; k += 8 * 4) {
-            const float v0 = part[((size_t)k * 2 + which) * n + j];
-            const float v1 = part[((size_t)(k + 8) * 2 + which) * n + j];
-            const float v2 = part[((size_t)(k + 16) * 2 + which) * n + j];
-            const float v3 = part[((size_t)(k + 24) * 2 + which) * n + j];
-            s += v0;
-            s += v1;
-            s += v2;
-            s += v3;
+        float v[10];
+#pragma unroll
+        for (int k = 0; k < 10; ++k) {
+            const int r = r0 + warp + 8 * k;
+            v[k] = r < r1 ? part[((size_t)r * 2 + which) * n + j] : 0.f;
         }
-        for (; k < kColRows; k += 8) s += part[((size_t)k * 2 + which) * n + j];
+#pragma unroll
+        for (int k = 0; k < 10; ++k) s += v[k];
     }
     s_part[warp][lane] = s;
     __syncthreads();
@@ -391,33 +434,39 @@ __global__ void __launch_bounds__(256) samu_dwh_colsum_kernel(const float* __res
         float t = s_part[0][lane];
 #pragma unroll
         for (int w = 1; w < 8; ++w) t += s_part[w][lane];
-        dwh[which * n + j] = t;
+        colpart[((size_t)blockIdx.z * 2 + which) * n + j] = t;
     }
 }
 
-// final: dnu, dtheta; the unit-direction projection dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||;
-// the amplitude gradients da = (sum partials) / sqrt(M) * (1 - tanh(a)^2).
+// final: dwh = sum of the column groups; the unit-direction projection
+// dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||; the amplitude gradients
+// da = (sum of partials) / sqrt(M) * (1 - tanh(a)^2).
+constexpr int kMaxCols = 4097;
+
 __global__ void __launch_bounds__(256) samu_param_final_kernel(SamuParamArgs a) {
-    __shared__ float s_dot[2][256];
-    __shared__ float s_amp[2][256];
+    __shared__ float s_dwh[2][kMaxCols];
+    __shared__ float s_red[4][256];
     const int tid = threadIdx.x;
     const int D = a.D;
-    const int M = D / 2;
     const int n = D + 1;
-    for (int m = tid; m < M; m += blockDim.x) {
-        float sx = 0.f, sy = 0.f;
-        for (int gi = 0; gi < kReduceGroups; ++gi) {
-            const float2 v = a.numod2[(size_t)gi * M + m];
-            sx += v.x;
-            sy += v.y;
-        }
-        a.dnu[m] = sx;
-        a.dtheta[m] = sy;
-    }
     float dp = 0.f, dr = 0.f;
     for (int j = tid; j < n; j += blockDim.x) {
-        dp = fmaf(a.wh[j], a.dwh[j], dp);
-        dr = fmaf(a.wh[n + j], a.dwh[n + j], dr);
+        float v[2][kColGroups];
+#pragma unroll
+        for (int z = 0; z < kColGroups; ++z) {
+            v[0][z] = a.dwh[((size_t)z * 2 + 0) * n + j];
+            v[1][z] = a.dwh[((size_t)z * 2 + 1) * n + j];
+        }
+        float sp = 0.f, sr = 0.f;
+#pragma unroll
+        for (int z = 0; z < kColGroups; ++z) {
+            sp += v[0][z];
+            sr += v[1][z];
+        }
+        s_dwh[0][j] = sp;
+        s_dwh[1][j] = sr;
+        dp = fmaf(a.wh[j], sp, dp);
+        dr = fmaf(a.wh[n + j], sr, dr);
     }
     float ap = 0.f, ar = 0.f;
     for (int k = tid; k < kCtrlBwdCtas; k += blockDim.x) {
@@ -425,70 +474,43 @@ __global__ void __launch_bounds__(256) samu_param_final_kernel(SamuParamArgs a) 
         ap += v.x;
         ar += v.y;
     }
-    s_dot[0][tid] = dp;
-    s_dot[1][tid] = dr;
-    s_amp[0][tid] = ap;
-    s_amp[1][tid] = ar;
+    s_red[0][tid] = dp;
+    s_red[1][tid] = dr;
+    s_red[2][tid] = ap;
+    s_red[3][tid] = ar;
     __syncthreads();
-    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-        if (tid < s) {
-            s_dot[0][tid] += s_dot[0][tid + s];
-            s_dot[1][tid] += s_dot[1][tid + s];
-            s_amp[0][tid] += s_amp[0][tid + s];
-            s_amp[1][tid] += s_amp[1][tid + s];
+    for (int s2 = blockDim.x / 2; s2 > 0; s2 >>= 1) {
+        if (tid < s2) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s_red[q][tid] += s_red[q][tid + s2];
         }
         __syncthreads();
     }
-    const float dot_p = s_dot[0][0];
-    const float dot_r = s_dot[1][0];
+    const float dot_p = s_red[0][0];
+    const float dot_r = s_red[1][0];
     const float nphi = a.misc[2];
     const float nr = a.misc[3];
     for (int j = tid; j < n; j += blockDim.x) {
-        a.dw_phi[j] = (a.dwh[j] - a.wh[j] * dot_p) / nphi;
-        a.dw_r[j] = (a.dwh[n + j] - a.wh[n + j] * dot_r) / nr;
+        a.dw_phi[j] = (s_dwh[0][j] - a.wh[j] * dot_p) / nphi;
+        a.dw_r[j] = (s_dwh[1][j] - a.wh[n + j] * dot_r) / nr;
     }
     if (tid == 0) {
         const float ta = a.misc[4], tr = a.misc[5], ism = a.misc[6];
-        a.da_phi[0] = s_amp[0][0] * ism * (1.0f - ta * ta);
-        a.da_r[0] = s_amp[1][0] * ism * (1.0f - tr * tr);
+        a.da_phi[0] = s_red[2][0] * ism * (1.0f - ta * ta);
+        a.da_r[0] = s_red[3][0] * ism * (1.0f - tr * tr);
     }
 }
 
-cudaError_t launch_samu_prep(const float* w_phi, const float* w_r, const float* a_phi,
-                             const float* a_r, const float* nu, const float* theta, int D,
-                             float* wh, float* misc, float4* modes, cudaStream_t s) {
-    const int M = D / 2;
-    const int grid = 1 + (M + kPrepThreads - 1) / kPrepThreads;
-    samu_prep_kernel<<<grid, kPrepThreads, 0, s>>>(w_phi, w_r, a_phi, a_r, nu, theta, D, wh, misc, modes);
+cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args_in, cudaStream_t s) {
+    SamuCtrlFwdArgs a = args_in;
+    const int M = a.D / 2;
+    int cols = ((a.D / 8) + 31) / 32 * 32;
+    if (cols < 64) cols = 64;
+    a.n_mode_ctas = (M + kModeThreads - 1) / kModeThreads;
+    const long long want = (a.BL + kCfTok - 1) / kCfTok;
+    a.n_tok_ctas = (int)(want < 152LL * 4 ? want : 152LL * 4);
+    samu_ctrl_fwd_kernel<<<a.n_mode_ctas + a.n_tok_ctas, cols, 0, s>>>(a);
     return cudaGetLastError();
-}
-
-template <int VPL>
-static cudaError_t launch_ctrl_fwd_t(const void* x, const uint8_t* reset, const float* wh,
-                                     const float* misc, long long BL, int D, float* p, float* r,
-                                     float4* ctrl, cudaStream_t s) {
-    const size_t smem = (size_t)2 * ((D + 1 + 3) & ~3) * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(samu_ctrl_fwd_kernel<VPL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    const long long want = (BL + kCtrlWarps - 1) / kCtrlWarps;
-    const long long grid = want < 152LL * 4 ? want : 152LL * 4;
-    samu_ctrl_fwd_kernel<VPL><<<(unsigned)grid, kCtrlWarps * 32, smem, s>>>(
-        reinterpret_cast<const uint4*>(x), reset, wh, misc, BL, D, p, r, ctrl);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_samu_ctrl_fwd(const void* x, const uint8_t* reset, const float* wh,
-                                 const float* misc, long long BL, int D, float* p, float* r,
-                                 float4* ctrl, cudaStream_t s) {
-    const int need = (D / 8 + 31) / 32;   // 16-byte vectors per lane
-    if (need <= 1) return launch_ctrl_fwd_t<1>(x, reset, wh, misc, BL, D, p, r, ctrl, s);
-    if (need <= 2) return launch_ctrl_fwd_t<2>(x, reset, wh, misc, BL, D, p, r, ctrl, s);
-    if (need <= 4) return launch_ctrl_fwd_t<4>(x, reset, wh, misc, BL, D, p, r, ctrl, s);
-    if (need <= 8) return launch_ctrl_fwd_t<8>(x, reset, wh, misc, BL, D, p, r, ctrl, s);
-    return launch_ctrl_fwd_t<16>(x, reset, wh, misc, BL, D, p, r, ctrl, s);
 }
 
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s) {
@@ -506,7 +528,10 @@ cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s) {
     samu_numod_stage1_kernel<<<g1, 256, 0, s>>>(args.numod, args.numod2, rows, M);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 g2((args.D + 1 + 31) / 32, 2);
+    samu_numod_stage2_kernel<<<(M + 255) / 256, 256, 0, s>>>(args.numod2, args.dnu, args.dtheta, M);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g2((args.D + 1 + 31) / 32, 2, kColGroups);
     samu_dwh_colsum_kernel<<<g2, 256, 0, s>>>(args.dwh_part, args.dwh, args.D);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

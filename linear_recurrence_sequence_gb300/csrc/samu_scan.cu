@@ -22,6 +22,73 @@
 
 namespace lrs {
 
+// Warp-uniform choice of the lambda variant for one sub-chunk: the polynomial
+// path when |nu| max|E - 1| < kPolyBound for every lane's modes.
+__device__ __forceinline__ bool use_fast_lambda(const float4* sc, int lane, const ModeConst& k0,
+                                                const ModeConst& k1) {
+    float e = 0.f;
+    if (lane < kSub) {
+        const float4 ct = sc[lane];
+        if (ct.w == kTokNormal) e = fabsf(ct.x);
+    }
+    const float emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(e)));
+    const bool ok = fabsf(k0.nu) * emax < kPolyBound && fabsf(k1.nu) * emax < kPolyBound;
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------------------
+// Forward: sub-chunk summary and replay.  sc = the warp's 16 control words,
+// wre/wim = the lane's column of the staged w box (row stride kGroup/2 words).
+// ---------------------------------------------------------------------------
+template <bool FAST>
+__device__ __forceinline__ void fwd_summary(const float4* sc, const uint32_t* wre, const uint32_t* wim,
+                                            const ModeConst& k0, const ModeConst& k1, float4& S0, float4& S1) {
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        const float4 ct = sc[i];
+        if (ct.w == kTokPad) break;
+        const float2 br = bf2_to_f2(wre[i * (kGroup / 2)]);
+        const float2 bi = bf2_to_f2(wim[i * (kGroup / 2)]);
+        if (ct.w == kTokNormal) {
+            S0 = compose_step(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), S0);
+            S1 = compose_step(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), S1);
+        } else {   // segment start: lambda = 0
+            S0 = make_float4(0.f, 0.f, br.x, bi.x);
+            S1 = make_float4(0.f, 0.f, br.y, bi.y);
+        }
+    }
+}
+
+template <bool FAST>
+__device__ __forceinline__ void fwd_replay(const float4* sc, const uint32_t* wre, const uint32_t* wim,
+                                           const ModeConst& k0, const ModeConst& k1, float2& z0, float2& z1,
+                                           uint32_t* yp, float* y32p, bool active, size_t row_words, int half_words) {
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        const float4 ct = sc[i];
+        if (ct.w == kTokPad) break;
+        const float2 br = bf2_to_f2(wre[i * (kGroup / 2)]);
+        const float2 bi = bf2_to_f2(wim[i * (kGroup / 2)]);
+        if (ct.w == kTokNormal) {
+            z0 = step_state(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), z0);
+            z1 = step_state(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), z1);
+        } else {
+            z0 = make_float2(br.x, bi.x);
+            z1 = make_float2(br.y, bi.y);
+        }
+        if (active) {
+            uint32_t* o = yp + (size_t)i * row_words;
+            __stcs(o, f2_to_bf2(z0.x, z1.x));
+            __stcs(o + half_words, f2_to_bf2(z0.y, z1.y));
+            if (y32p != nullptr) {
+                float* f = y32p + (size_t)i * 2 * row_words;
+                *reinterpret_cast<float2*>(f) = make_float2(z0.x, z1.x);
+                *reinterpret_cast<float2*>(f + 2 * half_words) = make_float2(z0.y, z1.y);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
@@ -66,7 +133,12 @@ __global__ void __launch_bounds__(kScanThreads, 3)
     }
     if (tid < kTile) {
         const int t = t0 + tid;
-        s_ctrl[tid] = t < L ? a.ctrl[(size_t)b * L + t] : make_float4(0.f, 1.f, 0.f, 0.f);
+        float4 ct = make_float4(0.f, 1.f, 0.f, kTokPad);
+        if (t < L) {
+            ct = a.ctrl[(size_t)b * L + t];
+            ct.w = ct.w != 0.f ? kTokReset : kTokNormal;
+        }
+        s_ctrl[tid] = ct;
     }
     ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
     if (active) {
@@ -84,24 +156,23 @@ __global__ void __launch_bounds__(kScanThreads, 3)
         mbar_wait_bounded(&s_bar, 0);
         return;
     }
+    const float4* sc = s_ctrl + r0;
+    const uint32_t* wre = &s_wre[r0][lane];
+    const uint32_t* wim = &s_wim[r0][lane];
+    const bool fast = use_fast_lambda(sc, lane, k0, k1);
 
     // sub-chunk summary S_w = T_e o ... o T_s
     float4 S0 = make_float4(1.f, 0.f, 0.f, 0.f), S1 = S0;
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        if (i < nsub) {
-            const float4 ct = s_ctrl[r0 + i];
-            const float2 br = bf2_to_f2(s_wre[r0 + i][lane]);
-            const float2 bi = bf2_to_f2(s_wim[r0 + i][lane]);
-            S0 = compose_step(samu_lambda(k0, ct), make_float2(br.x, bi.x), S0);
-            S1 = compose_step(samu_lambda(k1, ct), make_float2(br.y, bi.y), S1);
-        }
-    }
+    if (fast)
+        fwd_summary<true>(sc, wre, wim, k0, k1, S0, S1);
+    else
+        fwd_summary<false>(sc, wre, wim, k0, k1, S0, S1);
     s_map[warp][lane][0] = S0;
     s_map[warp][lane][1] = S1;
     __syncthreads();
 
-    // warp 0: tile map, look-back, entry states of the 8 sub-chunks, publish
+    // warp 0: tile map, entry state (directly from the previous tile when its
+    // state is already out, else by look-back), publish, sub-chunk entries
     if (warp == 0) {
         float4 A0 = s_map[0][lane][0], A1 = s_map[0][lane][1];
 #pragma unroll
@@ -119,15 +190,20 @@ __global__ void __launch_bounds__(kScanThreads, 3)
                 h1v = make_float2(hv.z, hv.w);
             }
         } else {
-            if (active) {
-                float4* ag = a.agg + ((size_t)b * CT + c) * M + m;
-                ag[0] = A0;
-                ag[1] = A1;
+            int j = -1;
+            if (ld_acquire_gpu(fl + c - 1) == kFlagIncl) {
+                j = c - 1;
+            } else {
+                if (active) {
+                    float4* ag = a.agg + ((size_t)b * CT + c) * M + m;
+                    ag[0] = A0;
+                    ag[1] = A1;
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
+                j = lookback_find_warp(fl, c, CT, -1);
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
-            const int j = lookback_find_warp(fl, c, CT, -1);
             if (j < 0) {
                 err = true;
             } else if (active) {
@@ -156,6 +232,16 @@ __global__ void __launch_bounds__(kScanThreads, 3)
             }
         }
         if (!err) {
+            if (active) {
+                const float2 i0 = capply(A0, h0v);
+                const float2 i1 = capply(A1, h1v);
+                *reinterpret_cast<float4*>(a.hsub + (hb + (size_t)(c + 1) * kScanWarps) * M + m) =
+                    make_float4(i0.x, i0.y, i1.x, i1.y);
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
+            // entry states of the sub-chunks (also kept for the backward)
             float2 e0 = h0v, e1 = h1v;
 #pragma unroll
             for (int w = 0; w < kScanWarps; ++w) {
@@ -166,15 +252,6 @@ __global__ void __launch_bounds__(kScanThreads, 3)
                 e0 = capply(s_map[w][lane][0], e0);
                 e1 = capply(s_map[w][lane][1], e1);
             }
-            if (active) {
-                const float2 i0 = capply(A0, h0v);
-                const float2 i1 = capply(A1, h1v);
-                *reinterpret_cast<float4*>(a.hsub + (hb + (size_t)(c + 1) * kScanWarps) * M + m) =
-                    make_float4(i0.x, i0.y, i1.x, i1.y);
-            }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
         } else if (lane == 0) {
             st_release_gpu(fl + c, kFlagErr);
             atomicOr(a.status, kStatusTimeout);
@@ -188,44 +265,126 @@ __global__ void __launch_bounds__(kScanThreads, 3)
     const float4 e = s_ent[warp][lane];
     float2 z0 = make_float2(e.x, e.y), z1 = make_float2(e.z, e.w);
     const size_t yrow = (((size_t)b * L + t0 + r0) * D + m) / 2;
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        if (i < nsub) {
-            const float4 ct = s_ctrl[r0 + i];
-            const float2 br = bf2_to_f2(s_wre[r0 + i][lane]);
-            const float2 bi = bf2_to_f2(s_wim[r0 + i][lane]);
-            z0 = step_state(samu_lambda(k0, ct), make_float2(br.x, bi.x), z0);
-            z1 = step_state(samu_lambda(k1, ct), make_float2(br.y, bi.y), z1);
-            if (active) {
-                const size_t o = yrow + (size_t)i * (D / 2);
-                __stcs(a.y + o, f2_to_bf2(z0.x, z1.x));
-                __stcs(a.y + o + M / 2, f2_to_bf2(z0.y, z1.y));
-                if (a.y32 != nullptr) {
-                    *reinterpret_cast<float2*>(a.y32 + 2 * o) = make_float2(z0.x, z1.x);
-                    *reinterpret_cast<float2*>(a.y32 + 2 * o + M) = make_float2(z0.y, z1.y);
-                }
-            }
-        }
-    }
+    uint32_t* yp = a.y + yrow;
+    float* y32p = a.y32 != nullptr ? a.y32 + 2 * yrow : nullptr;
+    if (fast)
+        fwd_replay<true>(sc, wre, wim, k0, k1, z0, z1, yp, y32p, active, D / 2, M / 2);
+    else
+        fwd_replay<false>(sc, wre, wim, k0, k1, z0, z1, yp, y32p, active, D / 2, M / 2);
     if (active && nsub > 0 && t0 + r0 + nsub == L)
         *reinterpret_cast<float4*>(a.hT + ((size_t)b * M + m) * 2) = make_float4(z0.x, z0.y, z1.x, z1.y);
 }
 
 // ---------------------------------------------------------------------------
-// Backward
-//
+// Backward: forward sweep (rebuild u_t = lambda_t z_{t-1} and the reverse map
+// of the sub-chunk) and reverse sweep (adjoint, dw, kappa sums).
+// ---------------------------------------------------------------------------
+template <bool FAST>
+__device__ __forceinline__ void bwd_forward_sweep(const float4* sc, const uint32_t* wre, const uint32_t* wim,
+                                                  const uint32_t* gre, const uint32_t* gim, const ModeConst& k0,
+                                                  const ModeConst& k1, float2 z0, float2 z1, float4 (&u)[kSub],
+                                                  float4& F0, float4& F1) {
+    float2 P0 = make_float2(1.f, 0.f), P1 = P0;
+    float2 q0 = make_float2(0.f, 0.f), q1 = q0;
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 ct = sc[i];
+        if (ct.w == kTokPad) continue;
+        const float2 br = bf2_to_f2(wre[i * (kGroup / 2)]);
+        const float2 bi = bf2_to_f2(wim[i * (kGroup / 2)]);
+        if (ct.w == kTokNormal) {
+            const float2 gr = bf2_to_f2(gre[i * (kGroup / 2)]);
+            const float2 gi = bf2_to_f2(gim[i * (kGroup / 2)]);
+            const float2 l0 = samu_lambda<FAST>(k0, ct);
+            const float2 l1 = samu_lambda<FAST>(k1, ct);
+            float2 u0, u1;
+            z0 = step_state(l0, make_float2(br.x, bi.x), z0, &u0);
+            z1 = step_state(l1, make_float2(br.y, bi.y), z1, &u1);
+            u[i] = make_float4(u0.x, u0.y, u1.x, u1.y);
+            P0 = cmul(l0, P0);
+            P1 = cmul(l1, P1);
+            const float2 c0 = cmulc(P0, make_float2(gr.x, gi.x));
+            const float2 c1 = cmulc(P1, make_float2(gr.y, gi.y));
+            q0 = make_float2(q0.x + c0.x, q0.y + c0.y);
+            q1 = make_float2(q1.x + c1.x, q1.y + c1.y);
+        } else {   // segment start: lambda = 0, nothing later reaches back past it
+            z0 = make_float2(br.x, bi.x);
+            z1 = make_float2(br.y, bi.y);
+            P0 = make_float2(0.f, 0.f);
+            P1 = P0;
+        }
+    }
+    F0 = make_float4(P0.x, -P0.y, q0.x, q0.y);
+    F1 = make_float4(P1.x, -P1.y, q1.x, q1.y);
+}
+
+template <bool FAST>
+__device__ __forceinline__ void bwd_reverse_sweep(const float4* sc, const uint32_t* gre, const uint32_t* gim,
+                                                  const ModeConst& k0, const ModeConst& k1, const float4 (&u)[kSub],
+                                                  float2& A0, float2& A1, float4& acc, uint32_t* dwb, float* dwf,
+                                                  bool fp32, bool active, size_t row_words, int half_words,
+                                                  float2* kp, int kp_stride, int lane) {
+#pragma unroll
+    for (int i = kSub - 1; i >= 0; --i) {
+        const float4 ct = sc[i];
+        if (ct.w == kTokPad) continue;
+        const float2 gr = bf2_to_f2(gre[i * (kGroup / 2)]);
+        const float2 gi = bf2_to_f2(gim[i * (kGroup / 2)]);
+        A0 = make_float2(A0.x + gr.x, A0.y + gi.x);
+        A1 = make_float2(A1.x + gr.y, A1.y + gi.y);
+        if (active) {
+            if (fp32) {
+                float* p = dwf + 2 * (size_t)i * row_words;
+                *reinterpret_cast<float2*>(p) = make_float2(A0.x, A1.x);
+                *reinterpret_cast<float2*>(p + 2 * half_words) = make_float2(A0.y, A1.y);
+            } else {
+                uint32_t* p = dwb + (size_t)i * row_words;
+                __stcs(p, f2_to_bf2(A0.x, A1.x));
+                __stcs(p + half_words, f2_to_bf2(A0.y, A1.y));
+            }
+        }
+        if (ct.w == kTokNormal) {
+            // kappa = A conj(u)
+            const float4 uu = u[i];
+            const float kr0 = __fmaf_rn(A0.x, uu.x, __fmul_rn(A0.y, uu.y));
+            const float ki0 = __fmaf_rn(A0.y, uu.x, -__fmul_rn(A0.x, uu.y));
+            const float kr1 = __fmaf_rn(A1.x, uu.z, __fmul_rn(A1.y, uu.w));
+            const float ki1 = __fmaf_rn(A1.y, uu.z, -__fmul_rn(A1.x, uu.w));
+            const float Et = 1.0f + ct.x;   // ct.x holds E - 1
+            acc.x = __fmaf_rn(-Et, kr0, acc.x);   // dnu_m
+            acc.y += ki0;                         // dtheta_m
+            acc.z = __fmaf_rn(-Et, kr1, acc.z);
+            acc.w += ki1;
+            float td = ki0 + ki1;
+            float te = -__fmaf_rn(k0.nu, kr0, __fmul_rn(k1.nu, kr1));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                td += __shfl_xor_sync(0xffffffffu, td, o);
+                te += __shfl_xor_sync(0xffffffffu, te, o);
+            }
+            if (lane == 0) kp[(size_t)i * kp_stride] = make_float2(td, te);
+            A0 = cmulc(samu_lambda<FAST>(k0, ct), A0);
+            A1 = cmulc(samu_lambda<FAST>(k1, ct), A1);
+        } else {   // segment start: no controller terms, the adjoint stops here
+            if (lane == 0) kp[(size_t)i * kp_stride] = make_float2(0.f, 0.f);
+            A0 = make_float2(0.f, 0.f);
+            A1 = A0;
+        }
+    }
+}
+
 // Tiles in reverse time order.  Forward sweep of each sub-chunk from its saved
 // entry state rebuilds lambda_t, u_t = lambda_t z_{t-1} (kept in registers for
 // kappa) and z_t, and accumulates the prefix product P_t = lambda_s..lambda_t
 // and q = sum_t conj(P_t) dy_t: the sub-chunk maps an adjoint R arriving at its
 // last token to the adjoint leaving it towards the past, R' = conj(P_e) R + q.
-// Warp 0 composes the 8 sub-chunk maps, looks back over later tiles, and hands
-// each sub-chunk its incoming adjoint.  Reverse sweep: A_t = dy_t + (adjoint
-// from t+1); dw_t = A_t; kappa_t = A_t conj(u_t);
-//   dtheta_m += Im kappa, dnu_m += -E_t Re kappa,
-//   dbar_t   += Im kappa, Ebar_t += -nu_m Re kappa  (reduced over the 64 modes
-//   of the warp and written as one per-token partial per mode group).
-// ---------------------------------------------------------------------------
+// Warp 0 composes the 8 sub-chunk maps, takes the incoming adjoint from the
+// next tile (or by look-back), and hands each sub-chunk its incoming adjoint.
+// Reverse sweep: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
+// kappa_t = A_t conj(u_t);  dtheta_m += Im kappa, dnu_m += -E_t Re kappa,
+// dbar_t += Im kappa, Ebar_t += -nu_m Re kappa (reduced over the 64 modes of
+// the warp: one per-token partial per mode group).
 __global__ void __launch_bounds__(kScanThreads, 2)
     samu_scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
                          SamuScanBwdArgs a) {
@@ -275,7 +434,12 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     }
     if (tid < kTile) {
         const int t = t0 + tid;
-        s_ctrl[tid] = t < L ? a.ctrl[(size_t)b * L + t] : make_float4(0.f, 1.f, 0.f, 0.f);
+        float4 ct = make_float4(0.f, 1.f, 0.f, kTokPad);
+        if (t < L) {
+            ct = a.ctrl[(size_t)b * L + t];
+            ct.w = ct.w != 0.f ? kTokReset : kTokNormal;
+        }
+        s_ctrl[tid] = ct;
     }
     ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
     const int r0 = warp * kSub;
@@ -300,39 +464,24 @@ __global__ void __launch_bounds__(kScanThreads, 2)
         mbar_wait_bounded(&s_bar, 0);
         return;
     }
+    const float4* sc = s_ctrl + r0;
+    const uint32_t* wre = &s_wre[r0][lane];
+    const uint32_t* wim = &s_wim[r0][lane];
+    const uint32_t* gre = &s_gre[r0][lane];
+    const uint32_t* gim = &s_gim[r0][lane];
+    const bool fast = use_fast_lambda(sc, lane, k0, k1);
 
-    // forward sweep
     float4 u[kSub];   // {u_m, u_m+1} per token
-    float2 P0 = make_float2(1.f, 0.f), P1 = P0;
-    float2 q0 = make_float2(0.f, 0.f), q1 = q0;
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < nsub) {
-            const float4 ct = s_ctrl[r0 + i];
-            const float2 l0 = samu_lambda(k0, ct);
-            const float2 l1 = samu_lambda(k1, ct);
-            const float2 br = bf2_to_f2(s_wre[r0 + i][lane]);
-            const float2 bi = bf2_to_f2(s_wim[r0 + i][lane]);
-            const float2 gr = bf2_to_f2(s_gre[r0 + i][lane]);
-            const float2 gi = bf2_to_f2(s_gim[r0 + i][lane]);
-            float2 u0, u1;
-            z0 = step_state(l0, make_float2(br.x, bi.x), z0, &u0);
-            z1 = step_state(l1, make_float2(br.y, bi.y), z1, &u1);
-            u[i] = make_float4(u0.x, u0.y, u1.x, u1.y);
-            P0 = cmul(l0, P0);
-            P1 = cmul(l1, P1);
-            const float2 c0 = cmulc(P0, make_float2(gr.x, gi.x));
-            const float2 c1 = cmulc(P1, make_float2(gr.y, gi.y));
-            q0 = make_float2(q0.x + c0.x, q0.y + c0.y);
-            q1 = make_float2(q1.x + c1.x, q1.y + c1.y);
-        }
-    }
-    s_map[warp][lane][0] = make_float4(P0.x, -P0.y, q0.x, q0.y);
-    s_map[warp][lane][1] = make_float4(P1.x, -P1.y, q1.x, q1.y);
+    float4 F0, F1;
+    if (fast)
+        bwd_forward_sweep<true>(sc, wre, wim, gre, gim, k0, k1, z0, z1, u, F0, F1);
+    else
+        bwd_forward_sweep<false>(sc, wre, wim, gre, gim, k0, k1, z0, z1, u, F0, F1);
+    s_map[warp][lane][0] = F0;
+    s_map[warp][lane][1] = F1;
     __syncthreads();
 
-    // warp 0: reverse tile map F_0 o F_1 o ... o F_7 (F_7 first), look-back, incoming adjoints
+    // warp 0: reverse tile map F_0 o F_1 o ... o F_7 (F_7 first), incoming adjoint, hand-out
     if (warp == 0) {
         float4 A0 = s_map[kScanWarps - 1][lane][0], A1 = s_map[kScanWarps - 1][lane][1];
 #pragma unroll
@@ -349,15 +498,20 @@ __global__ void __launch_bounds__(kScanThreads, 2)
                 R1 = make_float2(v.z, v.w);
             }
         } else {
-            if (active) {
-                float4* ag = a.agg + ((size_t)b * CT + c) * M + m;
-                ag[0] = A0;
-                ag[1] = A1;
+            int j = -1;
+            if (ld_acquire_gpu(fl + c + 1) == kFlagIncl) {
+                j = c + 1;
+            } else {
+                if (active) {
+                    float4* ag = a.agg + ((size_t)b * CT + c) * M + m;
+                    ag[0] = A0;
+                    ag[1] = A1;
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
+                j = lookback_find_warp(fl, c, CT, +1);
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
-            const int j = lookback_find_warp(fl, c, CT, +1);
             if (j < 0) {
                 err = true;
             } else if (active) {
@@ -385,13 +539,6 @@ __global__ void __launch_bounds__(kScanThreads, 2)
             }
         }
         if (!err) {
-            float2 r0v = R0, r1v = R1;
-#pragma unroll
-            for (int w = kScanWarps - 1; w >= 0; --w) {
-                s_ent[w][lane] = make_float4(r0v.x, r0v.y, r1v.x, r1v.y);
-                r0v = capply(s_map[w][lane][0], r0v);
-                r1v = capply(s_map[w][lane][1], r1v);
-            }
             if (active) {
                 const float2 o0 = capply(A0, R0);
                 const float2 o1 = capply(A1, R1);
@@ -400,6 +547,13 @@ __global__ void __launch_bounds__(kScanThreads, 2)
             __threadfence();
             __syncwarp();
             if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
+            float2 r0v = R0, r1v = R1;
+#pragma unroll
+            for (int w = kScanWarps - 1; w >= 0; --w) {
+                s_ent[w][lane] = make_float4(r0v.x, r0v.y, r1v.x, r1v.y);
+                r0v = capply(s_map[w][lane][0], r0v);
+                r1v = capply(s_map[w][lane][1], r1v);
+            }
         } else if (lane == 0) {
             st_release_gpu(fl + c, kFlagErr);
             atomicOr(a.status, kStatusTimeout);
@@ -412,56 +566,20 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     // reverse sweep
     const float4 e = s_ent[warp][lane];
     float2 A0 = make_float2(e.x, e.y), A1 = make_float2(e.z, e.w);
-    float dnu0 = 0.f, dth0 = 0.f, dnu1 = 0.f, dth1 = 0.f;
-    const float nu0 = k0.nu, nu1 = k1.nu;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // dnu_m, dtheta_m, dnu_m+1, dtheta_m+1
     const size_t row = (((size_t)b * L + t0 + r0) * D + m) / 2;
-    uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw);
-    float* dwf = reinterpret_cast<float*>(a.dw);
+    uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row;
+    float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row;
     float2* kp = a.kpart + ((size_t)b * L + t0 + r0) * g.n_groups + grp;
-#pragma unroll
-    for (int i = kSub - 1; i >= 0; --i) {
-        if (i < nsub) {
-            const float4 ct = s_ctrl[r0 + i];
-            const float2 gr = bf2_to_f2(s_gre[r0 + i][lane]);
-            const float2 gi = bf2_to_f2(s_gim[r0 + i][lane]);
-            A0 = make_float2(A0.x + gr.x, A0.y + gi.x);
-            A1 = make_float2(A1.x + gr.y, A1.y + gi.y);
-            if (active) {
-                const size_t o = row + (size_t)i * (D / 2);
-                if (a.grad_fp32) {
-                    *reinterpret_cast<float2*>(dwf + 2 * o) = make_float2(A0.x, A1.x);
-                    *reinterpret_cast<float2*>(dwf + 2 * o + M) = make_float2(A0.y, A1.y);
-                } else {
-                    __stcs(dwb + o, f2_to_bf2(A0.x, A1.x));
-                    __stcs(dwb + o + M / 2, f2_to_bf2(A0.y, A1.y));
-                }
-            }
-            // kappa = A conj(u)
-            const float4 uu = u[i];
-            const float kr0 = __fmaf_rn(A0.x, uu.x, __fmul_rn(A0.y, uu.y));
-            const float ki0 = __fmaf_rn(A0.y, uu.x, -__fmul_rn(A0.x, uu.y));
-            const float kr1 = __fmaf_rn(A1.x, uu.z, __fmul_rn(A1.y, uu.w));
-            const float ki1 = __fmaf_rn(A1.y, uu.z, -__fmul_rn(A1.x, uu.w));
-            const float Et = 1.0f + ct.x;   // ctl.x holds E - 1
-            dth0 += ki0;
-            dth1 += ki1;
-            dnu0 = __fmaf_rn(-Et, kr0, dnu0);
-            dnu1 = __fmaf_rn(-Et, kr1, dnu1);
-            float td = ki0 + ki1;
-            float te = -__fmaf_rn(nu0, kr0, __fmul_rn(nu1, kr1));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                td += __shfl_xor_sync(0xffffffffu, td, o);
-                te += __shfl_xor_sync(0xffffffffu, te, o);
-            }
-            if (lane == 0) kp[(size_t)i * g.n_groups] = make_float2(td, te);
-            A0 = cmulc(samu_lambda(k0, ct), A0);
-            A1 = cmulc(samu_lambda(k1, ct), A1);
-        }
-    }
+    if (fast)
+        bwd_reverse_sweep<true>(sc, gre, gim, k0, k1, u, A0, A1, acc, dwb, dwf, a.grad_fp32 != 0, active, D / 2,
+                                M / 2, kp, g.n_groups, lane);
+    else
+        bwd_reverse_sweep<false>(sc, gre, gim, k0, k1, u, A0, A1, acc, dwb, dwf, a.grad_fp32 != 0, active, D / 2,
+                                 M / 2, kp, g.n_groups, lane);
     if (c == 0 && warp == 0 && active)
         *reinterpret_cast<float4*>(a.dh0 + ((size_t)b * M + m) * 2) = make_float4(A0.x, A0.y, A1.x, A1.y);
-    s_acc[warp][lane] = make_float4(dnu0, dth0, dnu1, dth1);
+    s_acc[warp][lane] = acc;
     __syncthreads();
     if (warp == 0 && active) {
         float4 s = s_acc[0][lane];

@@ -40,12 +40,16 @@ DEFAULT_WORKLOAD = "width_2048"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 256 << 20
 
-# Algorithmic bytes per launch, in units of B*L*D (one BF16 [B,L,D] tensor = 2 units):
-#   controller forward: read x_sel (2)            scan forward: read w, write y (4)
-#   scan backward: read dy, w, write dw (6)       controller backward: read x_sel, write dx_sel (4)
+# Bytes each launch must move, in units of B*L*D (one BF16 [B,L,D] tensor = 2 units):
+#   controller forward: read x_sel (2)        forward maps: read w (2)
+#   forward replay: read w, write y (4)       backward maps: read dy (2)
+#   backward main: read dy, w, write dw (6)   controller backward: read x_sel, write dx_sel (4)
+# The step's algorithmic total (x_sel, w, dy read once; y, dx_sel, dw written) is
+# 16 units; the maps launches' second reads of w and dy are the price of the
+# two-launch scan and count towards the kernels, not towards the step.
 KERNEL_BYTES_PER_BLD = {
-    "samu_ctrl_fwd_kernel": 2.0, "samu_scan_fwd_kernel": 4.0,
-    "samu_scan_bwd_kernel": 6.0, "samu_ctrl_bwd_kernel": 4.0,
+    "samu_ctrl_fwd_kernel": 2.0, "samu_fwd_maps_kernel": 2.0, "samu_fwd_replay_kernel": 4.0,
+    "samu_bwd_maps_kernel": 2.0, "samu_bwd_main_kernel": 6.0, "samu_ctrl_bwd_kernel": 4.0,
 }
 STEP_BYTES_PER_BLD = 16.0
 LAUNCHES_PER_RECORD = {"samu_params_kernels": 3, "rglru_alpha_kernels": 2}

@@ -23,8 +23,8 @@ int check_samu_shape(int B, int L, int D) {
     int st = check_common(B, L, D);
     if (st != LRS_OK) return st;
     if (D % 16 != 0 || D > 4096) return LRS_ERR_UNSUPPORTED;
-    const ScanGeom g = make_geom(B, L, D / 2);
-    if (g.n_tiles > 0x7fffffffLL) return LRS_ERR_UNSUPPORTED;
+    const SegGeom g = samu_seg_geom(B, L, D / 2, 0);
+    if ((long long)g.n_chains * g.NSmax > 0x7fffffffLL) return LRS_ERR_UNSUPPORTED;
     return LRS_OK;
 }
 
@@ -32,7 +32,7 @@ int check_rglru_shape(int B, int L, int D) {
     int st = check_common(B, L, D);
     if (st != LRS_OK) return st;
     if (D % 8 != 0) return LRS_ERR_UNSUPPORTED;
-    const ScanGeom g = make_geom(B, L, D);
+    const ScanGeom g = make_geom(B, L, D, kRgTile);
     if (g.n_tiles > 0x7fffffffLL) return LRS_ERR_UNSUPPORTED;
     return LRS_OK;
 }
@@ -66,8 +66,9 @@ void prof_end(cudaStream_t s) {
 
 // Kernel ids reported by lrs_profile_end.
 enum {
-    KID_SAMU_PREP = 1, KID_SAMU_CTRL_FWD, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
-    KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA
+    KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
+    KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
+    KID_SAMU_BWD_MAPS, KID_SAMU_FWD_PREFIX, KID_SAMU_BWD_PREFIX
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -185,8 +186,6 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     float* r = at<float>(saved, sv.r);
     float4* ctrl = at<float4>(saved, sv.ctrl);
 
-    cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
-    if (e != cudaSuccess) return LRS_ERR_CUDA;
     float4* modes = at<float4>(saved, sv.modes);
     SamuCtrlFwdArgs cf;
     cf.BL = BL;
@@ -207,11 +206,11 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.modes = modes;
     LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream));
 
-    CUtensorMap tm_w;
-    if (!make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;
+    const SegGeom g = samu_scan_geom(B, L, M, false);
+    CUtensorMap tm_w, tm_ctrl;
+    if (!make_bf16_map(&tm_w, w, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub)) return LRS_ERR_CUDA;
     SamuScanFwdArgs a;
-    a.g = make_geom(B, L, M);
-    a.ctrl = ctrl;
+    a.g = g;
     a.modes = modes;
     a.nu = nu;
     a.h0 = h0;
@@ -219,11 +218,12 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     a.y32 = y32;
     a.hT = hT;
     a.hsub = at<float2>(saved, sv.hsub);
-    a.agg = at<float4>(scratch, sc.agg);
-    a.flags = at<uint32_t>(scratch, sc.flags);
-    a.counter = at<uint32_t>(scratch, sc.status + 4);
+    a.smap = at<float4>(scratch, sc.smap);
+    a.sent = at<float2>(scratch, sc.sent);
     a.status = at<uint32_t>(scratch, sc.status);
-    LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_scan_fwd(tm_w, a, stream));
+    LRS_LAUNCH(KID_SAMU_FWD_MAPS, stream, launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream));
+    LRS_LAUNCH(KID_SAMU_FWD_PREFIX, stream, launch_samu_fwd_prefix(a, stream));
+    LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream));
     return LRS_OK;
 }
 
@@ -249,17 +249,16 @@ int samu_backward(const void* dy, const float* dhT,
     const int M = D / 2;
     const SamuSaved sv = samu_saved_layout(B, L, D);
     const SamuScratch sc = samu_scratch_layout(B, L, D);
-    const ScanGeom g = make_geom(B, L, M);
+    const SegGeom g = samu_scan_geom(B, L, M, true);
     const int fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
 
-    cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
-    if (e != cudaSuccess) return LRS_ERR_CUDA;
-
-    CUtensorMap tm_dy, tm_w;
-    if (!make_bf16_map(&tm_dy, dy, B, L, D) || !make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;
+    const float4* ctrl = at<float4>(saved, sv.ctrl);
+    CUtensorMap tm_dy, tm_w, tm_ctrl;
+    if (!make_bf16_map(&tm_dy, dy, B, L, D, kSub) || !make_bf16_map(&tm_w, w, B, L, D, kSub) ||
+        !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub))
+        return LRS_ERR_CUDA;
     SamuScanBwdArgs s;
     s.g = g;
-    s.ctrl = at<float4>(saved, sv.ctrl);
     s.modes = at<float4>(saved, sv.modes);
     s.nu = nu;
     s.dhT = dhT;
@@ -267,14 +266,14 @@ int samu_backward(const void* dy, const float* dhT,
     s.dw = dw;
     s.grad_fp32 = fp32;
     s.dh0 = dh0;
-    s.agg = at<float4>(scratch, sc.agg);
-    s.rin = at<float2>(scratch, sc.rin);
+    s.smap = at<float4>(scratch, sc.smap);
+    s.sent = at<float2>(scratch, sc.sent);
     s.kpart = at<float2>(scratch, sc.kpart);
     s.numod = at<float2>(scratch, sc.numod);
-    s.flags = at<uint32_t>(scratch, sc.flags);
-    s.counter = at<uint32_t>(scratch, sc.status + 4);
     s.status = at<uint32_t>(scratch, sc.status);
-    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_scan_bwd(tm_dy, tm_w, s, stream));
+    LRS_LAUNCH(KID_SAMU_BWD_MAPS, stream, launch_samu_bwd_maps(tm_dy, tm_ctrl, s, stream));
+    LRS_LAUNCH(KID_SAMU_BWD_PREFIX, stream, launch_samu_bwd_prefix(s, stream));
+    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy, tm_w, tm_ctrl, s, stream));
 
     SamuCtrlBwdArgs cb;
     cb.B = B;
@@ -285,7 +284,7 @@ int samu_backward(const void* dy, const float* dhT,
     cb.kpart = s.kpart;
     cb.p = at<float>(saved, sv.p);
     cb.r = at<float>(saved, sv.r);
-    cb.ctrl = s.ctrl;
+    cb.ctrl = ctrl;
     cb.wh = at<float>(saved, sv.wh);
     cb.misc = at<float>(saved, sv.misc);
     cb.dx = dx_sel;
@@ -298,7 +297,7 @@ int samu_backward(const void* dy, const float* dhT,
     pa.B = B;
     pa.L = L;
     pa.D = D;
-    pa.CT = g.CT;
+    pa.n_part = g.NS;
     pa.numod = at<float2>(scratch, sc.numod);
     pa.numod2 = at<float2>(scratch, sc.numod2);
     pa.dwh_part = cb.dwh_part;
@@ -341,11 +340,11 @@ int rglru_forward(const void* x, const void* lx, const void* la, const float* al
     cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
     if (e != cudaSuccess) return LRS_ERR_CUDA;
     CUtensorMap tm_x, tm_lx, tm_la;
-    if (!make_bf16_map(&tm_x, x, B, L, D) || !make_bf16_map(&tm_lx, lx, B, L, D) ||
-        !make_bf16_map(&tm_la, la, B, L, D))
+    if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_bf16_map(&tm_lx, lx, B, L, D, kRgTile) ||
+        !make_bf16_map(&tm_la, la, B, L, D, kRgTile))
         return LRS_ERR_CUDA;
     RglruScanFwdArgs a;
-    a.g = make_geom(B, L, D);
+    a.g = make_geom(B, L, D, kRgTile);
     a.alpha = alpha;
     a.reset = reset;
     a.h0 = h0;
@@ -375,12 +374,12 @@ int rglru_backward(const void* dy, const float* dhT, const void* x, const void* 
         return LRS_ERR_ARG;
     const RglruSaved sv = rglru_saved_layout(B, L, D);
     const RglruScratch sc = rglru_scratch_layout(B, L, D);
-    const ScanGeom g = make_geom(B, L, D);
+    const ScanGeom g = make_geom(B, L, D, kRgTile);
     cudaError_t e = cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream);
     if (e != cudaSuccess) return LRS_ERR_CUDA;
     CUtensorMap tm_dy, tm_x, tm_lx, tm_la;
-    if (!make_bf16_map(&tm_dy, dy, B, L, D) || !make_bf16_map(&tm_x, x, B, L, D) ||
-        !make_bf16_map(&tm_lx, lx, B, L, D) || !make_bf16_map(&tm_la, la, B, L, D))
+    if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile) || !make_bf16_map(&tm_x, x, B, L, D, kRgTile) ||
+        !make_bf16_map(&tm_lx, lx, B, L, D, kRgTile) || !make_bf16_map(&tm_la, la, B, L, D, kRgTile))
         return LRS_ERR_CUDA;
     RglruScanBwdArgs a;
     a.g = g;

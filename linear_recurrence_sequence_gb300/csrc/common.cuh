@@ -15,15 +15,13 @@ namespace lrs {
 // ---------------------------------------------------------------------------
 // Tiling.  A chain is one (batch row, group of 64 modes or channels); each
 // lane of a warp owns two adjacent modes, so a warp covers a group and reads
-// 128 contiguous bytes of each BF16 half per token.  A tile is 128 tokens of
-// one chain, split over 8 warps of 16 tokens each (sub-chunks).
+// 128 contiguous bytes of each BF16 half per token.  A tile is a run of
+// 16-token sub-chunks of one chain, one sub-chunk per worker warp.  Entry
+// states are kept per sub-chunk, in slot t / 16 of the sequence.
 // ---------------------------------------------------------------------------
 constexpr int kGroup = 64;           // modes (SAMU) or channels (RG-LRU) per chain
 constexpr int kSub = 16;             // tokens per warp sub-chunk
-constexpr int kScanWarps = 8;        // sub-chunks per tile
-constexpr int kTile = kSub * kScanWarps;   // tokens per tile (128)
-constexpr int kScanThreads = kScanWarps * 32;
-constexpr int kBoxBytes = kTile * kGroup * 2;   // one BF16 [128 x 64] box (16 KB)
+constexpr int kRowBytes = kGroup * 2;   // one BF16 row of a box (128 bytes)
 
 // Look-back status values stored per (chain, chunk).
 constexpr uint32_t kFlagEmpty = 0u;
@@ -31,9 +29,11 @@ constexpr uint32_t kFlagAgg = 1u;    // the tile's own affine map is published
 constexpr uint32_t kFlagIncl = 2u;   // the state after the tile is published
 constexpr uint32_t kFlagErr = 3u;    // the tile gave up; waiters abort
 
-// Bounded spin: polls before a waiter records LRS_ERR_TIMEOUT and returns.
-// With the nanosleep back-off this is well under a second per wait.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Bounded waits.  Every wait on another warp, CTA or copy gives up after
+// kWaitLimitNs of %globaltimer time (far above any legitimate wait: a whole
+// scan takes well under a millisecond per 10^8 elements), records
+// LRS_ERR_TIMEOUT in the status word and lets the kernel return.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
 
 // Device status word bits (OR-ed together by failing CTAs).
 constexpr uint32_t kStatusTimeout = 1u;
@@ -55,6 +55,29 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 // L2-only loads (never served from a possibly stale L1 line).
 __device__ __forceinline__ float4 ldcg4(const float4* p) { return __ldcg(p); }
 __device__ __forceinline__ float2 ldcg2(const float2* p) { return __ldcg(p); }
+
+// Nanosecond global timer (PTX %globaltimer).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Deadline of one bounded wait: expired() is cheap (the timer is read every
+// 32nd poll) and turns true once kWaitLimitNs have passed since the first read.
+struct WaitClock {
+    uint64_t t0 = 0;
+    uint32_t n = 0;
+    __device__ __forceinline__ bool expired() {
+        if ((++n & 31u) != 0u) return false;
+        const uint64_t t = global_ns();
+        if (t0 == 0) {
+            t0 = t;
+            return false;
+        }
+        return t - t0 > kWaitLimitNs;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // Shared-memory barriers and TMA (cp.async.bulk.tensor) loads.
@@ -85,13 +108,36 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the barrier phase; false if kSpinLimit polls pass first.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait for the barrier phase of the given parity (try_wait lets the
+// hardware park the warp between polls); false once the deadline passes.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t n = 0; n < kSpinLimit; ++n) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if (n > 16) __nanosleep(32);
+    WaitClock clk;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clk.expired()) return false;
     }
-    return false;
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 3-D tiled tensor load of one box into shared memory, completing on `bar`.
@@ -105,12 +151,18 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// Warp-level chain search for the decoupled look-back (see lookback_find);
-// executed by one full warp, returns the same value in every lane.
+// Decoupled look-back, chain search, executed by one full warp.  For tile c
+// of one chain, finds the nearest predecessor (walking in direction dir: -1
+// towards tile 0, +1 towards tile C-1) whose state after the tile (kFlagIncl)
+// is published while every closer predecessor has at least published its map
+// (kFlagAgg).  Each poll inspects 32 predecessors (one per lane, acquire
+// loads).  Returns the same value in every lane; -1 if a predecessor failed or
+// the deadline passed.
 __device__ __forceinline__ int lookback_find_warp(const uint32_t* flags, int c, int C, int dir) {
     const int lane = threadIdx.x & 31;
     int base = c + dir;
     uint32_t polls = 0;
+    WaitClock clk;
     for (;;) {
         const int idx = base + dir * lane;
         const bool valid = idx >= 0 && idx < C;
@@ -123,55 +175,13 @@ __device__ __forceinline__ int lookback_find_warp(const uint32_t* flags, int c, 
         const unsigned before = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
         if (bad & upto) return -1;
         if (empty & before) {
-            if (++polls > kSpinLimit) return -1;
-            if (polls > 8) __nanosleep(64);
+            if (clk.expired()) return -1;
+            if (++polls > 8) __nanosleep(64);
             continue;
         }
         if (first < 32) return base + dir * first;
         base += 32 * dir;
     }
-}
-
-// Decoupled look-back, chain search.  For tile c of one chain, find the
-// nearest predecessor (walking in direction dir: -1 towards chunk 0, +1
-// towards chunk C-1) whose state after the chunk (kFlagIncl) is published,
-// while every closer predecessor has at least published its map (kFlagAgg).
-// Warp 0 inspects 32 predecessors per poll (one per lane, acquire loads) and
-// the answer is broadcast through *s_j after a CTA barrier; -1 means a
-// predecessor failed or the bounded wait ran out.  Must be called by every
-// thread of the CTA.
-__device__ __forceinline__ int lookback_find(const uint32_t* flags, int c, int C, int dir, int* s_j) {
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int base = c + dir;
-        int result = -1;
-        uint32_t polls = 0;
-        for (;;) {
-            const int idx = base + dir * lane;
-            const bool valid = idx >= 0 && idx < C;
-            const uint32_t f = valid ? ld_acquire_gpu(flags + idx) : kFlagAgg;
-            const unsigned incl = __ballot_sync(0xffffffffu, f == kFlagIncl);
-            const unsigned empty = __ballot_sync(0xffffffffu, f == kFlagEmpty);
-            const unsigned bad = __ballot_sync(0xffffffffu, f == kFlagErr);
-            const int first = incl ? (__ffs(incl) - 1) : 32;
-            const unsigned upto = first >= 31 ? 0xffffffffu : ((2u << first) - 1u);
-            const unsigned before = first >= 32 ? 0xffffffffu : ((1u << first) - 1u);
-            if (bad & upto) break;
-            if (empty & before) {
-                if (++polls > kSpinLimit) break;
-                if (polls > 8) __nanosleep(64);
-                continue;
-            }
-            if (first < 32) {
-                result = base + dir * first;
-                break;
-            }
-            base += 32 * dir;
-        }
-        if (lane == 0) *s_j = result;
-    }
-    __syncthreads();
-    return *s_j;
 }
 
 // 2^x on the SFU (PTX ex2.approx, documented relative error ~2^-22).

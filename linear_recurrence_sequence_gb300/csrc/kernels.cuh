@@ -34,13 +34,10 @@ __device__ __forceinline__ ModeConst load_mode(const float4* __restrict__ modes,
     return k;
 }
 
-// Per-token control word in shared memory: {E - 1, C, S, kind} with kind
-// kTokNormal, kTokReset (segment start: lambda = 0) or kTokPad (past the end
-// of the sequence: the token is skipped).  kind is the same for every lane,
+// Per-token control word, written by the controller forward and staged into
+// shared memory by TMA: {E_t - 1, C_t, S_t, reset_t} with reset_t 1 at a
+// segment start (lambda = 0) and 0 elsewhere.  It is the same for every lane,
 // so the branches on it are warp-uniform.
-constexpr float kTokNormal = 0.f;
-constexpr float kTokReset = 1.f;
-constexpr float kTokPad = 2.f;
 
 // Bound on |nu (E - 1)| under which the degree-3 polynomial below is exact to
 // < 2e-11 relative (the truncation term x^4/24), checked once per warp and tile.
@@ -82,25 +79,28 @@ __device__ __forceinline__ float4 compose_step(float2 l, float2 bb, float4 S) {
     return make_float4(L.x, L.y, Bv.x, Bv.y);
 }
 
+// Forward scan over segments: segment maps, chain prefix, replay.  w and
+// the control words reach the kernels through TMA tensor maps (16-token
+// boxes); everything indexed by segment is [B][NS][M] (per mode).
 struct SamuScanFwdArgs {
-    ScanGeom g;
-    const float4* ctrl;     // [B*L] {E - 1, C, S, reset}
+    SegGeom g;
     const float4* modes;    // [M] lbar hi/lo
     const float* nu;
     const float* h0;        // [B,M,2] or null
     uint32_t* y;            // BF16 pairs of y
     float* y32;             // optional
     float* hT;              // [B,M,2]
-    float2* hsub;           // [B][CS][M] sub-chunk entry states
-    float4* agg;            // [B][CT][M] tile maps
-    uint32_t* flags;        // [n_chains][CT]
-    uint32_t* counter;
-    uint32_t* status;
+    float2* hsub;           // [B][CS][M] entry state of every 16-token sub-chunk
+    float4* smap;           // [B][NS][M] segment maps
+    float2* sent;           // [B][NS][M] segment entry states
+    uint32_t* status;       // cleared by the maps kernel
 };
 
+// Backward scan over segments: adjoint segment maps, reverse chain prefix,
+// reverse replay.  sent holds the adjoint arriving at each segment's last
+// token from later tokens.
 struct SamuScanBwdArgs {
-    ScanGeom g;
-    const float4* ctrl;
+    SegGeom g;
     const float4* modes;
     const float* nu;
     const float* dhT;       // [B,M,2] or null
@@ -108,12 +108,10 @@ struct SamuScanBwdArgs {
     void* dw;               // BF16 pairs or FP32
     int grad_fp32;
     float* dh0;             // [B,M,2]
-    float4* agg;            // [B][CT][M] reverse tile maps
-    float2* rin;            // [B][CT][M] adjoint leaving each tile towards the past
+    float4* smap;           // [B][NS][M] adjoint segment maps
+    float2* sent;           // [B][NS][M] incoming adjoints
     float2* kpart;          // [B*L][n_groups] {sum Im kappa, sum -nu Re kappa}
-    float2* numod;          // [B][CT][M] {dnu, dtheta} per tile
-    uint32_t* flags;
-    uint32_t* counter;
+    float2* numod;          // [B][NS][M] {dnu, dtheta} per segment
     uint32_t* status;
 };
 
@@ -133,8 +131,9 @@ struct SamuCtrlBwdArgs {
 };
 
 struct SamuParamArgs {
-    int B, L, D, CT;
-    const float2* numod;    // [B*CT][M]
+    int B, L, D;
+    int n_part;             // numod rows per batch row
+    const float2* numod;    // [B*n_part][M]
     float2* numod2;         // [kReduceGroups][M]
     const float* dwh_part;  // [kCtrlBwdCtas * 2 halves][2][D+1]
     const float2* amp_part;
@@ -170,8 +169,20 @@ struct SamuCtrlFwdArgs {
 };
 
 cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s);
-cudaError_t launch_samu_scan_fwd(const CUtensorMap& tm_w, const SamuScanFwdArgs& args, cudaStream_t s);
-cudaError_t launch_samu_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_w,
+// Segment geometry of the forward (backward = false) or backward scan on the
+// current device: every segment of every chain resident at once.
+SegGeom samu_scan_geom(int B, int L, int M, bool backward);
+// Forward: maps (w read backwards in time), prefix, replay (forwards).
+cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
+                                 cudaStream_t s);
+cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s);
+cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
+                                   cudaStream_t s);
+// Backward: maps (dy read forwards in time), prefix, main (backwards).
+cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
+                                 cudaStream_t s);
+cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s);
+cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
                                  const SamuScanBwdArgs& args, cudaStream_t s);
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s);
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s);

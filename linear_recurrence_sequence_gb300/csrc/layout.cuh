@@ -17,28 +17,87 @@ constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status w
 
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+// Tile shapes.  RG-LRU: a tile is 128 tokens of one chain, one 16-token
+// sub-chunk per warp.
+constexpr int kRgWarps = 8;                        // RG-LRU: 8 warps
+constexpr int kRgTile = kRgWarps * kSub;           // 128 tokens
+
 // Geometry of one chunked scan over [B, L, lanes] (lanes = M modes for SAMU,
 // D channels for RG-LRU).  A chain is one (batch row, group of kGroup lanes);
-// its tiles are kTile consecutive tokens.
+// its tiles are `tile` consecutive tokens.
 struct ScanGeom {
     int B, L, lanes;
+    int tile;              // tokens per tile
+    int subs;              // 16-token sub-chunks per tile
     int n_groups;          // ceil(lanes / kGroup)
     int n_chains;          // B * n_groups
-    int CT;                // tiles per chain, ceil(L / kTile)
-    int CS;                // entry-state slots per batch row: one per sub-chunk, + 1
+    int CT;                // tiles per chain, ceil(L / tile)
+    int CS;                // entry-state slots per batch row (slot = t / 16, with slack)
     long long n_tiles;     // n_chains * CT
 };
 
-inline ScanGeom make_geom(int B, int L, int lanes) {
+inline ScanGeom make_geom(int B, int L, int lanes, int tile) {
     ScanGeom g;
     g.B = B;
     g.L = L;
     g.lanes = lanes;
+    g.tile = tile;
+    g.subs = tile / kSub;
     g.n_groups = (lanes + kGroup - 1) / kGroup;
     g.n_chains = B * g.n_groups;
-    g.CT = (L + kTile - 1) / kTile;
-    g.CS = g.CT * kScanWarps + 1;
+    g.CT = (L + tile - 1) / tile;
+    g.CS = (L + kSub - 1) / kSub + g.subs + 1;
     g.n_tiles = (long long)g.n_chains * g.CT;
+    return g;
+}
+
+// SAMU segments.  Every chain is cut into NS segments of `seg` tokens (a
+// multiple of 16; the last one ends at L), one per warp, with NS chosen so
+// that all segments of all chains run at once on the resident warps.  The
+// scratch arrays indexed by segment are sized for the most segments any
+// device can ask for: at least kSegMinTok tokens each and at most
+// kMaxSegWarps segments in all.
+constexpr int kSegMinTok = kSub;
+constexpr long long kMaxSegWarps = 16384;
+
+struct SegGeom {
+    int B, L, M;
+    int n_groups, n_chains;
+    int seg;               // tokens per segment
+    int NS;                // segments per chain
+    int NSmax;             // bound on NS for this (B, L, M) on any device
+    int CS;                // entry-state slots per batch row (slot = t / 16)
+};
+
+inline int round_up16(long long v) { return (int)((v + kSub - 1) / kSub * kSub); }
+
+// seg_min: the shortest segment any device may use for this problem.
+inline int seg_min_tokens(int L, int n_chains) {
+    const long long need = ((long long)L * n_chains + kMaxSegWarps - 1) / kMaxSegWarps;
+    const int s = round_up16(need);
+    return s < kSegMinTok ? kSegMinTok : s;
+}
+
+// Segment geometry for `warps` resident warps (warps <= 0: the bound only).
+inline SegGeom samu_seg_geom(int B, int L, int M, long long warps) {
+    SegGeom g;
+    g.B = B;
+    g.L = L;
+    g.M = M;
+    g.n_groups = (M + kGroup - 1) / kGroup;
+    g.n_chains = B * g.n_groups;
+    const int smin = seg_min_tokens(L, g.n_chains);
+    g.NSmax = (L + smin - 1) / smin;
+    int seg = smin;
+    if (warps > 0) {
+        const long long per_chain = warps / g.n_chains;     // segments per chain that fit at once
+        const long long want = per_chain >= 1 ? ((long long)L + per_chain - 1) / per_chain : L;
+        seg = round_up16(want);
+        if (seg < smin) seg = smin;
+    }
+    g.seg = seg;
+    g.NS = (L + seg - 1) / seg;
+    g.CS = (L + kSub - 1) / kSub + 1;
     return g;
 }
 
@@ -55,7 +114,7 @@ struct SamuSaved {
 
 inline SamuSaved samu_saved_layout(int B, int L, int D) {
     const int M = D / 2;
-    const ScanGeom g = make_geom(B, L, M);
+    const SegGeom g = samu_seg_geom(B, L, M, 0);
     const size_t BL = (size_t)B * L;
     SamuSaved s;
     size_t o = 0;
@@ -71,23 +130,21 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
 }
 
 struct SamuScratch {
-    size_t status, flags, agg, rin, kpart, numod, numod2, dwh_part, amp_part, dwh, total;
-    size_t memset_bytes;   // bytes cleared at the start of each call: status block + flags
+    size_t status, smap, sent, kpart, numod, numod2, dwh_part, amp_part, dwh, total;
 };
 
 inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     const int M = D / 2;
-    const ScanGeom g = make_geom(B, L, M);
+    const SegGeom g = samu_seg_geom(B, L, M, 0);
     const size_t BL = (size_t)B * L;
+    const size_t rows = (size_t)B * g.NSmax * M;
     SamuScratch s;
     size_t o = 0;
-    s.status = o;   o += kStatusBlock;
-    s.flags = o;    o = align_up(o + (size_t)g.n_tiles * 4);
-    s.memset_bytes = o;
-    s.agg = o;      o = align_up(o + (size_t)B * g.CT * M * 16);      // tile maps
-    s.rin = o;      o = align_up(o + (size_t)B * g.CT * M * 8);       // adjoint leaving each tile
+    s.status = o;   o = align_up(o + kStatusBlock);
+    s.smap = o;     o = align_up(o + rows * 16);                      // segment maps
+    s.sent = o;     o = align_up(o + rows * 8);                       // segment entry states / adjoints
     s.kpart = o;    o = align_up(o + BL * g.n_groups * 8);            // per-token controller partials
-    s.numod = o;    o = align_up(o + (size_t)B * g.CT * M * 8);       // per-tile (dnu, dtheta)
+    s.numod = o;    o = align_up(o + rows * 8);                       // per-segment (dnu, dtheta)
     s.numod2 = o;   o = align_up(o + (size_t)kReduceGroups * M * 8);
     s.dwh_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 2 * 2 * (D + 1) * 4);   // (cta, half) rows
     s.amp_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 8);
@@ -104,7 +161,7 @@ struct RglruSaved {
 };
 
 inline RglruSaved rglru_saved_layout(int B, int L, int D) {
-    const ScanGeom g = make_geom(B, L, D);
+    const ScanGeom g = make_geom(B, L, D, kRgTile);
     RglruSaved s;
     size_t o = 0;
     s.hsub = o; o = align_up(o + (size_t)B * g.CS * D * 4);
@@ -117,7 +174,7 @@ struct RglruScratch {
 };
 
 inline RglruScratch rglru_scratch_layout(int B, int L, int D) {
-    const ScanGeom g = make_geom(B, L, D);
+    const ScanGeom g = make_geom(B, L, D, kRgTile);
     RglruScratch s;
     size_t o = 0;
     s.status = o;  o += kStatusBlock;

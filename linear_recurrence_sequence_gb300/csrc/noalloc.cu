@@ -6,15 +6,15 @@
 // fragment the pool), or a latency-critical loop where cudaMalloc's implicit
 // device synchronisation is not acceptable.  For them this entry point runs
 // the same forward kernels as samu_forward with every intermediate (the
-// controller cache, the per-mode constants, the sub-chunk entry states, the
-// look-back flags and the tile maps) placed in one fixed array in device
+// controller cache, the per-mode constants, the sub-chunk entry states, and
+// the segment maps and entry states) placed in one fixed array in device
 // memory, declared below.  The array is part of the library's device image:
 // every GPU that loads the library holds LRS_NOALLOC_BYTES for it until the
 // process exits.  The paper describes no such entry point.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents; the parts that must start at zero (status word, tile counter,
-// look-back flags) are cleared by each call on its stream.  Two calls whose
+// contents; the one part that must start at zero, the status word, is
+// cleared by each call's first scan kernel.  Two calls whose
 // work overlaps on the GPU (different streams, or different host threads)
 // race on the array and give undefined results.
 #include <mutex>
@@ -68,11 +68,10 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
 
     // the same layout as samu_forward's saved + the forward part of its scratch
     const int M = D / 2;
-    const ScanGeom g = make_geom(B, L, M);
     const SamuSaved sv = samu_saved_layout(B, L, D);
     const SamuScratch sc = samu_scratch_layout(B, L, D);
     const size_t scratch_off = align_up(sv.total);
-    const size_t need = scratch_off + sc.agg + (size_t)B * g.CT * M * 16;   // through the tile maps
+    const size_t need = scratch_off + sc.sent + (size_t)B * samu_seg_geom(B, L, M, 0).NSmax * M * 8;
     if (need > (size_t)LRS_NOALLOC_BYTES) return LRS_ERR_TOO_LARGE;
 
     void* base = nullptr;
@@ -88,9 +87,6 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     float* r = reinterpret_cast<float*>(saved + sv.r);
     float4* ctrl = reinterpret_cast<float4*>(saved + sv.ctrl);
 
-    CUtensorMap tm_w;
-    if (!make_bf16_map(&tm_w, w, B, L, D)) return LRS_ERR_CUDA;
-    if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     SamuCtrlFwdArgs cf;
     cf.BL = (long long)B * L;
     cf.D = D;
@@ -110,9 +106,10 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     cf.modes = modes;
     if (launch_samu_ctrl_fwd(cf, stream) != cudaSuccess) return LRS_ERR_CUDA;
 
+    CUtensorMap tm_w, tm_ctrl;
+    if (!make_bf16_map(&tm_w, w, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub)) return LRS_ERR_CUDA;
     SamuScanFwdArgs a;
-    a.g = g;
-    a.ctrl = ctrl;
+    a.g = samu_scan_geom(B, L, M, false);
     a.modes = modes;
     a.nu = nu;
     a.h0 = h0;
@@ -120,10 +117,11 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     a.y32 = y32;
     a.hT = hT;
     a.hsub = reinterpret_cast<float2*>(saved + sv.hsub);
-    a.agg = reinterpret_cast<float4*>(scratch + sc.agg);
-    a.flags = reinterpret_cast<uint32_t*>(scratch + sc.flags);
-    a.counter = reinterpret_cast<uint32_t*>(scratch + sc.status + 4);
+    a.smap = reinterpret_cast<float4*>(scratch + sc.smap);
+    a.sent = reinterpret_cast<float2*>(scratch + sc.sent);
     a.status = reinterpret_cast<uint32_t*>(scratch + sc.status);
-    if (launch_samu_scan_fwd(tm_w, a, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_fwd_prefix(a, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream) != cudaSuccess) return LRS_ERR_CUDA;
     return LRS_OK;
 }

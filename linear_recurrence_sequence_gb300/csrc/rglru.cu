@@ -16,6 +16,9 @@
 
 namespace lrs {
 
+constexpr int kRgThreads = kRgWarps * 32;
+constexpr int kRgBoxBytes = kRgTile * kRowBytes;   // one BF16 [128 x 64] box
+
 struct RgGate {
     float a;    // retention (0 at a segment start)
     float n;    // write normaliser sqrt(1 - a^2) (1 at a segment start)
@@ -51,16 +54,16 @@ __device__ __forceinline__ float softplus_f(float v) {
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScanThreads, 2)
+__global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_lx,
                           const __grid_constant__ CUtensorMap tm_la, RglruScanFwdArgs a) {
     extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: x, l^x, l^a
     uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
-    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kBoxBytes);
-    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kBoxBytes);
-    __shared__ uint8_t s_rst[kTile];
-    __shared__ float4 s_map[kScanWarps][32];
-    __shared__ float2 s_ent[kScanWarps][32];
+    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kRgBoxBytes);
+    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kRgBoxBytes);
+    __shared__ uint8_t s_rst[kRgTile];
+    __shared__ float4 s_map[kRgWarps][32];
+    __shared__ float2 s_ent[kRgWarps][32];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint32_t s_tile;
     __shared__ int s_err;
@@ -82,19 +85,19 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     const int D = g.lanes;
     const int L = g.L;
     const int CT = g.CT;
-    const int t0 = c * kTile;
+    const int t0 = c * kRgTile;
     const int d = grp * kGroup + 2 * lane;
     const bool active = d < D;
     uint32_t* fl = a.flags + (size_t)chain * CT;
     const size_t hb = (size_t)b * g.CS;
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 3 * kBoxBytes);
+        mbar_arrive_expect_tx(&s_bar, 3 * kRgBoxBytes);
         tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
         tma_load_3d(&s_lx[0][0], &tm_lx, grp * kGroup, t0, b, &s_bar);
         tma_load_3d(&s_la[0][0], &tm_la, grp * kGroup, t0, b, &s_bar);
     }
-    if (tid < kTile) {
+    if (tid < kRgTile) {
         const int t = t0 + tid;
         s_rst[tid] = (t < L && a.reset != nullptr && a.reset[(size_t)b * L + t] != 0) ? 1 : 0;
     }
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     if (warp == 0) {
         float4 A = s_map[0][lane];
 #pragma unroll
-        for (int w = 1; w < kScanWarps; ++w) {
+        for (int w = 1; w < kRgWarps; ++w) {
             const float4 Sw = s_map[w][lane];
             const float2 t0v = rcompose(make_float2(Sw.x, Sw.y), make_float2(A.x, A.y));
             const float2 t1v = rcompose(make_float2(Sw.z, Sw.w), make_float2(A.z, A.w));
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kScanThreads, 2)
                 err = true;
             } else if (active) {
                 const float2 hv = __ldcg(reinterpret_cast<const float2*>(
-                    a.hsub + (hb + (size_t)(j + 1) * kScanWarps) * D + d));
+                    a.hsub + (hb + (size_t)(j + 1) * kRgWarps) * D + d));
                 h0v = hv.x;
                 h1v = hv.y;
                 for (int i = j + 1; i < c; i += 4) {
@@ -185,16 +188,16 @@ __global__ void __launch_bounds__(kScanThreads, 2)
         if (!err) {
             float e0 = h0v, e1 = h1v;
 #pragma unroll
-            for (int w = 0; w < kScanWarps; ++w) {
+            for (int w = 0; w < kRgWarps; ++w) {
                 s_ent[w][lane] = make_float2(e0, e1);
                 if (active && (w > 0 || c == 0))
-                    *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)c * kScanWarps + w) * D + d) = make_float2(e0, e1);
+                    *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)c * kRgWarps + w) * D + d) = make_float2(e0, e1);
                 const float4 Sw = s_map[w][lane];
                 e0 = rapply(make_float2(Sw.x, Sw.y), e0);
                 e1 = rapply(make_float2(Sw.z, Sw.w), e1);
             }
             if (active)
-                *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)(c + 1) * kScanWarps) * D + d) =
+                *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)(c + 1) * kRgWarps) * D + d) =
                     make_float2(rapply(make_float2(A.x, A.y), h0v), rapply(make_float2(A.z, A.w), h1v));
             __threadfence();
             __syncwarp();
@@ -238,19 +241,19 @@ __global__ void __launch_bounds__(kScanThreads, 2)
 //   dl^a = abar (-8 softplus(alpha)) a g^a (1 - g^a);
 //   dalpha += abar (-8 g^a) sigmoid(alpha) a.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScanThreads, 2)
+__global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_lx, const __grid_constant__ CUtensorMap tm_la,
                           RglruScanBwdArgs a) {
     extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: dy, x, l^x, l^a
     uint32_t (*s_g)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
-    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kBoxBytes);
-    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kBoxBytes);
-    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 3 * kBoxBytes);
-    __shared__ uint8_t s_rst[kTile];
-    __shared__ float4 s_map[kScanWarps][32];
-    __shared__ float2 s_ent[kScanWarps][32];
-    __shared__ float2 s_acc[kScanWarps][32];
+    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kRgBoxBytes);
+    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kRgBoxBytes);
+    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 3 * kRgBoxBytes);
+    __shared__ uint8_t s_rst[kRgTile];
+    __shared__ float4 s_map[kRgWarps][32];
+    __shared__ float2 s_ent[kRgWarps][32];
+    __shared__ float2 s_acc[kRgWarps][32];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint32_t s_tile;
     __shared__ int s_err;
@@ -272,20 +275,20 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     const int grp = chain % g.n_groups;
     const int D = g.lanes;
     const int L = g.L;
-    const int t0 = c * kTile;
+    const int t0 = c * kRgTile;
     const int d = grp * kGroup + 2 * lane;
     const bool active = d < D;
     uint32_t* fl = a.flags + (size_t)chain * CT;
     const size_t hb = (size_t)b * g.CS;
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 4 * kBoxBytes);
+        mbar_arrive_expect_tx(&s_bar, 4 * kRgBoxBytes);
         tma_load_3d(&s_g[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
         tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
         tma_load_3d(&s_lx[0][0], &tm_lx, grp * kGroup, t0, b, &s_bar);
         tma_load_3d(&s_la[0][0], &tm_la, grp * kGroup, t0, b, &s_bar);
     }
-    if (tid < kTile) {
+    if (tid < kRgTile) {
         const int t = t0 + tid;
         s_rst[tid] = (t < L && a.reset != nullptr && a.reset[(size_t)b * L + t] != 0) ? 1 : 0;
     }
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kScanThreads, 2)
         sa1 = 1.0f / (1.0f + expf(-al1));
         if (nsub > 0) {
             const float2 hv = __ldcg(reinterpret_cast<const float2*>(
-                a.hsub + (hb + (size_t)c * kScanWarps + warp) * D + d));
+                a.hsub + (hb + (size_t)c * kRgWarps + warp) * D + d));
             h0v = hv.x;
             h1v = hv.y;
         }
@@ -342,9 +345,9 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     __syncthreads();
 
     if (warp == 0) {
-        float4 A = s_map[kScanWarps - 1][lane];
+        float4 A = s_map[kRgWarps - 1][lane];
 #pragma unroll
-        for (int w = kScanWarps - 2; w >= 0; --w) {
+        for (int w = kRgWarps - 2; w >= 0; --w) {
             const float4 Fw = s_map[w][lane];
             const float2 t0v = rcompose(make_float2(Fw.x, Fw.y), make_float2(A.x, A.y));
             const float2 t1v = rcompose(make_float2(Fw.z, Fw.w), make_float2(A.z, A.w));
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kScanThreads, 2)
         if (!err) {
             float v0 = R0, v1 = R1;
 #pragma unroll
-            for (int w = kScanWarps - 1; w >= 0; --w) {
+            for (int w = kRgWarps - 1; w >= 0; --w) {
                 s_ent[w][lane] = make_float2(v0, v1);
                 const float4 Fw = s_map[w][lane];
                 v0 = rapply(make_float2(Fw.x, Fw.y), v0);
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kScanThreads, 2)
     if (warp == 0 && active) {
         float2 s = s_acc[0][lane];
 #pragma unroll
-        for (int w = 1; w < kScanWarps; ++w) {
+        for (int w = 1; w < kRgWarps; ++w) {
             s.x += s_acc[w][lane].x;
             s.y += s_acc[w][lane].y;
         }
@@ -501,19 +504,19 @@ __global__ void __launch_bounds__(256) rglru_alpha_stage2_kernel(const float* __
 
 cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
                                   const RglruScanFwdArgs& args, cudaStream_t s) {
-    const int smem = 3 * kBoxBytes;
+    const int smem = 3 * kRgBoxBytes;
     cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_fwd_kernel<<<(unsigned)args.g.n_tiles, kScanThreads, smem, s>>>(tm_x, tm_lx, tm_la, args);
+    rglru_scan_fwd_kernel<<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
                                   const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s) {
-    const int smem = 4 * kBoxBytes;
+    const int smem = 4 * kRgBoxBytes;
     cudaError_t e = cudaFuncSetAttribute(rglru_scan_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_bwd_kernel<<<(unsigned)args.g.n_tiles, kScanThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
+    rglru_scan_bwd_kernel<<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }
 

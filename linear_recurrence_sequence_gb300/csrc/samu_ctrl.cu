@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a
 // ---------------------------------------------------------------------------
 // Parameter reductions (fixed order, deterministic).
 // ---------------------------------------------------------------------------
-// stage 1: per-tile (dnu, dtheta) partials, rows = B*CT, into kReduceGroups groups
+// stage 1: per-segment (dnu, dtheta) partials, rows = B*n_part, into kReduceGroups groups
 __global__ void __launch_bounds__(256) samu_numod_stage1_kernel(const float2* __restrict__ numod,
                                                                 float2* __restrict__ numod2,
                                                                 int rows, int M) {
@@ -523,7 +523,7 @@ cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s) {
 
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s) {
     const int M = args.D / 2;
-    const int rows = args.B * args.CT;
+    const int rows = args.B * args.n_part;
     dim3 g1((M + 255) / 256, kReduceGroups);
     samu_numod_stage1_kernel<<<g1, 256, 0, s>>>(args.numod, args.numod2, rows, M);
     cudaError_t e = cudaGetLastError();

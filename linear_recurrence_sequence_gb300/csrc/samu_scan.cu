@@ -3,610 +3,841 @@
 // Equations: SAMU GPU page ("SAMU 与 RG-LRU 的 H800 训练性能对比"), section 05:
 // z_{t,m} = lambda_{t,m} z_{t-1,m} + b_{t,m} with lambda rebuilt in registers
 // from the shared per-token E, C, S and the static spectrum (no [B,L,M]
-// transition tensor); chunk summaries S_c = T_e o ... o T_s under
-// (l2,b2) o (l1,b1) = (l2 l1, l2 b1 + b2); replay from the chunk entry state
-// with the visible output fused; the backward runs the conjugate transition
-// in reverse time, zbar_{t-1} += conj(lambda_t) zbar_t, bbar_t = zbar_t, and
-// rebuilds lambda instead of storing it.
+// transition tensor); chunk summaries under (l2,b2) o (l1,b1) =
+// (l2 l1, l2 b1 + b2); a chunk prefix gives every chunk its entry state; the
+// replay from the entry state emits the visible output.  The backward runs
+// the conjugate transition in reverse time,
+// zbar_{t-1} = conj(lambda_t) zbar_t + dy_{t-1}, with the same three steps,
+// and rebuilds lambda and z instead of storing them.
 //
-// Tiling (GB300): a chain is one (batch row, group of 64 modes); a CTA owns
-// one 128-token tile of a chain, staged into shared memory by TMA
-// (cp.async.bulk.tensor, one 16 KB box per BF16 half).  Its 8 warps take
-// 16-token sub-chunks; lane l owns modes 2l, 2l+1 of the group.  Warp maps
-// are combined in shared memory, and tiles of a chain are linked by a
-// decoupled look-back (tile ids from an atomic counter, so every awaited tile
-// is already resident; all waits bounded).  Every state in the chain is
-// produced by the same capply sequence, so results equal the serial
-// chunk-entry propagation bit for bit, whatever the timing.
+// GB300 organisation.  A chain is one (batch row, group of 64 modes); lane l
+// of a warp owns modes 2l, 2l+1.  Each chain is cut into NS segments (a
+// multiple of 16 tokens each), one per warp, NS chosen on the host so that
+// the segments of all chains run at once on the resident warps: one wave,
+// equal work per warp.  A warp walks its segment 16 tokens at a time through
+// a private ring of two shared-memory slots that TMA fills one sub-chunk
+// ahead (a [16 x 64] BF16 box per half plus the 16 control words).
+//
+// Each direction is three launches with no waits between CTAs:
+//  1. maps:    every warp composes its segment's affine map, walking the
+//              segment in the opposite time direction to step 3;
+//  2. prefix:  one CTA per chain folds the segment maps into every segment's
+//              entry state (16 warps over 16 ranges, then a fixed-order
+//              combine);
+//  3. replay:  every warp replays its segment from its entry state.
+// Step 3 starts each segment where step 1 finished it, so its first reads of
+// w (forward) or dy (backward) hit in L2.  Every composition runs in a fixed
+// order: results are bitwise reproducible from run to run.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace lrs {
 
-// Warp-uniform choice of the lambda variant for one sub-chunk: the polynomial
-// path when |nu| max|E - 1| < kPolyBound for every lane's modes.
-__device__ __forceinline__ bool use_fast_lambda(const float4* sc, int lane, const ModeConst& k0,
-                                                const ModeConst& k1) {
-    float e = 0.f;
-    if (lane < kSub) {
-        const float4 ct = sc[lane];
-        if (ct.w == kTokNormal) e = fabsf(ct.x);
-    }
+constexpr int kEngineWarps = 4;                     // warps per CTA (each on its own segment)
+constexpr int kEngineThreads = kEngineWarps * 32;
+constexpr int kRing = 2;                            // staging slots per warp
+constexpr int kWords = kGroup / 2;                  // BF16 pairs per box row
+constexpr int kBoxBytes = kSub * kRowBytes;         // one [16 x 64] BF16 box: 2 KB
+constexpr int kItemBytes = 2 * kBoxBytes + kSub * 16;   // re box + im box + control words
+constexpr int kPrefixWarps = 16;
+
+// One warp's staging ring.  Every TMA destination starts on a 128-byte
+// boundary (box sizes are multiples of 128 bytes).
+struct alignas(128) WarpRing {
+    uint32_t box[kRing][2][kSub][kWords];   // [slot][re, im][token][pair]
+    float4 ctrl[kRing][kSub];
+    uint64_t full[kRing];
+};
+constexpr int kEngineSmem = kEngineWarps * (int)sizeof(WarpRing);
+
+// The segment of one warp.
+struct SegTask {
+    int b, grp, s;
+    int t_begin, t_end;   // tokens [t_begin, t_end)
+    int nsc;              // 16-token sub-chunks
+};
+
+__device__ __forceinline__ SegTask seg_task(const SegGeom& g, long long gw) {
+    SegTask T;
+    const int chain = (int)(gw / g.NS);
+    T.s = (int)(gw % g.NS);
+    T.b = chain / g.n_groups;
+    T.grp = chain % g.n_groups;
+    T.t_begin = T.s * g.seg;
+    T.t_end = min(g.L, T.t_begin + g.seg);
+    T.nsc = (T.t_end - T.t_begin + kSub - 1) / kSub;
+    return T;
+}
+
+__device__ __forceinline__ bool is_reset(const float4& ct) { return ct.w != 0.f; }
+
+// Warp-uniform facts about one sub-chunk that select the code path:
+//  fast:   |nu| max|E - 1| < kPolyBound for every lane's modes (polynomial
+//          lambda instead of ex2.approx);
+//  simple: all 16 tokens present and none of them a reset (no per-token
+//          checks).
+struct SubKind {
+    bool fast, simple;
+};
+
+__device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane, const ModeConst& k0,
+                                            const ModeConst& k1) {
+    const float4 ct = sc[lane & (kSub - 1)];
+    const bool mine = lane < nsub;
+    const float e = mine ? fabsf(ct.x) : 0.f;
     const float emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(e)));
     const bool ok = fabsf(k0.nu) * emax < kPolyBound && fabsf(k1.nu) * emax < kPolyBound;
-    return __all_sync(0xffffffffu, ok);
+    SubKind kd;
+    kd.fast = __all_sync(0xffffffffu, ok);
+    kd.simple = nsub == kSub && !__any_sync(0xffffffffu, mine && ct.w != 0.f);
+    return kd;
 }
 
-// ---------------------------------------------------------------------------
-// Forward: sub-chunk summary and replay.  sc = the warp's 16 control words,
-// wre/wim = the lane's column of the staged w box (row stride kGroup/2 words).
-// ---------------------------------------------------------------------------
-template <bool FAST>
-__device__ __forceinline__ void fwd_summary(const float4* sc, const uint32_t* wre, const uint32_t* wim,
-                                            const ModeConst& k0, const ModeConst& k1, float4& S0, float4& S1) {
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        const float4 ct = sc[i];
-        if (ct.w == kTokPad) break;
-        const float2 br = bf2_to_f2(wre[i * (kGroup / 2)]);
-        const float2 bi = bf2_to_f2(wim[i * (kGroup / 2)]);
-        if (ct.w == kTokNormal) {
-            S0 = compose_step(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), S0);
-            S1 = compose_step(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), S1);
-        } else {   // segment start: lambda = 0
-            S0 = make_float4(0.f, 0.f, br.x, bi.x);
-            S1 = make_float4(0.f, 0.f, br.y, bi.y);
-        }
-    }
+// Calls FN<FAST, SIMPLE>(args...) for the sub-chunk kind.
+#define LRS_SUB_DISPATCH(kd, FN, ...)                  \
+    do {                                               \
+        if (kd.fast) {                                 \
+            if (kd.simple)                             \
+                FN<true, true>(__VA_ARGS__);           \
+            else                                       \
+                FN<true, false>(__VA_ARGS__);          \
+        } else {                                       \
+            if (kd.simple)                             \
+                FN<false, true>(__VA_ARGS__);          \
+            else                                       \
+                FN<false, false>(__VA_ARGS__);         \
+        }                                              \
+    } while (0)
+
+// acc + P b (complex)
+__device__ __forceinline__ float2 cfma(float2 P, float2 bb, float2 acc) {
+    return make_float2(__fmaf_rn(P.x, bb.x, __fmaf_rn(-P.y, bb.y, acc.x)),
+                       __fmaf_rn(P.x, bb.y, __fmaf_rn(P.y, bb.x, acc.y)));
 }
 
-template <bool FAST>
-__device__ __forceinline__ void fwd_replay(const float4* sc, const uint32_t* wre, const uint32_t* wim,
-                                           const ModeConst& k0, const ModeConst& k1, float2& z0, float2& z1,
-                                           uint32_t* yp, float* y32p, bool active, size_t row_words, int half_words) {
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        const float4 ct = sc[i];
-        if (ct.w == kTokPad) break;
-        const float2 br = bf2_to_f2(wre[i * (kGroup / 2)]);
-        const float2 bi = bf2_to_f2(wim[i * (kGroup / 2)]);
-        if (ct.w == kTokNormal) {
-            z0 = step_state(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), z0);
-            z1 = step_state(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), z1);
-        } else {
-            z0 = make_float2(br.x, bi.x);
-            z1 = make_float2(br.y, bi.y);
-        }
-        if (active) {
-            uint32_t* o = yp + (size_t)i * row_words;
-            __stcs(o, f2_to_bf2(z0.x, z1.x));
-            __stcs(o + half_words, f2_to_bf2(z0.y, z1.y));
-            if (y32p != nullptr) {
-                float* f = y32p + (size_t)i * 2 * row_words;
-                *reinterpret_cast<float2*>(f) = make_float2(z0.x, z1.x);
-                *reinterpret_cast<float2*>(f + 2 * half_words) = make_float2(z0.y, z1.y);
-            }
-        }
+__device__ __forceinline__ float4 identity_map() { return make_float4(1.f, 0.f, 0.f, 0.f); }
+
+// Lane 0: stage the sub-chunk at token ts of tensor `tm` (both halves of the
+// warp's 64 modes) and its control words into ring slot `slot`.  The warp has
+// finished reading the slot (__syncwarp before the call).
+__device__ __forceinline__ void ring_issue(WarpRing& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
+                                           int x_re, int x_im, int ts, int b) {
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&R.full[slot], kItemBytes);
+    tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
+    tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
+    tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
+}
+
+__device__ __forceinline__ void ring_init(WarpRing& R, int lane) {
+    if (lane == 0) {
+        for (int i = 0; i < kRing; ++i) mbar_init(&R.full[i], 1);
     }
+    __syncwarp();
+}
+
+// Waits for item k of the ring (n_items in all).  If the copy never lands:
+// records the failure, waits (bounded) for the later items already issued,
+// and returns false so that the warp can leave.
+__device__ __forceinline__ bool ring_wait(WarpRing& R, int k, int n_items, uint32_t* status, int lane) {
+    if (mbar_wait_bounded(&R.full[k % kRing], (uint32_t)(k / kRing) & 1u)) return true;
+    if (lane == 0) atomicOr(status, kStatusTimeout);
+    for (int j = k + 1; j < k + kRing && j < n_items; ++j) mbar_wait_bounded(&R.full[j % kRing], (uint32_t)(j / kRing) & 1u);
+    return false;
 }
 
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScanThreads, 3)
-    samu_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, SamuScanFwdArgs a) {
-    __shared__ __align__(128) uint32_t s_wre[kTile][kGroup / 2];
-    __shared__ __align__(128) uint32_t s_wim[kTile][kGroup / 2];
-    __shared__ float4 s_ctrl[kTile];
-    __shared__ float4 s_map[kScanWarps][32][2];
-    __shared__ float4 s_ent[kScanWarps][32];
-    __shared__ __align__(8) uint64_t s_bar;
-    __shared__ uint32_t s_tile;
-    __shared__ int s_err;
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    if (tid == 0) {
-        s_tile = atomicAdd(a.counter, 1u);
-        mbar_init(&s_bar, 1);
-    }
-    __syncthreads();
-    const ScanGeom& g = a.g;
-    const long long tile = s_tile;
-    const int chain = (int)(tile % g.n_chains);
-    const int c = (int)(tile / g.n_chains);
-    const int b = chain / g.n_groups;
-    const int grp = chain % g.n_groups;
-    const int M = g.lanes;
-    const int L = g.L;
-    const int CT = g.CT;
-    const size_t D = 2 * (size_t)M;
-    const int t0 = c * kTile;
-    const int m = grp * kGroup + 2 * lane;
-    const bool active = m < M;
-    uint32_t* fl = a.flags + (size_t)chain * CT;
-
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 2 * kBoxBytes);
-        tma_load_3d(&s_wre[0][0], &tm_w, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_wim[0][0], &tm_w, M + grp * kGroup, t0, b, &s_bar);
-    }
-    if (tid < kTile) {
-        const int t = t0 + tid;
-        float4 ct = make_float4(0.f, 1.f, 0.f, kTokPad);
-        if (t < L) {
-            ct = a.ctrl[(size_t)b * L + t];
-            ct.w = ct.w != 0.f ? kTokReset : kTokNormal;
+// Appends the sub-chunk's tokens, latest first, to the map H = (P, beta) of
+// the tokens after them: H o T_t = (P lambda_t, P b_t + beta).
+template <bool FAST, bool SIMPLE>
+__device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
+                                             const ModeConst& k0, const ModeConst& k1, float2& P0, float2& P1,
+                                             float2& be0, float2& be1) {
+#pragma unroll
+    for (int i = kSub - 1; i >= 0; --i) {
+        if (SIMPLE || i < nsub) {
+            const float4 ct = sc[i];
+            const float2 br = bf2_to_f2(wre[i * kWords]);
+            const float2 bi = bf2_to_f2(wim[i * kWords]);
+            be0 = cfma(P0, make_float2(br.x, bi.x), be0);
+            be1 = cfma(P1, make_float2(br.y, bi.y), be1);
+            if (SIMPLE || !is_reset(ct)) {
+                P0 = cmul(samu_lambda<FAST>(k0, ct), P0);
+                P1 = cmul(samu_lambda<FAST>(k1, ct), P1);
+            } else {   // segment start: nothing before it reaches past it
+                P0 = make_float2(0.f, 0.f);
+                P1 = P0;
+            }
         }
-        s_ctrl[tid] = ct;
     }
+}
+
+template <bool FAST, bool SIMPLE>
+__device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
+                                               const ModeConst& k0, const ModeConst& k1, float2& z0, float2& z1,
+                                               uint32_t* yp, float* y32p, bool active, size_t row, int half) {
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        if (SIMPLE || i < nsub) {
+            const float4 ct = sc[i];
+            const float2 br = bf2_to_f2(wre[i * kWords]);
+            const float2 bi = bf2_to_f2(wim[i * kWords]);
+            if (SIMPLE || !is_reset(ct)) {
+                z0 = step_state(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), z0);
+                z1 = step_state(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), z1);
+            } else {
+                z0 = make_float2(br.x, bi.x);
+                z1 = make_float2(br.y, bi.y);
+            }
+            if (active) {
+                uint32_t* o = yp + (size_t)i * row;
+                __stcs(o, f2_to_bf2(z0.x, z1.x));
+                __stcs(o + half, f2_to_bf2(z0.y, z1.y));
+                if (y32p != nullptr) {
+                    float* f = y32p + (size_t)i * 2 * row;
+                    __stcs(reinterpret_cast<float2*>(f), make_float2(z0.x, z1.x));
+                    __stcs(reinterpret_cast<float2*>(f + 2 * half), make_float2(z0.y, z1.y));
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 6)
+    samu_fwd_maps_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ctrl,
+                         SamuScanFwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    const SegGeom& g = a.g;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
+    if (gw >= (long long)g.n_chains * g.NS) return;
+    const SegTask T = seg_task(g, gw);
+    const int M = g.M;
+    const int m = T.grp * kGroup + 2 * lane;
+    const bool active = m < M;
+    const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
+    ring_init(R, lane);
+    // item k is sub-chunk nsc-1-k: the segment from its end backwards
+    if (lane == 0)
+        for (int k = 0; k < kRing && k < T.nsc; ++k)
+            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kSub, T.b);
     ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
     if (active) {
         k0 = load_mode(a.modes, a.nu, m);
         k1 = load_mode(a.modes, a.nu, m + 1);
     }
-    const int r0 = warp * kSub;
-    const int nsub = max(0, min(kSub, L - t0 - r0));
-    const bool landed = mbar_wait_bounded(&s_bar, 0);
-    if (!__syncthreads_and(landed)) {
-        if (tid == 0) {
-            st_release_gpu(fl + c, kFlagErr);
-            atomicOr(a.status, kStatusTimeout);
-        }
-        mbar_wait_bounded(&s_bar, 0);
-        return;
-    }
-    const float4* sc = s_ctrl + r0;
-    const uint32_t* wre = &s_wre[r0][lane];
-    const uint32_t* wim = &s_wim[r0][lane];
-    const bool fast = use_fast_lambda(sc, lane, k0, k1);
-
-    // sub-chunk summary S_w = T_e o ... o T_s
-    float4 S0 = make_float4(1.f, 0.f, 0.f, 0.f), S1 = S0;
-    if (fast)
-        fwd_summary<true>(sc, wre, wim, k0, k1, S0, S1);
-    else
-        fwd_summary<false>(sc, wre, wim, k0, k1, S0, S1);
-    s_map[warp][lane][0] = S0;
-    s_map[warp][lane][1] = S1;
-    __syncthreads();
-
-    // warp 0: tile map, entry state (directly from the previous tile when its
-    // state is already out, else by look-back), publish, sub-chunk entries
-    if (warp == 0) {
-        float4 A0 = s_map[0][lane][0], A1 = s_map[0][lane][1];
-#pragma unroll
-        for (int w = 1; w < kScanWarps; ++w) {
-            A0 = compose_maps(s_map[w][lane][0], A0);
-            A1 = compose_maps(s_map[w][lane][1], A1);
-        }
-        float2 h0v = make_float2(0.f, 0.f), h1v = h0v;
-        bool err = false;
-        const size_t hb = (size_t)b * g.CS;
-        if (c == 0) {
-            if (active && a.h0 != nullptr) {
-                const float4 hv = *reinterpret_cast<const float4*>(a.h0 + ((size_t)b * M + m) * 2);
-                h0v = make_float2(hv.x, hv.y);
-                h1v = make_float2(hv.z, hv.w);
-            }
-        } else {
-            int j = -1;
-            if (ld_acquire_gpu(fl + c - 1) == kFlagIncl) {
-                j = c - 1;
-            } else {
-                if (active) {
-                    float4* ag = a.agg + ((size_t)b * CT + c) * M + m;
-                    ag[0] = A0;
-                    ag[1] = A1;
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
-                j = lookback_find_warp(fl, c, CT, -1);
-            }
-            if (j < 0) {
-                err = true;
-            } else if (active) {
-                const float4 hv = ldcg4(reinterpret_cast<const float4*>(
-                    a.hsub + (hb + (size_t)(j + 1) * kScanWarps) * M + m));
-                h0v = make_float2(hv.x, hv.y);
-                h1v = make_float2(hv.z, hv.w);
-                for (int i = j + 1; i < c; i += 4) {   // maps of tiles j+1 .. c-1, in time order
-                    float4 T[4][2];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (i + q < c) {
-                            const float4* ag = a.agg + ((size_t)b * CT + i + q) * M + m;
-                            T[q][0] = ldcg4(ag);
-                            T[q][1] = ldcg4(ag + 1);
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (i + q < c) {
-                            h0v = capply(T[q][0], h0v);
-                            h1v = capply(T[q][1], h1v);
-                        }
-                    }
-                }
-            }
-        }
-        if (!err) {
-            if (active) {
-                const float2 i0 = capply(A0, h0v);
-                const float2 i1 = capply(A1, h1v);
-                *reinterpret_cast<float4*>(a.hsub + (hb + (size_t)(c + 1) * kScanWarps) * M + m) =
-                    make_float4(i0.x, i0.y, i1.x, i1.y);
-            }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
-            // entry states of the sub-chunks (also kept for the backward)
-            float2 e0 = h0v, e1 = h1v;
-#pragma unroll
-            for (int w = 0; w < kScanWarps; ++w) {
-                s_ent[w][lane] = make_float4(e0.x, e0.y, e1.x, e1.y);
-                if (active && (w > 0 || c == 0))
-                    *reinterpret_cast<float4*>(a.hsub + (hb + (size_t)c * kScanWarps + w) * M + m) =
-                        make_float4(e0.x, e0.y, e1.x, e1.y);
-                e0 = capply(s_map[w][lane][0], e0);
-                e1 = capply(s_map[w][lane][1], e1);
-            }
-        } else if (lane == 0) {
-            st_release_gpu(fl + c, kFlagErr);
-            atomicOr(a.status, kStatusTimeout);
-        }
-        if (lane == 0) s_err = err ? 1 : 0;
-    }
-    __syncthreads();
-    if (s_err) return;
-
-    // replay the sub-chunk from its entry state and write y
-    const float4 e = s_ent[warp][lane];
-    float2 z0 = make_float2(e.x, e.y), z1 = make_float2(e.z, e.w);
-    const size_t yrow = (((size_t)b * L + t0 + r0) * D + m) / 2;
-    uint32_t* yp = a.y + yrow;
-    float* y32p = a.y32 != nullptr ? a.y32 + 2 * yrow : nullptr;
-    if (fast)
-        fwd_replay<true>(sc, wre, wim, k0, k1, z0, z1, yp, y32p, active, D / 2, M / 2);
-    else
-        fwd_replay<false>(sc, wre, wim, k0, k1, z0, z1, yp, y32p, active, D / 2, M / 2);
-    if (active && nsub > 0 && t0 + r0 + nsub == L)
-        *reinterpret_cast<float4*>(a.hT + ((size_t)b * M + m) * 2) = make_float4(z0.x, z0.y, z1.x, z1.y);
-}
-
-// ---------------------------------------------------------------------------
-// Backward: forward sweep (rebuild u_t = lambda_t z_{t-1} and the reverse map
-// of the sub-chunk) and reverse sweep (adjoint, dw, kappa sums).
-// ---------------------------------------------------------------------------
-template <bool FAST>
-__device__ __forceinline__ void bwd_forward_sweep(const float4* sc, const uint32_t* wre, const uint32_t* wim,
-                                                  const uint32_t* gre, const uint32_t* gim, const ModeConst& k0,
-                                                  const ModeConst& k1, float2 z0, float2 z1, float4 (&u)[kSub],
-                                                  float4& F0, float4& F1) {
     float2 P0 = make_float2(1.f, 0.f), P1 = P0;
-    float2 q0 = make_float2(0.f, 0.f), q1 = q0;
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 ct = sc[i];
-        if (ct.w == kTokPad) continue;
-        const float2 br = bf2_to_f2(wre[i * (kGroup / 2)]);
-        const float2 bi = bf2_to_f2(wim[i * (kGroup / 2)]);
-        if (ct.w == kTokNormal) {
-            const float2 gr = bf2_to_f2(gre[i * (kGroup / 2)]);
-            const float2 gi = bf2_to_f2(gim[i * (kGroup / 2)]);
-            const float2 l0 = samu_lambda<FAST>(k0, ct);
-            const float2 l1 = samu_lambda<FAST>(k1, ct);
-            float2 u0, u1;
-            z0 = step_state(l0, make_float2(br.x, bi.x), z0, &u0);
-            z1 = step_state(l1, make_float2(br.y, bi.y), z1, &u1);
-            u[i] = make_float4(u0.x, u0.y, u1.x, u1.y);
-            P0 = cmul(l0, P0);
-            P1 = cmul(l1, P1);
-            const float2 c0 = cmulc(P0, make_float2(gr.x, gi.x));
-            const float2 c1 = cmulc(P1, make_float2(gr.y, gi.y));
-            q0 = make_float2(q0.x + c0.x, q0.y + c0.y);
-            q1 = make_float2(q1.x + c1.x, q1.y + c1.y);
-        } else {   // segment start: lambda = 0, nothing later reaches back past it
-            z0 = make_float2(br.x, bi.x);
-            z1 = make_float2(br.y, bi.y);
-            P0 = make_float2(0.f, 0.f);
-            P1 = P0;
-        }
+    float2 be0 = make_float2(0.f, 0.f), be1 = be0;
+    for (int k = 0; k < T.nsc; ++k) {
+        const int slot = k % kRing;
+        const int ts = T.t_begin + (T.nsc - 1 - k) * kSub;
+        const int nsub = min(kSub, T.t_end - ts);
+        if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
+        const float4* sc = R.ctrl[slot];
+        const uint32_t* wre = &R.box[slot][0][0][lane];
+        const uint32_t* wim = &R.box[slot][1][0][lane];
+        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
+        LRS_SUB_DISPATCH(kd, fwd_maps_sub, sc, wre, wim, nsub, k0, k1, P0, P1, be0, be1);
+        __syncwarp();
+        if (lane == 0 && k + kRing < T.nsc)
+            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k - kRing) * kSub, T.b);
     }
-    F0 = make_float4(P0.x, -P0.y, q0.x, q0.y);
-    F1 = make_float4(P1.x, -P1.y, q1.x, q1.y);
+    if (active) {
+        float4* sm = a.smap + ((size_t)T.b * g.NS + T.s) * M + m;
+        sm[0] = make_float4(P0.x, P0.y, be0.x, be0.y);
+        sm[1] = make_float4(P1.x, P1.y, be1.x, be1.y);
+    }
 }
 
-template <bool FAST>
-__device__ __forceinline__ void bwd_reverse_sweep(const float4* sc, const uint32_t* gre, const uint32_t* gim,
-                                                  const ModeConst& k0, const ModeConst& k1, const float4 (&u)[kSub],
-                                                  float2& A0, float2& A1, float4& acc, uint32_t* dwb, float* dwf,
-                                                  bool fp32, bool active, size_t row_words, int half_words,
-                                                  float2* kp, int kp_stride, int lane) {
+// One CTA per chain: entry state of every segment from h0 and the segment
+// maps.  Warp w folds segments [NS*w/16, NS*(w+1)/16) in time order (the
+// first kPrefixChunk maps stay in registers for the second pass); the 16
+// partial maps are then applied in order and each warp walks its range.
+constexpr int kPrefixChunk = 8;    // maps kept in registers across the two passes
+constexpr int kPrefixChunk2 = 4;   // maps per load batch after the first kPrefixChunk
+
+template <int N>
+__device__ __forceinline__ void load_maps(const float4* __restrict__ maps, int M, int i0, int hi, float4 (&T)[N][2]) {
 #pragma unroll
-    for (int i = kSub - 1; i >= 0; --i) {
-        const float4 ct = sc[i];
-        if (ct.w == kTokPad) continue;
-        const float2 gr = bf2_to_f2(gre[i * (kGroup / 2)]);
-        const float2 gi = bf2_to_f2(gim[i * (kGroup / 2)]);
-        A0 = make_float2(A0.x + gr.x, A0.y + gi.x);
-        A1 = make_float2(A1.x + gr.y, A1.y + gi.y);
-        if (active) {
-            if (fp32) {
-                float* p = dwf + 2 * (size_t)i * row_words;
-                *reinterpret_cast<float2*>(p) = make_float2(A0.x, A1.x);
-                *reinterpret_cast<float2*>(p + 2 * half_words) = make_float2(A0.y, A1.y);
-            } else {
-                uint32_t* p = dwb + (size_t)i * row_words;
-                __stcs(p, f2_to_bf2(A0.x, A1.x));
-                __stcs(p + half_words, f2_to_bf2(A0.y, A1.y));
-            }
-        }
-        if (ct.w == kTokNormal) {
-            // kappa = A conj(u)
-            const float4 uu = u[i];
-            const float kr0 = __fmaf_rn(A0.x, uu.x, __fmul_rn(A0.y, uu.y));
-            const float ki0 = __fmaf_rn(A0.y, uu.x, -__fmul_rn(A0.x, uu.y));
-            const float kr1 = __fmaf_rn(A1.x, uu.z, __fmul_rn(A1.y, uu.w));
-            const float ki1 = __fmaf_rn(A1.y, uu.z, -__fmul_rn(A1.x, uu.w));
-            const float Et = 1.0f + ct.x;   // ct.x holds E - 1
-            acc.x = __fmaf_rn(-Et, kr0, acc.x);   // dnu_m
-            acc.y += ki0;                         // dtheta_m
-            acc.z = __fmaf_rn(-Et, kr1, acc.z);
-            acc.w += ki1;
-            float td = ki0 + ki1;
-            float te = -__fmaf_rn(k0.nu, kr0, __fmul_rn(k1.nu, kr1));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                td += __shfl_xor_sync(0xffffffffu, td, o);
-                te += __shfl_xor_sync(0xffffffffu, te, o);
-            }
-            if (lane == 0) kp[(size_t)i * kp_stride] = make_float2(td, te);
-            A0 = cmulc(samu_lambda<FAST>(k0, ct), A0);
-            A1 = cmulc(samu_lambda<FAST>(k1, ct), A1);
-        } else {   // segment start: no controller terms, the adjoint stops here
-            if (lane == 0) kp[(size_t)i * kp_stride] = make_float2(0.f, 0.f);
-            A0 = make_float2(0.f, 0.f);
-            A1 = A0;
+    for (int q = 0; q < N; ++q) {
+        if (i0 + q < hi) {
+            T[q][0] = maps[(size_t)(i0 + q) * M];
+            T[q][1] = maps[(size_t)(i0 + q) * M + 1];
         }
     }
 }
 
-// Tiles in reverse time order.  Forward sweep of each sub-chunk from its saved
-// entry state rebuilds lambda_t, u_t = lambda_t z_{t-1} (kept in registers for
-// kappa) and z_t, and accumulates the prefix product P_t = lambda_s..lambda_t
-// and q = sum_t conj(P_t) dy_t: the sub-chunk maps an adjoint R arriving at its
-// last token to the adjoint leaving it towards the past, R' = conj(P_e) R + q.
-// Warp 0 composes the 8 sub-chunk maps, takes the incoming adjoint from the
-// next tile (or by look-back), and hands each sub-chunk its incoming adjoint.
-// Reverse sweep: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
-// kappa_t = A_t conj(u_t);  dtheta_m += Im kappa, dnu_m += -E_t Re kappa,
-// dbar_t += Im kappa, Ebar_t += -nu_m Re kappa (reduced over the 64 modes of
-// the warp: one per-token partial per mode group).
-__global__ void __launch_bounds__(kScanThreads, 2)
-    samu_scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
-                         SamuScanBwdArgs a) {
-    extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: dy re, dy im, w re, w im
-    uint32_t (*s_gre)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
-    uint32_t (*s_gim)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kBoxBytes);
-    uint32_t (*s_wre)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kBoxBytes);
-    uint32_t (*s_wim)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 3 * kBoxBytes);
-    __shared__ float4 s_ctrl[kTile];
-    __shared__ float4 s_map[kScanWarps][32][2];
-    __shared__ float4 s_ent[kScanWarps][32];
-    __shared__ float4 s_acc[kScanWarps][32];
-    __shared__ __align__(8) uint64_t s_bar;
-    __shared__ uint32_t s_tile;
-    __shared__ int s_err;
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    if (tid == 0) {
-        s_tile = atomicAdd(a.counter, 1u);
-        mbar_init(&s_bar, 1);
-    }
-    __syncthreads();
-    const ScanGeom& g = a.g;
-    const long long tile = s_tile;
-    const int chain = (int)(tile % g.n_chains);
-    const int CT = g.CT;
-    const int c = CT - 1 - (int)(tile / g.n_chains);
+__global__ void __launch_bounds__(kPrefixWarps * 32) samu_fwd_prefix_kernel(SamuScanFwdArgs a) {
+    __shared__ float4 s_part[kPrefixWarps][32][2];
+    const SegGeom& g = a.g;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chain = blockIdx.x;
     const int b = chain / g.n_groups;
     const int grp = chain % g.n_groups;
-    const int M = g.lanes;
-    const int L = g.L;
-    const size_t D = 2 * (size_t)M;
-    const int t0 = c * kTile;
+    const int M = g.M;
     const int m = grp * kGroup + 2 * lane;
     const bool active = m < M;
-    uint32_t* fl = a.flags + (size_t)chain * CT;
-    const size_t hb = (size_t)b * g.CS;
-
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 4 * kBoxBytes);
-        tma_load_3d(&s_gre[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_gim[0][0], &tm_dy, M + grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_wre[0][0], &tm_w, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_wim[0][0], &tm_w, M + grp * kGroup, t0, b, &s_bar);
-    }
-    if (tid < kTile) {
-        const int t = t0 + tid;
-        float4 ct = make_float4(0.f, 1.f, 0.f, kTokPad);
-        if (t < L) {
-            ct = a.ctrl[(size_t)b * L + t];
-            ct.w = ct.w != 0.f ? kTokReset : kTokNormal;
+    const int NS = g.NS;
+    const int lo = NS * warp / kPrefixWarps, hi = NS * (warp + 1) / kPrefixWarps;
+    const float4* __restrict__ maps = a.smap + (size_t)b * NS * M + m;
+    float4 P0 = identity_map(), P1 = P0;
+    float4 T0[kPrefixChunk][2];
+    if (active) {
+        load_maps(maps, M, lo, hi, T0);
+#pragma unroll
+        for (int q = 0; q < kPrefixChunk; ++q) {
+            if (lo + q < hi) {
+                P0 = compose_maps(T0[q][0], P0);
+                P1 = compose_maps(T0[q][1], P1);
+            }
         }
-        s_ctrl[tid] = ct;
+        for (int i0 = lo + kPrefixChunk; i0 < hi; i0 += kPrefixChunk2) {
+            float4 T[kPrefixChunk2][2];
+            load_maps(maps, M, i0, hi, T);
+#pragma unroll
+            for (int q = 0; q < kPrefixChunk2; ++q) {
+                if (i0 + q < hi) {
+                    P0 = compose_maps(T[q][0], P0);
+                    P1 = compose_maps(T[q][1], P1);
+                }
+            }
+        }
     }
+    s_part[warp][lane][0] = P0;
+    s_part[warp][lane][1] = P1;
+    __syncthreads();
+    if (!active) return;
+    float2 z0 = make_float2(0.f, 0.f), z1 = z0;
+    if (a.h0 != nullptr) {
+        const float4 hv = *reinterpret_cast<const float4*>(a.h0 + ((size_t)b * M + m) * 2);
+        z0 = make_float2(hv.x, hv.y);
+        z1 = make_float2(hv.z, hv.w);
+    }
+    for (int v = 0; v < warp; ++v) {
+        z0 = capply(s_part[v][lane][0], z0);
+        z1 = capply(s_part[v][lane][1], z1);
+    }
+    float4* __restrict__ out = reinterpret_cast<float4*>(a.sent + (size_t)b * NS * M + m);
+#pragma unroll
+    for (int q = 0; q < kPrefixChunk; ++q) {
+        if (lo + q < hi) {
+            out[(size_t)(lo + q) * (M / 2)] = make_float4(z0.x, z0.y, z1.x, z1.y);
+            z0 = capply(T0[q][0], z0);
+            z1 = capply(T0[q][1], z1);
+        }
+    }
+    for (int i0 = lo + kPrefixChunk; i0 < hi; i0 += kPrefixChunk2) {
+        float4 T[kPrefixChunk2][2];
+        load_maps(maps, M, i0, hi, T);
+#pragma unroll
+        for (int q = 0; q < kPrefixChunk2; ++q) {
+            if (i0 + q < hi) {
+                out[(size_t)(i0 + q) * (M / 2)] = make_float4(z0.x, z0.y, z1.x, z1.y);
+                z0 = capply(T[q][0], z0);
+                z1 = capply(T[q][1], z1);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 6)
+    samu_fwd_replay_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ctrl,
+                           SamuScanFwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    const SegGeom& g = a.g;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
+    if (gw >= (long long)g.n_chains * g.NS) return;
+    const SegTask T = seg_task(g, gw);
+    const int M = g.M;
+    const int L = g.L;
+    const size_t D = 2 * (size_t)M;
+    const int m = T.grp * kGroup + 2 * lane;
+    const bool active = m < M;
+    const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
+    ring_init(R, lane);
+    if (lane == 0)
+        for (int k = 0; k < kRing && k < T.nsc; ++k)
+            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
     ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
-    const int r0 = warp * kSub;
-    const int nsub = max(0, min(kSub, L - t0 - r0));
     float2 z0 = make_float2(0.f, 0.f), z1 = z0;
     if (active) {
         k0 = load_mode(a.modes, a.nu, m);
         k1 = load_mode(a.modes, a.nu, m + 1);
-        if (nsub > 0) {
-            const float4 hv = ldcg4(reinterpret_cast<const float4*>(
-                a.hsub + (hb + (size_t)c * kScanWarps + warp) * M + m));
+        const float4 e = *reinterpret_cast<const float4*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m);
+        z0 = make_float2(e.x, e.y);
+        z1 = make_float2(e.z, e.w);
+    }
+    for (int k = 0; k < T.nsc; ++k) {
+        const int slot = k % kRing;
+        const int ts = T.t_begin + k * kSub;
+        const int nsub = min(kSub, T.t_end - ts);
+        if (active)
+            *reinterpret_cast<float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kSub) * M + m) =
+                make_float4(z0.x, z0.y, z1.x, z1.y);
+        if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
+        const float4* sc = R.ctrl[slot];
+        const uint32_t* wre = &R.box[slot][0][0][lane];
+        const uint32_t* wim = &R.box[slot][1][0][lane];
+        const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
+        float* y32p = a.y32 != nullptr ? a.y32 + 2 * row0 : nullptr;
+        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
+        LRS_SUB_DISPATCH(kd, fwd_replay_sub, sc, wre, wim, nsub, k0, k1, z0, z1, a.y + row0, y32p, active, D / 2,
+                         M / 2);
+        __syncwarp();
+        if (lane == 0 && k + kRing < T.nsc)
+            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (k + kRing) * kSub, T.b);
+    }
+    if (active && T.t_end == L)
+        *reinterpret_cast<float4*>(a.hT + ((size_t)T.b * M + m) * 2) = make_float4(z0.x, z0.y, z1.x, z1.y);
+}
+
+// ---------------------------------------------------------------------------
+// Backward.  The adjoint R arriving at a span's last token from later tokens
+// leaves the span towards the past as Q R + beta, Q = conj(product of the
+// span's lambdas); stored as {Q, beta} so that capply() applies it.  For one
+// token, R -> conj(lambda_t) (R + dy_t).
+// ---------------------------------------------------------------------------
+// Appends the sub-chunk's tokens, earliest first, to the map G of the tokens
+// before them: G o F_t = (Q conj(lambda_t), beta + Q conj(lambda_t) dy_t).
+template <bool FAST, bool SIMPLE>
+__device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nsub,
+                                             const ModeConst& k0, const ModeConst& k1, float2& Q0, float2& Q1,
+                                             float2& be0, float2& be1) {
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        if (SIMPLE || i < nsub) {
+            const float4 ct = sc[i];
+            const float2 r = bf2_to_f2(gre[i * kWords]);
+            const float2 im = bf2_to_f2(gim[i * kWords]);
+            if (SIMPLE || !is_reset(ct)) {
+                Q0 = cmulc(samu_lambda<FAST>(k0, ct), Q0);
+                Q1 = cmulc(samu_lambda<FAST>(k1, ct), Q1);
+                be0 = cfma(Q0, make_float2(r.x, im.x), be0);
+                be1 = cfma(Q1, make_float2(r.y, im.y), be1);
+            } else {   // segment start: nothing reaches back past it
+                Q0 = make_float2(0.f, 0.f);
+                Q1 = Q0;
+            }
+        }
+    }
+}
+
+// Forward sweep of one sub-chunk from its entry state: u_t = lambda_t z_{t-1}
+// (kept for kappa) and z_t = u_t + b_t.
+template <bool FAST, bool SIMPLE>
+__device__ __forceinline__ void bwd_forward_sweep(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
+                                                  const ModeConst& k0, const ModeConst& k1, float2 z0, float2 z1,
+                                                  float4 (&u)[kSub]) {
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) {
+        u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (SIMPLE || i < nsub) {
+            const float4 ct = sc[i];
+            const float2 br = bf2_to_f2(wre[i * kWords]);
+            const float2 bi = bf2_to_f2(wim[i * kWords]);
+            if (SIMPLE || !is_reset(ct)) {
+                float2 u0, u1;
+                z0 = step_state(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), z0, &u0);
+                z1 = step_state(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), z1, &u1);
+                u[i] = make_float4(u0.x, u0.y, u1.x, u1.y);
+            } else {
+                z0 = make_float2(br.x, bi.x);
+                z1 = make_float2(br.y, bi.y);
+            }
+        }
+    }
+}
+
+// Sums v[k] over the 32 lanes of the warp for every k at once: on return
+// lane L holds the total of v[L].  31 shuffles (a butterfly that halves the
+// live values at each of its five levels) in a fixed order.
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < o; ++k) {
+            const float send = up ? v[k] : v[k + o];
+            const float keep = up ? v[k + o] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+// Reverse sweep: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
+// kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa,
+// per token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64
+// modes of the warp (written to kp[token * kp_row + {0, 1}]); then
+// A <- conj(lambda_t) A.
+template <bool FAST, bool SIMPLE>
+__device__ __forceinline__ void bwd_reverse_sweep(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nsub,
+                                                  const ModeConst& k0, const ModeConst& k1, const float4 (&u)[kSub],
+                                                  float2& A0, float2& A1, float4& acc, uint32_t* dwb, float* dwf,
+                                                  bool fp32, bool active, size_t row, int half, float* kp,
+                                                  size_t kp_row, int lane) {
+    float v[2 * kSub];
+#pragma unroll
+    for (int i = kSub - 1; i >= 0; --i) {
+        v[2 * i] = 0.f;
+        v[2 * i + 1] = 0.f;
+        if (SIMPLE || i < nsub) {
+            const float4 ct = sc[i];
+            const float2 g_r = bf2_to_f2(gre[i * kWords]);
+            const float2 g_i = bf2_to_f2(gim[i * kWords]);
+            A0 = make_float2(A0.x + g_r.x, A0.y + g_i.x);
+            A1 = make_float2(A1.x + g_r.y, A1.y + g_i.y);
+            if (active) {
+                if (fp32) {
+                    float* p = dwf + 2 * (size_t)i * row;
+                    __stcs(reinterpret_cast<float2*>(p), make_float2(A0.x, A1.x));
+                    __stcs(reinterpret_cast<float2*>(p + 2 * half), make_float2(A0.y, A1.y));
+                } else {
+                    uint32_t* p = dwb + (size_t)i * row;
+                    __stcs(p, f2_to_bf2(A0.x, A1.x));
+                    __stcs(p + half, f2_to_bf2(A0.y, A1.y));
+                }
+            }
+            if (SIMPLE || !is_reset(ct)) {
+                const float4 uu = u[i];
+                const float kr0 = __fmaf_rn(A0.x, uu.x, __fmul_rn(A0.y, uu.y));
+                const float ki0 = __fmaf_rn(A0.y, uu.x, -__fmul_rn(A0.x, uu.y));
+                const float kr1 = __fmaf_rn(A1.x, uu.z, __fmul_rn(A1.y, uu.w));
+                const float ki1 = __fmaf_rn(A1.y, uu.z, -__fmul_rn(A1.x, uu.w));
+                const float Et = 1.0f + ct.x;   // ct.x holds E - 1
+                acc.x = __fmaf_rn(-Et, kr0, acc.x);   // dnu_m
+                acc.y += ki0;                         // dtheta_m
+                acc.z = __fmaf_rn(-Et, kr1, acc.z);
+                acc.w += ki1;
+                v[2 * i] = ki0 + ki1;
+                v[2 * i + 1] = -__fmaf_rn(k0.nu, kr0, __fmul_rn(k1.nu, kr1));
+                A0 = cmulc(samu_lambda<FAST>(k0, ct), A0);
+                A1 = cmulc(samu_lambda<FAST>(k1, ct), A1);
+            } else {   // segment start: no controller terms, the adjoint stops here
+                A0 = make_float2(0.f, 0.f);
+                A1 = A0;
+            }
+        }
+    }
+    const float tot = warp_reduce_scatter32(v, lane);
+    if ((lane >> 1) < nsub) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 6)
+    samu_bwd_maps_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_ctrl,
+                         SamuScanBwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    const SegGeom& g = a.g;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
+    if (gw >= (long long)g.n_chains * g.NS) return;
+    const SegTask T = seg_task(g, gw);
+    const int M = g.M;
+    const int m = T.grp * kGroup + 2 * lane;
+    const bool active = m < M;
+    const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
+    ring_init(R, lane);
+    // item k is sub-chunk k: the segment from its start forwards
+    if (lane == 0)
+        for (int k = 0; k < kRing && k < T.nsc; ++k)
+            ring_issue(R, k, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
+    ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
+    if (active) {
+        k0 = load_mode(a.modes, a.nu, m);
+        k1 = load_mode(a.modes, a.nu, m + 1);
+    }
+    float2 Q0 = make_float2(1.f, 0.f), Q1 = Q0;
+    float2 be0 = make_float2(0.f, 0.f), be1 = be0;
+    for (int k = 0; k < T.nsc; ++k) {
+        const int slot = k % kRing;
+        const int ts = T.t_begin + k * kSub;
+        const int nsub = min(kSub, T.t_end - ts);
+        if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
+        const float4* sc = R.ctrl[slot];
+        const uint32_t* gre = &R.box[slot][0][0][lane];
+        const uint32_t* gim = &R.box[slot][1][0][lane];
+        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
+        LRS_SUB_DISPATCH(kd, bwd_maps_sub, sc, gre, gim, nsub, k0, k1, Q0, Q1, be0, be1);
+        __syncwarp();
+        if (lane == 0 && k + kRing < T.nsc)
+            ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (k + kRing) * kSub, T.b);
+    }
+    if (active) {
+        float4* sm = a.smap + ((size_t)T.b * g.NS + T.s) * M + m;
+        sm[0] = make_float4(Q0.x, Q0.y, be0.x, be0.y);
+        sm[1] = make_float4(Q1.x, Q1.y, be1.x, be1.y);
+    }
+}
+
+// One CTA per chain: adjoint arriving at every segment's last token, from
+// dhT and the adjoint segment maps, the latest segments first.  Warp w
+// composes segments [NS*w/16, NS*(w+1)/16), the latest applied first.
+template <int N>
+__device__ __forceinline__ void load_maps_desc(const float4* __restrict__ maps, int M, int i0, int lo,
+                                               float4 (&T)[N][2]) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+        if (i0 - q >= lo) {
+            T[q][0] = maps[(size_t)(i0 - q) * M];
+            T[q][1] = maps[(size_t)(i0 - q) * M + 1];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPrefixWarps * 32) samu_bwd_prefix_kernel(SamuScanBwdArgs a) {
+    __shared__ float4 s_part[kPrefixWarps][32][2];
+    const SegGeom& g = a.g;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chain = blockIdx.x;
+    const int b = chain / g.n_groups;
+    const int grp = chain % g.n_groups;
+    const int M = g.M;
+    const int m = grp * kGroup + 2 * lane;
+    const bool active = m < M;
+    const int NS = g.NS;
+    const int lo = NS * warp / kPrefixWarps, hi = NS * (warp + 1) / kPrefixWarps;
+    const float4* __restrict__ maps = a.smap + (size_t)b * NS * M + m;
+    float4 P0 = identity_map(), P1 = P0;
+    float4 T0[kPrefixChunk][2];
+    if (active) {
+        load_maps_desc(maps, M, hi - 1, lo, T0);
+#pragma unroll
+        for (int q = 0; q < kPrefixChunk; ++q) {
+            if (hi - 1 - q >= lo) {
+                P0 = compose_maps(T0[q][0], P0);
+                P1 = compose_maps(T0[q][1], P1);
+            }
+        }
+        for (int i0 = hi - 1 - kPrefixChunk; i0 >= lo; i0 -= kPrefixChunk2) {
+            float4 T[kPrefixChunk2][2];
+            load_maps_desc(maps, M, i0, lo, T);
+#pragma unroll
+            for (int q = 0; q < kPrefixChunk2; ++q) {
+                if (i0 - q >= lo) {
+                    P0 = compose_maps(T[q][0], P0);
+                    P1 = compose_maps(T[q][1], P1);
+                }
+            }
+        }
+    }
+    s_part[warp][lane][0] = P0;
+    s_part[warp][lane][1] = P1;
+    __syncthreads();
+    if (!active) return;
+    float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+    if (a.dhT != nullptr) {
+        const float4 v = *reinterpret_cast<const float4*>(a.dhT + ((size_t)b * M + m) * 2);
+        r0 = make_float2(v.x, v.y);
+        r1 = make_float2(v.z, v.w);
+    }
+    for (int v = kPrefixWarps - 1; v > warp; --v) {
+        r0 = capply(s_part[v][lane][0], r0);
+        r1 = capply(s_part[v][lane][1], r1);
+    }
+    float4* __restrict__ out = reinterpret_cast<float4*>(a.sent + (size_t)b * NS * M + m);
+#pragma unroll
+    for (int q = 0; q < kPrefixChunk; ++q) {
+        if (hi - 1 - q >= lo) {
+            out[(size_t)(hi - 1 - q) * (M / 2)] = make_float4(r0.x, r0.y, r1.x, r1.y);
+            r0 = capply(T0[q][0], r0);
+            r1 = capply(T0[q][1], r1);
+        }
+    }
+    for (int i0 = hi - 1 - kPrefixChunk; i0 >= lo; i0 -= kPrefixChunk2) {
+        float4 T[kPrefixChunk2][2];
+        load_maps_desc(maps, M, i0, lo, T);
+#pragma unroll
+        for (int q = 0; q < kPrefixChunk2; ++q) {
+            if (i0 - q >= lo) {
+                out[(size_t)(i0 - q) * (M / 2)] = make_float4(r0.x, r0.y, r1.x, r1.y);
+                r0 = capply(T[q][0], r0);
+                r1 = capply(T[q][1], r1);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 4)
+    samu_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
+                         const __grid_constant__ CUtensorMap tm_ctrl, SamuScanBwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    const SegGeom& g = a.g;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
+    if (gw >= (long long)g.n_chains * g.NS) return;
+    const SegTask T = seg_task(g, gw);
+    const int M = g.M;
+    const int L = g.L;
+    const size_t D = 2 * (size_t)M;
+    const int m = T.grp * kGroup + 2 * lane;
+    const bool active = m < M;
+    const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
+    const int n_items = 2 * T.nsc;
+    // item k: sub-chunk nsc-1-k/2 (the segment from its end backwards); even
+    // items carry w (forward sweep), odd items dy (reverse sweep)
+    auto item_ts = [&](int k) { return T.t_begin + (T.nsc - 1 - (k >> 1)) * kSub; };
+    ring_init(R, lane);
+    if (lane == 0)
+        for (int k = 0; k < kRing && k < n_items; ++k)
+            ring_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
+    ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
+    float2 A0 = make_float2(0.f, 0.f), A1 = A0;
+    if (active) {
+        k0 = load_mode(a.modes, a.nu, m);
+        k1 = load_mode(a.modes, a.nu, m + 1);
+        const float4 e = *reinterpret_cast<const float4*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m);
+        A0 = make_float2(e.x, e.y);
+        A1 = make_float2(e.z, e.w);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // dnu_m, dtheta_m, dnu_m+1, dtheta_m+1
+    const bool fp32 = a.grad_fp32 != 0;
+    for (int k = 0; k < n_items; k += 2) {
+        const int ts = item_ts(k);
+        const int nsub = min(kSub, T.t_end - ts);
+        float2 z0 = make_float2(0.f, 0.f), z1 = z0;
+        if (active) {
+            const float4 hv = *reinterpret_cast<const float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kSub) * M + m);
             z0 = make_float2(hv.x, hv.y);
             z1 = make_float2(hv.z, hv.w);
         }
+        // w item: forward sweep
+        int slot = k % kRing;
+        if (!ring_wait(R, k, n_items, a.status, lane)) return;
+        const float4* sc = R.ctrl[slot];
+        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
+        float4 u[kSub];
+        LRS_SUB_DISPATCH(kd, bwd_forward_sweep, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nsub, k0, k1,
+                         z0, z1, u);
+        __syncwarp();
+        if (lane == 0 && k + kRing < n_items)
+            ring_issue(R, slot, ((k + kRing) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k + kRing), T.b);
+        // dy item: reverse sweep
+        slot = (k + 1) % kRing;
+        if (!ring_wait(R, k + 1, n_items, a.status, lane)) return;
+        sc = R.ctrl[slot];
+        const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
+        uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
+        float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
+        float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
+        LRS_SUB_DISPATCH(kd, bwd_reverse_sweep, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nsub, k0, k1,
+                         u, A0, A1, acc, dwb, dwf, fp32, active, D / 2, M / 2, kp, 2 * (size_t)g.n_groups, lane);
+        __syncwarp();
+        if (lane == 0 && k + 1 + kRing < n_items)
+            ring_issue(R, slot, ((k + 1 + kRing) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
+                       item_ts(k + 1 + kRing), T.b);
     }
-    const bool landed = mbar_wait_bounded(&s_bar, 0);
-    if (!__syncthreads_and(landed)) {
-        if (tid == 0) {
-            st_release_gpu(fl + c, kFlagErr);
-            atomicOr(a.status, kStatusTimeout);
-        }
-        mbar_wait_bounded(&s_bar, 0);
-        return;
-    }
-    const float4* sc = s_ctrl + r0;
-    const uint32_t* wre = &s_wre[r0][lane];
-    const uint32_t* wim = &s_wim[r0][lane];
-    const uint32_t* gre = &s_gre[r0][lane];
-    const uint32_t* gim = &s_gim[r0][lane];
-    const bool fast = use_fast_lambda(sc, lane, k0, k1);
-
-    float4 u[kSub];   // {u_m, u_m+1} per token
-    float4 F0, F1;
-    if (fast)
-        bwd_forward_sweep<true>(sc, wre, wim, gre, gim, k0, k1, z0, z1, u, F0, F1);
-    else
-        bwd_forward_sweep<false>(sc, wre, wim, gre, gim, k0, k1, z0, z1, u, F0, F1);
-    s_map[warp][lane][0] = F0;
-    s_map[warp][lane][1] = F1;
-    __syncthreads();
-
-    // warp 0: reverse tile map F_0 o F_1 o ... o F_7 (F_7 first), incoming adjoint, hand-out
-    if (warp == 0) {
-        float4 A0 = s_map[kScanWarps - 1][lane][0], A1 = s_map[kScanWarps - 1][lane][1];
-#pragma unroll
-        for (int w = kScanWarps - 2; w >= 0; --w) {
-            A0 = compose_maps(s_map[w][lane][0], A0);
-            A1 = compose_maps(s_map[w][lane][1], A1);
-        }
-        float2 R0 = make_float2(0.f, 0.f), R1 = R0;
-        bool err = false;
-        if (c == CT - 1) {
-            if (active && a.dhT != nullptr) {
-                const float4 v = *reinterpret_cast<const float4*>(a.dhT + ((size_t)b * M + m) * 2);
-                R0 = make_float2(v.x, v.y);
-                R1 = make_float2(v.z, v.w);
-            }
-        } else {
-            int j = -1;
-            if (ld_acquire_gpu(fl + c + 1) == kFlagIncl) {
-                j = c + 1;
-            } else {
-                if (active) {
-                    float4* ag = a.agg + ((size_t)b * CT + c) * M + m;
-                    ag[0] = A0;
-                    ag[1] = A1;
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
-                j = lookback_find_warp(fl, c, CT, +1);
-            }
-            if (j < 0) {
-                err = true;
-            } else if (active) {
-                const float4 rv = ldcg4(reinterpret_cast<const float4*>(a.rin + ((size_t)b * CT + j) * M + m));
-                R0 = make_float2(rv.x, rv.y);
-                R1 = make_float2(rv.z, rv.w);
-                for (int i = j - 1; i > c; i -= 4) {   // maps of tiles j-1 .. c+1 (later first)
-                    float4 T[4][2];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (i - q > c) {
-                            const float4* ag = a.agg + ((size_t)b * CT + i - q) * M + m;
-                            T[q][0] = ldcg4(ag);
-                            T[q][1] = ldcg4(ag + 1);
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (i - q > c) {
-                            R0 = capply(T[q][0], R0);
-                            R1 = capply(T[q][1], R1);
-                        }
-                    }
-                }
-            }
-        }
-        if (!err) {
-            if (active) {
-                const float2 o0 = capply(A0, R0);
-                const float2 o1 = capply(A1, R1);
-                *reinterpret_cast<float4*>(a.rin + ((size_t)b * CT + c) * M + m) = make_float4(o0.x, o0.y, o1.x, o1.y);
-            }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
-            float2 r0v = R0, r1v = R1;
-#pragma unroll
-            for (int w = kScanWarps - 1; w >= 0; --w) {
-                s_ent[w][lane] = make_float4(r0v.x, r0v.y, r1v.x, r1v.y);
-                r0v = capply(s_map[w][lane][0], r0v);
-                r1v = capply(s_map[w][lane][1], r1v);
-            }
-        } else if (lane == 0) {
-            st_release_gpu(fl + c, kFlagErr);
-            atomicOr(a.status, kStatusTimeout);
-        }
-        if (lane == 0) s_err = err ? 1 : 0;
-    }
-    __syncthreads();
-    if (s_err) return;
-
-    // reverse sweep
-    const float4 e = s_ent[warp][lane];
-    float2 A0 = make_float2(e.x, e.y), A1 = make_float2(e.z, e.w);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // dnu_m, dtheta_m, dnu_m+1, dtheta_m+1
-    const size_t row = (((size_t)b * L + t0 + r0) * D + m) / 2;
-    uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row;
-    float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row;
-    float2* kp = a.kpart + ((size_t)b * L + t0 + r0) * g.n_groups + grp;
-    if (fast)
-        bwd_reverse_sweep<true>(sc, gre, gim, k0, k1, u, A0, A1, acc, dwb, dwf, a.grad_fp32 != 0, active, D / 2,
-                                M / 2, kp, g.n_groups, lane);
-    else
-        bwd_reverse_sweep<false>(sc, gre, gim, k0, k1, u, A0, A1, acc, dwb, dwf, a.grad_fp32 != 0, active, D / 2,
-                                 M / 2, kp, g.n_groups, lane);
-    if (c == 0 && warp == 0 && active)
-        *reinterpret_cast<float4*>(a.dh0 + ((size_t)b * M + m) * 2) = make_float4(A0.x, A0.y, A1.x, A1.y);
-    s_acc[warp][lane] = acc;
-    __syncthreads();
-    if (warp == 0 && active) {
-        float4 s = s_acc[0][lane];
-#pragma unroll
-        for (int w = 1; w < kScanWarps; ++w) {
-            const float4 v = s_acc[w][lane];
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
-        }
-        *reinterpret_cast<float4*>(a.numod + ((size_t)b * CT + c) * M + m) = s;
+    if (active) {
+        *reinterpret_cast<float4*>(a.numod + ((size_t)T.b * g.NS + T.s) * M + m) = acc;
+        if (T.s == 0)
+            *reinterpret_cast<float4*>(a.dh0 + ((size_t)T.b * M + m) * 2) = make_float4(A0.x, A0.y, A1.x, A1.y);
     }
 }
 
 // ---------------------------------------------------------------------------
-cudaError_t launch_samu_scan_fwd(const CUtensorMap& tm_w, const SamuScanFwdArgs& args, cudaStream_t s) {
-    samu_scan_fwd_kernel<<<(unsigned)args.g.n_tiles, kScanThreads, 0, s>>>(tm_w, args);
+// Host side.
+namespace {
+
+struct EngineOccupancy {
+    bool done = false;
+    int sms = 0;
+    int fwd = 0;   // resident CTAs per SM for the forward pair (maps, replay)
+    int bwd = 0;   // ... and for the backward pair (maps, main)
+};
+
+EngineOccupancy g_occ[64];
+
+bool set_smem(const void* fn) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngineSmem) == cudaSuccess;
+}
+
+int occupancy(const void* fn) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kEngineThreads, kEngineSmem) != cudaSuccess) return 1;
+    return n > 0 ? n : 1;
+}
+
+const EngineOccupancy& engine_occupancy() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    EngineOccupancy& o = g_occ[dev];
+    if (!o.done) {
+        int v = 0;
+        o.sms = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;
+        const void* fm = reinterpret_cast<const void*>(samu_fwd_maps_kernel);
+        const void* fr = reinterpret_cast<const void*>(samu_fwd_replay_kernel);
+        const void* bm = reinterpret_cast<const void*>(samu_bwd_maps_kernel);
+        const void* bb = reinterpret_cast<const void*>(samu_bwd_main_kernel);
+        set_smem(fm);
+        set_smem(fr);
+        set_smem(bm);
+        set_smem(bb);
+        o.fwd = std::min(occupancy(fm), occupancy(fr));
+        o.bwd = std::min(occupancy(bm), occupancy(bb));
+        o.done = true;
+    }
+    return o;
+}
+
+unsigned engine_grid(const SegGeom& g) {
+    const long long warps = (long long)g.n_chains * g.NS;
+    return (unsigned)((warps + kEngineWarps - 1) / kEngineWarps);
+}
+
+}  // namespace
+
+SegGeom samu_scan_geom(int B, int L, int M, bool backward) {
+    const EngineOccupancy& o = engine_occupancy();
+    const long long warps = (long long)(backward ? o.bwd : o.fwd) * kEngineWarps * o.sms;
+    return samu_seg_geom(B, L, M, warps);
+}
+
+cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
+                                 cudaStream_t s) {
+    samu_fwd_maps_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_w, tm_ctrl, args);
     return cudaGetLastError();
 }
 
-cudaError_t launch_samu_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_w,
+cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s) {
+    samu_fwd_prefix_kernel<<<args.g.n_chains, kPrefixWarps * 32, 0, s>>>(args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
+                                   cudaStream_t s) {
+    samu_fwd_replay_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_w, tm_ctrl, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
+                                 cudaStream_t s) {
+    samu_bwd_maps_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_dy, tm_ctrl, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s) {
+    samu_bwd_prefix_kernel<<<args.g.n_chains, kPrefixWarps * 32, 0, s>>>(args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
                                  const SamuScanBwdArgs& args, cudaStream_t s) {
-    const int smem = 4 * kBoxBytes;
-    cudaError_t e = cudaFuncSetAttribute(samu_scan_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    samu_scan_bwd_kernel<<<(unsigned)args.g.n_tiles, kScanThreads, smem, s>>>(tm_dy, tm_w, args);
+    samu_bwd_main_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_dy, tm_w, tm_ctrl, args);
     return cudaGetLastError();
 }
 

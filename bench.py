@@ -52,7 +52,7 @@ KERNEL_BYTES_PER_BLD = {
     "samu_bwd_maps_kernel": 2.0, "samu_bwd_main_kernel": 6.0, "samu_ctrl_bwd_kernel": 4.0,
 }
 STEP_BYTES_PER_BLD = 16.0
-LAUNCHES_PER_RECORD = {"samu_params_kernels": 3, "rglru_alpha_kernels": 2}
+LAUNCHES_PER_RECORD = {"rglru_alpha_kernels": 2}
 
 
 def parse_args(argv=None):

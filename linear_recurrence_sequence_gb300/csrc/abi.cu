@@ -64,6 +64,11 @@ void prof_end(cudaStream_t s) {
     ++g_prof.n;
 }
 
+// Launches after the first of a call overlap their start with the previous
+// kernel (programmatic dependent launch), except while per-kernel timing is
+// on, so that every kernel's events bracket it alone.
+bool pdl_ok() { return !g_prof.on; }
+
 // Kernel ids reported by lrs_profile_end.
 enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
@@ -204,7 +209,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.wh = wh;
     cf.misc = misc;
     cf.modes = modes;
-    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream));
+    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream, false));
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
     CUtensorMap tm_w, tm_ctrl;
@@ -221,9 +226,9 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     a.smap = at<float4>(scratch, sc.smap);
     a.sent = at<float2>(scratch, sc.sent);
     a.status = at<uint32_t>(scratch, sc.status);
-    LRS_LAUNCH(KID_SAMU_FWD_MAPS, stream, launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream));
-    LRS_LAUNCH(KID_SAMU_FWD_PREFIX, stream, launch_samu_fwd_prefix(a, stream));
-    LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream));
+    LRS_LAUNCH(KID_SAMU_FWD_MAPS, stream, launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream, pdl_ok()));
+    LRS_LAUNCH(KID_SAMU_FWD_PREFIX, stream, launch_samu_fwd_prefix(a, stream, pdl_ok()));
+    LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream, pdl_ok()));
     return LRS_OK;
 }
 
@@ -271,9 +276,9 @@ int samu_backward(const void* dy, const float* dhT,
     s.kpart = at<float2>(scratch, sc.kpart);
     s.numod = at<float2>(scratch, sc.numod);
     s.status = at<uint32_t>(scratch, sc.status);
-    LRS_LAUNCH(KID_SAMU_BWD_MAPS, stream, launch_samu_bwd_maps(tm_dy, tm_ctrl, s, stream));
-    LRS_LAUNCH(KID_SAMU_BWD_PREFIX, stream, launch_samu_bwd_prefix(s, stream));
-    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy, tm_w, tm_ctrl, s, stream));
+    LRS_LAUNCH(KID_SAMU_BWD_MAPS, stream, launch_samu_bwd_maps(tm_dy, tm_ctrl, s, stream, false));
+    LRS_LAUNCH(KID_SAMU_BWD_PREFIX, stream, launch_samu_bwd_prefix(s, stream, pdl_ok()));
+    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy, tm_w, tm_ctrl, s, stream, pdl_ok()));
 
     SamuCtrlBwdArgs cb;
     cb.B = B;
@@ -291,7 +296,7 @@ int samu_backward(const void* dy, const float* dhT,
     cb.grad_fp32 = fp32;
     cb.dwh_part = at<float>(scratch, sc.dwh_part);
     cb.amp_part = at<float2>(scratch, sc.amp_part);
-    LRS_LAUNCH(KID_SAMU_CTRL_BWD, stream, launch_samu_ctrl_bwd(cb, stream));
+    LRS_LAUNCH(KID_SAMU_CTRL_BWD, stream, launch_samu_ctrl_bwd(cb, stream, pdl_ok()));
 
     SamuParamArgs pa;
     pa.B = B;
@@ -299,10 +304,10 @@ int samu_backward(const void* dy, const float* dhT,
     pa.D = D;
     pa.n_part = g.NS;
     pa.numod = at<float2>(scratch, sc.numod);
-    pa.numod2 = at<float2>(scratch, sc.numod2);
     pa.dwh_part = cb.dwh_part;
     pa.amp_part = cb.amp_part;
     pa.dwh = at<float>(scratch, sc.dwh);
+    pa.counter = at<uint32_t>(scratch, sc.status + 4);
     pa.wh = cb.wh;
     pa.misc = cb.misc;
     pa.dnu = dnu;
@@ -311,7 +316,7 @@ int samu_backward(const void* dy, const float* dhT,
     pa.dw_r = dw_r;
     pa.da_phi = da_phi;
     pa.da_r = da_r;
-    LRS_LAUNCH(KID_SAMU_PARAMS, stream, launch_samu_params(pa, stream));
+    LRS_LAUNCH(KID_SAMU_PARAMS, stream, launch_samu_params(pa, stream, pdl_ok()));
     return LRS_OK;
 }
 

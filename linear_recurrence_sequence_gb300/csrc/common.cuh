@@ -184,6 +184,30 @@ __device__ __forceinline__ int lookback_find_warp(const uint32_t* flags, int c, 
     }
 }
 
+// Programmatic dependent launch.  A kernel launched with
+// launch_ex(..., pdl = true) may start while the previous kernel on the
+// stream is still running; it must call pdl_wait() before it touches global
+// memory that earlier kernels write or read.  pdl_trigger() lets the next
+// kernel start once every CTA of this one has issued it.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // 2^x on the SFU (PTX ex2.approx, documented relative error ~2^-22).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

@@ -134,10 +134,10 @@ struct SamuParamArgs {
     int B, L, D;
     int n_part;             // numod rows per batch row
     const float2* numod;    // [B*n_part][M]
-    float2* numod2;         // [kReduceGroups][M]
     const float* dwh_part;  // [kCtrlBwdCtas * 2 halves][2][D+1]
     const float2* amp_part;
-    float* dwh;             // [8 groups][2][D+1] column sums of dwh_part
+    float* dwh;             // [2][D+1] column sums of dwh_part
+    uint32_t* counter;      // CTA arrival counter, zero on entry, left zero
     const float* wh;
     const float* misc;
     float* dnu;
@@ -168,24 +168,25 @@ struct SamuCtrlFwdArgs {
     float4* modes;                 // [M] lbar hi/lo
 };
 
-cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s);
+cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s, bool pdl);
 // Segment geometry of the forward (backward = false) or backward scan on the
 // current device: every segment of every chain resident at once.
 SegGeom samu_scan_geom(int B, int L, int M, bool backward);
 // Forward: maps (w read backwards in time), prefix, replay (forwards).
+// pdl: launch as a programmatic dependent of the previous kernel on s.
 cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
-                                 cudaStream_t s);
-cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s);
+                                 cudaStream_t s, bool pdl);
+cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
-                                   cudaStream_t s);
+                                   cudaStream_t s, bool pdl);
 // Backward: maps (dy read forwards in time), prefix, main (backwards).
 cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
-                                 cudaStream_t s);
-cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s);
+                                 cudaStream_t s, bool pdl);
+cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
-                                 const SamuScanBwdArgs& args, cudaStream_t s);
-cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s);
-cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s);
+                                 const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
+cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl);
+cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------------------
 // RG-LRU

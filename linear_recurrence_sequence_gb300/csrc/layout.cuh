@@ -12,8 +12,8 @@ namespace lrs {
 
 constexpr size_t kAlign = 256;
 constexpr int kCtrlBwdCtas = 304;     // fixed grid of the controller backward (2 x 152 SMs)
-constexpr int kReduceGroups = 64;     // first-stage groups of the per-tile parameter partials
-constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status word + tile counter
+constexpr int kReduceGroups = 64;     // first-stage groups of the RG-LRU per-tile alpha partials
+constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status word + counters
 
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -130,7 +130,7 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
 }
 
 struct SamuScratch {
-    size_t status, smap, sent, kpart, numod, numod2, dwh_part, amp_part, dwh, total;
+    size_t status, smap, sent, kpart, numod, dwh_part, amp_part, dwh, total;
 };
 
 inline SamuScratch samu_scratch_layout(int B, int L, int D) {
@@ -145,10 +145,9 @@ inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     s.sent = o;     o = align_up(o + rows * 8);                       // segment entry states / adjoints
     s.kpart = o;    o = align_up(o + BL * g.n_groups * 8);            // per-token controller partials
     s.numod = o;    o = align_up(o + rows * 8);                       // per-segment (dnu, dtheta)
-    s.numod2 = o;   o = align_up(o + (size_t)kReduceGroups * M * 8);
     s.dwh_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 2 * 2 * (D + 1) * 4);   // (cta, half) rows
     s.amp_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 8);
-    s.dwh = o;      o = align_up(o + (size_t)8 * 2 * (D + 1) * 4);             // column-sum groups
+    s.dwh = o;      o = align_up(o + (size_t)2 * (D + 1) * 4);                 // column sums
     s.total = o;
     return s;
 }

@@ -104,7 +104,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     cf.wh = wh;
     cf.misc = misc;
     cf.modes = modes;
-    if (launch_samu_ctrl_fwd(cf, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_ctrl_fwd(cf, stream, false) != cudaSuccess) return LRS_ERR_CUDA;
 
     CUtensorMap tm_w, tm_ctrl;
     if (!make_bf16_map(&tm_w, w, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub)) return LRS_ERR_CUDA;
@@ -120,8 +120,8 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     a.smap = reinterpret_cast<float4*>(scratch + sc.smap);
     a.sent = reinterpret_cast<float2*>(scratch + sc.sent);
     a.status = reinterpret_cast<uint32_t*>(scratch + sc.status);
-    if (launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream) != cudaSuccess) return LRS_ERR_CUDA;
-    if (launch_samu_fwd_prefix(a, stream) != cudaSuccess) return LRS_ERR_CUDA;
-    if (launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream, true) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_fwd_prefix(a, stream, true) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream, true) != cudaSuccess) return LRS_ERR_CUDA;
     return LRS_OK;
 }

@@ -49,6 +49,8 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 __global__ void __launch_bounds__(512) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
     __shared__ float s_red[2][512 / 32];
     __shared__ float s_part[512 / 32][2 * kCfTok];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int D = a.D;
     const int M = D / 2;
@@ -213,6 +215,8 @@ __global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a
     __shared__ float s_sphi[kCbTokBlock];
     __shared__ float s_sr[kCbTokBlock];
     __shared__ float s_red[4][kCbTokBlock];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int D = a.D;
     const int vecs = D / 8;
@@ -352,156 +356,146 @@ __global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a
 }
 
 // ---------------------------------------------------------------------------
-// Parameter reductions (fixed order, deterministic).
+// Parameter reductions (fixed order, deterministic), one launch:
+//  - CTAs [0, ceil(M/32)): 32 modes each; warp w sums the per-segment
+//    (dnu, dtheta) rows w, w+32, ...; the 32 warp sums are added in order;
+//  - the next 2*ceil((D+1)/32) CTAs: 32 columns of dw_hat_phi or dw_hat_r
+//    each, summed the same way over the controller-backward partial rows;
+//  - the CTA that arrives last (threadfence + counter) computes the
+//    unit-direction projection dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||
+//    and the amplitude gradients da = (sum of partials) / sqrt(M) (1 - tanh(a)^2),
+//    and clears the counter for the next call.
 // ---------------------------------------------------------------------------
-// stage 1: per-segment (dnu, dtheta) partials, rows = B*n_part, into kReduceGroups groups
-__global__ void __launch_bounds__(256) samu_numod_stage1_kernel(const float2* __restrict__ numod,
-                                                                float2* __restrict__ numod2,
-                                                                int rows, int M) {
-    const int m = blockIdx.x * blockDim.x + threadIdx.x;
-    const int gidx = blockIdx.y;
-    if (m >= M) return;
-    const int per = (rows + kReduceGroups - 1) / kReduceGroups;
-    const int r0 = gidx * per;
-    const int r1 = min(rows, r0 + per);
-    float sx = 0.f, sy = 0.f;
-    int r = r0;
-    for (; r + 8 <= r1; r += 8) {
-        float2 v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcs(numod + (size_t)(r + k) * M + m);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            sx += v[k].x;
-            sy += v[k].y;
-        }
-    }
-    for (; r < r1; ++r) {
-        const float2 v = __ldcs(numod + (size_t)r * M + m);
-        sx += v.x;
-        sy += v.y;
-    }
-    numod2[(size_t)gidx * M + m] = make_float2(sx, sy);
-}
+constexpr int kParamWarps = 32;
+constexpr int kParamThreads = kParamWarps * 32;
+constexpr int kColRows = 2 * kCtrlBwdCtas;   // (CTA, token half) partial rows
 
-// stage 2: dnu[m], dtheta[m] = sum over the kReduceGroups first-stage sums
-__global__ void __launch_bounds__(256) samu_numod_stage2_kernel(const float2* __restrict__ numod2,
-                                                                float* __restrict__ dnu,
-                                                                float* __restrict__ dtheta, int M) {
-    const int m = blockIdx.x * blockDim.x + threadIdx.x;
-    if (m >= M) return;
-    float sx = 0.f, sy = 0.f;
-#pragma unroll 16
-    for (int gi = 0; gi < kReduceGroups; ++gi) {
-        const float2 v = numod2[(size_t)gi * M + m];
-        sx += v.x;
-        sy += v.y;
-    }
-    dnu[m] = sx;
-    dtheta[m] = sy;
-}
-
-// column sums of the controller-backward partial rows, first stage: CTA
-// (column block of 32, which in {phi, r}, row group z) -> colpart[z][which][j].
-constexpr int kColRows = 2 * kCtrlBwdCtas;
-constexpr int kColGroups = 8;
-constexpr int kColRowsPerGroup = (kColRows + kColGroups - 1) / kColGroups;
-
-__global__ void __launch_bounds__(256) samu_dwh_colsum_kernel(const float* __restrict__ part,
-                                                              float* __restrict__ colpart, int D) {
-    __shared__ float s_part[8][32];
-    const int n = D + 1;
+// Block-wide sum of four values, fixed order; every thread gets the totals.
+__device__ __forceinline__ float4 block_sum4(float4 v, float4 (*s_w)[1]) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int j = blockIdx.x * 32 + lane;
-    const int which = blockIdx.y;
-    const int r0 = blockIdx.z * kColRowsPerGroup;
-    const int r1 = min(kColRows, r0 + kColRowsPerGroup);
-    float s = 0.f;
-    if (j < n) {
-        float v[10];
 #pragma unroll
-        for (int k = 0; k < 10; ++k) {
-            const int r = r0 + warp + 8 * k;
-            v[k] = r < r1 ? part[((size_t)r * 2 + which) * n + j] : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 10; ++k) s += v[k];
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
     }
-    s_part[warp][lane] = s;
+    if (lane == 0) s_w[warp][0] = v;
     __syncthreads();
-    if (warp == 0 && j < n) {
-        float t = s_part[0][lane];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) t += s_part[w][lane];
-        colpart[((size_t)blockIdx.z * 2 + which) * n + j] = t;
+    float4 t = s_w[0][0];
+    for (int w = 1; w < kParamWarps; ++w) {
+        const float4 u = s_w[w][0];
+        t.x += u.x;
+        t.y += u.y;
+        t.z += u.z;
+        t.w += u.w;
     }
+    return t;
 }
 
-// final: dwh = sum of the column groups; the unit-direction projection
-// dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||; the amplitude gradients
-// da = (sum of partials) / sqrt(M) * (1 - tanh(a)^2).
-constexpr int kMaxCols = 4097;
-
-__global__ void __launch_bounds__(256) samu_param_final_kernel(SamuParamArgs a) {
-    __shared__ float s_dwh[2][kMaxCols];
-    __shared__ float s_red[4][256];
-    const int tid = threadIdx.x;
-    const int D = a.D;
-    const int n = D + 1;
-    float dp = 0.f, dr = 0.f;
-    for (int j = tid; j < n; j += blockDim.x) {
-        float v[2][kColGroups];
+__global__ void __launch_bounds__(kParamThreads) samu_params_kernel(SamuParamArgs a) {
+    __shared__ float2 s_red[kParamWarps][32];
+    __shared__ float4 s_w[kParamWarps][1];
+    __shared__ int s_last;
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int M = a.D / 2;
+    const int n = a.D + 1;
+    const int n_num = (M + 31) / 32;
+    if ((int)blockIdx.x < n_num) {
+        const int m = blockIdx.x * 32 + lane;
+        const int rows = a.B * a.n_part;
+        float2 sum = make_float2(0.f, 0.f);
+        if (m < M) {
+            int r = warp;
+            for (; r + 3 * kParamWarps < rows; r += 4 * kParamWarps) {
+                float2 v[4];
 #pragma unroll
-        for (int z = 0; z < kColGroups; ++z) {
-            v[0][z] = a.dwh[((size_t)z * 2 + 0) * n + j];
-            v[1][z] = a.dwh[((size_t)z * 2 + 1) * n + j];
-        }
-        float sp = 0.f, sr = 0.f;
+                for (int q = 0; q < 4; ++q) v[q] = __ldcg(a.numod + (size_t)(r + q * kParamWarps) * M + m);
 #pragma unroll
-        for (int z = 0; z < kColGroups; ++z) {
-            sp += v[0][z];
-            sr += v[1][z];
+                for (int q = 0; q < 4; ++q) {
+                    sum.x += v[q].x;
+                    sum.y += v[q].y;
+                }
+            }
+            for (; r < rows; r += kParamWarps) {
+                const float2 v = __ldcg(a.numod + (size_t)r * M + m);
+                sum.x += v.x;
+                sum.y += v.y;
+            }
         }
-        s_dwh[0][j] = sp;
-        s_dwh[1][j] = sr;
-        dp = fmaf(a.wh[j], sp, dp);
-        dr = fmaf(a.wh[n + j], sr, dr);
-    }
-    float ap = 0.f, ar = 0.f;
-    for (int k = tid; k < kCtrlBwdCtas; k += blockDim.x) {
-        const float2 v = a.amp_part[k];
-        ap += v.x;
-        ar += v.y;
-    }
-    s_red[0][tid] = dp;
-    s_red[1][tid] = dr;
-    s_red[2][tid] = ap;
-    s_red[3][tid] = ar;
-    __syncthreads();
-    for (int s2 = blockDim.x / 2; s2 > 0; s2 >>= 1) {
-        if (tid < s2) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) s_red[q][tid] += s_red[q][tid + s2];
-        }
+        s_red[warp][lane] = sum;
         __syncthreads();
+        if (warp == 0 && m < M) {
+            float2 t = s_red[0][lane];
+            for (int w = 1; w < kParamWarps; ++w) {
+                t.x += s_red[w][lane].x;
+                t.y += s_red[w][lane].y;
+            }
+            a.dnu[m] = t.x;
+            a.dtheta[m] = t.y;
+        }
+    } else {
+        const int cb = blockIdx.x - n_num;
+        const int which = cb & 1;
+        const int j = (cb >> 1) * 32 + lane;
+        float sum = 0.f;
+        if (j < n) {
+            int r = warp;
+            for (; r + 3 * kParamWarps < kColRows; r += 4 * kParamWarps) {
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = __ldcg(a.dwh_part + ((size_t)(r + q * kParamWarps) * 2 + which) * n + j);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) sum += v[q];
+            }
+            for (; r < kColRows; r += kParamWarps) sum += __ldcg(a.dwh_part + ((size_t)r * 2 + which) * n + j);
+        }
+        s_red[warp][lane].x = sum;
+        __syncthreads();
+        if (warp == 0 && j < n) {
+            float t = s_red[0][lane].x;
+            for (int w = 1; w < kParamWarps; ++w) t += s_red[w][lane].x;
+            a.dwh[(size_t)which * n + j] = t;
+        }
     }
-    const float dot_p = s_red[0][0];
-    const float dot_r = s_red[1][0];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);   // w_hat . dw_hat (phi, r), amplitude sums (phi, r)
+    for (int j = threadIdx.x; j < n; j += kParamThreads) {
+        v.x = fmaf(a.wh[j], __ldcg(a.dwh + j), v.x);
+        v.y = fmaf(a.wh[n + j], __ldcg(a.dwh + n + j), v.y);
+    }
+    for (int k = threadIdx.x; k < kCtrlBwdCtas; k += kParamThreads) {
+        const float2 u = __ldcg(a.amp_part + k);
+        v.z += u.x;
+        v.w += u.y;
+    }
+    const float4 t = block_sum4(v, s_w);
     const float nphi = a.misc[2];
     const float nr = a.misc[3];
-    for (int j = tid; j < n; j += blockDim.x) {
-        a.dw_phi[j] = (s_dwh[0][j] - a.wh[j] * dot_p) / nphi;
-        a.dw_r[j] = (s_dwh[1][j] - a.wh[n + j] * dot_r) / nr;
+    for (int j = threadIdx.x; j < n; j += kParamThreads) {
+        a.dw_phi[j] = (__ldcg(a.dwh + j) - a.wh[j] * t.x) / nphi;
+        a.dw_r[j] = (__ldcg(a.dwh + n + j) - a.wh[n + j] * t.y) / nr;
     }
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
         const float ta = a.misc[4], tr = a.misc[5], ism = a.misc[6];
-        a.da_phi[0] = s_red[2][0] * ism * (1.0f - ta * ta);
-        a.da_r[0] = s_red[3][0] * ism * (1.0f - tr * tr);
+        a.da_phi[0] = t.z * ism * (1.0f - ta * ta);
+        a.da_r[0] = t.w * ism * (1.0f - tr * tr);
+        *a.counter = 0u;
     }
 }
 
-cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args_in, cudaStream_t s) {
+cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args_in, cudaStream_t s, bool pdl) {
     SamuCtrlFwdArgs a = args_in;
     const int M = a.D / 2;
     int cols = ((a.D / 8) + 31) / 32 * 32;
@@ -509,34 +503,20 @@ cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args_in, cudaStream_t s)
     a.n_mode_ctas = (M + kModeThreads - 1) / kModeThreads;
     const long long want = (a.BL + kCfTok - 1) / kCfTok;
     a.n_tok_ctas = (int)(want < 152LL * 4 ? want : 152LL * 4);
-    samu_ctrl_fwd_kernel<<<a.n_mode_ctas + a.n_tok_ctas, cols, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_ex(samu_ctrl_fwd_kernel, a.n_mode_ctas + a.n_tok_ctas, cols, 0, s, pdl, a);
 }
 
-cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s) {
+cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl) {
     int cols = ((args.D / 8) + 31) / 32 * 32;
     if (cols < kCbTokBlock / 2) cols = kCbTokBlock / 2;
     const int threads = 2 * cols <= 512 ? 2 * cols : cols;   // two token halves when they fit
-    samu_ctrl_bwd_kernel<<<kCtrlBwdCtas, threads, 0, s>>>(args);
-    return cudaGetLastError();
+    return launch_ex(samu_ctrl_bwd_kernel, kCtrlBwdCtas, threads, 0, s, pdl, args);
 }
 
-cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s) {
+cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl) {
     const int M = args.D / 2;
-    const int rows = args.B * args.n_part;
-    dim3 g1((M + 255) / 256, kReduceGroups);
-    samu_numod_stage1_kernel<<<g1, 256, 0, s>>>(args.numod, args.numod2, rows, M);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    samu_numod_stage2_kernel<<<(M + 255) / 256, 256, 0, s>>>(args.numod2, args.dnu, args.dtheta, M);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dim3 g2((args.D + 1 + 31) / 32, 2, kColGroups);
-    samu_dwh_colsum_kernel<<<g2, 256, 0, s>>>(args.dwh_part, args.dwh, args.D);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    samu_param_final_kernel<<<1, 256, 0, s>>>(args);
-    return cudaGetLastError();
+    const int blocks = (M + 31) / 32 + 2 * ((args.D + 1 + 31) / 32);
+    return launch_ex(samu_params_kernel, blocks, kParamThreads, 0, s, pdl, args);
 }
 
 }  // namespace lrs

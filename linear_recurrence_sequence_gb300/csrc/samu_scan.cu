@@ -214,7 +214,6 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const int lane = threadIdx.x & 31;
     WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
     const SegGeom& g = a.g;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     if (gw >= (long long)g.n_chains * g.NS) return;
     const SegTask T = seg_task(g, gw);
@@ -223,6 +222,9 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const bool active = m < M;
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     ring_init(R, lane);
+    pdl_trigger();
+    pdl_wait();
+    if (gw == 0 && lane == 0) *a.status = 0u;
     // item k is sub-chunk nsc-1-k: the segment from its end backwards
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
@@ -275,6 +277,8 @@ __device__ __forceinline__ void load_maps(const float4* __restrict__ maps, int M
 
 __global__ void __launch_bounds__(kPrefixWarps * 32) samu_fwd_prefix_kernel(SamuScanFwdArgs a) {
     __shared__ float4 s_part[kPrefixWarps][32][2];
+    pdl_trigger();
+    pdl_wait();
     const SegGeom& g = a.g;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -365,6 +369,8 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const bool active = m < M;
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     ring_init(R, lane);
+    pdl_trigger();
+    pdl_wait();
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
@@ -541,7 +547,6 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const int lane = threadIdx.x & 31;
     WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
     const SegGeom& g = a.g;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     if (gw >= (long long)g.n_chains * g.NS) return;
     const SegTask T = seg_task(g, gw);
@@ -550,6 +555,12 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const bool active = m < M;
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     ring_init(R, lane);
+    pdl_trigger();
+    pdl_wait();
+    if (gw == 0 && lane == 0) {
+        a.status[0] = 0u;   // status word
+        a.status[1] = 0u;   // arrival counter of the parameter reductions
+    }
     // item k is sub-chunk k: the segment from its start forwards
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
@@ -599,6 +610,8 @@ __device__ __forceinline__ void load_maps_desc(const float4* __restrict__ maps, 
 
 __global__ void __launch_bounds__(kPrefixWarps * 32) samu_bwd_prefix_kernel(SamuScanBwdArgs a) {
     __shared__ float4 s_part[kPrefixWarps][32][2];
+    pdl_trigger();
+    pdl_wait();
     const SegGeom& g = a.g;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -693,6 +706,8 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     // items carry w (forward sweep), odd items dy (reverse sweep)
     auto item_ts = [&](int k) { return T.t_begin + (T.nsc - 1 - (k >> 1)) * kSub; };
     ring_init(R, lane);
+    pdl_trigger();
+    pdl_wait();
     if (lane == 0)
         for (int k = 0; k < kRing && k < n_items; ++k)
             ring_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
@@ -808,37 +823,35 @@ SegGeom samu_scan_geom(int B, int L, int M, bool backward) {
 }
 
 cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
-                                 cudaStream_t s) {
-    samu_fwd_maps_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_w, tm_ctrl, args);
-    return cudaGetLastError();
+                                 cudaStream_t s, bool pdl) {
+    return launch_ex(samu_fwd_maps_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_w, tm_ctrl,
+                     args);
 }
 
-cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s) {
-    samu_fwd_prefix_kernel<<<args.g.n_chains, kPrefixWarps * 32, 0, s>>>(args);
-    return cudaGetLastError();
+cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s, bool pdl) {
+    return launch_ex(samu_fwd_prefix_kernel, args.g.n_chains, kPrefixWarps * 32, 0, s, pdl, args);
 }
 
 cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
-                                   cudaStream_t s) {
-    samu_fwd_replay_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_w, tm_ctrl, args);
-    return cudaGetLastError();
+                                   cudaStream_t s, bool pdl) {
+    return launch_ex(samu_fwd_replay_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_w, tm_ctrl,
+                     args);
 }
 
 cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
-                                 cudaStream_t s) {
-    samu_bwd_maps_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_dy, tm_ctrl, args);
-    return cudaGetLastError();
+                                 cudaStream_t s, bool pdl) {
+    return launch_ex(samu_bwd_maps_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_ctrl,
+                     args);
 }
 
-cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s) {
-    samu_bwd_prefix_kernel<<<args.g.n_chains, kPrefixWarps * 32, 0, s>>>(args);
-    return cudaGetLastError();
+cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
+    return launch_ex(samu_bwd_prefix_kernel, args.g.n_chains, kPrefixWarps * 32, 0, s, pdl, args);
 }
 
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
-                                 const SamuScanBwdArgs& args, cudaStream_t s) {
-    samu_bwd_main_kernel<<<engine_grid(args.g), kEngineThreads, kEngineSmem, s>>>(tm_dy, tm_w, tm_ctrl, args);
-    return cudaGetLastError();
+                                 const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
+    return launch_ex(samu_bwd_main_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_w,
+                     tm_ctrl, args);
 }
 
 }  // namespace lrs

@@ -209,6 +209,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.wh = wh;
     cf.misc = misc;
     cf.modes = modes;
+    cf.status = at<uint32_t>(scratch, sc.status);
     LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream, false));
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
@@ -281,10 +282,11 @@ int samu_backward(const void* dy, const float* dhT,
     LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy, tm_w, tm_ctrl, s, stream, pdl_ok()));
 
     SamuCtrlBwdArgs cb;
-    cb.B = B;
-    cb.L = L;
+    cb.BL = (long long)B * L;
     cb.D = D;
     cb.n_groups = g.n_groups;
+    cb.cg = samu_ctrl_geom(cb.BL, D, true);
+    cb.status = s.status;
     cb.x = static_cast<const uint4*>(x_sel);
     cb.kpart = s.kpart;
     cb.p = at<float>(saved, sv.p);
@@ -303,6 +305,7 @@ int samu_backward(const void* dy, const float* dhT,
     pa.L = L;
     pa.D = D;
     pa.n_part = g.NS;
+    pa.n_rows = cb.cg.n_ctas;
     pa.numod = at<float2>(scratch, sc.numod);
     pa.dwh_part = cb.dwh_part;
     pa.amp_part = cb.amp_part;

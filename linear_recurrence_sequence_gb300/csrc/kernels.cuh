@@ -115,8 +115,26 @@ struct SamuScanBwdArgs {
     uint32_t* status;
 };
 
+// Controller streaming geometry: every CTA owns a contiguous run of
+// `stage_tok`-token stages of x_sel (and of dx_sel), staged through a ring of
+// `ring` shared-memory slots by 1-D bulk copies; one producer warp plus
+// `consumers` warps of 32 threads, each thread owning 8 channels.
+struct CtrlGeom {
+    int stage_tok;          // tokens per stage (16, or 8 when 16 rows exceed 64 KB)
+    int ring;               // slots (at most 8, filling up to 192 KB)
+    int consumers;          // consumer warps
+    int threads;            // 32 * (1 + consumers)
+    int smem;               // dynamic shared memory bytes
+    int n_ctas;             // streaming CTAs
+    long long n_stages;     // ceil(B*L / stage_tok)
+};
+
+CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward);
+
 struct SamuCtrlBwdArgs {
-    int B, L, D, n_groups;
+    long long BL;
+    int D, n_groups;
+    CtrlGeom cg;
     const uint4* x;         // BF16 x_sel as 16-byte vectors
     const float2* kpart;
     const float* p;
@@ -126,15 +144,17 @@ struct SamuCtrlBwdArgs {
     const float* misc;
     void* dx;               // BF16 or FP32
     int grad_fp32;
-    float* dwh_part;        // [kCtrlBwdCtas * 2 halves][2][D+1]
-    float2* amp_part;       // [kCtrlBwdCtas]
+    float* dwh_part;        // [cg.n_ctas][2][D+1]
+    float2* amp_part;       // [cg.n_ctas]
+    uint32_t* status;
 };
 
 struct SamuParamArgs {
     int B, L, D;
     int n_part;             // numod rows per batch row
+    int n_rows;             // rows of dwh_part / amp_part
     const float2* numod;    // [B*n_part][M]
-    const float* dwh_part;  // [kCtrlBwdCtas * 2 halves][2][D+1]
+    const float* dwh_part;  // [n_rows][2][D+1]
     const float2* amp_part;
     float* dwh;             // [2][D+1] column sums of dwh_part
     uint32_t* counter;      // CTA arrival counter, zero on entry, left zero
@@ -151,7 +171,8 @@ struct SamuParamArgs {
 struct SamuCtrlFwdArgs {
     long long BL;
     int D;
-    int n_mode_ctas, n_tok_ctas;   // filled by the launcher
+    int n_mode_ctas;               // filled by the launcher
+    CtrlGeom cg;                   // filled by the launcher
     const uint4* x;                // BF16 x_sel as 16-byte vectors
     const uint8_t* reset;
     const float* w_phi;
@@ -166,6 +187,7 @@ struct SamuCtrlFwdArgs {
     float* wh;                     // [2][D+1]
     float* misc;
     float4* modes;                 // [M] lbar hi/lo
+    uint32_t* status;
 };
 
 cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s, bool pdl);

@@ -11,7 +11,7 @@
 namespace lrs {
 
 constexpr size_t kAlign = 256;
-constexpr int kCtrlBwdCtas = 304;     // fixed grid of the controller backward (2 x 152 SMs)
+constexpr int kCtrlRowsMax = 608;    // partial-sum rows of the controller backward (CTAs)
 constexpr int kReduceGroups = 64;     // first-stage groups of the RG-LRU per-tile alpha partials
 constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status word + counters
 
@@ -145,8 +145,8 @@ inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     s.sent = o;     o = align_up(o + rows * 8);                       // segment entry states / adjoints
     s.kpart = o;    o = align_up(o + BL * g.n_groups * 8);            // per-token controller partials
     s.numod = o;    o = align_up(o + rows * 8);                       // per-segment (dnu, dtheta)
-    s.dwh_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 2 * 2 * (D + 1) * 4);   // (cta, half) rows
-    s.amp_part = o; o = align_up(o + (size_t)kCtrlBwdCtas * 8);
+    s.dwh_part = o; o = align_up(o + (size_t)kCtrlRowsMax * 2 * (D + 1) * 4);   // one row per CTA
+    s.amp_part = o; o = align_up(o + (size_t)kCtrlRowsMax * 8);
     s.dwh = o;      o = align_up(o + (size_t)2 * (D + 1) * 4);                 // column sums
     s.total = o;
     return s;

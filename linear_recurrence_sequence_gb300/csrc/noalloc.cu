@@ -104,6 +104,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     cf.wh = wh;
     cf.misc = misc;
     cf.modes = modes;
+    cf.status = reinterpret_cast<uint32_t*>(scratch + sc.status);
     if (launch_samu_ctrl_fwd(cf, stream, false) != cudaSuccess) return LRS_ERR_CUDA;
 
     CUtensorMap tm_w, tm_ctrl;

@@ -15,25 +15,96 @@
 namespace lrs {
 
 // ---------------------------------------------------------------------------
-// Controller forward, with the parameter preparation folded in.
+// Streaming layout shared by the controller forward and backward.
 //
-// Grid = n_mode CTAs followed by controller CTAs.
-//  - Mode CTAs (32 active threads each): the per-mode transition constant
-//    lbar_m = e^{-nu_m} e^{i theta_m} as a double-float (hi, lo) in FP64; they
-//    run alongside the streaming CTAs, off the critical path.
-//  - Controller CTAs: the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
-//    fixed-order tree, recomputed identically by every CTA); each thread then
-//    owns 8 consecutive channels with its 16 unit-direction weights in
-//    registers, and the CTA walks its token range in batches of 8 tokens: one
-//    16-byte load of x_sel per token per thread, 16 partial dot products per
-//    thread, a 16-shuffle reduce-scatter inside each warp, a fixed-order sum
-//    over the warps, and 8 threads evaluate p, r, q(r), d, c and the shared
-//    E - 1 = expm1(c), C = cos d, S = sin d for the 8 tokens in parallel.
-//    The first controller CTA stores w_hat and the amplitude factors for the
-//    backward.
+// Every streaming CTA owns a contiguous run of stages of cg.stage_tok tokens.
+// Warp 0 is the producer: lane 0 copies each stage's x_sel rows (contiguous
+// in memory) into a ring of cg.ring shared-memory slots with one 1-D bulk
+// copy, and the warp does the per-token scalar work.  Warps 1..C are the
+// consumers: thread (warp, lane) owns channels 8v .. 8v+7, v = 32 (warp-1) +
+// lane, with its unit-direction weights in registers.
+//
+// Shared memory: ring[slot][token][D] BF16 | per-slot exchange buffer |
+// mbarriers.
 // ---------------------------------------------------------------------------
-constexpr int kCfTok = 8;              // tokens per batch
-constexpr int kModeThreads = 32;       // active threads of a mode CTA
+constexpr int kCtrlRingMax = 8;                 // ring slots (at most)
+constexpr int kCtrlRingBytes = 192 * 1024;      // shared memory for the ring
+constexpr int kCtrlMaxThreads = 32 * (1 + 16);   // D = 4096: 16 consumer warps
+constexpr int kModeThreads = 32;    // active threads of a mode CTA
+
+struct CtrlSmem {
+    uint8_t* ring;
+    float* xbuf;        // forward: partial dots [slot][consumer][32]; backward: float2 scalars [slot][token]
+    uint64_t* full;     // x rows landed (producer arrival + bytes)
+    uint64_t* ready;    // forward: partials written (consumers); backward: scalars written (producer)
+    uint64_t* empty;    // backward: slot consumed (consumers)
+};
+
+__host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D) {
+    return (size_t)cg.ring * cg.stage_tok * 2 * D;
+}
+
+__host__ __device__ inline size_t ctrl_xbuf_bytes(const CtrlGeom& cg, bool backward) {
+    return backward ? (size_t)cg.ring * cg.stage_tok * 8 : (size_t)cg.ring * cg.consumers * 32 * 4;
+}
+
+__device__ __forceinline__ CtrlSmem ctrl_smem(uint8_t* base, const CtrlGeom& cg, int D, bool backward) {
+    CtrlSmem sm;
+    sm.ring = base;
+    const size_t rb = ctrl_ring_bytes(cg, D);
+    sm.xbuf = reinterpret_cast<float*>(base + rb);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + rb + ((ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15)));
+    sm.full = bars;
+    sm.ready = bars + cg.ring;
+    sm.empty = bars + 2 * cg.ring;
+    return sm;
+}
+
+// Stages [s0, s1) of the streaming CTA `cta`.
+__device__ __forceinline__ void ctrl_stage_range(const CtrlGeom& cg, int cta, long long& s0, long long& s1) {
+    s0 = cg.n_stages * cta / cg.n_ctas;
+    s1 = cg.n_stages * (cta + 1) / cg.n_ctas;
+}
+
+// Producer lane 0: the rows of stage (token t0, n tokens) into ring slot `slot`.
+__device__ __forceinline__ void ctrl_issue(const CtrlSmem& sm, int slot, const uint4* x, long long t0, int n, int D,
+                                           const CtrlGeom& cg) {
+    const uint32_t bytes = (uint32_t)n * 2u * (uint32_t)D;
+    uint8_t* dst = sm.ring + (size_t)slot * cg.stage_tok * 2 * D;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&sm.full[slot], bytes);
+    bulk_load(dst, reinterpret_cast<const uint8_t*>(x) + (size_t)t0 * 2 * D, bytes, &sm.full[slot]);
+}
+
+// Sums v[k] over the 32 lanes for every k at once (V = 16 or 32 values):
+// on return lane L holds the total of v[L mod V].  Fixed order.
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
+#pragma unroll
+    for (int o = 16; o >= V; o >>= 1) {   // plain butterfly while there are fewer values than lanes
+#pragma unroll
+        for (int k = 0; k < V; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    }
+#pragma unroll
+    for (int o = V / 2; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < o; ++k) {
+            const float send = up ? v[k] : v[k + o];
+            const float keep = up ? v[k + o] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ void unpack8(const uint4 q, float (&x)[8]) {
+    float2 f;
+    f = bf2_to_f2(q.x); x[0] = f.x; x[1] = f.y;
+    f = bf2_to_f2(q.y); x[2] = f.x; x[3] = f.y;
+    f = bf2_to_f2(q.z); x[4] = f.x; x[5] = f.y;
+    f = bf2_to_f2(q.w); x[6] = f.x; x[7] = f.y;
+}
 
 __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, const float* __restrict__ theta,
                                                int M, float4* __restrict__ modes, int m) {
@@ -46,9 +117,107 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
     modes[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
 }
 
-__global__ void __launch_bounds__(512) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
-    __shared__ float s_red[2][512 / 32];
-    __shared__ float s_part[512 / 32][2 * kCfTok];
+// ---------------------------------------------------------------------------
+// Controller forward, with the parameter preparation folded in.
+//  - Mode CTAs (the first n_mode_ctas, 32 active threads each): the per-mode
+//    transition constant lbar_m = e^{-nu_m} e^{i theta_m} as a double-float
+//    (hi, lo) in FP64.
+//  - Streaming CTAs: the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
+//    fixed-order tree, the same in every CTA); consumers form their 16 partial
+//    dot products per token, reduce-scatter them over the warp and leave one
+//    (token, phi or r) partial per lane; the producer adds the consumers'
+//    partials in a fixed order and evaluates p = tanh(s_phi), r = tanh(s_r),
+//    q(r), d, c, and E - 1 = expm1(c), C = cos d, S = sin d, 16 tokens per
+//    stage in parallel.  The first streaming CTA stores w_hat and the
+//    amplitude factors for the backward.
+// ---------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void ctrl_fwd_consumer(const SamuCtrlFwdArgs& a, const CtrlSmem& sm, long long s0,
+                                                  long long s1, int cw, int lane, const float (&wp)[8],
+                                                  const float (&wr)[8], bool col_ok) {
+    const CtrlGeom& cg = a.cg;
+    const int D = a.D;
+    const int v_idx = 32 * cw + lane;
+    for (long long st = s0; st < s1; ++st) {
+        const int k = (int)(st - s0);
+        const int slot = k % cg.ring;
+        const long long t0 = st * N;
+        const int n = (int)min((long long)N, a.BL - t0);
+        if (!mbar_wait_bounded(&sm.full[slot], (uint32_t)(k / cg.ring) & 1u)) {
+            if (lane == 0) atomicOr(a.status, kStatusTimeout);
+            return;
+        }
+        const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
+        float v[2 * N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            float ap = 0.f, ar = 0.f;
+            if (col_ok && i < n) {
+                float x[8];
+                unpack8(rows[(size_t)i * (D / 8) + v_idx], x);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    ap = fmaf(x[c], wp[c], ap);
+                    ar = fmaf(x[c], wr[c], ar);
+                }
+            }
+            v[2 * i] = ap;
+            v[2 * i + 1] = ar;
+        }
+        const float tot = warp_reduce_scatter<2 * N>(v, lane);
+        sm.xbuf[((size_t)slot * cg.consumers + cw) * 32 + lane] = tot;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ready[slot]);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, const CtrlSmem& sm, long long s0,
+                                                  long long s1, int lane, float bias_p, float bias_r, float k_phi,
+                                                  float k_r) {
+    const CtrlGeom& cg = a.cg;
+    const int D = a.D;
+    constexpr int V = 2 * N;
+    if (lane == 0)
+        for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st)
+            ctrl_issue(sm, (int)(st - s0), a.x, st * N, (int)min((long long)N, a.BL - st * N), D, cg);
+    for (long long st = s0; st < s1; ++st) {
+        const int k = (int)(st - s0);
+        const int slot = k % cg.ring;
+        const long long t0 = st * N;
+        const int n = (int)min((long long)N, a.BL - t0);
+        if (!mbar_wait_bounded(&sm.ready[slot], (uint32_t)(k / cg.ring) & 1u)) {
+            if (lane == 0) atomicOr(a.status, kStatusTimeout);
+            return;
+        }
+        float tot = 0.f;
+        for (int c = 0; c < cg.consumers; ++c) tot += sm.xbuf[((size_t)slot * cg.consumers + c) * 32 + (lane & (V - 1))];
+        __syncwarp();
+        const long long nxt = st + cg.ring;
+        if (lane == 0 && nxt < s1) ctrl_issue(sm, slot, a.x, nxt * N, (int)min((long long)N, a.BL - nxt * N), D, cg);
+        const float s_phi = __shfl_sync(0xffffffffu, tot, lane & ~1);
+        const float s_r = __shfl_sync(0xffffffffu, tot, lane | 1);
+        const int i = lane >> 1;
+        if ((lane & 1) == 0 && lane < V && i < n) {
+            const long long t = t0 + i;
+            const float p = tanhf(s_phi + bias_p);
+            const float r = tanhf(s_r + bias_r);
+            const float qr = r / (1.0f + r * r);
+            const float d = k_phi * p;
+            const float c = k_r * qr;
+            float sn, cs;
+            sincosf(d, &sn, &cs);
+            const float rs = (a.reset != nullptr && a.reset[t] != 0) ? 1.0f : 0.0f;
+            a.p[t] = p;
+            a.r[t] = r;
+            a.ctrl[t] = make_float4(expm1f(c), cs, sn, rs);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ float s_red[2][kCtrlMaxThreads / 32];
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x;
@@ -59,10 +228,18 @@ __global__ void __launch_bounds__(512) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
         return;
     }
     const int cta = blockIdx.x - a.n_mode_ctas;
+    const CtrlGeom& cg = a.cg;
     const int n = D + 1;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
+    const CtrlSmem sm = ctrl_smem(smem_raw, cg, D, false);
+    if (tid == 0) {
+        for (int i = 0; i < cg.ring; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.ready[i], cg.consumers);
+        }
+    }
 
     // norms (FP32, fixed order: per-thread strided sum, warp tree, warp-order sum)
     float sp = 0.f, sr = 0.f;
@@ -91,15 +268,6 @@ __global__ void __launch_bounds__(512) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
     const float ta = tanhf(a.a_phi[0]), tra = tanhf(a.a_r[0]);
     const float ism = 1.0f / sqrtf((float)M);
     const float k_phi = ta * ism, k_r = tra * ism;
-    const int vecs = D / 8;
-    const bool col_ok = tid < vecs;
-    float wp[8], wr[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        wp[k] = col_ok ? a.w_phi[8 * tid + k] * inv_phi : 0.f;
-        wr[k] = col_ok ? a.w_r[8 * tid + k] * inv_r : 0.f;
-    }
-    const float bias_p = a.w_phi[D] * inv_phi, bias_r = a.w_r[D] * inv_r;
     if (cta == 0) {
         for (int j = tid; j < n; j += blockDim.x) {
             a.wh[j] = a.w_phi[j] * inv_phi;
@@ -115,243 +283,201 @@ __global__ void __launch_bounds__(512) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
             a.misc[6] = ism;
         }
     }
-
-    const long long BL = a.BL;
-    const long long per = (BL + a.n_tok_ctas - 1) / a.n_tok_ctas;
-    const long long tb = (long long)cta * per;
-    const long long te = min(BL, tb + per);
-    for (long long t0 = tb; t0 < te; t0 += kCfTok) {
-        uint4 q[kCfTok];
+    long long s0, s1;
+    ctrl_stage_range(cg, cta, s0, s1);
+    if (warp == 0) {
+        const float bias_p = a.w_phi[D] * inv_phi, bias_r = a.w_r[D] * inv_r;
+        if (cg.stage_tok == 16)
+            ctrl_fwd_producer<16>(a, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
+        else
+            ctrl_fwd_producer<8>(a, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
+    } else {
+        const int v_idx = 32 * (warp - 1) + lane;
+        const bool col_ok = v_idx < D / 8;
+        float wp[8], wr[8];
 #pragma unroll
-        for (int u = 0; u < kCfTok; ++u)
-            q[u] = (col_ok && t0 + u < te) ? __ldcs(a.x + (t0 + u) * vecs + tid) : make_uint4(0u, 0u, 0u, 0u);
-        float v[2 * kCfTok];   // v[2u] = phi partial of token u, v[2u+1] = r partial
-#pragma unroll
-        for (int u = 0; u < kCfTok; ++u) {
-            float2 f;
-            float ap = 0.f, ar = 0.f;
-            f = bf2_to_f2(q[u].x); ap = fmaf(f.x, wp[0], ap); ap = fmaf(f.y, wp[1], ap); ar = fmaf(f.x, wr[0], ar); ar = fmaf(f.y, wr[1], ar);
-            f = bf2_to_f2(q[u].y); ap = fmaf(f.x, wp[2], ap); ap = fmaf(f.y, wp[3], ap); ar = fmaf(f.x, wr[2], ar); ar = fmaf(f.y, wr[3], ar);
-            f = bf2_to_f2(q[u].z); ap = fmaf(f.x, wp[4], ap); ap = fmaf(f.y, wp[5], ap); ar = fmaf(f.x, wr[4], ar); ar = fmaf(f.y, wr[5], ar);
-            f = bf2_to_f2(q[u].w); ap = fmaf(f.x, wp[6], ap); ap = fmaf(f.y, wp[7], ap); ar = fmaf(f.x, wr[6], ar); ar = fmaf(f.y, wr[7], ar);
-            v[2 * u] = ap;
-            v[2 * u + 1] = ar;
+        for (int c = 0; c < 8; ++c) {
+            wp[c] = col_ok ? a.w_phi[8 * v_idx + c] * inv_phi : 0.f;
+            wr[c] = col_ok ? a.w_r[8 * v_idx + c] * inv_r : 0.f;
         }
-        // reduce-scatter of 16 values over the warp: after it, lanes 2i and
-        // 2i+1 both hold the warp sum of value sel(i)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const bool hi = lane & 16;
-            const float send = hi ? v[k] : v[k + 8];
-            const float keep = hi ? v[k + 8] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const bool hi = lane & 8;
-            const float send = hi ? v[k] : v[k + 4];
-            const float keep = hi ? v[k + 4] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const bool hi = lane & 4;
-            const float send = hi ? v[k] : v[k + 2];
-            const float keep = hi ? v[k + 2] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        {
-            const bool hi = lane & 2;
-            const float send = hi ? v[0] : v[1];
-            const float keep = hi ? v[1] : v[0];
-            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-        if ((lane & 1) == 0) {
-            const int sel = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-            s_part[warp][sel] = v[0];
-        }
-        __syncthreads();
-        if (tid < kCfTok && t0 + tid < te) {
-            const long long t = t0 + tid;
-            float s_phi = 0.f, s_r = 0.f;
-            for (int w = 0; w < nwarps; ++w) {
-                s_phi += s_part[w][2 * tid];
-                s_r += s_part[w][2 * tid + 1];
-            }
-            const float p = tanhf(s_phi + bias_p);
-            const float r = tanhf(s_r + bias_r);
-            const float qr = r / (1.0f + r * r);
-            const float d = k_phi * p;
-            const float c = k_r * qr;
-            float sn, cs;
-            sincosf(d, &sn, &cs);
-            const float rs = (a.reset != nullptr && a.reset[t] != 0) ? 1.0f : 0.0f;
-            a.p[t] = p;
-            a.r[t] = r;
-            a.ctrl[t] = make_float4(expm1f(c), cs, sn, rs);
-        }
-        __syncthreads();
+        if (cg.stage_tok == 16)
+            ctrl_fwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, wp, wr, col_ok);
+        else
+            ctrl_fwd_consumer<8>(a, sm, s0, s1, warp - 1, lane, wp, wr, col_ok);
     }
 }
 
 // ---------------------------------------------------------------------------
-// Controller backward.  A fixed grid of kCtrlBwdCtas CTAs, each owning a
-// contiguous token range, processed in blocks of kCbTokBlock tokens; the CTA
-// is two halves, each half owning one half of every block, and within a half
-// each thread owns 8 consecutive channels.
-// Per token:  dbar = sum_slices Im-kappa partials, cbar = E * sum_slices
-// (-nu Re kappa) partials (E = e^c);  pbar = dbar tanh(a_phi)/sqrt(M);
+// Controller backward.  Per token (producer):  dbar = sum over the mode groups
+// of the Im-kappa partials, cbar = E * sum of the (-nu Re kappa) partials
+// (E = e^c);  pbar = dbar tanh(a_phi)/sqrt(M);
 // rbar = cbar tanh(a_r)/sqrt(M) (1 - r^2)/(1 + r^2)^2;  through tanh:
-// sbar_phi = pbar (1 - p^2), sbar_r = rbar (1 - r^2);
-// dx_sel = sbar_phi w_hat_phi[:D] + sbar_r w_hat_r[:D];
-// dw_hat += sbar x~ (per-half partial rows, bias column included);
-// amplitude partials sum dbar p and sum cbar q(r).
+// sbar_phi = pbar (1 - p^2), sbar_r = rbar (1 - r^2); the bias column and
+// the amplitude partials sum dbar p and sum cbar q(r) in the producer lanes.
+// Per token and channel (consumers): dx_sel = sbar_phi w_hat_phi[:D] +
+// sbar_r w_hat_r[:D]; dw_hat += sbar x~.  One partial row per CTA.
 // ---------------------------------------------------------------------------
-constexpr int kCbTokBlock = 128;
-constexpr int kCbUnroll = 2;
-
-__global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
-    __shared__ float s_sphi[kCbTokBlock];
-    __shared__ float s_sr[kCbTokBlock];
-    __shared__ float s_red[4][kCbTokBlock];
-    pdl_trigger();
-    pdl_wait();
-    const int tid = threadIdx.x;
+template <int N>
+__device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
+                                                  long long s1, int lane, int cta) {
+    const CtrlGeom& cg = a.cg;
     const int D = a.D;
-    const int vecs = D / 8;
-    const int cols = max((vecs + 31) / 32 * 32, kCbTokBlock / 2);   // threads per half
-    const int halves = blockDim.x / cols;                           // 1 or 2
-    const int half = tid / cols;
-    const int col = tid - half * cols;
-    const long long BL = (long long)a.B * a.L;
-    const long long per = (BL + kCtrlBwdCtas - 1) / kCtrlBwdCtas;
-    const long long tb = (long long)blockIdx.x * per;
-    const long long te = min(BL, tb + per);
     const float k_phi = a.misc[0];
     const float k_r = a.misc[1];
-    const bool col_ok = col < vecs;
+    float bias_p = 0.f, bias_r = 0.f, amp_p = 0.f, amp_r = 0.f;
+    float2* sc = reinterpret_cast<float2*>(sm.xbuf);
+    for (long long st = s0; st < s1; ++st) {
+        const int k = (int)(st - s0);
+        const int slot = k % cg.ring;
+        const long long t0 = st * N;
+        const int n = (int)min((long long)N, a.BL - t0);
+        if (k >= cg.ring && !mbar_wait_bounded(&sm.empty[slot], (uint32_t)(k / cg.ring - 1) & 1u)) {
+            if (lane == 0) atomicOr(a.status, kStatusTimeout);
+            return;
+        }
+        if (lane == 0) ctrl_issue(sm, slot, a.x, t0, n, D, cg);
+        if (lane < N) {
+            float2 s = make_float2(0.f, 0.f);
+            if (lane < n) {
+                const long long t = t0 + lane;
+                const float2* kp = a.kpart + t * a.n_groups;
+                float dbar = 0.f, ebar = 0.f;
+                for (int g = 0; g < a.n_groups; ++g) {
+                    const float2 v = __ldcs(kp + g);
+                    dbar += v.x;
+                    ebar += v.y;
+                }
+                const float E = 1.0f + a.ctrl[t].x;   // ctrl.x holds E - 1
+                const float p = a.p[t];
+                const float r = a.r[t];
+                const float cbar = ebar * E;
+                const float opr = 1.0f + r * r;
+                const float pbar = dbar * k_phi;
+                const float rbar = cbar * k_r * (1.0f - r * r) / (opr * opr);
+                s = make_float2(pbar * (1.0f - p * p), rbar * (1.0f - r * r));
+                bias_p += s.x;
+                bias_r += s.y;
+                amp_p = fmaf(dbar, p, amp_p);
+                amp_r = fmaf(cbar, r / opr, amp_r);
+            }
+            sc[(size_t)slot * N + lane] = s;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ready[slot]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bias_p += __shfl_xor_sync(0xffffffffu, bias_p, o);
+        bias_r += __shfl_xor_sync(0xffffffffu, bias_r, o);
+        amp_p += __shfl_xor_sync(0xffffffffu, amp_p, o);
+        amp_r += __shfl_xor_sync(0xffffffffu, amp_r, o);
+    }
+    if (lane == 0) {
+        float* row = a.dwh_part + (size_t)cta * 2 * (D + 1);
+        row[D] = bias_p;
+        row[(D + 1) + D] = bias_r;
+        a.amp_part[cta] = make_float2(amp_p, amp_r);
+    }
+}
 
+template <int N>
+__device__ __forceinline__ void ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
+                                                  long long s1, int cw, int lane, int cta) {
+    const CtrlGeom& cg = a.cg;
+    const int D = a.D;
+    const int vecs = D / 8;
+    const int v_idx = 32 * cw + lane;
+    const bool col_ok = v_idx < vecs;
     float wp[8], wr[8], accp[8], accr[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        wp[k] = col_ok ? a.wh[8 * col + k] : 0.f;
-        wr[k] = col_ok ? a.wh[(D + 1) + 8 * col + k] : 0.f;
-        accp[k] = 0.f;
-        accr[k] = 0.f;
+    for (int c = 0; c < 8; ++c) {
+        wp[c] = col_ok ? a.wh[8 * v_idx + c] : 0.f;
+        wr[c] = col_ok ? a.wh[(D + 1) + 8 * v_idx + c] : 0.f;
+        accp[c] = 0.f;
+        accr[c] = 0.f;
     }
-    float bias_p = 0.f, bias_r = 0.f, amp_p = 0.f, amp_r = 0.f;   // threads < kCbTokBlock
-
-    for (long long blk = tb; blk < te; blk += kCbTokBlock) {
-        const int nb = (int)min((long long)kCbTokBlock, te - blk);
-        if (tid < nb) {
-            const long long t = blk + tid;
-            const float2* kp = a.kpart + t * a.n_groups;
-            float dbar = 0.f, ebar = 0.f;
-            for (int s2 = 0; s2 < a.n_groups; ++s2) {
-                const float2 v = kp[s2];
-                dbar += v.x;
-                ebar += v.y;
-            }
-            const float E = 1.0f + a.ctrl[t].x;   // ctrl.x holds E - 1
-            const float p = a.p[t];
-            const float r = a.r[t];
-            const float cbar = ebar * E;
-            const float opr = 1.0f + r * r;
-            const float pbar = dbar * k_phi;
-            const float rbar = cbar * k_r * (1.0f - r * r) / (opr * opr);
-            const float sp = pbar * (1.0f - p * p);
-            const float sr = rbar * (1.0f - r * r);
-            s_sphi[tid] = sp;
-            s_sr[tid] = sr;
-            bias_p += sp;
-            bias_r += sr;
-            amp_p = fmaf(dbar, p, amp_p);
-            amp_r = fmaf(cbar, r / opr, amp_r);
+    const float2* sc = reinterpret_cast<const float2*>(sm.xbuf);
+    for (long long st = s0; st < s1; ++st) {
+        const int k = (int)(st - s0);
+        const int slot = k % cg.ring;
+        const long long t0 = st * N;
+        const int n = (int)min((long long)N, a.BL - t0);
+        const uint32_t par = (uint32_t)(k / cg.ring) & 1u;
+        if (!mbar_wait_bounded(&sm.full[slot], par) || !mbar_wait_bounded(&sm.ready[slot], par)) {
+            if (lane == 0) atomicOr(a.status, kStatusTimeout);
+            return;
         }
-        __syncthreads();
-        const int h0 = halves == 2 ? (nb + 1) / 2 : nb;
-        const int i0 = half == 0 ? 0 : h0;
-        const int i1 = half == 0 ? h0 : nb;
         if (col_ok) {
-            for (int i = i0; i < i1; i += kCbUnroll) {
-                uint4 q[kCbUnroll];
+            const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
+#pragma unroll 4
+            for (int i = 0; i < n; ++i) {
+                float x[8];
+                unpack8(rows[(size_t)i * vecs + v_idx], x);
+                const float2 s = sc[(size_t)slot * N + i];
+                float dx[8];
 #pragma unroll
-                for (int u = 0; u < kCbUnroll; ++u)
-                    q[u] = (i + u < i1) ? __ldcs(a.x + (blk + i + u) * vecs + col) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int u = 0; u < kCbUnroll; ++u) {
-                    if (i + u < i1) {
-                        const long long t = blk + i + u;
-                        const float sp = s_sphi[i + u];
-                        const float sr = s_sr[i + u];
-                        float xv[8];
-                        float2 f;
-                        f = bf2_to_f2(q[u].x); xv[0] = f.x; xv[1] = f.y;
-                        f = bf2_to_f2(q[u].y); xv[2] = f.x; xv[3] = f.y;
-                        f = bf2_to_f2(q[u].z); xv[4] = f.x; xv[5] = f.y;
-                        f = bf2_to_f2(q[u].w); xv[6] = f.x; xv[7] = f.y;
-                        float dx[8];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            dx[k] = fmaf(sp, wp[k], sr * wr[k]);
-                            accp[k] = fmaf(sp, xv[k], accp[k]);
-                            accr[k] = fmaf(sr, xv[k], accr[k]);
-                        }
-                        if (a.grad_fp32) {
-                            float4* o = reinterpret_cast<float4*>(a.dx) + (t * vecs + col) * 2;
-                            __stcs(o, make_float4(dx[0], dx[1], dx[2], dx[3]));
-                            __stcs(o + 1, make_float4(dx[4], dx[5], dx[6], dx[7]));
-                        } else {
-                            uint4 o;
-                            o.x = f2_to_bf2(dx[0], dx[1]);
-                            o.y = f2_to_bf2(dx[2], dx[3]);
-                            o.z = f2_to_bf2(dx[4], dx[5]);
-                            o.w = f2_to_bf2(dx[6], dx[7]);
-                            __stcs(reinterpret_cast<uint4*>(a.dx) + t * vecs + col, o);
-                        }
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    dx[c] = fmaf(s.x, wp[c], s.y * wr[c]);
+                    accp[c] = fmaf(s.x, x[c], accp[c]);
+                    accr[c] = fmaf(s.y, x[c], accr[c]);
+                }
+                const long long t = t0 + i;
+                if (a.grad_fp32) {
+                    float4* o = reinterpret_cast<float4*>(a.dx) + (t * vecs + v_idx) * 2;
+                    __stcs(o, make_float4(dx[0], dx[1], dx[2], dx[3]));
+                    __stcs(o + 1, make_float4(dx[4], dx[5], dx[6], dx[7]));
+                } else {
+                    uint4 o;
+                    o.x = f2_to_bf2(dx[0], dx[1]);
+                    o.y = f2_to_bf2(dx[2], dx[3]);
+                    o.z = f2_to_bf2(dx[4], dx[5]);
+                    o.w = f2_to_bf2(dx[6], dx[7]);
+                    __stcs(reinterpret_cast<uint4*>(a.dx) + t * vecs + v_idx, o);
                 }
             }
         }
-        __syncthreads();
-    }
-    // partial rows: (cta, half); a single-half CTA leaves its second row zero
-    float* part = a.dwh_part + ((size_t)blockIdx.x * 2 + half) * 2 * (D + 1);
-    if (halves == 1) {
-        float* other = a.dwh_part + ((size_t)blockIdx.x * 2 + 1) * 2 * (D + 1);
-        for (int j = tid; j < 2 * (D + 1); j += blockDim.x) other[j] = 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
     if (col_ok) {
+        float* row = a.dwh_part + (size_t)cta * 2 * (D + 1);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            part[8 * col + k] = accp[k];
-            part[(D + 1) + 8 * col + k] = accr[k];
+        for (int c = 0; c < 8; ++c) {
+            row[8 * v_idx + c] = accp[c];
+            row[(D + 1) + 8 * v_idx + c] = accr[c];
         }
     }
-    // fixed-order tree over the token-scalar threads for the bias column and amplitudes
-    if (tid < kCbTokBlock) {
-        s_red[0][tid] = bias_p;
-        s_red[1][tid] = bias_r;
-        s_red[2][tid] = amp_p;
-        s_red[3][tid] = amp_r;
+}
+
+__global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const CtrlGeom& cg = a.cg;
+    const CtrlSmem sm = ctrl_smem(smem_raw, cg, a.D, true);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < cg.ring; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.ready[i], 1);
+            mbar_init(&sm.empty[i], cg.consumers);
+        }
     }
     __syncthreads();
-    for (int s2 = kCbTokBlock / 2; s2 > 0; s2 >>= 1) {
-        if (tid < s2) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) s_red[q][tid] += s_red[q][tid + s2];
-        }
-        __syncthreads();
-    }
-    if (tid == 0) {
-        float* p0 = a.dwh_part + (size_t)blockIdx.x * 2 * 2 * (D + 1);          // half-0 row
-        float* p1 = p0 + 2 * (D + 1);                                           // half-1 row
-        p0[D] = s_red[0][0];
-        p0[(D + 1) + D] = s_red[1][0];
-        p1[D] = 0.f;
-        p1[(D + 1) + D] = 0.f;
-        a.amp_part[blockIdx.x] = make_float2(s_red[2][0], s_red[3][0]);
+    long long s0, s1;
+    ctrl_stage_range(cg, cta, s0, s1);
+    if (warp == 0) {
+        if (cg.stage_tok == 16)
+            ctrl_bwd_producer<16>(a, sm, s0, s1, lane, cta);
+        else
+            ctrl_bwd_producer<8>(a, sm, s0, s1, lane, cta);
+    } else {
+        if (cg.stage_tok == 16)
+            ctrl_bwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, cta);
+        else
+            ctrl_bwd_consumer<8>(a, sm, s0, s1, warp - 1, lane, cta);
     }
 }
 
@@ -360,7 +486,8 @@ __global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a
 //  - CTAs [0, ceil(M/32)): 32 modes each; warp w sums the per-segment
 //    (dnu, dtheta) rows w, w+32, ...; the 32 warp sums are added in order;
 //  - the next 2*ceil((D+1)/32) CTAs: 32 columns of dw_hat_phi or dw_hat_r
-//    each, summed the same way over the controller-backward partial rows;
+//    each, summed the same way over the controller-backward partial rows
+//    (one per controller-backward CTA);
 //  - the CTA that arrives last (threadfence + counter) computes the
 //    unit-direction projection dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||
 //    and the amplitude gradients da = (sum of partials) / sqrt(M) (1 - tanh(a)^2),
@@ -368,7 +495,6 @@ __global__ void __launch_bounds__(512, 2) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a
 // ---------------------------------------------------------------------------
 constexpr int kParamWarps = 32;
 constexpr int kParamThreads = kParamWarps * 32;
-constexpr int kColRows = 2 * kCtrlBwdCtas;   // (CTA, token half) partial rows
 
 // Block-wide sum of four values, fixed order; every thread gets the totals.
 __device__ __forceinline__ float4 block_sum4(float4 v, float4 (*s_w)[1]) {
@@ -445,14 +571,14 @@ __global__ void __launch_bounds__(kParamThreads) samu_params_kernel(SamuParamArg
         float sum = 0.f;
         if (j < n) {
             int r = warp;
-            for (; r + 3 * kParamWarps < kColRows; r += 4 * kParamWarps) {
+            for (; r + 3 * kParamWarps < a.n_rows; r += 4 * kParamWarps) {
                 float v[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) v[q] = __ldcg(a.dwh_part + ((size_t)(r + q * kParamWarps) * 2 + which) * n + j);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) sum += v[q];
             }
-            for (; r < kColRows; r += kParamWarps) sum += __ldcg(a.dwh_part + ((size_t)r * 2 + which) * n + j);
+            for (; r < a.n_rows; r += kParamWarps) sum += __ldcg(a.dwh_part + ((size_t)r * 2 + which) * n + j);
         }
         s_red[warp][lane].x = sum;
         __syncthreads();
@@ -475,7 +601,7 @@ __global__ void __launch_bounds__(kParamThreads) samu_params_kernel(SamuParamArg
         v.x = fmaf(a.wh[j], __ldcg(a.dwh + j), v.x);
         v.y = fmaf(a.wh[n + j], __ldcg(a.dwh + n + j), v.y);
     }
-    for (int k = threadIdx.x; k < kCtrlBwdCtas; k += kParamThreads) {
+    for (int k = threadIdx.x; k < a.n_rows; k += kParamThreads) {
         const float2 u = __ldcg(a.amp_part + k);
         v.z += u.x;
         v.w += u.y;
@@ -495,22 +621,71 @@ __global__ void __launch_bounds__(kParamThreads) samu_params_kernel(SamuParamArg
     }
 }
 
+namespace {
+
+struct CtrlOcc {
+    bool done = false;
+    int sms = 0;
+};
+CtrlOcc g_ctrl_occ[64];
+
+int ctrl_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    CtrlOcc& o = g_ctrl_occ[dev];
+    if (!o.done) {
+        int v = 0;
+        o.sms = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;
+        o.done = true;
+    }
+    return o.sms;
+}
+
+}  // namespace
+
+CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
+    CtrlGeom cg;
+    // stages of 16 tokens (8 when 16 rows exceed 64 KB), as many slots as fit
+    // in kCtrlRingBytes
+    cg.stage_tok = 2 * D * 16 <= 64 * 1024 ? 16 : 8;
+    int ring = (int)(kCtrlRingBytes / ((size_t)cg.stage_tok * 2 * D));
+    if (ring > kCtrlRingMax) ring = kCtrlRingMax;
+    if (ring < 2) ring = 2;
+    cg.ring = ring;
+    cg.consumers = (D / 8 + 31) / 32;
+    if (cg.consumers < 1) cg.consumers = 1;
+    cg.threads = 32 * (1 + cg.consumers);
+    const size_t xb = (ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15);
+    cg.smem = (int)(ctrl_ring_bytes(cg, D) + xb + 3 * cg.ring * sizeof(uint64_t));
+    int per_sm = (int)((227 * 1024) / (cg.smem + 1024));
+    const int by_threads = 2048 / cg.threads;
+    if (per_sm > by_threads) per_sm = by_threads;
+    if (per_sm > 4) per_sm = 4;
+    if (per_sm < 1) per_sm = 1;
+    cg.n_stages = (BL + cg.stage_tok - 1) / cg.stage_tok;
+    long long ctas = (long long)ctrl_sms() * per_sm;
+    if (ctas > cg.n_stages) ctas = cg.n_stages;
+    if (ctas > kCtrlRowsMax) ctas = kCtrlRowsMax;
+    cg.n_ctas = (int)ctas;
+    return cg;
+}
+
 cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args_in, cudaStream_t s, bool pdl) {
     SamuCtrlFwdArgs a = args_in;
     const int M = a.D / 2;
-    int cols = ((a.D / 8) + 31) / 32 * 32;
-    if (cols < 64) cols = 64;
     a.n_mode_ctas = (M + kModeThreads - 1) / kModeThreads;
-    const long long want = (a.BL + kCfTok - 1) / kCfTok;
-    a.n_tok_ctas = (int)(want < 152LL * 4 ? want : 152LL * 4);
-    return launch_ex(samu_ctrl_fwd_kernel, a.n_mode_ctas + a.n_tok_ctas, cols, 0, s, pdl, a);
+    a.cg = samu_ctrl_geom(a.BL, a.D, false);
+    const cudaError_t e =
+        cudaFuncSetAttribute(samu_ctrl_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, a.cg.smem);
+    if (e != cudaSuccess) return e;
+    return launch_ex(samu_ctrl_fwd_kernel, a.n_mode_ctas + a.cg.n_ctas, a.cg.threads, (size_t)a.cg.smem, s, pdl, a);
 }
 
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl) {
-    int cols = ((args.D / 8) + 31) / 32 * 32;
-    if (cols < kCbTokBlock / 2) cols = kCbTokBlock / 2;
-    const int threads = 2 * cols <= 512 ? 2 * cols : cols;   // two token halves when they fit
-    return launch_ex(samu_ctrl_bwd_kernel, kCtrlBwdCtas, threads, 0, s, pdl, args);
+    const cudaError_t e =
+        cudaFuncSetAttribute(samu_ctrl_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, args.cg.smem);
+    if (e != cudaSuccess) return e;
+    return launch_ex(samu_ctrl_bwd_kernel, args.cg.n_ctas, args.cg.threads, (size_t)args.cg.smem, s, pdl, args);
 }
 
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl) {

@@ -259,9 +259,11 @@ int samu_backward(const void* dy, const float* dhT,
     const int fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
 
     const float4* ctrl = at<float4>(saved, sv.ctrl);
-    CUtensorMap tm_dy, tm_w, tm_ctrl;
-    if (!make_bf16_map(&tm_dy, dy, B, L, D, kSub) || !make_bf16_map(&tm_w, w, B, L, D, kSub) ||
-        !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub))
+    // 16-row boxes for the adjoint maps, 8-row boxes for the reverse replay
+    CUtensorMap tm_dy, tm_ctrl, tm_dy8, tm_w8, tm_ctrl8;
+    if (!make_bf16_map(&tm_dy, dy, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub) ||
+        !make_bf16_map(&tm_dy8, dy, B, L, D, kHalf) || !make_bf16_map(&tm_w8, w, B, L, D, kHalf) ||
+        !make_ctrl_map(&tm_ctrl8, ctrl, B, L, kHalf))
         return LRS_ERR_CUDA;
     SamuScanBwdArgs s;
     s.g = g;
@@ -279,7 +281,7 @@ int samu_backward(const void* dy, const float* dhT,
     s.status = at<uint32_t>(scratch, sc.status);
     LRS_LAUNCH(KID_SAMU_BWD_MAPS, stream, launch_samu_bwd_maps(tm_dy, tm_ctrl, s, stream, false));
     LRS_LAUNCH(KID_SAMU_BWD_PREFIX, stream, launch_samu_bwd_prefix(s, stream, pdl_ok()));
-    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy, tm_w, tm_ctrl, s, stream, pdl_ok()));
+    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy8, tm_w8, tm_ctrl8, s, stream, pdl_ok()));
 
     SamuCtrlBwdArgs cb;
     cb.BL = (long long)B * L;

@@ -127,6 +127,7 @@ struct CtrlGeom {
     int smem;               // dynamic shared memory bytes
     int n_ctas;             // streaming CTAs
     long long n_stages;     // ceil(B*L / stage_tok)
+    int max_cta_tok;        // tokens of the longest CTA range (backward scalar buffer)
 };
 
 CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward);
@@ -201,7 +202,8 @@ cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_
 cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
                                    cudaStream_t s, bool pdl);
-// Backward: maps (dy read forwards in time), prefix, main (backwards).
+// Backward: maps (dy read forwards in time, 16-row boxes), prefix, main
+// (backwards, 8-row boxes).
 cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
                                  cudaStream_t s, bool pdl);
 cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);

@@ -58,6 +58,7 @@ inline ScanGeom make_geom(int B, int L, int lanes, int tile) {
 // device can ask for: at least kSegMinTok tokens each and at most
 // kMaxSegWarps segments in all.
 constexpr int kSegMinTok = kSub;
+constexpr int kHalf = kSub / 2;     // tokens between SAMU state checkpoints
 constexpr long long kMaxSegWarps = 16384;
 
 struct SegGeom {
@@ -66,7 +67,7 @@ struct SegGeom {
     int seg;               // tokens per segment
     int NS;                // segments per chain
     int NSmax;             // bound on NS for this (B, L, M) on any device
-    int CS;                // entry-state slots per batch row (slot = t / 16)
+    int CS;                // state checkpoints per batch row (slot = t / 8)
 };
 
 inline int round_up16(long long v) { return (int)((v + kSub - 1) / kSub * kSub); }
@@ -97,7 +98,7 @@ inline SegGeom samu_seg_geom(int B, int L, int M, long long warps) {
     }
     g.seg = seg;
     g.NS = (L + seg - 1) / seg;
-    g.CS = (L + kSub - 1) / kSub + 1;
+    g.CS = (L + kHalf - 1) / kHalf + 1;
     return g;
 }
 
@@ -121,7 +122,7 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
     s.p = o;      o = align_up(o + BL * 4);                          // p_t
     s.r = o;      o = align_up(o + BL * 4);                          // r_t
     s.ctrl = o;   o = align_up(o + BL * 16);                         // {E-1, C, S, reset}
-    s.hsub = o;   o = align_up(o + (size_t)B * g.CS * M * 8);        // sub-chunk entry states
+    s.hsub = o;   o = align_up(o + (size_t)B * g.CS * M * 8);        // state every 8 tokens
     s.wh = o;     o = align_up(o + (size_t)2 * (D + 1) * 4);         // unit directions
     s.misc = o;   o = align_up(o + kMiscFloats * 4);
     s.modes = o;  o = align_up(o + (size_t)M * 16);                  // lbar hi/lo per mode

@@ -45,7 +45,7 @@ __host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D) {
 }
 
 __host__ __device__ inline size_t ctrl_xbuf_bytes(const CtrlGeom& cg, bool backward) {
-    return backward ? (size_t)cg.ring * cg.stage_tok * 8 : (size_t)cg.ring * cg.consumers * 32 * 4;
+    return backward ? (size_t)cg.max_cta_tok * 8 : (size_t)cg.ring * cg.consumers * 32 * 4;
 }
 
 __device__ __forceinline__ CtrlSmem ctrl_smem(uint8_t* base, const CtrlGeom& cg, int D, bool backward) {
@@ -308,75 +308,34 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrl
 }
 
 // ---------------------------------------------------------------------------
-// Controller backward.  Per token (producer):  dbar = sum over the mode groups
-// of the Im-kappa partials, cbar = E * sum of the (-nu Re kappa) partials
-// (E = e^c);  pbar = dbar tanh(a_phi)/sqrt(M);
-// rbar = cbar tanh(a_r)/sqrt(M) (1 - r^2)/(1 + r^2)^2;  through tanh:
-// sbar_phi = pbar (1 - p^2), sbar_r = rbar (1 - r^2); the bias column and
-// the amplitude partials sum dbar p and sum cbar q(r) in the producer lanes.
-// Per token and channel (consumers): dx_sel = sbar_phi w_hat_phi[:D] +
-// sbar_r w_hat_r[:D]; dw_hat += sbar x~.  One partial row per CTA.
+// Controller backward.  First, every thread of the CTA takes tokens of the
+// CTA's range in turn:  dbar = sum over the mode groups of the Im-kappa
+// partials, cbar = E * sum of the (-nu Re kappa) partials (E = e^c);
+// pbar = dbar tanh(a_phi)/sqrt(M); rbar = cbar tanh(a_r)/sqrt(M)
+// (1 - r^2)/(1 + r^2)^2; through tanh: sbar_phi = pbar (1 - p^2),
+// sbar_r = rbar (1 - r^2), kept in shared memory for the whole range; the
+// bias column (sum sbar) and the amplitude partials (sum dbar p,
+// sum cbar q(r)) are reduced over the CTA in a fixed order.  Then the
+// producer streams the x_sel rows and the consumers, per token and channel,
+// form dx_sel = sbar_phi w_hat_phi[:D] + sbar_r w_hat_r[:D] and accumulate
+// dw_hat += sbar x~.  One partial row per CTA.
 // ---------------------------------------------------------------------------
 template <int N>
 __device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
-                                                  long long s1, int lane, int cta) {
+                                                  long long s1, int lane) {
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
-    const float k_phi = a.misc[0];
-    const float k_r = a.misc[1];
-    float bias_p = 0.f, bias_r = 0.f, amp_p = 0.f, amp_r = 0.f;
-    float2* sc = reinterpret_cast<float2*>(sm.xbuf);
+    if (lane != 0) return;
     for (long long st = s0; st < s1; ++st) {
         const int k = (int)(st - s0);
         const int slot = k % cg.ring;
         const long long t0 = st * N;
         const int n = (int)min((long long)N, a.BL - t0);
         if (k >= cg.ring && !mbar_wait_bounded(&sm.empty[slot], (uint32_t)(k / cg.ring - 1) & 1u)) {
-            if (lane == 0) atomicOr(a.status, kStatusTimeout);
+            atomicOr(a.status, kStatusTimeout);
             return;
         }
-        if (lane == 0) ctrl_issue(sm, slot, a.x, t0, n, D, cg);
-        if (lane < N) {
-            float2 s = make_float2(0.f, 0.f);
-            if (lane < n) {
-                const long long t = t0 + lane;
-                const float2* kp = a.kpart + t * a.n_groups;
-                float dbar = 0.f, ebar = 0.f;
-                for (int g = 0; g < a.n_groups; ++g) {
-                    const float2 v = __ldcs(kp + g);
-                    dbar += v.x;
-                    ebar += v.y;
-                }
-                const float E = 1.0f + a.ctrl[t].x;   // ctrl.x holds E - 1
-                const float p = a.p[t];
-                const float r = a.r[t];
-                const float cbar = ebar * E;
-                const float opr = 1.0f + r * r;
-                const float pbar = dbar * k_phi;
-                const float rbar = cbar * k_r * (1.0f - r * r) / (opr * opr);
-                s = make_float2(pbar * (1.0f - p * p), rbar * (1.0f - r * r));
-                bias_p += s.x;
-                bias_r += s.y;
-                amp_p = fmaf(dbar, p, amp_p);
-                amp_r = fmaf(cbar, r / opr, amp_r);
-            }
-            sc[(size_t)slot * N + lane] = s;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ready[slot]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        bias_p += __shfl_xor_sync(0xffffffffu, bias_p, o);
-        bias_r += __shfl_xor_sync(0xffffffffu, bias_r, o);
-        amp_p += __shfl_xor_sync(0xffffffffu, amp_p, o);
-        amp_r += __shfl_xor_sync(0xffffffffu, amp_r, o);
-    }
-    if (lane == 0) {
-        float* row = a.dwh_part + (size_t)cta * 2 * (D + 1);
-        row[D] = bias_p;
-        row[(D + 1) + D] = bias_r;
-        a.amp_part[cta] = make_float2(amp_p, amp_r);
+        ctrl_issue(sm, slot, a.x, t0, n, D, cg);
     }
 }
 
@@ -402,18 +361,18 @@ __device__ __forceinline__ void ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, cons
         const int slot = k % cg.ring;
         const long long t0 = st * N;
         const int n = (int)min((long long)N, a.BL - t0);
-        const uint32_t par = (uint32_t)(k / cg.ring) & 1u;
-        if (!mbar_wait_bounded(&sm.full[slot], par) || !mbar_wait_bounded(&sm.ready[slot], par)) {
+        if (!mbar_wait_bounded(&sm.full[slot], (uint32_t)(k / cg.ring) & 1u)) {
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
             return;
         }
         if (col_ok) {
             const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
+            const float2* scs = sc + (size_t)k * N;
 #pragma unroll 4
             for (int i = 0; i < n; ++i) {
                 float x[8];
                 unpack8(rows[(size_t)i * vecs + v_idx], x);
-                const float2 s = sc[(size_t)slot * N + i];
+                const float2 s = scs[i];
                 float dx[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -451,28 +410,82 @@ __device__ __forceinline__ void ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, cons
 
 __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ float4 s_red[kCtrlMaxThreads / 32];
     pdl_trigger();
     pdl_wait();
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int cta = blockIdx.x;
     const CtrlGeom& cg = a.cg;
-    const CtrlSmem sm = ctrl_smem(smem_raw, cg, a.D, true);
-    if (threadIdx.x == 0) {
+    const int D = a.D;
+    const CtrlSmem sm = ctrl_smem(smem_raw, cg, D, true);
+    if (tid == 0) {
         for (int i = 0; i < cg.ring; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.ready[i], 1);
             mbar_init(&sm.empty[i], cg.consumers);
         }
     }
-    __syncthreads();
     long long s0, s1;
     ctrl_stage_range(cg, cta, s0, s1);
+    const long long tb = s0 * cg.stage_tok;
+    const long long te = min(a.BL, s1 * cg.stage_tok);
+
+    // per-token scalars of the whole range, and the bias / amplitude partials
+    const float k_phi = a.misc[0];
+    const float k_r = a.misc[1];
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);   // sum sbar_phi, sum sbar_r, sum dbar p, sum cbar q(r)
+    float2* sc = reinterpret_cast<float2*>(sm.xbuf);
+    for (long long t = tb + tid; t < te; t += blockDim.x) {
+        const float2* kp = a.kpart + t * a.n_groups;
+        float dbar = 0.f, ebar = 0.f;
+#pragma unroll 8
+        for (int g = 0; g < a.n_groups; ++g) {
+            const float2 v = __ldcs(kp + g);
+            dbar += v.x;
+            ebar += v.y;
+        }
+        const float E = 1.0f + a.ctrl[t].x;   // ctrl.x holds E - 1
+        const float p = a.p[t];
+        const float r = a.r[t];
+        const float cbar = ebar * E;
+        const float opr = 1.0f + r * r;
+        const float pbar = dbar * k_phi;
+        const float rbar = cbar * k_r * (1.0f - r * r) / (opr * opr);
+        const float2 s = make_float2(pbar * (1.0f - p * p), rbar * (1.0f - r * r));
+        sc[t - tb] = s;
+        part.x += s.x;
+        part.y += s.y;
+        part.z = fmaf(dbar, p, part.z);
+        part.w = fmaf(cbar, r / opr, part.w);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        part.x += __shfl_xor_sync(0xffffffffu, part.x, o);
+        part.y += __shfl_xor_sync(0xffffffffu, part.y, o);
+        part.z += __shfl_xor_sync(0xffffffffu, part.z, o);
+        part.w += __shfl_xor_sync(0xffffffffu, part.w, o);
+    }
+    if (lane == 0) s_red[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+        float4 t4 = s_red[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+            t4.x += s_red[w].x;
+            t4.y += s_red[w].y;
+            t4.z += s_red[w].z;
+            t4.w += s_red[w].w;
+        }
+        float* row = a.dwh_part + (size_t)cta * 2 * (D + 1);
+        row[D] = t4.x;
+        row[(D + 1) + D] = t4.y;
+        a.amp_part[cta] = make_float2(t4.z, t4.w);
+    }
     if (warp == 0) {
         if (cg.stage_tok == 16)
-            ctrl_bwd_producer<16>(a, sm, s0, s1, lane, cta);
+            ctrl_bwd_producer<16>(a, sm, s0, s1, lane);
         else
-            ctrl_bwd_producer<8>(a, sm, s0, s1, lane, cta);
+            ctrl_bwd_producer<8>(a, sm, s0, s1, lane);
     } else {
         if (cg.stage_tok == 16)
             ctrl_bwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, cta);
@@ -655,6 +668,11 @@ CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
     cg.consumers = (D / 8 + 31) / 32;
     if (cg.consumers < 1) cg.consumers = 1;
     cg.threads = 32 * (1 + cg.consumers);
+    cg.n_stages = (BL + cg.stage_tok - 1) / cg.stage_tok;
+    {   // tokens of the longest CTA range: there are at least min(stages, SMs) CTAs
+        const long long fewest = cg.n_stages < ctrl_sms() ? cg.n_stages : ctrl_sms();
+        cg.max_cta_tok = (int)((cg.n_stages + fewest - 1) / fewest * cg.stage_tok);
+    }
     const size_t xb = (ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15);
     cg.smem = (int)(ctrl_ring_bytes(cg, D) + xb + 3 * cg.ring * sizeof(uint64_t));
     int per_sm = (int)((227 * 1024) / (cg.smem + 1024));
@@ -662,7 +680,6 @@ CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
     if (per_sm > by_threads) per_sm = by_threads;
     if (per_sm > 4) per_sm = 4;
     if (per_sm < 1) per_sm = 1;
-    cg.n_stages = (BL + cg.stage_tok - 1) / cg.stage_tok;
     long long ctas = (long long)ctrl_sms() * per_sm;
     if (ctas > cg.n_stages) ctas = cg.n_stages;
     if (ctas > kCtrlRowsMax) ctas = kCtrlRowsMax;

@@ -175,12 +175,16 @@ __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* w
     }
 }
 
+// hmid: where the state entering token 8 of the sub-chunk is kept (the
+// backward restarts there), or null.
 template <bool FAST, bool SIMPLE>
 __device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
                                                const ModeConst& k0, const ModeConst& k1, float2& z0, float2& z1,
-                                               uint32_t* yp, float* y32p, bool active, size_t row, int half) {
+                                               uint32_t* yp, float* y32p, bool active, size_t row, int half,
+                                               float4* hmid) {
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
+        if (i == kHalf && hmid != nullptr && (SIMPLE || i < nsub)) *hmid = make_float4(z0.x, z0.y, z1.x, z1.y);
         if (SIMPLE || i < nsub) {
             const float4 ct = sc[i];
             const float2 br = bf2_to_f2(wre[i * kWords]);
@@ -387,9 +391,9 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
         const int slot = k % kRing;
         const int ts = T.t_begin + k * kSub;
         const int nsub = min(kSub, T.t_end - ts);
-        if (active)
-            *reinterpret_cast<float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kSub) * M + m) =
-                make_float4(z0.x, z0.y, z1.x, z1.y);
+        float4* hs = active ? reinterpret_cast<float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m) : nullptr;
+        if (active) hs[0] = make_float4(z0.x, z0.y, z1.x, z1.y);
+        float4* hmid = active ? hs + M / 2 : nullptr;   // slot ts/8 + 1
         if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
         float* y32p = a.y32 != nullptr ? a.y32 + 2 * row0 : nullptr;
         const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
         LRS_SUB_DISPATCH(kd, fwd_replay_sub, sc, wre, wim, nsub, k0, k1, z0, z1, a.y + row0, y32p, active, D / 2,
-                         M / 2);
+                         M / 2, hmid);
         __syncwarp();
         if (lane == 0 && k + kRing < T.nsc)
             ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (k + kRing) * kSub, T.b);
@@ -438,24 +442,77 @@ __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* g
     }
 }
 
-// Forward sweep of one sub-chunk from its entry state: u_t = lambda_t z_{t-1}
-// (kept for kappa) and z_t = u_t + b_t.
+// ---------------------------------------------------------------------------
+// Reverse replay.  It walks each segment backwards in units of 8 tokens, the
+// distance between the forward's state checkpoints, through a ring of 8-row
+// items: for every unit the w rows (forward sweep) and then the dy rows
+// (reverse sweep).  The forward sweep keeps lambda_t and u_t = lambda_t z_{t-1}
+// of all 8 tokens in registers, so lambda is evaluated once per token.
+// ---------------------------------------------------------------------------
+constexpr int kRingH = 4;                                   // slots of the 8-row ring
+constexpr int kHalfItemBytes = 2 * kHalf * kRowBytes + kHalf * 16;
+
+struct alignas(128) WarpRingH {
+    uint32_t box[kRingH][2][kHalf][kWords];   // [slot][re, im][token][pair]
+    float4 ctrl[kRingH][kHalf];
+    uint64_t full[kRingH];
+};
+static_assert(sizeof(WarpRingH) <= sizeof(WarpRing), "the 8-row ring must fit the engine's shared memory");
+
+__device__ __forceinline__ void ringh_issue(WarpRingH& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
+                                            int x_re, int x_im, int ts, int b) {
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&R.full[slot], kHalfItemBytes);
+    tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
+    tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
+    tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
+}
+
+__device__ __forceinline__ bool ringh_wait(WarpRingH& R, int k, int n_items, uint32_t* status, int lane) {
+    if (mbar_wait_bounded(&R.full[k % kRingH], (uint32_t)(k / kRingH) & 1u)) return true;
+    if (lane == 0) atomicOr(status, kStatusTimeout);
+    for (int j = k + 1; j < k + kRingH && j < n_items; ++j)
+        mbar_wait_bounded(&R.full[j % kRingH], (uint32_t)(j / kRingH) & 1u);
+    return false;
+}
+
+// The sub_kind() facts for a unit of 8 tokens.
+__device__ __forceinline__ SubKind unit_kind(const float4* sc, int nh, int lane, const ModeConst& k0,
+                                             const ModeConst& k1) {
+    const float4 ct = sc[lane & (kHalf - 1)];
+    const bool mine = lane < nh;
+    const float e = mine ? fabsf(ct.x) : 0.f;
+    const float emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(e)));
+    const bool ok = fabsf(k0.nu) * emax < kPolyBound && fabsf(k1.nu) * emax < kPolyBound;
+    SubKind kd;
+    kd.fast = __all_sync(0xffffffffu, ok);
+    kd.simple = nh == kHalf && !__any_sync(0xffffffffu, mine && ct.w != 0.f);
+    return kd;
+}
+
+// Forward sweep of one unit from its entry state: lam_t = lambda_t and
+// u_t = lambda_t z_{t-1} (kept for kappa), z_t = u_t + b_t.  A reset token
+// gets lam_t = 0.
 template <bool FAST, bool SIMPLE>
-__device__ __forceinline__ void bwd_forward_sweep(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
-                                                  const ModeConst& k0, const ModeConst& k1, float2 z0, float2 z1,
-                                                  float4 (&u)[kSub]) {
+__device__ __forceinline__ void bwd_forward_unit(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nh,
+                                                 const ModeConst& k0, const ModeConst& k1, float2 z0, float2 z1,
+                                                 float4 (&u)[kHalf], float4 (&lam)[kHalf]) {
 #pragma unroll
-    for (int i = 0; i < kSub; ++i) {
+    for (int i = 0; i < kHalf; ++i) {
         u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (SIMPLE || i < nsub) {
+        lam[i] = u[i];
+        if (SIMPLE || i < nh) {
             const float4 ct = sc[i];
             const float2 br = bf2_to_f2(wre[i * kWords]);
             const float2 bi = bf2_to_f2(wim[i * kWords]);
             if (SIMPLE || !is_reset(ct)) {
+                const float2 l0 = samu_lambda<FAST>(k0, ct);
+                const float2 l1 = samu_lambda<FAST>(k1, ct);
                 float2 u0, u1;
-                z0 = step_state(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), z0, &u0);
-                z1 = step_state(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), z1, &u1);
+                z0 = step_state(l0, make_float2(br.x, bi.x), z0, &u0);
+                z1 = step_state(l1, make_float2(br.y, bi.y), z1, &u1);
                 u[i] = make_float4(u0.x, u0.y, u1.x, u1.y);
+                lam[i] = make_float4(l0.x, l0.y, l1.x, l1.y);
             } else {
                 z0 = make_float2(br.x, bi.x);
                 z1 = make_float2(br.y, bi.y);
@@ -464,12 +521,12 @@ __device__ __forceinline__ void bwd_forward_sweep(const float4* sc, const uint32
     }
 }
 
-// Sums v[k] over the 32 lanes of the warp for every k at once: on return
-// lane L holds the total of v[L].  31 shuffles (a butterfly that halves the
-// live values at each of its five levels) in a fixed order.
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+// Sums v[k] over the 32 lanes for every k of 16 values at once: halving
+// exchanges inside each 16-lane half, then one exchange across the halves.
+// On return lane L holds the total of v[L mod 16].  Fixed order.
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane) {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int k = 0; k < o; ++k) {
@@ -478,26 +535,26 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
             v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
-    return v[0];
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
-// Reverse sweep: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
-// kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa,
-// per token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64
-// modes of the warp (written to kp[token * kp_row + {0, 1}]); then
+// Reverse sweep of one unit: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
+// kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa; per
+// token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64 modes
+// of the warp (written to kp[token * kp_row + {0, 1}]); then
 // A <- conj(lambda_t) A.
-template <bool FAST, bool SIMPLE>
-__device__ __forceinline__ void bwd_reverse_sweep(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nsub,
-                                                  const ModeConst& k0, const ModeConst& k1, const float4 (&u)[kSub],
-                                                  float2& A0, float2& A1, float4& acc, uint32_t* dwb, float* dwf,
-                                                  bool fp32, bool active, size_t row, int half, float* kp,
-                                                  size_t kp_row, int lane) {
-    float v[2 * kSub];
+template <bool SIMPLE>
+__device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nh,
+                                                 const ModeConst& k0, const ModeConst& k1, const float4 (&u)[kHalf],
+                                                 const float4 (&lam)[kHalf], float2& A0, float2& A1, float4& acc,
+                                                 uint32_t* dwb, float* dwf, bool fp32, bool active, size_t row,
+                                                 int half, float* kp, size_t kp_row, int lane) {
+    float v[2 * kHalf];
 #pragma unroll
-    for (int i = kSub - 1; i >= 0; --i) {
+    for (int i = kHalf - 1; i >= 0; --i) {
         v[2 * i] = 0.f;
         v[2 * i + 1] = 0.f;
-        if (SIMPLE || i < nsub) {
+        if (SIMPLE || i < nh) {
             const float4 ct = sc[i];
             const float2 g_r = bf2_to_f2(gre[i * kWords]);
             const float2 g_i = bf2_to_f2(gim[i * kWords]);
@@ -527,16 +584,17 @@ __device__ __forceinline__ void bwd_reverse_sweep(const float4* sc, const uint32
                 acc.w += ki1;
                 v[2 * i] = ki0 + ki1;
                 v[2 * i + 1] = -__fmaf_rn(k0.nu, kr0, __fmul_rn(k1.nu, kr1));
-                A0 = cmulc(samu_lambda<FAST>(k0, ct), A0);
-                A1 = cmulc(samu_lambda<FAST>(k1, ct), A1);
+                const float4 l = lam[i];
+                A0 = cmulc(make_float2(l.x, l.y), A0);
+                A1 = cmulc(make_float2(l.z, l.w), A1);
             } else {   // segment start: no controller terms, the adjoint stops here
                 A0 = make_float2(0.f, 0.f);
                 A1 = A0;
             }
         }
     }
-    const float tot = warp_reduce_scatter32(v, lane);
-    if ((lane >> 1) < nsub) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
+    const float tot = warp_reduce_scatter16(v, lane);
+    if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
 }
 
 __global__ void __launch_bounds__(kEngineThreads, 6)
@@ -690,7 +748,7 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    WarpRingH& R = reinterpret_cast<WarpRingH*>(smem_raw + (size_t)warp * sizeof(WarpRing))[0];
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     if (gw >= (long long)g.n_chains * g.NS) return;
@@ -701,16 +759,20 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     const int m = T.grp * kGroup + 2 * lane;
     const bool active = m < M;
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
-    const int n_items = 2 * T.nsc;
-    // item k: sub-chunk nsc-1-k/2 (the segment from its end backwards); even
+    const int n_units = (T.t_end - T.t_begin + kHalf - 1) / kHalf;
+    const int n_items = 2 * n_units;
+    // item k: unit n_units-1-k/2 (the segment from its end backwards); even
     // items carry w (forward sweep), odd items dy (reverse sweep)
-    auto item_ts = [&](int k) { return T.t_begin + (T.nsc - 1 - (k >> 1)) * kSub; };
-    ring_init(R, lane);
+    auto item_ts = [&](int k) { return T.t_begin + (n_units - 1 - (k >> 1)) * kHalf; };
+    if (lane == 0) {
+        for (int i = 0; i < kRingH; ++i) mbar_init(&R.full[i], 1);
+    }
+    __syncwarp();
     pdl_trigger();
     pdl_wait();
     if (lane == 0)
-        for (int k = 0; k < kRing && k < n_items; ++k)
-            ring_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
+        for (int k = 0; k < kRingH && k < n_items; ++k)
+            ringh_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
     ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
     float2 A0 = make_float2(0.f, 0.f), A1 = A0;
     if (active) {
@@ -724,38 +786,42 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     const bool fp32 = a.grad_fp32 != 0;
     for (int k = 0; k < n_items; k += 2) {
         const int ts = item_ts(k);
-        const int nsub = min(kSub, T.t_end - ts);
+        const int nh = min(kHalf, T.t_end - ts);
         float2 z0 = make_float2(0.f, 0.f), z1 = z0;
         if (active) {
-            const float4 hv = *reinterpret_cast<const float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kSub) * M + m);
+            const float4 hv = *reinterpret_cast<const float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m);
             z0 = make_float2(hv.x, hv.y);
             z1 = make_float2(hv.z, hv.w);
         }
         // w item: forward sweep
-        int slot = k % kRing;
-        if (!ring_wait(R, k, n_items, a.status, lane)) return;
+        int slot = k % kRingH;
+        if (!ringh_wait(R, k, n_items, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
-        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
-        float4 u[kSub];
-        LRS_SUB_DISPATCH(kd, bwd_forward_sweep, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nsub, k0, k1,
-                         z0, z1, u);
+        const SubKind kd = unit_kind(sc, nh, lane, k0, k1);
+        float4 u[kHalf], lam[kHalf];
+        LRS_SUB_DISPATCH(kd, bwd_forward_unit, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k0, k1,
+                         z0, z1, u, lam);
         __syncwarp();
-        if (lane == 0 && k + kRing < n_items)
-            ring_issue(R, slot, ((k + kRing) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k + kRing), T.b);
+        if (lane == 0 && k + kRingH < n_items)
+            ringh_issue(R, slot, ((k + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k + kRingH), T.b);
         // dy item: reverse sweep
-        slot = (k + 1) % kRing;
-        if (!ring_wait(R, k + 1, n_items, a.status, lane)) return;
+        slot = (k + 1) % kRingH;
+        if (!ringh_wait(R, k + 1, n_items, a.status, lane)) return;
         sc = R.ctrl[slot];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
         float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
         float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
-        LRS_SUB_DISPATCH(kd, bwd_reverse_sweep, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nsub, k0, k1,
-                         u, A0, A1, acc, dwb, dwf, fp32, active, D / 2, M / 2, kp, 2 * (size_t)g.n_groups, lane);
+        if (kd.simple)
+            bwd_reverse_unit<true>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k0, k1, u, lam, A0, A1,
+                                   acc, dwb, dwf, fp32, active, D / 2, M / 2, kp, 2 * (size_t)g.n_groups, lane);
+        else
+            bwd_reverse_unit<false>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k0, k1, u, lam, A0,
+                                    A1, acc, dwb, dwf, fp32, active, D / 2, M / 2, kp, 2 * (size_t)g.n_groups, lane);
         __syncwarp();
-        if (lane == 0 && k + 1 + kRing < n_items)
-            ring_issue(R, slot, ((k + 1 + kRing) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
-                       item_ts(k + 1 + kRing), T.b);
+        if (lane == 0 && k + 1 + kRingH < n_items)
+            ringh_issue(R, slot, ((k + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
+                        item_ts(k + 1 + kRingH), T.b);
     }
     if (active) {
         *reinterpret_cast<float4*>(a.numod + ((size_t)T.b * g.NS + T.s) * M + m) = acc;

@@ -9,6 +9,63 @@ namespace lrs {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// ---------------------------------------------------------------------------
+// Paired FP32 arithmetic.  Each lane of a scan warp owns the two adjacent
+// modes m, m+1; their values travel as one pair {mode m, mode m+1} in a
+// 64-bit register pair, and each arithmetic step on them is one paired
+// instruction (PTX fma/mul/add/sub.rn.f32x2): per element exactly the IEEE
+// round-to-nearest operation of the scalar form.
+// ---------------------------------------------------------------------------
+typedef unsigned long long f2x;
+
+__device__ __forceinline__ f2x pk2(float lo, float hi) {
+    f2x r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ f2x dup2(float v) { return pk2(v, v); }
+__device__ __forceinline__ void up2(f2x v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2x fma2(f2x a, f2x b, f2x c) {
+    f2x d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2x mul2(f2x a, f2x b) {
+    f2x d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2x add2(f2x a, f2x b) {
+    f2x d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2x sub2(f2x a, f2x b) {
+    f2x d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// A BF16 pair word (low half mode m, high half mode m+1) as an FP32 pair;
+// nbf2x gives the negated pair (sign bits flipped before widening).
+__device__ __forceinline__ f2x bf2x(uint32_t w) {
+    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ f2x nbf2x(uint32_t w) { return bf2x(w ^ 0x80008000u); }
+// An FP32 pair rounded to a BF16 pair word (round to nearest even).
+__device__ __forceinline__ uint32_t x2bf(f2x v) {
+    float a, b;
+    up2(v, a, b);
+    return f2_to_bf2(a, b);
+}
+
+// Complex values of the two modes: real-part pair and imaginary-part pair.
+struct c2x {
+    f2x re, im;
+};
+
 // Per-mode constants of the transition.  lambda_{t,m} = e^{-nu_m E_t} e^{i(theta_m + d_t)}
 // (SAMU GPU page, section 05, transition equation) is evaluated as
 //   lambda_{t,m} = lbar_m * delta_{t,m},  lbar_m = e^{-nu_m} e^{i theta_m},
@@ -17,66 +74,112 @@ constexpr float kLog2e = 1.4426950408889634f;
 // once in FP64), so no per-mode rounding of e^{-nu}, cos theta or sin theta
 // biases every step of a long chain; delta is close to 1 and formed per step
 // in FP32 from E_t - 1 = expm1(c_t) and the shared C_t, S_t.
-struct ModeConst {
-    float hr, hi, lr, li;   // lbar: hi part (re, im), lo part (re, im)
-    float nu;
+struct ModePair {
+    f2x hr, hi, nhi, lr, li;   // lbar hi part (re, im, -im), lo part (re, im)
+    f2x nu;
 };
 
-__device__ __forceinline__ ModeConst load_mode(const float4* __restrict__ modes,
-                                               const float* __restrict__ nu, int m) {
-    const float4 v = modes[m];
-    ModeConst k;
-    k.hr = v.x;
-    k.hi = v.y;
-    k.lr = v.z;
-    k.li = v.w;
-    k.nu = nu[m];
+__device__ __forceinline__ ModePair load_modes(const float4* __restrict__ modes, const float* __restrict__ nu,
+                                               int m) {
+    const float4 v0 = modes[m], v1 = modes[m + 1];
+    ModePair k;
+    k.hr = pk2(v0.x, v1.x);
+    k.hi = pk2(v0.y, v1.y);
+    k.nhi = pk2(-v0.y, -v1.y);
+    k.lr = pk2(v0.z, v1.z);
+    k.li = pk2(v0.w, v1.w);
+    k.nu = pk2(nu[m], nu[m + 1]);
+    return k;
+}
+
+__device__ __forceinline__ ModePair zero_modes() {
+    ModePair k;
+    k.hr = k.hi = k.nhi = k.lr = k.li = k.nu = 0ull;
     return k;
 }
 
 // Per-token control word, written by the controller forward and staged into
-// shared memory by TMA: {E_t - 1, C_t, S_t, reset_t} with reset_t 1 at a
-// segment start (lambda = 0) and 0 elsewhere.  It is the same for every lane,
-// so the branches on it are warp-uniform.
+// shared memory by TMA, each value duplicated so that it loads as a pair:
+// {E-1, E-1, C, C}, {S, S, reset, reset} (two float4), reset 1 at a segment
+// start (lambda = 0) and 0 elsewhere.  It is the same for every lane, so the
+// branches on it are warp-uniform.
+struct Ctl2 {
+    f2x e, c, s;   // E - 1, C, S
+    float reset;
+    float em1;     // E - 1 (scalar)
+};
+
+__device__ __forceinline__ Ctl2 load_ctl(const float4* sc, int i) {
+    const float4 a = sc[2 * i], b = sc[2 * i + 1];
+    Ctl2 ct;
+    ct.e = pk2(a.x, a.y);
+    ct.c = pk2(a.z, a.w);
+    ct.s = pk2(b.x, b.y);
+    ct.reset = b.z;
+    ct.em1 = a.x;
+    return ct;
+}
+
+__device__ __forceinline__ bool is_reset(const Ctl2& ct) { return ct.reset != 0.f; }
 
 // Bound on |nu (E - 1)| under which the degree-3 polynomial below is exact to
-// < 2e-11 relative (the truncation term x^4/24), checked once per warp and tile.
+// < 2e-11 relative (the truncation term x^4/24), checked once per warp and
+// sub-chunk.
 constexpr float kPolyBound = 1.0f / 64.0f;
 
-// lambda_{t,m} for a token that is not a reset: lbar_m * e^{-nu (E-1)} (C + iS).
-// FAST: e^{-x} by its degree-3 Taylor polynomial (valid for |x| < kPolyBound;
-// its rounding errors carry no per-mode bias); otherwise ex2.approx, whose
-// ~1e-7 error matters little for the short-memory modes that need it.
-// Every pass that needs lambda calls this, so the forward and the backward
-// rebuild the same bits.
+// lambda of both modes for a token that is not a reset:
+// lbar * e^{-nu (E-1)} (C + iS), with its negated imaginary part.  FAST:
+// e^{-x} by its degree-3 Taylor polynomial (valid for |x| < kPolyBound; its
+// rounding errors carry no per-mode bias); otherwise ex2.approx, whose ~1e-7
+// error matters little for the short-memory modes that need it.  Every pass
+// that needs lambda calls this, so the forward and the backward rebuild the
+// same bits.
+struct Lam2 {
+    f2x re, im, nim;
+};
+
 template <bool FAST>
-__device__ __forceinline__ float2 samu_lambda(const ModeConst& k, float4 ctl) {
-    const float x = __fmul_rn(k.nu, ctl.x);                 // nu (E - 1)
-    float q;                                                 // e^{-x}
+__device__ __forceinline__ Lam2 samu_lambda2(const ModePair& k, const Ctl2& ct) {
+    const f2x x = mul2(k.nu, ct.e);   // nu (E - 1)
+    f2x q;                            // e^{-x}
     if (FAST) {
-        q = __fmaf_rn(x, __fmaf_rn(x, __fmaf_rn(x, -1.0f / 6.0f, 0.5f), -1.0f), 1.0f);
+        q = fma2(x, fma2(x, fma2(x, dup2(-1.0f / 6.0f), dup2(0.5f)), dup2(-1.0f)), dup2(1.0f));
     } else {
-        q = ex2_approx(__fmul_rn(-x, kLog2e));
+        float a, b;
+        up2(x, a, b);
+        q = pk2(ex2_approx(__fmul_rn(-a, kLog2e)), ex2_approx(__fmul_rn(-b, kLog2e)));
     }
-    const float dr = __fmul_rn(q, ctl.y);
-    const float di = __fmul_rn(q, ctl.z);
-    return make_float2(__fmaf_rn(k.hr, dr, __fmaf_rn(-k.hi, di, k.lr)),
-                       __fmaf_rn(k.hr, di, __fmaf_rn(k.hi, dr, k.li)));
+    const f2x dr = mul2(q, ct.c);
+    const f2x di = mul2(q, ct.s);
+    Lam2 l;
+    l.re = fma2(k.hr, dr, fma2(k.nhi, di, k.lr));
+    l.im = fma2(k.hr, di, fma2(k.hi, dr, k.li));
+    l.nim = sub2(0ull, l.im);
+    return l;
 }
 
-// One state step z' = lambda z + b, formed as u = lambda z then u + b.  The
-// backward keeps u = lambda z_{t-1} for kappa, so both directions use this form.
-__device__ __forceinline__ float2 step_state(float2 l, float2 bb, float2 z, float2* u_out = nullptr) {
-    const float2 u = cmul(l, z);
-    if (u_out) *u_out = u;
-    return make_float2(__fadd_rn(u.x, bb.x), __fadd_rn(u.y, bb.y));
+// lambda z
+__device__ __forceinline__ c2x cmul2(const Lam2& l, const c2x& z) {
+    c2x r;
+    r.re = fma2(l.re, z.re, mul2(l.nim, z.im));
+    r.im = fma2(l.re, z.im, mul2(l.im, z.re));
+    return r;
 }
 
-// S <- T_t o S for T_t(h) = l h + bb, S = {Lambda, beta}.
-__device__ __forceinline__ float4 compose_step(float2 l, float2 bb, float4 S) {
-    const float2 L = cmul(l, make_float2(S.x, S.y));
-    const float2 Bv = capply(make_float4(l.x, l.y, bb.x, bb.y), make_float2(S.z, S.w));
-    return make_float4(L.x, L.y, Bv.x, Bv.y);
+// conj(lambda) z
+__device__ __forceinline__ c2x cmulc2(const Lam2& l, const c2x& z) {
+    c2x r;
+    r.re = fma2(l.re, z.re, mul2(l.im, z.im));
+    r.im = fma2(l.re, z.im, mul2(l.nim, z.re));
+    return r;
+}
+
+// acc + P b, given -Im b
+__device__ __forceinline__ c2x cfma2(const c2x& P, const c2x& bb, f2x nb_im, const c2x& acc) {
+    c2x r;
+    r.re = fma2(P.re, bb.re, fma2(P.im, nb_im, acc.re));
+    r.im = fma2(P.re, bb.im, fma2(P.im, bb.re, acc.im));
+    return r;
 }
 
 // Forward scan over segments: segment maps, chain prefix, replay.  w and
@@ -140,7 +243,7 @@ struct SamuCtrlBwdArgs {
     const float2* kpart;
     const float* p;
     const float* r;
-    const float4* ctrl;
+    const float4* ctrl;     // [B*L][2] control words
     const float* wh;        // [2][D+1]
     const float* misc;
     void* dx;               // BF16 or FP32
@@ -184,7 +287,7 @@ struct SamuCtrlFwdArgs {
     const float* theta;
     float* p;
     float* r;
-    float4* ctrl;                  // {E - 1, C, S, reset}
+    float4* ctrl;                  // [B*L][2] {E-1, E-1, C, C}, {S, S, reset, reset}
     float* wh;                     // [2][D+1]
     float* misc;
     float4* modes;                 // [M] lbar hi/lo

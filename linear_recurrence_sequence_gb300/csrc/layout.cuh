@@ -121,7 +121,7 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
     size_t o = 0;
     s.p = o;      o = align_up(o + BL * 4);                          // p_t
     s.r = o;      o = align_up(o + BL * 4);                          // r_t
-    s.ctrl = o;   o = align_up(o + BL * 16);                         // {E-1, C, S, reset}
+    s.ctrl = o;   o = align_up(o + BL * 32);                         // {E-1, E-1, C, C}, {S, S, reset, reset}
     s.hsub = o;   o = align_up(o + (size_t)B * g.CS * M * 8);        // state every 8 tokens
     s.wh = o;     o = align_up(o + (size_t)2 * (D + 1) * 4);         // unit directions
     s.misc = o;   o = align_up(o + kMiscFloats * 4);

@@ -210,7 +210,9 @@ __device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, cons
             const float rs = (a.reset != nullptr && a.reset[t] != 0) ? 1.0f : 0.0f;
             a.p[t] = p;
             a.r[t] = r;
-            a.ctrl[t] = make_float4(expm1f(c), cs, sn, rs);
+            const float em1 = expm1f(c);
+            a.ctrl[2 * t] = make_float4(em1, em1, cs, cs);
+            a.ctrl[2 * t + 1] = make_float4(sn, sn, rs, rs);
         }
     }
 }
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_bwd_kernel(SamuCtrl
             dbar += v.x;
             ebar += v.y;
         }
-        const float E = 1.0f + a.ctrl[t].x;   // ctrl.x holds E - 1
+        const float E = 1.0f + a.ctrl[2 * t].x;   // the control word starts with E - 1
         const float p = a.p[t];
         const float r = a.r[t];
         const float cbar = ebar * E;

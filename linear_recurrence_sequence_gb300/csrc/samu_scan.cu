@@ -39,14 +39,15 @@ constexpr int kEngineThreads = kEngineWarps * 32;
 constexpr int kRing = 2;                            // staging slots per warp
 constexpr int kWords = kGroup / 2;                  // BF16 pairs per box row
 constexpr int kBoxBytes = kSub * kRowBytes;         // one [16 x 64] BF16 box: 2 KB
-constexpr int kItemBytes = 2 * kBoxBytes + kSub * 16;   // re box + im box + control words
+constexpr int kCtlBytes = 32;                       // one token's control word (two float4)
+constexpr int kItemBytes = 2 * kBoxBytes + kSub * kCtlBytes;   // re box + im box + control words
 constexpr int kPrefixWarps = 16;
 
 // One warp's staging ring.  Every TMA destination starts on a 128-byte
 // boundary (box sizes are multiples of 128 bytes).
 struct alignas(128) WarpRing {
     uint32_t box[kRing][2][kSub][kWords];   // [slot][re, im][token][pair]
-    float4 ctrl[kRing][kSub];
+    float4 ctrl[kRing][2 * kSub];           // [slot][token: two float4]
     uint64_t full[kRing];
 };
 constexpr int kEngineSmem = kEngineWarps * (int)sizeof(WarpRing);
@@ -70,27 +71,29 @@ __device__ __forceinline__ SegTask seg_task(const SegGeom& g, long long gw) {
     return T;
 }
 
-__device__ __forceinline__ bool is_reset(const float4& ct) { return ct.w != 0.f; }
-
-// Warp-uniform facts about one sub-chunk that select the code path:
+// Warp-uniform facts about N consecutive tokens that select the code path:
 //  fast:   |nu| max|E - 1| < kPolyBound for every lane's modes (polynomial
 //          lambda instead of ex2.approx);
-//  simple: all 16 tokens present and none of them a reset (no per-token
+//  simple: all N tokens present and none of them a reset (no per-token
 //          checks).
 struct SubKind {
     bool fast, simple;
 };
 
-__device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane, const ModeConst& k0,
-                                            const ModeConst& k1) {
-    const float4 ct = sc[lane & (kSub - 1)];
+template <int N>
+__device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane, const ModePair& k) {
+    const int i = lane & (N - 1);
+    const float em1 = sc[2 * i].x;
+    const float rst = sc[2 * i + 1].z;
     const bool mine = lane < nsub;
-    const float e = mine ? fabsf(ct.x) : 0.f;
+    const float e = mine ? fabsf(em1) : 0.f;
     const float emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(e)));
-    const bool ok = fabsf(k0.nu) * emax < kPolyBound && fabsf(k1.nu) * emax < kPolyBound;
+    float n0, n1;
+    up2(k.nu, n0, n1);
+    const bool ok = fabsf(n0) * emax < kPolyBound && fabsf(n1) * emax < kPolyBound;
     SubKind kd;
     kd.fast = __all_sync(0xffffffffu, ok);
-    kd.simple = nsub == kSub && !__any_sync(0xffffffffu, mine && ct.w != 0.f);
+    kd.simple = nsub == N && !__any_sync(0xffffffffu, mine && rst != 0.f);
     return kd;
 }
 
@@ -110,13 +113,39 @@ __device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane
         }                                              \
     } while (0)
 
-// acc + P b (complex)
-__device__ __forceinline__ float2 cfma(float2 P, float2 bb, float2 acc) {
-    return make_float2(__fmaf_rn(P.x, bb.x, __fmaf_rn(-P.y, bb.y, acc.x)),
-                       __fmaf_rn(P.x, bb.y, __fmaf_rn(P.y, bb.x, acc.y)));
+__device__ __forceinline__ float4 identity_map() { return make_float4(1.f, 0.f, 0.f, 0.f); }
+
+__device__ __forceinline__ c2x czero() {
+    c2x z;
+    z.re = 0ull;
+    z.im = 0ull;
+    return z;
 }
 
-__device__ __forceinline__ float4 identity_map() { return make_float4(1.f, 0.f, 0.f, 0.f); }
+// A lane's two modes of an [.., M, 2] FP32 array (re, im per mode) as pairs.
+__device__ __forceinline__ c2x load_c2(const float* p) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    c2x z;
+    z.re = pk2(v.x, v.z);
+    z.im = pk2(v.y, v.w);
+    return z;
+}
+__device__ __forceinline__ void store_c2(float* p, const c2x& z) {
+    float r0, r1, i0, i1;
+    up2(z.re, r0, r1);
+    up2(z.im, i0, i1);
+    *reinterpret_cast<float4*>(p) = make_float4(r0, i0, r1, i1);
+}
+// An affine map of each of the two modes, as stored per mode {l.re, l.im, b.re, b.im}.
+__device__ __forceinline__ void store_map2(float4* p, const c2x& l, const c2x& bb) {
+    float lr0, lr1, li0, li1, br0, br1, bi0, bi1;
+    up2(l.re, lr0, lr1);
+    up2(l.im, li0, li1);
+    up2(bb.re, br0, br1);
+    up2(bb.im, bi0, bi1);
+    p[0] = make_float4(lr0, li0, br0, bi0);
+    p[1] = make_float4(lr1, li1, br1, bi1);
+}
 
 // Lane 0: stage the sub-chunk at token ts of tensor `tm` (both halves of the
 // warp's 64 modes) and its control words into ring slot `slot`.  The warp has
@@ -143,7 +172,8 @@ __device__ __forceinline__ void ring_init(WarpRing& R, int lane) {
 __device__ __forceinline__ bool ring_wait(WarpRing& R, int k, int n_items, uint32_t* status, int lane) {
     if (mbar_wait_bounded(&R.full[k % kRing], (uint32_t)(k / kRing) & 1u)) return true;
     if (lane == 0) atomicOr(status, kStatusTimeout);
-    for (int j = k + 1; j < k + kRing && j < n_items; ++j) mbar_wait_bounded(&R.full[j % kRing], (uint32_t)(j / kRing) & 1u);
+    for (int j = k + 1; j < k + kRing && j < n_items; ++j)
+        mbar_wait_bounded(&R.full[j % kRing], (uint32_t)(j / kRing) & 1u);
     return false;
 }
 
@@ -154,23 +184,20 @@ __device__ __forceinline__ bool ring_wait(WarpRing& R, int k, int n_items, uint3
 // the tokens after them: H o T_t = (P lambda_t, P b_t + beta).
 template <bool FAST, bool SIMPLE>
 __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
-                                             const ModeConst& k0, const ModeConst& k1, float2& P0, float2& P1,
-                                             float2& be0, float2& be1) {
+                                             const ModePair& k, c2x& P, c2x& be) {
 #pragma unroll
     for (int i = kSub - 1; i >= 0; --i) {
         if (SIMPLE || i < nsub) {
-            const float4 ct = sc[i];
-            const float2 br = bf2_to_f2(wre[i * kWords]);
-            const float2 bi = bf2_to_f2(wim[i * kWords]);
-            be0 = cfma(P0, make_float2(br.x, bi.x), be0);
-            be1 = cfma(P1, make_float2(br.y, bi.y), be1);
-            if (SIMPLE || !is_reset(ct)) {
-                P0 = cmul(samu_lambda<FAST>(k0, ct), P0);
-                P1 = cmul(samu_lambda<FAST>(k1, ct), P1);
-            } else {   // segment start: nothing before it reaches past it
-                P0 = make_float2(0.f, 0.f);
-                P1 = P0;
-            }
+            const Ctl2 ct = load_ctl(sc, i);
+            const uint32_t wr = wre[i * kWords], wi = wim[i * kWords];
+            c2x bb;
+            bb.re = bf2x(wr);
+            bb.im = bf2x(wi);
+            be = cfma2(P, bb, nbf2x(wi), be);
+            if (SIMPLE || !is_reset(ct))
+                P = cmul2(samu_lambda2<FAST>(k, ct), P);
+            else   // segment start: nothing before it reaches past it
+                P = czero();
         }
     }
 }
@@ -179,31 +206,34 @@ __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* w
 // backward restarts there), or null.
 template <bool FAST, bool SIMPLE>
 __device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
-                                               const ModeConst& k0, const ModeConst& k1, float2& z0, float2& z1,
-                                               uint32_t* yp, float* y32p, bool active, size_t row, int half,
-                                               float4* hmid) {
+                                               const ModePair& k, c2x& z, uint32_t* yp, float* y32p, bool active,
+                                               size_t row, int half, f2x* hmid) {
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
-        if (i == kHalf && hmid != nullptr && (SIMPLE || i < nsub)) *hmid = make_float4(z0.x, z0.y, z1.x, z1.y);
+        if (i == kHalf && hmid != nullptr && (SIMPLE || i < nsub)) {
+            hmid[0] = z.re;
+            hmid[1] = z.im;
+        }
         if (SIMPLE || i < nsub) {
-            const float4 ct = sc[i];
-            const float2 br = bf2_to_f2(wre[i * kWords]);
-            const float2 bi = bf2_to_f2(wim[i * kWords]);
+            const Ctl2 ct = load_ctl(sc, i);
+            c2x bb;
+            bb.re = bf2x(wre[i * kWords]);
+            bb.im = bf2x(wim[i * kWords]);
             if (SIMPLE || !is_reset(ct)) {
-                z0 = step_state(samu_lambda<FAST>(k0, ct), make_float2(br.x, bi.x), z0);
-                z1 = step_state(samu_lambda<FAST>(k1, ct), make_float2(br.y, bi.y), z1);
+                const c2x u = cmul2(samu_lambda2<FAST>(k, ct), z);
+                z.re = add2(u.re, bb.re);
+                z.im = add2(u.im, bb.im);
             } else {
-                z0 = make_float2(br.x, bi.x);
-                z1 = make_float2(br.y, bi.y);
+                z = bb;
             }
             if (active) {
                 uint32_t* o = yp + (size_t)i * row;
-                __stcs(o, f2_to_bf2(z0.x, z1.x));
-                __stcs(o + half, f2_to_bf2(z0.y, z1.y));
+                __stcs(o, x2bf(z.re));
+                __stcs(o + half, x2bf(z.im));
                 if (y32p != nullptr) {
-                    float* f = y32p + (size_t)i * 2 * row;
-                    __stcs(reinterpret_cast<float2*>(f), make_float2(z0.x, z1.x));
-                    __stcs(reinterpret_cast<float2*>(f + 2 * half), make_float2(z0.y, z1.y));
+                    f2x* f = reinterpret_cast<f2x*>(y32p + (size_t)i * 2 * row);
+                    f[0] = z.re;
+                    f[half] = z.im;   // M floats further: the imaginary half
                 }
             }
         }
@@ -233,32 +263,26 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kSub, T.b);
-    ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
-    if (active) {
-        k0 = load_mode(a.modes, a.nu, m);
-        k1 = load_mode(a.modes, a.nu, m + 1);
-    }
-    float2 P0 = make_float2(1.f, 0.f), P1 = P0;
-    float2 be0 = make_float2(0.f, 0.f), be1 = be0;
-    for (int k = 0; k < T.nsc; ++k) {
-        const int slot = k % kRing;
-        const int ts = T.t_begin + (T.nsc - 1 - k) * kSub;
+    const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    c2x P;
+    P.re = dup2(1.f);
+    P.im = 0ull;
+    c2x be = czero();
+    for (int it = 0; it < T.nsc; ++it) {
+        const int slot = it % kRing;
+        const int ts = T.t_begin + (T.nsc - 1 - it) * kSub;
         const int nsub = min(kSub, T.t_end - ts);
-        if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
+        if (!ring_wait(R, it, T.nsc, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
-        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
-        LRS_SUB_DISPATCH(kd, fwd_maps_sub, sc, wre, wim, nsub, k0, k1, P0, P1, be0, be1);
+        const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
+        LRS_SUB_DISPATCH(kd, fwd_maps_sub, sc, wre, wim, nsub, k, P, be);
         __syncwarp();
-        if (lane == 0 && k + kRing < T.nsc)
-            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k - kRing) * kSub, T.b);
+        if (lane == 0 && it + kRing < T.nsc)
+            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - it - kRing) * kSub, T.b);
     }
-    if (active) {
-        float4* sm = a.smap + ((size_t)T.b * g.NS + T.s) * M + m;
-        sm[0] = make_float4(P0.x, P0.y, be0.x, be0.y);
-        sm[1] = make_float4(P1.x, P1.y, be1.x, be1.y);
-    }
+    if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, P, be);
 }
 
 // One CTA per chain: entry state of every segment from h0 and the segment
@@ -378,37 +402,33 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
-    ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
-    float2 z0 = make_float2(0.f, 0.f), z1 = z0;
-    if (active) {
-        k0 = load_mode(a.modes, a.nu, m);
-        k1 = load_mode(a.modes, a.nu, m + 1);
-        const float4 e = *reinterpret_cast<const float4*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m);
-        z0 = make_float2(e.x, e.y);
-        z1 = make_float2(e.z, e.w);
-    }
-    for (int k = 0; k < T.nsc; ++k) {
-        const int slot = k % kRing;
-        const int ts = T.t_begin + k * kSub;
+    const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    c2x z = czero();
+    if (active) z = load_c2(reinterpret_cast<const float*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m));
+    for (int it = 0; it < T.nsc; ++it) {
+        const int slot = it % kRing;
+        const int ts = T.t_begin + it * kSub;
         const int nsub = min(kSub, T.t_end - ts);
-        float4* hs = active ? reinterpret_cast<float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m) : nullptr;
-        if (active) hs[0] = make_float4(z0.x, z0.y, z1.x, z1.y);
-        float4* hmid = active ? hs + M / 2 : nullptr;   // slot ts/8 + 1
-        if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
+        // checkpoints: the state entering tokens ts and ts + 8, as pairs {re, im}
+        f2x* hs = active ? reinterpret_cast<f2x*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m) : nullptr;
+        if (active) {
+            hs[0] = z.re;
+            hs[1] = z.im;
+        }
+        f2x* hmid = active ? hs + M : nullptr;   // slot ts/8 + 1
+        if (!ring_wait(R, it, T.nsc, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         float* y32p = a.y32 != nullptr ? a.y32 + 2 * row0 : nullptr;
-        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
-        LRS_SUB_DISPATCH(kd, fwd_replay_sub, sc, wre, wim, nsub, k0, k1, z0, z1, a.y + row0, y32p, active, D / 2,
-                         M / 2, hmid);
+        const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
+        LRS_SUB_DISPATCH(kd, fwd_replay_sub, sc, wre, wim, nsub, k, z, a.y + row0, y32p, active, D / 2, M / 2, hmid);
         __syncwarp();
-        if (lane == 0 && k + kRing < T.nsc)
-            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (k + kRing) * kSub, T.b);
+        if (lane == 0 && it + kRing < T.nsc)
+            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
     }
-    if (active && T.t_end == L)
-        *reinterpret_cast<float4*>(a.hT + ((size_t)T.b * M + m) * 2) = make_float4(z0.x, z0.y, z1.x, z1.y);
+    if (active && T.t_end == L) store_c2(a.hT + ((size_t)T.b * M + m) * 2, z);
 }
 
 // ---------------------------------------------------------------------------
@@ -421,180 +441,23 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
 // before them: G o F_t = (Q conj(lambda_t), beta + Q conj(lambda_t) dy_t).
 template <bool FAST, bool SIMPLE>
 __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nsub,
-                                             const ModeConst& k0, const ModeConst& k1, float2& Q0, float2& Q1,
-                                             float2& be0, float2& be1) {
+                                             const ModePair& k, c2x& Q, c2x& be) {
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
         if (SIMPLE || i < nsub) {
-            const float4 ct = sc[i];
-            const float2 r = bf2_to_f2(gre[i * kWords]);
-            const float2 im = bf2_to_f2(gim[i * kWords]);
+            const Ctl2 ct = load_ctl(sc, i);
+            const uint32_t gr = gre[i * kWords], gi = gim[i * kWords];
             if (SIMPLE || !is_reset(ct)) {
-                Q0 = cmulc(samu_lambda<FAST>(k0, ct), Q0);
-                Q1 = cmulc(samu_lambda<FAST>(k1, ct), Q1);
-                be0 = cfma(Q0, make_float2(r.x, im.x), be0);
-                be1 = cfma(Q1, make_float2(r.y, im.y), be1);
+                Q = cmulc2(samu_lambda2<FAST>(k, ct), Q);
+                c2x gg;
+                gg.re = bf2x(gr);
+                gg.im = bf2x(gi);
+                be = cfma2(Q, gg, nbf2x(gi), be);
             } else {   // segment start: nothing reaches back past it
-                Q0 = make_float2(0.f, 0.f);
-                Q1 = Q0;
+                Q = czero();
             }
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// Reverse replay.  It walks each segment backwards in units of 8 tokens, the
-// distance between the forward's state checkpoints, through a ring of 8-row
-// items: for every unit the w rows (forward sweep) and then the dy rows
-// (reverse sweep).  The forward sweep keeps lambda_t and u_t = lambda_t z_{t-1}
-// of all 8 tokens in registers, so lambda is evaluated once per token.
-// ---------------------------------------------------------------------------
-constexpr int kRingH = 4;                                   // slots of the 8-row ring
-constexpr int kHalfItemBytes = 2 * kHalf * kRowBytes + kHalf * 16;
-
-struct alignas(128) WarpRingH {
-    uint32_t box[kRingH][2][kHalf][kWords];   // [slot][re, im][token][pair]
-    float4 ctrl[kRingH][kHalf];
-    uint64_t full[kRingH];
-};
-static_assert(sizeof(WarpRingH) <= sizeof(WarpRing), "the 8-row ring must fit the engine's shared memory");
-
-__device__ __forceinline__ void ringh_issue(WarpRingH& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
-                                            int x_re, int x_im, int ts, int b) {
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&R.full[slot], kHalfItemBytes);
-    tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
-    tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
-    tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
-}
-
-__device__ __forceinline__ bool ringh_wait(WarpRingH& R, int k, int n_items, uint32_t* status, int lane) {
-    if (mbar_wait_bounded(&R.full[k % kRingH], (uint32_t)(k / kRingH) & 1u)) return true;
-    if (lane == 0) atomicOr(status, kStatusTimeout);
-    for (int j = k + 1; j < k + kRingH && j < n_items; ++j)
-        mbar_wait_bounded(&R.full[j % kRingH], (uint32_t)(j / kRingH) & 1u);
-    return false;
-}
-
-// The sub_kind() facts for a unit of 8 tokens.
-__device__ __forceinline__ SubKind unit_kind(const float4* sc, int nh, int lane, const ModeConst& k0,
-                                             const ModeConst& k1) {
-    const float4 ct = sc[lane & (kHalf - 1)];
-    const bool mine = lane < nh;
-    const float e = mine ? fabsf(ct.x) : 0.f;
-    const float emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(e)));
-    const bool ok = fabsf(k0.nu) * emax < kPolyBound && fabsf(k1.nu) * emax < kPolyBound;
-    SubKind kd;
-    kd.fast = __all_sync(0xffffffffu, ok);
-    kd.simple = nh == kHalf && !__any_sync(0xffffffffu, mine && ct.w != 0.f);
-    return kd;
-}
-
-// Forward sweep of one unit from its entry state: lam_t = lambda_t and
-// u_t = lambda_t z_{t-1} (kept for kappa), z_t = u_t + b_t.  A reset token
-// gets lam_t = 0.
-template <bool FAST, bool SIMPLE>
-__device__ __forceinline__ void bwd_forward_unit(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nh,
-                                                 const ModeConst& k0, const ModeConst& k1, float2 z0, float2 z1,
-                                                 float4 (&u)[kHalf], float4 (&lam)[kHalf]) {
-#pragma unroll
-    for (int i = 0; i < kHalf; ++i) {
-        u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        lam[i] = u[i];
-        if (SIMPLE || i < nh) {
-            const float4 ct = sc[i];
-            const float2 br = bf2_to_f2(wre[i * kWords]);
-            const float2 bi = bf2_to_f2(wim[i * kWords]);
-            if (SIMPLE || !is_reset(ct)) {
-                const float2 l0 = samu_lambda<FAST>(k0, ct);
-                const float2 l1 = samu_lambda<FAST>(k1, ct);
-                float2 u0, u1;
-                z0 = step_state(l0, make_float2(br.x, bi.x), z0, &u0);
-                z1 = step_state(l1, make_float2(br.y, bi.y), z1, &u1);
-                u[i] = make_float4(u0.x, u0.y, u1.x, u1.y);
-                lam[i] = make_float4(l0.x, l0.y, l1.x, l1.y);
-            } else {
-                z0 = make_float2(br.x, bi.x);
-                z1 = make_float2(br.y, bi.y);
-            }
-        }
-    }
-}
-
-// Sums v[k] over the 32 lanes for every k of 16 values at once: halving
-// exchanges inside each 16-lane half, then one exchange across the halves.
-// On return lane L holds the total of v[L mod 16].  Fixed order.
-__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane) {
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int k = 0; k < o; ++k) {
-            const float send = up ? v[k] : v[k + o];
-            const float keep = up ? v[k + o] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
-}
-
-// Reverse sweep of one unit: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
-// kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa; per
-// token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64 modes
-// of the warp (written to kp[token * kp_row + {0, 1}]); then
-// A <- conj(lambda_t) A.
-template <bool SIMPLE>
-__device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nh,
-                                                 const ModeConst& k0, const ModeConst& k1, const float4 (&u)[kHalf],
-                                                 const float4 (&lam)[kHalf], float2& A0, float2& A1, float4& acc,
-                                                 uint32_t* dwb, float* dwf, bool fp32, bool active, size_t row,
-                                                 int half, float* kp, size_t kp_row, int lane) {
-    float v[2 * kHalf];
-#pragma unroll
-    for (int i = kHalf - 1; i >= 0; --i) {
-        v[2 * i] = 0.f;
-        v[2 * i + 1] = 0.f;
-        if (SIMPLE || i < nh) {
-            const float4 ct = sc[i];
-            const float2 g_r = bf2_to_f2(gre[i * kWords]);
-            const float2 g_i = bf2_to_f2(gim[i * kWords]);
-            A0 = make_float2(A0.x + g_r.x, A0.y + g_i.x);
-            A1 = make_float2(A1.x + g_r.y, A1.y + g_i.y);
-            if (active) {
-                if (fp32) {
-                    float* p = dwf + 2 * (size_t)i * row;
-                    __stcs(reinterpret_cast<float2*>(p), make_float2(A0.x, A1.x));
-                    __stcs(reinterpret_cast<float2*>(p + 2 * half), make_float2(A0.y, A1.y));
-                } else {
-                    uint32_t* p = dwb + (size_t)i * row;
-                    __stcs(p, f2_to_bf2(A0.x, A1.x));
-                    __stcs(p + half, f2_to_bf2(A0.y, A1.y));
-                }
-            }
-            if (SIMPLE || !is_reset(ct)) {
-                const float4 uu = u[i];
-                const float kr0 = __fmaf_rn(A0.x, uu.x, __fmul_rn(A0.y, uu.y));
-                const float ki0 = __fmaf_rn(A0.y, uu.x, -__fmul_rn(A0.x, uu.y));
-                const float kr1 = __fmaf_rn(A1.x, uu.z, __fmul_rn(A1.y, uu.w));
-                const float ki1 = __fmaf_rn(A1.y, uu.z, -__fmul_rn(A1.x, uu.w));
-                const float Et = 1.0f + ct.x;   // ct.x holds E - 1
-                acc.x = __fmaf_rn(-Et, kr0, acc.x);   // dnu_m
-                acc.y += ki0;                         // dtheta_m
-                acc.z = __fmaf_rn(-Et, kr1, acc.z);
-                acc.w += ki1;
-                v[2 * i] = ki0 + ki1;
-                v[2 * i + 1] = -__fmaf_rn(k0.nu, kr0, __fmul_rn(k1.nu, kr1));
-                const float4 l = lam[i];
-                A0 = cmulc(make_float2(l.x, l.y), A0);
-                A1 = cmulc(make_float2(l.z, l.w), A1);
-            } else {   // segment start: no controller terms, the adjoint stops here
-                A0 = make_float2(0.f, 0.f);
-                A1 = A0;
-            }
-        }
-    }
-    const float tot = warp_reduce_scatter16(v, lane);
-    if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
 }
 
 __global__ void __launch_bounds__(kEngineThreads, 6)
@@ -623,32 +486,26 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue(R, k, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
-    ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
-    if (active) {
-        k0 = load_mode(a.modes, a.nu, m);
-        k1 = load_mode(a.modes, a.nu, m + 1);
-    }
-    float2 Q0 = make_float2(1.f, 0.f), Q1 = Q0;
-    float2 be0 = make_float2(0.f, 0.f), be1 = be0;
-    for (int k = 0; k < T.nsc; ++k) {
-        const int slot = k % kRing;
-        const int ts = T.t_begin + k * kSub;
+    const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    c2x Q;
+    Q.re = dup2(1.f);
+    Q.im = 0ull;
+    c2x be = czero();
+    for (int it = 0; it < T.nsc; ++it) {
+        const int slot = it % kRing;
+        const int ts = T.t_begin + it * kSub;
         const int nsub = min(kSub, T.t_end - ts);
-        if (!ring_wait(R, k, T.nsc, a.status, lane)) return;
+        if (!ring_wait(R, it, T.nsc, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
         const uint32_t* gre = &R.box[slot][0][0][lane];
         const uint32_t* gim = &R.box[slot][1][0][lane];
-        const SubKind kd = sub_kind(sc, nsub, lane, k0, k1);
-        LRS_SUB_DISPATCH(kd, bwd_maps_sub, sc, gre, gim, nsub, k0, k1, Q0, Q1, be0, be1);
+        const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
+        LRS_SUB_DISPATCH(kd, bwd_maps_sub, sc, gre, gim, nsub, k, Q, be);
         __syncwarp();
-        if (lane == 0 && k + kRing < T.nsc)
-            ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (k + kRing) * kSub, T.b);
+        if (lane == 0 && it + kRing < T.nsc)
+            ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
     }
-    if (active) {
-        float4* sm = a.smap + ((size_t)T.b * g.NS + T.s) * M + m;
-        sm[0] = make_float4(Q0.x, Q0.y, be0.x, be0.y);
-        sm[1] = make_float4(Q1.x, Q1.y, be1.x, be1.y);
-    }
+    if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, Q, be);
 }
 
 // One CTA per chain: adjoint arriving at every segment's last token, from
@@ -742,6 +599,146 @@ __global__ void __launch_bounds__(kPrefixWarps * 32) samu_bwd_prefix_kernel(Samu
     }
 }
 
+// ---------------------------------------------------------------------------
+// Reverse replay.  It walks each segment backwards in units of 8 tokens, the
+// distance between the forward's state checkpoints, through a ring of 8-row
+// items: for every unit the w rows (forward sweep) and then the dy rows
+// (reverse sweep).  The forward sweep keeps lambda_t and u_t = lambda_t z_{t-1}
+// of all 8 tokens in registers, so lambda is evaluated once per token.
+// ---------------------------------------------------------------------------
+constexpr int kRingH = 4;                                   // slots of the 8-row ring
+constexpr int kHalfItemBytes = 2 * kHalf * kRowBytes + kHalf * kCtlBytes;
+
+struct alignas(128) WarpRingH {
+    uint32_t box[kRingH][2][kHalf][kWords];   // [slot][re, im][token][pair]
+    float4 ctrl[kRingH][2 * kHalf];
+    uint64_t full[kRingH];
+};
+static_assert(sizeof(WarpRingH) <= sizeof(WarpRing), "the 8-row ring must fit the engine's shared memory");
+
+__device__ __forceinline__ void ringh_issue(WarpRingH& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
+                                            int x_re, int x_im, int ts, int b) {
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&R.full[slot], kHalfItemBytes);
+    tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
+    tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
+    tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
+}
+
+__device__ __forceinline__ bool ringh_wait(WarpRingH& R, int k, int n_items, uint32_t* status, int lane) {
+    if (mbar_wait_bounded(&R.full[k % kRingH], (uint32_t)(k / kRingH) & 1u)) return true;
+    if (lane == 0) atomicOr(status, kStatusTimeout);
+    for (int j = k + 1; j < k + kRingH && j < n_items; ++j)
+        mbar_wait_bounded(&R.full[j % kRingH], (uint32_t)(j / kRingH) & 1u);
+    return false;
+}
+
+// Forward sweep of one unit from its entry state: lambda_t and
+// u_t = lambda_t z_{t-1} (kept for kappa), z_t = u_t + b_t.  A reset token
+// gets lambda_t = 0.
+template <bool FAST, bool SIMPLE>
+__device__ __forceinline__ void bwd_forward_unit(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nh,
+                                                 const ModePair& k, c2x z, c2x (&u)[kHalf], f2x (&lre)[kHalf],
+                                                 f2x (&lim)[kHalf]) {
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) {
+        u[i] = czero();
+        lre[i] = 0ull;
+        lim[i] = 0ull;
+        if (SIMPLE || i < nh) {
+            const Ctl2 ct = load_ctl(sc, i);
+            c2x bb;
+            bb.re = bf2x(wre[i * kWords]);
+            bb.im = bf2x(wim[i * kWords]);
+            if (SIMPLE || !is_reset(ct)) {
+                const Lam2 l = samu_lambda2<FAST>(k, ct);
+                u[i] = cmul2(l, z);
+                z.re = add2(u[i].re, bb.re);
+                z.im = add2(u[i].im, bb.im);
+                lre[i] = l.re;
+                lim[i] = l.im;
+            } else {
+                z = bb;
+            }
+        }
+    }
+}
+
+// Sums v[k] over the 32 lanes for every k of 16 values at once: halving
+// exchanges inside each 16-lane half, then one exchange across the halves.
+// On return lane L holds the total of v[L mod 16].  Fixed order.
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float send = up ? v[j] : v[j + o];
+            const float keep = up ? v[j + o] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Reverse sweep of one unit: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
+// kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa; per
+// token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64 modes
+// of the warp (written to kp[token * kp_row + {0, 1}]); then
+// A <- conj(lambda_t) A.
+template <bool SIMPLE>
+__device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nh,
+                                                 float nu0, float nu1, const c2x (&u)[kHalf],
+                                                 const f2x (&lre)[kHalf], const f2x (&lim)[kHalf], c2x& A,
+                                                 f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf, bool fp32,
+                                                 bool active, size_t row, int half, float* kp, size_t kp_row,
+                                                 int lane) {
+    float v[2 * kHalf];
+#pragma unroll
+    for (int i = kHalf - 1; i >= 0; --i) {
+        v[2 * i] = 0.f;
+        v[2 * i + 1] = 0.f;
+        if (SIMPLE || i < nh) {
+            const Ctl2 ct = load_ctl(sc, i);
+            A.re = add2(A.re, bf2x(gre[i * kWords]));
+            A.im = add2(A.im, bf2x(gim[i * kWords]));
+            if (active) {
+                if (fp32) {
+                    f2x* p = reinterpret_cast<f2x*>(dwf + 2 * (size_t)i * row);
+                    p[0] = A.re;
+                    p[half] = A.im;   // M floats further: the imaginary half
+                } else {
+                    uint32_t* p = dwb + (size_t)i * row;
+                    __stcs(p, x2bf(A.re));
+                    __stcs(p + half, x2bf(A.im));
+                }
+            }
+            if (SIMPLE || !is_reset(ct)) {
+                // kappa = A conj(u)
+                const f2x kr = fma2(A.re, u[i].re, mul2(A.im, u[i].im));
+                const f2x ki = fma2(A.im, u[i].re, mul2(sub2(0ull, A.re), u[i].im));
+                const f2x nE = sub2(dup2(-1.0f), ct.e);   // -E_t
+                acc_nu = fma2(nE, kr, acc_nu);
+                acc_th = add2(acc_th, ki);
+                float ki0, ki1, kr0, kr1;
+                up2(ki, ki0, ki1);
+                up2(kr, kr0, kr1);
+                v[2 * i] = ki0 + ki1;
+                v[2 * i + 1] = -__fmaf_rn(nu0, kr0, __fmul_rn(nu1, kr1));
+                Lam2 l;
+                l.re = lre[i];
+                l.im = lim[i];
+                l.nim = sub2(0ull, lim[i]);
+                A = cmulc2(l, A);
+            } else {   // segment start: no controller terms, the adjoint stops here
+                A = czero();
+            }
+        }
+    }
+    const float tot = warp_reduce_scatter16(v, lane);
+    if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
+}
+
 __global__ void __launch_bounds__(kEngineThreads, 4)
     samu_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_ctrl, SamuScanBwdArgs a) {
@@ -773,60 +770,62 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     if (lane == 0)
         for (int k = 0; k < kRingH && k < n_items; ++k)
             ringh_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
-    ModeConst k0 = {0.f, 0.f, 0.f, 0.f, 0.f}, k1 = k0;
-    float2 A0 = make_float2(0.f, 0.f), A1 = A0;
-    if (active) {
-        k0 = load_mode(a.modes, a.nu, m);
-        k1 = load_mode(a.modes, a.nu, m + 1);
-        const float4 e = *reinterpret_cast<const float4*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m);
-        A0 = make_float2(e.x, e.y);
-        A1 = make_float2(e.z, e.w);
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // dnu_m, dtheta_m, dnu_m+1, dtheta_m+1
+    const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    float nu0, nu1;
+    up2(k.nu, nu0, nu1);
+    c2x A = czero();
+    if (active) A = load_c2(reinterpret_cast<const float*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m));
+    f2x acc_nu = 0ull, acc_th = 0ull;
     const bool fp32 = a.grad_fp32 != 0;
-    for (int k = 0; k < n_items; k += 2) {
-        const int ts = item_ts(k);
+    for (int it = 0; it < n_items; it += 2) {
+        const int ts = item_ts(it);
         const int nh = min(kHalf, T.t_end - ts);
-        float2 z0 = make_float2(0.f, 0.f), z1 = z0;
+        c2x z = czero();
         if (active) {
-            const float4 hv = *reinterpret_cast<const float4*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m);
-            z0 = make_float2(hv.x, hv.y);
-            z1 = make_float2(hv.z, hv.w);
+            const f2x* hs = reinterpret_cast<const f2x*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m);
+            z.re = hs[0];
+            z.im = hs[1];
         }
         // w item: forward sweep
-        int slot = k % kRingH;
-        if (!ringh_wait(R, k, n_items, a.status, lane)) return;
+        int slot = it % kRingH;
+        if (!ringh_wait(R, it, n_items, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
-        const SubKind kd = unit_kind(sc, nh, lane, k0, k1);
-        float4 u[kHalf], lam[kHalf];
-        LRS_SUB_DISPATCH(kd, bwd_forward_unit, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k0, k1,
-                         z0, z1, u, lam);
+        const SubKind kd = sub_kind<kHalf>(sc, nh, lane, k);
+        c2x u[kHalf];
+        f2x lre[kHalf], lim[kHalf];
+        LRS_SUB_DISPATCH(kd, bwd_forward_unit, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k, z, u,
+                         lre, lim);
         __syncwarp();
-        if (lane == 0 && k + kRingH < n_items)
-            ringh_issue(R, slot, ((k + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k + kRingH), T.b);
+        if (lane == 0 && it + kRingH < n_items)
+            ringh_issue(R, slot, ((it + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(it + kRingH),
+                        T.b);
         // dy item: reverse sweep
-        slot = (k + 1) % kRingH;
-        if (!ringh_wait(R, k + 1, n_items, a.status, lane)) return;
+        slot = (it + 1) % kRingH;
+        if (!ringh_wait(R, it + 1, n_items, a.status, lane)) return;
         sc = R.ctrl[slot];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
         float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
         float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
         if (kd.simple)
-            bwd_reverse_unit<true>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k0, k1, u, lam, A0, A1,
-                                   acc, dwb, dwf, fp32, active, D / 2, M / 2, kp, 2 * (size_t)g.n_groups, lane);
+            bwd_reverse_unit<true>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre, lim,
+                                   A, acc_nu, acc_th, dwb, dwf, fp32, active, D / 2, M / 2, kp,
+                                   2 * (size_t)g.n_groups, lane);
         else
-            bwd_reverse_unit<false>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k0, k1, u, lam, A0,
-                                    A1, acc, dwb, dwf, fp32, active, D / 2, M / 2, kp, 2 * (size_t)g.n_groups, lane);
+            bwd_reverse_unit<false>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre,
+                                    lim, A, acc_nu, acc_th, dwb, dwf, fp32, active, D / 2, M / 2, kp,
+                                    2 * (size_t)g.n_groups, lane);
         __syncwarp();
-        if (lane == 0 && k + 1 + kRingH < n_items)
-            ringh_issue(R, slot, ((k + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
-                        item_ts(k + 1 + kRingH), T.b);
+        if (lane == 0 && it + 1 + kRingH < n_items)
+            ringh_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
+                        item_ts(it + 1 + kRingH), T.b);
     }
     if (active) {
-        *reinterpret_cast<float4*>(a.numod + ((size_t)T.b * g.NS + T.s) * M + m) = acc;
-        if (T.s == 0)
-            *reinterpret_cast<float4*>(a.dh0 + ((size_t)T.b * M + m) * 2) = make_float4(A0.x, A0.y, A1.x, A1.y);
+        float n0, n1, t0, t1;
+        up2(acc_nu, n0, n1);
+        up2(acc_th, t0, t1);
+        *reinterpret_cast<float4*>(a.numod + ((size_t)T.b * g.NS + T.s) * M + m) = make_float4(n0, t0, n1, t1);
+        if (T.s == 0) store_c2(a.dh0 + ((size_t)T.b * M + m) * 2, A);
     }
 }
 

@@ -40,18 +40,27 @@ struct CtrlSmem {
     uint64_t* empty;    // backward: slot consumed (consumers)
 };
 
-__host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D) {
-    return (size_t)cg.ring * cg.stage_tok * 2 * D;
+// Bytes between consecutive x_sel rows in a ring slot: the backward keeps
+// rows packed; the forward pads each row by 16 bytes so that the eight rows
+// an ldmatrix reads fall in distinct banks.
+__host__ __device__ inline size_t ctrl_row_bytes(int D, bool backward) { return 2 * (size_t)D + (backward ? 0 : 16); }
+
+__host__ __device__ inline size_t ctrl_slot_bytes(const CtrlGeom& cg, int D, bool backward) {
+    return (size_t)cg.stage_tok * ctrl_row_bytes(D, backward);
+}
+
+__host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D, bool backward) {
+    return (size_t)cg.ring * ctrl_slot_bytes(cg, D, backward);
 }
 
 __host__ __device__ inline size_t ctrl_xbuf_bytes(const CtrlGeom& cg, bool backward) {
-    return backward ? (size_t)cg.max_cta_tok * 8 : (size_t)cg.ring * cg.consumers * 32 * 4;
+    return backward ? (size_t)cg.max_cta_tok * 8 : (size_t)cg.ring * cg.consumers * 32 * 16;
 }
 
 __device__ __forceinline__ CtrlSmem ctrl_smem(uint8_t* base, const CtrlGeom& cg, int D, bool backward) {
     CtrlSmem sm;
     sm.ring = base;
-    const size_t rb = ctrl_ring_bytes(cg, D);
+    const size_t rb = ctrl_ring_bytes(cg, D, backward);
     sm.xbuf = reinterpret_cast<float*>(base + rb);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + rb + ((ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15)));
     sm.full = bars;
@@ -66,36 +75,21 @@ __device__ __forceinline__ void ctrl_stage_range(const CtrlGeom& cg, int cta, lo
     s1 = cg.n_stages * (cta + 1) / cg.n_ctas;
 }
 
-// Producer lane 0: the rows of stage (token t0, n tokens) into ring slot `slot`.
+// Producer lane 0: the rows of stage (token t0, n tokens) into ring slot
+// `slot`, as one bulk copy (packed rows) or one per row (padded rows).
 __device__ __forceinline__ void ctrl_issue(const CtrlSmem& sm, int slot, const uint4* x, long long t0, int n, int D,
-                                           const CtrlGeom& cg) {
-    const uint32_t bytes = (uint32_t)n * 2u * (uint32_t)D;
-    uint8_t* dst = sm.ring + (size_t)slot * cg.stage_tok * 2 * D;
+                                           const CtrlGeom& cg, bool backward) {
+    const uint32_t row = 2u * (uint32_t)D;
+    uint8_t* dst = sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D, backward);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(x) + (size_t)t0 * row;
     fence_proxy_async();
-    mbar_arrive_expect_tx(&sm.full[slot], bytes);
-    bulk_load(dst, reinterpret_cast<const uint8_t*>(x) + (size_t)t0 * 2 * D, bytes, &sm.full[slot]);
-}
-
-// Sums v[k] over the 32 lanes for every k at once (V = 16 or 32 values):
-// on return lane L holds the total of v[L mod V].  Fixed order.
-template <int V>
-__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
-#pragma unroll
-    for (int o = 16; o >= V; o >>= 1) {   // plain butterfly while there are fewer values than lanes
-#pragma unroll
-        for (int k = 0; k < V; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
+    if (backward) {
+        bulk_load(dst, src, (uint32_t)n * row, &sm.full[slot]);
+    } else {
+        const size_t pitch = ctrl_row_bytes(D, false);
+        for (int i = 0; i < n; ++i) bulk_load(dst + (size_t)i * pitch, src + (size_t)i * row, row, &sm.full[slot]);
     }
-#pragma unroll
-    for (int o = V / 2; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int k = 0; k < o; ++k) {
-            const float send = up ? v[k] : v[k + o];
-            const float keep = up ? v[k + o] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    return v[0];
 }
 
 __device__ __forceinline__ void unpack8(const uint4 q, float (&x)[8]) {
@@ -123,49 +117,104 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 //    transition constant lbar_m = e^{-nu_m} e^{i theta_m} as a double-float
 //    (hi, lo) in FP64.
 //  - Streaming CTAs: the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
-//    fixed-order tree, the same in every CTA); consumers form their 16 partial
-//    dot products per token, reduce-scatter them over the warp and leave one
-//    (token, phi or r) partial per lane; the producer adds the consumers'
-//    partials in a fixed order and evaluates p = tanh(s_phi), r = tanh(s_r),
-//    q(r), d, c, and E - 1 = expm1(c), C = cos d, S = sin d, 16 tokens per
-//    stage in parallel.  The first streaming CTA stores w_hat and the
-//    amplitude factors for the backward.
+//    fixed-order tree, the same in every CTA).  The dot products x~ . w_hat of
+//    a stage of 16 tokens are one tensor-core contraction [16 tokens x D] x
+//    [D x 8]: consumer warp c takes the 16-channel k-steps 16c .. 16c+15
+//    (mma.sync m16n8k16, BF16 operands, FP32 accumulation), A is the x_sel
+//    rows in shared memory (ldmatrix), B holds per channel the exact
+//    three-way BF16 split w_hat = hi + mid + lo of both directions in columns
+//    0-2 (phi) and 3-5 (r), so each product is exact and the sum is FP32.
+//    The producer adds the consumers' partial tiles and the three split
+//    columns in a fixed order and evaluates p = tanh(s_phi), r = tanh(s_r),
+//    q(r), d, c, and E - 1 = expm1(c), C = cos d, S = sin d, one token per
+//    lane.  The first streaming CTA stores w_hat and the amplitude factors
+//    for the backward.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// c += A B for one m16n8k16 tile (BF16 A row-major, B column-major, FP32 c).
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// w = hi + mid + lo with each part a BF16 value (exactly, up to 2^-24 |w|):
+// every subtraction is exact.  part 0, 1 or 2.
+__device__ __forceinline__ float bf16_part(float w, int part) {
+    const float h = __bfloat162float(__float2bfloat16_rn(w));
+    if (part == 0) return h;
+    const float r1 = w - h;
+    const float m = __bfloat162float(__float2bfloat16_rn(r1));
+    if (part == 1) return m;
+    return __bfloat162float(__float2bfloat16_rn(r1 - m));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) { return f2_to_bf2(lo, hi); }
+
+constexpr int kCtrlKMax = 16;   // k-steps (16 channels each) per consumer warp
+
 template <int N>
 __device__ __forceinline__ void ctrl_fwd_consumer(const SamuCtrlFwdArgs& a, const CtrlSmem& sm, long long s0,
-                                                  long long s1, int cw, int lane, const float (&wp)[8],
-                                                  const float (&wr)[8], bool col_ok) {
+                                                  long long s1, int cw, int lane, float inv_phi, float inv_r) {
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
-    const int v_idx = 32 * cw + lane;
+    const int ks0 = kCtrlKMax * cw;
+    const int nk = min(kCtrlKMax, D / 16 - ks0);
+    // B fragments: thread (g, t) holds column n = g at k = 2t, 2t+1 (b0) and
+    // 2t+8, 2t+9 (b1) of every k-step
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t bf[kCtrlKMax][2];
+#pragma unroll
+    for (int j = 0; j < kCtrlKMax; ++j) {
+        bf[j][0] = 0u;
+        bf[j][1] = 0u;
+        if (j < nk && g < 6) {
+            const float* w = g < 3 ? a.w_phi : a.w_r;
+            const float inv = g < 3 ? inv_phi : inv_r;
+            const int part = g % 3;
+            const int c0 = 16 * (ks0 + j) + 2 * t;
+            bf[j][0] = pack_bf16(bf16_part(w[c0] * inv, part), bf16_part(w[c0 + 1] * inv, part));
+            bf[j][1] = pack_bf16(bf16_part(w[c0 + 8] * inv, part), bf16_part(w[c0 + 9] * inv, part));
+        }
+    }
+    const uint32_t pitch = (uint32_t)ctrl_row_bytes(D, false);
+    // ldmatrix row of this lane: token lane % 16 (rows past the stage's
+    // token count repeat earlier rows; their results are not used), channel
+    // half lane / 16 of each k-step
+    const uint32_t lane_off = (uint32_t)((lane & 15) % N) * pitch + (uint32_t)(lane >> 4) * 16u;
+    float4* xb = reinterpret_cast<float4*>(sm.xbuf);
     for (long long st = s0; st < s1; ++st) {
         const int k = (int)(st - s0);
         const int slot = k % cg.ring;
-        const long long t0 = st * N;
-        const int n = (int)min((long long)N, a.BL - t0);
         if (!mbar_wait_bounded(&sm.full[slot], (uint32_t)(k / cg.ring) & 1u)) {
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
             return;
         }
-        const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
-        float v[2 * N];
+        const uint32_t base = smem_u32(sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D, false)) + lane_off;
+        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            float ap = 0.f, ar = 0.f;
-            if (col_ok && i < n) {
-                float x[8];
-                unpack8(rows[(size_t)i * (D / 8) + v_idx], x);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    ap = fmaf(x[c], wp[c], ap);
-                    ar = fmaf(x[c], wr[c], ar);
-                }
+        for (int j = 0; j < kCtrlKMax; j += 2) {
+            if (j < nk) {
+                uint32_t fa[4];
+                ldsm_x4(base + (uint32_t)(ks0 + j) * 32u, fa);
+                mma_16816(ce, fa, bf[j][0], bf[j][1]);
             }
-            v[2 * i] = ap;
-            v[2 * i + 1] = ar;
+            if (j + 1 < nk) {
+                uint32_t fa[4];
+                ldsm_x4(base + (uint32_t)(ks0 + j + 1) * 32u, fa);
+                mma_16816(co, fa, bf[j + 1][0], bf[j + 1][1]);
+            }
         }
-        const float tot = warp_reduce_scatter<2 * N>(v, lane);
-        sm.xbuf[((size_t)slot * cg.consumers + cw) * 32 + lane] = tot;
+        xb[((size_t)slot * cg.consumers + cw) * 32 + lane] =
+            make_float4(ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.ready[slot]);
     }
@@ -177,10 +226,16 @@ __device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, cons
                                                   float k_r) {
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
-    constexpr int V = 2 * N;
     if (lane == 0)
         for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st)
-            ctrl_issue(sm, (int)(st - s0), a.x, st * N, (int)min((long long)N, a.BL - st * N), D, cg);
+            ctrl_issue(sm, (int)(st - s0), a.x, st * N, (int)min((long long)N, a.BL - st * N), D, cg, false);
+    const float4* xb = reinterpret_cast<const float4*>(sm.xbuf);
+    // token i = lane (i < N): row i of the partial tiles is held by lanes
+    // 4 (i mod 8) + {0, 1, 2} (columns {0,1}, {2,3}, {4,5}), in the first two
+    // values for rows 0-7 and the last two for rows 8-15
+    const int i = lane;
+    const int src = 4 * (i & 7);
+    const bool upper = (i & 8) != 0;
     for (long long st = s0; st < s1; ++st) {
         const int k = (int)(st - s0);
         const int slot = k % cg.ring;
@@ -190,15 +245,23 @@ __device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, cons
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
             return;
         }
-        float tot = 0.f;
-        for (int c = 0; c < cg.consumers; ++c) tot += sm.xbuf[((size_t)slot * cg.consumers + c) * 32 + (lane & (V - 1))];
+        float s_phi = 0.f, s_r = 0.f;
+        if (i < N) {
+            for (int c = 0; c < cg.consumers; ++c) {
+                const float4* tile = xb + ((size_t)slot * cg.consumers + c) * 32 + src;
+                const float4 p01 = tile[0], p23 = tile[1], p45 = tile[2];
+                const float c0 = upper ? p01.z : p01.x, c1 = upper ? p01.w : p01.y;
+                const float c2 = upper ? p23.z : p23.x, c3 = upper ? p23.w : p23.y;
+                const float c4 = upper ? p45.z : p45.x, c5 = upper ? p45.w : p45.y;
+                s_phi += (c0 + c1) + c2;
+                s_r += (c3 + c4) + c5;
+            }
+        }
         __syncwarp();
         const long long nxt = st + cg.ring;
-        if (lane == 0 && nxt < s1) ctrl_issue(sm, slot, a.x, nxt * N, (int)min((long long)N, a.BL - nxt * N), D, cg);
-        const float s_phi = __shfl_sync(0xffffffffu, tot, lane & ~1);
-        const float s_r = __shfl_sync(0xffffffffu, tot, lane | 1);
-        const int i = lane >> 1;
-        if ((lane & 1) == 0 && lane < V && i < n) {
+        if (lane == 0 && nxt < s1)
+            ctrl_issue(sm, slot, a.x, nxt * N, (int)min((long long)N, a.BL - nxt * N), D, cg, false);
+        if (i < n) {
             const long long t = t0 + i;
             const float p = tanhf(s_phi + bias_p);
             const float r = tanhf(s_r + bias_r);
@@ -294,18 +357,10 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrl
         else
             ctrl_fwd_producer<8>(a, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
     } else {
-        const int v_idx = 32 * (warp - 1) + lane;
-        const bool col_ok = v_idx < D / 8;
-        float wp[8], wr[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            wp[c] = col_ok ? a.w_phi[8 * v_idx + c] * inv_phi : 0.f;
-            wr[c] = col_ok ? a.w_r[8 * v_idx + c] * inv_r : 0.f;
-        }
         if (cg.stage_tok == 16)
-            ctrl_fwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, wp, wr, col_ok);
+            ctrl_fwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, inv_phi, inv_r);
         else
-            ctrl_fwd_consumer<8>(a, sm, s0, s1, warp - 1, lane, wp, wr, col_ok);
+            ctrl_fwd_consumer<8>(a, sm, s0, s1, warp - 1, lane, inv_phi, inv_r);
     }
 }
 
@@ -337,7 +392,7 @@ __device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, cons
             atomicOr(a.status, kStatusTimeout);
             return;
         }
-        ctrl_issue(sm, slot, a.x, t0, n, D, cg);
+        ctrl_issue(sm, slot, a.x, t0, n, D, cg, true);
     }
 }
 
@@ -663,7 +718,7 @@ CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
     // stages of 16 tokens (8 when 16 rows exceed 64 KB), as many slots as fit
     // in kCtrlRingBytes
     cg.stage_tok = 2 * D * 16 <= 64 * 1024 ? 16 : 8;
-    int ring = (int)(kCtrlRingBytes / ((size_t)cg.stage_tok * 2 * D));
+    int ring = (int)(kCtrlRingBytes / ((size_t)cg.stage_tok * ctrl_row_bytes(D, backward)));
     if (ring > kCtrlRingMax) ring = kCtrlRingMax;
     if (ring < 2) ring = 2;
     cg.ring = ring;
@@ -676,7 +731,7 @@ CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
         cg.max_cta_tok = (int)((cg.n_stages + fewest - 1) / fewest * cg.stage_tok);
     }
     const size_t xb = (ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15);
-    cg.smem = (int)(ctrl_ring_bytes(cg, D) + xb + 3 * cg.ring * sizeof(uint64_t));
+    cg.smem = (int)(ctrl_ring_bytes(cg, D, backward) + xb + 3 * cg.ring * sizeof(uint64_t));
     int per_sm = (int)((227 * 1024) / (cg.smem + 1024));
     const int by_threads = 2048 / cg.threads;
     if (per_sm > by_threads) per_sm = by_threads;

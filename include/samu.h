@@ -88,8 +88,7 @@ int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
  * capacity) kernels, their id (2 controller forward, 3 SAMU forward replay,
  * 4 SAMU backward main, 5 controller backward, 6 SAMU parameter reductions,
  * 7 RG-LRU scan forward, 8 RG-LRU scan backward, 9 RG-LRU alpha reduction,
- * 10 SAMU forward maps, 11 SAMU backward maps, 12 SAMU forward prefix,
- * 13 SAMU backward prefix) and duration in milliseconds; *count receives the number of
+ * 10 SAMU forward maps, 11 SAMU backward maps) and duration in milliseconds; *count receives the number of
  * kernels launched while profiling was on.  Not thread-safe: one profiling
  * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),
  * LRS_ERR_CUDA. */

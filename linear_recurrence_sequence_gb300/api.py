@@ -299,8 +299,7 @@ KERNEL_NAMES = {
     2: "samu_ctrl_fwd_kernel", 3: "samu_fwd_replay_kernel",
     4: "samu_bwd_main_kernel", 5: "samu_ctrl_bwd_kernel", 6: "samu_params_kernel",
     7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
-    10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel", 12: "samu_fwd_prefix_kernel",
-    13: "samu_bwd_prefix_kernel",
+    10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel",
 }
 
 

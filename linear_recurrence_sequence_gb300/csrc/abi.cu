@@ -73,7 +73,7 @@ bool pdl_ok() { return !g_prof.on; }
 enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
     KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
-    KID_SAMU_BWD_MAPS, KID_SAMU_FWD_PREFIX, KID_SAMU_BWD_PREFIX
+    KID_SAMU_BWD_MAPS
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -210,6 +210,8 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.misc = misc;
     cf.modes = modes;
     cf.status = at<uint32_t>(scratch, sc.status);
+    cf.counters = at<uint32_t>(scratch, sc.counters);   // the forward's half
+    cf.n_counters = samu_seg_geom(B, L, M, 0).n_chains;
     LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream, false));
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
@@ -225,10 +227,11 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     a.hT = hT;
     a.hsub = at<float2>(saved, sv.hsub);
     a.smap = at<float4>(scratch, sc.smap);
-    a.sent = at<float2>(scratch, sc.sent);
+    a.cmap = at<float4>(scratch, sc.cmap);
+    a.cent = at<float2>(scratch, sc.cent);
+    a.counters = at<uint32_t>(scratch, sc.counters);
     a.status = at<uint32_t>(scratch, sc.status);
     LRS_LAUNCH(KID_SAMU_FWD_MAPS, stream, launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream, pdl_ok()));
-    LRS_LAUNCH(KID_SAMU_FWD_PREFIX, stream, launch_samu_fwd_prefix(a, stream, pdl_ok()));
     LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream, pdl_ok()));
     return LRS_OK;
 }
@@ -259,6 +262,8 @@ int samu_backward(const void* dy, const float* dhT,
     const int fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
 
     const float4* ctrl = at<float4>(saved, sv.ctrl);
+    // status word, parameter-reduction counter and the chain arrival counters start at zero
+    if (cudaMemsetAsync(scratch, 0, sc.zero_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     // 16-row boxes for the adjoint maps, 8-row boxes for the reverse replay
     CUtensorMap tm_dy, tm_ctrl, tm_dy8, tm_w8, tm_ctrl8;
     if (!make_bf16_map(&tm_dy, dy, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub) ||
@@ -275,12 +280,13 @@ int samu_backward(const void* dy, const float* dhT,
     s.grad_fp32 = fp32;
     s.dh0 = dh0;
     s.smap = at<float4>(scratch, sc.smap);
-    s.sent = at<float2>(scratch, sc.sent);
+    s.cmap = at<float4>(scratch, sc.cmap);
+    s.cent = at<float2>(scratch, sc.cent);
+    s.counters = at<uint32_t>(scratch, sc.counters) + g.n_chains;
     s.kpart = at<float2>(scratch, sc.kpart);
     s.numod = at<float2>(scratch, sc.numod);
     s.status = at<uint32_t>(scratch, sc.status);
     LRS_LAUNCH(KID_SAMU_BWD_MAPS, stream, launch_samu_bwd_maps(tm_dy, tm_ctrl, s, stream, false));
-    LRS_LAUNCH(KID_SAMU_BWD_PREFIX, stream, launch_samu_bwd_prefix(s, stream, pdl_ok()));
     LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy8, tm_w8, tm_ctrl8, s, stream, pdl_ok()));
 
     SamuCtrlBwdArgs cb;

@@ -193,9 +193,11 @@ struct SamuScanFwdArgs {
     uint32_t* y;            // BF16 pairs of y
     float* y32;             // optional
     float* hT;              // [B,M,2]
-    float2* hsub;           // [B][CS][M] entry state of every 16-token sub-chunk
+    float2* hsub;           // [B][CS][M] the state every 8 tokens
     float4* smap;           // [B][NS][M] segment maps
-    float2* sent;           // [B][NS][M] segment entry states
+    float4* cmap;           // [B][NC][M] CTA maps (four consecutive segments)
+    float2* cent;           // [B][NC][M] CTA entry states
+    uint32_t* counters;     // [n_chains] arrivals of the maps CTAs, zero on entry, left zero
     uint32_t* status;       // cleared by the maps kernel
 };
 
@@ -212,7 +214,9 @@ struct SamuScanBwdArgs {
     int grad_fp32;
     float* dh0;             // [B,M,2]
     float4* smap;           // [B][NS][M] adjoint segment maps
-    float2* sent;           // [B][NS][M] incoming adjoints
+    float4* cmap;           // [B][NC][M] adjoint CTA maps
+    float2* cent;           // [B][NC][M] adjoints arriving at each CTA's last token
+    uint32_t* counters;     // [n_chains] arrivals of the maps CTAs, zero on entry, left zero
     float2* kpart;          // [B*L][n_groups] {sum Im kappa, sum -nu Re kappa}
     float2* numod;          // [B][NS][M] {dnu, dtheta} per segment
     uint32_t* status;
@@ -291,6 +295,8 @@ struct SamuCtrlFwdArgs {
     float* wh;                     // [2][D+1]
     float* misc;
     float4* modes;                 // [M] lbar hi/lo
+    uint32_t* counters;            // [n_counters] chain arrival counters of the forward scan, zeroed here
+    int n_counters;
     uint32_t* status;
 };
 
@@ -298,18 +304,17 @@ cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s, bo
 // Segment geometry of the forward (backward = false) or backward scan on the
 // current device: every segment of every chain resident at once.
 SegGeom samu_scan_geom(int B, int L, int M, bool backward);
-// Forward: maps (w read backwards in time), prefix, replay (forwards).
+// Forward: maps (w read backwards in time; the last CTA of each chain folds
+// the chain's CTA maps into entry states), replay (forwards).
 // pdl: launch as a programmatic dependent of the previous kernel on s.
 cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
                                  cudaStream_t s, bool pdl);
-cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
                                    cudaStream_t s, bool pdl);
-// Backward: maps (dy read forwards in time, 16-row boxes), prefix, main
-// (backwards, 8-row boxes).
+// Backward: maps (dy read forwards in time, 16-row boxes; the last CTA of
+// each chain folds the adjoint CTA maps), main (backwards, 8-row boxes).
 cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
                                  cudaStream_t s, bool pdl);
-cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
                                  const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl);

@@ -65,12 +65,18 @@ struct SegGeom {
     int B, L, M;
     int n_groups, n_chains;
     int seg;               // tokens per segment
-    int NS;                // segments per chain
+    int NS;                // segments per chain (a multiple of kSegPerCta)
+    int NC;                // CTAs per chain, NS / kSegPerCta
     int NSmax;             // bound on NS for this (B, L, M) on any device
     int CS;                // state checkpoints per batch row (slot = t / 8)
 };
 
+// Segments (warps) per CTA of the scan engine; the segments of a CTA are
+// consecutive segments of one chain.
+constexpr int kSegPerCta = 8;
+
 inline int round_up16(long long v) { return (int)((v + kSub - 1) / kSub * kSub); }
+inline int round_up_cta(long long v) { return (int)((v + kSegPerCta - 1) / kSegPerCta * kSegPerCta); }
 
 // seg_min: the shortest segment any device may use for this problem.
 inline int seg_min_tokens(int L, int n_chains) {
@@ -80,6 +86,8 @@ inline int seg_min_tokens(int L, int n_chains) {
 }
 
 // Segment geometry for `warps` resident warps (warps <= 0: the bound only).
+// Segments past the end of the sequence (NS is rounded up to whole CTAs) are
+// empty.
 inline SegGeom samu_seg_geom(int B, int L, int M, long long warps) {
     SegGeom g;
     g.B = B;
@@ -88,16 +96,18 @@ inline SegGeom samu_seg_geom(int B, int L, int M, long long warps) {
     g.n_groups = (M + kGroup - 1) / kGroup;
     g.n_chains = B * g.n_groups;
     const int smin = seg_min_tokens(L, g.n_chains);
-    g.NSmax = (L + smin - 1) / smin;
+    g.NSmax = round_up_cta((L + smin - 1) / smin);
     int seg = smin;
     if (warps > 0) {
-        const long long per_chain = warps / g.n_chains;     // segments per chain that fit at once
-        const long long want = per_chain >= 1 ? ((long long)L + per_chain - 1) / per_chain : L;
-        seg = round_up16(want);
+        // whole CTAs of segments per chain that fit at once
+        const long long per_chain = warps / g.n_chains / kSegPerCta * kSegPerCta;
+        const long long parts = per_chain >= kSegPerCta ? per_chain : kSegPerCta;
+        seg = round_up16(((long long)L + parts - 1) / parts);
         if (seg < smin) seg = smin;
     }
     g.seg = seg;
-    g.NS = (L + seg - 1) / seg;
+    g.NS = round_up_cta((L + seg - 1) / seg);
+    g.NC = g.NS / kSegPerCta;
     g.CS = (L + kHalf - 1) / kHalf + 1;
     return g;
 }
@@ -131,7 +141,8 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
 }
 
 struct SamuScratch {
-    size_t status, smap, sent, kpart, numod, dwh_part, amp_part, dwh, total;
+    size_t status, counters, smap, cmap, cent, kpart, numod, dwh_part, amp_part, dwh, total;
+    size_t zero_bytes;     // status block + counters: cleared at the start of a backward call
 };
 
 inline SamuScratch samu_scratch_layout(int B, int L, int D) {
@@ -141,9 +152,14 @@ inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     const size_t rows = (size_t)B * g.NSmax * M;
     SamuScratch s;
     size_t o = 0;
-    s.status = o;   o = align_up(o + kStatusBlock);
+    s.status = o;   o += kStatusBlock;
+    s.counters = o; o += (size_t)2 * g.n_chains * 4;                   // chain arrivals (forward, backward)
+    s.zero_bytes = o;
+    o = align_up(o);
+    const size_t crows = (size_t)B * (g.NSmax / kSegPerCta) * M;
     s.smap = o;     o = align_up(o + rows * 16);                      // segment maps
-    s.sent = o;     o = align_up(o + rows * 8);                       // segment entry states / adjoints
+    s.cmap = o;     o = align_up(o + crows * 16);                     // CTA maps (4 segments)
+    s.cent = o;     o = align_up(o + crows * 8);                      // CTA entry states / incoming adjoints
     s.kpart = o;    o = align_up(o + BL * g.n_groups * 8);            // per-token controller partials
     s.numod = o;    o = align_up(o + rows * 8);                       // per-segment (dnu, dtheta)
     s.dwh_part = o; o = align_up(o + (size_t)kCtrlRowsMax * 2 * (D + 1) * 4);   // one row per CTA

@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrl
             a.wh[j] = a.w_phi[j] * inv_phi;
             a.wh[n + j] = a.w_r[j] * inv_r;
         }
+        for (int j = tid; j < a.n_counters; j += blockDim.x) a.counters[j] = 0u;
         if (tid == 0) {
             a.misc[0] = k_phi;
             a.misc[1] = k_r;

@@ -34,14 +34,14 @@
 
 namespace lrs {
 
-constexpr int kEngineWarps = 4;                     // warps per CTA (each on its own segment)
+constexpr int kEngineWarps = 8;                     // warps per CTA (each on its own segment)
 constexpr int kEngineThreads = kEngineWarps * 32;
 constexpr int kRing = 2;                            // staging slots per warp
 constexpr int kWords = kGroup / 2;                  // BF16 pairs per box row
 constexpr int kBoxBytes = kSub * kRowBytes;         // one [16 x 64] BF16 box: 2 KB
 constexpr int kCtlBytes = 32;                       // one token's control word (two float4)
 constexpr int kItemBytes = 2 * kBoxBytes + kSub * kCtlBytes;   // re box + im box + control words
-constexpr int kPrefixWarps = 16;
+static_assert(kEngineWarps == kSegPerCta, "a CTA holds the segments of one chain");
 
 // One warp's staging ring.  Every TMA destination starts on a 128-byte
 // boundary (box sizes are multiples of 128 bytes).
@@ -67,7 +67,7 @@ __device__ __forceinline__ SegTask seg_task(const SegGeom& g, long long gw) {
     T.grp = chain % g.n_groups;
     T.t_begin = T.s * g.seg;
     T.t_end = min(g.L, T.t_begin + g.seg);
-    T.nsc = (T.t_end - T.t_begin + kSub - 1) / kSub;
+    T.nsc = T.t_end > T.t_begin ? (T.t_end - T.t_begin + kSub - 1) / kSub : 0;   // 0: a segment past L
     return T;
 }
 
@@ -240,7 +240,100 @@ __device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t*
     }
 }
 
-__global__ void __launch_bounds__(kEngineThreads, 6)
+// ---------------------------------------------------------------------------
+// Chain prefix, run at the end of the maps kernel by the CTA that finishes a
+// chain last (its arrival makes the counter reach NC).  Its kEngineWarps
+// warps take equal ranges of the chain's NC CTA maps: each composes its
+// range, the partial maps are applied in a fixed order, and each warp walks
+// its range writing the state entering every CTA (forward) or the adjoint
+// arriving at every CTA's last token (backward).  Maps are per mode
+// {l.re, l.im, b.re, b.im}; lane l handles modes m, m+1 (cm and out point at
+// mode m, CTA 0).
+// ---------------------------------------------------------------------------
+constexpr int kFoldChunk = 4;
+
+template <int N>
+__device__ __forceinline__ void ld_maps(const float4* __restrict__ cm, int M, int i0, int lo, int hi, int dir,
+                                        float4 (&T)[N][2]) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+        const int i = i0 + dir * q;
+        if (i >= lo && i < hi) {
+            T[q][0] = __ldcg(cm + (size_t)i * M);
+            T[q][1] = __ldcg(cm + (size_t)i * M + 1);
+        }
+    }
+}
+
+// forward: entry of CTA i = C_{i-1} o ... o C_0 (h0)
+__device__ __forceinline__ void chain_prefix_fwd(const float4* __restrict__ cm, float4* __restrict__ out, int n,
+                                                 int M, const float* h0p, float4 (*part)[32][2], int warp, int lane,
+                                                 bool active) {
+    const int lo = n * warp / kEngineWarps, hi = n * (warp + 1) / kEngineWarps;
+    float4 P0 = identity_map(), P1 = P0;
+    if (active) {
+        for (int i0 = lo; i0 < hi; i0 += kFoldChunk) {
+            float4 T[kFoldChunk][2];
+            ld_maps(cm, M, i0, lo, hi, 1, T);
+#pragma unroll
+            for (int q = 0; q < kFoldChunk; ++q) {
+                if (i0 + q < hi) {
+                    P0 = compose_maps(T[q][0], P0);
+                    P1 = compose_maps(T[q][1], P1);
+                }
+            }
+        }
+    }
+    part[warp][lane][0] = P0;
+    part[warp][lane][1] = P1;
+    __syncthreads();
+    if (!active) return;
+    float2 z0 = make_float2(0.f, 0.f), z1 = z0;
+    if (h0p != nullptr) {
+        const float4 hv = *reinterpret_cast<const float4*>(h0p);
+        z0 = make_float2(hv.x, hv.y);
+        z1 = make_float2(hv.z, hv.w);
+    }
+    for (int v = 0; v < warp; ++v) {
+        z0 = capply(part[v][lane][0], z0);
+        z1 = capply(part[v][lane][1], z1);
+    }
+    for (int i0 = lo; i0 < hi; i0 += kFoldChunk) {
+        float4 T[kFoldChunk][2];
+        ld_maps(cm, M, i0, lo, hi, 1, T);
+#pragma unroll
+        for (int q = 0; q < kFoldChunk; ++q) {
+            if (i0 + q < hi) {
+                out[(size_t)(i0 + q) * (M / 2)] = make_float4(z0.x, z0.y, z1.x, z1.y);
+                z0 = capply(T[q][0], z0);
+                z1 = capply(T[q][1], z1);
+            }
+        }
+    }
+}
+
+// Shared memory of the maps kernels' last phase, on top of the drained
+// staging rings: the CTA's segment maps, the fold partials and the last-CTA
+// flag each sit in the box area of one warp's ring (warps 0, 1, 2), never on
+// a ring's mbarriers (whose memory is not reused).
+struct EpilogueSmem {
+    float4 (*seg)[32][2];
+    float4 (*part)[32][2];
+    int* last;
+};
+static_assert(sizeof(float4) * kEngineWarps * 32 * 2 <= sizeof(((WarpRing*)nullptr)->box),
+              "segment maps and partials must fit a ring's box area");
+
+__device__ __forceinline__ EpilogueSmem epilogue_smem(uint8_t* smem_raw) {
+    WarpRing* rings = reinterpret_cast<WarpRing*>(smem_raw);
+    EpilogueSmem e;
+    e.seg = reinterpret_cast<float4 (*)[32][2]>(&rings[0].box[0][0][0][0]);
+    e.part = reinterpret_cast<float4 (*)[32][2]>(&rings[1].box[0][0][0][0]);
+    e.last = reinterpret_cast<int*>(&rings[2].box[0][0][0][0]);
+    return e;
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 3)
     samu_fwd_maps_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ctrl,
                          SamuScanFwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -248,8 +341,7 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const int lane = threadIdx.x & 31;
     WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
     const SegGeom& g = a.g;
-    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
-    if (gw >= (long long)g.n_chains * g.NS) return;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;   // < n_chains * NS: whole CTAs
     const SegTask T = seg_task(g, gw);
     const int M = g.M;
     const int m = T.grp * kGroup + 2 * lane;
@@ -272,7 +364,7 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
         const int slot = it % kRing;
         const int ts = T.t_begin + (T.nsc - 1 - it) * kSub;
         const int nsub = min(kSub, T.t_end - ts);
-        if (!ring_wait(R, it, T.nsc, a.status, lane)) return;
+        if (!ring_wait(R, it, T.nsc, a.status, lane)) break;   // status set; the CTA still reaches its barriers
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
@@ -283,103 +375,40 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
             ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - it - kRing) * kSub, T.b);
     }
     if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, P, be);
-}
 
-// One CTA per chain: entry state of every segment from h0 and the segment
-// maps.  Warp w folds segments [NS*w/16, NS*(w+1)/16) in time order (the
-// first kPrefixChunk maps stay in registers for the second pass); the 16
-// partial maps are then applied in order and each warp walks its range.
-constexpr int kPrefixChunk = 8;    // maps kept in registers across the two passes
-constexpr int kPrefixChunk2 = 4;   // maps per load batch after the first kPrefixChunk
-
-template <int N>
-__device__ __forceinline__ void load_maps(const float4* __restrict__ maps, int M, int i0, int hi, float4 (&T)[N][2]) {
-#pragma unroll
-    for (int q = 0; q < N; ++q) {
-        if (i0 + q < hi) {
-            T[q][0] = maps[(size_t)(i0 + q) * M];
-            T[q][1] = maps[(size_t)(i0 + q) * M + 1];
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kPrefixWarps * 32) samu_fwd_prefix_kernel(SamuScanFwdArgs a) {
-    __shared__ float4 s_part[kPrefixWarps][32][2];
-    pdl_trigger();
-    pdl_wait();
-    const SegGeom& g = a.g;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int chain = blockIdx.x;
-    const int b = chain / g.n_groups;
-    const int grp = chain % g.n_groups;
-    const int M = g.M;
-    const int m = grp * kGroup + 2 * lane;
-    const bool active = m < M;
-    const int NS = g.NS;
-    const int lo = NS * warp / kPrefixWarps, hi = NS * (warp + 1) / kPrefixWarps;
-    const float4* __restrict__ maps = a.smap + (size_t)b * NS * M + m;
-    float4 P0 = identity_map(), P1 = P0;
-    float4 T0[kPrefixChunk][2];
-    if (active) {
-        load_maps(maps, M, lo, hi, T0);
-#pragma unroll
-        for (int q = 0; q < kPrefixChunk; ++q) {
-            if (lo + q < hi) {
-                P0 = compose_maps(T0[q][0], P0);
-                P1 = compose_maps(T0[q][1], P1);
-            }
-        }
-        for (int i0 = lo + kPrefixChunk; i0 < hi; i0 += kPrefixChunk2) {
-            float4 T[kPrefixChunk2][2];
-            load_maps(maps, M, i0, hi, T);
-#pragma unroll
-            for (int q = 0; q < kPrefixChunk2; ++q) {
-                if (i0 + q < hi) {
-                    P0 = compose_maps(T[q][0], P0);
-                    P1 = compose_maps(T[q][1], P1);
-                }
-            }
-        }
-    }
-    s_part[warp][lane][0] = P0;
-    s_part[warp][lane][1] = P1;
+    // CTA map (its four segments in time order), then the chain prefix in the
+    // CTA that completes the chain
+    __syncthreads();   // rings drained
+    const EpilogueSmem E = epilogue_smem(smem_raw);
+    store_map2(&E.seg[warp][lane][0], P, be);
     __syncthreads();
-    if (!active) return;
-    float2 z0 = make_float2(0.f, 0.f), z1 = z0;
-    if (a.h0 != nullptr) {
-        const float4 hv = *reinterpret_cast<const float4*>(a.h0 + ((size_t)b * M + m) * 2);
-        z0 = make_float2(hv.x, hv.y);
-        z1 = make_float2(hv.z, hv.w);
-    }
-    for (int v = 0; v < warp; ++v) {
-        z0 = capply(s_part[v][lane][0], z0);
-        z1 = capply(s_part[v][lane][1], z1);
-    }
-    float4* __restrict__ out = reinterpret_cast<float4*>(a.sent + (size_t)b * NS * M + m);
+    const int chain = blockIdx.x / g.NC, cc = blockIdx.x % g.NC;
+    if (warp == 0) {
+        float4 A0 = E.seg[0][lane][0], A1 = E.seg[0][lane][1];
 #pragma unroll
-    for (int q = 0; q < kPrefixChunk; ++q) {
-        if (lo + q < hi) {
-            out[(size_t)(lo + q) * (M / 2)] = make_float4(z0.x, z0.y, z1.x, z1.y);
-            z0 = capply(T0[q][0], z0);
-            z1 = capply(T0[q][1], z1);
+        for (int w = 1; w < kEngineWarps; ++w) {
+            A0 = compose_maps(E.seg[w][lane][0], A0);
+            A1 = compose_maps(E.seg[w][lane][1], A1);
         }
-    }
-    for (int i0 = lo + kPrefixChunk; i0 < hi; i0 += kPrefixChunk2) {
-        float4 T[kPrefixChunk2][2];
-        load_maps(maps, M, i0, hi, T);
-#pragma unroll
-        for (int q = 0; q < kPrefixChunk2; ++q) {
-            if (i0 + q < hi) {
-                out[(size_t)(i0 + q) * (M / 2)] = make_float4(z0.x, z0.y, z1.x, z1.y);
-                z0 = capply(T[q][0], z0);
-                z1 = capply(T[q][1], z1);
-            }
+        if (active) {
+            float4* cm = a.cmap + ((size_t)T.b * g.NC + cc) * M + m;
+            cm[0] = A0;
+            cm[1] = A1;
         }
+        __threadfence();
     }
+    __syncthreads();
+    if (threadIdx.x == 0) *E.last = atomicAdd(a.counters + chain, 1u) == (uint32_t)(g.NC - 1) ? 1 : 0;
+    __syncthreads();
+    if (!*E.last) return;
+    __threadfence();
+    chain_prefix_fwd(a.cmap + (size_t)T.b * g.NC * M + m, reinterpret_cast<float4*>(a.cent + (size_t)T.b * g.NC * M + m),
+                     g.NC, M, a.h0 != nullptr ? a.h0 + ((size_t)T.b * M + m) * 2 : nullptr, E.part, warp, lane,
+                     active);
+    if (threadIdx.x == 0) a.counters[chain] = 0u;
 }
 
-__global__ void __launch_bounds__(kEngineThreads, 6)
+__global__ void __launch_bounds__(kEngineThreads, 3)
     samu_fwd_replay_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ctrl,
                            SamuScanFwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -404,7 +433,31 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
             ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x z = czero();
-    if (active) z = load_c2(reinterpret_cast<const float*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m));
+    if (active) {   // entry: the CTA's entry state through the maps of the earlier segments of the CTA
+        const int cc = T.s / kSegPerCta;
+        const float4 e = *reinterpret_cast<const float4*>(a.cent + ((size_t)T.b * g.NC + cc) * M + m);
+        float2 z0 = make_float2(e.x, e.y), z1 = make_float2(e.z, e.w);
+        for (int v0 = cc * kSegPerCta; v0 < T.s; v0 += 4) {   // the CTA's earlier segments, 4 loads at a time
+            float4 Tm[4][2];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (v0 + q < T.s) {
+                    const float4* sm = a.smap + ((size_t)T.b * g.NS + v0 + q) * M + m;
+                    Tm[q][0] = sm[0];
+                    Tm[q][1] = sm[1];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (v0 + q < T.s) {
+                    z0 = capply(Tm[q][0], z0);
+                    z1 = capply(Tm[q][1], z1);
+                }
+            }
+        }
+        z.re = pk2(z0.x, z1.x);
+        z.im = pk2(z0.y, z1.y);
+    }
     for (int it = 0; it < T.nsc; ++it) {
         const int slot = it % kRing;
         const int ts = T.t_begin + it * kSub;
@@ -428,7 +481,7 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
         if (lane == 0 && it + kRing < T.nsc)
             ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
     }
-    if (active && T.t_end == L) store_c2(a.hT + ((size_t)T.b * M + m) * 2, z);
+    if (active && T.nsc > 0 && T.t_end == L) store_c2(a.hT + ((size_t)T.b * M + m) * 2, z);
 }
 
 // ---------------------------------------------------------------------------
@@ -460,7 +513,54 @@ __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* g
     }
 }
 
-__global__ void __launch_bounds__(kEngineThreads, 6)
+// backward: adjoint arriving at CTA i's last token = C_{i+1} o ... o C_{n-1} (dhT)
+__device__ __forceinline__ void chain_prefix_bwd(const float4* __restrict__ cm, float4* __restrict__ out, int n,
+                                                 int M, const float* dhTp, float4 (*part)[32][2], int warp,
+                                                 int lane, bool active) {
+    const int lo = n * warp / kEngineWarps, hi = n * (warp + 1) / kEngineWarps;
+    float4 P0 = identity_map(), P1 = P0;
+    if (active) {
+        for (int i0 = hi - 1; i0 >= lo; i0 -= kFoldChunk) {
+            float4 T[kFoldChunk][2];
+            ld_maps(cm, M, i0, lo, hi, -1, T);
+#pragma unroll
+            for (int q = 0; q < kFoldChunk; ++q) {
+                if (i0 - q >= lo) {
+                    P0 = compose_maps(T[q][0], P0);
+                    P1 = compose_maps(T[q][1], P1);
+                }
+            }
+        }
+    }
+    part[warp][lane][0] = P0;
+    part[warp][lane][1] = P1;
+    __syncthreads();
+    if (!active) return;
+    float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+    if (dhTp != nullptr) {
+        const float4 v = *reinterpret_cast<const float4*>(dhTp);
+        r0 = make_float2(v.x, v.y);
+        r1 = make_float2(v.z, v.w);
+    }
+    for (int v = kEngineWarps - 1; v > warp; --v) {
+        r0 = capply(part[v][lane][0], r0);
+        r1 = capply(part[v][lane][1], r1);
+    }
+    for (int i0 = hi - 1; i0 >= lo; i0 -= kFoldChunk) {
+        float4 T[kFoldChunk][2];
+        ld_maps(cm, M, i0, lo, hi, -1, T);
+#pragma unroll
+        for (int q = 0; q < kFoldChunk; ++q) {
+            if (i0 - q >= lo) {
+                out[(size_t)(i0 - q) * (M / 2)] = make_float4(r0.x, r0.y, r1.x, r1.y);
+                r0 = capply(T[q][0], r0);
+                r1 = capply(T[q][1], r1);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 3)
     samu_bwd_maps_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_ctrl,
                          SamuScanBwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -468,8 +568,7 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     const int lane = threadIdx.x & 31;
     WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
     const SegGeom& g = a.g;
-    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
-    if (gw >= (long long)g.n_chains * g.NS) return;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;   // < n_chains * NS: whole CTAs
     const SegTask T = seg_task(g, gw);
     const int M = g.M;
     const int m = T.grp * kGroup + 2 * lane;
@@ -478,10 +577,6 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
     ring_init(R, lane);
     pdl_trigger();
     pdl_wait();
-    if (gw == 0 && lane == 0) {
-        a.status[0] = 0u;   // status word
-        a.status[1] = 0u;   // arrival counter of the parameter reductions
-    }
     // item k is sub-chunk k: the segment from its start forwards
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
@@ -495,7 +590,7 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
         const int slot = it % kRing;
         const int ts = T.t_begin + it * kSub;
         const int nsub = min(kSub, T.t_end - ts);
-        if (!ring_wait(R, it, T.nsc, a.status, lane)) return;
+        if (!ring_wait(R, it, T.nsc, a.status, lane)) break;   // status set; the CTA still reaches its barriers
         const float4* sc = R.ctrl[slot];
         const uint32_t* gre = &R.box[slot][0][0][lane];
         const uint32_t* gim = &R.box[slot][1][0][lane];
@@ -506,97 +601,37 @@ __global__ void __launch_bounds__(kEngineThreads, 6)
             ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
     }
     if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, Q, be);
-}
 
-// One CTA per chain: adjoint arriving at every segment's last token, from
-// dhT and the adjoint segment maps, the latest segments first.  Warp w
-// composes segments [NS*w/16, NS*(w+1)/16), the latest applied first.
-template <int N>
-__device__ __forceinline__ void load_maps_desc(const float4* __restrict__ maps, int M, int i0, int lo,
-                                               float4 (&T)[N][2]) {
-#pragma unroll
-    for (int q = 0; q < N; ++q) {
-        if (i0 - q >= lo) {
-            T[q][0] = maps[(size_t)(i0 - q) * M];
-            T[q][1] = maps[(size_t)(i0 - q) * M + 1];
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kPrefixWarps * 32) samu_bwd_prefix_kernel(SamuScanBwdArgs a) {
-    __shared__ float4 s_part[kPrefixWarps][32][2];
-    pdl_trigger();
-    pdl_wait();
-    const SegGeom& g = a.g;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int chain = blockIdx.x;
-    const int b = chain / g.n_groups;
-    const int grp = chain % g.n_groups;
-    const int M = g.M;
-    const int m = grp * kGroup + 2 * lane;
-    const bool active = m < M;
-    const int NS = g.NS;
-    const int lo = NS * warp / kPrefixWarps, hi = NS * (warp + 1) / kPrefixWarps;
-    const float4* __restrict__ maps = a.smap + (size_t)b * NS * M + m;
-    float4 P0 = identity_map(), P1 = P0;
-    float4 T0[kPrefixChunk][2];
-    if (active) {
-        load_maps_desc(maps, M, hi - 1, lo, T0);
-#pragma unroll
-        for (int q = 0; q < kPrefixChunk; ++q) {
-            if (hi - 1 - q >= lo) {
-                P0 = compose_maps(T0[q][0], P0);
-                P1 = compose_maps(T0[q][1], P1);
-            }
-        }
-        for (int i0 = hi - 1 - kPrefixChunk; i0 >= lo; i0 -= kPrefixChunk2) {
-            float4 T[kPrefixChunk2][2];
-            load_maps_desc(maps, M, i0, lo, T);
-#pragma unroll
-            for (int q = 0; q < kPrefixChunk2; ++q) {
-                if (i0 - q >= lo) {
-                    P0 = compose_maps(T[q][0], P0);
-                    P1 = compose_maps(T[q][1], P1);
-                }
-            }
-        }
-    }
-    s_part[warp][lane][0] = P0;
-    s_part[warp][lane][1] = P1;
+    // adjoint CTA map (the latest segment applied first), then the reverse
+    // chain prefix in the CTA that completes the chain
+    __syncthreads();   // rings drained
+    const EpilogueSmem E = epilogue_smem(smem_raw);
+    store_map2(&E.seg[warp][lane][0], Q, be);
     __syncthreads();
-    if (!active) return;
-    float2 r0 = make_float2(0.f, 0.f), r1 = r0;
-    if (a.dhT != nullptr) {
-        const float4 v = *reinterpret_cast<const float4*>(a.dhT + ((size_t)b * M + m) * 2);
-        r0 = make_float2(v.x, v.y);
-        r1 = make_float2(v.z, v.w);
-    }
-    for (int v = kPrefixWarps - 1; v > warp; --v) {
-        r0 = capply(s_part[v][lane][0], r0);
-        r1 = capply(s_part[v][lane][1], r1);
-    }
-    float4* __restrict__ out = reinterpret_cast<float4*>(a.sent + (size_t)b * NS * M + m);
+    const int chain = blockIdx.x / g.NC, cc = blockIdx.x % g.NC;
+    if (warp == 0) {
+        float4 A0 = E.seg[kEngineWarps - 1][lane][0], A1 = E.seg[kEngineWarps - 1][lane][1];
 #pragma unroll
-    for (int q = 0; q < kPrefixChunk; ++q) {
-        if (hi - 1 - q >= lo) {
-            out[(size_t)(hi - 1 - q) * (M / 2)] = make_float4(r0.x, r0.y, r1.x, r1.y);
-            r0 = capply(T0[q][0], r0);
-            r1 = capply(T0[q][1], r1);
+        for (int w = kEngineWarps - 2; w >= 0; --w) {
+            A0 = compose_maps(E.seg[w][lane][0], A0);
+            A1 = compose_maps(E.seg[w][lane][1], A1);
         }
-    }
-    for (int i0 = hi - 1 - kPrefixChunk; i0 >= lo; i0 -= kPrefixChunk2) {
-        float4 T[kPrefixChunk2][2];
-        load_maps_desc(maps, M, i0, lo, T);
-#pragma unroll
-        for (int q = 0; q < kPrefixChunk2; ++q) {
-            if (i0 - q >= lo) {
-                out[(size_t)(i0 - q) * (M / 2)] = make_float4(r0.x, r0.y, r1.x, r1.y);
-                r0 = capply(T[q][0], r0);
-                r1 = capply(T[q][1], r1);
-            }
+        if (active) {
+            float4* cm = a.cmap + ((size_t)T.b * g.NC + cc) * M + m;
+            cm[0] = A0;
+            cm[1] = A1;
         }
+        __threadfence();
     }
+    __syncthreads();
+    if (threadIdx.x == 0) *E.last = atomicAdd(a.counters + chain, 1u) == (uint32_t)(g.NC - 1) ? 1 : 0;
+    __syncthreads();
+    if (!*E.last) return;
+    __threadfence();
+    chain_prefix_bwd(a.cmap + (size_t)T.b * g.NC * M + m, reinterpret_cast<float4*>(a.cent + (size_t)T.b * g.NC * M + m),
+                     g.NC, M, a.dhT != nullptr ? a.dhT + ((size_t)T.b * M + m) * 2 : nullptr, E.part, warp, lane,
+                     active);
+    if (threadIdx.x == 0) a.counters[chain] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -739,7 +774,7 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_
     if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
 }
 
-__global__ void __launch_bounds__(kEngineThreads, 4)
+__global__ void __launch_bounds__(kEngineThreads, 2)
     samu_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_ctrl, SamuScanBwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -756,7 +791,7 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     const int m = T.grp * kGroup + 2 * lane;
     const bool active = m < M;
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
-    const int n_units = (T.t_end - T.t_begin + kHalf - 1) / kHalf;
+    const int n_units = T.t_end > T.t_begin ? (T.t_end - T.t_begin + kHalf - 1) / kHalf : 0;
     const int n_items = 2 * n_units;
     // item k: unit n_units-1-k/2 (the segment from its end backwards); even
     // items carry w (forward sweep), odd items dy (reverse sweep)
@@ -774,7 +809,31 @@ __global__ void __launch_bounds__(kEngineThreads, 4)
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
     c2x A = czero();
-    if (active) A = load_c2(reinterpret_cast<const float*>(a.sent + ((size_t)T.b * g.NS + T.s) * M + m));
+    if (active) {   // the adjoint arriving at the CTA through the maps of the later segments of the CTA
+        const int cc = T.s / kSegPerCta;
+        const float4 e = *reinterpret_cast<const float4*>(a.cent + ((size_t)T.b * g.NC + cc) * M + m);
+        float2 r0 = make_float2(e.x, e.y), r1 = make_float2(e.z, e.w);
+        for (int v1 = (cc + 1) * kSegPerCta - 1; v1 > T.s; v1 -= 4) {   // the CTA's later segments, latest first
+            float4 Tm[4][2];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (v1 - q > T.s) {
+                    const float4* sm = a.smap + ((size_t)T.b * g.NS + v1 - q) * M + m;
+                    Tm[q][0] = sm[0];
+                    Tm[q][1] = sm[1];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (v1 - q > T.s) {
+                    r0 = capply(Tm[q][0], r0);
+                    r1 = capply(Tm[q][1], r1);
+                }
+            }
+        }
+        A.re = pk2(r0.x, r1.x);
+        A.im = pk2(r0.y, r1.y);
+    }
     f2x acc_nu = 0ull, acc_th = 0ull;
     const bool fp32 = a.grad_fp32 != 0;
     for (int it = 0; it < n_items; it += 2) {
@@ -893,10 +952,6 @@ cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_
                      args);
 }
 
-cudaError_t launch_samu_fwd_prefix(const SamuScanFwdArgs& args, cudaStream_t s, bool pdl) {
-    return launch_ex(samu_fwd_prefix_kernel, args.g.n_chains, kPrefixWarps * 32, 0, s, pdl, args);
-}
-
 cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
                                    cudaStream_t s, bool pdl) {
     return launch_ex(samu_fwd_replay_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_w, tm_ctrl,
@@ -907,10 +962,6 @@ cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm
                                  cudaStream_t s, bool pdl) {
     return launch_ex(samu_bwd_maps_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_ctrl,
                      args);
-}
-
-cudaError_t launch_samu_bwd_prefix(const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
-    return launch_ex(samu_bwd_prefix_kernel, args.g.n_chains, kPrefixWarps * 32, 0, s, pdl, args);
 }
 
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,

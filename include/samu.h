@@ -77,7 +77,8 @@ int lrs_version(void);
 /* Reads the device status word kept in `scratch` (a buffer last used by one
  * of the calls below; every call clears the word when it starts, so it covers
  * the most recent call).  SYNCHRONISES `stream`.  *status receives LRS_OK or
- * LRS_ERR_TIMEOUT.  Returns LRS_ERR_ARG / LRS_ERR_CUDA on failure. */
+ * LRS_ERR_TIMEOUT (LRS_ERR_CUDA if a kernel found its shared memory
+ * misaligned and copied nothing).  Returns LRS_ERR_ARG / LRS_ERR_CUDA on failure. */
 int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
 
 /* Opt-in per-kernel timing for benchmarks (not needed for computing).

@@ -154,7 +154,7 @@ int lrs_device_status(void* scratch, int* status, cudaStream_t stream) {
     if (e != cudaSuccess) return LRS_ERR_CUDA;
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return LRS_ERR_CUDA;
-    *status = (v & (kStatusTimeout | kStatusUpstream)) ? LRS_ERR_TIMEOUT : LRS_OK;
+    *status = (v & kStatusLayout) ? LRS_ERR_CUDA : (v & (kStatusTimeout | kStatusUpstream)) ? LRS_ERR_TIMEOUT : LRS_OK;
     return LRS_OK;
 }
 
@@ -212,7 +212,12 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.status = at<uint32_t>(scratch, sc.status);
     cf.counters = at<uint32_t>(scratch, sc.counters);   // the forward's half
     cf.n_counters = samu_seg_geom(B, L, M, 0).n_chains;
-    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream, false));
+    CUtensorMap tm_x{};
+    {
+        const CtrlGeom cgf = samu_ctrl_geom(BL, D, false);
+        if (cgf.swz && !make_ctrl_x_map(&tm_x, x_sel, BL, D, cgf.stage_tok)) return LRS_ERR_CUDA;
+    }
+    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(tm_x, cf, stream, false));
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
     CUtensorMap tm_w, tm_ctrl;
@@ -262,7 +267,7 @@ int samu_backward(const void* dy, const float* dhT,
     const int fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
 
     const float4* ctrl = at<float4>(saved, sv.ctrl);
-    // status word, parameter-reduction counter and the chain arrival counters start at zero
+    // status word and the chain arrival counters start at zero
     if (cudaMemsetAsync(scratch, 0, sc.zero_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     // 16-row boxes for the adjoint maps, 8-row boxes for the reverse replay
     CUtensorMap tm_dy, tm_ctrl, tm_dy8, tm_w8, tm_ctrl8;
@@ -304,25 +309,23 @@ int samu_backward(const void* dy, const float* dhT,
     cb.misc = at<float>(saved, sv.misc);
     cb.dx = dx_sel;
     cb.grad_fp32 = fp32;
+    cb.numod = s.numod;
+    cb.numod_rows = B * g.NS;
     cb.dwh_part = at<float>(scratch, sc.dwh_part);
     cb.amp_part = at<float2>(scratch, sc.amp_part);
+    cb.dot_part = at<float2>(scratch, sc.dot_part);
+    cb.dnu = dnu;
+    cb.dtheta = dtheta;
     LRS_LAUNCH(KID_SAMU_CTRL_BWD, stream, launch_samu_ctrl_bwd(cb, stream, pdl_ok()));
 
     SamuParamArgs pa;
-    pa.B = B;
-    pa.L = L;
     pa.D = D;
-    pa.n_part = g.NS;
     pa.n_rows = cb.cg.n_ctas;
-    pa.numod = at<float2>(scratch, sc.numod);
     pa.dwh_part = cb.dwh_part;
     pa.amp_part = cb.amp_part;
-    pa.dwh = at<float>(scratch, sc.dwh);
-    pa.counter = at<uint32_t>(scratch, sc.status + 4);
+    pa.dot_part = cb.dot_part;
     pa.wh = cb.wh;
     pa.misc = cb.misc;
-    pa.dnu = dnu;
-    pa.dtheta = dtheta;
     pa.dw_phi = dw_phi;
     pa.dw_r = dw_r;
     pa.da_phi = da_phi;

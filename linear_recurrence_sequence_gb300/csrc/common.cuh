@@ -38,6 +38,7 @@ constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
 // Device status word bits (OR-ed together by failing CTAs).
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusUpstream = 2u;
+constexpr uint32_t kStatusLayout = 4u;    // a shared-memory buffer missed its required alignment (nothing copied)
 
 // ---------------------------------------------------------------------------
 // Memory-model primitives (PTX).

@@ -100,13 +100,14 @@ __device__ __forceinline__ ModePair zero_modes() {
 
 // Per-token control word, written by the controller forward and staged into
 // shared memory by TMA, each value duplicated so that it loads as a pair:
-// {E-1, E-1, C, C}, {S, S, reset, reset} (two float4), reset 1 at a segment
-// start (lambda = 0) and 0 elsewhere.  It is the same for every lane, so the
-// branches on it are warp-uniform.
+// {E-1, E-1, C, C}, {S, S, R, R} (two float4), R = -E for an ordinary token
+// and R = +0 at a segment start (lambda = 0); E = e^c > 0, so the sign tells
+// them apart.  It is the same for every lane, so the branches on it are
+// warp-uniform.
 struct Ctl2 {
     f2x e, c, s;   // E - 1, C, S
-    float reset;
-    float em1;     // E - 1 (scalar)
+    f2x ne;        // -E (ordinary tokens)
+    float rflag;   // R
 };
 
 __device__ __forceinline__ Ctl2 load_ctl(const float4* sc, int i) {
@@ -115,16 +116,17 @@ __device__ __forceinline__ Ctl2 load_ctl(const float4* sc, int i) {
     ct.e = pk2(a.x, a.y);
     ct.c = pk2(a.z, a.w);
     ct.s = pk2(b.x, b.y);
-    ct.reset = b.z;
-    ct.em1 = a.x;
+    ct.ne = pk2(b.z, b.w);
+    ct.rflag = b.z;
     return ct;
 }
 
-__device__ __forceinline__ bool is_reset(const Ctl2& ct) { return ct.reset != 0.f; }
+__device__ __forceinline__ bool is_reset_word(float r) { return r >= 0.f; }
+__device__ __forceinline__ bool is_reset(const Ctl2& ct) { return is_reset_word(ct.rflag); }
 
 // Bound on |nu (E - 1)| under which the degree-3 polynomial below is exact to
-// < 2e-11 relative (the truncation term x^4/24), checked once per warp and
-// sub-chunk.
+// < 2.5e-9 relative (the truncation term x^4/24, about 0.04 FP32 ulp),
+// checked once per warp and sub-chunk.
 constexpr float kPolyBound = 1.0f / 64.0f;
 
 // lambda of both modes for a token that is not a reset:
@@ -227,14 +229,15 @@ struct SamuScanBwdArgs {
 // `ring` shared-memory slots by 1-D bulk copies; one producer warp plus
 // `consumers` warps of 32 threads, each thread owning 8 channels.
 struct CtrlGeom {
-    int stage_tok;          // tokens per stage (16, or 8 when 16 rows exceed 64 KB)
-    int ring;               // slots (at most 8, filling up to 192 KB)
+    int stage_tok;          // tokens per stage (16, or 8 when 16 rows exceed 36 KB)
+    int ring;               // slots (2 to 8, as many as fit)
     int consumers;          // consumer warps
     int threads;            // 32 * (1 + consumers)
     int smem;               // dynamic shared memory bytes
     int n_ctas;             // streaming CTAs
     long long n_stages;     // ceil(B*L / stage_tok)
     int max_cta_tok;        // tokens of the longest CTA range (backward scalar buffer)
+    int swz;                // forward: stages as swizzled tiled copies (D a multiple of 64)
 };
 
 CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward);
@@ -250,26 +253,26 @@ struct SamuCtrlBwdArgs {
     const float4* ctrl;     // [B*L][2] control words
     const float* wh;        // [2][D+1]
     const float* misc;
+    const float2* numod;    // [numod_rows][M] per-segment (dnu, dtheta)
+    int numod_rows;
     void* dx;               // BF16 or FP32
     int grad_fp32;
-    float* dwh_part;        // [cg.n_ctas][2][D+1]
+    float* dwh_part;        // [cg.n_ctas][2][ns], ns = ctrl_half_stride(D)
     float2* amp_part;       // [cg.n_ctas]
+    float2* dot_part;       // [cg.n_ctas] w_hat . (partial row), phi and r
+    float* dnu;
+    float* dtheta;
     uint32_t* status;
 };
 
 struct SamuParamArgs {
-    int B, L, D;
-    int n_part;             // numod rows per batch row
-    int n_rows;             // rows of dwh_part / amp_part
-    const float2* numod;    // [B*n_part][M]
-    const float* dwh_part;  // [n_rows][2][D+1]
+    int D;
+    int n_rows;             // rows of dwh_part / amp_part / dot_part (controller-backward CTAs)
+    const float* dwh_part;  // [n_rows][2][ns]
     const float2* amp_part;
-    float* dwh;             // [2][D+1] column sums of dwh_part
-    uint32_t* counter;      // CTA arrival counter, zero on entry, left zero
+    const float2* dot_part;
     const float* wh;
     const float* misc;
-    float* dnu;
-    float* dtheta;
     float* dw_phi;
     float* dw_r;
     float* da_phi;
@@ -279,7 +282,6 @@ struct SamuParamArgs {
 struct SamuCtrlFwdArgs {
     long long BL;
     int D;
-    int n_mode_ctas;               // filled by the launcher
     CtrlGeom cg;                   // filled by the launcher
     const uint4* x;                // BF16 x_sel as 16-byte vectors
     const uint8_t* reset;
@@ -291,7 +293,7 @@ struct SamuCtrlFwdArgs {
     const float* theta;
     float* p;
     float* r;
-    float4* ctrl;                  // [B*L][2] {E-1, E-1, C, C}, {S, S, reset, reset}
+    float4* ctrl;                  // [B*L][2] {E-1, E-1, C, C}, {S, S, R, R}
     float* wh;                     // [2][D+1]
     float* misc;
     float4* modes;                 // [M] lbar hi/lo
@@ -300,7 +302,9 @@ struct SamuCtrlFwdArgs {
     uint32_t* status;
 };
 
-cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s, bool pdl);
+// tm_x: make_ctrl_x_map over x_sel with samu_ctrl_geom(B*L, D, false).stage_tok
+// rows when that geometry's swz is set (unused otherwise).
+cudaError_t launch_samu_ctrl_fwd(const CUtensorMap& tm_x, const SamuCtrlFwdArgs& args, cudaStream_t s, bool pdl);
 // Segment geometry of the forward (backward = false) or backward scan on the
 // current device: every segment of every chain resident at once.
 SegGeom samu_scan_geom(int B, int L, int M, bool backward);
@@ -317,6 +321,8 @@ cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm
                                  cudaStream_t s, bool pdl);
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
                                  const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
+// Controller backward (with the (dnu, dtheta) reductions), then the
+// reductions of the unit-direction and amplitude gradients.
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl);
 

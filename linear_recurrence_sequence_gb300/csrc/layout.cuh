@@ -17,6 +17,10 @@ constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status w
 
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+// Floats per half (phi, r) of a controller-backward partial row: D + 1
+// rounded up to a multiple of 4, so that rows are float4 arrays.
+__host__ __device__ inline int ctrl_half_stride(int D) { return (D + 1 + 3) & ~3; }
+
 // Tile shapes.  RG-LRU: a tile is 128 tokens of one chain, one 16-token
 // sub-chunk per warp.
 constexpr int kRgWarps = 8;                        // RG-LRU: 8 warps
@@ -131,7 +135,7 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
     size_t o = 0;
     s.p = o;      o = align_up(o + BL * 4);                          // p_t
     s.r = o;      o = align_up(o + BL * 4);                          // r_t
-    s.ctrl = o;   o = align_up(o + BL * 32);                         // {E-1, E-1, C, C}, {S, S, reset, reset}
+    s.ctrl = o;   o = align_up(o + BL * 32);                         // {E-1, E-1, C, C}, {S, S, R, R}, R = -E or +0 at a reset
     s.hsub = o;   o = align_up(o + (size_t)B * g.CS * M * 8);        // state every 8 tokens
     s.wh = o;     o = align_up(o + (size_t)2 * (D + 1) * 4);         // unit directions
     s.misc = o;   o = align_up(o + kMiscFloats * 4);
@@ -141,7 +145,7 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
 }
 
 struct SamuScratch {
-    size_t status, counters, smap, cmap, cent, kpart, numod, dwh_part, amp_part, dwh, total;
+    size_t status, counters, smap, cmap, cent, kpart, numod, dwh_part, amp_part, dot_part, total;
     size_t zero_bytes;     // status block + counters: cleared at the start of a backward call
 };
 
@@ -162,9 +166,10 @@ inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     s.cent = o;     o = align_up(o + crows * 8);                      // CTA entry states / incoming adjoints
     s.kpart = o;    o = align_up(o + BL * g.n_groups * 8);            // per-token controller partials
     s.numod = o;    o = align_up(o + rows * 8);                       // per-segment (dnu, dtheta)
-    s.dwh_part = o; o = align_up(o + (size_t)kCtrlRowsMax * 2 * (D + 1) * 4);   // one row per CTA
+    const size_t prow = (size_t)2 * ctrl_half_stride(D) * 4;              // one partial row, bytes
+    s.dwh_part = o; o = align_up(o + (size_t)kCtrlRowsMax * prow);        // one row per CTA
     s.amp_part = o; o = align_up(o + (size_t)kCtrlRowsMax * 8);
-    s.dwh = o;      o = align_up(o + (size_t)2 * (D + 1) * 4);                 // column sums
+    s.dot_part = o; o = align_up(o + (size_t)kCtrlRowsMax * 8);           // w_hat . (partial row)
     s.total = o;
     return s;
 }

@@ -27,10 +27,11 @@ namespace lrs {
 // Shared memory: ring[slot][token][D] BF16 | per-slot exchange buffer |
 // mbarriers.
 // ---------------------------------------------------------------------------
-constexpr int kCtrlRingMax = 8;                 // ring slots (at most)
-constexpr int kCtrlRingBytes = 192 * 1024;      // shared memory for the ring
-constexpr int kCtrlMaxThreads = 32 * (1 + 16);   // D = 4096: 16 consumer warps
-constexpr int kModeThreads = 32;    // active threads of a mode CTA
+constexpr int kCtrlRingMax = 8;                        // ring slots (at most)
+constexpr size_t kCtrlFwdSmemMax = 226 * 1024;          // forward: ring + exchange buffer + barriers
+constexpr size_t kCtrlBwdSmemMax = 200 * 1024;          // backward: leaves room for the reduction CTAs
+constexpr int kCtrlMaxThreads = 32 * (2 + 16);      // forward, D = 4096: 16 consumer warps + 2
+constexpr int kCtrlBwdMaxThreads = 32 * (2 + 16);   // backward: plus the reducer warp
 
 struct CtrlSmem {
     uint8_t* ring;
@@ -40,21 +41,31 @@ struct CtrlSmem {
     uint64_t* empty;    // backward: slot consumed (consumers)
 };
 
-// Bytes between consecutive x_sel rows in a ring slot: the backward keeps
-// rows packed; the forward pads each row by 16 bytes so that the eight rows
-// an ldmatrix reads fall in distinct banks.
-__host__ __device__ inline size_t ctrl_row_bytes(int D, bool backward) { return 2 * (size_t)D + (backward ? 0 : 16); }
+// Shared-memory bytes per x_sel row in a ring slot.  The backward keeps rows
+// packed (one bulk copy per stage).  The forward, when D is a multiple of 64,
+// stages each stage with one tiled TMA copy in the 128-byte swizzled layout
+// [64-channel chunk][token][128 bytes] (16-byte unit u of (chunk c, token r)
+// stored at unit u ^ (r mod 8)), so that the eight rows an ldmatrix reads
+// fall in distinct banks; otherwise it pads each row by 16 bytes (one bulk
+// copy per row).
+__host__ __device__ inline size_t ctrl_row_bytes(const CtrlGeom& cg, int D, bool backward) {
+    return 2 * (size_t)D + ((backward || cg.swz) ? 0 : 16);
+}
 
 __host__ __device__ inline size_t ctrl_slot_bytes(const CtrlGeom& cg, int D, bool backward) {
-    return (size_t)cg.stage_tok * ctrl_row_bytes(D, backward);
+    return (size_t)cg.stage_tok * ctrl_row_bytes(cg, D, backward);
 }
 
 __host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D, bool backward) {
     return (size_t)cg.ring * ctrl_slot_bytes(cg, D, backward);
 }
 
+// Forward: the consumers' partial tiles, ring + 1 sets (stage k uses set
+// k mod (ring + 1); stage k + ring + 1 is issued only after the producer has
+// read set k); backward: the per-token scalars of the range.
+__host__ __device__ inline int ctrl_xsets(const CtrlGeom& cg) { return cg.ring + 1; }
 __host__ __device__ inline size_t ctrl_xbuf_bytes(const CtrlGeom& cg, bool backward) {
-    return backward ? (size_t)cg.max_cta_tok * 8 : (size_t)cg.ring * cg.consumers * 32 * 16;
+    return backward ? (size_t)cg.max_cta_tok * 8 : (size_t)ctrl_xsets(cg) * cg.consumers * 32 * 16;
 }
 
 __device__ __forceinline__ CtrlSmem ctrl_smem(uint8_t* base, const CtrlGeom& cg, int D, bool backward) {
@@ -76,18 +87,24 @@ __device__ __forceinline__ void ctrl_stage_range(const CtrlGeom& cg, int cta, lo
 }
 
 // Producer lane 0: the rows of stage (token t0, n tokens) into ring slot
-// `slot`, as one bulk copy (packed rows) or one per row (padded rows).
-__device__ __forceinline__ void ctrl_issue(const CtrlSmem& sm, int slot, const uint4* x, long long t0, int n, int D,
-                                           const CtrlGeom& cg, bool backward) {
+// `slot`: one bulk copy (backward, packed rows), one tiled copy of the whole
+// stage box (forward, swizzled; rows past B*L read as zero and count towards
+// the transaction bytes), or one bulk copy per row (forward, padded rows).
+__device__ __forceinline__ void ctrl_issue(const CtrlSmem& sm, int slot, const uint4* x, const CUtensorMap* tm,
+                                           long long t0, int n, int D, const CtrlGeom& cg, bool backward) {
     const uint32_t row = 2u * (uint32_t)D;
     uint8_t* dst = sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D, backward);
     const uint8_t* src = reinterpret_cast<const uint8_t*>(x) + (size_t)t0 * row;
     fence_proxy_async();
-    mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
     if (backward) {
+        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
         bulk_load(dst, src, (uint32_t)n * row, &sm.full[slot]);
+    } else if (cg.swz) {
+        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)cg.stage_tok * row);
+        tma_load_3d(dst, tm, 0, (int)t0, 0, &sm.full[slot]);
     } else {
-        const size_t pitch = ctrl_row_bytes(D, false);
+        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
+        const size_t pitch = ctrl_row_bytes(cg, D, false);
         for (int i = 0; i < n; ++i) bulk_load(dst + (size_t)i * pitch, src + (size_t)i * row, row, &sm.full[slot]);
     }
 }
@@ -112,11 +129,13 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 }
 
 // ---------------------------------------------------------------------------
-// Controller forward, with the parameter preparation folded in.
-//  - Mode CTAs (the first n_mode_ctas, 32 active threads each): the per-mode
-//    transition constant lbar_m = e^{-nu_m} e^{i theta_m} as a double-float
-//    (hi, lo) in FP64.
-//  - Streaming CTAs: the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
+// Controller forward, with the parameter preparation folded in.  One CTA per
+// SM, each on a contiguous run of stages; thread 0 starts the first stages'
+// copies before anything else.
+//  - A mode warp computes the CTA's share of the per-mode transition
+//    constants lbar_m = e^{-nu_m} e^{i theta_m} as double-floats (hi, lo) in
+//    FP64, beside the stream (warps: 0 producer, 1 modes, 2.. consumers).
+//  - Every CTA computes the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
 //    fixed-order tree, the same in every CTA).  The dot products x~ . w_hat of
 //    a stage of 16 tokens are one tensor-core contraction [16 tokens x D] x
 //    [D x 8]: consumer warp c takes the 16-channel k-steps 16c .. 16c+15
@@ -127,8 +146,8 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 //    The producer adds the consumers' partial tiles and the three split
 //    columns in a fixed order and evaluates p = tanh(s_phi), r = tanh(s_r),
 //    q(r), d, c, and E - 1 = expm1(c), C = cos d, S = sin d, one token per
-//    lane.  The first streaming CTA stores w_hat and the amplitude factors
-//    for the backward.
+//    lane; a slot is refilled as soon as its partial tiles are in.  CTA 0
+//    stores w_hat and the amplitude factors for the backward.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -185,11 +204,17 @@ __device__ __forceinline__ void ctrl_fwd_consumer(const SamuCtrlFwdArgs& a, cons
             bf[j][1] = pack_bf16(bf16_part(w[c0 + 8] * inv, part), bf16_part(w[c0 + 9] * inv, part));
         }
     }
-    const uint32_t pitch = (uint32_t)ctrl_row_bytes(D, false);
+    const uint32_t pitch = (uint32_t)ctrl_row_bytes(cg, D, false);
     // ldmatrix row of this lane: token lane % 16 (rows past the stage's
     // token count repeat earlier rows; their results are not used), channel
-    // half lane / 16 of each k-step
-    const uint32_t lane_off = (uint32_t)((lane & 15) % N) * pitch + (uint32_t)(lane >> 4) * 16u;
+    // half lane / 16 of each k-step.  Swizzled layout: k-step kk lies in
+    // chunk kk / 4, 16-byte unit 2 (kk mod 4) + half, stored at that unit
+    // xor (token mod 8); the consumer's first k-step is a multiple of 4.
+    const uint32_t r = (uint32_t)((lane & 15) % N), hf = (uint32_t)(lane >> 4);
+    const uint32_t lane_off = cg.swz ? r * 128u : r * pitch + hf * 16u;
+    uint32_t unit_off[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unit_off[q] = ((2u * q + hf) ^ (r & 7u)) * 16u;
     float4* xb = reinterpret_cast<float4*>(sm.xbuf);
     for (long long st = s0; st < s1; ++st) {
         const int k = (int)(st - s0);
@@ -200,20 +225,24 @@ __device__ __forceinline__ void ctrl_fwd_consumer(const SamuCtrlFwdArgs& a, cons
         }
         const uint32_t base = smem_u32(sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D, false)) + lane_off;
         float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
+        // byte offset of k-step kk for this lane
+        auto koff = [&](int kk) -> uint32_t {
+            return cg.swz ? (uint32_t)(kk >> 2) * (uint32_t)N * 128u + unit_off[kk & 3] : (uint32_t)kk * 32u;
+        };
 #pragma unroll
         for (int j = 0; j < kCtrlKMax; j += 2) {
             if (j < nk) {
                 uint32_t fa[4];
-                ldsm_x4(base + (uint32_t)(ks0 + j) * 32u, fa);
+                ldsm_x4(base + koff(ks0 + j), fa);
                 mma_16816(ce, fa, bf[j][0], bf[j][1]);
             }
             if (j + 1 < nk) {
                 uint32_t fa[4];
-                ldsm_x4(base + (uint32_t)(ks0 + j + 1) * 32u, fa);
+                ldsm_x4(base + koff(ks0 + j + 1), fa);
                 mma_16816(co, fa, bf[j + 1][0], bf[j + 1][1]);
             }
         }
-        xb[((size_t)slot * cg.consumers + cw) * 32 + lane] =
+        xb[((size_t)(k % ctrl_xsets(cg)) * cg.consumers + cw) * 32 + lane] =
             make_float4(ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.ready[slot]);
@@ -221,14 +250,11 @@ __device__ __forceinline__ void ctrl_fwd_consumer(const SamuCtrlFwdArgs& a, cons
 }
 
 template <int N>
-__device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, const CtrlSmem& sm, long long s0,
-                                                  long long s1, int lane, float bias_p, float bias_r, float k_phi,
-                                                  float k_r) {
+__device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, const CUtensorMap* tm, const CtrlSmem& sm,
+                                                  long long s0, long long s1, int lane, float bias_p, float bias_r,
+                                                  float k_phi, float k_r) {
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
-    if (lane == 0)
-        for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st)
-            ctrl_issue(sm, (int)(st - s0), a.x, st * N, (int)min((long long)N, a.BL - st * N), D, cg, false);
     const float4* xb = reinterpret_cast<const float4*>(sm.xbuf);
     // token i = lane (i < N): row i of the partial tiles is held by lanes
     // 4 (i mod 8) + {0, 1, 2} (columns {0,1}, {2,3}, {4,5}), in the first two
@@ -245,10 +271,15 @@ __device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, cons
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
             return;
         }
+        // the consumers are done with the slot: refill it first
+        const long long nxt = st + cg.ring;
+        if (lane == 0 && nxt < s1)
+            ctrl_issue(sm, slot, a.x, tm, nxt * N, (int)min((long long)N, a.BL - nxt * N), D, cg, false);
         float s_phi = 0.f, s_r = 0.f;
         if (i < N) {
+            const float4* set = xb + (size_t)(k % ctrl_xsets(cg)) * cg.consumers * 32;
             for (int c = 0; c < cg.consumers; ++c) {
-                const float4* tile = xb + ((size_t)slot * cg.consumers + c) * 32 + src;
+                const float4* tile = set + (size_t)c * 32 + src;
                 const float4 p01 = tile[0], p23 = tile[1], p45 = tile[2];
                 const float c0 = upper ? p01.z : p01.x, c1 = upper ? p01.w : p01.y;
                 const float c2 = upper ? p23.z : p23.x, c3 = upper ? p23.w : p23.y;
@@ -257,10 +288,6 @@ __device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, cons
                 s_r += (c3 + c4) + c5;
             }
         }
-        __syncwarp();
-        const long long nxt = st + cg.ring;
-        if (lane == 0 && nxt < s1)
-            ctrl_issue(sm, slot, a.x, nxt * N, (int)min((long long)N, a.BL - nxt * N), D, cg, false);
         if (i < n) {
             const long long t = t0 + i;
             const float p = tanhf(s_phi + bias_p);
@@ -270,39 +297,48 @@ __device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, cons
             const float c = k_r * qr;
             float sn, cs;
             sincosf(d, &sn, &cs);
-            const float rs = (a.reset != nullptr && a.reset[t] != 0) ? 1.0f : 0.0f;
             a.p[t] = p;
             a.r[t] = r;
             const float em1 = expm1f(c);
+            // R = -E, or +0 at a reset
+            const float rw = (a.reset != nullptr && a.reset[t] != 0) ? 0.0f : -(1.0f + em1);
             a.ctrl[2 * t] = make_float4(em1, em1, cs, cs);
-            a.ctrl[2 * t + 1] = make_float4(sn, sn, rs, rs);
+            a.ctrl[2 * t + 1] = make_float4(sn, sn, rw, rw);
         }
     }
 }
 
-__global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
+__global__ void __launch_bounds__(kCtrlMaxThreads)
+    samu_ctrl_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, SamuCtrlFwdArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ float s_red[2][kCtrlMaxThreads / 32];
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x;
     const int D = a.D;
     const int M = D / 2;
-    if ((int)blockIdx.x < a.n_mode_ctas) {
-        if (tid < kModeThreads) mode_constants(a.nu, a.theta, M, a.modes, blockIdx.x * kModeThreads + tid);
-        return;
-    }
-    const int cta = blockIdx.x - a.n_mode_ctas;
+    const int cta = blockIdx.x;
     const CtrlGeom& cg = a.cg;
     const int n = D + 1;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
     const CtrlSmem sm = ctrl_smem(smem_raw, cg, D, false);
-    if (tid == 0) {
+    long long s0, s1;
+    ctrl_stage_range(cg, cta, s0, s1);
+    if (cg.swz && (smem_u32(smem_raw) & 1023u) != 0u) {   // the swizzled copies need 1024-byte aligned slots
+        if (tid == 0) atomicOr(a.status, kStatusLayout);
+        return;
+    }
+    if (tid == 0) {   // the first stages go out before anything else
         for (int i = 0; i < cg.ring; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.ready[i], cg.consumers);
+        }
+        for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st) {
+            const int nn = cg.stage_tok;
+            ctrl_issue(sm, (int)(st - s0), a.x, &tm_x, st * nn, (int)min((long long)nn, a.BL - st * nn), D, cg,
+                       false);
         }
     }
 
@@ -349,25 +385,27 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrl
             a.misc[6] = ism;
         }
     }
-    long long s0, s1;
-    ctrl_stage_range(cg, cta, s0, s1);
     if (warp == 0) {
         const float bias_p = a.w_phi[D] * inv_phi, bias_r = a.w_r[D] * inv_r;
         if (cg.stage_tok == 16)
-            ctrl_fwd_producer<16>(a, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
+            ctrl_fwd_producer<16>(a, &tm_x, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
         else
-            ctrl_fwd_producer<8>(a, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
+            ctrl_fwd_producer<8>(a, &tm_x, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
+    } else if (warp == 1) {
+        // this CTA's share of the per-mode constants, off the streaming path
+        const int m0 = (int)((long long)M * cta / cg.n_ctas), m1 = (int)((long long)M * (cta + 1) / cg.n_ctas);
+        for (int m = m0 + lane; m < m1; m += 32) mode_constants(a.nu, a.theta, M, a.modes, m);
     } else {
         if (cg.stage_tok == 16)
-            ctrl_fwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, inv_phi, inv_r);
+            ctrl_fwd_consumer<16>(a, sm, s0, s1, warp - 2, lane, inv_phi, inv_r);
         else
-            ctrl_fwd_consumer<8>(a, sm, s0, s1, warp - 1, lane, inv_phi, inv_r);
+            ctrl_fwd_consumer<8>(a, sm, s0, s1, warp - 2, lane, inv_phi, inv_r);
     }
 }
 
 // ---------------------------------------------------------------------------
-// Controller backward.  First, every thread of the CTA takes tokens of the
-// CTA's range in turn:  dbar = sum over the mode groups of the Im-kappa
+// Controller backward.  Thread 0 starts the first x_sel copies; then every
+// thread of the CTA takes tokens of the CTA's range in turn:  dbar = sum over the mode groups of the Im-kappa
 // partials, cbar = E * sum of the (-nu Re kappa) partials (E = e^c);
 // pbar = dbar tanh(a_phi)/sqrt(M); rbar = cbar tanh(a_r)/sqrt(M)
 // (1 - r^2)/(1 + r^2)^2; through tanh: sbar_phi = pbar (1 - p^2),
@@ -376,7 +414,9 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_fwd_kernel(SamuCtrl
 // sum cbar q(r)) are reduced over the CTA in a fixed order.  Then the
 // producer streams the x_sel rows and the consumers, per token and channel,
 // form dx_sel = sbar_phi w_hat_phi[:D] + sbar_r w_hat_r[:D] and accumulate
-// dw_hat += sbar x~.  One partial row per CTA.
+// dw_hat += sbar x~.  One partial row per CTA.  Meanwhile a reducer warp sums
+// the reverse replay's per-segment (dnu, dtheta) rows for the CTA's share of
+// the modes.  Warps: 0 producer, 1 reducer, 2.. consumers.
 // ---------------------------------------------------------------------------
 template <int N>
 __device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
@@ -384,22 +424,25 @@ __device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, cons
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
     if (lane != 0) return;
-    for (long long st = s0; st < s1; ++st) {
+    for (long long st = s0 + cg.ring; st < s1; ++st) {   // the first cg.ring stages went out at the start
         const int k = (int)(st - s0);
         const int slot = k % cg.ring;
         const long long t0 = st * N;
         const int n = (int)min((long long)N, a.BL - t0);
-        if (k >= cg.ring && !mbar_wait_bounded(&sm.empty[slot], (uint32_t)(k / cg.ring - 1) & 1u)) {
+        if (!mbar_wait_bounded(&sm.empty[slot], (uint32_t)(k / cg.ring - 1) & 1u)) {
             atomicOr(a.status, kStatusTimeout);
-            return;
+            break;
         }
-        ctrl_issue(sm, slot, a.x, t0, n, D, cg, true);
+        ctrl_issue(sm, slot, a.x, nullptr, t0, n, D, cg, true);
     }
 }
 
+// Returns the thread's share of the partial row's projection on w_hat:
+// (sum_c w_hat_phi[c] dw_hat_phi[c], sum_c w_hat_r[c] dw_hat_r[c]) over its
+// eight channels.
 template <int N>
-__device__ __forceinline__ void ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
-                                                  long long s1, int cw, int lane, int cta) {
+__device__ __forceinline__ float2 ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
+                                                    long long s1, int cw, int lane, int cta) {
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
     const int vecs = D / 8;
@@ -421,7 +464,7 @@ __device__ __forceinline__ void ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, cons
         const int n = (int)min((long long)N, a.BL - t0);
         if (!mbar_wait_bounded(&sm.full[slot], (uint32_t)(k / cg.ring) & 1u)) {
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
-            return;
+            break;   // status set; the CTA still reaches its barriers
         }
         if (col_ok) {
             const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
@@ -457,18 +500,99 @@ __device__ __forceinline__ void ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, cons
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
     if (col_ok) {
-        float* row = a.dwh_part + (size_t)cta * 2 * (D + 1);
+        const int ns = ctrl_half_stride(D);
+        float4* row = reinterpret_cast<float4*>(a.dwh_part + (size_t)cta * 2 * ns);
+        row[2 * v_idx] = make_float4(accp[0], accp[1], accp[2], accp[3]);
+        row[2 * v_idx + 1] = make_float4(accp[4], accp[5], accp[6], accp[7]);
+        row[ns / 4 + 2 * v_idx] = make_float4(accr[0], accr[1], accr[2], accr[3]);
+        row[ns / 4 + 2 * v_idx + 1] = make_float4(accr[4], accr[5], accr[6], accr[7]);
+    }
+    float2 d = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            row[8 * v_idx + c] = accp[c];
-            row[(D + 1) + 8 * v_idx + c] = accr[c];
+    for (int c = 0; c < 8; ++c) {
+        d.x = fmaf(wp[c], accp[c], d.x);
+        d.y = fmaf(wr[c], accr[c], d.y);
+    }
+    return d;
+}
+
+// The reducer warp: the CTA's share of the modes, (dnu, dtheta) summed over
+// the per-segment rows of the reverse replay.  Lanes split the rows of up to
+// 32 modes into 32 / (modes) interleaved phases; the phase sums are added in
+// phase order.  Fixed order throughout.
+__device__ __forceinline__ void ctrl_bwd_modes(const SamuCtrlBwdArgs& a, int cta, int lane, float2* s_nm) {
+    const int M = a.D / 2;
+    const int m0 = (int)((long long)M * cta / a.cg.n_ctas), m1 = (int)((long long)M * (cta + 1) / a.cg.n_ctas);
+    const int rows = a.numod_rows;
+    for (int mc = m0; mc < m1; mc += 32) {
+        const int nm = min(32, m1 - mc);
+        const int q = 32 / nm;
+        const int mi = lane % nm, ph = lane / nm;
+        float2 acc = make_float2(0.f, 0.f);
+        if (ph < q) {
+            const float2* col = a.numod + mc + mi;
+            int r = ph;
+            for (; r + 3 * q < rows; r += 4 * q) {
+                float2 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = __ldcg(col + (size_t)(r + u * q) * M);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                }
+            }
+            for (; r < rows; r += q) {
+                const float2 v = __ldcg(col + (size_t)r * M);
+                acc.x += v.x;
+                acc.y += v.y;
+            }
         }
+        s_nm[lane] = acc;
+        __syncwarp();
+        if (lane < nm) {
+            float2 t = s_nm[lane];
+            for (int p = 1; p < q; ++p) {
+                t.x += s_nm[p * nm + lane].x;
+                t.y += s_nm[p * nm + lane].y;
+            }
+            a.dnu[mc + lane] = t.x;
+            a.dtheta[mc + lane] = t.y;
+        }
+        __syncwarp();
     }
 }
 
-__global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
+// Block-wide sum of four values, fixed order; every thread gets the totals.
+__device__ __forceinline__ float4 block_sum4(float4 v, float4* s_w) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+    }
+    __syncthreads();
+    if (lane == 0) s_w[warp] = v;
+    __syncthreads();
+    float4 t = s_w[0];
+    for (int w = 1; w < nwarps; ++w) {
+        const float4 u = s_w[w];
+        t.x += u.x;
+        t.y += u.y;
+        t.z += u.z;
+        t.w += u.w;
+    }
+    return t;
+}
+
+__global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    __shared__ float4 s_red[kCtrlMaxThreads / 32];
+    __shared__ float4 s_red[kCtrlBwdMaxThreads / 32];
+    __shared__ float2 s_nm[32];
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x;
@@ -478,14 +602,19 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_bwd_kernel(SamuCtrl
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
     const CtrlSmem sm = ctrl_smem(smem_raw, cg, D, true);
-    if (tid == 0) {
+    long long s0, s1;
+    ctrl_stage_range(cg, cta, s0, s1);
+    if (tid == 0) {   // the first stages go out before the scalar phase
         for (int i = 0; i < cg.ring; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], cg.consumers);
         }
+        for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st) {
+            const int nn = cg.stage_tok;
+            ctrl_issue(sm, (int)(st - s0), a.x, nullptr, st * nn, (int)min((long long)nn, a.BL - st * nn), D, cg,
+                       true);
+        }
     }
-    long long s0, s1;
-    ctrl_stage_range(cg, cta, s0, s1);
     const long long tb = s0 * cg.stage_tok;
     const long long te = min(a.BL, s1 * cg.stage_tok);
 
@@ -510,185 +639,175 @@ __global__ void __launch_bounds__(kCtrlMaxThreads) samu_ctrl_bwd_kernel(SamuCtrl
         const float opr = 1.0f + r * r;
         const float pbar = dbar * k_phi;
         const float rbar = cbar * k_r * (1.0f - r * r) / (opr * opr);
-        const float2 s = make_float2(pbar * (1.0f - p * p), rbar * (1.0f - r * r));
-        sc[t - tb] = s;
-        part.x += s.x;
-        part.y += s.y;
+        const float2 sv = make_float2(pbar * (1.0f - p * p), rbar * (1.0f - r * r));
+        sc[t - tb] = sv;
+        part.x += sv.x;
+        part.y += sv.y;
         part.z = fmaf(dbar, p, part.z);
         part.w = fmaf(cbar, r / opr, part.w);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        part.x += __shfl_xor_sync(0xffffffffu, part.x, o);
-        part.y += __shfl_xor_sync(0xffffffffu, part.y, o);
-        part.z += __shfl_xor_sync(0xffffffffu, part.z, o);
-        part.w += __shfl_xor_sync(0xffffffffu, part.w, o);
-    }
-    if (lane == 0) s_red[warp] = part;
-    __syncthreads();
+    const float4 tot = block_sum4(part, s_red);
     if (tid == 0) {
-        float4 t4 = s_red[0];
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-            t4.x += s_red[w].x;
-            t4.y += s_red[w].y;
-            t4.z += s_red[w].z;
-            t4.w += s_red[w].w;
-        }
-        float* row = a.dwh_part + (size_t)cta * 2 * (D + 1);
-        row[D] = t4.x;
-        row[(D + 1) + D] = t4.y;
-        a.amp_part[cta] = make_float2(t4.z, t4.w);
+        float* row = a.dwh_part + (size_t)cta * 2 * ctrl_half_stride(D);
+        row[D] = tot.x;
+        row[ctrl_half_stride(D) + D] = tot.y;
+        a.amp_part[cta] = make_float2(tot.z, tot.w);
     }
+    float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);   // this thread's share of w_hat . (partial row)
     if (warp == 0) {
         if (cg.stage_tok == 16)
             ctrl_bwd_producer<16>(a, sm, s0, s1, lane);
         else
             ctrl_bwd_producer<8>(a, sm, s0, s1, lane);
+        if (lane == 0) {   // the bias column
+            dv.x = a.wh[D] * tot.x;
+            dv.y = a.wh[2 * D + 1] * tot.y;
+        }
+    } else if (warp == 1) {
+        ctrl_bwd_modes(a, cta, lane, s_nm);
     } else {
-        if (cg.stage_tok == 16)
-            ctrl_bwd_consumer<16>(a, sm, s0, s1, warp - 1, lane, cta);
-        else
-            ctrl_bwd_consumer<8>(a, sm, s0, s1, warp - 1, lane, cta);
+        const float2 d = cg.stage_tok == 16 ? ctrl_bwd_consumer<16>(a, sm, s0, s1, warp - 2, lane, cta)
+                                            : ctrl_bwd_consumer<8>(a, sm, s0, s1, warp - 2, lane, cta);
+        dv.x = d.x;
+        dv.y = d.y;
     }
+    // w_hat . (this CTA's partial row), fixed order; summed over the CTAs by
+    // the parameter reduction (sum_r w_hat . row_r = w_hat . dw_hat)
+    const float4 dt = block_sum4(dv, s_red);
+    if (tid == 0) a.dot_part[cta] = make_float2(dt.x, dt.y);
 }
 
 // ---------------------------------------------------------------------------
-// Parameter reductions (fixed order, deterministic), one launch:
-//  - CTAs [0, ceil(M/32)): 32 modes each; warp w sums the per-segment
-//    (dnu, dtheta) rows w, w+32, ...; the 32 warp sums are added in order;
-//  - the next 2*ceil((D+1)/32) CTAs: 32 columns of dw_hat_phi or dw_hat_r
-//    each, summed the same way over the controller-backward partial rows
-//    (one per controller-backward CTA);
-//  - the CTA that arrives last (threadfence + counter) computes the
-//    unit-direction projection dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||
-//    and the amplitude gradients da = (sum of partials) / sqrt(M) (1 - tanh(a)^2),
-//    and clears the counter for the next call.
+// Parameter-gradient reductions, one launch right after the controller
+// backward (it waits for it with griddepcontrol.wait; its CTAs are small
+// enough to be resident beside it).  The controller backward's partial rows
+// (one per CTA; phi and r halves of ns = D+1 rounded up to 4 floats) are
+// summed column by column: warps 1..7 of CTA c take float4 columns of the
+// CTA's slice, lane l the rows l, l+32, ... in order, and the 32 lane sums
+// are combined by a fixed xor butterfly.  Warp 0 meanwhile sums the CTAs'
+// shares of w_hat . dw_hat (the same fixed order in every CTA), so each
+// column is projected onto the unit sphere's tangent at once,
+// dw = (dw_hat - w_hat (w_hat . dw_hat)) / ||w||; CTA 0 also forms the
+// amplitude gradients da = (sum of partials) / sqrt(M) (1 - tanh(a)^2).
 // ---------------------------------------------------------------------------
-constexpr int kParamWarps = 32;
-constexpr int kParamThreads = kParamWarps * 32;
+constexpr int kParamWarps = 8;
+constexpr int kParamThreads = 32 * kParamWarps;
+constexpr int kParamColWarps = kParamWarps - 1;
 
-// Block-wide sum of four values, fixed order; every thread gets the totals.
-__device__ __forceinline__ float4 block_sum4(float4 v, float4 (*s_w)[1]) {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+__device__ __forceinline__ float4 shfl_xor4(float4 v, int o) {
+    v.x = __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y = __shfl_xor_sync(0xffffffffu, v.y, o);
+    v.z = __shfl_xor_sync(0xffffffffu, v.z, o);
+    v.w = __shfl_xor_sync(0xffffffffu, v.w, o);
+    return v;
+}
+
+// Sum of src[0 .. count) over one warp: lane l adds elements l, l+32, ... in
+// order, then a fixed xor butterfly; every lane gets the total.
+__device__ __forceinline__ float2 warp_sum2(const float2* __restrict__ src, int count, int lane) {
+    float2 acc = make_float2(0.f, 0.f);
+    int i = lane;
+    for (; i + 96 < count; i += 128) {
+        float2 x[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-        v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
-        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+        for (int q = 0; q < 4; ++q) x[q] = __ldcg(src + i + 32 * q);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc.x += x[q].x;
+            acc.y += x[q].y;
+        }
     }
-    if (lane == 0) s_w[warp][0] = v;
-    __syncthreads();
-    float4 t = s_w[0][0];
-    for (int w = 1; w < kParamWarps; ++w) {
-        const float4 u = s_w[w][0];
-        t.x += u.x;
-        t.y += u.y;
-        t.z += u.z;
-        t.w += u.w;
+    for (; i < count; i += 32) {
+        const float2 x = __ldcg(src + i);
+        acc.x += x.x;
+        acc.y += x.y;
     }
-    return t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+    }
+    return acc;
+}
+
+// Column v (float4) of the [rows][nv] partial rows, summed over the rows as
+// above; every lane gets the total.
+__device__ __forceinline__ float4 column_sum(const float4* __restrict__ rows, int n_rows, int nv, int v, int lane) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int r = lane;
+    for (; r + 224 < n_rows; r += 256) {
+        float4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = __ldcg(rows + (size_t)(r + 32 * q) * nv + v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc = add4(acc, x[q]);
+    }
+    {
+        float4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            x[q] = r + 32 * q < n_rows ? __ldcg(rows + (size_t)(r + 32 * q) * nv + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (r + 32 * q < n_rows) acc = add4(acc, x[q]);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) acc = add4(acc, shfl_xor4(acc, o));
+    return acc;
+}
+
+__device__ __forceinline__ void project_column(const SamuParamArgs& a, int v, float4 acc, float2 t, int n, int ns) {
+    const float c[4] = {acc.x, acc.y, acc.z, acc.w};
+    const float nphi = a.misc[2], nr = a.misc[3];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int j = 4 * v + e;   // position in the flattened [2][ns] row
+        if (j < n)
+            a.dw_phi[j] = (c[e] - a.wh[j] * t.x) / nphi;
+        else if (j >= ns && j - ns < n)
+            a.dw_r[j - ns] = (c[e] - a.wh[n + (j - ns)] * t.y) / nr;
+    }
 }
 
 __global__ void __launch_bounds__(kParamThreads) samu_params_kernel(SamuParamArgs a) {
-    __shared__ float2 s_red[kParamWarps][32];
-    __shared__ float4 s_w[kParamWarps][1];
-    __shared__ int s_last;
+    __shared__ float2 s_t;
     pdl_trigger();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int M = a.D / 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = a.D + 1;
-    const int n_num = (M + 31) / 32;
-    if ((int)blockIdx.x < n_num) {
-        const int m = blockIdx.x * 32 + lane;
-        const int rows = a.B * a.n_part;
-        float2 sum = make_float2(0.f, 0.f);
-        if (m < M) {
-            int r = warp;
-            for (; r + 3 * kParamWarps < rows; r += 4 * kParamWarps) {
-                float2 v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = __ldcg(a.numod + (size_t)(r + q * kParamWarps) * M + m);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    sum.x += v[q].x;
-                    sum.y += v[q].y;
-                }
+    const int ns = ctrl_half_stride(a.D);
+    const int nv = ns / 2;   // float4 columns per row (2 ns floats)
+    const int cta = blockIdx.x, nc = gridDim.x;
+    const int v_lo = (int)((long long)nv * cta / nc), v_hi = (int)((long long)nv * (cta + 1) / nc);
+    const float4* rows = reinterpret_cast<const float4*>(a.dwh_part);
+    if (warp == 0) {
+        const float2 t = warp_sum2(a.dot_part, a.n_rows, lane);
+        if (lane == 0) s_t = t;
+        if (cta == 0) {
+            const float2 am = warp_sum2(a.amp_part, a.n_rows, lane);
+            if (lane == 0) {
+                const float ta = a.misc[4], tr = a.misc[5], ism = a.misc[6];
+                a.da_phi[0] = am.x * ism * (1.0f - ta * ta);
+                a.da_r[0] = am.y * ism * (1.0f - tr * tr);
             }
-            for (; r < rows; r += kParamWarps) {
-                const float2 v = __ldcg(a.numod + (size_t)r * M + m);
-                sum.x += v.x;
-                sum.y += v.y;
-            }
-        }
-        s_red[warp][lane] = sum;
-        __syncthreads();
-        if (warp == 0 && m < M) {
-            float2 t = s_red[0][lane];
-            for (int w = 1; w < kParamWarps; ++w) {
-                t.x += s_red[w][lane].x;
-                t.y += s_red[w][lane].y;
-            }
-            a.dnu[m] = t.x;
-            a.dtheta[m] = t.y;
-        }
-    } else {
-        const int cb = blockIdx.x - n_num;
-        const int which = cb & 1;
-        const int j = (cb >> 1) * 32 + lane;
-        float sum = 0.f;
-        if (j < n) {
-            int r = warp;
-            for (; r + 3 * kParamWarps < a.n_rows; r += 4 * kParamWarps) {
-                float v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = __ldcg(a.dwh_part + ((size_t)(r + q * kParamWarps) * 2 + which) * n + j);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) sum += v[q];
-            }
-            for (; r < a.n_rows; r += kParamWarps) sum += __ldcg(a.dwh_part + ((size_t)r * 2 + which) * n + j);
-        }
-        s_red[warp][lane].x = sum;
-        __syncthreads();
-        if (warp == 0 && j < n) {
-            float t = s_red[0][lane].x;
-            for (int w = 1; w < kParamWarps; ++w) t += s_red[w][lane].x;
-            a.dwh[(size_t)which * n + j] = t;
         }
     }
+    const int v0 = v_lo + warp - 1;
+    const bool own = warp > 0 && v0 < v_hi;
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (own) acc0 = column_sum(rows, a.n_rows, nv, v0, lane);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1 ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);   // w_hat . dw_hat (phi, r), amplitude sums (phi, r)
-    for (int j = threadIdx.x; j < n; j += kParamThreads) {
-        v.x = fmaf(a.wh[j], __ldcg(a.dwh + j), v.x);
-        v.y = fmaf(a.wh[n + j], __ldcg(a.dwh + n + j), v.y);
-    }
-    for (int k = threadIdx.x; k < a.n_rows; k += kParamThreads) {
-        const float2 u = __ldcg(a.amp_part + k);
-        v.z += u.x;
-        v.w += u.y;
-    }
-    const float4 t = block_sum4(v, s_w);
-    const float nphi = a.misc[2];
-    const float nr = a.misc[3];
-    for (int j = threadIdx.x; j < n; j += kParamThreads) {
-        a.dw_phi[j] = (__ldcg(a.dwh + j) - a.wh[j] * t.x) / nphi;
-        a.dw_r[j] = (__ldcg(a.dwh + n + j) - a.wh[n + j] * t.y) / nr;
-    }
-    if (threadIdx.x == 0) {
-        const float ta = a.misc[4], tr = a.misc[5], ism = a.misc[6];
-        a.da_phi[0] = t.z * ism * (1.0f - ta * ta);
-        a.da_r[0] = t.w * ism * (1.0f - tr * tr);
-        *a.counter = 0u;
+    const float2 t = s_t;
+    if (own && lane == 0) project_column(a, v0, acc0, t, n, ns);
+    if (warp > 0) {
+        for (int v = v0 + kParamColWarps; v < v_hi; v += kParamColWarps) {
+            const float4 acc = column_sum(rows, a.n_rows, nv, v, lane);
+            if (lane == 0) project_column(a, v, acc, t, n, ns);
+        }
     }
 }
 
@@ -716,23 +835,28 @@ int ctrl_sms() {
 
 CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
     CtrlGeom cg;
-    // stages of 16 tokens (8 when 16 rows exceed 64 KB), as many slots as fit
-    // in kCtrlRingBytes
-    cg.stage_tok = 2 * D * 16 <= 64 * 1024 ? 16 : 8;
-    int ring = (int)(kCtrlRingBytes / ((size_t)cg.stage_tok * ctrl_row_bytes(D, backward)));
-    if (ring > kCtrlRingMax) ring = kCtrlRingMax;
-    if (ring < 2) ring = 2;
-    cg.ring = ring;
+    // forward: swizzled tiled copies when D is a multiple of 64 (and token
+    // coordinates fit the copy's 32-bit coordinates)
+    cg.swz = (!backward && D % 64 == 0 && BL < (1ll << 31)) ? 1 : 0;
+    const size_t row = ctrl_row_bytes(cg, D, backward);
+    // stages of 16 tokens, or 8 when 16 rows exceed 72 KB
+    cg.stage_tok = 16 * row <= 72 * 1024 ? 16 : 8;
     cg.consumers = (D / 8 + 31) / 32;
     if (cg.consumers < 1) cg.consumers = 1;
-    cg.threads = 32 * (1 + cg.consumers);
+    cg.threads = 32 * (2 + cg.consumers);   // producer, mode (forward) or reducer (backward) warp, consumers
     cg.n_stages = (BL + cg.stage_tok - 1) / cg.stage_tok;
     {   // tokens of the longest CTA range: there are at least min(stages, SMs) CTAs
         const long long fewest = cg.n_stages < ctrl_sms() ? cg.n_stages : ctrl_sms();
         cg.max_cta_tok = (int)((cg.n_stages + fewest - 1) / fewest * cg.stage_tok);
     }
-    const size_t xb = (ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15);
-    cg.smem = (int)(ctrl_ring_bytes(cg, D, backward) + xb + 3 * cg.ring * sizeof(uint64_t));
+    // as many ring slots (2 .. kCtrlRingMax) as fit with the exchange buffer
+    // and the barriers
+    const size_t cap = backward ? kCtrlBwdSmemMax : kCtrlFwdSmemMax;
+    for (cg.ring = kCtrlRingMax;; --cg.ring) {
+        const size_t xb = (ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15);
+        cg.smem = (int)(ctrl_ring_bytes(cg, D, backward) + xb + 3 * cg.ring * sizeof(uint64_t));
+        if ((size_t)cg.smem <= cap || cg.ring == 2) break;
+    }
     int per_sm = (int)((227 * 1024) / (cg.smem + 1024));
     const int by_threads = 2048 / cg.threads;
     if (per_sm > by_threads) per_sm = by_threads;
@@ -745,15 +869,20 @@ CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
     return cg;
 }
 
-cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args_in, cudaStream_t s, bool pdl) {
+cudaError_t launch_samu_ctrl_fwd(const CUtensorMap& tm_x, const SamuCtrlFwdArgs& args_in, cudaStream_t s, bool pdl) {
     SamuCtrlFwdArgs a = args_in;
-    const int M = a.D / 2;
-    a.n_mode_ctas = (M + kModeThreads - 1) / kModeThreads;
     a.cg = samu_ctrl_geom(a.BL, a.D, false);
     const cudaError_t e =
         cudaFuncSetAttribute(samu_ctrl_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, a.cg.smem);
     if (e != cudaSuccess) return e;
-    return launch_ex(samu_ctrl_fwd_kernel, a.n_mode_ctas + a.cg.n_ctas, a.cg.threads, (size_t)a.cg.smem, s, pdl, a);
+    return launch_ex(samu_ctrl_fwd_kernel, a.cg.n_ctas, a.cg.threads, (size_t)a.cg.smem, s, pdl, tm_x, a);
+}
+
+cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl) {
+    // one float4 column per column warp
+    const int nv = ctrl_half_stride(args.D) / 2;
+    const int ctas = (nv + kParamColWarps - 1) / kParamColWarps;
+    return launch_ex(samu_params_kernel, ctas, kParamThreads, 0, s, pdl, args);
 }
 
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl) {
@@ -763,10 +892,5 @@ cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bo
     return launch_ex(samu_ctrl_bwd_kernel, args.cg.n_ctas, args.cg.threads, (size_t)args.cg.smem, s, pdl, args);
 }
 
-cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl) {
-    const int M = args.D / 2;
-    const int blocks = (M + 31) / 32 + 2 * ((args.D + 1 + 31) / 32);
-    return launch_ex(samu_params_kernel, blocks, kParamThreads, 0, s, pdl, args);
-}
 
 }  // namespace lrs

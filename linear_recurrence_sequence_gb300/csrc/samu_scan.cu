@@ -93,7 +93,7 @@ __device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane
     const bool ok = fabsf(n0) * emax < kPolyBound && fabsf(n1) * emax < kPolyBound;
     SubKind kd;
     kd.fast = __all_sync(0xffffffffu, ok);
-    kd.simple = nsub == N && !__any_sync(0xffffffffu, mine && rst != 0.f);
+    kd.simple = nsub == N && !__any_sync(0xffffffffu, mine && is_reset_word(rst));
     return kd;
 }
 
@@ -110,6 +110,22 @@ __device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane
                 FN<false, true>(__VA_ARGS__);          \
             else                                       \
                 FN<false, false>(__VA_ARGS__);         \
+        }                                              \
+    } while (0)
+
+// The same with a third template argument X passed through.
+#define LRS_SUB_DISPATCH_X(kd, FN, X, ...)             \
+    do {                                               \
+        if (kd.fast) {                                 \
+            if (kd.simple)                             \
+                FN<true, true, X>(__VA_ARGS__);        \
+            else                                       \
+                FN<true, false, X>(__VA_ARGS__);       \
+        } else {                                       \
+            if (kd.simple)                             \
+                FN<false, true, X>(__VA_ARGS__);       \
+            else                                       \
+                FN<false, false, X>(__VA_ARGS__);      \
         }                                              \
     } while (0)
 
@@ -203,34 +219,37 @@ __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* w
 }
 
 // hmid: where the state entering token 8 of the sub-chunk is kept (the
-// backward restarts there), or null.
-template <bool FAST, bool SIMPLE>
+// backward restarts there); written by active lanes only.  The step
+// z <- lambda z + b is one complex fused multiply-add (four paired FMAs).
+template <bool FAST, bool SIMPLE, bool Y32>
 __device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
                                                const ModePair& k, c2x& z, uint32_t* yp, float* y32p, bool active,
                                                size_t row, int half, f2x* hmid) {
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
-        if (i == kHalf && hmid != nullptr && (SIMPLE || i < nsub)) {
+        if (i == kHalf && active && (SIMPLE || i < nsub)) {
             hmid[0] = z.re;
             hmid[1] = z.im;
         }
         if (SIMPLE || i < nsub) {
             const Ctl2 ct = load_ctl(sc, i);
-            c2x bb;
-            bb.re = bf2x(wre[i * kWords]);
-            bb.im = bf2x(wim[i * kWords]);
+            const f2x bre = bf2x(wre[i * kWords]);
+            const f2x bim = bf2x(wim[i * kWords]);
             if (SIMPLE || !is_reset(ct)) {
-                const c2x u = cmul2(samu_lambda2<FAST>(k, ct), z);
-                z.re = add2(u.re, bb.re);
-                z.im = add2(u.im, bb.im);
+                const Lam2 l = samu_lambda2<FAST>(k, ct);
+                const f2x zr = fma2(l.re, z.re, fma2(l.nim, z.im, bre));
+                const f2x zi = fma2(l.re, z.im, fma2(l.im, z.re, bim));
+                z.re = zr;
+                z.im = zi;
             } else {
-                z = bb;
+                z.re = bre;
+                z.im = bim;
             }
             if (active) {
                 uint32_t* o = yp + (size_t)i * row;
                 __stcs(o, x2bf(z.re));
                 __stcs(o + half, x2bf(z.im));
-                if (y32p != nullptr) {
+                if (Y32) {
                     f2x* f = reinterpret_cast<f2x*>(y32p + (size_t)i * 2 * row);
                     f[0] = z.re;
                     f[half] = z.im;   // M floats further: the imaginary half
@@ -408,6 +427,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     if (threadIdx.x == 0) a.counters[chain] = 0u;
 }
 
+template <bool Y32>
 __global__ void __launch_bounds__(kEngineThreads, 3)
     samu_fwd_replay_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ctrl,
                            SamuScanFwdArgs a) {
@@ -474,9 +494,10 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
-        float* y32p = a.y32 != nullptr ? a.y32 + 2 * row0 : nullptr;
+        float* y32p = Y32 ? a.y32 + 2 * row0 : nullptr;
         const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
-        LRS_SUB_DISPATCH(kd, fwd_replay_sub, sc, wre, wim, nsub, k, z, a.y + row0, y32p, active, D / 2, M / 2, hmid);
+        LRS_SUB_DISPATCH_X(kd, fwd_replay_sub, Y32, sc, wre, wim, nsub, k, z, a.y + row0, y32p, active, D / 2, M / 2,
+                           hmid);
         __syncwarp();
         if (lane == 0 && it + kRing < T.nsc)
             ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
@@ -721,11 +742,11 @@ __device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane)
 // token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64 modes
 // of the warp (written to kp[token * kp_row + {0, 1}]); then
 // A <- conj(lambda_t) A.
-template <bool SIMPLE>
+template <bool SIMPLE, bool FP32>
 __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nh,
                                                  float nu0, float nu1, const c2x (&u)[kHalf],
                                                  const f2x (&lre)[kHalf], const f2x (&lim)[kHalf], c2x& A,
-                                                 f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf, bool fp32,
+                                                 f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf,
                                                  bool active, size_t row, int half, float* kp, size_t kp_row,
                                                  int lane) {
     float v[2 * kHalf];
@@ -738,7 +759,7 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_
             A.re = add2(A.re, bf2x(gre[i * kWords]));
             A.im = add2(A.im, bf2x(gim[i * kWords]));
             if (active) {
-                if (fp32) {
+                if (FP32) {
                     f2x* p = reinterpret_cast<f2x*>(dwf + 2 * (size_t)i * row);
                     p[0] = A.re;
                     p[half] = A.im;   // M floats further: the imaginary half
@@ -752,8 +773,7 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_
                 // kappa = A conj(u)
                 const f2x kr = fma2(A.re, u[i].re, mul2(A.im, u[i].im));
                 const f2x ki = fma2(A.im, u[i].re, mul2(sub2(0ull, A.re), u[i].im));
-                const f2x nE = sub2(dup2(-1.0f), ct.e);   // -E_t
-                acc_nu = fma2(nE, kr, acc_nu);
+                acc_nu = fma2(ct.ne, kr, acc_nu);   // -E_t Re kappa
                 acc_th = add2(acc_th, ki);
                 float ki0, ki1, kr0, kr1;
                 up2(ki, ki0, ki1);
@@ -774,6 +794,7 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_
     if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
 }
 
+template <bool FP32>
 __global__ void __launch_bounds__(kEngineThreads, 2)
     samu_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_ctrl, SamuScanBwdArgs a) {
@@ -835,7 +856,6 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         A.im = pk2(r0.y, r1.y);
     }
     f2x acc_nu = 0ull, acc_th = 0ull;
-    const bool fp32 = a.grad_fp32 != 0;
     for (int it = 0; it < n_items; it += 2) {
         const int ts = item_ts(it);
         const int nh = min(kHalf, T.t_end - ts);
@@ -867,13 +887,13 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
         float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
         if (kd.simple)
-            bwd_reverse_unit<true>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre, lim,
-                                   A, acc_nu, acc_th, dwb, dwf, fp32, active, D / 2, M / 2, kp,
-                                   2 * (size_t)g.n_groups, lane);
+            bwd_reverse_unit<true, FP32>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre,
+                                         lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
+                                         2 * (size_t)g.n_groups, lane);
         else
-            bwd_reverse_unit<false>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre,
-                                    lim, A, acc_nu, acc_th, dwb, dwf, fp32, active, D / 2, M / 2, kp,
-                                    2 * (size_t)g.n_groups, lane);
+            bwd_reverse_unit<false, FP32>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u,
+                                          lre, lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
+                                          2 * (size_t)g.n_groups, lane);
         __syncwarp();
         if (lane == 0 && it + 1 + kRingH < n_items)
             ringh_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
@@ -919,15 +939,19 @@ const EngineOccupancy& engine_occupancy() {
         int v = 0;
         o.sms = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;
         const void* fm = reinterpret_cast<const void*>(samu_fwd_maps_kernel);
-        const void* fr = reinterpret_cast<const void*>(samu_fwd_replay_kernel);
+        const void* fr = reinterpret_cast<const void*>(samu_fwd_replay_kernel<false>);
+        const void* fr32 = reinterpret_cast<const void*>(samu_fwd_replay_kernel<true>);
         const void* bm = reinterpret_cast<const void*>(samu_bwd_maps_kernel);
-        const void* bb = reinterpret_cast<const void*>(samu_bwd_main_kernel);
+        const void* bb = reinterpret_cast<const void*>(samu_bwd_main_kernel<false>);
+        const void* bb32 = reinterpret_cast<const void*>(samu_bwd_main_kernel<true>);
         set_smem(fm);
         set_smem(fr);
+        set_smem(fr32);
         set_smem(bm);
         set_smem(bb);
-        o.fwd = std::min(occupancy(fm), occupancy(fr));
-        o.bwd = std::min(occupancy(bm), occupancy(bb));
+        set_smem(bb32);
+        o.fwd = std::min(occupancy(fm), std::min(occupancy(fr), occupancy(fr32)));
+        o.bwd = std::min(occupancy(bm), std::min(occupancy(bb), occupancy(bb32)));
         o.done = true;
     }
     return o;
@@ -954,8 +978,11 @@ cudaError_t launch_samu_fwd_maps(const CUtensorMap& tm_w, const CUtensorMap& tm_
 
 cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl, const SamuScanFwdArgs& args,
                                    cudaStream_t s, bool pdl) {
-    return launch_ex(samu_fwd_replay_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_w, tm_ctrl,
-                     args);
+    if (args.y32 != nullptr)
+        return launch_ex(samu_fwd_replay_kernel<true>, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_w,
+                         tm_ctrl, args);
+    return launch_ex(samu_fwd_replay_kernel<false>, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_w,
+                     tm_ctrl, args);
 }
 
 cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
@@ -966,8 +993,11 @@ cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm
 
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
                                  const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
-    return launch_ex(samu_bwd_main_kernel, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_w,
-                     tm_ctrl, args);
+    if (args.grad_fp32)
+        return launch_ex(samu_bwd_main_kernel<true>, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy,
+                         tm_w, tm_ctrl, args);
+    return launch_ex(samu_bwd_main_kernel<false>, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy,
+                     tm_w, tm_ctrl, args);
 }
 
 }  // namespace lrs

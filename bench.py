@@ -3,9 +3,12 @@
 
 One step = samu_forward + samu_backward (BF16 gradients) through the C ABI on
 the B=1, L=32768, D=2048 workload (the metric's configuration), inputs
-resident in HBM.  L2 is flushed (256 MiB memset) before every timed step and
-each step is timed with its own CUDA events; the memset is outside the timed
-events.  Alongside the device-timed value the line carries:
+resident in HBM.  The step's launches are captured once as a CUDA graph and
+replayed; L2 is flushed (256 MiB memset) before every timed step and each step
+is timed with its own CUDA events; the memset is outside the timed events.
+Per-kernel durations come from a second, eager pass with the library's own
+events around every launch.  Alongside the device-timed value the line
+carries:
   e2e          the same metric through the public Python API with host (pinned)
                inputs copied in and results copied out inside the timed region;
   roofline     the dominant kernel's algorithmic bytes / its average CUDA-event
@@ -268,9 +271,15 @@ def run_ours(args, rank, world, local):
     scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
     fo = {"y": torch.empty((B, L, D), dtype=torch.bfloat16, device=dev),
           "hT": torch.empty((B, M, 2), dtype=torch.float32, device=dev)}
-    go = {k: None for k in ("dx_sel", "dw", "dh0", "dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r")}
-    go["dx_sel"] = torch.empty((B, L, D), dtype=torch.bfloat16, device=dev)
-    go["dw"] = torch.empty((B, L, D), dtype=torch.bfloat16, device=dev)
+    go = {"dx_sel": torch.empty((B, L, D), dtype=torch.bfloat16, device=dev),
+          "dw": torch.empty((B, L, D), dtype=torch.bfloat16, device=dev),
+          "dh0": torch.empty((B, M, 2), dtype=torch.float32, device=dev),
+          "dnu": torch.empty((M,), dtype=torch.float32, device=dev),
+          "dtheta": torch.empty((M,), dtype=torch.float32, device=dev),
+          "dw_phi": torch.empty((D + 1,), dtype=torch.float32, device=dev),
+          "dw_r": torch.empty((D + 1,), dtype=torch.float32, device=dev),
+          "da_phi": torch.empty((1,), dtype=torch.float32, device=dev),
+          "da_r": torch.empty((1,), dtype=torch.float32, device=dev)}
 
     def step(x_sel, w, dy):
         api.samu_forward(x_sel, w, t["h0"], t["reset"], t["nu"], t["theta"], t["w_phi"], t["w_r"],
@@ -287,26 +296,39 @@ def run_ours(args, rank, world, local):
     if api.device_status(scratch) != 0:
         raise RuntimeError("device-side wait timed out during warm-up")
 
+    # The step as one CUDA graph (the same launches, without the per-call host
+    # work); captured on a side stream after the eager warm-up.
+    cap_stream = torch.cuda.Stream(dev)
+    cap_stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cap_stream):
+        step(t["x_sel"], t["w"], t["dy"])
+    torch.cuda.current_stream(dev).wait_stream(cap_stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap_stream):
+        step(t["x_sel"], t["w"], t["dy"])
+    for _ in range(3):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize(dev)
+
     K = args.steps
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     sampler = ClockSampler(gpu_selector(dev))
     sampler.start()
     time.sleep(0.1)
-    cap = K * 8
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    api.profile_begin(cap)
     for i in range(K):
         flush.zero_()
         ev0[i].record()
-        step(t["x_sel"], t["w"], t["dy"])
+        graph.replay()
         ev1[i].record()
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
-    records, n_launch_records = api.profile_end(cap)
     clocks = sampler.stop()
     if api.device_status(scratch) != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -315,12 +337,27 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_ms / K
     value = world * B * L * K / (total_ms / 1e3) / 1e6
 
+    # Per-kernel durations: the same steps again, eagerly, with the library's
+    # own CUDA events around every launch (on the launching stream; this
+    # serialises the launches, so these steps are not part of the value).
+    KP = max(3, min(K, 20))
+    cap = KP * 8
+    api.profile_begin(cap)
+    for i in range(KP):
+        flush.zero_()
+        step(t["x_sel"], t["w"], t["dy"])
+    torch.cuda.synchronize(dev)
+    records, n_launch_records = api.profile_end(cap)
+    if api.device_status(scratch) != 0:
+        raise RuntimeError("device-side wait timed out during the per-kernel pass")
+
     # per-kernel averages and the dominant kernel's roofline
     per = {}
-    launches = 0
+    launches_prof = 0
     for name, ms in records:
         per.setdefault(name, []).append(ms)
-        launches += LAUNCHES_PER_RECORD.get(name, 1)
+        launches_prof += LAUNCHES_PER_RECORD.get(name, 1)
+    launches = launches_prof // KP * K   # the timed steps launch the same kernels
     avg = {k: sum(v) / len(v) for k, v in per.items()}
     dom = max((k for k in avg if k in KERNEL_BYTES_PER_BLD), key=lambda k: avg[k] * len(per[k]))
     peak, peak_src = load_peak()
@@ -330,7 +367,7 @@ def run_ours(args, rank, world, local):
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": load_traffic(dom, BLD), "algorithmic_bytes": alg,
-                "avg_launch_ms": round(avg[dom], 5)}
+                "avg_launch_ms": round(avg[dom], 5), "timing": f"library CUDA events, {KP} eager steps"}
 
     # end to end through the public API with pinned host buffers: every step
     # copies its inputs in (pinned host -> device) and its results out
@@ -420,6 +457,7 @@ def run_ours(args, rank, world, local):
         "config": {"workload": f"samu_fb_B{B}_L{L}_D{D}", "B": B, "L": L, "D": D, "grad_dtype": "bf16",
                    "h0": wl.h0, "reset_p": wl.reset_p, "seed": shard_seed(wl.seeds[0], rank),
                    "l2": "flushed before every timed step (256 MiB memset outside the step events)",
+                   "launch": "the step (forward + backward through the C ABI) replayed as one CUDA graph",
                    "per_gpu_batch": B},
         "achieved_step_gbs": round(STEP_BYTES_PER_BLD * BLD / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": roofline,

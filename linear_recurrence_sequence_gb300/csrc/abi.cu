@@ -212,12 +212,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.status = at<uint32_t>(scratch, sc.status);
     cf.counters = at<uint32_t>(scratch, sc.counters);   // the forward's half
     cf.n_counters = samu_seg_geom(B, L, M, 0).n_chains;
-    CUtensorMap tm_x{};
-    {
-        const CtrlGeom cgf = samu_ctrl_geom(BL, D, false);
-        if (cgf.swz && !make_ctrl_x_map(&tm_x, x_sel, BL, D, cgf.stage_tok)) return LRS_ERR_CUDA;
-    }
-    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(tm_x, cf, stream, false));
+    LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream, false));
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
     CUtensorMap tm_w, tm_ctrl;
@@ -298,7 +293,7 @@ int samu_backward(const void* dy, const float* dhT,
     cb.BL = (long long)B * L;
     cb.D = D;
     cb.n_groups = g.n_groups;
-    cb.cg = samu_ctrl_geom(cb.BL, D, true);
+    cb.cg = samu_ctrl_geom(cb.BL, D);
     cb.status = s.status;
     cb.x = static_cast<const uint4*>(x_sel);
     cb.kpart = s.kpart;

@@ -224,23 +224,22 @@ struct SamuScanBwdArgs {
     uint32_t* status;
 };
 
-// Controller streaming geometry: every CTA owns a contiguous run of
+// Controller-backward streaming geometry: every CTA owns a contiguous run of
 // `stage_tok`-token stages of x_sel (and of dx_sel), staged through a ring of
-// `ring` shared-memory slots by 1-D bulk copies; one producer warp plus
-// `consumers` warps of 32 threads, each thread owning 8 channels.
+// `ring` shared-memory slots by 1-D bulk copies; a producer warp, a reducer
+// warp and `consumers` warps of 32 threads, each thread owning 8 channels.
 struct CtrlGeom {
-    int stage_tok;          // tokens per stage (16, or 8 when 16 rows exceed 36 KB)
+    int stage_tok;          // tokens per stage (16, or 8 when 16 rows exceed 72 KB)
     int ring;               // slots (2 to 8, as many as fit)
     int consumers;          // consumer warps
-    int threads;            // 32 * (1 + consumers)
+    int threads;            // 32 * (2 + consumers)
     int smem;               // dynamic shared memory bytes
     int n_ctas;             // streaming CTAs
     long long n_stages;     // ceil(B*L / stage_tok)
-    int max_cta_tok;        // tokens of the longest CTA range (backward scalar buffer)
-    int swz;                // forward: stages as swizzled tiled copies (D a multiple of 64)
+    int max_cta_tok;        // tokens of the longest CTA range (scalar buffer)
 };
 
-CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward);
+CtrlGeom samu_ctrl_geom(long long BL, int D);
 
 struct SamuCtrlBwdArgs {
     long long BL;
@@ -282,7 +281,6 @@ struct SamuParamArgs {
 struct SamuCtrlFwdArgs {
     long long BL;
     int D;
-    CtrlGeom cg;                   // filled by the launcher
     const uint4* x;                // BF16 x_sel as 16-byte vectors
     const uint8_t* reset;
     const float* w_phi;
@@ -302,9 +300,7 @@ struct SamuCtrlFwdArgs {
     uint32_t* status;
 };
 
-// tm_x: make_ctrl_x_map over x_sel with samu_ctrl_geom(B*L, D, false).stage_tok
-// rows when that geometry's swz is set (unused otherwise).
-cudaError_t launch_samu_ctrl_fwd(const CUtensorMap& tm_x, const SamuCtrlFwdArgs& args, cudaStream_t s, bool pdl);
+cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& args, cudaStream_t s, bool pdl);
 // Segment geometry of the forward (backward = false) or backward scan on the
 // current device: every segment of every chain resident at once.
 SegGeom samu_scan_geom(int B, int L, int M, bool backward);

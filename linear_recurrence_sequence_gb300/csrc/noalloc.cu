@@ -107,12 +107,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     cf.status = reinterpret_cast<uint32_t*>(scratch + sc.status);
     cf.counters = reinterpret_cast<uint32_t*>(scratch + sc.counters);   // the forward's half
     cf.n_counters = samu_seg_geom(B, L, M, 0).n_chains;
-    CUtensorMap tm_x{};
-    {
-        const CtrlGeom cgf = samu_ctrl_geom(cf.BL, D, false);
-        if (cgf.swz && !make_ctrl_x_map(&tm_x, x_sel, cf.BL, D, cgf.stage_tok)) return LRS_ERR_CUDA;
-    }
-    if (launch_samu_ctrl_fwd(tm_x, cf, stream, false) != cudaSuccess) return LRS_ERR_CUDA;
+    if (launch_samu_ctrl_fwd(cf, stream, false) != cudaSuccess) return LRS_ERR_CUDA;
 
     CUtensorMap tm_w, tm_ctrl;
     if (!make_bf16_map(&tm_w, w, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub)) return LRS_ERR_CUDA;

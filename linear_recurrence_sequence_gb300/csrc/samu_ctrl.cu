@@ -15,98 +15,64 @@
 namespace lrs {
 
 // ---------------------------------------------------------------------------
-// Streaming layout shared by the controller forward and backward.
+// Streaming layout of the controller backward.
 //
-// Every streaming CTA owns a contiguous run of stages of cg.stage_tok tokens.
-// Warp 0 is the producer: lane 0 copies each stage's x_sel rows (contiguous
-// in memory) into a ring of cg.ring shared-memory slots with one 1-D bulk
-// copy, and the warp does the per-token scalar work.  Warps 1..C are the
-// consumers: thread (warp, lane) owns channels 8v .. 8v+7, v = 32 (warp-1) +
+// Every CTA owns a contiguous run of stages of cg.stage_tok tokens.  Warp 0
+// is the producer: lane 0 copies each stage's x_sel rows (contiguous in
+// memory) into a ring of cg.ring shared-memory slots with one 1-D bulk copy.
+// Warp 1 is the reducer (per-mode parameter sums).  Warps 2..C+1 are the
+// consumers: thread (warp, lane) owns channels 8v .. 8v+7, v = 32 (warp-2) +
 // lane, with its unit-direction weights in registers.
 //
-// Shared memory: ring[slot][token][D] BF16 | per-slot exchange buffer |
+// Shared memory: ring[slot][token][D] BF16 | per-token scalars of the range |
 // mbarriers.
 // ---------------------------------------------------------------------------
 constexpr int kCtrlRingMax = 8;                        // ring slots (at most)
-constexpr size_t kCtrlFwdSmemMax = 226 * 1024;          // forward: ring + exchange buffer + barriers
-constexpr size_t kCtrlBwdSmemMax = 200 * 1024;          // backward: leaves room for the reduction CTAs
-constexpr int kCtrlMaxThreads = 32 * (2 + 16);      // forward, D = 4096: 16 consumer warps + 2
-constexpr int kCtrlBwdMaxThreads = 32 * (2 + 16);   // backward: plus the reducer warp
+constexpr size_t kCtrlBwdSmemMax = 200 * 1024;          // leaves room for the reduction CTAs
+constexpr int kCtrlBwdMaxThreads = 32 * (2 + 16);       // D = 4096: 16 consumer warps + 2
 
 struct CtrlSmem {
     uint8_t* ring;
-    float* xbuf;        // forward: partial dots [slot][consumer][32]; backward: float2 scalars [slot][token]
+    float* xbuf;        // float2 scalars [token of the range]
     uint64_t* full;     // x rows landed (producer arrival + bytes)
-    uint64_t* ready;    // forward: partials written (consumers); backward: scalars written (producer)
-    uint64_t* empty;    // backward: slot consumed (consumers)
+    uint64_t* empty;    // slot consumed (consumers)
 };
 
-// Shared-memory bytes per x_sel row in a ring slot.  The backward keeps rows
-// packed (one bulk copy per stage).  The forward, when D is a multiple of 64,
-// stages each stage with one tiled TMA copy in the 128-byte swizzled layout
-// [64-channel chunk][token][128 bytes] (16-byte unit u of (chunk c, token r)
-// stored at unit u ^ (r mod 8)), so that the eight rows an ldmatrix reads
-// fall in distinct banks; otherwise it pads each row by 16 bytes (one bulk
-// copy per row).
-__host__ __device__ inline size_t ctrl_row_bytes(const CtrlGeom& cg, int D, bool backward) {
-    return 2 * (size_t)D + ((backward || cg.swz) ? 0 : 16);
+__host__ __device__ inline size_t ctrl_slot_bytes(const CtrlGeom& cg, int D) {
+    return (size_t)cg.stage_tok * 2 * (size_t)D;
 }
 
-__host__ __device__ inline size_t ctrl_slot_bytes(const CtrlGeom& cg, int D, bool backward) {
-    return (size_t)cg.stage_tok * ctrl_row_bytes(cg, D, backward);
-}
+__host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D) { return (size_t)cg.ring * ctrl_slot_bytes(cg, D); }
 
-__host__ __device__ inline size_t ctrl_ring_bytes(const CtrlGeom& cg, int D, bool backward) {
-    return (size_t)cg.ring * ctrl_slot_bytes(cg, D, backward);
-}
+__host__ __device__ inline size_t ctrl_xbuf_bytes(const CtrlGeom& cg) { return (size_t)cg.max_cta_tok * 8; }
 
-// Forward: the consumers' partial tiles, ring + 1 sets (stage k uses set
-// k mod (ring + 1); stage k + ring + 1 is issued only after the producer has
-// read set k); backward: the per-token scalars of the range.
-__host__ __device__ inline int ctrl_xsets(const CtrlGeom& cg) { return cg.ring + 1; }
-__host__ __device__ inline size_t ctrl_xbuf_bytes(const CtrlGeom& cg, bool backward) {
-    return backward ? (size_t)cg.max_cta_tok * 8 : (size_t)ctrl_xsets(cg) * cg.consumers * 32 * 16;
-}
-
-__device__ __forceinline__ CtrlSmem ctrl_smem(uint8_t* base, const CtrlGeom& cg, int D, bool backward) {
+__device__ __forceinline__ CtrlSmem ctrl_smem(uint8_t* base, const CtrlGeom& cg, int D) {
     CtrlSmem sm;
     sm.ring = base;
-    const size_t rb = ctrl_ring_bytes(cg, D, backward);
+    const size_t rb = ctrl_ring_bytes(cg, D);
     sm.xbuf = reinterpret_cast<float*>(base + rb);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + rb + ((ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15)));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + rb + ((ctrl_xbuf_bytes(cg) + 15) & ~size_t(15)));
     sm.full = bars;
-    sm.ready = bars + cg.ring;
-    sm.empty = bars + 2 * cg.ring;
+    sm.empty = bars + cg.ring;
     return sm;
 }
 
-// Stages [s0, s1) of the streaming CTA `cta`.
+// Stages [s0, s1) of the CTA `cta`.
 __device__ __forceinline__ void ctrl_stage_range(const CtrlGeom& cg, int cta, long long& s0, long long& s1) {
     s0 = cg.n_stages * cta / cg.n_ctas;
     s1 = cg.n_stages * (cta + 1) / cg.n_ctas;
 }
 
 // Producer lane 0: the rows of stage (token t0, n tokens) into ring slot
-// `slot`: one bulk copy (backward, packed rows), one tiled copy of the whole
-// stage box (forward, swizzled; rows past B*L read as zero and count towards
-// the transaction bytes), or one bulk copy per row (forward, padded rows).
-__device__ __forceinline__ void ctrl_issue(const CtrlSmem& sm, int slot, const uint4* x, const CUtensorMap* tm,
-                                           long long t0, int n, int D, const CtrlGeom& cg, bool backward) {
+// `slot` as one bulk copy.
+__device__ __forceinline__ void ctrl_issue(const CtrlSmem& sm, int slot, const uint4* x, long long t0, int n, int D,
+                                           const CtrlGeom& cg) {
     const uint32_t row = 2u * (uint32_t)D;
-    uint8_t* dst = sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D, backward);
+    uint8_t* dst = sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D);
     const uint8_t* src = reinterpret_cast<const uint8_t*>(x) + (size_t)t0 * row;
     fence_proxy_async();
-    if (backward) {
-        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
-        bulk_load(dst, src, (uint32_t)n * row, &sm.full[slot]);
-    } else if (cg.swz) {
-        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)cg.stage_tok * row);
-        tma_load_3d(dst, tm, 0, (int)t0, 0, &sm.full[slot]);
-    } else {
-        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
-        const size_t pitch = ctrl_row_bytes(cg, D, false);
-        for (int i = 0; i < n; ++i) bulk_load(dst + (size_t)i * pitch, src + (size_t)i * row, row, &sm.full[slot]);
-    }
+    mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)n * row);
+    bulk_load(dst, src, (uint32_t)n * row, &sm.full[slot]);
 }
 
 __device__ __forceinline__ void unpack8(const uint4 q, float (&x)[8]) {
@@ -129,225 +95,99 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 }
 
 // ---------------------------------------------------------------------------
-// Controller forward, with the parameter preparation folded in.  One CTA per
-// SM, each on a contiguous run of stages; thread 0 starts the first stages'
-// copies before anything else.
-//  - A mode warp computes the CTA's share of the per-mode transition
-//    constants lbar_m = e^{-nu_m} e^{i theta_m} as double-floats (hi, lo) in
-//    FP64, beside the stream (warps: 0 producer, 1 modes, 2.. consumers).
-//  - Every CTA computes the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32,
-//    fixed-order tree, the same in every CTA).  The dot products x~ . w_hat of
-//    a stage of 16 tokens are one tensor-core contraction [16 tokens x D] x
-//    [D x 8]: consumer warp c takes the 16-channel k-steps 16c .. 16c+15
-//    (mma.sync m16n8k16, BF16 operands, FP32 accumulation), A is the x_sel
-//    rows in shared memory (ldmatrix), B holds per channel the exact
-//    three-way BF16 split w_hat = hi + mid + lo of both directions in columns
-//    0-2 (phi) and 3-5 (r), so each product is exact and the sum is FP32.
-//    The producer adds the consumers' partial tiles and the three split
-//    columns in a fixed order and evaluates p = tanh(s_phi), r = tanh(s_r),
-//    q(r), d, c, and E - 1 = expm1(c), C = cos d, S = sin d, one token per
-//    lane; a slot is refilled as soon as its partial tiles are in.  CTA 0
-//    stores w_hat and the amplitude factors for the backward.
+// Controller forward, with the parameter preparation folded in.
+//  - Every CTA stages the raw directions w_phi, w_r (first D entries) in
+//    shared memory as one 80-byte block per 8-channel chunk {phi 0-7, r 0-7,
+//    pad} and computes the norms ||w_phi||, ||w_r|| over all D+1 entries
+//    (FP32: per-thread strided sums, warp xor tree, warp-order sum; the same
+//    in every CTA).
+//  - A warp takes groups of kCfTok consecutive tokens (group g, g + W, ...
+//    for its global warp index g out of W).  Lane l owns the chunks l, l+32,
+//    ... of every token of the group: 16-byte loads straight from x_sel (one
+//    warp load = 512 contiguous bytes of one row), FP32 dot products with the
+//    raw directions, then a fixed-order reduce-scatter of the 2 kCfTok sums
+//    across the lanes.  One lane per token scales by 1/||w||, adds the bias
+//    entry and evaluates p = tanh(s_phi), r = tanh(s_r), q(r), d, c, and
+//    E - 1 = expm1(c), C = cos d, S = sin d.
+//  - The last ceil(M/32) warps of the grid (those with the fewest groups)
+//    first compute the per-mode transition constants
+//    lbar_m = e^{-nu_m} e^{i theta_m} as double-floats (hi, lo) in FP64.
+//  - CTA 0 stores w_hat and the amplitude factors for the backward and clears
+//    the forward scan's chain counters.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
+constexpr int kCfWarps = 8;
+constexpr int kCfThreads = 32 * kCfWarps;
+constexpr int kCfTok = 4;      // tokens per warp group
+constexpr int kCfBatch = 4;    // chunks per lane per load batch
+constexpr int kCfBlock = 5;    // float4 per staged weight chunk (80 bytes: conflict-free for 8 distinct chunks)
+
+// Sums of the 8 channels of chunk q (BF16) against both staged directions.
+__device__ __forceinline__ void dot8(const uint4 q, const float4* __restrict__ wb, float& sp, float& sr) {
+    float x[8];
+    unpack8(q, x);
+    const float4 p0 = wb[0], p1 = wb[1], r0 = wb[2], r1 = wb[3];
+    sp = fmaf(x[0], p0.x, sp);
+    sp = fmaf(x[1], p0.y, sp);
+    sp = fmaf(x[2], p0.z, sp);
+    sp = fmaf(x[3], p0.w, sp);
+    sp = fmaf(x[4], p1.x, sp);
+    sp = fmaf(x[5], p1.y, sp);
+    sp = fmaf(x[6], p1.z, sp);
+    sp = fmaf(x[7], p1.w, sp);
+    sr = fmaf(x[0], r0.x, sr);
+    sr = fmaf(x[1], r0.y, sr);
+    sr = fmaf(x[2], r0.z, sr);
+    sr = fmaf(x[3], r0.w, sr);
+    sr = fmaf(x[4], r1.x, sr);
+    sr = fmaf(x[5], r1.y, sr);
+    sr = fmaf(x[6], r1.z, sr);
+    sr = fmaf(x[7], r1.w, sr);
 }
 
-// c += A B for one m16n8k16 tile (BF16 A row-major, B column-major, FP32 c).
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// The per-token scalars from the two dot products (raw directions).
+__device__ __forceinline__ void ctrl_fwd_token(const SamuCtrlFwdArgs& a, long long t, float dp, float dr,
+                                               float inv_phi, float inv_r, float bias_p, float bias_r, float k_phi,
+                                               float k_r) {
+    const float p = tanhf(fmaf(dp, inv_phi, bias_p));
+    const float r = tanhf(fmaf(dr, inv_r, bias_r));
+    const float qr = r / (1.0f + r * r);
+    const float d = k_phi * p;
+    const float c = k_r * qr;
+    float sn, cs;
+    sincosf(d, &sn, &cs);
+    a.p[t] = p;
+    a.r[t] = r;
+    const float em1 = expm1f(c);
+    // R = -E, or +0 at a reset
+    const float rw = (a.reset != nullptr && a.reset[t] != 0) ? 0.0f : -(1.0f + em1);
+    a.ctrl[2 * t] = make_float4(em1, em1, cs, cs);
+    a.ctrl[2 * t + 1] = make_float4(sn, sn, rw, rw);
 }
 
-// w = hi + mid + lo with each part a BF16 value (exactly, up to 2^-24 |w|):
-// every subtraction is exact.  part 0, 1 or 2.
-__device__ __forceinline__ float bf16_part(float w, int part) {
-    const float h = __bfloat162float(__float2bfloat16_rn(w));
-    if (part == 0) return h;
-    const float r1 = w - h;
-    const float m = __bfloat162float(__float2bfloat16_rn(r1));
-    if (part == 1) return m;
-    return __bfloat162float(__float2bfloat16_rn(r1 - m));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) { return f2_to_bf2(lo, hi); }
-
-constexpr int kCtrlKMax = 16;   // k-steps (16 channels each) per consumer warp
-
-template <int N>
-__device__ __forceinline__ void ctrl_fwd_consumer(const SamuCtrlFwdArgs& a, const CtrlSmem& sm, long long s0,
-                                                  long long s1, int cw, int lane, float inv_phi, float inv_r) {
-    const CtrlGeom& cg = a.cg;
-    const int D = a.D;
-    const int ks0 = kCtrlKMax * cw;
-    const int nk = min(kCtrlKMax, D / 16 - ks0);
-    // B fragments: thread (g, t) holds column n = g at k = 2t, 2t+1 (b0) and
-    // 2t+8, 2t+9 (b1) of every k-step
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t bf[kCtrlKMax][2];
-#pragma unroll
-    for (int j = 0; j < kCtrlKMax; ++j) {
-        bf[j][0] = 0u;
-        bf[j][1] = 0u;
-        if (j < nk && g < 6) {
-            const float* w = g < 3 ? a.w_phi : a.w_r;
-            const float inv = g < 3 ? inv_phi : inv_r;
-            const int part = g % 3;
-            const int c0 = 16 * (ks0 + j) + 2 * t;
-            bf[j][0] = pack_bf16(bf16_part(w[c0] * inv, part), bf16_part(w[c0 + 1] * inv, part));
-            bf[j][1] = pack_bf16(bf16_part(w[c0 + 8] * inv, part), bf16_part(w[c0 + 9] * inv, part));
-        }
-    }
-    const uint32_t pitch = (uint32_t)ctrl_row_bytes(cg, D, false);
-    // ldmatrix row of this lane: token lane % 16 (rows past the stage's
-    // token count repeat earlier rows; their results are not used), channel
-    // half lane / 16 of each k-step.  Swizzled layout: k-step kk lies in
-    // chunk kk / 4, 16-byte unit 2 (kk mod 4) + half, stored at that unit
-    // xor (token mod 8); the consumer's first k-step is a multiple of 4.
-    const uint32_t r = (uint32_t)((lane & 15) % N), hf = (uint32_t)(lane >> 4);
-    const uint32_t lane_off = cg.swz ? r * 128u : r * pitch + hf * 16u;
-    uint32_t unit_off[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) unit_off[q] = ((2u * q + hf) ^ (r & 7u)) * 16u;
-    float4* xb = reinterpret_cast<float4*>(sm.xbuf);
-    for (long long st = s0; st < s1; ++st) {
-        const int k = (int)(st - s0);
-        const int slot = k % cg.ring;
-        if (!mbar_wait_bounded(&sm.full[slot], (uint32_t)(k / cg.ring) & 1u)) {
-            if (lane == 0) atomicOr(a.status, kStatusTimeout);
-            return;
-        }
-        const uint32_t base = smem_u32(sm.ring + (size_t)slot * ctrl_slot_bytes(cg, D, false)) + lane_off;
-        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
-        // byte offset of k-step kk for this lane
-        auto koff = [&](int kk) -> uint32_t {
-            return cg.swz ? (uint32_t)(kk >> 2) * (uint32_t)N * 128u + unit_off[kk & 3] : (uint32_t)kk * 32u;
-        };
-#pragma unroll
-        for (int j = 0; j < kCtrlKMax; j += 2) {
-            if (j < nk) {
-                uint32_t fa[4];
-                ldsm_x4(base + koff(ks0 + j), fa);
-                mma_16816(ce, fa, bf[j][0], bf[j][1]);
-            }
-            if (j + 1 < nk) {
-                uint32_t fa[4];
-                ldsm_x4(base + koff(ks0 + j + 1), fa);
-                mma_16816(co, fa, bf[j + 1][0], bf[j + 1][1]);
-            }
-        }
-        xb[((size_t)(k % ctrl_xsets(cg)) * cg.consumers + cw) * 32 + lane] =
-            make_float4(ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ready[slot]);
-    }
-}
-
-template <int N>
-__device__ __forceinline__ void ctrl_fwd_producer(const SamuCtrlFwdArgs& a, const CUtensorMap* tm, const CtrlSmem& sm,
-                                                  long long s0, long long s1, int lane, float bias_p, float bias_r,
-                                                  float k_phi, float k_r) {
-    const CtrlGeom& cg = a.cg;
-    const int D = a.D;
-    const float4* xb = reinterpret_cast<const float4*>(sm.xbuf);
-    // token i = lane (i < N): row i of the partial tiles is held by lanes
-    // 4 (i mod 8) + {0, 1, 2} (columns {0,1}, {2,3}, {4,5}), in the first two
-    // values for rows 0-7 and the last two for rows 8-15
-    const int i = lane;
-    const int src = 4 * (i & 7);
-    const bool upper = (i & 8) != 0;
-    for (long long st = s0; st < s1; ++st) {
-        const int k = (int)(st - s0);
-        const int slot = k % cg.ring;
-        const long long t0 = st * N;
-        const int n = (int)min((long long)N, a.BL - t0);
-        if (!mbar_wait_bounded(&sm.ready[slot], (uint32_t)(k / cg.ring) & 1u)) {
-            if (lane == 0) atomicOr(a.status, kStatusTimeout);
-            return;
-        }
-        // the consumers are done with the slot: refill it first
-        const long long nxt = st + cg.ring;
-        if (lane == 0 && nxt < s1)
-            ctrl_issue(sm, slot, a.x, tm, nxt * N, (int)min((long long)N, a.BL - nxt * N), D, cg, false);
-        float s_phi = 0.f, s_r = 0.f;
-        if (i < N) {
-            const float4* set = xb + (size_t)(k % ctrl_xsets(cg)) * cg.consumers * 32;
-            for (int c = 0; c < cg.consumers; ++c) {
-                const float4* tile = set + (size_t)c * 32 + src;
-                const float4 p01 = tile[0], p23 = tile[1], p45 = tile[2];
-                const float c0 = upper ? p01.z : p01.x, c1 = upper ? p01.w : p01.y;
-                const float c2 = upper ? p23.z : p23.x, c3 = upper ? p23.w : p23.y;
-                const float c4 = upper ? p45.z : p45.x, c5 = upper ? p45.w : p45.y;
-                s_phi += (c0 + c1) + c2;
-                s_r += (c3 + c4) + c5;
-            }
-        }
-        if (i < n) {
-            const long long t = t0 + i;
-            const float p = tanhf(s_phi + bias_p);
-            const float r = tanhf(s_r + bias_r);
-            const float qr = r / (1.0f + r * r);
-            const float d = k_phi * p;
-            const float c = k_r * qr;
-            float sn, cs;
-            sincosf(d, &sn, &cs);
-            a.p[t] = p;
-            a.r[t] = r;
-            const float em1 = expm1f(c);
-            // R = -E, or +0 at a reset
-            const float rw = (a.reset != nullptr && a.reset[t] != 0) ? 0.0f : -(1.0f + em1);
-            a.ctrl[2 * t] = make_float4(em1, em1, cs, cs);
-            a.ctrl[2 * t + 1] = make_float4(sn, sn, rw, rw);
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kCtrlMaxThreads)
-    samu_ctrl_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, SamuCtrlFwdArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ float s_red[2][kCtrlMaxThreads / 32];
+__global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
+    extern __shared__ __align__(16) float4 wsm[];   // [D/8][kCfBlock]
+    __shared__ float s_red[2][kCfWarps];
     pdl_trigger();
     pdl_wait();
-    const int tid = threadIdx.x;
-    const int D = a.D;
-    const int M = D / 2;
-    const int cta = blockIdx.x;
-    const CtrlGeom& cg = a.cg;
-    const int n = D + 1;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int nwarps = blockDim.x >> 5;
-    const CtrlSmem sm = ctrl_smem(smem_raw, cg, D, false);
-    long long s0, s1;
-    ctrl_stage_range(cg, cta, s0, s1);
-    if (cg.swz && (smem_u32(smem_raw) & 1023u) != 0u) {   // the swizzled copies need 1024-byte aligned slots
-        if (tid == 0) atomicOr(a.status, kStatusLayout);
-        return;
-    }
-    if (tid == 0) {   // the first stages go out before anything else
-        for (int i = 0; i < cg.ring; ++i) {
-            mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.ready[i], cg.consumers);
-        }
-        for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st) {
-            const int nn = cg.stage_tok;
-            ctrl_issue(sm, (int)(st - s0), a.x, &tm_x, st * nn, (int)min((long long)nn, a.BL - st * nn), D, cg,
-                       false);
-        }
-    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int D = a.D, M = D / 2, n = D + 1, nch = D / 8;
+    const long long BL = a.BL;
+    const long long W = (long long)gridDim.x * kCfWarps;
+    const long long gw = (long long)blockIdx.x * kCfWarps + warp;
+    const long long n_groups = (BL + kCfTok - 1) / kCfTok;
+    const int cpl = (nch + 31) / 32;   // chunks per lane
 
-    // norms (FP32, fixed order: per-thread strided sum, warp tree, warp-order sum)
+    // staged raw directions and the norms
     float sp = 0.f, sr = 0.f;
-    for (int j = tid; j < n; j += blockDim.x) {
+    for (int j = tid; j < n; j += kCfThreads) {
         const float x = a.w_phi[j], y = a.w_r[j];
         sp = fmaf(x, x, sp);
         sr = fmaf(y, y, sr);
+        if (j < D) {
+            float* blk = reinterpret_cast<float*>(wsm + (size_t)(j >> 3) * kCfBlock);
+            blk[j & 7] = x;
+            blk[8 + (j & 7)] = y;
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -360,7 +200,7 @@ __global__ void __launch_bounds__(kCtrlMaxThreads)
     }
     __syncthreads();
     float tp = 0.f, tr = 0.f;
-    for (int w = 0; w < nwarps; ++w) {
+    for (int w = 0; w < kCfWarps; ++w) {
         tp += s_red[0][w];
         tr += s_red[1][w];
     }
@@ -369,12 +209,13 @@ __global__ void __launch_bounds__(kCtrlMaxThreads)
     const float ta = tanhf(a.a_phi[0]), tra = tanhf(a.a_r[0]);
     const float ism = 1.0f / sqrtf((float)M);
     const float k_phi = ta * ism, k_r = tra * ism;
-    if (cta == 0) {
-        for (int j = tid; j < n; j += blockDim.x) {
+    const float bias_p = a.w_phi[D] * inv_phi, bias_r = a.w_r[D] * inv_r;
+    if (blockIdx.x == 0) {
+        for (int j = tid; j < n; j += kCfThreads) {
             a.wh[j] = a.w_phi[j] * inv_phi;
             a.wh[n + j] = a.w_r[j] * inv_r;
         }
-        for (int j = tid; j < a.n_counters; j += blockDim.x) a.counters[j] = 0u;
+        for (int j = tid; j < a.n_counters; j += kCfThreads) a.counters[j] = 0u;
         if (tid == 0) {
             a.misc[0] = k_phi;
             a.misc[1] = k_r;
@@ -385,21 +226,64 @@ __global__ void __launch_bounds__(kCtrlMaxThreads)
             a.misc[6] = ism;
         }
     }
-    if (warp == 0) {
-        const float bias_p = a.w_phi[D] * inv_phi, bias_r = a.w_r[D] * inv_r;
-        if (cg.stage_tok == 16)
-            ctrl_fwd_producer<16>(a, &tm_x, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
-        else
-            ctrl_fwd_producer<8>(a, &tm_x, sm, s0, s1, lane, bias_p, bias_r, k_phi, k_r);
-    } else if (warp == 1) {
-        // this CTA's share of the per-mode constants, off the streaming path
-        const int m0 = (int)((long long)M * cta / cg.n_ctas), m1 = (int)((long long)M * (cta + 1) / cg.n_ctas);
-        for (int m = m0 + lane; m < m1; m += 32) mode_constants(a.nu, a.theta, M, a.modes, m);
-    } else {
-        if (cg.stage_tok == 16)
-            ctrl_fwd_consumer<16>(a, sm, s0, s1, warp - 2, lane, inv_phi, inv_r);
-        else
-            ctrl_fwd_consumer<8>(a, sm, s0, s1, warp - 2, lane, inv_phi, inv_r);
+    {   // per-mode constants: the last warps of the grid, 32 modes each
+        const long long nmw = (M + 31) / 32;
+        const long long first = W > nmw ? W - nmw : 0;
+        for (long long mw = gw - first; gw >= first && mw < nmw; mw += W - first) {
+            const int m = (int)mw * 32 + lane;
+            mode_constants(a.nu, a.theta, M, a.modes, m);
+        }
+    }
+
+    const uint4* x = a.x;
+    for (long long g = gw; g < n_groups; g += W) {
+        const long long t0 = g * kCfTok;
+        float acc[2 * kCfTok];
+#pragma unroll
+        for (int v = 0; v < 2 * kCfTok; ++v) acc[v] = 0.f;
+        for (int i0 = 0; i0 < cpl; i0 += kCfBatch) {
+            uint4 xv[kCfBatch][kCfTok];
+#pragma unroll
+            for (int b = 0; b < kCfBatch; ++b) {
+                const int c = lane + 32 * (i0 + b);
+#pragma unroll
+                for (int k = 0; k < kCfTok; ++k) {
+                    const bool ok = i0 + b < cpl && c < nch && t0 + k < BL;
+                    xv[b][k] = ok ? __ldg(x + (size_t)(t0 + k) * nch + c) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kCfBatch; ++b) {
+                const int c = lane + 32 * (i0 + b);
+                if (i0 + b < cpl && c < nch) {
+                    const float4* wb = wsm + (size_t)c * kCfBlock;
+#pragma unroll
+                    for (int k = 0; k < kCfTok; ++k) dot8(xv[b][k], wb, acc[2 * k], acc[2 * k + 1]);
+                }
+            }
+        }
+        // reduce-scatter of the 8 sums {token k: phi, r} over the lanes:
+        // halving exchanges at distances 16, 8, 4 (lane bit b keeps the upper
+        // half), then full sums at distances 2, 1.  Lane L ends with value
+        // 4 bit4(L) + 2 bit3(L) + bit2(L): lanes 8k hold s_phi of token k,
+        // lanes 8k + 4 its s_r.
+#pragma unroll
+        for (int o = 16, h = kCfTok; o >= 4; o >>= 1, h >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < h; ++j) {
+                const float send = up ? acc[j] : acc[j + h];
+                const float keep = up ? acc[j + h] : acc[j];
+                acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        float s = acc[0];
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        const float s_r = __shfl_down_sync(0xffffffffu, s, 4);
+        const int k = lane >> 3;
+        if ((lane & 7) == 0 && t0 + k < BL)
+            ctrl_fwd_token(a, t0 + k, s, s_r, inv_phi, inv_r, bias_p, bias_r, k_phi, k_r);
     }
 }
 
@@ -433,7 +317,7 @@ __device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, cons
             atomicOr(a.status, kStatusTimeout);
             break;
         }
-        ctrl_issue(sm, slot, a.x, nullptr, t0, n, D, cg, true);
+        ctrl_issue(sm, slot, a.x, t0, n, D, cg);
     }
 }
 
@@ -601,7 +485,7 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     const int cta = blockIdx.x;
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
-    const CtrlSmem sm = ctrl_smem(smem_raw, cg, D, true);
+    const CtrlSmem sm = ctrl_smem(smem_raw, cg, D);
     long long s0, s1;
     ctrl_stage_range(cg, cta, s0, s1);
     if (tid == 0) {   // the first stages go out before the scalar phase
@@ -611,8 +495,7 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
         }
         for (long long st = s0; st < s1 && st < s0 + cg.ring; ++st) {
             const int nn = cg.stage_tok;
-            ctrl_issue(sm, (int)(st - s0), a.x, nullptr, st * nn, (int)min((long long)nn, a.BL - st * nn), D, cg,
-                       true);
+            ctrl_issue(sm, (int)(st - s0), a.x, st * nn, (int)min((long long)nn, a.BL - st * nn), D, cg);
         }
     }
     const long long tb = s0 * cg.stage_tok;
@@ -833,29 +716,24 @@ int ctrl_sms() {
 
 }  // namespace
 
-CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
+CtrlGeom samu_ctrl_geom(long long BL, int D) {
     CtrlGeom cg;
-    // forward: swizzled tiled copies when D is a multiple of 64 (and token
-    // coordinates fit the copy's 32-bit coordinates)
-    cg.swz = (!backward && D % 64 == 0 && BL < (1ll << 31)) ? 1 : 0;
-    const size_t row = ctrl_row_bytes(cg, D, backward);
     // stages of 16 tokens, or 8 when 16 rows exceed 72 KB
-    cg.stage_tok = 16 * row <= 72 * 1024 ? 16 : 8;
+    cg.stage_tok = 16 * 2 * (size_t)D <= 72 * 1024 ? 16 : 8;
     cg.consumers = (D / 8 + 31) / 32;
     if (cg.consumers < 1) cg.consumers = 1;
-    cg.threads = 32 * (2 + cg.consumers);   // producer, mode (forward) or reducer (backward) warp, consumers
+    cg.threads = 32 * (2 + cg.consumers);   // producer, reducer, consumers
     cg.n_stages = (BL + cg.stage_tok - 1) / cg.stage_tok;
     {   // tokens of the longest CTA range: there are at least min(stages, SMs) CTAs
         const long long fewest = cg.n_stages < ctrl_sms() ? cg.n_stages : ctrl_sms();
         cg.max_cta_tok = (int)((cg.n_stages + fewest - 1) / fewest * cg.stage_tok);
     }
-    // as many ring slots (2 .. kCtrlRingMax) as fit with the exchange buffer
-    // and the barriers
-    const size_t cap = backward ? kCtrlBwdSmemMax : kCtrlFwdSmemMax;
+    // as many ring slots (2 .. kCtrlRingMax) as fit with the scalar buffer and
+    // the barriers
     for (cg.ring = kCtrlRingMax;; --cg.ring) {
-        const size_t xb = (ctrl_xbuf_bytes(cg, backward) + 15) & ~size_t(15);
-        cg.smem = (int)(ctrl_ring_bytes(cg, D, backward) + xb + 3 * cg.ring * sizeof(uint64_t));
-        if ((size_t)cg.smem <= cap || cg.ring == 2) break;
+        const size_t xb = (ctrl_xbuf_bytes(cg) + 15) & ~size_t(15);
+        cg.smem = (int)(ctrl_ring_bytes(cg, D) + xb + 2 * cg.ring * sizeof(uint64_t));
+        if ((size_t)cg.smem <= kCtrlBwdSmemMax || cg.ring == 2) break;
     }
     int per_sm = (int)((227 * 1024) / (cg.smem + 1024));
     const int by_threads = 2048 / cg.threads;
@@ -869,13 +747,18 @@ CtrlGeom samu_ctrl_geom(long long BL, int D, bool backward) {
     return cg;
 }
 
-cudaError_t launch_samu_ctrl_fwd(const CUtensorMap& tm_x, const SamuCtrlFwdArgs& args_in, cudaStream_t s, bool pdl) {
-    SamuCtrlFwdArgs a = args_in;
-    a.cg = samu_ctrl_geom(a.BL, a.D, false);
+cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& a, cudaStream_t s, bool pdl) {
+    // two CTAs per SM (one wave), fewer for short inputs
+    const long long groups = (a.BL + kCfTok - 1) / kCfTok;
+    long long ctas = (long long)ctrl_sms() * 2;
+    const long long need = (groups + kCfWarps - 1) / kCfWarps;
+    if (ctas > need) ctas = need;
+    if (ctas < 1) ctas = 1;
+    const size_t smem = (size_t)(a.D / 8) * kCfBlock * sizeof(float4);
     const cudaError_t e =
-        cudaFuncSetAttribute(samu_ctrl_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, a.cg.smem);
+        cudaFuncSetAttribute(samu_ctrl_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_ex(samu_ctrl_fwd_kernel, a.cg.n_ctas, a.cg.threads, (size_t)a.cg.smem, s, pdl, tm_x, a);
+    return launch_ex(samu_ctrl_fwd_kernel, (unsigned)ctas, kCfThreads, smem, s, pdl, a);
 }
 
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl) {

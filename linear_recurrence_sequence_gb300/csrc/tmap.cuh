@@ -53,21 +53,4 @@ inline bool make_ctrl_map(CUtensorMap* map, const void* ptr, int B, int L, int r
     return r == CUDA_SUCCESS;
 }
 
-// 3-D tensor map over x_sel [B*L, D] BF16 (D a multiple of 64) viewed as
-// (channel within a 64-channel chunk, token, chunk), with a box of `rows`
-// tokens x all chunks copied into shared memory as [chunk][token][128 bytes]
-// in the 128-byte swizzle (rows past B*L read as zero).
-inline bool make_ctrl_x_map(CUtensorMap* map, const void* ptr, long long BL, int D, int rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (fn == nullptr || D % 64 != 0 || D / 64 > 256) return false;
-    cuuint64_t dims[3] = {64, (cuuint64_t)BL, (cuuint64_t)(D / 64)};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)rows, (cuuint32_t)(D / 64)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace lrs

@@ -216,7 +216,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
     CUtensorMap tm_w, tm_ctrl;
-    if (!make_bf16_map(&tm_w, w, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub)) return LRS_ERR_CUDA;
+    if (!make_bf16_map(&tm_w, w, B, L, D, kMapRows) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kMapRows)) return LRS_ERR_CUDA;
     SamuScanFwdArgs a;
     a.g = g;
     a.modes = modes;
@@ -266,7 +266,7 @@ int samu_backward(const void* dy, const float* dhT,
     if (cudaMemsetAsync(scratch, 0, sc.zero_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     // 16-row boxes for the adjoint maps, 8-row boxes for the reverse replay
     CUtensorMap tm_dy, tm_ctrl, tm_dy8, tm_w8, tm_ctrl8;
-    if (!make_bf16_map(&tm_dy, dy, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub) ||
+    if (!make_bf16_map(&tm_dy, dy, B, L, D, kMapRows) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kMapRows) ||
         !make_bf16_map(&tm_dy8, dy, B, L, D, kHalf) || !make_bf16_map(&tm_w8, w, B, L, D, kHalf) ||
         !make_ctrl_map(&tm_ctrl8, ctrl, B, L, kHalf))
         return LRS_ERR_CUDA;

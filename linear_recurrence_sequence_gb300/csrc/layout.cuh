@@ -63,6 +63,9 @@ inline ScanGeom make_geom(int B, int L, int lanes, int tile) {
 // kMaxSegWarps segments in all.
 constexpr int kSegMinTok = kSub;
 constexpr int kHalf = kSub / 2;     // tokens between SAMU state checkpoints
+constexpr int kMapRows = 16;        // tokens per staged item of the SAMU maps and replay kernels
+constexpr int kMapSlots = 2;        // items in flight per warp there
+static_assert(kMapRows % kHalf == 0, "items start on state checkpoints");
 constexpr long long kMaxSegWarps = 16384;
 
 struct SegGeom {

@@ -110,7 +110,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     if (launch_samu_ctrl_fwd(cf, stream, false) != cudaSuccess) return LRS_ERR_CUDA;
 
     CUtensorMap tm_w, tm_ctrl;
-    if (!make_bf16_map(&tm_w, w, B, L, D, kSub) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kSub)) return LRS_ERR_CUDA;
+    if (!make_bf16_map(&tm_w, w, B, L, D, kMapRows) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kMapRows)) return LRS_ERR_CUDA;
     SamuScanFwdArgs a;
     a.g = samu_scan_geom(B, L, M, false);
     a.modes = modes;

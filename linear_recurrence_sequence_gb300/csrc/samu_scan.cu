@@ -36,27 +36,40 @@ namespace lrs {
 
 constexpr int kEngineWarps = 8;                     // warps per CTA (each on its own segment)
 constexpr int kEngineThreads = kEngineWarps * 32;
-constexpr int kRing = 2;                            // staging slots per warp
 constexpr int kWords = kGroup / 2;                  // BF16 pairs per box row
-constexpr int kBoxBytes = kSub * kRowBytes;         // one [16 x 64] BF16 box: 2 KB
 constexpr int kCtlBytes = 32;                       // one token's control word (two float4)
-constexpr int kItemBytes = 2 * kBoxBytes + kSub * kCtlBytes;   // re box + im box + control words
 static_assert(kEngineWarps == kSegPerCta, "a CTA holds the segments of one chain");
 
-// One warp's staging ring.  Every TMA destination starts on a 128-byte
-// boundary (box sizes are multiples of 128 bytes).
-struct alignas(128) WarpRing {
-    uint32_t box[kRing][2][kSub][kWords];   // [slot][re, im][token][pair]
-    float4 ctrl[kRing][2 * kSub];           // [slot][token: two float4]
-    uint64_t full[kRing];
+// One warp's staging ring of S items of R tokens: a [R x 64] BF16 box per
+// half of the warp's 64 modes plus the R control words.  Every TMA
+// destination starts on a 128-byte boundary (box sizes are multiples of 128
+// bytes).
+template <int R, int S>
+struct alignas(128) WarpRingT {
+    static constexpr int kRows = R;
+    static constexpr int kSlots = S;
+    static constexpr int kItemBytes = 2 * R * kRowBytes + R * kCtlBytes;
+    uint32_t box[S][2][R][kWords];   // [slot][re, im][token][pair]
+    float4 ctrl[S][2 * R];           // [slot][token: two float4]
+    uint64_t full[S];
 };
-constexpr int kEngineSmem = kEngineWarps * (int)sizeof(WarpRing);
+// The maps and replay kernels stage kMapRows-token items, kMapSlots per warp;
+// the reverse replay 8-token units (a w item and a dy item each), 4 per warp.
+using MapRing = WarpRingT<kMapRows, kMapSlots>;
+using RevRing = WarpRingT<kHalf, 4>;
+constexpr int kWarpSmem = (int)(sizeof(MapRing) > sizeof(RevRing) ? sizeof(MapRing) : sizeof(RevRing));
+constexpr int kEngineSmem = kEngineWarps * kWarpSmem;
+
+template <class Ring>
+__device__ __forceinline__ Ring& warp_ring(uint8_t* smem_raw, int warp) {
+    return *reinterpret_cast<Ring*>(smem_raw + (size_t)warp * kWarpSmem);
+}
 
 // The segment of one warp.
 struct SegTask {
     int b, grp, s;
     int t_begin, t_end;   // tokens [t_begin, t_end)
-    int nsc;              // 16-token sub-chunks
+    int nsc;              // kMapRows-token items
 };
 
 __device__ __forceinline__ SegTask seg_task(const SegGeom& g, long long gw) {
@@ -67,7 +80,7 @@ __device__ __forceinline__ SegTask seg_task(const SegGeom& g, long long gw) {
     T.grp = chain % g.n_groups;
     T.t_begin = T.s * g.seg;
     T.t_end = min(g.L, T.t_begin + g.seg);
-    T.nsc = T.t_end > T.t_begin ? (T.t_end - T.t_begin + kSub - 1) / kSub : 0;   // 0: a segment past L
+    T.nsc = T.t_end > T.t_begin ? (T.t_end - T.t_begin + kMapRows - 1) / kMapRows : 0;   // 0: a segment past L
     return T;
 }
 
@@ -113,19 +126,33 @@ __device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane
         }                                              \
     } while (0)
 
-// The same with a third template argument X passed through.
-#define LRS_SUB_DISPATCH_X(kd, FN, X, ...)             \
+// The same for FN<N, FAST, SIMPLE> and FN<N, FAST, SIMPLE, X>.
+#define LRS_SUB_DISPATCH_N(kd, FN, N, ...)             \
     do {                                               \
         if (kd.fast) {                                 \
             if (kd.simple)                             \
-                FN<true, true, X>(__VA_ARGS__);        \
+                FN<N, true, true>(__VA_ARGS__);        \
             else                                       \
-                FN<true, false, X>(__VA_ARGS__);       \
+                FN<N, true, false>(__VA_ARGS__);       \
         } else {                                       \
             if (kd.simple)                             \
-                FN<false, true, X>(__VA_ARGS__);       \
+                FN<N, false, true>(__VA_ARGS__);       \
             else                                       \
-                FN<false, false, X>(__VA_ARGS__);      \
+                FN<N, false, false>(__VA_ARGS__);      \
+        }                                              \
+    } while (0)
+#define LRS_SUB_DISPATCH_NX(kd, FN, N, X, ...)         \
+    do {                                               \
+        if (kd.fast) {                                 \
+            if (kd.simple)                             \
+                FN<N, true, true, X>(__VA_ARGS__);     \
+            else                                       \
+                FN<N, true, false, X>(__VA_ARGS__);    \
+        } else {                                       \
+            if (kd.simple)                             \
+                FN<N, false, true, X>(__VA_ARGS__);    \
+            else                                       \
+                FN<N, false, false, X>(__VA_ARGS__);   \
         }                                              \
     } while (0)
 
@@ -163,21 +190,23 @@ __device__ __forceinline__ void store_map2(float4* p, const c2x& l, const c2x& b
     p[1] = make_float4(lr1, li1, br1, bi1);
 }
 
-// Lane 0: stage the sub-chunk at token ts of tensor `tm` (both halves of the
+// Lane 0: stage the item at token ts of tensor `tm` (both halves of the
 // warp's 64 modes) and its control words into ring slot `slot`.  The warp has
 // finished reading the slot (__syncwarp before the call).
-__device__ __forceinline__ void ring_issue(WarpRing& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
+template <class Ring>
+__device__ __forceinline__ void ring_issue(Ring& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
                                            int x_re, int x_im, int ts, int b) {
     fence_proxy_async();
-    mbar_arrive_expect_tx(&R.full[slot], kItemBytes);
+    mbar_arrive_expect_tx(&R.full[slot], Ring::kItemBytes);
     tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
     tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
     tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
 }
 
-__device__ __forceinline__ void ring_init(WarpRing& R, int lane) {
+template <class Ring>
+__device__ __forceinline__ void ring_init(Ring& R, int lane) {
     if (lane == 0) {
-        for (int i = 0; i < kRing; ++i) mbar_init(&R.full[i], 1);
+        for (int i = 0; i < Ring::kSlots; ++i) mbar_init(&R.full[i], 1);
     }
     __syncwarp();
 }
@@ -185,11 +214,12 @@ __device__ __forceinline__ void ring_init(WarpRing& R, int lane) {
 // Waits for item k of the ring (n_items in all).  If the copy never lands:
 // records the failure, waits (bounded) for the later items already issued,
 // and returns false so that the warp can leave.
-__device__ __forceinline__ bool ring_wait(WarpRing& R, int k, int n_items, uint32_t* status, int lane) {
-    if (mbar_wait_bounded(&R.full[k % kRing], (uint32_t)(k / kRing) & 1u)) return true;
+template <class Ring>
+__device__ __forceinline__ bool ring_wait(Ring& R, int k, int n_items, uint32_t* status, int lane) {
+    constexpr int S = Ring::kSlots;
+    if (mbar_wait_bounded(&R.full[k % S], (uint32_t)(k / S) & 1u)) return true;
     if (lane == 0) atomicOr(status, kStatusTimeout);
-    for (int j = k + 1; j < k + kRing && j < n_items; ++j)
-        mbar_wait_bounded(&R.full[j % kRing], (uint32_t)(j / kRing) & 1u);
+    for (int j = k + 1; j < k + S && j < n_items; ++j) mbar_wait_bounded(&R.full[j % S], (uint32_t)(j / S) & 1u);
     return false;
 }
 
@@ -198,11 +228,11 @@ __device__ __forceinline__ bool ring_wait(WarpRing& R, int k, int n_items, uint3
 // ---------------------------------------------------------------------------
 // Appends the sub-chunk's tokens, latest first, to the map H = (P, beta) of
 // the tokens after them: H o T_t = (P lambda_t, P b_t + beta).
-template <bool FAST, bool SIMPLE>
+template <int N, bool FAST, bool SIMPLE>
 __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
                                              const ModePair& k, c2x& P, c2x& be) {
 #pragma unroll
-    for (int i = kSub - 1; i >= 0; --i) {
+    for (int i = N - 1; i >= 0; --i) {
         if (SIMPLE || i < nsub) {
             const Ctl2 ct = load_ctl(sc, i);
             const uint32_t wr = wre[i * kWords], wi = wim[i * kWords];
@@ -218,18 +248,21 @@ __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* w
     }
 }
 
-// hmid: where the state entering token 8 of the sub-chunk is kept (the
-// backward restarts there); written by active lanes only.  The step
-// z <- lambda z + b is one complex fused multiply-add (four paired FMAs).
-template <bool FAST, bool SIMPLE, bool Y32>
+// hs: the item's first state checkpoint (the state entering its first
+// token); the states entering its tokens 8, 16, ... go to the following
+// checkpoints (the backward restarts there); written by active lanes only.
+// The step z <- lambda z + b is one complex fused multiply-add (four paired
+// FMAs).
+template <int N, bool FAST, bool SIMPLE, bool Y32>
 __device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nsub,
                                                const ModePair& k, c2x& z, uint32_t* yp, float* y32p, bool active,
-                                               size_t row, int half, f2x* hmid) {
+                                               size_t row, int half, f2x* hs, int M) {
 #pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        if (i == kHalf && active && (SIMPLE || i < nsub)) {
-            hmid[0] = z.re;
-            hmid[1] = z.im;
+    for (int i = 0; i < N; ++i) {
+        if (i > 0 && i % kHalf == 0 && active && (SIMPLE || i < nsub)) {
+            f2x* h = hs + (size_t)(i / kHalf) * M;
+            h[0] = z.re;
+            h[1] = z.im;
         }
         if (SIMPLE || i < nsub) {
             const Ctl2 ct = load_ctl(sc, i);
@@ -340,15 +373,14 @@ struct EpilogueSmem {
     float4 (*part)[32][2];
     int* last;
 };
-static_assert(sizeof(float4) * kEngineWarps * 32 * 2 <= sizeof(((WarpRing*)nullptr)->box),
+static_assert(sizeof(float4) * kEngineWarps * 32 * 2 <= sizeof(((MapRing*)nullptr)->box),
               "segment maps and partials must fit a ring's box area");
 
 __device__ __forceinline__ EpilogueSmem epilogue_smem(uint8_t* smem_raw) {
-    WarpRing* rings = reinterpret_cast<WarpRing*>(smem_raw);
     EpilogueSmem e;
-    e.seg = reinterpret_cast<float4 (*)[32][2]>(&rings[0].box[0][0][0][0]);
-    e.part = reinterpret_cast<float4 (*)[32][2]>(&rings[1].box[0][0][0][0]);
-    e.last = reinterpret_cast<int*>(&rings[2].box[0][0][0][0]);
+    e.seg = reinterpret_cast<float4 (*)[32][2]>(&warp_ring<MapRing>(smem_raw, 0).box[0][0][0][0]);
+    e.part = reinterpret_cast<float4 (*)[32][2]>(&warp_ring<MapRing>(smem_raw, 1).box[0][0][0][0]);
+    e.last = reinterpret_cast<int*>(&warp_ring<MapRing>(smem_raw, 2).box[0][0][0][0]);
     return e;
 }
 
@@ -358,7 +390,9 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    MapRing& R = warp_ring<MapRing>(smem_raw, warp);
+    constexpr int kRing = MapRing::kSlots;
+    constexpr int kN = MapRing::kRows;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;   // < n_chains * NS: whole CTAs
     const SegTask T = seg_task(g, gw);
@@ -373,7 +407,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     // item k is sub-chunk nsc-1-k: the segment from its end backwards
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
-            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kSub, T.b);
+            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x P;
     P.re = dup2(1.f);
@@ -381,17 +415,17 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     c2x be = czero();
     for (int it = 0; it < T.nsc; ++it) {
         const int slot = it % kRing;
-        const int ts = T.t_begin + (T.nsc - 1 - it) * kSub;
-        const int nsub = min(kSub, T.t_end - ts);
+        const int ts = T.t_begin + (T.nsc - 1 - it) * kN;
+        const int nsub = min(kN, T.t_end - ts);
         if (!ring_wait(R, it, T.nsc, a.status, lane)) break;   // status set; the CTA still reaches its barriers
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
-        const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
-        LRS_SUB_DISPATCH(kd, fwd_maps_sub, sc, wre, wim, nsub, k, P, be);
+        const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
+        LRS_SUB_DISPATCH_N(kd, fwd_maps_sub, kN, sc, wre, wim, nsub, k, P, be);
         __syncwarp();
         if (lane == 0 && it + kRing < T.nsc)
-            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - it - kRing) * kSub, T.b);
+            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - it - kRing) * kN, T.b);
     }
     if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, P, be);
 
@@ -434,7 +468,9 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    MapRing& R = warp_ring<MapRing>(smem_raw, warp);
+    constexpr int kRing = MapRing::kSlots;
+    constexpr int kN = MapRing::kRows;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     if (gw >= (long long)g.n_chains * g.NS) return;
@@ -450,7 +486,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     pdl_wait();
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
-            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
+            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x z = czero();
     if (active) {   // entry: the CTA's entry state through the maps of the earlier segments of the CTA
@@ -480,27 +516,28 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     }
     for (int it = 0; it < T.nsc; ++it) {
         const int slot = it % kRing;
-        const int ts = T.t_begin + it * kSub;
-        const int nsub = min(kSub, T.t_end - ts);
-        // checkpoints: the state entering tokens ts and ts + 8, as pairs {re, im}
+        const int ts = T.t_begin + it * kN;
+        const int nsub = min(kN, T.t_end - ts);
+        // checkpoints (pairs {re, im}): the state entering token ts here, those
+        // entering ts + 8, ... inside the item
         f2x* hs = active ? reinterpret_cast<f2x*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m) : nullptr;
         if (active) {
             hs[0] = z.re;
             hs[1] = z.im;
         }
-        f2x* hmid = active ? hs + M : nullptr;   // slot ts/8 + 1
+
         if (!ring_wait(R, it, T.nsc, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         float* y32p = Y32 ? a.y32 + 2 * row0 : nullptr;
-        const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
-        LRS_SUB_DISPATCH_X(kd, fwd_replay_sub, Y32, sc, wre, wim, nsub, k, z, a.y + row0, y32p, active, D / 2, M / 2,
-                           hmid);
+        const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
+        LRS_SUB_DISPATCH_NX(kd, fwd_replay_sub, kN, Y32, sc, wre, wim, nsub, k, z, a.y + row0, y32p, active, D / 2,
+                            M / 2, hs, M);
         __syncwarp();
         if (lane == 0 && it + kRing < T.nsc)
-            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
+            ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kN, T.b);
     }
     if (active && T.nsc > 0 && T.t_end == L) store_c2(a.hT + ((size_t)T.b * M + m) * 2, z);
 }
@@ -513,11 +550,11 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
 // ---------------------------------------------------------------------------
 // Appends the sub-chunk's tokens, earliest first, to the map G of the tokens
 // before them: G o F_t = (Q conj(lambda_t), beta + Q conj(lambda_t) dy_t).
-template <bool FAST, bool SIMPLE>
+template <int N, bool FAST, bool SIMPLE>
 __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nsub,
                                              const ModePair& k, c2x& Q, c2x& be) {
 #pragma unroll
-    for (int i = 0; i < kSub; ++i) {
+    for (int i = 0; i < N; ++i) {
         if (SIMPLE || i < nsub) {
             const Ctl2 ct = load_ctl(sc, i);
             const uint32_t gr = gre[i * kWords], gi = gim[i * kWords];
@@ -587,7 +624,9 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    WarpRing& R = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+    MapRing& R = warp_ring<MapRing>(smem_raw, warp);
+    constexpr int kRing = MapRing::kSlots;
+    constexpr int kN = MapRing::kRows;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;   // < n_chains * NS: whole CTAs
     const SegTask T = seg_task(g, gw);
@@ -601,7 +640,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     // item k is sub-chunk k: the segment from its start forwards
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
-            ring_issue(R, k, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + k * kSub, T.b);
+            ring_issue(R, k, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + k * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x Q;
     Q.re = dup2(1.f);
@@ -609,17 +648,17 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     c2x be = czero();
     for (int it = 0; it < T.nsc; ++it) {
         const int slot = it % kRing;
-        const int ts = T.t_begin + it * kSub;
-        const int nsub = min(kSub, T.t_end - ts);
+        const int ts = T.t_begin + it * kN;
+        const int nsub = min(kN, T.t_end - ts);
         if (!ring_wait(R, it, T.nsc, a.status, lane)) break;   // status set; the CTA still reaches its barriers
         const float4* sc = R.ctrl[slot];
         const uint32_t* gre = &R.box[slot][0][0][lane];
         const uint32_t* gim = &R.box[slot][1][0][lane];
-        const SubKind kd = sub_kind<kSub>(sc, nsub, lane, k);
-        LRS_SUB_DISPATCH(kd, bwd_maps_sub, sc, gre, gim, nsub, k, Q, be);
+        const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
+        LRS_SUB_DISPATCH_N(kd, bwd_maps_sub, kN, sc, gre, gim, nsub, k, Q, be);
         __syncwarp();
         if (lane == 0 && it + kRing < T.nsc)
-            ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kSub, T.b);
+            ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kN, T.b);
     }
     if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, Q, be);
 
@@ -662,33 +701,6 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
 // (reverse sweep).  The forward sweep keeps lambda_t and u_t = lambda_t z_{t-1}
 // of all 8 tokens in registers, so lambda is evaluated once per token.
 // ---------------------------------------------------------------------------
-constexpr int kRingH = 4;                                   // slots of the 8-row ring
-constexpr int kHalfItemBytes = 2 * kHalf * kRowBytes + kHalf * kCtlBytes;
-
-struct alignas(128) WarpRingH {
-    uint32_t box[kRingH][2][kHalf][kWords];   // [slot][re, im][token][pair]
-    float4 ctrl[kRingH][2 * kHalf];
-    uint64_t full[kRingH];
-};
-static_assert(sizeof(WarpRingH) <= sizeof(WarpRing), "the 8-row ring must fit the engine's shared memory");
-
-__device__ __forceinline__ void ringh_issue(WarpRingH& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
-                                            int x_re, int x_im, int ts, int b) {
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&R.full[slot], kHalfItemBytes);
-    tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
-    tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
-    tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
-}
-
-__device__ __forceinline__ bool ringh_wait(WarpRingH& R, int k, int n_items, uint32_t* status, int lane) {
-    if (mbar_wait_bounded(&R.full[k % kRingH], (uint32_t)(k / kRingH) & 1u)) return true;
-    if (lane == 0) atomicOr(status, kStatusTimeout);
-    for (int j = k + 1; j < k + kRingH && j < n_items; ++j)
-        mbar_wait_bounded(&R.full[j % kRingH], (uint32_t)(j / kRingH) & 1u);
-    return false;
-}
-
 // Forward sweep of one unit from its entry state: lambda_t and
 // u_t = lambda_t z_{t-1} (kept for kappa), z_t = u_t + b_t.  A reset token
 // gets lambda_t = 0.
@@ -801,7 +813,8 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    WarpRingH& R = reinterpret_cast<WarpRingH*>(smem_raw + (size_t)warp * sizeof(WarpRing))[0];
+    RevRing& R = warp_ring<RevRing>(smem_raw, warp);
+    constexpr int kRingH = RevRing::kSlots;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     if (gw >= (long long)g.n_chains * g.NS) return;
@@ -817,15 +830,12 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     // item k: unit n_units-1-k/2 (the segment from its end backwards); even
     // items carry w (forward sweep), odd items dy (reverse sweep)
     auto item_ts = [&](int k) { return T.t_begin + (n_units - 1 - (k >> 1)) * kHalf; };
-    if (lane == 0) {
-        for (int i = 0; i < kRingH; ++i) mbar_init(&R.full[i], 1);
-    }
-    __syncwarp();
+    ring_init(R, lane);
     pdl_trigger();
     pdl_wait();
     if (lane == 0)
         for (int k = 0; k < kRingH && k < n_items; ++k)
-            ringh_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
+            ring_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
@@ -867,7 +877,7 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         }
         // w item: forward sweep
         int slot = it % kRingH;
-        if (!ringh_wait(R, it, n_items, a.status, lane)) return;
+        if (!ring_wait(R, it, n_items, a.status, lane)) return;
         const float4* sc = R.ctrl[slot];
         const SubKind kd = sub_kind<kHalf>(sc, nh, lane, k);
         c2x u[kHalf];
@@ -876,11 +886,11 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
                          lre, lim);
         __syncwarp();
         if (lane == 0 && it + kRingH < n_items)
-            ringh_issue(R, slot, ((it + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(it + kRingH),
+            ring_issue(R, slot, ((it + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(it + kRingH),
                         T.b);
         // dy item: reverse sweep
         slot = (it + 1) % kRingH;
-        if (!ringh_wait(R, it + 1, n_items, a.status, lane)) return;
+        if (!ring_wait(R, it + 1, n_items, a.status, lane)) return;
         sc = R.ctrl[slot];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
@@ -896,7 +906,7 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
                                           2 * (size_t)g.n_groups, lane);
         __syncwarp();
         if (lane == 0 && it + 1 + kRingH < n_items)
-            ringh_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
+            ring_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
                         item_ts(it + 1 + kRingH), T.b);
     }
     if (active) {

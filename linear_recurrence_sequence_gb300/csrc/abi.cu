@@ -287,7 +287,9 @@ int samu_backward(const void* dy, const float* dhT,
     s.numod = at<float2>(scratch, sc.numod);
     s.status = at<uint32_t>(scratch, sc.status);
     LRS_LAUNCH(KID_SAMU_BWD_MAPS, stream, launch_samu_bwd_maps(tm_dy, tm_ctrl, s, stream, false));
-    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy8, tm_w8, tm_ctrl8, s, stream, pdl_ok()));
+    CUtensorMap tm_dw8{};
+    if (!fp32 && !make_bf16_map(&tm_dw8, dw, B, L, D, kHalf)) return LRS_ERR_CUDA;
+    LRS_LAUNCH(KID_SAMU_SCAN_BWD, stream, launch_samu_bwd_main(tm_dy8, tm_w8, tm_ctrl8, tm_dw8, s, stream, pdl_ok()));
 
     SamuCtrlBwdArgs cb;
     cb.BL = (long long)B * L;

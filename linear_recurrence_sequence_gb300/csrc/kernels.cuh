@@ -315,8 +315,10 @@ cudaError_t launch_samu_fwd_replay(const CUtensorMap& tm_w, const CUtensorMap& t
 // each chain folds the adjoint CTA maps), main (backwards, 8-row boxes).
 cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm_ctrl, const SamuScanBwdArgs& args,
                                  cudaStream_t s, bool pdl);
+// tm_dw: an 8-row map over dw (BF16 gradients; used when M is a multiple of
+// 64, the rows are then written by TMA from shared memory).
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
-                                 const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
+                                 const CUtensorMap& tm_dw, const SamuScanBwdArgs& args, cudaStream_t s, bool pdl);
 // Controller backward (with the (dnu, dtheta) reductions), then the
 // reductions of the unit-direction and amplitude gradients.
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl);

@@ -104,8 +104,9 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 //  - A warp takes groups of kCfTok consecutive tokens (group g, g + W, ...
 //    for its global warp index g out of W).  Lane l owns the chunks l, l+32,
 //    ... of every token of the group: 16-byte loads straight from x_sel (one
-//    warp load = 512 contiguous bytes of one row), FP32 dot products with the
-//    raw directions, then a fixed-order reduce-scatter of the 2 kCfTok sums
+//    warp load = 512 contiguous bytes of one row), paired FP32 dot products
+//    with the raw directions (even and odd channels summed apart, then
+//    added), then a fixed-order reduce-scatter of the 2 kCfTok sums
 //    across the lanes.  One lane per token scales by 1/||w||, adds the bias
 //    entry and evaluates p = tanh(s_phi), r = tanh(s_r), q(r), d, c, and
 //    E - 1 = expm1(c), C = cos d, S = sin d.
@@ -121,27 +122,19 @@ constexpr int kCfTok = 4;      // tokens per warp group
 constexpr int kCfBatch = 4;    // chunks per lane per load batch
 constexpr int kCfBlock = 5;    // float4 per staged weight chunk (80 bytes: conflict-free for 8 distinct chunks)
 
-// Sums of the 8 channels of chunk q (BF16) against both staged directions.
-__device__ __forceinline__ void dot8(const uint4 q, const float4* __restrict__ wb, float& sp, float& sr) {
-    float x[8];
-    unpack8(q, x);
+// Sums of the 8 channels of chunk q (BF16) against both staged directions,
+// as paired FP32 (even and odd channels in the two halves of each pair).
+__device__ __forceinline__ void dot8(const uint4 q, const float4* __restrict__ wb, f2x& sp, f2x& sr) {
     const float4 p0 = wb[0], p1 = wb[1], r0 = wb[2], r1 = wb[3];
-    sp = fmaf(x[0], p0.x, sp);
-    sp = fmaf(x[1], p0.y, sp);
-    sp = fmaf(x[2], p0.z, sp);
-    sp = fmaf(x[3], p0.w, sp);
-    sp = fmaf(x[4], p1.x, sp);
-    sp = fmaf(x[5], p1.y, sp);
-    sp = fmaf(x[6], p1.z, sp);
-    sp = fmaf(x[7], p1.w, sp);
-    sr = fmaf(x[0], r0.x, sr);
-    sr = fmaf(x[1], r0.y, sr);
-    sr = fmaf(x[2], r0.z, sr);
-    sr = fmaf(x[3], r0.w, sr);
-    sr = fmaf(x[4], r1.x, sr);
-    sr = fmaf(x[5], r1.y, sr);
-    sr = fmaf(x[6], r1.z, sr);
-    sr = fmaf(x[7], r1.w, sr);
+    const f2x x0 = bf2x(q.x), x1 = bf2x(q.y), x2 = bf2x(q.z), x3 = bf2x(q.w);
+    sp = fma2(x0, pk2(p0.x, p0.y), sp);
+    sp = fma2(x1, pk2(p0.z, p0.w), sp);
+    sp = fma2(x2, pk2(p1.x, p1.y), sp);
+    sp = fma2(x3, pk2(p1.z, p1.w), sp);
+    sr = fma2(x0, pk2(r0.x, r0.y), sr);
+    sr = fma2(x1, pk2(r0.z, r0.w), sr);
+    sr = fma2(x2, pk2(r1.x, r1.y), sr);
+    sr = fma2(x3, pk2(r1.z, r1.w), sr);
 }
 
 // The per-token scalars from the two dot products (raw directions).
@@ -238,9 +231,9 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
     const uint4* x = a.x;
     for (long long g = gw; g < n_groups; g += W) {
         const long long t0 = g * kCfTok;
-        float acc[2 * kCfTok];
+        f2x pacc[2 * kCfTok];   // {token k: phi, r} as even/odd-channel pairs
 #pragma unroll
-        for (int v = 0; v < 2 * kCfTok; ++v) acc[v] = 0.f;
+        for (int v = 0; v < 2 * kCfTok; ++v) pacc[v] = 0ull;
         for (int i0 = 0; i0 < cpl; i0 += kCfBatch) {
             uint4 xv[kCfBatch][kCfTok];
 #pragma unroll
@@ -258,9 +251,16 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
                 if (i0 + b < cpl && c < nch) {
                     const float4* wb = wsm + (size_t)c * kCfBlock;
 #pragma unroll
-                    for (int k = 0; k < kCfTok; ++k) dot8(xv[b][k], wb, acc[2 * k], acc[2 * k + 1]);
+                    for (int k = 0; k < kCfTok; ++k) dot8(xv[b][k], wb, pacc[2 * k], pacc[2 * k + 1]);
                 }
             }
+        }
+        float acc[2 * kCfTok];
+#pragma unroll
+        for (int v = 0; v < 2 * kCfTok; ++v) {
+            float lo, hi;
+            up2(pacc[v], lo, hi);
+            acc[v] = lo + hi;
         }
         // reduce-scatter of the 8 sums {token k: phi, r} over the lanes:
         // halving exchanges at distances 16, 8, 4 (lane bit b keeps the upper
@@ -478,7 +478,6 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     __shared__ float4 s_red[kCtrlBwdMaxThreads / 32];
     __shared__ float2 s_nm[32];
     pdl_trigger();
-    pdl_wait();
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -488,7 +487,7 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     const CtrlSmem sm = ctrl_smem(smem_raw, cg, D);
     long long s0, s1;
     ctrl_stage_range(cg, cta, s0, s1);
-    if (tid == 0) {   // the first stages go out before the scalar phase
+    if (tid == 0) {   // the first stages go out before the dependency wait and the scalar phase
         for (int i = 0; i < cg.ring; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], cg.consumers);
@@ -498,6 +497,7 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
             ctrl_issue(sm, (int)(st - s0), a.x, st * nn, (int)min((long long)nn, a.BL - st * nn), D, cg);
         }
     }
+    pdl_wait();   // x_sel is an input; everything below reads the earlier kernels' results
     const long long tb = s0 * cg.stage_tok;
     const long long te = min(a.BL, s1 * cg.stage_tok);
 

@@ -29,6 +29,7 @@
 // w (forward) or dy (backward) hit in L2.  Every composition runs in a fixed
 // order: results are bitwise reproducible from run to run.
 #include <algorithm>
+#include <type_traits>
 
 #include "kernels.cuh"
 
@@ -57,6 +58,9 @@ struct alignas(128) WarpRingT {
 // the reverse replay 8-token units (a w item and a dy item each), 4 per warp.
 using MapRing = WarpRingT<kMapRows, kMapSlots>;
 using RevRing = WarpRingT<kHalf, 4>;
+using RevRingTma = WarpRingT<kHalf, 6>;   // dw staged in the dy slots: two more slots cover the deferred refill
+constexpr int kRevTmaSmem = kEngineWarps * (int)sizeof(RevRingTma);
+static_assert(RevRingTma::kSlots % 2 == 0, "w and dy items alternate over the slots");
 constexpr int kWarpSmem = (int)(sizeof(MapRing) > sizeof(RevRing) ? sizeof(MapRing) : sizeof(RevRing));
 constexpr int kEngineSmem = kEngineWarps * kWarpSmem;
 
@@ -193,14 +197,25 @@ __device__ __forceinline__ void store_map2(float4* p, const c2x& l, const c2x& b
 // Lane 0: stage the item at token ts of tensor `tm` (both halves of the
 // warp's 64 modes) and its control words into ring slot `slot`.  The warp has
 // finished reading the slot (__syncwarp before the call).
+// The item's two boxes (the slot's expected bytes include the control words,
+// so the slot completes only once ring_issue_ctrl has been issued too).
 template <class Ring>
-__device__ __forceinline__ void ring_issue(Ring& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
-                                           int x_re, int x_im, int ts, int b) {
+__device__ __forceinline__ void ring_issue_data(Ring& R, int slot, const CUtensorMap* tm, int x_re, int x_im, int ts,
+                                                int b) {
     fence_proxy_async();
     mbar_arrive_expect_tx(&R.full[slot], Ring::kItemBytes);
     tma_load_3d(&R.box[slot][0][0][0], tm, x_re, ts, b, &R.full[slot]);
     tma_load_3d(&R.box[slot][1][0][0], tm, x_im, ts, b, &R.full[slot]);
+}
+template <class Ring>
+__device__ __forceinline__ void ring_issue_ctrl(Ring& R, int slot, const CUtensorMap* tm_ctrl, int ts, int b) {
     tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
+}
+template <class Ring>
+__device__ __forceinline__ void ring_issue(Ring& R, int slot, const CUtensorMap* tm, const CUtensorMap* tm_ctrl,
+                                           int x_re, int x_im, int ts, int b) {
+    ring_issue_data(R, slot, tm, x_re, x_im, ts, b);
+    ring_issue_ctrl(R, slot, tm_ctrl, ts, b);
 }
 
 template <class Ring>
@@ -402,12 +417,17 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     ring_init(R, lane);
     pdl_trigger();
-    pdl_wait();
-    if (gw == 0 && lane == 0) *a.status = 0u;
-    // item k is sub-chunk nsc-1-k: the segment from its end backwards
+    // item k is sub-chunk nsc-1-k: the segment from its end backwards.  w is an
+    // input no earlier kernel of the call writes: its first boxes go out
+    // before the wait for the controller forward; the control words after it.
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
-            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
+            ring_issue_data(R, k, &tm_w, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
+    pdl_wait();
+    if (gw == 0 && lane == 0) *a.status = 0u;
+    if (lane == 0)
+        for (int k = 0; k < kRing && k < T.nsc; ++k)
+            ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x P;
     P.re = dup2(1.f);
@@ -483,10 +503,11 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     ring_init(R, lane);
     pdl_trigger();
+    if (lane == 0)   // w (an input) before the wait for the maps kernel, control words after it
+        for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_data(R, k, &tm_w, x_re, x_im, T.t_begin + k * kN, T.b);
     pdl_wait();
     if (lane == 0)
-        for (int k = 0; k < kRing && k < T.nsc; ++k)
-            ring_issue(R, k, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + k * kN, T.b);
+        for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + k * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x z = czero();
     if (active) {   // entry: the CTA's entry state through the maps of the earlier segments of the CTA
@@ -636,11 +657,13 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     ring_init(R, lane);
     pdl_trigger();
-    pdl_wait();
-    // item k is sub-chunk k: the segment from its start forwards
+    // item k is sub-chunk k: the segment from its start forwards (dy, an
+    // input, before the dependency wait; control words after it)
     if (lane == 0)
-        for (int k = 0; k < kRing && k < T.nsc; ++k)
-            ring_issue(R, k, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + k * kN, T.b);
+        for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_data(R, k, &tm_dy, x_re, x_im, T.t_begin + k * kN, T.b);
+    pdl_wait();
+    if (lane == 0)
+        for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + k * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x Q;
     Q.re = dup2(1.f);
@@ -749,13 +772,17 @@ __device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane)
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
+// How the reverse replay writes dw.
+enum DwStore { kDwBf16 = 0, kDwFp32 = 1, kDwBf16Tma = 2 };
+
 // Reverse sweep of one unit: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
 // kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa; per
 // token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64 modes
 // of the warp (written to kp[token * kp_row + {0, 1}]); then
-// A <- conj(lambda_t) A.
-template <bool SIMPLE, bool FP32>
-__device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_t* gre, const uint32_t* gim, int nh,
+// A <- conj(lambda_t) A.  DW == kDwBf16Tma: dw_t replaces dy_t in the staged
+// box (every lane active), stored by TMA afterwards.
+template <bool SIMPLE, int DW>
+__device__ __forceinline__ void bwd_reverse_unit(const float4* sc, uint32_t* gre, uint32_t* gim, int nh,
                                                  float nu0, float nu1, const c2x (&u)[kHalf],
                                                  const f2x (&lre)[kHalf], const f2x (&lim)[kHalf], c2x& A,
                                                  f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf,
@@ -770,8 +797,11 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_
             const Ctl2 ct = load_ctl(sc, i);
             A.re = add2(A.re, bf2x(gre[i * kWords]));
             A.im = add2(A.im, bf2x(gim[i * kWords]));
-            if (active) {
-                if (FP32) {
+            if (DW == kDwBf16Tma) {
+                gre[i * kWords] = x2bf(A.re);
+                gim[i * kWords] = x2bf(A.im);
+            } else if (active) {
+                if (DW == kDwFp32) {
                     f2x* p = reinterpret_cast<f2x*>(dwf + 2 * (size_t)i * row);
                     p[0] = A.re;
                     p[half] = A.im;   // M floats further: the imaginary half
@@ -806,15 +836,17 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, const uint32_
     if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
 }
 
-template <bool FP32>
+template <int DW>
 __global__ void __launch_bounds__(kEngineThreads, 2)
     samu_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
-                         const __grid_constant__ CUtensorMap tm_ctrl, SamuScanBwdArgs a) {
+                         const __grid_constant__ CUtensorMap tm_ctrl, const __grid_constant__ CUtensorMap tm_dw,
+                         SamuScanBwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    RevRing& R = warp_ring<RevRing>(smem_raw, warp);
-    constexpr int kRingH = RevRing::kSlots;
+    using Ring = typename std::conditional<DW == kDwBf16Tma, RevRingTma, RevRing>::type;
+    Ring& R = *reinterpret_cast<Ring*>(smem_raw + (size_t)warp * sizeof(Ring));
+    constexpr int kRingH = Ring::kSlots;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     if (gw >= (long long)g.n_chains * g.NS) return;
@@ -832,10 +864,12 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     auto item_ts = [&](int k) { return T.t_begin + (n_units - 1 - (k >> 1)) * kHalf; };
     ring_init(R, lane);
     pdl_trigger();
+    if (lane == 0)   // w and dy (inputs) before the wait for the maps kernel, control words after it
+        for (int k = 0; k < kRingH && k < n_items; ++k)
+            ring_issue_data(R, k, (k & 1) ? &tm_dy : &tm_w, x_re, x_im, item_ts(k), T.b);
     pdl_wait();
     if (lane == 0)
-        for (int k = 0; k < kRingH && k < n_items; ++k)
-            ring_issue(R, k, (k & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(k), T.b);
+        for (int k = 0; k < kRingH && k < n_items; ++k) ring_issue_ctrl(R, k, &tm_ctrl, item_ts(k), T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
@@ -877,7 +911,10 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         }
         // w item: forward sweep
         int slot = it % kRingH;
-        if (!ring_wait(R, it, n_items, a.status, lane)) return;
+        if (!ring_wait(R, it, n_items, a.status, lane)) {
+            if (DW == kDwBf16Tma && lane == 0) bulk_wait_all();
+            return;
+        }
         const float4* sc = R.ctrl[slot];
         const SubKind kd = sub_kind<kHalf>(sc, nh, lane, k);
         c2x u[kHalf];
@@ -890,25 +927,46 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
                         T.b);
         // dy item: reverse sweep
         slot = (it + 1) % kRingH;
-        if (!ring_wait(R, it + 1, n_items, a.status, lane)) return;
+        if (!ring_wait(R, it + 1, n_items, a.status, lane)) {
+            if (DW == kDwBf16Tma && lane == 0) bulk_wait_all();
+            return;
+        }
         sc = R.ctrl[slot];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
         float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
         float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
         if (kd.simple)
-            bwd_reverse_unit<true, FP32>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre,
-                                         lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
-                                         2 * (size_t)g.n_groups, lane);
+            bwd_reverse_unit<true, DW>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre,
+                                       lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
+                                       2 * (size_t)g.n_groups, lane);
         else
-            bwd_reverse_unit<false, FP32>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u,
-                                          lre, lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
-                                          2 * (size_t)g.n_groups, lane);
-        __syncwarp();
-        if (lane == 0 && it + 1 + kRingH < n_items)
-            ring_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
-                        item_ts(it + 1 + kRingH), T.b);
+            bwd_reverse_unit<false, DW>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u,
+                                        lre, lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
+                                        2 * (size_t)g.n_groups, lane);
+        if (DW == kDwBf16Tma) {
+            // the unit's dw rows are in this slot: TMA-store them, then refill
+            // the previous unit's dy slot once its store has read it
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&tm_dw, x_re, ts, T.b, &R.box[slot][0][0][0]);
+                tma_store_3d(&tm_dw, x_im, ts, T.b, &R.box[slot][1][0][0]);
+                bulk_commit();
+                const int j = it - 1 + kRingH;   // a dy item (kRingH is even)
+                if (it >= 2 && j < n_items) {
+                    bulk_wait_read<1>();
+                    ring_issue(R, (it - 1) % kRingH, &tm_dy, &tm_ctrl, x_re, x_im, item_ts(j), T.b);
+                }
+            }
+        } else {
+            __syncwarp();
+            if (lane == 0 && it + 1 + kRingH < n_items)
+                ring_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
+                            item_ts(it + 1 + kRingH), T.b);
+        }
     }
+    if (DW == kDwBf16Tma && lane == 0) bulk_wait_all();
     if (active) {
         float n0, n1, t0, t1;
         up2(acc_nu, n0, n1);
@@ -931,13 +989,13 @@ struct EngineOccupancy {
 
 EngineOccupancy g_occ[64];
 
-bool set_smem(const void* fn) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngineSmem) == cudaSuccess;
+bool set_smem(const void* fn, int smem) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
 }
 
-int occupancy(const void* fn) {
+int occupancy(const void* fn, int smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kEngineThreads, kEngineSmem) != cudaSuccess) return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kEngineThreads, smem) != cudaSuccess) return 1;
     return n > 0 ? n : 1;
 }
 
@@ -948,20 +1006,24 @@ const EngineOccupancy& engine_occupancy() {
     if (!o.done) {
         int v = 0;
         o.sms = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;
-        const void* fm = reinterpret_cast<const void*>(samu_fwd_maps_kernel);
-        const void* fr = reinterpret_cast<const void*>(samu_fwd_replay_kernel<false>);
-        const void* fr32 = reinterpret_cast<const void*>(samu_fwd_replay_kernel<true>);
-        const void* bm = reinterpret_cast<const void*>(samu_bwd_maps_kernel);
-        const void* bb = reinterpret_cast<const void*>(samu_bwd_main_kernel<false>);
-        const void* bb32 = reinterpret_cast<const void*>(samu_bwd_main_kernel<true>);
-        set_smem(fm);
-        set_smem(fr);
-        set_smem(fr32);
-        set_smem(bm);
-        set_smem(bb);
-        set_smem(bb32);
-        o.fwd = std::min(occupancy(fm), std::min(occupancy(fr), occupancy(fr32)));
-        o.bwd = std::min(occupancy(bm), std::min(occupancy(bb), occupancy(bb32)));
+        const void* fwd[] = {reinterpret_cast<const void*>(samu_fwd_maps_kernel),
+                             reinterpret_cast<const void*>(samu_fwd_replay_kernel<false>),
+                             reinterpret_cast<const void*>(samu_fwd_replay_kernel<true>)};
+        const void* bwd[] = {reinterpret_cast<const void*>(samu_bwd_maps_kernel),
+                             reinterpret_cast<const void*>(samu_bwd_main_kernel<kDwBf16>),
+                             reinterpret_cast<const void*>(samu_bwd_main_kernel<kDwFp32>),
+                             reinterpret_cast<const void*>(samu_bwd_main_kernel<kDwBf16Tma>)};
+        const int bwd_smem[] = {kEngineSmem, kEngineSmem, kEngineSmem, kRevTmaSmem};
+        o.fwd = 1 << 30;
+        for (const void* f : fwd) {
+            set_smem(f, kEngineSmem);
+            o.fwd = std::min(o.fwd, occupancy(f, kEngineSmem));
+        }
+        o.bwd = 1 << 30;
+        for (int i = 0; i < 4; ++i) {
+            set_smem(bwd[i], bwd_smem[i]);
+            o.bwd = std::min(o.bwd, occupancy(bwd[i], bwd_smem[i]));
+        }
         o.done = true;
     }
     return o;
@@ -1002,12 +1064,16 @@ cudaError_t launch_samu_bwd_maps(const CUtensorMap& tm_dy, const CUtensorMap& tm
 }
 
 cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm_w, const CUtensorMap& tm_ctrl,
-                                 const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
+                                 const CUtensorMap& tm_dw, const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
+    const unsigned grid = engine_grid(args.g);
     if (args.grad_fp32)
-        return launch_ex(samu_bwd_main_kernel<true>, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy,
-                         tm_w, tm_ctrl, args);
-    return launch_ex(samu_bwd_main_kernel<false>, engine_grid(args.g), kEngineThreads, kEngineSmem, s, pdl, tm_dy,
-                     tm_w, tm_ctrl, args);
+        return launch_ex(samu_bwd_main_kernel<kDwFp32>, grid, kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_w, tm_ctrl,
+                         tm_dw, args);
+    if (args.g.M % kGroup == 0)
+        return launch_ex(samu_bwd_main_kernel<kDwBf16Tma>, grid, kEngineThreads, kRevTmaSmem, s, pdl, tm_dy, tm_w,
+                         tm_ctrl, tm_dw, args);
+    return launch_ex(samu_bwd_main_kernel<kDwBf16>, grid, kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_w, tm_ctrl,
+                     tm_dw, args);
 }
 
 }  // namespace lrs

@@ -67,6 +67,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--sweep", action="store_true",
+                   help="time every workload family (one JSON line each) instead of the headline line")
     return p.parse_args(argv)
 
 
@@ -474,6 +476,114 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# --sweep: every workload family, F+B replayed as a CUDA graph (L2 flushed
+# before every step), per-kernel durations from an eager pass with the
+# library's events, achieved bytes against the algorithmic minimum
+# (SAMU 16 B*L*D, RG-LRU 22 B*L*D with BF16 gradients).  One JSON line each.
+SWEEP_BYTES_PER_BLD = {"samu": 16.0, "rglru": 22.0}
+
+
+def sweep_one(name, dev, K, W):
+    import torch
+    from linear_recurrence_sequence_gb300 import api, synth
+    wl = synth.WORKLOADS[name]
+    B, L, D = wl.B, wl.L, wl.D
+    inp = wl.make()
+    bf, f32 = torch.bfloat16, torch.float32
+    if wl.kind == "samu":
+        M = D // 2
+        t = api.samu_tensors_from_numpy(inp, dev)
+        nsaved, nscratch = api.samu_workspace_bytes(B, L, D)
+        fo = {"y": torch.empty((B, L, D), dtype=bf, device=dev), "hT": torch.empty((B, M, 2), dtype=f32, device=dev)}
+        go = {"dx_sel": torch.empty((B, L, D), dtype=bf, device=dev), "dw": torch.empty((B, L, D), dtype=bf, device=dev),
+              "dh0": torch.empty((B, M, 2), dtype=f32, device=dev), "dnu": torch.empty((M,), dtype=f32, device=dev),
+              "dtheta": torch.empty((M,), dtype=f32, device=dev), "dw_phi": torch.empty((D + 1,), dtype=f32, device=dev),
+              "dw_r": torch.empty((D + 1,), dtype=f32, device=dev), "da_phi": torch.empty((1,), dtype=f32, device=dev),
+              "da_r": torch.empty((1,), dtype=f32, device=dev)}
+    else:
+        t = api.rglru_tensors_from_numpy(inp, dev)
+        nsaved, nscratch = api.rglru_workspace_bytes(B, L, D)
+        fo = {"y": torch.empty((B, L, D), dtype=bf, device=dev), "hT": torch.empty((B, D), dtype=f32, device=dev)}
+        go = {"dx": torch.empty((B, L, D), dtype=bf, device=dev), "dlx": torch.empty((B, L, D), dtype=bf, device=dev),
+              "dla": torch.empty((B, L, D), dtype=bf, device=dev), "dalpha": torch.empty((D,), dtype=f32, device=dev),
+              "dh0": torch.empty((B, D), dtype=f32, device=dev)}
+    saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+
+    def step():
+        if wl.kind == "samu":
+            api.samu_forward(t["x_sel"], t["w"], t["h0"], t["reset"], t["nu"], t["theta"], t["w_phi"], t["w_r"],
+                             t["a_phi"], t["a_r"], out=fo, saved=saved, scratch=scratch)
+            api.samu_backward(t["dy"], t["dhT"], t["x_sel"], t["w"], t["h0"], t["reset"], t["nu"], t["theta"],
+                              t["w_phi"], t["w_r"], t["a_phi"], t["a_r"], saved, out=go, scratch=scratch)
+        else:
+            api.rglru_forward(t["x"], t["lx"], t["la"], t["alpha"], t["h0"], t["reset"], out=fo, saved=saved,
+                              scratch=scratch)
+            api.rglru_backward(t["dy"], t["dhT"], t["x"], t["lx"], t["la"], t["alpha"], t["h0"], t["reset"], saved,
+                               out=go, scratch=scratch)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(cs)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        step()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record()
+        graph.replay()
+        ev1[i].record()
+    torch.cuda.synchronize(dev)
+    if api.device_status(scratch) != 0:
+        raise RuntimeError(f"device-side wait timed out ({name})")
+    ms = sorted(ev0[i].elapsed_time(ev1[i]) for i in range(K))
+    ms_mean = sum(ms) / K
+    KP = max(3, min(K, 10))
+    api.profile_begin(KP * 10)
+    for _ in range(KP):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    records, _ = api.profile_end(KP * 10)
+    per = {}
+    for kname, kms in records:
+        per.setdefault(kname, []).append(kms)
+    BLD = B * L * D
+    peak, _ = load_peak()
+    alg = SWEEP_BYTES_PER_BLD[wl.kind] * BLD
+    gbs = alg / (ms_mean / 1e3) / 1e9
+    return {"workload": name, "kind": wl.kind, "B": B, "L": L, "D": D, "steps": K,
+            "ms_per_step": round(ms_mean, 5), "ms_min": round(ms[0], 5), "ms_max": round(ms[-1], 5),
+            "Mtok_per_s": round(B * L / (ms_mean / 1e3) / 1e6, 3),
+            "algorithmic_bytes": alg, "achieved_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+            "frac_of_8tbs": round(gbs / 8000.0, 4),
+            "kernels_avg_ms": {k: round(sum(v) / len(v), 5) for k, v in sorted(per.items())}}
+
+
+def run_sweep(args, local):
+    import torch
+    from linear_recurrence_sequence_gb300 import synth
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K = max(5, min(args.steps, 50))
+    W = max(3, args.warmup)
+    for name in synth.WORKLOADS:
+        line = sweep_one(name, dev, K, W)
+        print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
@@ -481,6 +591,10 @@ def main(argv=None):
         if rank != 0:
             return 0
         run_reference(args)
+        return 0
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args, local)
         return 0
     if world > 1:
         import torch.distributed as dist

@@ -69,6 +69,7 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--sweep", action="store_true",
                    help="time every workload family (one JSON line each) instead of the headline line")
+    p.add_argument("--only", default=None, help="with --sweep: comma-separated workload names")
     return p.parse_args(argv)
 
 
@@ -578,7 +579,8 @@ def run_sweep(args, local):
     torch.cuda.set_device(dev)
     K = max(5, min(args.steps, 50))
     W = max(3, args.warmup)
-    for name in synth.WORKLOADS:
+    names = args.only.split(",") if args.only else list(synth.WORKLOADS)
+    for name in names:
         line = sweep_one(name, dev, K, W)
         print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()

@@ -6,7 +6,10 @@
 // preparation fused into the scan (no materialised a/b tensors) and, at a
 // segment start, a_t = 0 and a unit normaliser ("Griffin 第 4、5 节 H800 对照
 // 协议", "RG-LRU 的固定方程").  1 - a^2 is evaluated as -expm1(2 log a) so the
-// normaliser keeps full FP32 relative accuracy when a is close to 1.
+// normaliser keeps full FP32 relative accuracy when a is close to 1.  The
+// gate functions use the SFU's approximations (sigmoid, square roots) and a
+// short series for expm1: the IEEE-rounded library forms cost several times
+// the instructions and the recurrence does not amplify these errors.
 //
 // Tiling as in the SAMU scan: a chain is (batch row, 64 channels), a CTA owns
 // a 128-token tile (x, l^x, l^a and, backward, dy staged by TMA), 8 warps of
@@ -27,8 +30,28 @@ struct RgGate {
     float ga;   // sigmoid(l^a)
 };
 
+// 1 / (1 + e^{-v}) from two SFU operations.  Its ~2^-22 relative error only
+// scales the write gate and, through log a = g^a (-8 softplus), moves log a by
+// at most ~1e-8 absolute: nothing accumulates through the recurrence.
 __device__ __forceinline__ float sigmoid_f(float v) {
-    return __frcp_rn(1.0f + ex2_approx(-v * kLog2e));
+    return rcp_approx(1.0f + ex2_approx(-v * kLog2e));
+}
+
+// e^v - 1.  For |v| < 1/4 its Taylor series through v^8 (coefficients 1/k!;
+// the remainder is below 1e-10 relative there), so that 1 - a^2 keeps full
+// relative accuracy when a is close to 1; otherwise e^v - 1 from ex2, where
+// the cancellation costs at most a factor 4.
+__device__ __forceinline__ float expm1_fast(float v) {
+    float p = fmaf(v, 1.0f / 40320.0f, 1.0f / 5040.0f);
+    p = fmaf(v, p, 1.0f / 720.0f);
+    p = fmaf(v, p, 1.0f / 120.0f);
+    p = fmaf(v, p, 1.0f / 24.0f);
+    p = fmaf(v, p, 1.0f / 6.0f);
+    p = fmaf(v, p, 0.5f);
+    p = fmaf(v, p, 1.0f);
+    const float series = v * p;
+    const float direct = ex2_approx(v * kLog2e) - 1.0f;
+    return fabsf(v) < 0.25f ? series : direct;
 }
 
 // nsp = -8 softplus(alpha) for this channel
@@ -38,8 +61,8 @@ __device__ __forceinline__ RgGate rg_gate(float lx, float la, float nsp, bool is
     gt.ga = sigmoid_f(la);
     const float lg = gt.ga * nsp;                 // log a
     gt.a = ex2_approx(lg * kLog2e);
-    gt.u = -expm1f(2.0f * lg);
-    gt.n = sqrtf(fmaxf(gt.u, 0.0f));
+    gt.u = -expm1_fast(2.0f * lg);
+    gt.n = sqrt_approx(fmaxf(gt.u, 0.0f));
     if (is_reset) {
         gt.a = 0.0f;
         gt.n = 1.0f;
@@ -434,8 +457,8 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             const float dlx1 = H1 * xx.y * g1.n * g1.gx * (1.f - g1.gx);
             float dla0 = 0.f, dla1 = 0.f;
             if (!rs) {
-                const float ab0 = fmaf(H0, hp[i].x, H0 * xx.x * g0.gx * (-2.f * g0.a) * rsqrtf(fmaxf(4.f * g0.u, 1e-6f)));
-                const float ab1 = fmaf(H1, hp[i].y, H1 * xx.y * g1.gx * (-2.f * g1.a) * rsqrtf(fmaxf(4.f * g1.u, 1e-6f)));
+                const float ab0 = fmaf(H0, hp[i].x, H0 * xx.x * g0.gx * (-2.f * g0.a) * rsqrt_approx(fmaxf(4.f * g0.u, 1e-6f)));
+                const float ab1 = fmaf(H1, hp[i].y, H1 * xx.y * g1.gx * (-2.f * g1.a) * rsqrt_approx(fmaxf(4.f * g1.u, 1e-6f)));
                 dla0 = ab0 * nsp0 * g0.a * g0.ga * (1.f - g0.ga);
                 dla1 = ab1 * nsp1 * g1.a * g1.ga * (1.f - g1.ga);
                 da0 = fmaf(ab0, -8.f * g0.ga * sa0 * g0.a, da0);

@@ -77,30 +77,64 @@ __device__ __forceinline__ float softplus_f(float v) {
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
+// Lane 0 of thread 0: the three boxes of `tile` into ring slot `slot`.
+__device__ __forceinline__ void rg_fwd_issue(uint8_t* slot_base, uint64_t* bar, const CUtensorMap* tm_x,
+                                             const CUtensorMap* tm_lx, const CUtensorMap* tm_la, const ScanGeom& g,
+                                             long long tile) {
+    const int chain = (int)(tile % g.n_chains);
+    const int c = (int)(tile / g.n_chains);
+    const int b = chain / g.n_groups, grp = chain % g.n_groups;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(bar, 3 * kRgBoxBytes);
+    tma_load_3d(slot_base, tm_x, grp * kGroup, c * kRgTile, b, bar);
+    tma_load_3d(slot_base + kRgBoxBytes, tm_lx, grp * kGroup, c * kRgTile, b, bar);
+    tma_load_3d(slot_base + 2 * kRgBoxBytes, tm_la, grp * kGroup, c * kRgTile, b, bar);
+}
+
+// Persistent CTAs: each takes tiles in ticket order (atomic counter) and keeps
+// the next ticket's boxes in flight in the second slot of a two-slot ring
+// while it works on the current one.  Tickets are taken in increasing order
+// by every CTA and each CTA finishes its current tile before its prefetched
+// one, so the smallest tile in progress always finds its predecessors done.
 __global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_lx,
                           const __grid_constant__ CUtensorMap tm_la, RglruScanFwdArgs a) {
-    extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: x, l^x, l^a
-    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
-    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kRgBoxBytes);
-    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kRgBoxBytes);
+    extern __shared__ __align__(128) uint8_t s_dyn[];   // [slot][x, l^x, l^a boxes]
     __shared__ uint8_t s_rst[kRgTile];
     __shared__ float4 s_map[kRgWarps][32];
     __shared__ float2 s_ent[kRgWarps][32];
-    __shared__ __align__(8) uint64_t s_bar;
-    __shared__ uint32_t s_tile;
+    __shared__ __align__(8) uint64_t s_bars[2];
+    __shared__ uint32_t s_tick[2];
     __shared__ int s_err;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const ScanGeom& g = a.g;
+    const uint32_t n_tiles = (uint32_t)g.n_tiles;
     if (tid == 0) {
-        s_tile = atomicAdd(a.counter, 1u);
-        mbar_init(&s_bar, 1);
+        mbar_init(&s_bars[0], 1);
+        mbar_init(&s_bars[1], 1);
+        s_tick[0] = atomicAdd(a.counter, 1u);
+        if (s_tick[0] < n_tiles) rg_fwd_issue(s_dyn, &s_bars[0], &tm_x, &tm_lx, &tm_la, g, s_tick[0]);
     }
     __syncthreads();
-    const ScanGeom& g = a.g;
-    const long long tile = s_tile;
+    int pend = -1;   // iteration whose prefetched copy is outstanding when the loop is left early
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    const uint32_t tile_u = s_tick[slot];
+    if (tile_u >= n_tiles) break;
+    if (tid == 0) {   // the next ticket into the other slot (free since the end of the previous tile)
+        s_tick[slot ^ 1] = atomicAdd(a.counter, 1u);
+        if (s_tick[slot ^ 1] < n_tiles)
+            rg_fwd_issue(s_dyn + (size_t)(slot ^ 1) * 3 * kRgBoxBytes, &s_bars[slot ^ 1], &tm_x, &tm_lx, &tm_la, g,
+                         s_tick[slot ^ 1]);
+    }
+    uint8_t* sb = s_dyn + (size_t)slot * 3 * kRgBoxBytes;
+    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb);
+    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb + kRgBoxBytes);
+    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb + 2 * kRgBoxBytes);
+    const long long tile = tile_u;
     const int chain = (int)(tile % g.n_chains);
     const int c = (int)(tile / g.n_chains);
     const int b = chain / g.n_groups;
@@ -114,12 +148,6 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     uint32_t* fl = a.flags + (size_t)chain * CT;
     const size_t hb = (size_t)b * g.CS;
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 3 * kRgBoxBytes);
-        tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_lx[0][0], &tm_lx, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_la[0][0], &tm_la, grp * kGroup, t0, b, &s_bar);
-    }
     if (tid < kRgTile) {
         const int t = t0 + tid;
         s_rst[tid] = (t < L && a.reset != nullptr && a.reset[(size_t)b * L + t] != 0) ? 1 : 0;
@@ -131,14 +159,14 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     }
     const int r0 = warp * kSub;
     const int nsub = max(0, min(kSub, L - t0 - r0));
-    const bool landed = mbar_wait_bounded(&s_bar, 0);
+    const bool landed = mbar_wait_bounded(&s_bars[slot], (uint32_t)(it >> 1) & 1u);
     if (!__syncthreads_and(landed)) {
         if (tid == 0) {
             st_release_gpu(fl + c, kFlagErr);
             atomicOr(a.status, kStatusTimeout);
         }
-        mbar_wait_bounded(&s_bar, 0);
-        return;
+        pend = it + 1;
+        break;
     }
 
     float4 ab[kSub];   // {a_d, b_d, a_d+1, b_d+1}
@@ -232,7 +260,10 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         if (lane == 0) s_err = err ? 1 : 0;
     }
     __syncthreads();
-    if (s_err) return;
+    if (s_err) {
+        pend = it + 1;
+        break;
+    }
 
     const float2 e = s_ent[warp][lane];
     float z0 = e.x, z1 = e.y;
@@ -251,6 +282,11 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     }
     if (active && nsub > 0 && t0 + r0 + nsub == L)
         *reinterpret_cast<float2*>(a.hT + (size_t)b * D + d) = make_float2(z0, z1);
+    __syncthreads();   // this slot and s_rst free; the next ticket visible
+  }
+    // leaving early (a failed wait): the next ticket's copy may still be in flight
+    if (tid == 0 && pend >= 0 && s_tick[pend & 1] < n_tiles)
+        mbar_wait_bounded(&s_bars[pend & 1], (uint32_t)(pend >> 1) & 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -525,12 +561,25 @@ __global__ void __launch_bounds__(256) rglru_alpha_stage2_kernel(const float* __
     dalpha[d] = s;
 }
 
+// Persistent grid: as many CTAs as are resident at once, at most one per tile.
+template <typename K>
+unsigned rg_grid(K kernel, int smem, long long n_tiles) {
+    int dev = 0, sms = 1, per = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kRgThreads, smem) != cudaSuccess || per < 1)
+        per = 1;
+    const long long n = (long long)sms * per;
+    return (unsigned)(n < n_tiles ? n : (n_tiles > 0 ? n_tiles : 1));
+}
+
 cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
                                   const RglruScanFwdArgs& args, cudaStream_t s) {
-    const int smem = 3 * kRgBoxBytes;
+    const int smem = 2 * 3 * kRgBoxBytes;   // two slots
     cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_fwd_kernel<<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_x, tm_lx, tm_la, args);
+    rglru_scan_fwd_kernel<<<rg_grid(rglru_scan_fwd_kernel, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
+        tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }
 

@@ -210,8 +210,6 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.misc = misc;
     cf.modes = modes;
     cf.status = at<uint32_t>(scratch, sc.status);
-    cf.counters = at<uint32_t>(scratch, sc.counters);   // the forward's half
-    cf.n_counters = samu_seg_geom(B, L, M, 0).n_chains;
     LRS_LAUNCH(KID_SAMU_CTRL_FWD, stream, launch_samu_ctrl_fwd(cf, stream, false));
 
     const SegGeom g = samu_scan_geom(B, L, M, false);
@@ -228,8 +226,6 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     a.hsub = at<float2>(saved, sv.hsub);
     a.smap = at<float4>(scratch, sc.smap);
     a.cmap = at<float4>(scratch, sc.cmap);
-    a.cent = at<float2>(scratch, sc.cent);
-    a.counters = at<uint32_t>(scratch, sc.counters);
     a.status = at<uint32_t>(scratch, sc.status);
     LRS_LAUNCH(KID_SAMU_FWD_MAPS, stream, launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream, pdl_ok()));
     LRS_LAUNCH(KID_SAMU_SCAN_FWD, stream, launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream, pdl_ok()));
@@ -262,7 +258,7 @@ int samu_backward(const void* dy, const float* dhT,
     const int fp32 = grad_dtype == LRS_GRAD_FP32 ? 1 : 0;
 
     const float4* ctrl = at<float4>(saved, sv.ctrl);
-    // status word and the chain arrival counters start at zero
+    // the status word starts at zero
     if (cudaMemsetAsync(scratch, 0, sc.zero_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     // 16-row boxes for the adjoint maps, 8-row boxes for the reverse replay
     CUtensorMap tm_dy, tm_ctrl, tm_dy8, tm_w8, tm_ctrl8;
@@ -281,8 +277,6 @@ int samu_backward(const void* dy, const float* dhT,
     s.dh0 = dh0;
     s.smap = at<float4>(scratch, sc.smap);
     s.cmap = at<float4>(scratch, sc.cmap);
-    s.cent = at<float2>(scratch, sc.cent);
-    s.counters = at<uint32_t>(scratch, sc.counters) + g.n_chains;
     s.kpart = at<float2>(scratch, sc.kpart);
     s.numod = at<float2>(scratch, sc.numod);
     s.status = at<uint32_t>(scratch, sc.status);

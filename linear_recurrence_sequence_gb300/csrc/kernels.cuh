@@ -198,8 +198,6 @@ struct SamuScanFwdArgs {
     float2* hsub;           // [B][CS][M] the state every 8 tokens
     float4* smap;           // [B][NS][M] segment maps
     float4* cmap;           // [B][NC][M] CTA maps (four consecutive segments)
-    float2* cent;           // [B][NC][M] CTA entry states
-    uint32_t* counters;     // [n_chains] arrivals of the maps CTAs, zero on entry, left zero
     uint32_t* status;       // cleared by the maps kernel
 };
 
@@ -217,8 +215,6 @@ struct SamuScanBwdArgs {
     float* dh0;             // [B,M,2]
     float4* smap;           // [B][NS][M] adjoint segment maps
     float4* cmap;           // [B][NC][M] adjoint CTA maps
-    float2* cent;           // [B][NC][M] adjoints arriving at each CTA's last token
-    uint32_t* counters;     // [n_chains] arrivals of the maps CTAs, zero on entry, left zero
     float2* kpart;          // [B*L][n_groups] {sum Im kappa, sum -nu Re kappa}
     float2* numod;          // [B][NS][M] {dnu, dtheta} per segment
     uint32_t* status;
@@ -295,8 +291,6 @@ struct SamuCtrlFwdArgs {
     float* wh;                     // [2][D+1]
     float* misc;
     float4* modes;                 // [M] lbar hi/lo
-    uint32_t* counters;            // [n_counters] chain arrival counters of the forward scan, zeroed here
-    int n_counters;
     uint32_t* status;
 };
 

@@ -13,7 +13,7 @@ namespace lrs {
 constexpr size_t kAlign = 256;
 constexpr int kCtrlRowsMax = 608;    // partial-sum rows of the controller backward (CTAs)
 constexpr int kReduceGroups = 64;     // first-stage groups of the RG-LRU per-tile alpha partials
-constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status word + counters
+constexpr int kStatusBlock = 64;      // bytes at the start of scratch: status word + arrival counter
 
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -148,8 +148,8 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
 }
 
 struct SamuScratch {
-    size_t status, counters, smap, cmap, cent, kpart, numod, dwh_part, amp_part, dot_part, total;
-    size_t zero_bytes;     // status block + counters: cleared at the start of a backward call
+    size_t status, smap, cmap, kpart, numod, dwh_part, amp_part, dot_part, total;
+    size_t zero_bytes;     // status block: cleared at the start of a backward call
 };
 
 inline SamuScratch samu_scratch_layout(int B, int L, int D) {
@@ -160,13 +160,11 @@ inline SamuScratch samu_scratch_layout(int B, int L, int D) {
     SamuScratch s;
     size_t o = 0;
     s.status = o;   o += kStatusBlock;
-    s.counters = o; o += (size_t)2 * g.n_chains * 4;                   // chain arrivals (forward, backward)
     s.zero_bytes = o;
     o = align_up(o);
     const size_t crows = (size_t)B * (g.NSmax / kSegPerCta) * M;
     s.smap = o;     o = align_up(o + rows * 16);                      // segment maps
-    s.cmap = o;     o = align_up(o + crows * 16);                     // CTA maps (4 segments)
-    s.cent = o;     o = align_up(o + crows * 8);                      // CTA entry states / incoming adjoints
+    s.cmap = o;     o = align_up(o + crows * 16);                     // CTA maps (8 segments)
     s.kpart = o;    o = align_up(o + BL * g.n_groups * 8);            // per-token controller partials
     s.numod = o;    o = align_up(o + rows * 8);                       // per-segment (dnu, dtheta)
     const size_t prow = (size_t)2 * ctrl_half_stride(D) * 4;              // one partial row, bytes

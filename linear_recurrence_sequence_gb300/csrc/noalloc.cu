@@ -71,7 +71,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     const SamuSaved sv = samu_saved_layout(B, L, D);
     const SamuScratch sc = samu_scratch_layout(B, L, D);
     const size_t scratch_off = align_up(sv.total);
-    const size_t need = scratch_off + sc.cent + (size_t)B * (samu_seg_geom(B, L, M, 0).NSmax / kSegPerCta) * M * 8;
+    const size_t need = scratch_off + sc.cmap + (size_t)B * (samu_seg_geom(B, L, M, 0).NSmax / kSegPerCta) * M * 16;
     if (need > (size_t)LRS_NOALLOC_BYTES) return LRS_ERR_TOO_LARGE;
 
     void* base = nullptr;
@@ -105,8 +105,6 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     cf.misc = misc;
     cf.modes = modes;
     cf.status = reinterpret_cast<uint32_t*>(scratch + sc.status);
-    cf.counters = reinterpret_cast<uint32_t*>(scratch + sc.counters);   // the forward's half
-    cf.n_counters = samu_seg_geom(B, L, M, 0).n_chains;
     if (launch_samu_ctrl_fwd(cf, stream, false) != cudaSuccess) return LRS_ERR_CUDA;
 
     CUtensorMap tm_w, tm_ctrl;
@@ -122,8 +120,6 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     a.hsub = reinterpret_cast<float2*>(saved + sv.hsub);
     a.smap = reinterpret_cast<float4*>(scratch + sc.smap);
     a.cmap = reinterpret_cast<float4*>(scratch + sc.cmap);
-    a.cent = reinterpret_cast<float2*>(scratch + sc.cent);
-    a.counters = reinterpret_cast<uint32_t*>(scratch + sc.counters);
     a.status = reinterpret_cast<uint32_t*>(scratch + sc.status);
     if (launch_samu_fwd_maps(tm_w, tm_ctrl, a, stream, true) != cudaSuccess) return LRS_ERR_CUDA;
     if (launch_samu_fwd_replay(tm_w, tm_ctrl, a, stream, true) != cudaSuccess) return LRS_ERR_CUDA;

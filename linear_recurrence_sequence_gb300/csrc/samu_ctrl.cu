@@ -113,8 +113,7 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
 //  - The last ceil(M/32) warps of the grid (those with the fewest groups)
 //    first compute the per-mode transition constants
 //    lbar_m = e^{-nu_m} e^{i theta_m} as double-floats (hi, lo) in FP64.
-//  - CTA 0 stores w_hat and the amplitude factors for the backward and clears
-//    the forward scan's chain counters.
+//  - CTA 0 stores w_hat and the amplitude factors for the backward.
 // ---------------------------------------------------------------------------
 constexpr int kCfWarps = 8;
 constexpr int kCfThreads = 32 * kCfWarps;
@@ -208,7 +207,6 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
             a.wh[j] = a.w_phi[j] * inv_phi;
             a.wh[n + j] = a.w_r[j] * inv_r;
         }
-        for (int j = tid; j < a.n_counters; j += kCfThreads) a.counters[j] = 0u;
         if (tid == 0) {
             a.misc[0] = k_phi;
             a.misc[1] = k_r;

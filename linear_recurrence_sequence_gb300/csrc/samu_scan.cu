@@ -18,14 +18,14 @@
 // a private ring of two shared-memory slots that TMA fills one sub-chunk
 // ahead (a [16 x 64] BF16 box per half plus the 16 control words).
 //
-// Each direction is three launches with no waits between CTAs:
+// Each direction is two launches with no waits between CTAs:
 //  1. maps:    every warp composes its segment's affine map, walking the
-//              segment in the opposite time direction to step 3;
-//  2. prefix:  one CTA per chain folds the segment maps into every segment's
-//              entry state (16 warps over 16 ranges, then a fixed-order
-//              combine);
-//  3. replay:  every warp replays its segment from its entry state.
-// Step 3 starts each segment where step 1 finished it, so its first reads of
+//              segment in the opposite time direction to step 2, and a CTA
+//              (8 consecutive segments of one chain) composes its CTA map;
+//  2. replay:  every CTA first folds the chain's earlier (later) CTA maps into
+//              its entry state (adjoint), every warp applies the earlier
+//              (later) segment maps of its CTA and replays its segment.
+// Step 2 starts each segment where step 1 finished it, so its first reads of
 // w (forward) or dy (backward) hit in L2.  Every composition runs in a fixed
 // order: results are bitwise reproducible from run to run.
 #include <algorithm>
@@ -308,14 +308,11 @@ __device__ __forceinline__ void fwd_replay_sub(const float4* sc, const uint32_t*
 }
 
 // ---------------------------------------------------------------------------
-// Chain prefix, run at the end of the maps kernel by the CTA that finishes a
-// chain last (its arrival makes the counter reach NC).  Its kEngineWarps
-// warps take equal ranges of the chain's NC CTA maps: each composes its
-// range, the partial maps are applied in a fixed order, and each warp walks
-// its range writing the state entering every CTA (forward) or the adjoint
-// arriving at every CTA's last token (backward).  Maps are per mode
-// {l.re, l.im, b.re, b.im}; lane l handles modes m, m+1 (cm and out point at
-// mode m, CTA 0).
+// Chain prefix, run by every replay CTA for itself at its start: its
+// kEngineWarps warps take equal ranges of the earlier (forward) or later
+// (backward) CTA maps of the chain, compose them, and the partial maps are
+// applied in a fixed order.  Maps are per mode {l.re, l.im, b.re, b.im}; lane
+// l handles modes m, m+1 (cm points at mode m, CTA 0).
 // ---------------------------------------------------------------------------
 constexpr int kFoldChunk = 4;
 
@@ -332,11 +329,17 @@ __device__ __forceinline__ void ld_maps(const float4* __restrict__ cm, int M, in
     }
 }
 
-// forward: entry of CTA i = C_{i-1} o ... o C_0 (h0)
-__device__ __forceinline__ void chain_prefix_fwd(const float4* __restrict__ cm, float4* __restrict__ out, int n,
-                                                 int M, const float* h0p, float4 (*part)[32][2], int warp, int lane,
-                                                 bool active) {
-    const int lo = n * warp / kEngineWarps, hi = n * (warp + 1) / kEngineWarps;
+// The state entering CTA cc of a chain, C_{cc-1} o ... o C_0 (h0), formed by
+// the CTA's kEngineWarps warps: warp w composes the CTA maps of its range
+// [cc w / 8, cc (w+1) / 8) in order (one batch of loads per kFoldChunk maps)
+// and leaves the result in `xch(w)` (per lane 2 float4); after a CTA
+// barrier every warp applies the 8 partial maps to h0 in warp order.  cm
+// points at CTA 0's map of the lane's first mode; xch(w) must not be written
+// by anything else meanwhile.  Fixed order; every warp gets the same bits.
+template <class Xch>
+__device__ __forceinline__ c2x cta_entry_fwd(const float4* __restrict__ cm, int cc, int M, const float* h0p, Xch xch,
+                                             int warp, int lane, bool active) {
+    const int lo = cc * warp / kEngineWarps, hi = cc * (warp + 1) / kEngineWarps;
     float4 P0 = identity_map(), P1 = P0;
     if (active) {
         for (int i0 = lo; i0 < hi; i0 += kFoldChunk) {
@@ -351,51 +354,39 @@ __device__ __forceinline__ void chain_prefix_fwd(const float4* __restrict__ cm, 
             }
         }
     }
-    part[warp][lane][0] = P0;
-    part[warp][lane][1] = P1;
+    xch(warp)[2 * lane] = P0;
+    xch(warp)[2 * lane + 1] = P1;
     __syncthreads();
-    if (!active) return;
     float2 z0 = make_float2(0.f, 0.f), z1 = z0;
-    if (h0p != nullptr) {
+    if (active && h0p != nullptr) {
         const float4 hv = *reinterpret_cast<const float4*>(h0p);
         z0 = make_float2(hv.x, hv.y);
         z1 = make_float2(hv.z, hv.w);
     }
-    for (int v = 0; v < warp; ++v) {
-        z0 = capply(part[v][lane][0], z0);
-        z1 = capply(part[v][lane][1], z1);
-    }
-    for (int i0 = lo; i0 < hi; i0 += kFoldChunk) {
-        float4 T[kFoldChunk][2];
-        ld_maps(cm, M, i0, lo, hi, 1, T);
 #pragma unroll
-        for (int q = 0; q < kFoldChunk; ++q) {
-            if (i0 + q < hi) {
-                out[(size_t)(i0 + q) * (M / 2)] = make_float4(z0.x, z0.y, z1.x, z1.y);
-                z0 = capply(T[q][0], z0);
-                z1 = capply(T[q][1], z1);
-            }
-        }
+    for (int v = 0; v < kEngineWarps; ++v) {
+        z0 = capply(xch(v)[2 * lane], z0);
+        z1 = capply(xch(v)[2 * lane + 1], z1);
     }
+    __syncthreads();   // the exchange areas are free again
+    c2x z;
+    z.re = pk2(z0.x, z1.x);
+    z.im = pk2(z0.y, z1.y);
+    return z;
 }
 
 // Shared memory of the maps kernels' last phase, on top of the drained
-// staging rings: the CTA's segment maps, the fold partials and the last-CTA
-// flag each sit in the box area of one warp's ring (warps 0, 1, 2), never on
-// a ring's mbarriers (whose memory is not reused).
+// staging rings: the CTA's segment maps sit in the box area of warp 0's
+// ring, never on a ring's mbarriers (whose memory is not reused).
 struct EpilogueSmem {
     float4 (*seg)[32][2];
-    float4 (*part)[32][2];
-    int* last;
 };
 static_assert(sizeof(float4) * kEngineWarps * 32 * 2 <= sizeof(((MapRing*)nullptr)->box),
-              "segment maps and partials must fit a ring's box area");
+              "segment maps must fit a ring's box area");
 
 __device__ __forceinline__ EpilogueSmem epilogue_smem(uint8_t* smem_raw) {
     EpilogueSmem e;
     e.seg = reinterpret_cast<float4 (*)[32][2]>(&warp_ring<MapRing>(smem_raw, 0).box[0][0][0][0]);
-    e.part = reinterpret_cast<float4 (*)[32][2]>(&warp_ring<MapRing>(smem_raw, 1).box[0][0][0][0]);
-    e.last = reinterpret_cast<int*>(&warp_ring<MapRing>(smem_raw, 2).box[0][0][0][0]);
     return e;
 }
 
@@ -449,14 +440,13 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     }
     if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, P, be);
 
-    // CTA map (its four segments in time order), then the chain prefix in the
-    // CTA that completes the chain
+    // CTA map: its segments composed in time order
     __syncthreads();   // rings drained
     const EpilogueSmem E = epilogue_smem(smem_raw);
     store_map2(&E.seg[warp][lane][0], P, be);
     __syncthreads();
-    const int chain = blockIdx.x / g.NC, cc = blockIdx.x % g.NC;
     if (warp == 0) {
+        const int cc = blockIdx.x % g.NC;
         float4 A0 = E.seg[0][lane][0], A1 = E.seg[0][lane][1];
 #pragma unroll
         for (int w = 1; w < kEngineWarps; ++w) {
@@ -468,17 +458,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
             cm[0] = A0;
             cm[1] = A1;
         }
-        __threadfence();
     }
-    __syncthreads();
-    if (threadIdx.x == 0) *E.last = atomicAdd(a.counters + chain, 1u) == (uint32_t)(g.NC - 1) ? 1 : 0;
-    __syncthreads();
-    if (!*E.last) return;
-    __threadfence();
-    chain_prefix_fwd(a.cmap + (size_t)T.b * g.NC * M + m, reinterpret_cast<float4*>(a.cent + (size_t)T.b * g.NC * M + m),
-                     g.NC, M, a.h0 != nullptr ? a.h0 + ((size_t)T.b * M + m) * 2 : nullptr, E.part, warp, lane,
-                     active);
-    if (threadIdx.x == 0) a.counters[chain] = 0u;
 }
 
 template <bool Y32>
@@ -492,8 +472,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     constexpr int kRing = MapRing::kSlots;
     constexpr int kN = MapRing::kRows;
     const SegGeom& g = a.g;
-    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
-    if (gw >= (long long)g.n_chains * g.NS) return;
+    const long long gw = (long long)blockIdx.x * kEngineWarps + warp;   // < n_chains * NS: whole CTAs
     const SegTask T = seg_task(g, gw);
     const int M = g.M;
     const int L = g.L;
@@ -506,14 +485,22 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     if (lane == 0)   // w (an input) before the wait for the maps kernel, control words after it
         for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_data(R, k, &tm_w, x_re, x_im, T.t_begin + k * kN, T.b);
     pdl_wait();
-    if (lane == 0)
+    // the CTA's entry state from the earlier CTAs' maps (the rings' control-word
+    // areas, not yet filled, carry the warps' partial maps)
+    const int cc = T.s / kSegPerCta;
+    const c2x e0 = cta_entry_fwd(
+        a.cmap + (size_t)T.b * g.NC * M + m, cc, M, a.h0 != nullptr ? a.h0 + ((size_t)T.b * M + m) * 2 : nullptr,
+        [&](int w) { return &warp_ring<MapRing>(smem_raw, w).ctrl[0][0]; }, warp, lane, active);
+    if (lane == 0) {
+        fence_proxy_async();
         for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + k * kN, T.b);
+    }
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     c2x z = czero();
     if (active) {   // entry: the CTA's entry state through the maps of the earlier segments of the CTA
-        const int cc = T.s / kSegPerCta;
-        const float4 e = *reinterpret_cast<const float4*>(a.cent + ((size_t)T.b * g.NC + cc) * M + m);
-        float2 z0 = make_float2(e.x, e.y), z1 = make_float2(e.z, e.w);
+        float2 z0, z1;
+        up2(e0.re, z0.x, z1.x);
+        up2(e0.im, z0.y, z1.y);
         for (int v0 = cc * kSegPerCta; v0 < T.s; v0 += 4) {   // the CTA's earlier segments, 4 loads at a time
             float4 Tm[4][2];
 #pragma unroll
@@ -592,11 +579,14 @@ __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* g
     }
 }
 
-// backward: adjoint arriving at CTA i's last token = C_{i+1} o ... o C_{n-1} (dhT)
-__device__ __forceinline__ void chain_prefix_bwd(const float4* __restrict__ cm, float4* __restrict__ out, int n,
-                                                 int M, const float* dhTp, float4 (*part)[32][2], int warp,
-                                                 int lane, bool active) {
-    const int lo = n * warp / kEngineWarps, hi = n * (warp + 1) / kEngineWarps;
+// The adjoint arriving at the last token of CTA cc of a chain,
+// C_{cc+1} o ... o C_{n-1} (dhT), formed like cta_entry_fwd over the later
+// CTAs [cc+1, n): warp w composes its range from the latest map down.
+template <class Xch>
+__device__ __forceinline__ c2x cta_entry_bwd(const float4* __restrict__ cm, int cc, int n, int M, const float* dhTp,
+                                             Xch xch, int warp, int lane, bool active) {
+    const int cnt = n - 1 - cc;
+    const int lo = cc + 1 + cnt * warp / kEngineWarps, hi = cc + 1 + cnt * (warp + 1) / kEngineWarps;
     float4 P0 = identity_map(), P1 = P0;
     if (active) {
         for (int i0 = hi - 1; i0 >= lo; i0 -= kFoldChunk) {
@@ -611,32 +601,25 @@ __device__ __forceinline__ void chain_prefix_bwd(const float4* __restrict__ cm, 
             }
         }
     }
-    part[warp][lane][0] = P0;
-    part[warp][lane][1] = P1;
+    xch(warp)[2 * lane] = P0;
+    xch(warp)[2 * lane + 1] = P1;
     __syncthreads();
-    if (!active) return;
     float2 r0 = make_float2(0.f, 0.f), r1 = r0;
-    if (dhTp != nullptr) {
+    if (active && dhTp != nullptr) {
         const float4 v = *reinterpret_cast<const float4*>(dhTp);
         r0 = make_float2(v.x, v.y);
         r1 = make_float2(v.z, v.w);
     }
-    for (int v = kEngineWarps - 1; v > warp; --v) {
-        r0 = capply(part[v][lane][0], r0);
-        r1 = capply(part[v][lane][1], r1);
-    }
-    for (int i0 = hi - 1; i0 >= lo; i0 -= kFoldChunk) {
-        float4 T[kFoldChunk][2];
-        ld_maps(cm, M, i0, lo, hi, -1, T);
 #pragma unroll
-        for (int q = 0; q < kFoldChunk; ++q) {
-            if (i0 - q >= lo) {
-                out[(size_t)(i0 - q) * (M / 2)] = make_float4(r0.x, r0.y, r1.x, r1.y);
-                r0 = capply(T[q][0], r0);
-                r1 = capply(T[q][1], r1);
-            }
-        }
+    for (int v = kEngineWarps - 1; v >= 0; --v) {
+        r0 = capply(xch(v)[2 * lane], r0);
+        r1 = capply(xch(v)[2 * lane + 1], r1);
     }
+    __syncthreads();
+    c2x A;
+    A.re = pk2(r0.x, r1.x);
+    A.im = pk2(r0.y, r1.y);
+    return A;
 }
 
 __global__ void __launch_bounds__(kEngineThreads, 3)
@@ -685,14 +668,13 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     }
     if (active) store_map2(a.smap + ((size_t)T.b * g.NS + T.s) * M + m, Q, be);
 
-    // adjoint CTA map (the latest segment applied first), then the reverse
-    // chain prefix in the CTA that completes the chain
+    // adjoint CTA map (the latest segment applied first)
     __syncthreads();   // rings drained
     const EpilogueSmem E = epilogue_smem(smem_raw);
     store_map2(&E.seg[warp][lane][0], Q, be);
     __syncthreads();
-    const int chain = blockIdx.x / g.NC, cc = blockIdx.x % g.NC;
     if (warp == 0) {
+        const int cc = blockIdx.x % g.NC;
         float4 A0 = E.seg[kEngineWarps - 1][lane][0], A1 = E.seg[kEngineWarps - 1][lane][1];
 #pragma unroll
         for (int w = kEngineWarps - 2; w >= 0; --w) {
@@ -704,17 +686,7 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
             cm[0] = A0;
             cm[1] = A1;
         }
-        __threadfence();
     }
-    __syncthreads();
-    if (threadIdx.x == 0) *E.last = atomicAdd(a.counters + chain, 1u) == (uint32_t)(g.NC - 1) ? 1 : 0;
-    __syncthreads();
-    if (!*E.last) return;
-    __threadfence();
-    chain_prefix_bwd(a.cmap + (size_t)T.b * g.NC * M + m, reinterpret_cast<float4*>(a.cent + (size_t)T.b * g.NC * M + m),
-                     g.NC, M, a.dhT != nullptr ? a.dhT + ((size_t)T.b * M + m) * 2 : nullptr, E.part, warp, lane,
-                     active);
-    if (threadIdx.x == 0) a.counters[chain] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -849,7 +821,6 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     constexpr int kRingH = Ring::kSlots;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
-    if (gw >= (long long)g.n_chains * g.NS) return;
     const SegTask T = seg_task(g, gw);
     const int M = g.M;
     const int L = g.L;
@@ -868,16 +839,25 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         for (int k = 0; k < kRingH && k < n_items; ++k)
             ring_issue_data(R, k, (k & 1) ? &tm_dy : &tm_w, x_re, x_im, item_ts(k), T.b);
     pdl_wait();
-    if (lane == 0)
+    // the adjoint arriving at the CTA from the later CTAs' maps (the rings'
+    // control-word areas, not yet filled, carry the warps' partial maps)
+    const int cc = T.s / kSegPerCta;
+    const c2x a0 = cta_entry_bwd(
+        a.cmap + (size_t)T.b * g.NC * M + m, cc, g.NC, M, a.dhT != nullptr ? a.dhT + ((size_t)T.b * M + m) * 2 : nullptr,
+        [&](int w) { return &reinterpret_cast<Ring*>(smem_raw + (size_t)w * sizeof(Ring))->ctrl[0][0]; }, warp, lane,
+        active);
+    if (lane == 0) {
+        fence_proxy_async();
         for (int k = 0; k < kRingH && k < n_items; ++k) ring_issue_ctrl(R, k, &tm_ctrl, item_ts(k), T.b);
+    }
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
     c2x A = czero();
     if (active) {   // the adjoint arriving at the CTA through the maps of the later segments of the CTA
-        const int cc = T.s / kSegPerCta;
-        const float4 e = *reinterpret_cast<const float4*>(a.cent + ((size_t)T.b * g.NC + cc) * M + m);
-        float2 r0 = make_float2(e.x, e.y), r1 = make_float2(e.z, e.w);
+        float2 r0, r1;
+        up2(a0.re, r0.x, r1.x);
+        up2(a0.im, r0.y, r1.y);
         for (int v1 = (cc + 1) * kSegPerCta - 1; v1 > T.s; v1 -= 4) {   // the CTA's later segments, latest first
             float4 Tm[4][2];
 #pragma unroll

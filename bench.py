@@ -572,6 +572,70 @@ def sweep_one(name, dev, K, W):
             "kernels_avg_ms": {k: round(sum(v) / len(v), 5) for k, v in sorted(per.items())}}
 
 
+# Decode step (one token of each of B sequences): 14 B*D bytes per step
+# (x_sel, w, y in BF16; the FP32 state read and written).
+DECODE_WORKLOADS = {"decode_B256_D2048": (256, 2048), "decode_B4096_D2048": (4096, 2048),
+                    "decode_B16384_D1024": (16384, 1024)}
+
+
+def sweep_decode(name, dev, K, W):
+    import torch
+    from linear_recurrence_sequence_gb300 import api, synth
+    B, D = DECODE_WORKLOADS[name]
+    M = D // 2
+    inp = synth.samu_inputs(B, 1, D, 0, h0=True, reset_p=0.0)
+    t = api.samu_tensors_from_numpy(inp, dev)
+    x, w = t["x_sel"][:, 0].contiguous(), t["w"][:, 0].contiguous()
+    params = api.samu_decode_prepare(t["nu"], t["theta"], t["w_phi"], t["w_r"], t["a_phi"], t["a_r"])
+    state = t["h0"].clone()
+    out = {"y": torch.empty((B, D), dtype=torch.bfloat16, device=dev)}
+
+    def step():
+        api.samu_decode_step(x, w, state, params, None, out=out)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(cs)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        step()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record()
+        graph.replay()
+        ev1[i].record()
+    torch.cuda.synchronize(dev)
+    ms = sorted(ev0[i].elapsed_time(ev1[i]) for i in range(K))
+    ms_mean = sum(ms) / K
+    KP = max(3, min(K, 10))
+    api.profile_begin(KP * 2)
+    for _ in range(KP):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    records, _ = api.profile_end(KP * 2)
+    kms = [r[1] for r in records]
+    peak, _ = load_peak()
+    alg = 14.0 * B * D
+    gbs = alg / (ms_mean / 1e3) / 1e9
+    return {"workload": name, "kind": "samu_decode", "B": B, "L": 1, "D": D, "steps": K,
+            "ms_per_step": round(ms_mean, 5), "ms_min": round(ms[0], 5), "ms_max": round(ms[-1], 5),
+            "Mtok_per_s": round(B / (ms_mean / 1e3) / 1e6, 3),
+            "algorithmic_bytes": alg, "achieved_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+            "frac_of_8tbs": round(gbs / 8000.0, 4),
+            "kernels_avg_ms": {"samu_decode_step_kernel": round(sum(kms) / max(1, len(kms)), 5)}}
+
+
 def run_sweep(args, local):
     import torch
     from linear_recurrence_sequence_gb300 import synth
@@ -579,9 +643,9 @@ def run_sweep(args, local):
     torch.cuda.set_device(dev)
     K = max(5, min(args.steps, 50))
     W = max(3, args.warmup)
-    names = args.only.split(",") if args.only else list(synth.WORKLOADS)
+    names = args.only.split(",") if args.only else list(synth.WORKLOADS) + list(DECODE_WORKLOADS)
     for name in names:
-        line = sweep_one(name, dev, K, W)
+        line = sweep_decode(name, dev, K, W) if name in DECODE_WORKLOADS else sweep_one(name, dev, K, W)
         print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
 

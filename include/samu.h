@@ -89,7 +89,8 @@ int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
  * capacity) kernels, their id (2 controller forward, 3 SAMU forward replay,
  * 4 SAMU backward main, 5 controller backward, 6 SAMU parameter reductions,
  * 7 RG-LRU scan forward, 8 RG-LRU scan backward, 9 RG-LRU alpha reduction,
- * 10 SAMU forward maps, 11 SAMU backward maps) and duration in milliseconds; *count receives the number of
+ * 10 SAMU forward maps, 11 SAMU backward maps, 12 SAMU decode prepare,
+ * 13 SAMU decode step) and duration in milliseconds; *count receives the number of
  * kernels launched while profiling was on.  Not thread-safe: one profiling
  * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),
  * LRS_ERR_CUDA. */
@@ -160,6 +161,43 @@ int samu_backward(const void* dy, const float* dhT,
                   const void* saved, void* dx_sel, void* dw, int grad_dtype,
                   float* dh0, float* dnu, float* dtheta, float* dw_phi, float* dw_r,
                   float* da_phi, float* da_r, void* scratch, cudaStream_t stream);
+
+/* ======================================================================== */
+/* SAMU single-token decode step                                              */
+/* ======================================================================== */
+
+/* Floats of the caller-owned decode parameter block for width D (pure host
+ * function; the block must be 16-byte aligned).  Errors: LRS_ERR_ARG
+ * (floats NULL), LRS_ERR_UNSUPPORTED (D as for samu_forward). */
+int samu_decode_params_floats(int D, size_t* floats);
+
+/* Prepares the per-parameter part of the decode step ([SAMU page] section 05:
+ * w_hat = w / ||w|| over all D+1 entries, the amplitude factors
+ * tanh(a)/sqrt(M), and lbar_m = e^{-nu_m} e^{i theta_m} formed in FP64) into
+ * `params` (device, samu_decode_params_floats(D) floats).  Inputs as for
+ * samu_forward.  Call again whenever the parameters change.  One launch,
+ * asynchronous on `stream`. */
+int samu_decode_prepare(const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                        const float* a_phi, const float* a_r, int D, float* params, cudaStream_t stream);
+
+/* One token of each of B sequences ([SAMU page] section 05 applied to one
+ * token with the carried state as z_{t-1}):  p, r, d, c, E, C, S from the
+ * token's x_sel row; z_m <- lambda_m z_m + b_m (lambda = 0 where reset[b] != 0);
+ * y = z in the halves layout.  Applying it token after token equals
+ * samu_forward over the sequence.
+ *
+ *   x_sel, w    [B,D] BF16 (in): the token of every sequence
+ *   state_in    [B,M,2] FP32 (in): z_{t-1};  state_out [B,M,2] FP32 (out),
+ *               may be the same buffer as state_in (updated in place)
+ *   reset       [B] uint8 (in) or NULL
+ *   params      prepared by samu_decode_prepare (in)
+ *   y           [B,D] BF16 (out);  y32 [B,D] FP32 (out) or NULL
+ * One launch (one CTA per sequence), asynchronous on `stream`.
+ * Errors: LRS_ERR_ARG (null or misaligned pointer, B < 1), LRS_ERR_UNSUPPORTED
+ * (D as for samu_forward), LRS_ERR_CUDA. */
+int samu_decode_step(const void* x_sel, const void* w, const float* state_in, float* state_out,
+                     const uint8_t* reset, const float* params, int B, int D, void* y, float* y32,
+                     cudaStream_t stream);
 
 /* ======================================================================== */
 /* RG-LRU (comparison path on the same engine)                               */

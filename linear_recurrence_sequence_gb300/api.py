@@ -37,6 +37,9 @@ _SIGNATURES = {
     "samu_forward": ([_P] * 10 + [_I, _I, _I] + [_P] * 6, _I),
     "samu_backward": ([_P] * 12 + [_I, _I, _I] + [_P, _P, _P, _I] + [_P] * 9, _I),
     "samu_forward_noalloc": ([_P] * 10 + [_I, _I, _I] + [_P] * 4, _I),
+    "samu_decode_params_floats": ([_I, _SZP], _I),
+    "samu_decode_prepare": ([_P] * 6 + [_I, _P, _P], _I),
+    "samu_decode_step": ([_P] * 6 + [_I, _I, _P, _P, _P], _I),
     "rglru_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
     "rglru_forward": ([_P] * 6 + [_I, _I, _I] + [_P] * 6, _I),
     "rglru_backward": ([_P] * 8 + [_I, _I, _I] + [_P] * 4 + [_I] + [_P] * 4, _I),
@@ -225,6 +228,56 @@ def samu_forward_noalloc(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r,
 
 
 # ---------------------------------------------------------------------------
+# SAMU decode step
+# ---------------------------------------------------------------------------
+def samu_decode_params_floats(D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("samu_decode_params_floats", _load().samu_decode_params_floats(D, ctypes.byref(n)))
+    return int(n.value)
+
+
+def samu_decode_prepare(nu, theta, w_phi, w_r, a_phi, a_r, *, params=None):
+    """Per-parameter part of the decode step through ``samu_decode_prepare``.  Returns the parameter block."""
+    dev = nu.device
+    M = nu.shape[0]
+    D = 2 * M
+    _need(nu, "nu", torch.float32, dev, (M,))
+    _need(theta, "theta", torch.float32, dev, (M,))
+    _need(w_phi, "w_phi", torch.float32, dev, (D + 1,))
+    _need(w_r, "w_r", torch.float32, dev, (D + 1,))
+    _need(a_phi, "a_phi", torch.float32, dev, (1,))
+    _need(a_r, "a_r", torch.float32, dev, (1,))
+    n = samu_decode_params_floats(D)
+    if params is None:
+        params = torch.empty(n, dtype=torch.float32, device=dev)
+    if params.numel() < n:
+        raise ValueError("params block is too small")
+    _check("samu_decode_prepare", _load().samu_decode_prepare(_ptr(nu), _ptr(theta), _ptr(w_phi), _ptr(w_r),
+                                                             _ptr(a_phi), _ptr(a_r), D, _ptr(params), _stream(dev)))
+    return params
+
+
+def samu_decode_step(x_sel, w, state, params, reset=None, *, state_out=None, want_y32=False, out=None):
+    """One token of each of B sequences through ``samu_decode_step``.  x_sel, w: [B,D] BF16; state: [B,M,2] FP32.
+
+    state_out defaults to ``state`` (updated in place).  Returns dict(y, y32, state)."""
+    dev = x_sel.device
+    B, D = x_sel.shape
+    M = D // 2
+    _need(x_sel, "x_sel", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev, (B, D))
+    _need(state, "state", torch.float32, dev, (B, M, 2))
+    _opt(reset, "reset", torch.uint8, dev, (B,))
+    so = state if state_out is None else state_out
+    _need(so, "state_out", torch.float32, dev, (B, M, 2))
+    y = _empty((B, D), torch.bfloat16, dev, out, "y")
+    y32 = _empty((B, D), torch.float32, dev, out, "y32") if want_y32 else None
+    _check("samu_decode_step", _load().samu_decode_step(_ptr(x_sel), _ptr(w), _ptr(state), _ptr(so), _ptr(reset),
+                                                       _ptr(params), B, D, _ptr(y), _ptr(y32), _stream(dev)))
+    return {"y": y, "y32": y32, "state": so}
+
+
+# ---------------------------------------------------------------------------
 # RG-LRU
 # ---------------------------------------------------------------------------
 def rglru_workspace_bytes(B: int, L: int, D: int):
@@ -299,7 +352,8 @@ KERNEL_NAMES = {
     2: "samu_ctrl_fwd_kernel", 3: "samu_fwd_replay_kernel",
     4: "samu_bwd_main_kernel", 5: "samu_ctrl_bwd_kernel", 6: "samu_params_kernel",
     7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
-    10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel",
+    10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel", 12: "samu_decode_prepare_kernel",
+    13: "samu_decode_step_kernel",
 }
 
 

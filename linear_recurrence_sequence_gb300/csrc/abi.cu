@@ -73,7 +73,7 @@ bool pdl_ok() { return !g_prof.on; }
 enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
     KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
-    KID_SAMU_BWD_MAPS
+    KID_SAMU_BWD_MAPS, KID_SAMU_DECODE_PREP, KID_SAMU_DECODE_STEP
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -322,6 +322,58 @@ int samu_backward(const void* dy, const float* dhT,
     pa.da_phi = da_phi;
     pa.da_r = da_r;
     LRS_LAUNCH(KID_SAMU_PARAMS, stream, launch_samu_params(pa, stream, pdl_ok()));
+    return LRS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// SAMU decode step
+// ---------------------------------------------------------------------------
+int samu_decode_params_floats(int D, size_t* floats) {
+    if (floats == nullptr) return LRS_ERR_ARG;
+    const int st = check_samu_shape(1, 1, D);
+    if (st != LRS_OK) return st;
+    *floats = samu_decode_params_floats(D);
+    return LRS_OK;
+}
+
+int samu_decode_prepare(const float* nu, const float* theta, const float* w_phi, const float* w_r,
+                        const float* a_phi, const float* a_r, int D, float* params, cudaStream_t stream) {
+    const int st = check_samu_shape(1, 1, D);
+    if (st != LRS_OK) return st;
+    if (!req(nu) || !req(theta) || !req(w_phi) || !req(w_r) || a_phi == nullptr || a_r == nullptr || !req(params))
+        return LRS_ERR_ARG;
+    SamuDecodePrepArgs a;
+    a.D = D;
+    a.nu = nu;
+    a.theta = theta;
+    a.w_phi = w_phi;
+    a.w_r = w_r;
+    a.a_phi = a_phi;
+    a.a_r = a_r;
+    a.params = params;
+    LRS_LAUNCH(KID_SAMU_DECODE_PREP, stream, launch_samu_decode_prepare(a, stream));
+    return LRS_OK;
+}
+
+int samu_decode_step(const void* x_sel, const void* w, const float* state_in, float* state_out,
+                     const uint8_t* reset, const float* params, int B, int D, void* y, float* y32,
+                     cudaStream_t stream) {
+    const int st = check_samu_shape(B, 1, D);
+    if (st != LRS_OK) return st;
+    if (!req(x_sel) || !req(w) || !req(state_in) || !req(state_out) || !req(params) || !req(y) || !opt(y32))
+        return LRS_ERR_ARG;
+    SamuDecodeStepArgs a;
+    a.B = B;
+    a.D = D;
+    a.x = static_cast<const uint16_t*>(x_sel);
+    a.w = static_cast<const uint16_t*>(w);
+    a.state_in = state_in;
+    a.state_out = state_out;
+    a.reset = reset;
+    a.params = params;
+    a.y = static_cast<uint16_t*>(y);
+    a.y32 = y32;
+    LRS_LAUNCH(KID_SAMU_DECODE_STEP, stream, launch_samu_decode_step(a, stream));
     return LRS_OK;
 }
 

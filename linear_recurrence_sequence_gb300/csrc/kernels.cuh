@@ -92,6 +92,20 @@ __device__ __forceinline__ ModePair load_modes(const float4* __restrict__ modes,
     return k;
 }
 
+// lbar_m = e^{-nu_m} e^{i theta_m} in FP64, stored as the double-float
+// {hi.re, hi.im, lo.re, lo.im} (hi the FP32 rounding, lo the FP32 rounding of
+// the remainder) that samu_lambda2 consumes.
+__device__ __forceinline__ void mode_constants(const float* __restrict__ nu, const float* __restrict__ theta,
+                                               int M, float4* __restrict__ modes, int m) {
+    if (m >= M) return;
+    const double r = exp(-(double)nu[m]);
+    double sn, cs;
+    sincos((double)theta[m], &sn, &cs);
+    const double re = r * cs, im = r * sn;
+    const float hr = (float)re, hi = (float)im;
+    modes[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
+}
+
 __device__ __forceinline__ ModePair zero_modes() {
     ModePair k;
     k.hr = k.hi = k.nhi = k.lr = k.li = k.nu = 0ull;
@@ -317,6 +331,37 @@ cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm
 // reductions of the unit-direction and amplitude gradients.
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------------------
+// SAMU single-token decode step
+// ---------------------------------------------------------------------------
+struct SamuDecodePrepArgs {
+    int D;
+    const float* nu;
+    const float* theta;
+    const float* w_phi;
+    const float* w_r;
+    const float* a_phi;
+    const float* a_r;
+    float* params;          // samu_decode_params_floats(D) floats, 16-byte aligned
+};
+
+struct SamuDecodeStepArgs {
+    long long B;
+    int D;
+    const uint16_t* x;      // [B][D] BF16
+    const uint16_t* w;      // [B][D] BF16
+    const float* state_in;  // [B][M][2]
+    float* state_out;       // [B][M][2] (may be state_in)
+    const uint8_t* reset;   // [B] or null
+    const float* params;
+    uint16_t* y;            // [B][D] BF16
+    float* y32;             // [B][D] or null
+};
+
+size_t samu_decode_params_floats(int D);
+cudaError_t launch_samu_decode_prepare(const SamuDecodePrepArgs& args, cudaStream_t s);
+cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // RG-LRU

@@ -83,17 +83,6 @@ __device__ __forceinline__ void unpack8(const uint4 q, float (&x)[8]) {
     f = bf2_to_f2(q.w); x[6] = f.x; x[7] = f.y;
 }
 
-__device__ __forceinline__ void mode_constants(const float* __restrict__ nu, const float* __restrict__ theta,
-                                               int M, float4* __restrict__ modes, int m) {
-    if (m >= M) return;
-    const double r = exp(-(double)nu[m]);
-    double sn, cs;
-    sincos((double)theta[m], &sn, &cs);
-    const double re = r * cs, im = r * sn;
-    const float hr = (float)re, hi = (float)im;
-    modes[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
-}
-
 // ---------------------------------------------------------------------------
 // Controller forward, with the parameter preparation folded in.
 //  - Every CTA stages the raw directions w_phi, w_r (first D entries) in

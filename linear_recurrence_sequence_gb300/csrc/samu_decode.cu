@@ -1,0 +1,198 @@
+// SAMU single-token decode step on sm_103a: one token of each of B
+// sequences, controller projection + transition + FP32 state update + BF16
+// output in one launch.
+//
+// Equations: SAMU GPU page ("SAMU 与 RG-LRU 的 H800 训练性能对比"), section 05
+// (controller, transition, recurrence), applied to one token with the carried
+// state as z_{t-1}: the forward over a sequence equals the decode step applied
+// token after token.  The per-parameter work that does not depend on the token
+// (unit directions, amplitude factors, lbar_m = e^{-nu_m} e^{i theta_m} as a
+// double-float formed in FP64) is done once by samu_decode_prepare into a
+// caller-owned parameter block, so that the step itself is one launch.
+//
+// GB300 organisation: one 256-thread CTA per sequence.  Thread t owns the
+// 8-channel chunks t, t+256, ... of the token's x_sel row for the two dot
+// products (16-byte loads, paired FP32 arithmetic), reduced over the CTA in a
+// fixed order; thread 0 forms the token's scalars.  Then thread t owns the
+// mode pairs (2t, 2t+1), (2t+512, 2t+513), ...: state, w and the outputs move
+// as 16-byte (state) and 4-byte (BF16 pairs) accesses, coalesced across the
+// CTA.  Bandwidth-bound: per sequence 2D (x_sel) + 2D (w) + 2D (y) + 8D (state
+// read and written) bytes.
+#include "kernels.cuh"
+
+namespace lrs {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+
+// Parameter block (floats from the start of the caller's buffer):
+//   wh  [2][D+1]   unit directions w_hat_phi, w_hat_r
+//   misc[8]        k_phi, k_r, (unused)
+//   nu  [M]
+//   modes [M] float4 lbar hi/lo (16-byte aligned)
+__host__ __device__ inline size_t dec_off_misc(int D) { return (size_t)2 * (D + 1); }
+__host__ __device__ inline size_t dec_off_nu(int D) { return dec_off_misc(D) + 8; }
+__host__ __device__ inline size_t dec_off_modes(int D) { return (dec_off_nu(D) + D / 2 + 3) & ~size_t(3); }
+size_t samu_decode_params_floats(int D) { return dec_off_modes(D) + (size_t)4 * (D / 2); }
+
+// Block 0: the norms ||w_phi||, ||w_r|| over all D+1 entries (FP32, fixed
+// order: per-thread strided sums, warp xor tree, warp-order sum), the unit
+// directions and the amplitude factors.  Blocks 1..: the per-mode constants
+// (FP64) and nu.
+__global__ void __launch_bounds__(kDecThreads) samu_decode_prepare_kernel(SamuDecodePrepArgs a) {
+    __shared__ float s_red[2][kDecWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int D = a.D, M = D / 2, n = D + 1;
+    float* wh = a.params;
+    float* misc = a.params + dec_off_misc(D);
+    float* nu_out = a.params + dec_off_nu(D);
+    float4* modes = reinterpret_cast<float4*>(a.params + dec_off_modes(D));
+    if (blockIdx.x > 0) {
+        const int m = (blockIdx.x - 1) * kDecThreads + tid;
+        mode_constants(a.nu, a.theta, M, modes, m);
+        if (m < M) nu_out[m] = a.nu[m];
+        return;
+    }
+    float sp = 0.f, sr = 0.f;
+    for (int j = tid; j < n; j += kDecThreads) {
+        const float x = a.w_phi[j], y = a.w_r[j];
+        sp = fmaf(x, x, sp);
+        sr = fmaf(y, y, sr);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+        sr += __shfl_xor_sync(0xffffffffu, sr, o);
+    }
+    if (lane == 0) {
+        s_red[0][warp] = sp;
+        s_red[1][warp] = sr;
+    }
+    __syncthreads();
+    float tp = 0.f, tr = 0.f;
+    for (int w = 0; w < kDecWarps; ++w) {
+        tp += s_red[0][w];
+        tr += s_red[1][w];
+    }
+    const float inv_phi = 1.0f / sqrtf(tp), inv_r = 1.0f / sqrtf(tr);
+    for (int j = tid; j < n; j += kDecThreads) {
+        wh[j] = a.w_phi[j] * inv_phi;
+        wh[n + j] = a.w_r[j] * inv_r;
+    }
+    if (tid == 0) {
+        const float ism = 1.0f / sqrtf((float)M);
+        misc[0] = tanhf(a.a_phi[0]) * ism;
+        misc[1] = tanhf(a.a_r[0]) * ism;
+    }
+}
+
+// One token of sequence blockIdx.x.
+__global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecodeStepArgs a) {
+    __shared__ float2 s_red[kDecWarps];
+    __shared__ float4 s_ctl;   // {E - 1, C, S, reset}
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int D = a.D, M = D / 2, nch = D / 8;
+    const size_t b = blockIdx.x;
+    const float* wh = a.params;
+    const float* misc = a.params + dec_off_misc(D);
+    const float* nu = a.params + dec_off_nu(D);
+    const float4* modes = reinterpret_cast<const float4*>(a.params + dec_off_modes(D));
+
+    // controller: x~ . w_hat for both directions
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x) + b * nch;
+    f2x pp = 0ull, pr = 0ull;
+    for (int c = tid; c < nch; c += kDecThreads) {
+        const uint4 q = __ldcs(xr + c);
+        const float* w0 = wh + 8 * c;               // w_hat_phi of the chunk's channels
+        const float* wq = wh + (D + 1) + 8 * c;     // w_hat_r (rows of D+1: scalar loads)
+        const f2x x0 = bf2x(q.x), x1 = bf2x(q.y), x2 = bf2x(q.z), x3 = bf2x(q.w);
+        pp = fma2(x0, pk2(w0[0], w0[1]), pp);
+        pp = fma2(x1, pk2(w0[2], w0[3]), pp);
+        pp = fma2(x2, pk2(w0[4], w0[5]), pp);
+        pp = fma2(x3, pk2(w0[6], w0[7]), pp);
+        pr = fma2(x0, pk2(wq[0], wq[1]), pr);
+        pr = fma2(x1, pk2(wq[2], wq[3]), pr);
+        pr = fma2(x2, pk2(wq[4], wq[5]), pr);
+        pr = fma2(x3, pk2(wq[6], wq[7]), pr);
+    }
+    float a0, a1, b0, b1;
+    up2(pp, a0, a1);
+    up2(pr, b0, b1);
+    float sp = a0 + a1, sr = b0 + b1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+        sr += __shfl_xor_sync(0xffffffffu, sr, o);
+    }
+    if (lane == 0) s_red[warp] = make_float2(sp, sr);
+    __syncthreads();
+    if (tid == 0) {
+        float tp = wh[D], tr = wh[(D + 1) + D];   // the appended constant 1 times the bias weight
+        for (int w = 0; w < kDecWarps; ++w) {
+            tp += s_red[w].x;
+            tr += s_red[w].y;
+        }
+        const float p = tanhf(tp), r = tanhf(tr);
+        const float d = misc[0] * p, c = misc[1] * (r / (1.0f + r * r));
+        float sn, cs;
+        sincosf(d, &sn, &cs);
+        const float rs = (a.reset != nullptr && a.reset[b] != 0) ? 1.0f : 0.0f;
+        s_ctl = make_float4(expm1f(c), cs, sn, rs);
+    }
+    __syncthreads();
+    const float4 ctl = s_ctl;
+    Ctl2 ct;
+    ct.e = dup2(ctl.x);
+    ct.c = dup2(ctl.y);
+    ct.s = dup2(ctl.z);
+    const bool reset = ctl.w != 0.f;
+
+    // modes: thread t owns the pairs (2t, 2t+1), (2t + 2*256, ...)
+    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(a.w) + b * (size_t)(D / 2);
+    uint32_t* yrow = reinterpret_cast<uint32_t*>(a.y) + b * (size_t)(D / 2);
+    for (int m = 2 * tid; m < M; m += 2 * kDecThreads) {
+        const float4 z4 = *reinterpret_cast<const float4*>(a.state_in + (b * M + m) * 2);   // re0, im0, re1, im1
+        const uint32_t wre = wrow[m / 2], wim = wrow[(M + m) / 2];
+        const f2x bre = bf2x(wre), bim = bf2x(wim);
+        c2x z;
+        if (reset) {
+            z.re = bre;
+            z.im = bim;
+        } else {
+            const ModePair k = load_modes(modes, nu, m);
+            float n0, n1;
+            up2(k.nu, n0, n1);
+            const float em = fabsf(ctl.x);
+            const Lam2 l = (fabsf(n0) * em < kPolyBound && fabsf(n1) * em < kPolyBound) ? samu_lambda2<true>(k, ct)
+                                                                                      : samu_lambda2<false>(k, ct);
+            const f2x zr = pk2(z4.x, z4.z), zi = pk2(z4.y, z4.w);
+            z.re = fma2(l.re, zr, fma2(l.nim, zi, bre));
+            z.im = fma2(l.re, zi, fma2(l.im, zr, bim));
+        }
+        float r0, r1, i0, i1;
+        up2(z.re, r0, r1);
+        up2(z.im, i0, i1);
+        *reinterpret_cast<float4*>(a.state_out + (b * M + m) * 2) = make_float4(r0, i0, r1, i1);
+        yrow[m / 2] = x2bf(z.re);
+        yrow[(M + m) / 2] = x2bf(z.im);
+        if (a.y32 != nullptr) {
+            float* y32 = a.y32 + b * (size_t)D;
+            *reinterpret_cast<float2*>(y32 + m) = make_float2(r0, r1);
+            *reinterpret_cast<float2*>(y32 + M + m) = make_float2(i0, i1);
+        }
+    }
+}
+
+cudaError_t launch_samu_decode_prepare(const SamuDecodePrepArgs& args, cudaStream_t s) {
+    const int M = args.D / 2;
+    const unsigned blocks = 1 + (unsigned)((M + kDecThreads - 1) / kDecThreads);
+    samu_decode_prepare_kernel<<<blocks, kDecThreads, 0, s>>>(args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t s) {
+    samu_decode_step_kernel<<<(unsigned)args.B, kDecThreads, 0, s>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace lrs

@@ -120,6 +120,19 @@ def samu_forward(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r):
     return {"y": y, "hT": hT, "ctrl": ctrl}
 
 
+def samu_decode_step(x_sel, w, state, reset, nu, theta, w_phi, w_r, a_phi, a_r):
+    """One token of each of B sequences: the forward definition ([SAMU page]
+    section 05) over a single token with the carried state as z_{t-1}.
+
+    x_sel, w: [B,D]; state: [B,M,2]; reset: [B] or None.  Returns dict(y=[B,D],
+    state=[B,M,2], ctrl=[B,5]).  Token after token it reproduces samu_forward
+    over the sequence (pinned in tests/test_oracle_pins.py)."""
+    x_sel, w = _f64(x_sel), _f64(w)
+    rs = None if reset is None else np.asarray(reset).reshape(-1, 1)
+    f = samu_forward(x_sel[:, None, :], w[:, None, :], state, rs, nu, theta, w_phi, w_r, a_phi, a_r)
+    return {"y": f["y"][:, 0, :], "state": f["hT"], "ctrl": f["ctrl"][:, 0, :]}
+
+
 def samu_backward(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r, dy, dhT):
     """SAMU mixer backward (hand-derived adjoint).  dhT may be None (zero).
 

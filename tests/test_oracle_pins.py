@@ -473,3 +473,38 @@ def test_rglru_sqrt_derivative_is_bounded():
     inp["la"][:] = -40.0          # sigmoid ~ 4e-18 -> a ~ 1 - 1e-19 -> u ~ 0
     g = oracle.rglru_backward(**inp, dy=np.ones((B, L, D)), dhT=None)
     assert np.all(np.isfinite(g["dla"])) and np.all(np.isfinite(g["dalpha"]))
+
+
+# ---------------------------------------------------------------------------
+# Decode step (one token of each sequence, carried state)
+# ---------------------------------------------------------------------------
+
+def test_decode_step_token_by_token_equals_forward():
+    """The decode step applied token after token reproduces the forward over
+    the sequence exactly (the same FP64 operations in the same order)."""
+    B, L, D = 3, 17, 12
+    inp = _samu_rand(B, L, D, seed=21, reset_p=0.1)
+    ref = oracle.samu_forward(**inp)
+    state = inp["h0"].copy()
+    common = {k: inp[k] for k in ("nu", "theta", "w_phi", "w_r", "a_phi", "a_r")}
+    for t in range(L):
+        out = oracle.samu_decode_step(inp["x_sel"][:, t], inp["w"][:, t], state, inp["reset"][:, t], **common)
+        np.testing.assert_array_equal(out["y"], ref["y"][:, t])
+        np.testing.assert_array_equal(out["ctrl"], ref["ctrl"][:, t])
+        state = out["state"]
+    np.testing.assert_array_equal(state, ref["hT"])
+
+
+def test_decode_step_zero_amplitudes_closed_form():
+    """With a_phi = a_r = 0 the controller drops out (d = c = 0, E = 1): one
+    step is z <- e^{-nu} e^{i theta} z + b, written out with numpy complex."""
+    B, D = 4, 10
+    M = D // 2
+    inp = _samu_rand(B, 1, D, seed=22, amps=False)
+    state = inp["h0"]
+    out = oracle.samu_decode_step(inp["x_sel"][:, 0], inp["w"][:, 0], state, None,
+                                  **{k: inp[k] for k in ("nu", "theta", "w_phi", "w_r", "a_phi", "a_r")})
+    lam = np.exp(-inp["nu"]) * np.exp(1j * inp["theta"])
+    z = lam[None, :] * (state[..., 0] + 1j * state[..., 1]) + _cplx(inp["w"][:, 0], M)
+    np.testing.assert_allclose(_cplx(out["y"], M), z, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(out["state"][..., 0] + 1j * out["state"][..., 1], z, rtol=1e-13, atol=1e-13)

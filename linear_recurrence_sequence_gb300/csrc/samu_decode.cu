@@ -24,13 +24,15 @@ namespace lrs {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kDecPairs = 4;   // mode pairs per thread: M <= 2 * kDecThreads * kDecPairs = 2048 (D <= 4096)
 
 // Parameter block (floats from the start of the caller's buffer):
-//   wh  [2][D+1]   unit directions w_hat_phi, w_hat_r
+//   w_hat_phi [D+1], w_hat_r [D+1], each starting on a 16-byte boundary
 //   misc[8]        k_phi, k_r, (unused)
 //   nu  [M]
 //   modes [M] float4 lbar hi/lo (16-byte aligned)
-__host__ __device__ inline size_t dec_off_misc(int D) { return (size_t)2 * (D + 1); }
+__host__ __device__ inline size_t dec_row(int D) { return (size_t)(D + 1 + 3) & ~size_t(3); }
+__host__ __device__ inline size_t dec_off_misc(int D) { return 2 * dec_row(D); }
 __host__ __device__ inline size_t dec_off_nu(int D) { return dec_off_misc(D) + 8; }
 __host__ __device__ inline size_t dec_off_modes(int D) { return (dec_off_nu(D) + D / 2 + 3) & ~size_t(3); }
 size_t samu_decode_params_floats(int D) { return dec_off_modes(D) + (size_t)4 * (D / 2); }
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_prepare_kernel(SamuDe
     const float inv_phi = 1.0f / sqrtf(tp), inv_r = 1.0f / sqrtf(tr);
     for (int j = tid; j < n; j += kDecThreads) {
         wh[j] = a.w_phi[j] * inv_phi;
-        wh[n + j] = a.w_r[j] * inv_r;
+        wh[dec_row(D) + j] = a.w_r[j] * inv_r;
     }
     if (tid == 0) {
         const float ism = 1.0f / sqrtf((float)M);
@@ -98,22 +100,39 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
     const float* nu = a.params + dec_off_nu(D);
     const float4* modes = reinterpret_cast<const float4*>(a.params + dec_off_modes(D));
 
+    // this thread's mode pairs (2t, 2t+1), (2t + 512, ...): state and w go out
+    // first, independent of the token's controls
+    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(a.w) + b * (size_t)(D / 2);
+    uint32_t* yrow = reinterpret_cast<uint32_t*>(a.y) + b * (size_t)(D / 2);
+    float4 zs[kDecPairs];
+    uint32_t wre[kDecPairs], wim[kDecPairs];
+#pragma unroll
+    for (int j = 0; j < kDecPairs; ++j) {
+        const int m = 2 * tid + j * 2 * kDecThreads;
+        if (m < M) {
+            zs[j] = __ldcs(reinterpret_cast<const float4*>(a.state_in + (b * M + m) * 2));   // re0, im0, re1, im1
+            wre[j] = __ldcs(wrow + m / 2);
+            wim[j] = __ldcs(wrow + (M + m) / 2);
+        }
+    }
+
     // controller: x~ . w_hat for both directions
     const uint4* xr = reinterpret_cast<const uint4*>(a.x) + b * nch;
     f2x pp = 0ull, pr = 0ull;
     for (int c = tid; c < nch; c += kDecThreads) {
         const uint4 q = __ldcs(xr + c);
-        const float* w0 = wh + 8 * c;               // w_hat_phi of the chunk's channels
-        const float* wq = wh + (D + 1) + 8 * c;     // w_hat_r (rows of D+1: scalar loads)
+        const float4* w0 = reinterpret_cast<const float4*>(wh + 8 * c);                 // w_hat_phi of the chunk
+        const float4* wq = reinterpret_cast<const float4*>(wh + dec_row(D) + 8 * c);    // w_hat_r
+        const float4 p0 = w0[0], p1 = w0[1], r0 = wq[0], r1 = wq[1];
         const f2x x0 = bf2x(q.x), x1 = bf2x(q.y), x2 = bf2x(q.z), x3 = bf2x(q.w);
-        pp = fma2(x0, pk2(w0[0], w0[1]), pp);
-        pp = fma2(x1, pk2(w0[2], w0[3]), pp);
-        pp = fma2(x2, pk2(w0[4], w0[5]), pp);
-        pp = fma2(x3, pk2(w0[6], w0[7]), pp);
-        pr = fma2(x0, pk2(wq[0], wq[1]), pr);
-        pr = fma2(x1, pk2(wq[2], wq[3]), pr);
-        pr = fma2(x2, pk2(wq[4], wq[5]), pr);
-        pr = fma2(x3, pk2(wq[6], wq[7]), pr);
+        pp = fma2(x0, pk2(p0.x, p0.y), pp);
+        pp = fma2(x1, pk2(p0.z, p0.w), pp);
+        pp = fma2(x2, pk2(p1.x, p1.y), pp);
+        pp = fma2(x3, pk2(p1.z, p1.w), pp);
+        pr = fma2(x0, pk2(r0.x, r0.y), pr);
+        pr = fma2(x1, pk2(r0.z, r0.w), pr);
+        pr = fma2(x2, pk2(r1.x, r1.y), pr);
+        pr = fma2(x3, pk2(r1.z, r1.w), pr);
     }
     float a0, a1, b0, b1;
     up2(pp, a0, a1);
@@ -127,7 +146,7 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
     if (lane == 0) s_red[warp] = make_float2(sp, sr);
     __syncthreads();
     if (tid == 0) {
-        float tp = wh[D], tr = wh[(D + 1) + D];   // the appended constant 1 times the bias weight
+        float tp = wh[D], tr = wh[dec_row(D) + D];   // the appended constant 1 times the bias weight
         for (int w = 0; w < kDecWarps; ++w) {
             tp += s_red[w].x;
             tr += s_red[w].y;
@@ -147,13 +166,12 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
     ct.s = dup2(ctl.z);
     const bool reset = ctl.w != 0.f;
 
-    // modes: thread t owns the pairs (2t, 2t+1), (2t + 2*256, ...)
-    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(a.w) + b * (size_t)(D / 2);
-    uint32_t* yrow = reinterpret_cast<uint32_t*>(a.y) + b * (size_t)(D / 2);
-    for (int m = 2 * tid; m < M; m += 2 * kDecThreads) {
-        const float4 z4 = *reinterpret_cast<const float4*>(a.state_in + (b * M + m) * 2);   // re0, im0, re1, im1
-        const uint32_t wre = wrow[m / 2], wim = wrow[(M + m) / 2];
-        const f2x bre = bf2x(wre), bim = bf2x(wim);
+#pragma unroll
+    for (int j = 0; j < kDecPairs; ++j) {
+        const int m = 2 * tid + j * 2 * kDecThreads;
+        if (m >= M) continue;
+        const float4 z4 = zs[j];
+        const f2x bre = bf2x(wre[j]), bim = bf2x(wim[j]);
         c2x z;
         if (reset) {
             z.re = bre;

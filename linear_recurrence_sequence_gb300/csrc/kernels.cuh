@@ -241,6 +241,7 @@ struct SamuScanBwdArgs {
 struct CtrlGeom {
     int stage_tok;          // tokens per stage (16, or 8 when 16 rows exceed 72 KB)
     int ring;               // slots (2 to 8, as many as fit)
+    int chunks;             // 8-channel chunks per consumer lane (1, or 2 for D > 3584)
     int consumers;          // consumer warps
     int threads;            // 32 * (2 + consumers)
     int smem;               // dynamic shared memory bytes

@@ -29,7 +29,8 @@ namespace lrs {
 // ---------------------------------------------------------------------------
 constexpr int kCtrlRingMax = 8;                        // ring slots (at most)
 constexpr size_t kCtrlBwdSmemMax = 200 * 1024;          // leaves room for the reduction CTAs
-constexpr int kCtrlBwdMaxThreads = 32 * (2 + 16);       // D = 4096: 16 consumer warps + 2
+constexpr int kCtrlBwdMaxThreads = 32 * (2 + 14);       // 14 consumer warps + producer + reducer
+constexpr int kCtrlBwdNarrowVecs = 32 * 14;             // 8-channel chunks with one chunk per consumer lane
 
 struct CtrlSmem {
     uint8_t* ring;
@@ -310,22 +311,27 @@ __device__ __forceinline__ void ctrl_bwd_producer(const SamuCtrlBwdArgs& a, cons
 
 // Returns the thread's share of the partial row's projection on w_hat:
 // (sum_c w_hat_phi[c] dw_hat_phi[c], sum_c w_hat_r[c] dw_hat_r[c]) over its
-// eight channels.
-template <int N>
+// channels: CH chunks of eight, columns 32 cw + lane + 32 consumers j.
+template <int N, int CH>
 __device__ __forceinline__ float2 ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, const CtrlSmem& sm, long long s0,
                                                     long long s1, int cw, int lane, int cta) {
     const CtrlGeom& cg = a.cg;
     const int D = a.D;
     const int vecs = D / 8;
-    const int v_idx = 32 * cw + lane;
-    const bool col_ok = v_idx < vecs;
-    float wp[8], wr[8], accp[8], accr[8];
+    int v_idx[CH];
+    bool col_ok[CH];
+    float wp[CH][8], wr[CH][8], accp[CH][8], accr[CH][8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        wp[c] = col_ok ? a.wh[8 * v_idx + c] : 0.f;
-        wr[c] = col_ok ? a.wh[(D + 1) + 8 * v_idx + c] : 0.f;
-        accp[c] = 0.f;
-        accr[c] = 0.f;
+    for (int j = 0; j < CH; ++j) {
+        v_idx[j] = 32 * (cw + j * cg.consumers) + lane;
+        col_ok[j] = v_idx[j] < vecs;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            wp[j][c] = col_ok[j] ? a.wh[8 * v_idx[j] + c] : 0.f;
+            wr[j][c] = col_ok[j] ? a.wh[(D + 1) + 8 * v_idx[j] + c] : 0.f;
+            accp[j][c] = 0.f;
+            accr[j][c] = 0.f;
+        }
     }
     const float2* sc = reinterpret_cast<const float2*>(sm.xbuf);
     for (long long st = s0; st < s1; ++st) {
@@ -337,24 +343,26 @@ __device__ __forceinline__ float2 ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, co
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
             break;   // status set; the CTA still reaches its barriers
         }
-        if (col_ok) {
-            const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
-            const float2* scs = sc + (size_t)k * N;
+        const uint4* rows = reinterpret_cast<const uint4*>(sm.ring + (size_t)slot * N * 2 * D);
+        const float2* scs = sc + (size_t)k * N;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (!col_ok[j]) continue;
 #pragma unroll 4
             for (int i = 0; i < n; ++i) {
                 float x[8];
-                unpack8(rows[(size_t)i * vecs + v_idx], x);
+                unpack8(rows[(size_t)i * vecs + v_idx[j]], x);
                 const float2 s = scs[i];
                 float dx[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    dx[c] = fmaf(s.x, wp[c], s.y * wr[c]);
-                    accp[c] = fmaf(s.x, x[c], accp[c]);
-                    accr[c] = fmaf(s.y, x[c], accr[c]);
+                    dx[c] = fmaf(s.x, wp[j][c], s.y * wr[j][c]);
+                    accp[j][c] = fmaf(s.x, x[c], accp[j][c]);
+                    accr[j][c] = fmaf(s.y, x[c], accr[j][c]);
                 }
                 const long long t = t0 + i;
                 if (a.grad_fp32) {
-                    float4* o = reinterpret_cast<float4*>(a.dx) + (t * vecs + v_idx) * 2;
+                    float4* o = reinterpret_cast<float4*>(a.dx) + (t * vecs + v_idx[j]) * 2;
                     __stcs(o, make_float4(dx[0], dx[1], dx[2], dx[3]));
                     __stcs(o + 1, make_float4(dx[4], dx[5], dx[6], dx[7]));
                 } else {
@@ -363,26 +371,30 @@ __device__ __forceinline__ float2 ctrl_bwd_consumer(const SamuCtrlBwdArgs& a, co
                     o.y = f2_to_bf2(dx[2], dx[3]);
                     o.z = f2_to_bf2(dx[4], dx[5]);
                     o.w = f2_to_bf2(dx[6], dx[7]);
-                    __stcs(reinterpret_cast<uint4*>(a.dx) + t * vecs + v_idx, o);
+                    __stcs(reinterpret_cast<uint4*>(a.dx) + t * vecs + v_idx[j], o);
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
-    if (col_ok) {
-        const int ns = ctrl_half_stride(D);
-        float4* row = reinterpret_cast<float4*>(a.dwh_part + (size_t)cta * 2 * ns);
-        row[2 * v_idx] = make_float4(accp[0], accp[1], accp[2], accp[3]);
-        row[2 * v_idx + 1] = make_float4(accp[4], accp[5], accp[6], accp[7]);
-        row[ns / 4 + 2 * v_idx] = make_float4(accr[0], accr[1], accr[2], accr[3]);
-        row[ns / 4 + 2 * v_idx + 1] = make_float4(accr[4], accr[5], accr[6], accr[7]);
-    }
+    const int ns = ctrl_half_stride(D);
+    float4* row = reinterpret_cast<float4*>(a.dwh_part + (size_t)cta * 2 * ns);
     float2 d = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        d.x = fmaf(wp[c], accp[c], d.x);
-        d.y = fmaf(wr[c], accr[c], d.y);
+    for (int j = 0; j < CH; ++j) {
+        if (col_ok[j]) {
+            const int v = v_idx[j];
+            row[2 * v] = make_float4(accp[j][0], accp[j][1], accp[j][2], accp[j][3]);
+            row[2 * v + 1] = make_float4(accp[j][4], accp[j][5], accp[j][6], accp[j][7]);
+            row[ns / 4 + 2 * v] = make_float4(accr[j][0], accr[j][1], accr[j][2], accr[j][3]);
+            row[ns / 4 + 2 * v + 1] = make_float4(accr[j][4], accr[j][5], accr[j][6], accr[j][7]);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            d.x = fmaf(wp[j][c], accp[j][c], d.x);
+            d.y = fmaf(wr[j][c], accr[j][c], d.y);
+        }
     }
     return d;
 }
@@ -460,10 +472,8 @@ __device__ __forceinline__ float4 block_sum4(float4 v, float4* s_w) {
     return t;
 }
 
-__global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    __shared__ float4 s_red[kCtrlBwdMaxThreads / 32];
-    __shared__ float2 s_nm[32];
+template <int CH>
+__device__ __forceinline__ void ctrl_bwd_body(const SamuCtrlBwdArgs& a, uint8_t* smem_raw, float4* s_red, float2* s_nm) {
     pdl_trigger();
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -536,8 +546,8 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     } else if (warp == 1) {
         ctrl_bwd_modes(a, cta, lane, s_nm);
     } else {
-        const float2 d = cg.stage_tok == 16 ? ctrl_bwd_consumer<16>(a, sm, s0, s1, warp - 2, lane, cta)
-                                            : ctrl_bwd_consumer<8>(a, sm, s0, s1, warp - 2, lane, cta);
+        const float2 d = cg.stage_tok == 16 ? ctrl_bwd_consumer<16, CH>(a, sm, s0, s1, warp - 2, lane, cta)
+                                            : ctrl_bwd_consumer<8, CH>(a, sm, s0, s1, warp - 2, lane, cta);
         dv.x = d.x;
         dv.y = d.y;
     }
@@ -545,6 +555,25 @@ __global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
     // the parameter reduction (sum_r w_hat . row_r = w_hat . dw_hat)
     const float4 dt = block_sum4(dv, s_red);
     if (tid == 0) a.dot_part[cta] = make_float2(dt.x, dt.y);
+}
+
+// One chunk of eight channels per consumer lane (D <= 3584: at most 14
+// consumer warps, 16 warps of 112 registers in all).
+__global__ void __maxnreg__(112) samu_ctrl_bwd_kernel(SamuCtrlBwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ float4 s_red[kCtrlBwdMaxThreads / 32];
+    __shared__ float2 s_nm[32];
+    ctrl_bwd_body<1>(a, smem_raw, s_red, s_nm);
+}
+
+// Two chunks per consumer lane for the widest rows (D up to 4096: 8 consumer
+// warps, 10 warps in all); the per-lane accumulators double, so the register
+// cap is higher (three warps of 168 registers per SM sub-partition).
+__global__ void __maxnreg__(168) samu_ctrl_bwd_wide_kernel(SamuCtrlBwdArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ float4 s_red[kCtrlBwdMaxThreads / 32];
+    __shared__ float2 s_nm[32];
+    ctrl_bwd_body<2>(a, smem_raw, s_red, s_nm);
 }
 
 // ---------------------------------------------------------------------------
@@ -707,7 +736,9 @@ CtrlGeom samu_ctrl_geom(long long BL, int D) {
     CtrlGeom cg;
     // stages of 16 tokens, or 8 when 16 rows exceed 72 KB
     cg.stage_tok = 16 * 2 * (size_t)D <= 72 * 1024 ? 16 : 8;
-    cg.consumers = (D / 8 + 31) / 32;
+    // one 8-channel chunk per consumer lane, two beyond 14 consumer warps
+    cg.chunks = D / 8 <= kCtrlBwdNarrowVecs ? 1 : 2;
+    cg.consumers = (D / 8 + 32 * cg.chunks - 1) / (32 * cg.chunks);
     if (cg.consumers < 1) cg.consumers = 1;
     cg.threads = 32 * (2 + cg.consumers);   // producer, reducer, consumers
     cg.n_stages = (BL + cg.stage_tok - 1) / cg.stage_tok;
@@ -756,10 +787,10 @@ cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool p
 }
 
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(samu_ctrl_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, args.cg.smem);
+    auto* fn = args.cg.chunks == 1 ? samu_ctrl_bwd_kernel : samu_ctrl_bwd_wide_kernel;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, args.cg.smem);
     if (e != cudaSuccess) return e;
-    return launch_ex(samu_ctrl_bwd_kernel, args.cg.n_ctas, args.cg.threads, (size_t)args.cg.smem, s, pdl, args);
+    return launch_ex(fn, args.cg.n_ctas, args.cg.threads, (size_t)args.cg.smem, s, pdl, args);
 }
 
 

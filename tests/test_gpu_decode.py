@@ -34,7 +34,7 @@ def _common(inp):
 
 
 @pytest.mark.parametrize("B,D,reset_p,seed", [(64, 256, 0.0, 31), (48, 64, 0.25, 32), (5, 400, 0.2, 33),
-                                              (3, 16, 0.0, 34)])
+                                              (3, 16, 0.0, 34), (7, 4096, 0.1, 37)])
 def test_decode_single_step(B, D, reset_p, seed, dev):
     import torch
     from linear_recurrence_sequence_gb300 import api

@@ -27,6 +27,8 @@ SMALL = {
     "one_tile_plus_one_L129_D96": dict(B=2, L=129, D=96, seed=20, h0=True, reset_p=0.02),
     "partial_group_B2_L300_D1552": dict(B=2, L=300, D=1552, seed=14, h0=True, reset_p=0.01),
     "many_chunks_B1_L5003_D32": dict(B=1, L=5003, D=32, seed=15, h0=True, reset_p=0.002),
+    "widest_B1_L300_D4096": dict(B=1, L=300, D=4096, seed=17, h0=True, reset_p=0.01),
+    "many_rows_B64_L40_D128": dict(B=64, L=40, D=128, seed=18, h0=True, reset_p=0.02),
 }
 
 

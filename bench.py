@@ -70,7 +70,15 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="time every workload family (one JSON line each) instead of the headline line")
     p.add_argument("--only", default=None, help="with --sweep: comma-separated workload names")
+    p.add_argument("--transition", choices=["closed_form", "chained"], default="closed_form",
+                   help="form of the SAMU maps kernels' 16-token item transitions")
     return p.parse_args(argv)
+
+
+def set_transition(args):
+    from linear_recurrence_sequence_gb300 import api
+    api.samu_set_chunk_transition(api.LRS_TRANSITION_CLOSED_FORM if args.transition == "closed_form"
+                                  else api.LRS_TRANSITION_CHAINED)
 
 
 def dist_env():
@@ -461,7 +469,7 @@ def run_ours(args, rank, world, local):
                    "h0": wl.h0, "reset_p": wl.reset_p, "seed": shard_seed(wl.seeds[0], rank),
                    "l2": "flushed before every timed step (256 MiB memset outside the step events)",
                    "launch": "the step (forward + backward through the C ABI) replayed as one CUDA graph",
-                   "per_gpu_batch": B},
+                   "per_gpu_batch": B, "item_transition": args.transition},
         "achieved_step_gbs": round(STEP_BYTES_PER_BLD * BLD / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": roofline,
         "kernels_avg_ms": {k: round(v, 5) for k, v in sorted(avg.items())},
@@ -485,7 +493,7 @@ def run_ours(args, rank, world, local):
 SWEEP_BYTES_PER_BLD = {"samu": 16.0, "rglru": 22.0}
 
 
-def sweep_one(name, dev, K, W):
+def sweep_one(name, dev, K, W, transition):
     import torch
     from linear_recurrence_sequence_gb300 import api, synth
     wl = synth.WORKLOADS[name]
@@ -565,6 +573,7 @@ def sweep_one(name, dev, K, W):
     alg = SWEEP_BYTES_PER_BLD[wl.kind] * BLD
     gbs = alg / (ms_mean / 1e3) / 1e9
     return {"workload": name, "kind": wl.kind, "B": B, "L": L, "D": D, "steps": K,
+            "item_transition": transition if wl.kind == "samu" else None,
             "ms_per_step": round(ms_mean, 5), "ms_min": round(ms[0], 5), "ms_max": round(ms[-1], 5),
             "Mtok_per_s": round(B * L / (ms_mean / 1e3) / 1e6, 3),
             "algorithmic_bytes": alg, "achieved_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
@@ -645,7 +654,7 @@ def run_sweep(args, local):
     W = max(3, args.warmup)
     names = args.only.split(",") if args.only else list(synth.WORKLOADS) + list(DECODE_WORKLOADS)
     for name in names:
-        line = sweep_decode(name, dev, K, W) if name in DECODE_WORKLOADS else sweep_one(name, dev, K, W)
+        line = sweep_decode(name, dev, K, W) if name in DECODE_WORKLOADS else sweep_one(name, dev, K, W, args.transition)
         print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
 
@@ -660,12 +669,14 @@ def main(argv=None):
         return 0
     if args.sweep:
         if rank == 0:
+            set_transition(args)
             run_sweep(args, local)
         return 0
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
     try:
+        set_transition(args)
         run_ours(args, rank, world, local)
     finally:
         if world > 1:

@@ -101,6 +101,24 @@ int lrs_profile_end(int* kernel_ids, float* ms, int capacity, int* count);
 /* SAMU mixer                                                                */
 /* ======================================================================== */
 
+/* How the SAMU maps kernels form the transition of a 16-token item.
+ * CHAINED multiplies the per-token transitions one by one.  CLOSED_FORM uses
+ * the item's two shared statistics instead ([SAMU page] section 05, "exact
+ * chunk closed form"): prod_t lambda_{t,m} = lbar_m^16 e^{-nu_m G} e^{i D},
+ * with G = sum_t (E_t - 1) and D = sum_t d_t over the item's tokens, and
+ * lbar_m^16 formed in FP64.  An item that holds a reset, or is cut short by
+ * the end of the sequence, is always chained.  Both give the same function
+ * within FP32 rounding.  The setting is process-wide.  It applies to the
+ * samu_forward / samu_backward calls made after it, including CUDA graphs
+ * captured after it (a captured graph keeps the form it was captured with).
+ * Not synchronised with calls running on other host threads.
+ * Errors: LRS_ERR_ARG for an unknown kind. */
+#define LRS_TRANSITION_CHAINED 0
+#define LRS_TRANSITION_CLOSED_FORM 1
+int samu_set_chunk_transition(int kind);
+/* The current setting (LRS_TRANSITION_CLOSED_FORM unless changed). */
+int samu_get_chunk_transition(void);
+
 /* Bytes of the caller-owned `saved` buffer (forward -> backward) and of the
  * `scratch` buffer for problems of shape (B, L, D).  Either output pointer may
  * be NULL.  Pure host function. */

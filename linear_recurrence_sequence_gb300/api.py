@@ -22,6 +22,8 @@ _lib = None
 
 LRS_GRAD_BF16 = 0
 LRS_GRAD_FP32 = 1
+LRS_TRANSITION_CHAINED = 0
+LRS_TRANSITION_CLOSED_FORM = 1
 
 # names and argument kinds of every exported symbol (checked by the tests)
 _P = ctypes.c_void_p
@@ -33,6 +35,8 @@ _SIGNATURES = {
     "lrs_device_status": ([_P, ctypes.POINTER(_I), _P], _I),
     "lrs_profile_begin": ([_I], _I),
     "lrs_profile_end": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
+    "samu_set_chunk_transition": ([_I], _I),
+    "samu_get_chunk_transition": ([], _I),
     "samu_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
     "samu_forward": ([_P] * 10 + [_I, _I, _I] + [_P] * 6, _I),
     "samu_backward": ([_P] * 12 + [_I, _I, _I] + [_P, _P, _P, _I] + [_P] * 9, _I),
@@ -225,6 +229,16 @@ def samu_forward_noalloc(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r,
                                       _ptr(y), _ptr(y32), _ptr(hT), _stream(dev))
     _check("samu_forward_noalloc", st)
     return {"y": y, "y32": y32, "hT": hT}
+
+
+def samu_set_chunk_transition(kind: int) -> None:
+    """Process-wide form of the SAMU maps kernels' item transitions
+    (LRS_TRANSITION_CHAINED or LRS_TRANSITION_CLOSED_FORM) for later calls."""
+    _check("samu_set_chunk_transition", _load().samu_set_chunk_transition(int(kind)))
+
+
+def samu_get_chunk_transition() -> int:
+    return int(_load().samu_get_chunk_transition())
 
 
 # ---------------------------------------------------------------------------

@@ -69,6 +69,9 @@ void prof_end(cudaStream_t s) {
 // on, so that every kernel's events bracket it alone.
 bool pdl_ok() { return !g_prof.on; }
 
+// samu_set_chunk_transition
+int g_transition = LRS_TRANSITION_CLOSED_FORM;
+
 // Kernel ids reported by lrs_profile_end.
 enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
@@ -110,6 +113,14 @@ const char* lrs_status_string(int status) {
 }
 
 int lrs_version(void) { return 100; }
+
+int samu_set_chunk_transition(int kind) {
+    if (kind != LRS_TRANSITION_CHAINED && kind != LRS_TRANSITION_CLOSED_FORM) return LRS_ERR_ARG;
+    g_transition = kind;
+    return LRS_OK;
+}
+
+int samu_get_chunk_transition(void) { return g_transition; }
 
 int lrs_profile_begin(int capacity) {
     if (capacity < 1) return LRS_ERR_ARG;
@@ -219,6 +230,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     a.g = g;
     a.modes = modes;
     a.nu = nu;
+    a.closed_form = g_transition == LRS_TRANSITION_CLOSED_FORM;
     a.h0 = h0;
     a.y = static_cast<uint32_t*>(y);
     a.y32 = y32;
@@ -270,6 +282,7 @@ int samu_backward(const void* dy, const float* dhT,
     s.g = g;
     s.modes = at<float4>(saved, sv.modes);
     s.nu = nu;
+    s.closed_form = g_transition == LRS_TRANSITION_CLOSED_FORM;
     s.dhT = dhT;
     s.hsub = at<float2>(saved, sv.hsub);
     s.dw = dw;

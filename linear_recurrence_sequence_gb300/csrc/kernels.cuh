@@ -106,6 +106,21 @@ __device__ __forceinline__ void mode_constants(const float* __restrict__ nu, con
     modes[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
 }
 
+// lbar_m^K = e^{-K nu_m} e^{i K theta_m}, formed in FP64 (K theta_m is exact
+// there, and the reduction of the phase, up to 2 pi K, is done in FP64 too) and
+// stored as the same double-float: the closed-form transition of K
+// consecutive tokens is lbar_m^K e^{-nu_m G} e^{i D} (G, D below).
+__device__ __forceinline__ void mode_power_constants(const float* __restrict__ nu, const float* __restrict__ theta,
+                                                     int M, int K, float4* __restrict__ out, int m) {
+    if (m >= M) return;
+    const double r = exp(-(double)K * (double)nu[m]);
+    double sn, cs;
+    sincos((double)K * (double)theta[m], &sn, &cs);
+    const double re = r * cs, im = r * sn;
+    const float hr = (float)re, hi = (float)im;
+    out[m] = make_float4(hr, hi, (float)(re - (double)hr), (float)(im - (double)hi));
+}
+
 __device__ __forceinline__ ModePair zero_modes() {
     ModePair k;
     k.hr = k.hi = k.nhi = k.lr = k.li = k.nu = 0ull;
@@ -114,7 +129,7 @@ __device__ __forceinline__ ModePair zero_modes() {
 
 // Per-token control word, written by the controller forward and staged into
 // shared memory by TMA, each value duplicated so that it loads as a pair:
-// {E-1, E-1, C, C}, {S, S, R, R} (two float4), R = -E for an ordinary token
+// {E-1, E-1, C, C}, {S, S, R, d} (two float4), R = -E for an ordinary token
 // and R = +0 at a segment start (lambda = 0); E = e^c > 0, so the sign tells
 // them apart.  It is the same for every lane, so the branches on it are
 // warp-uniform.
@@ -130,7 +145,7 @@ __device__ __forceinline__ Ctl2 load_ctl(const float4* sc, int i) {
     ct.e = pk2(a.x, a.y);
     ct.c = pk2(a.z, a.w);
     ct.s = pk2(b.x, b.y);
-    ct.ne = pk2(b.z, b.w);
+    ct.ne = pk2(b.z, b.z);
     ct.rflag = b.z;
     return ct;
 }
@@ -203,8 +218,9 @@ __device__ __forceinline__ c2x cfma2(const c2x& P, const c2x& bb, f2x nb_im, con
 // boxes); everything indexed by segment is [B][NS][M] (per mode).
 struct SamuScanFwdArgs {
     SegGeom g;
-    const float4* modes;    // [M] lbar hi/lo
+    const float4* modes;    // [2][M] lbar, lbar^16 (hi/lo)
     const float* nu;
+    int closed_form;        // full items without a reset: closed-form transition
     const float* h0;        // [B,M,2] or null
     uint32_t* y;            // BF16 pairs of y
     float* y32;             // optional
@@ -220,8 +236,9 @@ struct SamuScanFwdArgs {
 // token from later tokens.
 struct SamuScanBwdArgs {
     SegGeom g;
-    const float4* modes;
+    const float4* modes;    // [2][M] lbar, lbar^16 (hi/lo)
     const float* nu;
+    int closed_form;        // full items without a reset: closed-form transition
     const float* dhT;       // [B,M,2] or null
     const float2* hsub;     // [B][CS][M] (the forward's sub-chunk entry states)
     void* dw;               // BF16 pairs or FP32
@@ -302,10 +319,10 @@ struct SamuCtrlFwdArgs {
     const float* theta;
     float* p;
     float* r;
-    float4* ctrl;                  // [B*L][2] {E-1, E-1, C, C}, {S, S, R, R}
+    float4* ctrl;                  // [B*L][2] {E-1, E-1, C, C}, {S, S, R, d}
     float* wh;                     // [2][D+1]
     float* misc;
-    float4* modes;                 // [M] lbar hi/lo
+    float4* modes;                 // [2][M] lbar, lbar^16 hi/lo
     uint32_t* status;
 };
 

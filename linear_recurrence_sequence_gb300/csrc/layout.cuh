@@ -138,11 +138,11 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
     size_t o = 0;
     s.p = o;      o = align_up(o + BL * 4);                          // p_t
     s.r = o;      o = align_up(o + BL * 4);                          // r_t
-    s.ctrl = o;   o = align_up(o + BL * 32);                         // {E-1, E-1, C, C}, {S, S, R, R}, R = -E or +0 at a reset
+    s.ctrl = o;   o = align_up(o + BL * 32);                         // {E-1, E-1, C, C}, {S, S, R, d}, R = -E or +0 at a reset
     s.hsub = o;   o = align_up(o + (size_t)B * g.CS * M * 8);        // state every 8 tokens
     s.wh = o;     o = align_up(o + (size_t)2 * (D + 1) * 4);         // unit directions
     s.misc = o;   o = align_up(o + kMiscFloats * 4);
-    s.modes = o;  o = align_up(o + (size_t)M * 16);                  // lbar hi/lo per mode
+    s.modes = o;  o = align_up(o + (size_t)M * 32);                  // [2][M]: lbar, then lbar^16, hi/lo per mode
     s.total = o;
     return s;
 }

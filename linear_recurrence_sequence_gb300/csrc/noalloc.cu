@@ -113,6 +113,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     a.g = samu_scan_geom(B, L, M, false);
     a.modes = modes;
     a.nu = nu;
+    a.closed_form = samu_get_chunk_transition() == LRS_TRANSITION_CLOSED_FORM;
     a.h0 = h0;
     a.y = static_cast<uint32_t*>(y);
     a.y32 = y32;

@@ -140,10 +140,10 @@ __device__ __forceinline__ void ctrl_fwd_token(const SamuCtrlFwdArgs& a, long lo
     a.p[t] = p;
     a.r[t] = r;
     const float em1 = expm1f(c);
-    // R = -E, or +0 at a reset
+    // R = -E, or +0 at a reset; d for the closed-form item transitions
     const float rw = (a.reset != nullptr && a.reset[t] != 0) ? 0.0f : -(1.0f + em1);
     a.ctrl[2 * t] = make_float4(em1, em1, cs, cs);
-    a.ctrl[2 * t + 1] = make_float4(sn, sn, rw, rw);
+    a.ctrl[2 * t + 1] = make_float4(sn, sn, rw, d);
 }
 
 __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
         for (long long mw = gw - first; gw >= first && mw < nmw; mw += W - first) {
             const int m = (int)mw * 32 + lane;
             mode_constants(a.nu, a.theta, M, a.modes, m);
+            mode_power_constants(a.nu, a.theta, M, kMapRows, a.modes + M, m);
         }
     }
 

@@ -263,6 +263,94 @@ __device__ __forceinline__ void fwd_maps_sub(const float4* sc, const uint32_t* w
     }
 }
 
+// ---------------------------------------------------------------------------
+// Closed-form item transitions (SAMU GPU page, section 05, "exact chunk closed
+// form"): over tokens without a reset the product of the transitions is
+//   prod_t lambda_{t,m} = lbar_m^K e^{-nu_m G} e^{i D},
+//   G = sum_t (E_t - 1),  D = sum_t d_t,
+// two statistics per item shared by all modes.  lbar_m^K is the FP64-formed
+// double-float of mode_power_constants (the phase K theta_m is never rounded
+// to FP32), so the product is one rounding away from exact instead of K.
+// An item's map is then its affine part by Horner's rule (four paired FMAs
+// per token, against eight for the running product and the affine part)
+// and this product, composed with the maps of the other items as before.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ c2x cmulx(const c2x& a, const c2x& b) {   // a b
+    c2x r;
+    r.re = fma2(a.re, b.re, mul2(sub2(0ull, a.im), b.im));
+    r.im = fma2(a.re, b.im, mul2(a.im, b.re));
+    return r;
+}
+
+// The transition of one full item of N tokens, none a reset, for the lane's
+// two modes (zero for an inactive lane).  G and D are summed over the item's
+// tokens by a fixed xor tree within each half-warp (both halves hold the
+// same tokens, so every lane gets the same bits).
+template <int N>
+__device__ __forceinline__ c2x item_transition(const float4* sc, const float4* __restrict__ modes_n,
+                                               const ModePair& k, int m, bool active, int lane) {
+    static_assert(N <= 16 && (N & (N - 1)) == 0, "an item fits a half-warp");
+    const int j = lane & (N - 1);
+    float G = sc[2 * j].x, Dsum = sc[2 * j + 1].w;
+#pragma unroll
+    for (int o = N / 2; o > 0; o >>= 1) {
+        G += __shfl_xor_sync(0xffffffffu, G, o);
+        Dsum += __shfl_xor_sync(0xffffffffu, Dsum, o);
+    }
+    float sn, cs;
+    sincosf(Dsum, &sn, &cs);
+    float n0, n1;
+    up2(k.nu, n0, n1);
+    const float x0 = n0 * G, x1 = n1 * G;   // nu G
+    f2x q;                                   // e^{-nu G}
+    if (fabsf(x0) < kPolyBound && fabsf(x1) < kPolyBound) {
+        const f2x x = pk2(x0, x1);
+        q = fma2(x, fma2(x, fma2(x, dup2(-1.0f / 6.0f), dup2(0.5f)), dup2(-1.0f)), dup2(1.0f));
+    } else {
+        q = pk2(ex2_approx(__fmul_rn(-x0, kLog2e)), ex2_approx(__fmul_rn(-x1, kLog2e)));
+    }
+    const f2x dr = mul2(q, dup2(cs)), di = mul2(q, dup2(sn));
+    float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+    if (active) {
+        v0 = modes_n[m];
+        v1 = modes_n[m + 1];
+    }
+    const f2x hr = pk2(v0.x, v1.x), hi = pk2(v0.y, v1.y), lr = pk2(v0.z, v1.z), li = pk2(v0.w, v1.w);
+    // (hi + lo)(dr + i di), the lo products added first
+    c2x L;
+    L.re = fma2(hr, dr, fma2(sub2(0ull, hi), di, fma2(lr, dr, mul2(sub2(0ull, li), di))));
+    L.im = fma2(hr, di, fma2(hi, dr, fma2(lr, di, mul2(li, dr))));
+    return L;
+}
+
+// A full item of the forward maps (N tokens, none a reset), appended to the
+// map H = (P, beta) of the tokens after it: H o T_item = (P L, P h + beta),
+// h = lambda_{N-1}(... (lambda_1 b_0 + b_1) ...) + b_{N-1}.
+template <int N, bool FAST>
+__device__ __forceinline__ void fwd_maps_item_cf(const float4* sc, const uint32_t* wre, const uint32_t* wim,
+                                                 const ModePair& k, const float4* __restrict__ modes_n, int m,
+                                                 bool active, int lane, c2x& P, c2x& be) {
+    c2x h;
+    h.re = bf2x(wre[0]);
+    h.im = bf2x(wim[0]);
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+        const Ctl2 ct = load_ctl(sc, i);
+        const f2x bre = bf2x(wre[i * kWords]);
+        const f2x bim = bf2x(wim[i * kWords]);
+        const Lam2 l = samu_lambda2<FAST>(k, ct);
+        const f2x hr = fma2(l.re, h.re, fma2(l.nim, h.im, bre));
+        const f2x hi = fma2(l.re, h.im, fma2(l.im, h.re, bim));
+        h.re = hr;
+        h.im = hi;
+    }
+    const c2x L = item_transition<N>(sc, modes_n, k, m, active, lane);
+    const c2x Ph = cmulx(P, h);
+    be.re = add2(be.re, Ph.re);
+    be.im = add2(be.im, Ph.im);
+    P = cmulx(P, L);
+}
+
 // hs: the item's first state checkpoint (the state entering its first
 // token); the states entering its tokens 8, 16, ... go to the following
 // checkpoints (the backward restarts there); written by active lanes only.
@@ -433,7 +521,14 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
         const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
-        LRS_SUB_DISPATCH_N(kd, fwd_maps_sub, kN, sc, wre, wim, nsub, k, P, be);
+        if (a.closed_form && kd.simple) {
+            if (kd.fast)
+                fwd_maps_item_cf<kN, true>(sc, wre, wim, k, a.modes + M, m, active, lane, P, be);
+            else
+                fwd_maps_item_cf<kN, false>(sc, wre, wim, k, a.modes + M, m, active, lane, P, be);
+        } else {
+            LRS_SUB_DISPATCH_N(kd, fwd_maps_sub, kN, sc, wre, wim, nsub, k, P, be);
+        }
         __syncwarp();
         if (lane == 0 && it + kRing < T.nsc)
             ring_issue(R, slot, &tm_w, &tm_ctrl, x_re, x_im, T.t_begin + (T.nsc - 1 - it - kRing) * kN, T.b);
@@ -579,6 +674,36 @@ __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* g
     }
 }
 
+// A full item of the adjoint maps (N tokens, none a reset), appended to the
+// map G = (Q, beta) of the tokens before it: G o F_item = (Q conj(L), beta + Q x),
+// x = conj(lambda_0) y_0 with y_{N-1} = g_{N-1} and
+// y_i = g_i + conj(lambda_{i+1}) y_{i+1} (four paired FMAs per token).
+template <int N, bool FAST>
+__device__ __forceinline__ void bwd_maps_item_cf(const float4* sc, const uint32_t* gre, const uint32_t* gim,
+                                                 const ModePair& k, const float4* __restrict__ modes_n, int m,
+                                                 bool active, int lane, c2x& Q, c2x& be) {
+    c2x y;
+    y.re = bf2x(gre[(N - 1) * kWords]);
+    y.im = bf2x(gim[(N - 1) * kWords]);
+#pragma unroll
+    for (int i = N - 1; i > 0; --i) {
+        const Lam2 l = samu_lambda2<FAST>(k, load_ctl(sc, i));
+        const f2x gr = bf2x(gre[(i - 1) * kWords]);
+        const f2x gi = bf2x(gim[(i - 1) * kWords]);
+        const f2x yr = fma2(l.re, y.re, fma2(l.im, y.im, gr));
+        const f2x yi = fma2(l.re, y.im, fma2(l.nim, y.re, gi));
+        y.re = yr;
+        y.im = yi;
+    }
+    const c2x x = cmulc2(samu_lambda2<FAST>(k, load_ctl(sc, 0)), y);
+    c2x L = item_transition<N>(sc, modes_n, k, m, active, lane);
+    L.im = sub2(0ull, L.im);   // conj
+    const c2x Qx = cmulx(Q, x);
+    be.re = add2(be.re, Qx.re);
+    be.im = add2(be.im, Qx.im);
+    Q = cmulx(Q, L);
+}
+
 // The adjoint arriving at the last token of CTA cc of a chain,
 // C_{cc+1} o ... o C_{n-1} (dhT), formed like cta_entry_fwd over the later
 // CTAs [cc+1, n): warp w composes its range from the latest map down.
@@ -661,7 +786,14 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         const uint32_t* gre = &R.box[slot][0][0][lane];
         const uint32_t* gim = &R.box[slot][1][0][lane];
         const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
-        LRS_SUB_DISPATCH_N(kd, bwd_maps_sub, kN, sc, gre, gim, nsub, k, Q, be);
+        if (a.closed_form && kd.simple) {
+            if (kd.fast)
+                bwd_maps_item_cf<kN, true>(sc, gre, gim, k, a.modes + M, m, active, lane, Q, be);
+            else
+                bwd_maps_item_cf<kN, false>(sc, gre, gim, k, a.modes + M, m, active, lane, Q, be);
+        } else {
+            LRS_SUB_DISPATCH_N(kd, bwd_maps_sub, kN, sc, gre, gim, nsub, k, Q, be);
+        }
         __syncwarp();
         if (lane == 0 && it + kRing < T.nsc)
             ring_issue(R, slot, &tm_dy, &tm_ctrl, x_re, x_im, T.t_begin + (it + kRing) * kN, T.b);

@@ -133,6 +133,22 @@ def samu_decode_step(x_sel, w, state, reset, nu, theta, w_phi, w_r, a_phi, a_r):
     return {"y": f["y"][:, 0, :], "state": f["hT"], "ctrl": f["ctrl"][:, 0, :]}
 
 
+def samu_chunk_transition(nu, theta, E, d, reset=None):
+    """Transition of a chunk of K consecutive tokens, P_m = prod_t lambda_{t,m},
+    by the closed form of the SAMU GPU page (section 05, exact chunk closed
+    form): P_m = e^{-nu_m G} e^{i (K theta_m + D)} with G = sum_t E_t and
+    D = sum_t d_t; zero when a token of the chunk is a reset (lambda = 0 there).
+
+    nu, theta: [M]; E, d: [K] (the chunk's per-token controls); reset: [K] or
+    None.  FP64 numpy; returns complex [M]."""
+    nu, theta = np.asarray(nu, np.float64), np.asarray(theta, np.float64)
+    E, d = np.asarray(E, np.float64), np.asarray(d, np.float64)
+    if reset is not None and np.any(np.asarray(reset) != 0):
+        return np.zeros(nu.shape, np.complex128)
+    K = E.shape[0]
+    return np.exp(-nu * E.sum()) * np.exp(1j * (K * theta + d.sum()))
+
+
 def samu_backward(x_sel, w, h0, reset, nu, theta, w_phi, w_r, a_phi, a_r, dy, dhT):
     """SAMU mixer backward (hand-derived adjoint).  dhT may be None (zero).
 

@@ -124,3 +124,14 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(api, "_HERE", str(tmp_path))
     with pytest.raises(RuntimeError, match="not built"):
         api._load()
+
+
+def test_chunk_transition_setting(lib):
+    """Host-only: the process-wide item-transition form (closed form by default)."""
+    assert lib.samu_get_chunk_transition() == 1
+    assert lib.samu_set_chunk_transition(0) == 0
+    assert lib.samu_get_chunk_transition() == 0
+    assert lib.samu_set_chunk_transition(7) == 1          # LRS_ERR_ARG, setting unchanged
+    assert lib.samu_get_chunk_transition() == 0
+    assert lib.samu_set_chunk_transition(1) == 0
+    assert lib.samu_get_chunk_transition() == 1

@@ -94,6 +94,47 @@ def test_samu_run_to_run_bitwise(dev):
         assert torch.equal(b1[k], b2[k]), k
 
 
+@pytest.fixture
+def chained():
+    """Item transitions by the running product instead of the closed form."""
+    from linear_recurrence_sequence_gb300 import api
+    api.samu_set_chunk_transition(api.LRS_TRANSITION_CHAINED)
+    yield
+    api.samu_set_chunk_transition(api.LRS_TRANSITION_CLOSED_FORM)
+
+
+@pytest.mark.parametrize("name", ["tiny_B2_L2048_D256", "ragged_B3_L77_D64", "partial_group_B2_L300_D1552",
+                                  "many_chunks_B1_L5003_D32"])
+def test_samu_chained_item_transitions(name, dev, chained):
+    from linear_recurrence_sequence_gb300 import api
+    assert api.samu_get_chunk_transition() == api.LRS_TRANSITION_CHAINED
+    inp = _case(**SMALL[name])
+    ref_f, ref_b = run_samu_oracle(inp)
+    fwd, bwd = run_samu_gpu(inp, dev, grad_fp32=True)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, grad_fp32=True, label=f"chained/{name}")
+
+
+@pytest.mark.parametrize("form", ["closed_form", "chained"])
+def test_samu_long_memory_modes(form, dev):
+    """Modes that remember thousands of tokens (|lbar| up to 1 - 1e-4) and phases
+    spread over [0, 2 pi): the item transitions' rounding accumulates over the
+    longest chains here, in either form."""
+    from linear_recurrence_sequence_gb300 import api
+    inp = _case(B=1, L=8192, D=512, seed=23, h0=True)
+    r = np.random.default_rng(123)
+    M = 256
+    inp["nu"] = (-np.log(r.uniform(0.999, 0.9999, M))).astype(np.float32)
+    inp["theta"] = r.uniform(0, 2 * np.pi, M).astype(np.float32)
+    kind = api.LRS_TRANSITION_CLOSED_FORM if form == "closed_form" else api.LRS_TRANSITION_CHAINED
+    api.samu_set_chunk_transition(kind)
+    try:
+        ref_f, ref_b = run_samu_oracle(inp)
+        fwd, bwd = run_samu_gpu(inp, dev, grad_fp32=True)
+    finally:
+        api.samu_set_chunk_transition(api.LRS_TRANSITION_CLOSED_FORM)
+    check_samu(inp, fwd, bwd, ref_f, ref_b, grad_fp32=True, label=f"long_memory/{form}")
+
+
 WORKLOADS = ["short", "length_8k", "length_32k", "length_64k", "length_128k",
              "width_1024", "width_1536", "width_2048", "width_2560", "medium_8k_2560"]
 

@@ -20,7 +20,9 @@ fails at least one of them:
   * the algebra of the affine composition (associativity, chunked and grouped
     prefix compositions equal the step recurrence);
   * central finite differences of the forward for every input and parameter;
-  * the pages' printed parameter counts.
+  * the pages' printed parameter counts;
+  * the chunk closed form (section 05) against the forward's own state
+    transition over a chunk with zero writes.
 """
 import math
 import os
@@ -508,3 +510,63 @@ def test_decode_step_zero_amplitudes_closed_form():
     z = lam[None, :] * (state[..., 0] + 1j * state[..., 1]) + _cplx(inp["w"][:, 0], M)
     np.testing.assert_allclose(_cplx(out["y"], M), z, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(out["state"][..., 0] + 1j * out["state"][..., 1], z, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Closed-form chunk transition (SAMU GPU page, section 05, exact chunk closed form)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,seed", [(1, 30), (16, 31), (32, 32), (61, 33)])
+def test_chunk_closed_form_equals_forward_transition(K, seed):
+    """With zero writes and h0 = 1 in every mode, the forward's final state over
+    K tokens is the product of the K transitions; the closed form built from
+    the controller's own E_t and d_t = tanh(a_phi) p_t / sqrt(M) must equal it."""
+    D = 14
+    M = D // 2
+    inp = _samu_rand(1, K, D, seed=seed)
+    inp["w"] = np.zeros_like(inp["w"])
+    h0 = np.zeros((1, M, 2))
+    h0[..., 0] = 1.0
+    inp["h0"] = h0
+    ref = oracle.samu_forward(**inp)
+    ctrl = ref["ctrl"][0]
+    E = ctrl[:, 2]
+    d = math.tanh(inp["a_phi"]) / math.sqrt(M) * ctrl[:, 0]
+    np.testing.assert_allclose(np.arctan2(ctrl[:, 4], ctrl[:, 3]), d, rtol=0, atol=1e-15)   # S, C are sin d, cos d
+    P = oracle.samu_chunk_transition(inp["nu"], inp["theta"], E, d)
+    hT = ref["hT"][0, :, 0] + 1j * ref["hT"][0, :, 1]
+    np.testing.assert_allclose(P, hT, rtol=1e-12, atol=0)
+
+
+def test_chunk_closed_form_reset_and_split():
+    """A reset anywhere in the chunk zeroes its transition; and the closed form
+    of a chunk is the product of the closed forms of its two halves."""
+    r = rng0(34)
+    M, K = 9, 32
+    nu, theta = -np.log(r.uniform(0.9, 0.999, M)), r.uniform(0, 2 * math.pi, M)
+    E, d = np.exp(r.uniform(-0.05, 0.05, K)), r.uniform(-0.05, 0.05, K)
+    rs = np.zeros(K, np.uint8)
+    rs[17] = 1
+    assert not np.any(oracle.samu_chunk_transition(nu, theta, E, d, rs))
+    whole = oracle.samu_chunk_transition(nu, theta, E, d)
+    halves = (oracle.samu_chunk_transition(nu, theta, E[:11], d[:11])
+              * oracle.samu_chunk_transition(nu, theta, E[11:], d[11:]))
+    np.testing.assert_allclose(whole, halves, rtol=1e-13)
+
+
+def test_chunk_closed_form_phase_needs_more_than_fp32():
+    """Why the closed form is formed with the phase K theta in FP64: rounding
+    K theta + D to FP32 (|K theta| up to 2 pi K) already moves the transition by
+    more than the pages' 5e-6 output gate at K = 32, while rounding the FP64
+    result lbar^K once to FP32 stays near FP32 precision."""
+    K = 32
+    theta = np.array([6.2831])                   # theta near 2 pi: the largest phase
+    nu = np.array([1e-3])
+    E, d = np.ones(K), np.full(K, 0.01)
+    exact = oracle.samu_chunk_transition(nu, theta, E, d)
+    phase32 = np.float32(np.float32(K) * np.float32(theta[0])) + np.float32(d.sum())
+    fp32_phase = np.exp(-nu * E.sum()) * np.exp(1j * np.float64(phase32))
+    lbarK = np.exp(-K * nu) * np.exp(1j * K * theta)
+    once = np.complex64(lbarK) * np.exp(1j * d.sum())
+    assert abs(fp32_phase - exact)[0] / abs(exact)[0] > 5e-6
+    assert abs(once - exact)[0] / abs(exact)[0] < 2e-7

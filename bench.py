@@ -490,7 +490,7 @@ def run_ours(args, rank, world, local):
 # before every step), per-kernel durations from an eager pass with the
 # library's events, achieved bytes against the algorithmic minimum
 # (SAMU 16 B*L*D, RG-LRU 22 B*L*D with BF16 gradients).  One JSON line each.
-SWEEP_BYTES_PER_BLD = {"samu": 16.0, "rglru": 22.0}
+SWEEP_BYTES_PER_BLD = {"samu": 16.0, "rglru": 22.0, "rglru_proj": 10.0}
 
 
 def sweep_one(name, dev, K, W, transition):
@@ -510,6 +510,16 @@ def sweep_one(name, dev, K, W, transition):
               "dtheta": torch.empty((M,), dtype=f32, device=dev), "dw_phi": torch.empty((D + 1,), dtype=f32, device=dev),
               "dw_r": torch.empty((D + 1,), dtype=f32, device=dev), "da_phi": torch.empty((1,), dtype=f32, device=dev),
               "da_r": torch.empty((1,), dtype=f32, device=dev)}
+    elif wl.kind == "rglru_proj":
+        t = api.rglru_proj_tensors_from_numpy(inp, dev)
+        nsaved, nscratch = api.rglru_proj_workspace_bytes(B, L, D)
+        dk = D // api.PROJ_BLOCKS
+        fo = {"y": torch.empty((B, L, D), dtype=bf, device=dev), "hT": torch.empty((B, D), dtype=f32, device=dev)}
+        go = {"dx": torch.empty((B, L, D), dtype=bf, device=dev),
+              "dw_x": torch.empty((api.PROJ_BLOCKS, dk, dk), dtype=f32, device=dev),
+              "dw_a": torch.empty((api.PROJ_BLOCKS, dk, dk), dtype=f32, device=dev),
+              "db_x": torch.empty((D,), dtype=f32, device=dev), "db_a": torch.empty((D,), dtype=f32, device=dev),
+              "dalpha": torch.empty((D,), dtype=f32, device=dev), "dh0": torch.empty((B, D), dtype=f32, device=dev)}
     else:
         t = api.rglru_tensors_from_numpy(inp, dev)
         nsaved, nscratch = api.rglru_workspace_bytes(B, L, D)
@@ -526,6 +536,10 @@ def sweep_one(name, dev, K, W, transition):
                              t["a_phi"], t["a_r"], out=fo, saved=saved, scratch=scratch)
             api.samu_backward(t["dy"], t["dhT"], t["x_sel"], t["w"], t["h0"], t["reset"], t["nu"], t["theta"],
                               t["w_phi"], t["w_r"], t["a_phi"], t["a_r"], saved, out=go, scratch=scratch)
+        elif wl.kind == "rglru_proj":
+            p = (t["x"], t["w_x"], t["b_x"], t["w_a"], t["b_a"], t["alpha"], t["h0"], t["reset"])
+            api.rglru_proj_forward(*p, out=fo, saved=saved, scratch=scratch)
+            api.rglru_proj_backward(t["dy"], t["dhT"], *p, saved, out=go, scratch=scratch)
         else:
             api.rglru_forward(t["x"], t["lx"], t["la"], t["alpha"], t["h0"], t["reset"], out=fo, saved=saved,
                               scratch=scratch)

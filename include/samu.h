@@ -90,7 +90,9 @@ int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
  * 4 SAMU backward main, 5 controller backward, 6 SAMU parameter reductions,
  * 7 RG-LRU scan forward, 8 RG-LRU scan backward, 9 RG-LRU alpha reduction,
  * 10 SAMU forward maps, 11 SAMU backward maps, 12 SAMU decode prepare,
- * 13 SAMU decode step) and duration in milliseconds; *count receives the number of
+ * 13 SAMU decode step, 14 RG-LRU gate-projection GEMMs, 15 RG-LRU projection
+ * backward GEMMs, 16 FP32-to-BF16 conversion; 9 also covers the bias-gradient
+ * reductions) and duration in milliseconds; *count receives the number of
  * kernels launched while profiling was on.  Not thread-safe: one profiling
  * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),
  * LRS_ERR_CUDA. */
@@ -254,6 +256,52 @@ int rglru_backward(const void* dy, const float* dhT, const void* x, const void* 
                    int B, int L, int D, const void* saved, void* dx, void* dlx, void* dla,
                    int grad_dtype, float* dalpha, float* dh0, void* scratch,
                    cudaStream_t stream);
+
+/* ======================================================================== */
+/* RG-LRU with its block-diagonal gate projections                           */
+/* ======================================================================== */
+
+/* The RG-LRU mixer's two gate projections ahead of the scan ([SAMU page]
+ * section 04, forward: "two canonical block-diagonal projections produce the
+ * write- and keep-gate raw values"; [Protocol] "RG-LRU 的固定方程": 16-block
+ * block-diagonal linear layers; section 06 parameter count 2 D^2/16 + 3 D):
+ *   lx_t[h dk + o] = sum_i x_t[h dk + i] w_x[h][i][o] + b_x[h dk + o],
+ *   la_t likewise with w_a, b_a;  h = 0..15, dk = D/16,
+ * then the RG-LRU scan of rglru_forward on (x, lx, la).  The products are
+ * formed from the BF16 x and BF16 weights with FP32 accumulation (cuBLAS
+ * batched GEMMs) and stay in FP32 (no rounding of the logits).
+ *
+ *   x           [B,L,D] BF16 (in)
+ *   w_x, w_a    [16][dk][dk] BF16 (in), row i = input channel, column o = output
+ *   b_x, b_a    [D] FP32 (in);  alpha [D] FP32 (in)
+ *   h0, reset, y, y32, hT: as rglru_forward
+ *   saved, scratch: rglru_proj_workspace_bytes() (scratch holds the FP32
+ *               logits and the GEMM library's workspace)
+ * The first call on a host thread creates that thread's cuBLAS handle (the
+ * one place where this library allocates device memory itself).
+ * Errors: as rglru_forward, plus LRS_ERR_UNSUPPORTED unless D is a multiple
+ * of 128 (dk a multiple of 8). */
+int rglru_proj_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes);
+int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const void* w_a, const float* b_a,
+                       const float* alpha, const float* h0, const uint8_t* reset, int B, int L, int D,
+                       void* y, float* y32, float* hT, void* saved, void* scratch, cudaStream_t stream);
+
+/* Backward of rglru_proj_forward: the scan backward with the logits
+ * recomputed, then dx = dx_scan + dlx W_x^T + dla W_a^T per block,
+ * dW_x = x^T dlx, dW_a = x^T dla, db = sum over tokens of dl.  The gate
+ * gradients enter the products as BF16 leading parts plus BF16 remainders
+ * (16 significant bits); the bias and alpha gradients are fixed-order sums.
+ *
+ *   dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, B, L, D, saved: as above
+ *   dx          [B,L,D] BF16 or FP32 by grad_dtype (out)
+ *   dw_x, dw_a  [16][dk][dk] FP32 (out);  db_x, db_a, dalpha [D] FP32 (out)
+ *   dh0         [B,D] FP32 (out)
+ * Errors: as rglru_backward. */
+int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const void* w_x, const float* b_x,
+                        const void* w_a, const float* b_a, const float* alpha, const float* h0,
+                        const uint8_t* reset, int B, int L, int D, const void* saved, void* dx, int grad_dtype,
+                        float* dw_x, float* db_x, float* dw_a, float* db_a, float* dalpha, float* dh0,
+                        void* scratch, cudaStream_t stream);
 
 /* ======================================================================== */
 /* SAMU forward without allocation                                           */

@@ -47,6 +47,9 @@ _SIGNATURES = {
     "rglru_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
     "rglru_forward": ([_P] * 6 + [_I, _I, _I] + [_P] * 6, _I),
     "rglru_backward": ([_P] * 8 + [_I, _I, _I] + [_P] * 4 + [_I] + [_P] * 4, _I),
+    "rglru_proj_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
+    "rglru_proj_forward": ([_P] * 8 + [_I, _I, _I] + [_P] * 6, _I),
+    "rglru_proj_backward": ([_P] * 10 + [_I, _I, _I] + [_P] * 2 + [_I] + [_P] * 8, _I),
 }
 
 
@@ -354,6 +357,85 @@ def rglru_backward(dy, dhT, x, lx, la, alpha, h0, reset, saved, *, grad_fp32=Fal
     return o
 
 
+# ---------------------------------------------------------------------------
+# RG-LRU with its block-diagonal gate projections
+# ---------------------------------------------------------------------------
+PROJ_BLOCKS = 16
+
+
+def rglru_proj_workspace_bytes(B: int, L: int, D: int):
+    lib = _load()
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    _check("rglru_proj_workspace_bytes", lib.rglru_proj_workspace_bytes(B, L, D, ctypes.byref(s), ctypes.byref(c)))
+    return int(s.value), int(c.value)
+
+
+def _proj_params(x, w_x, b_x, w_a, b_a, alpha):
+    dev = x.device
+    B, L, D = x.shape
+    dk = D // PROJ_BLOCKS
+    _need(x, "x", torch.bfloat16, dev)
+    for t, n in ((w_x, "w_x"), (w_a, "w_a")):
+        _need(t, n, torch.bfloat16, dev, (PROJ_BLOCKS, dk, dk))
+    for t, n in ((b_x, "b_x"), (b_a, "b_a"), (alpha, "alpha")):
+        _need(t, n, torch.float32, dev, (D,))
+    return dev, B, L, D, dk
+
+
+def rglru_proj_forward(x, w_x, b_x, w_a, b_a, alpha, h0, reset, *, want_y32=False, out=None, saved=None,
+                       scratch=None):
+    """RG-LRU forward with the block-diagonal gate projections (``rglru_proj_forward``).
+    Returns dict(y, y32, hT, saved, scratch)."""
+    dev, B, L, D, dk = _proj_params(x, w_x, b_x, w_a, b_a, alpha)
+    _opt(h0, "h0", torch.float32, dev, (B, D))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    nsaved, nscratch = rglru_proj_workspace_bytes(B, L, D)
+    y = _empty((B, L, D), torch.bfloat16, dev, out, "y")
+    y32 = _empty((B, L, D), torch.float32, dev, out, "y32") if want_y32 else None
+    hT = _empty((B, D), torch.float32, dev, out, "hT")
+    if saved is None:
+        saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    st = _load().rglru_proj_forward(_ptr(x), _ptr(w_x), _ptr(b_x), _ptr(w_a), _ptr(b_a), _ptr(alpha), _ptr(h0),
+                                    _ptr(reset), B, L, D, _ptr(y), _ptr(y32), _ptr(hT), _ptr(saved), _ptr(scratch),
+                                    _stream(dev))
+    _check("rglru_proj_forward", st)
+    return {"y": y, "y32": y32, "hT": hT, "saved": saved, "scratch": scratch}
+
+
+def rglru_proj_backward(dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, saved, *, grad_fp32=False, out=None,
+                        scratch=None):
+    """Backward of rglru_proj_forward (``rglru_proj_backward``).
+    Returns dict(dx, dw_x, db_x, dw_a, db_a, dalpha, dh0, scratch)."""
+    dev, B, L, D, dk = _proj_params(x, w_x, b_x, w_a, b_a, alpha)
+    _need(dy, "dy", torch.bfloat16, dev, (B, L, D))
+    _opt(dhT, "dhT", torch.float32, dev, (B, D))
+    nsaved, nscratch = rglru_proj_workspace_bytes(B, L, D)
+    if saved is None or saved.numel() < nsaved:
+        raise ValueError("saved must be the forward's saved buffer")
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    o = {
+        "dx": _empty((B, L, D), torch.float32 if grad_fp32 else torch.bfloat16, dev, out, "dx"),
+        "dw_x": _empty((PROJ_BLOCKS, dk, dk), torch.float32, dev, out, "dw_x"),
+        "db_x": _empty((D,), torch.float32, dev, out, "db_x"),
+        "dw_a": _empty((PROJ_BLOCKS, dk, dk), torch.float32, dev, out, "dw_a"),
+        "db_a": _empty((D,), torch.float32, dev, out, "db_a"),
+        "dalpha": _empty((D,), torch.float32, dev, out, "dalpha"),
+        "dh0": _empty((B, D), torch.float32, dev, out, "dh0"),
+    }
+    st = _load().rglru_proj_backward(_ptr(dy), _ptr(dhT), _ptr(x), _ptr(w_x), _ptr(b_x), _ptr(w_a), _ptr(b_a),
+                                     _ptr(alpha), _ptr(h0), _ptr(reset), B, L, D, _ptr(saved), _ptr(o["dx"]),
+                                     LRS_GRAD_FP32 if grad_fp32 else LRS_GRAD_BF16, _ptr(o["dw_x"]), _ptr(o["db_x"]),
+                                     _ptr(o["dw_a"]), _ptr(o["db_a"]), _ptr(o["dalpha"]), _ptr(o["dh0"]),
+                                     _ptr(scratch), _stream(dev))
+    _check("rglru_proj_backward", st)
+    o["scratch"] = scratch
+    return o
+
+
 def device_status(scratch, device=None) -> int:
     """Status word of the most recent call that used ``scratch`` (synchronises the stream)."""
     dev = scratch.device if device is None else device
@@ -367,7 +449,8 @@ KERNEL_NAMES = {
     4: "samu_bwd_main_kernel", 5: "samu_ctrl_bwd_kernel", 6: "samu_params_kernel",
     7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
     10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel", 12: "samu_decode_prepare_kernel",
-    13: "samu_decode_step_kernel",
+    13: "samu_decode_step_kernel", 14: "rglru_proj_gemms (cuBLAS)", 15: "rglru_proj_bwd_gemms (cuBLAS)",
+    16: "rglru_to_bf16_kernel",
 }
 
 
@@ -403,6 +486,14 @@ def _f32(a, device):
 def samu_tensors_from_numpy(inp: dict, device) -> dict:
     out = {k: _bf16(inp[k], device) for k in ("x_sel", "w", "dy")}
     for k in ("nu", "theta", "w_phi", "w_r", "a_phi", "a_r", "h0", "dhT"):
+        out[k] = _f32(inp[k], device)
+    out["reset"] = None if inp["reset"] is None else torch.from_numpy(inp["reset"]).to(device)
+    return out
+
+
+def rglru_proj_tensors_from_numpy(inp: dict, device) -> dict:
+    out = {k: _bf16(inp[k], device) for k in ("x", "w_x", "w_a", "dy")}
+    for k in ("b_x", "b_a", "alpha", "h0", "dhT"):
         out[k] = _f32(inp[k], device)
     out["reset"] = None if inp["reset"] is None else torch.from_numpy(inp["reset"]).to(device)
     return out

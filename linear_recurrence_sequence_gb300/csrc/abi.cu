@@ -3,6 +3,7 @@
 // (except lrs_device_status, which documents that it synchronises).
 #include <cstdint>
 #include <cstring>
+#include <cublas_v2.h>
 #include "kernels.cuh"
 #include "tmap.cuh"
 
@@ -76,7 +77,8 @@ int g_transition = LRS_TRANSITION_CLOSED_FORM;
 enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
     KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
-    KID_SAMU_BWD_MAPS, KID_SAMU_DECODE_PREP, KID_SAMU_DECODE_STEP
+    KID_SAMU_BWD_MAPS, KID_SAMU_DECODE_PREP, KID_SAMU_DECODE_STEP, KID_RGLRU_PROJ_FWD, KID_RGLRU_PROJ_BWD,
+    KID_RGLRU_TO_BF16
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -86,6 +88,101 @@ enum {
         prof_end(stream);                       \
         if (e_ != cudaSuccess) return LRS_ERR_CUDA; \
     } while (0)
+
+// ---------------------------------------------------------------------------
+// Block-diagonal gate projections through cuBLAS (plain batched GEMMs, BF16
+// operands, FP32 accumulation and output): one handle per host thread,
+// created on first use (the library allocates its own small device state
+// then), with the caller's scratch as its workspace on every call.
+// Row-major [rows x D] activations are column-major [D x rows] matrices to
+// cuBLAS; block h is the D/16-wide column slice h, batched with stride D/16.
+// ---------------------------------------------------------------------------
+cublasHandle_t gemm_handle() {
+    thread_local cublasHandle_t h = nullptr;
+    if (h == nullptr && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
+    return h;
+}
+
+struct Gemm {
+    cublasHandle_t h;
+    int rows, D, dk;
+};
+
+cudaError_t gemm_begin(Gemm& gm, int rows, int D, void* ws, cudaStream_t s) {
+    gm.h = gemm_handle();
+    gm.rows = rows;
+    gm.D = D;
+    gm.dk = D / kProjBlocks;
+    if (gm.h == nullptr) return cudaErrorUnknown;
+    if (cublasSetStream(gm.h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    if (cublasSetWorkspace(gm.h, ws, kGemmWorkspace) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    return cudaSuccess;
+}
+
+// out[t][h dk + o] (+)= sum_i in[t][h dk + i] W[h][i][o]   (l = x W)
+cudaError_t gemm_xw(const Gemm& gm, const void* in, const void* w, float* out, float beta) {
+    const float one = 1.0f;
+    const cublasStatus_t st = cublasGemmStridedBatchedEx(
+        gm.h, CUBLAS_OP_N, CUBLAS_OP_N, gm.dk, gm.rows, gm.dk, &one, w, CUDA_R_16BF, gm.dk,
+        (long long)gm.dk * gm.dk, in, CUDA_R_16BF, gm.D, gm.dk, &beta, out, CUDA_R_32F, gm.D, gm.dk, kProjBlocks,
+        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// out[t][h dk + i] += sum_o g[t][h dk + o] W[h][i][o]   (dx += dl W^T)
+cudaError_t gemm_gwt(const Gemm& gm, const void* g, const void* w, float* out) {
+    const float one = 1.0f;
+    const cublasStatus_t st = cublasGemmStridedBatchedEx(
+        gm.h, CUBLAS_OP_T, CUBLAS_OP_N, gm.dk, gm.rows, gm.dk, &one, w, CUDA_R_16BF, gm.dk,
+        (long long)gm.dk * gm.dk, g, CUDA_R_16BF, gm.D, gm.dk, &one, out, CUDA_R_32F, gm.D, gm.dk, kProjBlocks,
+        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// dW[h][i][o] (+)= sum_t x[t][h dk + i] g[t][h dk + o]   (dW = x^T dl)
+cudaError_t gemm_xtg(const Gemm& gm, const void* x, const void* g, float* dw, float beta) {
+    const float one = 1.0f;
+    const cublasStatus_t st = cublasGemmStridedBatchedEx(
+        gm.h, CUBLAS_OP_N, CUBLAS_OP_T, gm.dk, gm.dk, gm.rows, &one, g, CUDA_R_16BF, gm.D, gm.dk, x, CUDA_R_16BF,
+        gm.D, gm.dk, &beta, dw, CUDA_R_32F, gm.dk, (long long)gm.dk * gm.dk, kProjBlocks, CUBLAS_COMPUTE_32F,
+        CUBLAS_GEMM_DEFAULT);
+    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// Both gates' products x W_x, x W_a (FP32, biases excluded) into scratch.
+cudaError_t proj_forward_gemms(int rows, int D, const void* x, const void* w_x, const void* w_a, float* lx, float* la,
+                               void* ws, cudaStream_t s) {
+    Gemm gm;
+    cudaError_t e = gemm_begin(gm, rows, D, ws, s);
+    if (e == cudaSuccess) e = gemm_xw(gm, x, w_x, lx, 0.0f);
+    if (e == cudaSuccess) e = gemm_xw(gm, x, w_a, la, 0.0f);
+    return e;
+}
+
+// dx32 += (hi + lo)(dl^x) W_x^T + (hi + lo)(dl^a) W_a^T; dW = x^T (hi + lo).
+cudaError_t proj_backward_gemms(int rows, int D, const void* x, const void* w_x, const void* w_a, const void* gx_hi,
+                                const void* gx_lo, const void* ga_hi, const void* ga_lo, float* dx32, float* dw_x,
+                                float* dw_a, void* ws, cudaStream_t s) {
+    Gemm gm;
+    cudaError_t e = gemm_begin(gm, rows, D, ws, s);
+    if (e == cudaSuccess) e = gemm_gwt(gm, gx_hi, w_x, dx32);
+    if (e == cudaSuccess) e = gemm_gwt(gm, gx_lo, w_x, dx32);
+    if (e == cudaSuccess) e = gemm_gwt(gm, ga_hi, w_a, dx32);
+    if (e == cudaSuccess) e = gemm_gwt(gm, ga_lo, w_a, dx32);
+    if (e == cudaSuccess) e = gemm_xtg(gm, x, gx_hi, dw_x, 0.0f);
+    if (e == cudaSuccess) e = gemm_xtg(gm, x, gx_lo, dw_x, 1.0f);
+    if (e == cudaSuccess) e = gemm_xtg(gm, x, ga_hi, dw_a, 0.0f);
+    if (e == cudaSuccess) e = gemm_xtg(gm, x, ga_lo, dw_a, 1.0f);
+    return e;
+}
+
+int check_rglru_proj_shape(int B, int L, int D) {
+    const int st = check_rglru_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (D % kProjBlocks != 0 || (D / kProjBlocks) % 8 != 0) return LRS_ERR_UNSUPPORTED;
+    if ((long long)B * L > 0x7fffffffLL) return LRS_ERR_UNSUPPORTED;
+    return LRS_OK;
+}
 
 template <typename T>
 T* at(void* base, size_t off) {
@@ -476,6 +573,117 @@ int rglru_backward(const void* dy, const float* dhT, const void* x, const void* 
     LRS_LAUNCH(KID_RGLRU_SCAN_BWD, stream, launch_rglru_scan_bwd(tm_dy, tm_x, tm_lx, tm_la, a, stream));
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream,
                launch_rglru_alpha(a.apart, at<float>(scratch, sc.apart2), dalpha, B * g.CT, D, stream));
+    return LRS_OK;
+}
+
+int rglru_proj_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes) {
+    const int st = check_rglru_proj_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (saved_bytes) *saved_bytes = rglru_saved_layout(B, L, D).total;
+    if (scratch_bytes) *scratch_bytes = rglru_proj_scratch_layout(B, L, D).total;
+    return LRS_OK;
+}
+
+int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const void* w_a, const float* b_a,
+                       const float* alpha, const float* h0, const uint8_t* reset, int B, int L, int D,
+                       void* y, float* y32, float* hT, void* saved, void* scratch, cudaStream_t stream) {
+    const int st = check_rglru_proj_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (!req(x) || !req(w_x) || !req(b_x) || !req(w_a) || !req(b_a) || !req(alpha) || !opt(h0) || !req(y) ||
+        !opt(y32) || !req(hT) || !req(saved) || !req(scratch))
+        return LRS_ERR_ARG;
+    const RglruSaved sv = rglru_saved_layout(B, L, D);
+    const RglruProjScratch ps = rglru_proj_scratch_layout(B, L, D);
+    const RglruScratch& sc = ps.scan;
+    float* lx = at<float>(scratch, ps.lx);
+    float* la = at<float>(scratch, ps.la);
+    if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
+               proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, at<void>(scratch, ps.gemm_ws), stream));
+    CUtensorMap tm_x, tm_lx, tm_la;
+    if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) ||
+        !make_f32_map(&tm_la, la, B, L, D, kRgTile))
+        return LRS_ERR_CUDA;
+    RglruScanFwdArgs a;
+    a.g = make_geom(B, L, D, kRgTile);
+    a.alpha = alpha;
+    a.bx = b_x;
+    a.ba = b_a;
+    a.reset = reset;
+    a.h0 = h0;
+    a.y = static_cast<uint32_t*>(y);
+    a.y32 = y32;
+    a.hT = hT;
+    a.hsub = at<float>(saved, sv.hsub);
+    a.agg = at<float2>(scratch, sc.agg);
+    a.flags = at<uint32_t>(scratch, sc.flags);
+    a.counter = at<uint32_t>(scratch, sc.status + 4);
+    a.status = at<uint32_t>(scratch, sc.status);
+    LRS_LAUNCH(KID_RGLRU_SCAN_FWD, stream, launch_rglru_scan_fwd(tm_x, tm_lx, tm_la, a, stream, true));
+    return LRS_OK;
+}
+
+int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const void* w_x, const float* b_x,
+                        const void* w_a, const float* b_a, const float* alpha, const float* h0,
+                        const uint8_t* reset, int B, int L, int D, const void* saved, void* dx, int grad_dtype,
+                        float* dw_x, float* db_x, float* dw_a, float* db_a, float* dalpha, float* dh0,
+                        void* scratch, cudaStream_t stream) {
+    (void)h0;
+    const int st = check_rglru_proj_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (grad_dtype != LRS_GRAD_BF16 && grad_dtype != LRS_GRAD_FP32) return LRS_ERR_ARG;
+    if (!req(dy) || !opt(dhT) || !req(x) || !req(w_x) || !req(b_x) || !req(w_a) || !req(b_a) || !req(alpha) ||
+        !req(saved) || !req(dx) || !req(dw_x) || !req(db_x) || !req(dw_a) || !req(db_a) || !req(dalpha) ||
+        !req(dh0) || !req(scratch))
+        return LRS_ERR_ARG;
+    const RglruSaved sv = rglru_saved_layout(B, L, D);
+    const RglruProjScratch ps = rglru_proj_scratch_layout(B, L, D);
+    const RglruScratch& sc = ps.scan;
+    const ScanGeom g = make_geom(B, L, D, kRgTile);
+    float* lx = at<float>(scratch, ps.lx);
+    float* la = at<float>(scratch, ps.la);
+    const bool fp32 = grad_dtype == LRS_GRAD_FP32;
+    float* dx32 = fp32 ? static_cast<float*>(dx) : at<float>(scratch, ps.dx32);
+    void* ws = at<void>(scratch, ps.gemm_ws);
+    if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream, proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, ws, stream));
+    CUtensorMap tm_dy, tm_x, tm_lx, tm_la;
+    if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile) || !make_bf16_map(&tm_x, x, B, L, D, kRgTile) ||
+        !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) || !make_f32_map(&tm_la, la, B, L, D, kRgTile))
+        return LRS_ERR_CUDA;
+    RglruScanBwdArgs a;
+    a.g = g;
+    a.alpha = alpha;
+    a.bx = b_x;
+    a.ba = b_a;
+    a.reset = reset;
+    a.dhT = dhT;
+    a.hsub = at<float>(saved, sv.hsub);
+    a.dx = dx32;
+    a.dlx = at<void>(scratch, ps.dlx_hi);
+    a.dla = at<void>(scratch, ps.dla_hi);
+    a.dlx_lo = at<uint32_t>(scratch, ps.dlx_lo);
+    a.dla_lo = at<uint32_t>(scratch, ps.dla_lo);
+    a.bxpart = at<float>(scratch, ps.bxpart);
+    a.bapart = at<float>(scratch, ps.bapart);
+    a.grad_fp32 = 1;
+    a.dh0 = dh0;
+    a.agg = at<float2>(scratch, sc.agg);
+    a.rin = at<float>(scratch, sc.rin);
+    a.apart = at<float>(scratch, sc.apart);
+    a.flags = at<uint32_t>(scratch, sc.flags);
+    a.counter = at<uint32_t>(scratch, sc.status + 4);
+    a.status = at<uint32_t>(scratch, sc.status);
+    LRS_LAUNCH(KID_RGLRU_SCAN_BWD, stream, launch_rglru_scan_bwd(tm_dy, tm_x, tm_lx, tm_la, a, stream, true));
+    float* apart2 = at<float>(scratch, sc.apart2);
+    LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.apart, apart2, dalpha, B * g.CT, D, stream));
+    LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bxpart, apart2, db_x, B * g.CT, D, stream));
+    LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bapart, apart2, db_a, B * g.CT, D, stream));
+    LRS_LAUNCH(KID_RGLRU_PROJ_BWD, stream,
+               proj_backward_gemms(B * L, D, x, w_x, w_a, a.dlx, a.dlx_lo, a.dla, a.dla_lo, dx32, dw_x, dw_a, ws,
+                                   stream));
+    if (!fp32)
+        LRS_LAUNCH(KID_RGLRU_TO_BF16, stream, launch_rglru_to_bf16(dx32, dx, (size_t)B * L * D, stream));
     return LRS_OK;
 }
 

@@ -384,9 +384,13 @@ cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t
 // ---------------------------------------------------------------------------
 // RG-LRU
 // ---------------------------------------------------------------------------
+// With projected gates (the kernels' PL variant) l^x and l^a are FP32
+// [B,L,D] (x W without the bias) and bx, ba the biases added on reading.
 struct RglruScanFwdArgs {
     ScanGeom g;
     const float* alpha;
+    const float* bx;        // [D], PL only
+    const float* ba;
     const uint8_t* reset;
     const float* h0;        // [B,D] or null
     uint32_t* y;
@@ -399,15 +403,25 @@ struct RglruScanFwdArgs {
     uint32_t* status;
 };
 
+// PL variant: dx is FP32; dlx / dla receive the BF16 pairs of the leading
+// BF16 part of the gate gradients and dlx_lo / dla_lo those of the
+// remainder (dl = hi + lo to 16 significant bits); bxpart / bapart the
+// per-tile sums of the gate gradients (the bias gradients' partials).
 struct RglruScanBwdArgs {
     ScanGeom g;
     const float* alpha;
+    const float* bx;
+    const float* ba;
     const uint8_t* reset;
     const float* dhT;
     const float* hsub;
     void* dx;
     void* dlx;
     void* dla;
+    uint32_t* dlx_lo;
+    uint32_t* dla_lo;
+    float* bxpart;          // [B*CT][D]
+    float* bapart;
     int grad_fp32;
     float* dh0;
     float2* agg;
@@ -419,10 +433,13 @@ struct RglruScanBwdArgs {
 };
 
 cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
-                                  const RglruScanFwdArgs& args, cudaStream_t s);
+                                  const RglruScanFwdArgs& args, cudaStream_t s, bool projected = false);
 cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
-                                  const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s);
+                                  const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s,
+                                  bool projected = false);
 cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,
                                cudaStream_t s);
+// n FP32 values (n even) to BF16, round to nearest even.
+cudaError_t launch_rglru_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
 
 }  // namespace lrs

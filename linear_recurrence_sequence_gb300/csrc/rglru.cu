@@ -22,6 +22,24 @@ namespace lrs {
 constexpr int kRgThreads = kRgWarps * 32;
 constexpr int kRgBoxBytes = kRgTile * kRowBytes;   // one BF16 [128 x 64] box
 
+// Gate-logit boxes: BF16 [128 x 64] (raw l^x, l^a inputs) or, with projected
+// gates (PL), FP32 [128 x 64] products x W whose biases are added on reading.
+template <bool PL>
+struct RgLogits {
+    static constexpr int kBoxBytes = PL ? 2 * kRgBoxBytes : kRgBoxBytes;
+    static constexpr int kSlotBytes = kRgBoxBytes + 2 * kBoxBytes;   // x, l^x, l^a
+};
+
+// The lane's two logits of token row r (bias added for PL).
+template <bool PL>
+__device__ __forceinline__ float2 rg_logit(const uint8_t* box, int r, int lane, float2 bias) {
+    if (PL) {
+        const float2 v = reinterpret_cast<const float2*>(box)[r * 32 + lane];
+        return make_float2(v.x + bias.x, v.y + bias.y);
+    }
+    return bf2_to_f2(reinterpret_cast<const uint32_t*>(box)[r * 32 + lane]);
+}
+
 struct RgGate {
     float a;    // retention (0 at a segment start)
     float n;    // write normaliser sqrt(1 - a^2) (1 at a segment start)
@@ -78,17 +96,19 @@ __device__ __forceinline__ float softplus_f(float v) {
 // Forward
 // ---------------------------------------------------------------------------
 // Lane 0 of thread 0: the three boxes of `tile` into ring slot `slot`.
+template <bool PL>
 __device__ __forceinline__ void rg_fwd_issue(uint8_t* slot_base, uint64_t* bar, const CUtensorMap* tm_x,
                                              const CUtensorMap* tm_lx, const CUtensorMap* tm_la, const ScanGeom& g,
                                              long long tile) {
+    constexpr int LB = RgLogits<PL>::kBoxBytes;
     const int chain = (int)(tile % g.n_chains);
     const int c = (int)(tile / g.n_chains);
     const int b = chain / g.n_groups, grp = chain % g.n_groups;
     fence_proxy_async();
-    mbar_arrive_expect_tx(bar, 3 * kRgBoxBytes);
+    mbar_arrive_expect_tx(bar, RgLogits<PL>::kSlotBytes);
     tma_load_3d(slot_base, tm_x, grp * kGroup, c * kRgTile, b, bar);
     tma_load_3d(slot_base + kRgBoxBytes, tm_lx, grp * kGroup, c * kRgTile, b, bar);
-    tma_load_3d(slot_base + 2 * kRgBoxBytes, tm_la, grp * kGroup, c * kRgTile, b, bar);
+    tma_load_3d(slot_base + kRgBoxBytes + LB, tm_la, grp * kGroup, c * kRgTile, b, bar);
 }
 
 // Persistent CTAs: each takes tiles in ticket order (atomic counter) and keeps
@@ -96,9 +116,12 @@ __device__ __forceinline__ void rg_fwd_issue(uint8_t* slot_base, uint64_t* bar, 
 // while it works on the current one.  Tickets are taken in increasing order
 // by every CTA and each CTA finishes its current tile before its prefetched
 // one, so the smallest tile in progress always finds its predecessors done.
+template <bool PL>
 __global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_lx,
                           const __grid_constant__ CUtensorMap tm_la, RglruScanFwdArgs a) {
+    constexpr int LB = RgLogits<PL>::kBoxBytes;
+    constexpr int SB = RgLogits<PL>::kSlotBytes;
     extern __shared__ __align__(128) uint8_t s_dyn[];   // [slot][x, l^x, l^a boxes]
     __shared__ uint8_t s_rst[kRgTile];
     __shared__ float4 s_map[kRgWarps][32];
@@ -116,7 +139,7 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         mbar_init(&s_bars[0], 1);
         mbar_init(&s_bars[1], 1);
         s_tick[0] = atomicAdd(a.counter, 1u);
-        if (s_tick[0] < n_tiles) rg_fwd_issue(s_dyn, &s_bars[0], &tm_x, &tm_lx, &tm_la, g, s_tick[0]);
+        if (s_tick[0] < n_tiles) rg_fwd_issue<PL>(s_dyn, &s_bars[0], &tm_x, &tm_lx, &tm_la, g, s_tick[0]);
     }
     __syncthreads();
     int pend = -1;   // iteration whose prefetched copy is outstanding when the loop is left early
@@ -127,13 +150,13 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     if (tid == 0) {   // the next ticket into the other slot (free since the end of the previous tile)
         s_tick[slot ^ 1] = atomicAdd(a.counter, 1u);
         if (s_tick[slot ^ 1] < n_tiles)
-            rg_fwd_issue(s_dyn + (size_t)(slot ^ 1) * 3 * kRgBoxBytes, &s_bars[slot ^ 1], &tm_x, &tm_lx, &tm_la, g,
-                         s_tick[slot ^ 1]);
+            rg_fwd_issue<PL>(s_dyn + (size_t)(slot ^ 1) * SB, &s_bars[slot ^ 1], &tm_x, &tm_lx, &tm_la, g,
+                             s_tick[slot ^ 1]);
     }
-    uint8_t* sb = s_dyn + (size_t)slot * 3 * kRgBoxBytes;
+    uint8_t* sb = s_dyn + (size_t)slot * SB;
     uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb);
-    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb + kRgBoxBytes);
-    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb + 2 * kRgBoxBytes);
+    const uint8_t* s_lx = sb + kRgBoxBytes;
+    const uint8_t* s_la = sb + kRgBoxBytes + LB;
     const long long tile = tile_u;
     const int chain = (int)(tile % g.n_chains);
     const int c = (int)(tile / g.n_chains);
@@ -153,9 +176,14 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         s_rst[tid] = (t < L && a.reset != nullptr && a.reset[(size_t)b * L + t] != 0) ? 1 : 0;
     }
     float nsp0 = 0.f, nsp1 = 0.f;
+    float2 bxv = make_float2(0.f, 0.f), bav = bxv;
     if (active) {
         nsp0 = -8.0f * softplus_f(a.alpha[d]);
         nsp1 = -8.0f * softplus_f(a.alpha[d + 1]);
+        if (PL) {
+            bxv = *reinterpret_cast<const float2*>(a.bx + d);
+            bav = *reinterpret_cast<const float2*>(a.ba + d);
+        }
     }
     const int r0 = warp * kSub;
     const int nsub = max(0, min(kSub, L - t0 - r0));
@@ -177,8 +205,8 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
             const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
-            const float2 gl = bf2_to_f2(s_lx[r0 + i][lane]);
-            const float2 al = bf2_to_f2(s_la[r0 + i][lane]);
+            const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
+            const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
             const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
             const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
             ab[i] = make_float4(g0.a, xx.x * g0.gx * g0.n, g1.a, xx.y * g1.gx * g1.n);
@@ -300,19 +328,29 @@ __global__ void __launch_bounds__(kRgThreads, 2)
 //   dl^a = abar (-8 softplus(alpha)) a g^a (1 - g^a);
 //   dalpha += abar (-8 g^a) sigmoid(alpha) a.
 // ---------------------------------------------------------------------------
+// The leading BF16 pair of (v0, v1) and the BF16 pair of the remainders.
+__device__ __forceinline__ void split_bf2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    hi = f2_to_bf2(v0, v1);
+    const float2 h = bf2_to_f2(hi);
+    lo = f2_to_bf2(v0 - h.x, v1 - h.y);
+}
+
+template <bool PL>
 __global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_lx, const __grid_constant__ CUtensorMap tm_la,
                           RglruScanBwdArgs a) {
+    constexpr int LB = RgLogits<PL>::kBoxBytes;
     extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: dy, x, l^x, l^a
     uint32_t (*s_g)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
     uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kRgBoxBytes);
-    uint32_t (*s_lx)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 2 * kRgBoxBytes);
-    uint32_t (*s_la)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + 3 * kRgBoxBytes);
+    const uint8_t* s_lx = s_dyn + 2 * kRgBoxBytes;
+    const uint8_t* s_la = s_dyn + 2 * kRgBoxBytes + LB;
     __shared__ uint8_t s_rst[kRgTile];
     __shared__ float4 s_map[kRgWarps][32];
     __shared__ float2 s_ent[kRgWarps][32];
     __shared__ float2 s_acc[kRgWarps][32];
+    __shared__ float4 s_bacc[PL ? kRgWarps : 1][32];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint32_t s_tile;
     __shared__ int s_err;
@@ -341,11 +379,11 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     const size_t hb = (size_t)b * g.CS;
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 4 * kRgBoxBytes);
+        mbar_arrive_expect_tx(&s_bar, 2 * kRgBoxBytes + 2 * LB);
         tma_load_3d(&s_g[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
         tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_lx[0][0], &tm_lx, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_la[0][0], &tm_la, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(s_dyn + 2 * kRgBoxBytes, &tm_lx, grp * kGroup, t0, b, &s_bar);
+        tma_load_3d(s_dyn + 2 * kRgBoxBytes + LB, &tm_la, grp * kGroup, t0, b, &s_bar);
     }
     if (tid < kRgTile) {
         const int t = t0 + tid;
@@ -355,7 +393,12 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     const int nsub = max(0, min(kSub, L - t0 - r0));
     float nsp0 = 0.f, nsp1 = 0.f, sa0 = 0.f, sa1 = 0.f;
     float h0v = 0.f, h1v = 0.f;
+    float2 bxv = make_float2(0.f, 0.f), bav = bxv;
     if (active) {
+        if (PL) {
+            bxv = *reinterpret_cast<const float2*>(a.bx + d);
+            bav = *reinterpret_cast<const float2*>(a.ba + d);
+        }
         const float al0 = a.alpha[d], al1 = a.alpha[d + 1];
         nsp0 = -8.0f * softplus_f(al0);
         nsp1 = -8.0f * softplus_f(al1);
@@ -386,8 +429,8 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
             const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
-            const float2 gl = bf2_to_f2(s_lx[r0 + i][lane]);
-            const float2 al = bf2_to_f2(s_la[r0 + i][lane]);
+            const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
+            const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
             const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
             const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
             const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
@@ -475,14 +518,15 @@ __global__ void __launch_bounds__(kRgThreads, 2)
 
     const float2 e = s_ent[warp][lane];
     float H0 = e.x, H1 = e.y, da0 = 0.f, da1 = 0.f;
+    float4 bs = make_float4(0.f, 0.f, 0.f, 0.f);   // PL: sums of dl^x, dl^a over the lane's tokens
     const size_t row = (((size_t)b * L + t0 + r0) * D + d) / 2;
 #pragma unroll
     for (int i = kSub - 1; i >= 0; --i) {
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
             const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
-            const float2 gl = bf2_to_f2(s_lx[r0 + i][lane]);
-            const float2 al = bf2_to_f2(s_la[r0 + i][lane]);
+            const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
+            const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
             const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
             const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
             const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
@@ -500,7 +544,23 @@ __global__ void __launch_bounds__(kRgThreads, 2)
                 da0 = fmaf(ab0, -8.f * g0.ga * sa0 * g0.a, da0);
                 da1 = fmaf(ab1, -8.f * g1.ga * sa1 * g1.a, da1);
             }
-            if (active) {
+            if (PL) {
+                bs.x += dlx0;
+                bs.y += dlx1;
+                bs.z += dla0;
+                bs.w += dla1;
+            }
+            if (PL && active) {
+                const size_t o = row + (size_t)i * (D / 2);
+                *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.dx) + 2 * o) = make_float2(dx0, dx1);
+                uint32_t hi, lo;
+                split_bf2(dlx0, dlx1, hi, lo);
+                __stcs(reinterpret_cast<uint32_t*>(a.dlx) + o, hi);
+                __stcs(a.dlx_lo + o, lo);
+                split_bf2(dla0, dla1, hi, lo);
+                __stcs(reinterpret_cast<uint32_t*>(a.dla) + o, hi);
+                __stcs(a.dla_lo + o, lo);
+            } else if (active) {
                 const size_t o = row + (size_t)i * (D / 2);
                 if (a.grad_fp32) {
                     *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.dx) + 2 * o) = make_float2(dx0, dx1);
@@ -518,6 +578,7 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     }
     if (c == 0 && warp == 0 && active) *reinterpret_cast<float2*>(a.dh0 + (size_t)b * D + d) = make_float2(H0, H1);
     s_acc[warp][lane] = make_float2(da0, da1);
+    if (PL) s_bacc[warp][lane] = bs;
     __syncthreads();
     if (warp == 0 && active) {
         float2 s = s_acc[0][lane];
@@ -527,6 +588,20 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             s.y += s_acc[w][lane].y;
         }
         *reinterpret_cast<float2*>(a.apart + ((size_t)b * CT + c) * D + d) = s;
+    }
+    if (PL && warp == 1 && active) {   // the tile's bias-gradient partials, warps in order
+        float4 s = s_bacc[0][lane];
+#pragma unroll
+        for (int w = 1; w < kRgWarps; ++w) {
+            const float4 v = s_bacc[w][lane];
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        const size_t o = ((size_t)b * CT + c) * D + d;
+        *reinterpret_cast<float2*>(a.bxpart + o) = make_float2(s.x, s.y);
+        *reinterpret_cast<float2*>(a.bapart + o) = make_float2(s.z, s.w);
     }
 }
 
@@ -561,6 +636,28 @@ __global__ void __launch_bounds__(256) rglru_alpha_stage2_kernel(const float* __
     dalpha[d] = s;
 }
 
+// FP32 pairs to BF16 pairs (round to nearest even), grid-strided.
+__global__ void __launch_bounds__(256) rglru_to_bf16_kernel(const float2* __restrict__ src,
+                                                            uint32_t* __restrict__ dst, size_t n_pairs) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_pairs; i += (size_t)gridDim.x * blockDim.x) {
+        const float2 v = __ldcs(src + i);
+        __stcs(dst + i, f2_to_bf2(v.x, v.y));
+    }
+}
+
+cudaError_t launch_rglru_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s) {
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+    const size_t pairs = n / 2;
+    size_t blocks = (pairs + 255) / 256;
+    if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
+    if (blocks < 1) blocks = 1;
+    rglru_to_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float2*>(src),
+                                                          static_cast<uint32_t*>(dst), pairs);
+    return cudaGetLastError();
+}
+
 // Persistent grid: as many CTAs as are resident at once, at most one per tile.
 template <typename K>
 unsigned rg_grid(K kernel, int smem, long long n_tiles) {
@@ -573,23 +670,37 @@ unsigned rg_grid(K kernel, int smem, long long n_tiles) {
     return (unsigned)(n < n_tiles ? n : (n_tiles > 0 ? n_tiles : 1));
 }
 
-cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
-                                  const RglruScanFwdArgs& args, cudaStream_t s) {
-    const int smem = 2 * 3 * kRgBoxBytes;   // two slots
-    cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <bool PL>
+cudaError_t launch_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
+                       const RglruScanFwdArgs& args, cudaStream_t s) {
+    const int smem = 2 * RgLogits<PL>::kSlotBytes;   // two slots
+    cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel<PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_fwd_kernel<<<rg_grid(rglru_scan_fwd_kernel, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
+    rglru_scan_fwd_kernel<PL><<<rg_grid(rglru_scan_fwd_kernel<PL>, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
         tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }
 
-cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
-                                  const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s) {
-    const int smem = 4 * kRgBoxBytes;
-    cudaError_t e = cudaFuncSetAttribute(rglru_scan_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
+                                  const RglruScanFwdArgs& args, cudaStream_t s, bool projected) {
+    return projected ? launch_fwd<true>(tm_x, tm_lx, tm_la, args, s) : launch_fwd<false>(tm_x, tm_lx, tm_la, args, s);
+}
+
+template <bool PL>
+cudaError_t launch_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
+                       const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s) {
+    const int smem = 2 * kRgBoxBytes + 2 * RgLogits<PL>::kBoxBytes;
+    cudaError_t e = cudaFuncSetAttribute(rglru_scan_bwd_kernel<PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_bwd_kernel<<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
+    rglru_scan_bwd_kernel<PL><<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
+}
+
+cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
+                                  const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s,
+                                  bool projected) {
+    return projected ? launch_bwd<true>(tm_dy, tm_x, tm_lx, tm_la, args, s)
+                     : launch_bwd<false>(tm_dy, tm_x, tm_lx, tm_la, args, s);
 }
 
 cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,

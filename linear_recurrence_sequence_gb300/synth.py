@@ -125,6 +125,39 @@ def rglru_inputs(B: int, L: int, D: int, seed: int, *, h0: bool = False,
             "reset": rmask, "dy": dy, "dhT": dhT, "B": B, "L": L, "D": D}
 
 
+PROJ_BLOCKS = 16   # diagonal blocks of each RG-LRU gate projection
+
+
+def rglru_proj_inputs(B: int, L: int, D: int, seed: int, *, h0: bool = False,
+                      resets: str = "segments") -> dict:
+    """Seeded inputs of the RG-LRU mixer with its two block-diagonal gate
+    projections.  x, dy: uint16 BF16 bits [B,L,D]; w_x, w_a: uint16 BF16 bits
+    [16][D/16][D/16] with entries N(0, 1/(D/16)) (so that the logits x W are
+    about N(0,1) like the raw-logit workloads); b_x, b_a float32 [D] N(0, 0.1^2);
+    alpha, h0, reset, dhT as rglru_inputs.  Draw order: x, w_x, w_a, b_x, b_a,
+    alpha, h0, reset, dy, dhT."""
+    rng = np.random.default_rng(seed)
+    dk = D // PROJ_BLOCKS
+    x = _normal_bf16(rng, (B, L, D))
+    w_x = f32_to_bf16_bits(rng.standard_normal((PROJ_BLOCKS, dk, dk)) / math.sqrt(dk))
+    w_a = f32_to_bf16_bits(rng.standard_normal((PROJ_BLOCKS, dk, dk)) / math.sqrt(dk))
+    b_x = (0.1 * rng.standard_normal(D)).astype(np.float32)
+    b_a = (0.1 * rng.standard_normal(D)).astype(np.float32)
+    sp = -np.log(rng.uniform(0.9, 0.999, size=D)) / 8.0          # softplus(alpha)
+    alpha = np.log(np.expm1(sp)).astype(np.float32)
+    h0_arr = (0.1 * rng.standard_normal((B, D))).astype(np.float32)
+    if resets == "segments":
+        rmask = segment_starts(rng, B, L)
+    elif resets == "none":
+        rmask = None
+    else:
+        rmask = (rng.random((B, L)) < float(resets)).astype(np.uint8)
+    dy = _normal_bf16(rng, (B, L, D))
+    dhT = rng.standard_normal((B, D)).astype(np.float32)
+    return {"x": x, "w_x": w_x, "w_a": w_a, "b_x": b_x, "b_a": b_a, "alpha": alpha,
+            "h0": h0_arr if h0 else None, "reset": rmask, "dy": dy, "dhT": dhT, "B": B, "L": L, "D": D}
+
+
 @dataclass(frozen=True)
 class Workload:
     name: str
@@ -141,6 +174,9 @@ class Workload:
         s = self.seeds[0] if seed is None else seed
         if self.kind == "samu":
             return samu_inputs(self.B, self.L, self.D, s, h0=self.h0, reset_p=self.reset_p)
+        if self.kind == "rglru_proj":
+            return rglru_proj_inputs(self.B, self.L, self.D, s, h0=self.h0,
+                                     resets=self.extra.get("resets", "segments"))
         return rglru_inputs(self.B, self.L, self.D, s, h0=self.h0,
                             resets=self.extra.get("resets", "segments"))
 
@@ -162,4 +198,7 @@ WORKLOADS = {
     "rglru_4k": Workload("rglru_4k", "rglru", 8, 4096, 1024, (0,), h0=False),
     "rglru_8k": Workload("rglru_8k", "rglru", 8, 8192, 1024, (0,), h0=False),
     "rglru_16k": Workload("rglru_16k", "rglru", 8, 16384, 1024, (0,), h0=False),
+    # the RG-LRU mixer with its 16-block gate projections (the pages' mixer scope)
+    "rglru_proj_8k": Workload("rglru_proj_8k", "rglru_proj", 8, 8192, 1024, (0,), h0=False),
+    "rglru_proj_16k": Workload("rglru_proj_16k", "rglru_proj", 8, 16384, 1024, (0,), h0=False),
 }

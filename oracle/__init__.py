@@ -204,3 +204,57 @@ def rglru_backward(x, lx, la, alpha, h0, reset, dy, dhT):
                               _dptr(out["dx"]), _dptr(out["dlx"]), _dptr(out["dla"]),
                               _dptr(out["dalpha"]), _dptr(out["dh0"]))
     return out
+
+
+# ---------------------------------------------------------------------------
+# RG-LRU mixer with its two block-diagonal gate projections (SAMU GPU page,
+# section 04 forward "two canonical block-diagonal projections" and the
+# section 06 parameter table; protocol page "RG-LRU 的固定方程": 16-block
+# block-diagonal linear layers).  Plain FP64 numpy for the projections and
+# their chain rule, the C oracle above for the scan.
+# ---------------------------------------------------------------------------
+def rglru_gate_projection(x, w, b):
+    """l[..., h dk + o] = sum_i x[..., h dk + i] w[h, i, o] + b[h dk + o].
+
+    x: [..., D]; w: [H, dk, dk] with H dk = D; b: [D].  FP64."""
+    x, w, b = _f64(x), _f64(w), _f64(b)
+    H, dk, _ = w.shape
+    xf = x.reshape(-1, H, dk)
+    out = np.empty(xf.shape)
+    for h in range(H):                       # one matrix product per diagonal block
+        out[:, h, :] = xf[:, h, :] @ w[h]
+    return out.reshape(x.shape) + b
+
+
+def rglru_proj_forward(x, w_x, b_x, w_a, b_a, alpha, h0, reset):
+    """RG-LRU forward on the projected logits.  Returns dict(y, hT, lx, la)."""
+    lx = rglru_gate_projection(x, w_x, b_x)
+    la = rglru_gate_projection(x, w_a, b_a)
+    out = rglru_forward(x, lx, la, alpha, h0, reset)
+    out["lx"], out["la"] = lx, la
+    return out
+
+
+def rglru_proj_backward(x, w_x, b_x, w_a, b_a, alpha, h0, reset, dy, dhT):
+    """Backward of rglru_proj_forward: the scan's own gradients (dx through the
+    write term, dl^x, dl^a, dalpha, dh0) and the chain rule through the two
+    projections: dx += dl W^T per block, dW[h] = sum_{b,t} x_h^T dl_h,
+    db = sum_{b,t} dl.  Returns dict(dx, dw_x, db_x, dw_a, db_a, dalpha, dh0)."""
+    x = _f64(x)
+    lx = rglru_gate_projection(x, w_x, b_x)
+    la = rglru_gate_projection(x, w_a, b_a)
+    g = rglru_backward(x, lx, la, alpha, h0, reset, dy, dhT)
+    w_x, w_a = _f64(w_x), _f64(w_a)
+    H, dk, _ = w_x.shape
+    xf, gx, ga = x.reshape(-1, H, dk), g["dlx"].reshape(-1, H, dk), g["dla"].reshape(-1, H, dk)
+    dxp = np.empty(xf.shape)
+    dw_x, dw_a = np.empty(w_x.shape), np.empty(w_a.shape)
+    for h in range(H):                       # per diagonal block: dx += dl W^T, dW = x^T dl
+        dxp[:, h, :] = gx[:, h, :] @ w_x[h].T + ga[:, h, :] @ w_a[h].T
+        dw_x[h] = xf[:, h, :].T @ gx[:, h, :]
+        dw_a[h] = xf[:, h, :].T @ ga[:, h, :]
+    lead = tuple(range(x.ndim - 1))
+    return {"dx": g["dx"] + dxp.reshape(x.shape),
+            "dw_x": dw_x, "db_x": g["dlx"].sum(axis=lead),
+            "dw_a": dw_a, "db_a": g["dla"].sum(axis=lead),
+            "dalpha": g["dalpha"], "dh0": g["dh0"]}

@@ -177,3 +177,50 @@ def check_rglru(inp, fwd, bwd, ref_f, ref_b, grad_fp32=True, label=""):
     assert err["dh0"] <= TOL_GRAD, msg
     assert err["dalpha"] <= TOL_PARAM, msg
     return err
+
+
+# ---------------------------------------------------------------------------
+# RG-LRU with its block-diagonal gate projections
+# ---------------------------------------------------------------------------
+def run_rglru_proj_oracle(inp):
+    f64 = synth.bf16_bits_to_f64
+    x, dy, w_x, w_a = f64(inp["x"]), f64(inp["dy"]), f64(inp["w_x"]), f64(inp["w_a"])
+    args = (x, w_x, inp["b_x"], w_a, inp["b_a"], inp["alpha"], inp["h0"], inp["reset"])
+    return oracle.rglru_proj_forward(*args), oracle.rglru_proj_backward(*args, dy, inp["dhT"])
+
+
+def run_rglru_proj_gpu(inp, device, grad_fp32=True):
+    import torch
+    from linear_recurrence_sequence_gb300 import api
+    t = api.rglru_proj_tensors_from_numpy(inp, device)
+    p = (t["x"], t["w_x"], t["b_x"], t["w_a"], t["b_a"], t["alpha"], t["h0"], t["reset"])
+    fwd = api.rglru_proj_forward(*p, want_y32=True)
+    bwd = api.rglru_proj_backward(t["dy"], t["dhT"], *p, fwd["saved"], grad_fp32=grad_fp32)
+    torch.cuda.synchronize(device)
+    assert api.device_status(bwd["scratch"]) == 0
+    return fwd, bwd
+
+
+def check_rglru_proj(inp, fwd, bwd, ref_f, ref_b, grad_fp32=True, label=""):
+    err = {}
+    err["y32"] = rel_l2(fwd["y32"].cpu().numpy(), ref_f["y"])
+    err["hT"] = rel_l2(fwd["hT"].cpu().numpy(), ref_f["hT"])
+    scale = np.broadcast_to(np.sqrt(np.mean(ref_f["y"] ** 2, axis=1, keepdims=True)), ref_f["y"].shape)
+    mx, n_bad, n_bad_big = bf16_ulp_report(torch_bits(fwd["y"]), ref_f["y"], scale)
+    err["y_ulp_max"], err["y_ulp_gt1"], err["y_ulp_gt1_above_floor"] = mx, n_bad, n_bad_big
+    err["dx"] = rel_l2(bwd["dx"].float().cpu().numpy(), ref_b["dx"])
+    for k in ("dh0",):
+        err[k] = rel_l2(bwd[k].cpu().numpy(), ref_b[k])
+    for k in ("dw_x", "db_x", "dw_a", "db_a", "dalpha"):
+        err[k] = rel_l2(bwd[k].cpu().numpy(), ref_b[k])
+    msg = f"{label} errors: " + ", ".join(f"{k}={v:.3g}" if isinstance(v, float) else f"{k}={v}"
+                                          for k, v in err.items())
+    print(msg)
+    assert err["y32"] <= TOL_OUT, msg
+    assert err["hT"] <= TOL_OUT, msg
+    assert err["y_ulp_gt1_above_floor"] == 0, msg
+    assert err["dx"] <= (TOL_GRAD if grad_fp32 else TOL_BF16_GRAD), msg
+    assert err["dh0"] <= TOL_GRAD, msg
+    for k in ("dw_x", "db_x", "dw_a", "db_a", "dalpha"):
+        assert err[k] <= TOL_PARAM, msg
+    return err

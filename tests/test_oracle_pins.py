@@ -570,3 +570,81 @@ def test_chunk_closed_form_phase_needs_more_than_fp32():
     once = np.complex64(lbarK) * np.exp(1j * d.sum())
     assert abs(fp32_phase - exact)[0] / abs(exact)[0] > 5e-6
     assert abs(once - exact)[0] / abs(exact)[0] < 2e-7
+
+
+# ---------------------------------------------------------------------------
+# RG-LRU block-diagonal gate projections (SAMU GPU page, sections 04 and 06;
+# protocol page "RG-LRU 的固定方程")
+# ---------------------------------------------------------------------------
+
+def _proj_rand(B, L, D, seed, reset_p=0.0):
+    r = rng0(seed)
+    H, dk = 16, D // 16
+    return dict(
+        x=r.standard_normal((B, L, D)),
+        w_x=r.standard_normal((H, dk, dk)) / math.sqrt(dk),
+        b_x=0.1 * r.standard_normal(D),
+        w_a=r.standard_normal((H, dk, dk)) / math.sqrt(dk),
+        b_a=0.1 * r.standard_normal(D),
+        alpha=np.log(np.expm1(-np.log(r.uniform(0.9, 0.999, D)) / 8.0)),
+        h0=0.1 * r.standard_normal((B, D)),
+        reset=(r.random((B, L)) < reset_p).astype(np.uint8) if reset_p > 0 else None,
+    )
+
+
+def test_gate_projection_is_a_dense_block_diagonal_product():
+    """The projection equals x times the dense [D, D] matrix assembled by
+    scipy's block_diag from the 16 blocks, plus the bias (an independent
+    construction: no per-block indexing)."""
+    from scipy.linalg import block_diag
+    inp = _proj_rand(2, 7, 48, seed=60)
+    dense = block_diag(*inp["w_x"])
+    want = inp["x"] @ dense + inp["b_x"]
+    np.testing.assert_allclose(oracle.rglru_gate_projection(inp["x"], inp["w_x"], inp["b_x"]), want,
+                               rtol=1e-13, atol=1e-13)
+    # block 0's outputs (channels 0..2) depend on its inputs 0..2 only
+    base = oracle.rglru_gate_projection(inp["x"], inp["w_x"], inp["b_x"])
+    pert2 = inp["x"].copy()
+    pert2[..., 3:] = 0.0
+    only0 = oracle.rglru_gate_projection(pert2, inp["w_x"], inp["b_x"])
+    np.testing.assert_allclose(only0[..., :3], base[..., :3], rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("D,count", [(1024, 134_144), (2048, 530_432), (2560, 826_880)])
+def test_rglru_mixer_parameter_count_matches_pages_table(D, count):
+    """Two 16-block diagonal projections, two biases and alpha: the pages'
+    RG-LRU mixer parameter counts (SAMU GPU page, section 06 table)."""
+    from linear_recurrence_sequence_gb300 import synth
+    dk = D // synth.PROJ_BLOCKS
+    shapes = {"w_x": (16, dk, dk), "w_a": (16, dk, dk), "b_x": (D,), "b_a": (D,), "alpha": (D,)}
+    assert sum(int(np.prod(s)) for s in shapes.values()) == count
+    inp = synth.rglru_proj_inputs(1, 2, D, 0)
+    for k, s in shapes.items():
+        assert inp[k].shape == s, k
+
+
+def _proj_loss(inp, G, GT):
+    out = oracle.rglru_proj_forward(**inp)
+    return float(np.sum(out["y"] * G) + np.sum(out["hT"] * GT))
+
+
+@pytest.mark.parametrize("seed,reset_p", [(61, 0.0), (62, 0.15)])
+def test_rglru_proj_backward_matches_finite_differences(seed, reset_p):
+    B, L, D = 2, 13, 32
+    inp = _proj_rand(B, L, D, seed=seed, reset_p=reset_p)
+    r = rng0(seed + 100)
+    G = r.standard_normal((B, L, D))
+    GT = r.standard_normal((B, D))
+    g = oracle.rglru_proj_backward(**inp, dy=G, dhT=GT)
+    names = {"x": "dx", "w_x": "dw_x", "b_x": "db_x", "w_a": "dw_a", "b_a": "db_a", "alpha": "dalpha", "h0": "dh0"}
+    eps = 1e-6
+    for key, gname in names.items():
+        for trial in range(2):
+            v = r.standard_normal(inp[key].shape)
+            plus = dict(inp)
+            minus = dict(inp)
+            plus[key] = inp[key] + eps * v
+            minus[key] = inp[key] - eps * v
+            fd = (_proj_loss(plus, G, GT) - _proj_loss(minus, G, GT)) / (2 * eps)
+            an = float(np.sum(g[gname] * v))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (key, fd, an)

@@ -91,8 +91,8 @@ int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
  * 7 RG-LRU scan forward, 8 RG-LRU scan backward, 9 RG-LRU alpha reduction,
  * 10 SAMU forward maps, 11 SAMU backward maps, 12 SAMU decode prepare,
  * 13 SAMU decode step, 14 RG-LRU gate-projection GEMMs, 15 RG-LRU projection
- * backward GEMMs, 16 FP32-to-BF16 conversion; 9 also covers the bias-gradient
- * reductions) and duration in milliseconds; *count receives the number of
+ * backward GEMMs, 16 RG-LRU weight packing and dW combination; 9 also covers
+ * the bias-gradient reductions) and duration in milliseconds; *count receives the number of
  * kernels launched while profiling was on.  Not thread-safe: one profiling
  * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),
  * LRS_ERR_CUDA. */
@@ -289,8 +289,9 @@ int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const v
 /* Backward of rglru_proj_forward: the scan backward with the logits
  * recomputed, then dx = dx_scan + dlx W_x^T + dla W_a^T per block,
  * dW_x = x^T dlx, dW_a = x^T dla, db = sum over tokens of dl.  The gate
- * gradients enter the products as BF16 leading parts plus BF16 remainders
- * (16 significant bits); the bias and alpha gradients are fixed-order sums.
+ * gradients and dx_scan enter the two GEMMs (one for dx with K = 6 D/16, one
+ * for dW with K = B L) as BF16 leading parts plus BF16 remainders (16
+ * significant bits); the bias and alpha gradients are fixed-order sums.
  *
  *   dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, B, L, D, saved: as above
  *   dx          [B,L,D] BF16 or FP32 by grad_dtype (out)

@@ -78,7 +78,7 @@ enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
     KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
     KID_SAMU_BWD_MAPS, KID_SAMU_DECODE_PREP, KID_SAMU_DECODE_STEP, KID_RGLRU_PROJ_FWD, KID_RGLRU_PROJ_BWD,
-    KID_RGLRU_TO_BF16
+    KID_RGLRU_PROJ_PACK
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -129,26 +129,6 @@ cudaError_t gemm_xw(const Gemm& gm, const void* in, const void* w, float* out, f
     return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
 }
 
-// out[t][h dk + i] += sum_o g[t][h dk + o] W[h][i][o]   (dx += dl W^T)
-cudaError_t gemm_gwt(const Gemm& gm, const void* g, const void* w, float* out) {
-    const float one = 1.0f;
-    const cublasStatus_t st = cublasGemmStridedBatchedEx(
-        gm.h, CUBLAS_OP_T, CUBLAS_OP_N, gm.dk, gm.rows, gm.dk, &one, w, CUDA_R_16BF, gm.dk,
-        (long long)gm.dk * gm.dk, g, CUDA_R_16BF, gm.D, gm.dk, &one, out, CUDA_R_32F, gm.D, gm.dk, kProjBlocks,
-        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-}
-
-// dW[h][i][o] (+)= sum_t x[t][h dk + i] g[t][h dk + o]   (dW = x^T dl)
-cudaError_t gemm_xtg(const Gemm& gm, const void* x, const void* g, float* dw, float beta) {
-    const float one = 1.0f;
-    const cublasStatus_t st = cublasGemmStridedBatchedEx(
-        gm.h, CUBLAS_OP_N, CUBLAS_OP_T, gm.dk, gm.dk, gm.rows, &one, g, CUDA_R_16BF, gm.D, gm.dk, x, CUDA_R_16BF,
-        gm.D, gm.dk, &beta, dw, CUDA_R_32F, gm.dk, (long long)gm.dk * gm.dk, kProjBlocks, CUBLAS_COMPUTE_32F,
-        CUBLAS_GEMM_DEFAULT);
-    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-}
-
 // Both gates' products x W_x, x W_a (FP32, biases excluded) into scratch.
 cudaError_t proj_forward_gemms(int rows, int D, const void* x, const void* w_x, const void* w_a, float* lx, float* la,
                                void* ws, cudaStream_t s) {
@@ -159,21 +139,27 @@ cudaError_t proj_forward_gemms(int rows, int D, const void* x, const void* w_x, 
     return e;
 }
 
-// dx32 += (hi + lo)(dl^x) W_x^T + (hi + lo)(dl^a) W_a^T; dW = x^T (hi + lo).
-cudaError_t proj_backward_gemms(int rows, int D, const void* x, const void* w_x, const void* w_a, const void* gx_hi,
-                                const void* gx_lo, const void* ga_hi, const void* ga_lo, float* dx32, float* dw_x,
-                                float* dw_a, void* ws, cudaStream_t s) {
+// The backward products from the six gradient parts G [rows][16][6][dk]
+// (dl^x hi, lo; dl^a hi, lo; dx-through-the-write-term hi, lo):
+//   dx[t][h dk + i] = sum_k Wcat[h](i, k) G[t][h][k]   (K = 6 dk, one GEMM, the
+//                     write-term parts through identity blocks; BF16 or FP32 out)
+//   Gx[h](k, i)     = sum_t G[t][h][k] x[t][h dk + i]  (k < 4 dk, K = rows)
+cudaError_t proj_backward_gemms(int rows, int D, const void* x, const void* gparts, const void* wcat, void* dx,
+                                bool dx_fp32, float* dwcat, void* ws, cudaStream_t s) {
     Gemm gm;
     cudaError_t e = gemm_begin(gm, rows, D, ws, s);
-    if (e == cudaSuccess) e = gemm_gwt(gm, gx_hi, w_x, dx32);
-    if (e == cudaSuccess) e = gemm_gwt(gm, gx_lo, w_x, dx32);
-    if (e == cudaSuccess) e = gemm_gwt(gm, ga_hi, w_a, dx32);
-    if (e == cudaSuccess) e = gemm_gwt(gm, ga_lo, w_a, dx32);
-    if (e == cudaSuccess) e = gemm_xtg(gm, x, gx_hi, dw_x, 0.0f);
-    if (e == cudaSuccess) e = gemm_xtg(gm, x, gx_lo, dw_x, 1.0f);
-    if (e == cudaSuccess) e = gemm_xtg(gm, x, ga_hi, dw_a, 0.0f);
-    if (e == cudaSuccess) e = gemm_xtg(gm, x, ga_lo, dw_a, 1.0f);
-    return e;
+    if (e != cudaSuccess) return e;
+    const int dk = gm.dk;
+    const float one = 1.0f, zero = 0.0f;
+    cublasStatus_t st = cublasGemmStridedBatchedEx(
+        gm.h, CUBLAS_OP_N, CUBLAS_OP_N, dk, rows, 6 * dk, &one, wcat, CUDA_R_16BF, dk, (long long)6 * dk * dk,
+        gparts, CUDA_R_16BF, 6 * D, 6 * dk, &zero, dx, dx_fp32 ? CUDA_R_32F : CUDA_R_16BF, D, dk, kProjBlocks,
+        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    if (st != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    st = cublasGemmStridedBatchedEx(gm.h, CUBLAS_OP_N, CUBLAS_OP_T, 4 * dk, dk, rows, &one, gparts, CUDA_R_16BF,
+                                    6 * D, 6 * dk, x, CUDA_R_16BF, D, dk, &zero, dwcat, CUDA_R_32F, 4 * dk,
+                                    (long long)4 * dk * dk, kProjBlocks, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
 }
 
 int check_rglru_proj_shape(int B, int L, int D) {
@@ -643,8 +629,8 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     float* lx = at<float>(scratch, ps.lx);
     float* la = at<float>(scratch, ps.la);
     const bool fp32 = grad_dtype == LRS_GRAD_FP32;
-    float* dx32 = fp32 ? static_cast<float*>(dx) : at<float>(scratch, ps.dx32);
     void* ws = at<void>(scratch, ps.gemm_ws);
+    const int dk = D / kProjBlocks;
     if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream, proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, ws, stream));
     CUtensorMap tm_dy, tm_x, tm_lx, tm_la;
@@ -659,11 +645,11 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     a.reset = reset;
     a.dhT = dhT;
     a.hsub = at<float>(saved, sv.hsub);
-    a.dx = dx32;
-    a.dlx = at<void>(scratch, ps.dlx_hi);
-    a.dla = at<void>(scratch, ps.dla_hi);
-    a.dlx_lo = at<uint32_t>(scratch, ps.dlx_lo);
-    a.dla_lo = at<uint32_t>(scratch, ps.dla_lo);
+    a.dx = nullptr;
+    a.dlx = nullptr;
+    a.dla = nullptr;
+    a.gparts = at<uint32_t>(scratch, ps.gparts);
+    a.dk = dk;
     a.bxpart = at<float>(scratch, ps.bxpart);
     a.bapart = at<float>(scratch, ps.bapart);
     a.grad_fp32 = 1;
@@ -679,11 +665,12 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.apart, apart2, dalpha, B * g.CT, D, stream));
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bxpart, apart2, db_x, B * g.CT, D, stream));
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bapart, apart2, db_a, B * g.CT, D, stream));
+    void* wcat = at<void>(scratch, ps.wcat);
+    float* dwcat = at<float>(scratch, ps.dwcat);
+    LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream, launch_rglru_proj_pack(w_x, w_a, wcat, dk, stream));
     LRS_LAUNCH(KID_RGLRU_PROJ_BWD, stream,
-               proj_backward_gemms(B * L, D, x, w_x, w_a, a.dlx, a.dlx_lo, a.dla, a.dla_lo, dx32, dw_x, dw_a, ws,
-                                   stream));
-    if (!fp32)
-        LRS_LAUNCH(KID_RGLRU_TO_BF16, stream, launch_rglru_to_bf16(dx32, dx, (size_t)B * L * D, stream));
+               proj_backward_gemms(B * L, D, x, a.gparts, wcat, dx, fp32, dwcat, ws, stream));
+    LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream, launch_rglru_proj_dw(dwcat, dw_x, dw_a, dk, stream));
     return LRS_OK;
 }
 

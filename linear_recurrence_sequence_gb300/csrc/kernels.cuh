@@ -403,10 +403,11 @@ struct RglruScanFwdArgs {
     uint32_t* status;
 };
 
-// PL variant: dx is FP32; dlx / dla receive the BF16 pairs of the leading
-// BF16 part of the gate gradients and dlx_lo / dla_lo those of the
-// remainder (dl = hi + lo to 16 significant bits); bxpart / bapart the
-// per-tile sums of the gate gradients (the bias gradients' partials).
+// PL variant: the token's gradients go to gparts [B*L][16][6][dk] BF16 as
+// leading BF16 parts and BF16 remainders (v = hi + lo to 16 significant
+// bits): parts 0/1 dl^x, 2/3 dl^a, 4/5 dx through the write term; bxpart /
+// bapart receive the per-tile sums of the gate gradients (the bias
+// gradients' partials).
 struct RglruScanBwdArgs {
     ScanGeom g;
     const float* alpha;
@@ -418,8 +419,8 @@ struct RglruScanBwdArgs {
     void* dx;
     void* dlx;
     void* dla;
-    uint32_t* dlx_lo;
-    uint32_t* dla_lo;
+    uint32_t* gparts;       // PL only
+    int dk;                 // PL only: D / 16
     float* bxpart;          // [B*CT][D]
     float* bapart;
     int grad_fp32;
@@ -439,7 +440,10 @@ cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& t
                                   bool projected = false);
 cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,
                                cudaStream_t s);
-// n FP32 values (n even) to BF16, round to nearest even.
-cudaError_t launch_rglru_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
+// Packed backward weights [16][6 dk][dk] (column-major dk x 6dk per block:
+// W_x, W_x, W_a, W_a transposed into (o, i), then two identity blocks) and
+// the combination dW_x = P0 + P1, dW_a = P2 + P3 of the [16][dk][4 dk] GEMM output.
+cudaError_t launch_rglru_proj_pack(const void* w_x, const void* w_a, void* wcat, int dk, cudaStream_t s);
+cudaError_t launch_rglru_proj_dw(const float* dwcat, float* dw_x, float* dw_a, int dk, cudaStream_t s);
 
 }  // namespace lrs

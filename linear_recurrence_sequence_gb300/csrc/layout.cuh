@@ -211,15 +211,15 @@ inline RglruScratch rglru_scratch_layout(int B, int L, int D) {
 }
 
 // RG-LRU with the block-diagonal gate projections: the scan's scratch, then
-// the FP32 products x W of both gates, the BF16 leading parts and remainders
-// of both gate gradients, an FP32 dx, the bias-gradient partials and the
-// GEMM library's workspace.
+// the FP32 products x W of both gates, the six BF16 gradient parts per token
+// and block ([B*L][16][6][dk]), the packed backward weights, the dW product,
+// the bias-gradient partials and the GEMM library's workspace.
 constexpr int kProjBlocks = 16;                      // diagonal blocks of each gate projection
 constexpr size_t kGemmWorkspace = 32u << 20;
 
 struct RglruProjScratch {
     RglruScratch scan;
-    size_t lx, la, dlx_hi, dlx_lo, dla_hi, dla_lo, dx32, bxpart, bapart, gemm_ws, total;
+    size_t lx, la, gparts, wcat, dwcat, bxpart, bapart, gemm_ws, total;
 };
 
 inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
@@ -230,11 +230,10 @@ inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
     size_t o = s.scan.total;
     s.lx = o;      o = align_up(o + bld * 4);
     s.la = o;      o = align_up(o + bld * 4);
-    s.dlx_hi = o;  o = align_up(o + bld * 2);
-    s.dlx_lo = o;  o = align_up(o + bld * 2);
-    s.dla_hi = o;  o = align_up(o + bld * 2);
-    s.dla_lo = o;  o = align_up(o + bld * 2);
-    s.dx32 = o;    o = align_up(o + bld * 4);
+    const size_t dk = (size_t)D / kProjBlocks;
+    s.gparts = o;  o = align_up(o + bld * 6 * 2);
+    s.wcat = o;    o = align_up(o + (size_t)kProjBlocks * 6 * dk * dk * 2);
+    s.dwcat = o;   o = align_up(o + (size_t)kProjBlocks * 4 * dk * dk * 4);
     s.bxpart = o;  o = align_up(o + (size_t)B * g.CT * D * 4);
     s.bapart = o;  o = align_up(o + (size_t)B * g.CT * D * 4);
     s.gemm_ws = o; o = align_up(o + kGemmWorkspace);

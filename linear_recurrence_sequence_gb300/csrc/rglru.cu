@@ -551,15 +551,20 @@ __global__ void __launch_bounds__(kRgThreads, 2)
                 bs.w += dla1;
             }
             if (PL && active) {
-                const size_t o = row + (size_t)i * (D / 2);
-                *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.dx) + 2 * o) = make_float2(dx0, dx1);
+                // token t, channels d, d+1 of block h at offset ob: parts p at gp + p * dk / 2
+                uint32_t* gp = a.gparts + ((((size_t)b * L + t0 + r0 + i) * D) * 6 + (size_t)(d / a.dk) * 6 * a.dk +
+                                           d % a.dk) / 2;
+                const int ps = a.dk / 2;
                 uint32_t hi, lo;
                 split_bf2(dlx0, dlx1, hi, lo);
-                __stcs(reinterpret_cast<uint32_t*>(a.dlx) + o, hi);
-                __stcs(a.dlx_lo + o, lo);
+                __stcs(gp, hi);
+                __stcs(gp + ps, lo);
                 split_bf2(dla0, dla1, hi, lo);
-                __stcs(reinterpret_cast<uint32_t*>(a.dla) + o, hi);
-                __stcs(a.dla_lo + o, lo);
+                __stcs(gp + 2 * ps, hi);
+                __stcs(gp + 3 * ps, lo);
+                split_bf2(dx0, dx1, hi, lo);
+                __stcs(gp + 4 * ps, hi);
+                __stcs(gp + 5 * ps, lo);
             } else if (active) {
                 const size_t o = row + (size_t)i * (D / 2);
                 if (a.grad_fp32) {
@@ -636,25 +641,56 @@ __global__ void __launch_bounds__(256) rglru_alpha_stage2_kernel(const float* __
     dalpha[d] = s;
 }
 
-// FP32 pairs to BF16 pairs (round to nearest even), grid-strided.
-__global__ void __launch_bounds__(256) rglru_to_bf16_kernel(const float2* __restrict__ src,
-                                                            uint32_t* __restrict__ dst, size_t n_pairs) {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_pairs; i += (size_t)gridDim.x * blockDim.x) {
-        const float2 v = __ldcs(src + i);
-        __stcs(dst + i, f2_to_bf2(v.x, v.y));
+// Packed backward weights: block h is the column-major [dk x 6 dk] matrix
+// A(i, p dk + o) = W_x[h][i][o] (p = 0, 1), W_a[h][i][o] (p = 2, 3), [i == o]
+// (p = 4, 5), so that dx = A . (parts of the token's gradients).
+__global__ void __launch_bounds__(256) rglru_proj_pack_kernel(const uint16_t* __restrict__ w_x,
+                                                              const uint16_t* __restrict__ w_a,
+                                                              uint16_t* __restrict__ wcat, int dk) {
+    const size_t n = (size_t)16 * 6 * dk * dk;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+        const int i = (int)(e % dk);
+        const size_t k = e / dk % ((size_t)6 * dk);
+        const int h = (int)(e / ((size_t)6 * dk * dk));
+        const int p = (int)(k / dk), o = (int)(k % dk);
+        const size_t wi = ((size_t)h * dk + i) * dk + o;
+        uint16_t v;
+        if (p < 2)
+            v = w_x[wi];
+        else if (p < 4)
+            v = w_a[wi];
+        else
+            v = i == o ? (uint16_t)0x3F80u : (uint16_t)0;   // BF16 1.0 and 0.0
+        wcat[e] = v;
     }
 }
 
-cudaError_t launch_rglru_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s) {
-    int dev = 0, sms = 1;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-    const size_t pairs = n / 2;
-    size_t blocks = (pairs + 255) / 256;
-    if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
-    if (blocks < 1) blocks = 1;
-    rglru_to_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float2*>(src),
-                                                          static_cast<uint32_t*>(dst), pairs);
+// dW_x[h][i][o] = G(o, i) + G(dk + o, i), dW_a from rows 2 dk, 3 dk, where G is
+// block h's column-major [4 dk x dk] product of the gradient parts with x.
+__global__ void __launch_bounds__(256) rglru_proj_dw_kernel(const float* __restrict__ g, float* __restrict__ dw_x,
+                                                            float* __restrict__ dw_a, int dk) {
+    const size_t n = (size_t)16 * dk * dk;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+        const int o = (int)(e % dk);
+        const int i = (int)(e / dk % dk);
+        const size_t h = e / ((size_t)dk * dk);
+        const float* gb = g + h * 4 * dk * dk + (size_t)i * 4 * dk;
+        dw_x[e] = gb[o] + gb[dk + o];
+        dw_a[e] = gb[2 * dk + o] + gb[3 * dk + o];
+    }
+}
+
+cudaError_t launch_rglru_proj_pack(const void* w_x, const void* w_a, void* wcat, int dk, cudaStream_t s) {
+    const size_t n = (size_t)16 * 6 * dk * dk;
+    rglru_proj_pack_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(
+        static_cast<const uint16_t*>(w_x), static_cast<const uint16_t*>(w_a), static_cast<uint16_t*>(wcat), dk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rglru_proj_dw(const float* dwcat, float* dw_x, float* dw_a, int dk, cudaStream_t s) {
+    const size_t n = (size_t)16 * dk * dk;
+    rglru_proj_dw_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(dwcat, dw_x,
+                                                                                                      dw_a, dk);
     return cudaGetLastError();
 }
 

@@ -501,7 +501,7 @@ int rglru_forward(const void* x, const void* lx, const void* la, const float* al
     if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_bf16_map(&tm_lx, lx, B, L, D, kRgTile) ||
         !make_bf16_map(&tm_la, la, B, L, D, kRgTile))
         return LRS_ERR_CUDA;
-    RglruScanFwdArgs a;
+    RglruScanFwdArgs a{};
     a.g = make_geom(B, L, D, kRgTile);
     a.alpha = alpha;
     a.reset = reset;
@@ -539,7 +539,7 @@ int rglru_backward(const void* dy, const float* dhT, const void* x, const void* 
     if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile) || !make_bf16_map(&tm_x, x, B, L, D, kRgTile) ||
         !make_bf16_map(&tm_lx, lx, B, L, D, kRgTile) || !make_bf16_map(&tm_la, la, B, L, D, kRgTile))
         return LRS_ERR_CUDA;
-    RglruScanBwdArgs a;
+    RglruScanBwdArgs a{};
     a.g = g;
     a.alpha = alpha;
     a.reset = reset;
@@ -583,18 +583,29 @@ int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const v
     const RglruScratch& sc = ps.scan;
     float* lx = at<float>(scratch, ps.lx);
     float* la = at<float>(scratch, ps.la);
+    // in-kernel logits on the tensor cores when the diagonal blocks tile the
+    // 64-channel groups (D/16 divides 64); otherwise the GEMM path
+    const bool fused = 64 % (D / kProjBlocks) == 0;
     if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
-    LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
-               proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, at<void>(scratch, ps.gemm_ws), stream));
     CUtensorMap tm_x, tm_lx, tm_la;
-    if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) ||
-        !make_f32_map(&tm_la, la, B, L, D, kRgTile))
-        return LRS_ERR_CUDA;
-    RglruScanFwdArgs a;
+    if (fused) {
+        LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream, launch_rglru_proj_wimg(w_x, w_a, at<void>(scratch, ps.wimg), D, stream));
+        if (!make_bf16_map_sw128(&tm_x, x, B, L, D, kRgTile)) return LRS_ERR_CUDA;
+        tm_lx = tm_x;
+        tm_la = tm_x;
+    } else {
+        LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
+                   proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, at<void>(scratch, ps.gemm_ws), stream));
+        if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) ||
+            !make_f32_map(&tm_la, la, B, L, D, kRgTile))
+            return LRS_ERR_CUDA;
+    }
+    RglruScanFwdArgs a{};
     a.g = make_geom(B, L, D, kRgTile);
     a.alpha = alpha;
     a.bx = b_x;
     a.ba = b_a;
+    a.wimg = at<uint8_t>(scratch, ps.wimg);
     a.reset = reset;
     a.h0 = h0;
     a.y = static_cast<uint32_t*>(y);
@@ -605,7 +616,7 @@ int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const v
     a.flags = at<uint32_t>(scratch, sc.flags);
     a.counter = at<uint32_t>(scratch, sc.status + 4);
     a.status = at<uint32_t>(scratch, sc.status);
-    LRS_LAUNCH(KID_RGLRU_SCAN_FWD, stream, launch_rglru_scan_fwd(tm_x, tm_lx, tm_la, a, stream, true));
+    LRS_LAUNCH(KID_RGLRU_SCAN_FWD, stream, launch_rglru_scan_fwd(tm_x, tm_lx, tm_la, a, stream, fused ? 2 : 1));
     return LRS_OK;
 }
 
@@ -637,7 +648,7 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile) || !make_bf16_map(&tm_x, x, B, L, D, kRgTile) ||
         !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) || !make_f32_map(&tm_la, la, B, L, D, kRgTile))
         return LRS_ERR_CUDA;
-    RglruScanBwdArgs a;
+    RglruScanBwdArgs a{};
     a.g = g;
     a.alpha = alpha;
     a.bx = b_x;

@@ -391,6 +391,7 @@ struct RglruScanFwdArgs {
     const float* alpha;
     const float* bx;        // [D], PL only
     const float* ba;
+    const uint8_t* wimg;    // logits mode 2: the groups' weight images
     const uint8_t* reset;
     const float* h0;        // [B,D] or null
     uint32_t* y;
@@ -433,8 +434,15 @@ struct RglruScanBwdArgs {
     uint32_t* status;
 };
 
+// logits: 0 raw BF16 l^x, l^a; 1 FP32 products x W (+ biases); 2 products
+// formed in the kernel on the tensor cores from args.wimg (+ biases); for 2,
+// tm_x must be the 128-byte-swizzled map of x and tm_lx, tm_la are unused.
 cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
-                                  const RglruScanFwdArgs& args, cudaStream_t s, bool projected = false);
+                                  const RglruScanFwdArgs& args, cudaStream_t s, int logits = 0);
+// The groups' weight images for logits mode 2: per 64-channel group and gate the
+// [64 outputs][64 inputs] BF16 matrix (zero outside the diagonal blocks;
+// dk = D/16 must divide 64) in the K-major 128-byte-swizzled layout.
+cudaError_t launch_rglru_proj_wimg(const void* w_x, const void* w_a, void* wimg, int D, cudaStream_t s);
 cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
                                   const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s,
                                   bool projected = false);

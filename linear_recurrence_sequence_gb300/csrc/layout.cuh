@@ -219,7 +219,7 @@ constexpr size_t kGemmWorkspace = 32u << 20;
 
 struct RglruProjScratch {
     RglruScratch scan;
-    size_t lx, la, gparts, wcat, dwcat, bxpart, bapart, gemm_ws, total;
+    size_t lx, la, gparts, wcat, dwcat, wimg, bxpart, bapart, gemm_ws, total;
 };
 
 inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
@@ -234,6 +234,7 @@ inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
     s.gparts = o;  o = align_up(o + bld * 6 * 2);
     s.wcat = o;    o = align_up(o + (size_t)kProjBlocks * 6 * dk * dk * 2);
     s.dwcat = o;   o = align_up(o + (size_t)kProjBlocks * 4 * dk * dk * 4);
+    s.wimg = o;    o = align_up(o + (size_t)(D / 64) * 2 * 64 * 64 * 2);   // in-kernel logits: weight images
     s.bxpart = o;  o = align_up(o + (size_t)B * g.CT * D * 4);
     s.bapart = o;  o = align_up(o + (size_t)B * g.CT * D * 4);
     s.gemm_ws = o; o = align_up(o + kGemmWorkspace);

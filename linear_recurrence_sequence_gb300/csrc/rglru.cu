@@ -16,28 +16,48 @@
 // 16-token sub-chunks, lane l owns channels 2l, 2l+1, decoupled look-back
 // between tiles.
 #include "kernels.cuh"
+#include "umma.cuh"
 
 namespace lrs {
 
 constexpr int kRgThreads = kRgWarps * 32;
 constexpr int kRgBoxBytes = kRgTile * kRowBytes;   // one BF16 [128 x 64] box
 
-// Gate-logit boxes: BF16 [128 x 64] (raw l^x, l^a inputs) or, with projected
-// gates (PL), FP32 [128 x 64] products x W whose biases are added on reading.
-template <bool PL>
+// Where the gate logits come from (the kernels' LM parameter):
+//   0  BF16 [128 x 64] boxes of the raw l^x, l^a inputs;
+//   1  FP32 [128 x 64] boxes of the products x W (cuBLAS), biases added on reading;
+//   2  computed in the kernel on the tensor cores (forward): the tile's x box
+//      (TMA, 128-byte swizzle) times the group's packed weights (both gates),
+//      FP32 accumulators in tensor memory, staged to shared memory as
+//      [128 tokens][kStageRow] FP32 per gate; biases added on reading.
+constexpr int kStageRow = 68;                              // padded row: conflict-free staging stores
+constexpr int kStageBytes = 2 * kRgTile * kStageRow * 4;   // both gates
+constexpr int kWimgBytes = 2 * kGroup * kGroup * 2;        // both gates' [64 x 64] BF16 weight images
+
+template <int LM>
 struct RgLogits {
-    static constexpr int kBoxBytes = PL ? 2 * kRgBoxBytes : kRgBoxBytes;
-    static constexpr int kSlotBytes = kRgBoxBytes + 2 * kBoxBytes;   // x, l^x, l^a
+    static constexpr int kBoxBytes = LM == 2 ? 0 : (LM == 1 ? 2 * kRgBoxBytes : kRgBoxBytes);
+    static constexpr int kSlotBytes = LM == 2 ? kRgBoxBytes + kWimgBytes : kRgBoxBytes + 2 * kBoxBytes;
 };
 
-// The lane's two logits of token row r (bias added for PL).
-template <bool PL>
+// The lane's two logits of token row r (biases added for LM >= 1).
+template <int LM>
 __device__ __forceinline__ float2 rg_logit(const uint8_t* box, int r, int lane, float2 bias) {
-    if (PL) {
-        const float2 v = reinterpret_cast<const float2*>(box)[r * 32 + lane];
+    if (LM >= 1) {
+        const float2 v = LM == 2 ? reinterpret_cast<const float2*>(box)[(r * kStageRow) / 2 + lane]
+                                 : reinterpret_cast<const float2*>(box)[r * 32 + lane];
         return make_float2(v.x + bias.x, v.y + bias.y);
     }
     return bf2_to_f2(reinterpret_cast<const uint32_t*>(box)[r * 32 + lane]);
+}
+
+// The lane's two x values of token row r (the box is 128-byte swizzled for LM 2:
+// the 16-byte chunk j of row r sits at chunk j ^ (r % 8)).
+template <int LM>
+__device__ __forceinline__ float2 rg_x(const uint8_t* box, int r, int lane) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(box);
+    if (LM == 2) return bf2_to_f2(w[r * 32 + ((((lane >> 2) ^ (r & 7))) << 2) + (lane & 3)]);
+    return bf2_to_f2(w[r * 32 + lane]);
 }
 
 struct RgGate {
@@ -95,20 +115,25 @@ __device__ __forceinline__ float softplus_f(float v) {
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-// Lane 0 of thread 0: the three boxes of `tile` into ring slot `slot`.
-template <bool PL>
+// Thread 0: the boxes of `tile` into ring slot `slot` (LM 2: the x box and
+// the group's weight images).
+template <int LM>
 __device__ __forceinline__ void rg_fwd_issue(uint8_t* slot_base, uint64_t* bar, const CUtensorMap* tm_x,
-                                             const CUtensorMap* tm_lx, const CUtensorMap* tm_la, const ScanGeom& g,
-                                             long long tile) {
-    constexpr int LB = RgLogits<PL>::kBoxBytes;
+                                             const CUtensorMap* tm_lx, const CUtensorMap* tm_la,
+                                             const uint8_t* wimg, const ScanGeom& g, long long tile) {
+    constexpr int LB = RgLogits<LM>::kBoxBytes;
     const int chain = (int)(tile % g.n_chains);
     const int c = (int)(tile / g.n_chains);
     const int b = chain / g.n_groups, grp = chain % g.n_groups;
     fence_proxy_async();
-    mbar_arrive_expect_tx(bar, RgLogits<PL>::kSlotBytes);
+    mbar_arrive_expect_tx(bar, RgLogits<LM>::kSlotBytes);
     tma_load_3d(slot_base, tm_x, grp * kGroup, c * kRgTile, b, bar);
-    tma_load_3d(slot_base + kRgBoxBytes, tm_lx, grp * kGroup, c * kRgTile, b, bar);
-    tma_load_3d(slot_base + kRgBoxBytes + LB, tm_la, grp * kGroup, c * kRgTile, b, bar);
+    if (LM == 2) {
+        bulk_load(slot_base + kRgBoxBytes, wimg + (size_t)grp * kWimgBytes, kWimgBytes, bar);
+    } else {
+        tma_load_3d(slot_base + kRgBoxBytes, tm_lx, grp * kGroup, c * kRgTile, b, bar);
+        tma_load_3d(slot_base + kRgBoxBytes + LB, tm_la, grp * kGroup, c * kRgTile, b, bar);
+    }
 }
 
 // Persistent CTAs: each takes tiles in ticket order (atomic counter) and keeps
@@ -116,17 +141,21 @@ __device__ __forceinline__ void rg_fwd_issue(uint8_t* slot_base, uint64_t* bar, 
 // while it works on the current one.  Tickets are taken in increasing order
 // by every CTA and each CTA finishes its current tile before its prefetched
 // one, so the smallest tile in progress always finds its predecessors done.
-template <bool PL>
+template <int LM>
 __global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_lx,
                           const __grid_constant__ CUtensorMap tm_la, RglruScanFwdArgs a) {
-    constexpr int LB = RgLogits<PL>::kBoxBytes;
-    constexpr int SB = RgLogits<PL>::kSlotBytes;
-    extern __shared__ __align__(128) uint8_t s_dyn[];   // [slot][x, l^x, l^a boxes]
+    constexpr bool PL = LM >= 1;
+    constexpr int LB = RgLogits<LM>::kBoxBytes;
+    constexpr int SB = RgLogits<LM>::kSlotBytes;
+    constexpr uint32_t kIdesc = umma_idesc_bf16(kRgTile, kGroup);
+    extern __shared__ __align__(1024) uint8_t s_raw[];   // [slot][x, l^x, l^a boxes] (+ LM 2 staging)
     __shared__ uint8_t s_rst[kRgTile];
     __shared__ float4 s_map[kRgWarps][32];
     __shared__ float2 s_ent[kRgWarps][32];
     __shared__ __align__(8) uint64_t s_bars[2];
+    __shared__ __align__(8) uint64_t s_mma_bar;
+    __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_tick[2];
     __shared__ int s_err;
 
@@ -135,14 +164,26 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     const int lane = tid & 31;
     const ScanGeom& g = a.g;
     const uint32_t n_tiles = (uint32_t)g.n_tiles;
+    // the slots start on a 1024-byte boundary (the 128-byte swizzle's atom; one
+    // spare kilobyte of dynamic shared memory is requested for this)
+    uint8_t* s_dyn = s_raw + ((1024u - (smem_u32(s_raw) & 1023u)) & 1023u);
+    uint8_t* s_stage = s_dyn + 2 * SB;
+    if (LM == 2 && warp == 0) {   // two gates x 64 FP32 columns of tensor memory
+        tmem_alloc(&s_tmem, 2 * kGroup);
+        tmem_fence_before_sync();
+    }
     if (tid == 0) {
         mbar_init(&s_bars[0], 1);
         mbar_init(&s_bars[1], 1);
+        if (LM == 2) mbar_init(&s_mma_bar, 1);
         s_tick[0] = atomicAdd(a.counter, 1u);
-        if (s_tick[0] < n_tiles) rg_fwd_issue<PL>(s_dyn, &s_bars[0], &tm_x, &tm_lx, &tm_la, g, s_tick[0]);
+        if (s_tick[0] < n_tiles) rg_fwd_issue<LM>(s_dyn, &s_bars[0], &tm_x, &tm_lx, &tm_la, a.wimg, g, s_tick[0]);
     }
     __syncthreads();
-    int pend = -1;   // iteration whose prefetched copy is outstanding when the loop is left early
+    if (LM == 2) tmem_fence_after_sync();
+    const uint32_t tmem = LM == 2 ? s_tmem : 0u;
+    int pend = -1;       // iteration whose prefetched copy is outstanding when the loop is left early
+    int mma_lost = -1;   // LM 2: iteration whose MMA completion was not seen
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     const uint32_t tile_u = s_tick[slot];
@@ -150,13 +191,13 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     if (tid == 0) {   // the next ticket into the other slot (free since the end of the previous tile)
         s_tick[slot ^ 1] = atomicAdd(a.counter, 1u);
         if (s_tick[slot ^ 1] < n_tiles)
-            rg_fwd_issue<PL>(s_dyn + (size_t)(slot ^ 1) * SB, &s_bars[slot ^ 1], &tm_x, &tm_lx, &tm_la, g,
+            rg_fwd_issue<LM>(s_dyn + (size_t)(slot ^ 1) * SB, &s_bars[slot ^ 1], &tm_x, &tm_lx, &tm_la, a.wimg, g,
                              s_tick[slot ^ 1]);
     }
     uint8_t* sb = s_dyn + (size_t)slot * SB;
-    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(sb);
-    const uint8_t* s_lx = sb + kRgBoxBytes;
-    const uint8_t* s_la = sb + kRgBoxBytes + LB;
+    const uint8_t* s_x = sb;
+    const uint8_t* s_lx = LM == 2 ? s_stage : sb + kRgBoxBytes;
+    const uint8_t* s_la = LM == 2 ? s_stage + kRgTile * kStageRow * 4 : sb + kRgBoxBytes + LB;
     const long long tile = tile_u;
     const int chain = (int)(tile % g.n_chains);
     const int c = (int)(tile / g.n_chains);
@@ -196,6 +237,47 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         pend = it + 1;
         break;
     }
+    if (LM == 2) {
+        // logits of the tile: D_gate[128 x 64] = x[128 x 64] . Wimg_gate[64 x 64]^T,
+        // four K = 16 steps per gate, issued by one thread
+        if (tid == 0) {
+            tmem_fence_after_sync();
+            const uint32_t xa = smem_u32(sb), wa = smem_u32(sb + kRgBoxBytes);
+#pragma unroll
+            for (int gt = 0; gt < 2; ++gt)
+#pragma unroll
+                for (int ks = 0; ks < kGroup / 16; ++ks)
+                    umma_bf16(tmem + (uint32_t)(gt * kGroup), umma_desc_sw128(xa + 32u * ks),
+                              umma_desc_sw128(wa + (uint32_t)(gt * kGroup * kGroup * 2) + 32u * ks), kIdesc, ks > 0);
+            umma_commit(&s_mma_bar);
+        }
+        const bool done = mbar_wait_bounded(&s_mma_bar, (uint32_t)it & 1u);
+        if (!__syncthreads_and(done)) {
+            if (tid == 0) {
+                st_release_gpu(fl + c, kFlagErr);
+                atomicOr(a.status, kStatusTimeout);
+            }
+            pend = it + 1;
+            mma_lost = it;
+            break;
+        }
+        tmem_fence_after_sync();
+        {   // warp w: tokens 32 (w % 4) .. + 31 (its tensor-memory lanes) of gate w / 4
+            const int q = warp & 3, gt = warp >> 2;
+            float* st = reinterpret_cast<float*>(s_stage) + (size_t)gt * kRgTile * kStageRow +
+                        (size_t)(32 * q + lane) * kStageRow;
+#pragma unroll
+            for (int col = 0; col < kGroup; col += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gt * kGroup + col), v);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(st + col + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+        }
+        tmem_fence_before_sync();
+        __syncthreads();
+    }
 
     float4 ab[kSub];   // {a_d, b_d, a_d+1, b_d+1}
     float2 S0 = make_float2(1.f, 0.f), S1 = S0;
@@ -204,9 +286,9 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         ab[i] = make_float4(1.f, 0.f, 1.f, 0.f);
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
-            const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
-            const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
-            const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
+            const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
+            const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
+            const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
             const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
             const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
             ab[i] = make_float4(g0.a, xx.x * g0.gx * g0.n, g1.a, xx.y * g1.gx * g1.n);
@@ -312,9 +394,18 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         *reinterpret_cast<float2*>(a.hT + (size_t)b * D + d) = make_float2(z0, z1);
     __syncthreads();   // this slot and s_rst free; the next ticket visible
   }
-    // leaving early (a failed wait): the next ticket's copy may still be in flight
+    // leaving early (a failed wait): the next ticket's copy, or the tile's
+    // MMA, may still be in flight
     if (tid == 0 && pend >= 0 && s_tick[pend & 1] < n_tiles)
         mbar_wait_bounded(&s_bars[pend & 1], (uint32_t)(pend >> 1) & 1u);
+    if (LM == 2) {
+        if (tid == 0 && mma_lost >= 0) mbar_wait_bounded(&s_mma_bar, (uint32_t)mma_lost & 1u);
+        __syncthreads();
+        if (warp == 0) {
+            tmem_fence_after_sync();
+            tmem_dealloc(tmem, 2 * kGroup);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -680,6 +771,38 @@ __global__ void __launch_bounds__(256) rglru_proj_dw_kernel(const float* __restr
     }
 }
 
+// Weight images for the in-kernel logits: group g, gate q, output n, input k
+// (channels 64 g + n, 64 g + k) hold W_q[h][i][o] when both channels lie in
+// diagonal block h (i, o their offsets in it), else 0; stored K-major with the
+// 128-byte swizzle (row n: 128 bytes, chunk k / 8 at k / 8 ^ n % 8).
+__global__ void __launch_bounds__(256) rglru_proj_wimg_kernel(const uint16_t* __restrict__ w_x,
+                                                              const uint16_t* __restrict__ w_a,
+                                                              uint16_t* __restrict__ img, int D) {
+    const int dk = D / kProjBlocks;
+    const size_t n_el = (size_t)(D / kGroup) * 2 * kGroup * kGroup;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_el; e += (size_t)gridDim.x * blockDim.x) {
+        const int k = (int)(e % kGroup);
+        const int n = (int)(e / kGroup % kGroup);
+        const int q = (int)(e / (kGroup * kGroup) % 2);
+        const size_t grp = e / (2 * kGroup * kGroup);
+        const int co = (int)grp * kGroup + n, ci = (int)grp * kGroup + k;
+        const int h = co / dk;
+        uint16_t v = 0;
+        if (ci / dk == h) {
+            const uint16_t* w = q == 0 ? w_x : w_a;
+            v = w[((size_t)h * dk + (ci - h * dk)) * dk + (co - h * dk)];
+        }
+        img[(grp * 2 + q) * kGroup * kGroup + (size_t)n * kGroup + ((((k >> 3) ^ (n & 7))) << 3) + (k & 7)] = v;
+    }
+}
+
+cudaError_t launch_rglru_proj_wimg(const void* w_x, const void* w_a, void* wimg, int D, cudaStream_t s) {
+    const size_t n = (size_t)(D / kGroup) * 2 * kGroup * kGroup;
+    rglru_proj_wimg_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(
+        static_cast<const uint16_t*>(w_x), static_cast<const uint16_t*>(w_a), static_cast<uint16_t*>(wimg), D);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rglru_proj_pack(const void* w_x, const void* w_a, void* wcat, int dk, cudaStream_t s) {
     const size_t n = (size_t)16 * 6 * dk * dk;
     rglru_proj_pack_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(
@@ -706,20 +829,23 @@ unsigned rg_grid(K kernel, int smem, long long n_tiles) {
     return (unsigned)(n < n_tiles ? n : (n_tiles > 0 ? n_tiles : 1));
 }
 
-template <bool PL>
+template <int LM>
 cudaError_t launch_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
                        const RglruScanFwdArgs& args, cudaStream_t s) {
-    const int smem = 2 * RgLogits<PL>::kSlotBytes;   // two slots
-    cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel<PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // two slots, the staging area (LM 2) and a spare kilobyte for 1024-byte alignment
+    const int smem = 2 * RgLogits<LM>::kSlotBytes + (LM == 2 ? kStageBytes : 0) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel<LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_fwd_kernel<PL><<<rg_grid(rglru_scan_fwd_kernel<PL>, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
+    rglru_scan_fwd_kernel<LM><<<rg_grid(rglru_scan_fwd_kernel<LM>, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
         tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const CUtensorMap& tm_la,
-                                  const RglruScanFwdArgs& args, cudaStream_t s, bool projected) {
-    return projected ? launch_fwd<true>(tm_x, tm_lx, tm_la, args, s) : launch_fwd<false>(tm_x, tm_lx, tm_la, args, s);
+                                  const RglruScanFwdArgs& args, cudaStream_t s, int logits) {
+    if (logits == 2) return launch_fwd<2>(tm_x, tm_lx, tm_la, args, s);
+    if (logits == 1) return launch_fwd<1>(tm_x, tm_lx, tm_la, args, s);
+    return launch_fwd<0>(tm_x, tm_lx, tm_la, args, s);
 }
 
 template <bool PL>

@@ -37,6 +37,22 @@ inline bool make_bf16_map(CUtensorMap* map, const void* ptr, int B, int L, int D
     return r == CUDA_SUCCESS;
 }
 
+// The same BF16 map with the 128-byte swizzle (the box rows are 128 bytes:
+// kGroup channels), for boxes that feed the tensor cores; the destination
+// must be 1024-byte aligned.
+inline bool make_bf16_map_sw128(CUtensorMap* map, const void* ptr, int B, int L, int D, int rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * (cuuint64_t)D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kGroup, (cuuint32_t)rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // The same over a contiguous [B, L, D] FP32 tensor (256-byte box rows).
 inline bool make_f32_map(CUtensorMap* map, const void* ptr, int B, int L, int D, int rows) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();

@@ -1,0 +1,97 @@
+// Fifth-generation tensor-core helpers for sm_103a (tcgen05): tensor-memory
+// allocation, shared-memory matrix descriptors, the BF16 MMA with an FP32
+// accumulator in tensor memory, its completion on an mbarrier, and loads of
+// the accumulator into registers.  Inline PTX only.
+//
+// Operand layout used here: K-major with the 128-byte swizzle, i.e. rows of
+// 64 BF16 values (128 bytes), eight-row atoms of 1024 bytes in which the
+// 16-byte chunk j of row r sits at chunk j ^ (r % 8).  This is the layout a
+// TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes for a box whose inner
+// extent is 128 bytes, into a 1024-byte-aligned destination.
+#pragma once
+
+#include "common.cuh"
+
+namespace lrs {
+
+// Shared-memory matrix descriptor (K-major, 128-byte swizzle): start address
+// and stride between eight-row atoms (1024 bytes), both in 16-byte units;
+// the leading-dimension offset is unused for this layout (set to 1); version
+// field 1; layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;                        // leading byte offset (unused)
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;  // stride byte offset: one atom
+    d |= (uint64_t)1u << 46;                        // descriptor version
+    d |= (uint64_t)2u << 61;                        // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with BF16 A and B, FP32 accumulator,
+// both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+    return (1u << 4)                          // D format: F32
+           | (1u << 7)                        // A format: BF16
+           | (1u << 10)                       // B format: BF16
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Tensor-memory allocation of `ncols` columns (a power of two >= 32) by one
+// whole warp; the base address is written to *slot (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T for one K = 16 slice, issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Arrives once on `bar` when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive FP32 columns of one tensor-memory lane per thread: thread t
+// of the warp reads lane (taddr's lane + t); the warp's lanes must be its own
+// quarter (32 (warp % 4) ...).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    // the wait sits in the same statement, so the outputs are complete when it ends
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace lrs

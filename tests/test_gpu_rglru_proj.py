@@ -21,6 +21,8 @@ SMALL = {
     "D1024_L129_tile_edge": dict(B=1, L=129, D=1024, seed=72, h0=False, resets="none"),
     "D2048_L200": dict(B=1, L=200, D=2048, seed=73, h0=True, resets="segments"),
     "single_token_D128": dict(B=3, L=1, D=128, seed=74, h0=True, resets="none"),
+    "D512_L513_resets": dict(B=2, L=513, D=512, seed=77, h0=True, resets=0.01),
+    "D1536_L140_gemm_path": dict(B=1, L=140, D=1536, seed=78, h0=True, resets="none"),
 }
 
 

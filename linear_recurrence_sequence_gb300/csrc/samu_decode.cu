@@ -10,21 +10,26 @@
 // double-float formed in FP64) is done once by samu_decode_prepare into a
 // caller-owned parameter block, so that the step itself is one launch.
 //
-// GB300 organisation: one 256-thread CTA per sequence.  Thread t owns the
-// 8-channel chunks t, t+256, ... of the token's x_sel row for the two dot
-// products (16-byte loads, paired FP32 arithmetic), reduced over the CTA in a
-// fixed order; thread 0 forms the token's scalars.  Then thread t owns the
-// mode pairs (2t, 2t+1), (2t+512, 2t+513), ...: state, w and the outputs move
-// as 16-byte (state) and 4-byte (BF16 pairs) accesses, coalesced across the
-// CTA.  Bandwidth-bound: per sequence 2D (x_sel) + 2D (w) + 2D (y) + 8D (state
-// read and written) bytes.
+// GB300 organisation: one CTA of T threads per sequence (T = 128 for
+// D <= 1024, else 256, so that every thread owns one to four mode pairs; at
+// most 64 registers, so that 32 warps of it are resident per SM).
+// Thread t owns the 8-channel chunks t, t+T, ... of the token's x_sel row for
+// the two dot products (16-byte loads, paired FP32 arithmetic), reduced over
+// the CTA in a fixed order behind a CTA barrier; lane 0 of every warp then
+// forms the token's scalars from the warp sums (the same operations in every
+// warp, so the same bits) and broadcasts them by shuffle (T = 256: thread 0
+// forms them behind a second barrier).  Thread t owns
+// the mode pairs (2t, 2t+1), (2t+2T, 2t+2T+1), ...: state, w and the outputs
+// move as 16-byte (state) and 4-byte (BF16 pairs) accesses, coalesced across
+// the CTA.  Bandwidth-bound: per sequence 2D (x_sel) + 2D (w) + 2D (y) + 8D
+// (state read and written) bytes.
 #include "kernels.cuh"
 
 namespace lrs {
 
-constexpr int kDecThreads = 256;
+constexpr int kDecThreads = 256;              // the prepare kernel, and the step for D > 1024
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kDecPairs = 4;   // mode pairs per thread: M <= 2 * kDecThreads * kDecPairs = 2048 (D <= 4096)
+constexpr int kDecPairs = 4;   // mode pairs per thread: M <= 2 * 256 * kDecPairs = 2048 (D <= 4096)
 
 // Parameter block (floats from the start of the caller's buffer):
 //   w_hat_phi [D+1], w_hat_r [D+1], each starting on a 16-byte boundary
@@ -88,10 +93,11 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_prepare_kernel(SamuDe
     }
 }
 
-// One token of sequence blockIdx.x.
-__global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecodeStepArgs a) {
-    __shared__ float2 s_red[kDecWarps];
-    __shared__ float4 s_ctl;   // {E - 1, C, S, reset}
+// One token of sequence blockIdx.x, T threads.
+template <int T>
+__global__ void __launch_bounds__(T, 1024 / T) samu_decode_step_kernel(SamuDecodeStepArgs a) {
+    constexpr int W = T / 32;
+    __shared__ float2 s_red[W];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int D = a.D, M = D / 2, nch = D / 8;
     const size_t b = blockIdx.x;
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
     uint32_t wre[kDecPairs], wim[kDecPairs];
 #pragma unroll
     for (int j = 0; j < kDecPairs; ++j) {
-        const int m = 2 * tid + j * 2 * kDecThreads;
+        const int m = 2 * tid + j * 2 * T;
         if (m < M) {
             zs[j] = __ldcs(reinterpret_cast<const float4*>(a.state_in + (b * M + m) * 2));   // re0, im0, re1, im1
             wre[j] = __ldcs(wrow + m / 2);
@@ -119,7 +125,7 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
     // controller: x~ . w_hat for both directions
     const uint4* xr = reinterpret_cast<const uint4*>(a.x) + b * nch;
     f2x pp = 0ull, pr = 0ull;
-    for (int c = tid; c < nch; c += kDecThreads) {
+    for (int c = tid; c < nch; c += T) {
         const uint4 q = __ldcs(xr + c);
         const float4* w0 = reinterpret_cast<const float4*>(wh + 8 * c);                 // w_hat_phi of the chunk
         const float4* wq = reinterpret_cast<const float4*>(wh + dec_row(D) + 8 * c);    // w_hat_r
@@ -145,9 +151,15 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
     }
     if (lane == 0) s_red[warp] = make_float2(sp, sr);
     __syncthreads();
-    if (tid == 0) {
+    // {E - 1, C, S, reset}: with four warps every warp forms them (lane 0) and
+    // broadcasts by shuffle; with eight, thread 0 forms them behind a second
+    // barrier (eight copies of the transcendental chain cost more than it)
+    constexpr bool kPerWarp = W <= 4;
+    __shared__ float4 s_ctl;
+    float4 ctl = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kPerWarp ? lane == 0 : tid == 0) {
         float tp = wh[D], tr = wh[dec_row(D) + D];   // the appended constant 1 times the bias weight
-        for (int w = 0; w < kDecWarps; ++w) {
+        for (int w = 0; w < W; ++w) {
             tp += s_red[w].x;
             tr += s_red[w].y;
         }
@@ -156,10 +168,18 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
         float sn, cs;
         sincosf(d, &sn, &cs);
         const float rs = (a.reset != nullptr && a.reset[b] != 0) ? 1.0f : 0.0f;
-        s_ctl = make_float4(expm1f(c), cs, sn, rs);
+        ctl = make_float4(expm1f(c), cs, sn, rs);
+        if (!kPerWarp) s_ctl = ctl;
     }
-    __syncthreads();
-    const float4 ctl = s_ctl;
+    if (kPerWarp) {
+        ctl.x = __shfl_sync(0xffffffffu, ctl.x, 0);
+        ctl.y = __shfl_sync(0xffffffffu, ctl.y, 0);
+        ctl.z = __shfl_sync(0xffffffffu, ctl.z, 0);
+        ctl.w = __shfl_sync(0xffffffffu, ctl.w, 0);
+    } else {
+        __syncthreads();
+        ctl = s_ctl;
+    }
     Ctl2 ct;
     ct.e = dup2(ctl.x);
     ct.c = dup2(ctl.y);
@@ -168,7 +188,7 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_step_kernel(SamuDecod
 
 #pragma unroll
     for (int j = 0; j < kDecPairs; ++j) {
-        const int m = 2 * tid + j * 2 * kDecThreads;
+        const int m = 2 * tid + j * 2 * T;
         if (m >= M) continue;
         const float4 z4 = zs[j];
         const f2x bre = bf2x(wre[j]), bim = bf2x(wim[j]);
@@ -209,7 +229,10 @@ cudaError_t launch_samu_decode_prepare(const SamuDecodePrepArgs& args, cudaStrea
 }
 
 cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t s) {
-    samu_decode_step_kernel<<<(unsigned)args.B, kDecThreads, 0, s>>>(args);
+    if (args.D <= 1024)
+        samu_decode_step_kernel<128><<<(unsigned)args.B, 128, 0, s>>>(args);
+    else
+        samu_decode_step_kernel<kDecThreads><<<(unsigned)args.B, kDecThreads, 0, s>>>(args);
     return cudaGetLastError();
 }
 

@@ -60,50 +60,65 @@ __device__ __forceinline__ float2 rg_x(const uint8_t* box, int r, int lane) {
     return bf2_to_f2(w[r * 32 + lane]);
 }
 
-struct RgGate {
-    float a;    // retention (0 at a segment start)
-    float n;    // write normaliser sqrt(1 - a^2) (1 at a segment start)
-    float u;    // 1 - a^2
-    float gx;   // sigmoid(l^x)
-    float ga;   // sigmoid(l^a)
+// Gate arithmetic for the lane's two channels at once, as FP32 pairs (paired
+// f32x2 instructions; the SFU approximations run per element).
+//  - sigmoid(v) = 1 / (1 + e^{-v}) from two SFU operations.  Its ~2^-22
+//    relative error only scales the write gate and, through
+//    log a = g^a (-8 softplus), moves log a by at most ~1e-8 absolute:
+//    nothing accumulates through the recurrence.
+//  - e^v - 1: for |v| < 1/4 its Taylor series through v^8 (coefficients 1/k!;
+//    the remainder is below 1e-10 relative there), so that 1 - a^2 keeps full
+//    relative accuracy when a is close to 1; otherwise e^v - 1 from ex2, where
+//    the cancellation costs at most a factor 4.
+//  - a = e^{log a}, u = 1 - a^2 = -(e^{2 log a} - 1), n = sqrt(max(u, 0));
+//    at a segment start a = 0 and n = 1.
+struct RgGate2 {
+    f2x a, n, u, gx, ga;   // retention, write normaliser, 1 - a^2, sigmoid(l^x), sigmoid(l^a)
 };
 
-// 1 / (1 + e^{-v}) from two SFU operations.  Its ~2^-22 relative error only
-// scales the write gate and, through log a = g^a (-8 softplus), moves log a by
-// at most ~1e-8 absolute: nothing accumulates through the recurrence.
-__device__ __forceinline__ float sigmoid_f(float v) {
-    return rcp_approx(1.0f + ex2_approx(-v * kLog2e));
+__device__ __forceinline__ f2x sfu_ex2(f2x t) {
+    float t0, t1;
+    up2(t, t0, t1);
+    return pk2(ex2_approx(t0), ex2_approx(t1));
 }
 
-// e^v - 1.  For |v| < 1/4 its Taylor series through v^8 (coefficients 1/k!;
-// the remainder is below 1e-10 relative there), so that 1 - a^2 keeps full
-// relative accuracy when a is close to 1; otherwise e^v - 1 from ex2, where
-// the cancellation costs at most a factor 4.
-__device__ __forceinline__ float expm1_fast(float v) {
-    float p = fmaf(v, 1.0f / 40320.0f, 1.0f / 5040.0f);
-    p = fmaf(v, p, 1.0f / 720.0f);
-    p = fmaf(v, p, 1.0f / 120.0f);
-    p = fmaf(v, p, 1.0f / 24.0f);
-    p = fmaf(v, p, 1.0f / 6.0f);
-    p = fmaf(v, p, 0.5f);
-    p = fmaf(v, p, 1.0f);
-    const float series = v * p;
-    const float direct = ex2_approx(v * kLog2e) - 1.0f;
-    return fabsf(v) < 0.25f ? series : direct;
+__device__ __forceinline__ f2x sigmoid2(f2x v) {
+    float d0, d1;
+    up2(add2(dup2(1.0f), sfu_ex2(mul2(v, dup2(-kLog2e)))), d0, d1);
+    return pk2(rcp_approx(d0), rcp_approx(d1));
 }
 
-// nsp = -8 softplus(alpha) for this channel
-__device__ __forceinline__ RgGate rg_gate(float lx, float la, float nsp, bool is_reset) {
-    RgGate gt;
-    gt.gx = sigmoid_f(lx);
-    gt.ga = sigmoid_f(la);
-    const float lg = gt.ga * nsp;                 // log a
-    gt.a = ex2_approx(lg * kLog2e);
-    gt.u = -expm1_fast(2.0f * lg);
-    gt.n = sqrt_approx(fmaxf(gt.u, 0.0f));
+__device__ __forceinline__ f2x expm1_2(f2x v) {
+    f2x p = fma2(v, dup2(1.0f / 40320.0f), dup2(1.0f / 5040.0f));
+    p = fma2(v, p, dup2(1.0f / 720.0f));
+    p = fma2(v, p, dup2(1.0f / 120.0f));
+    p = fma2(v, p, dup2(1.0f / 24.0f));
+    p = fma2(v, p, dup2(1.0f / 6.0f));
+    p = fma2(v, p, dup2(0.5f));
+    p = fma2(v, p, dup2(1.0f));
+    const f2x series = mul2(v, p);
+    float v0, v1;
+    up2(v, v0, v1);
+    if (fabsf(v0) < 0.25f && fabsf(v1) < 0.25f) return series;
+    float s0, s1;
+    up2(series, s0, s1);
+    return pk2(fabsf(v0) < 0.25f ? s0 : ex2_approx(v0 * kLog2e) - 1.0f,
+               fabsf(v1) < 0.25f ? s1 : ex2_approx(v1 * kLog2e) - 1.0f);
+}
+
+__device__ __forceinline__ RgGate2 rg_gate2(f2x lx, f2x la, f2x nsp, bool is_reset) {
+    RgGate2 gt;
+    gt.gx = sigmoid2(lx);
+    gt.ga = sigmoid2(la);
+    const f2x lg = mul2(gt.ga, nsp);   // log a
+    gt.a = sfu_ex2(mul2(lg, dup2(kLog2e)));
+    gt.u = sub2(0ull, expm1_2(mul2(dup2(2.0f), lg)));
+    float u0, u1;
+    up2(gt.u, u0, u1);
+    gt.n = pk2(sqrt_approx(fmaxf(u0, 0.0f)), sqrt_approx(fmaxf(u1, 0.0f)));
     if (is_reset) {
-        gt.a = 0.0f;
-        gt.n = 1.0f;
+        gt.a = 0ull;
+        gt.n = dup2(1.0f);
     }
     return gt;
 }
@@ -279,24 +294,32 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         __syncthreads();
     }
 
-    float4 ab[kSub];   // {a_d, b_d, a_d+1, b_d+1}
-    float2 S0 = make_float2(1.f, 0.f), S1 = S0;
+    // the lane's two channels as pairs: a_t, b_t per token; the sub-chunk map (SA, SB)
+    f2x av[kSub], bv[kSub];
+    f2x SA = dup2(1.0f), SB = 0ull;
+    const f2x nsp = pk2(nsp0, nsp1);
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
-        ab[i] = make_float4(1.f, 0.f, 1.f, 0.f);
+        av[i] = dup2(1.0f);
+        bv[i] = 0ull;
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
             const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
             const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
             const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
-            const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
-            const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
-            ab[i] = make_float4(g0.a, xx.x * g0.gx * g0.n, g1.a, xx.y * g1.gx * g1.n);
-            S0 = rcompose(make_float2(ab[i].x, ab[i].y), S0);
-            S1 = rcompose(make_float2(ab[i].z, ab[i].w), S1);
+            const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+            av[i] = gt.a;
+            bv[i] = mul2(mul2(pk2(xx.x, xx.y), gt.gx), gt.n);
+            SA = mul2(av[i], SA);                // (a, b) o (A, B) = (a A, a B + b)
+            SB = fma2(av[i], SB, bv[i]);
         }
     }
-    s_map[warp][lane] = make_float4(S0.x, S0.y, S1.x, S1.y);
+    {
+        float A0, A1, B0, B1;
+        up2(SA, A0, A1);
+        up2(SB, B0, B1);
+        s_map[warp][lane] = make_float4(A0, B0, A1, B1);
+    }
     __syncthreads();
 
     if (warp == 0) {
@@ -376,22 +399,26 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     }
 
     const float2 e = s_ent[warp][lane];
-    float z0 = e.x, z1 = e.y;
+    f2x z = pk2(e.x, e.y);
     const size_t row = (((size_t)b * L + t0 + r0) * D + d) / 2;
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
         if (i < nsub) {
-            z0 = __fmaf_rn(ab[i].x, z0, ab[i].y);
-            z1 = __fmaf_rn(ab[i].z, z1, ab[i].w);
+            z = fma2(av[i], z, bv[i]);
             if (active) {
                 const size_t o = row + (size_t)i * (D / 2);
+                float z0, z1;
+                up2(z, z0, z1);
                 __stcs(a.y + o, f2_to_bf2(z0, z1));
                 if (a.y32 != nullptr) *reinterpret_cast<float2*>(a.y32 + 2 * o) = make_float2(z0, z1);
             }
         }
     }
-    if (active && nsub > 0 && t0 + r0 + nsub == L)
+    if (active && nsub > 0 && t0 + r0 + nsub == L) {
+        float z0, z1;
+        up2(z, z0, z1);
         *reinterpret_cast<float2*>(a.hT + (size_t)b * D + d) = make_float2(z0, z1);
+    }
     __syncthreads();   // this slot and s_rst free; the next ticket visible
   }
     // leaving early (a failed wait): the next ticket's copy, or the tile's
@@ -512,29 +539,32 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         return;
     }
 
-    float2 hp[kSub];   // h_{t-1} per token
-    float P0 = 1.f, P1 = 1.f, q0 = 0.f, q1 = 0.f;
+    // the lane's two channels as pairs (the same IEEE operations per element)
+    const f2x nsp = pk2(nsp0, nsp1);
+    f2x hp[kSub];   // h_{t-1} per token
+    f2x hv = pk2(h0v, h1v), P = dup2(1.0f), q = 0ull;
 #pragma unroll
     for (int i = 0; i < kSub; ++i) {
-        hp[i] = make_float2(0.f, 0.f);
+        hp[i] = 0ull;
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
             const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
             const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
             const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
             const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
-            const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
-            const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
-            hp[i] = make_float2(h0v, h1v);
-            h0v = __fmaf_rn(g0.a, h0v, xx.x * g0.gx * g0.n);
-            h1v = __fmaf_rn(g1.a, h1v, xx.y * g1.gx * g1.n);
-            P0 *= g0.a;
-            P1 *= g1.a;
-            q0 = fmaf(P0, gg.x, q0);
-            q1 = fmaf(P1, gg.y, q1);
+            const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+            hp[i] = hv;
+            hv = fma2(gt.a, hv, mul2(mul2(pk2(xx.x, xx.y), gt.gx), gt.n));
+            P = mul2(P, gt.a);
+            q = fma2(P, pk2(gg.x, gg.y), q);
         }
     }
-    s_map[warp][lane] = make_float4(P0, q0, P1, q1);
+    {
+        float P0, P1, q0, q1;
+        up2(P, P0, P1);
+        up2(q, q0, q1);
+        s_map[warp][lane] = make_float4(P0, q0, P1, q1);
+    }
     __syncthreads();
 
     if (warp == 0) {
@@ -608,39 +638,40 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     if (s_err) return;
 
     const float2 e = s_ent[warp][lane];
-    float H0 = e.x, H1 = e.y, da0 = 0.f, da1 = 0.f;
-    float4 bs = make_float4(0.f, 0.f, 0.f, 0.f);   // PL: sums of dl^x, dl^a over the lane's tokens
+    f2x H = pk2(e.x, e.y), da = 0ull;
+    const f2x sa = pk2(sa0, sa1);
+    f2x bsx = 0ull, bsa = 0ull;   // PL: sums of dl^x, dl^a over the lane's tokens
     const size_t row = (((size_t)b * L + t0 + r0) * D + d) / 2;
 #pragma unroll
     for (int i = kSub - 1; i >= 0; --i) {
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
-            const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
+            const float2 xf = bf2_to_f2(s_x[r0 + i][lane]);
             const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
             const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
             const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
-            const RgGate g0 = rg_gate(gl.x, al.x, nsp0, rs);
-            const RgGate g1 = rg_gate(gl.y, al.y, nsp1, rs);
-            H0 += gg.x;
-            H1 += gg.y;
-            const float dx0 = H0 * g0.gx * g0.n, dx1 = H1 * g1.gx * g1.n;
-            const float dlx0 = H0 * xx.x * g0.n * g0.gx * (1.f - g0.gx);
-            const float dlx1 = H1 * xx.y * g1.n * g1.gx * (1.f - g1.gx);
-            float dla0 = 0.f, dla1 = 0.f;
+            const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+            const f2x xx = pk2(xf.x, xf.y);
+            H = add2(H, pk2(gg.x, gg.y));
+            const f2x dx2 = mul2(mul2(H, gt.gx), gt.n);
+            const f2x dlx2 = mul2(mul2(mul2(mul2(H, xx), gt.n), gt.gx), sub2(dup2(1.0f), gt.gx));
+            f2x dla2 = 0ull;
             if (!rs) {
-                const float ab0 = fmaf(H0, hp[i].x, H0 * xx.x * g0.gx * (-2.f * g0.a) * rsqrt_approx(fmaxf(4.f * g0.u, 1e-6f)));
-                const float ab1 = fmaf(H1, hp[i].y, H1 * xx.y * g1.gx * (-2.f * g1.a) * rsqrt_approx(fmaxf(4.f * g1.u, 1e-6f)));
-                dla0 = ab0 * nsp0 * g0.a * g0.ga * (1.f - g0.ga);
-                dla1 = ab1 * nsp1 * g1.a * g1.ga * (1.f - g1.ga);
-                da0 = fmaf(ab0, -8.f * g0.ga * sa0 * g0.a, da0);
-                da1 = fmaf(ab1, -8.f * g1.ga * sa1 * g1.a, da1);
+                float u0, u1;
+                up2(mul2(dup2(4.0f), gt.u), u0, u1);
+                const f2x rq = pk2(rsqrt_approx(fmaxf(u0, 1e-6f)), rsqrt_approx(fmaxf(u1, 1e-6f)));
+                const f2x ab = fma2(H, hp[i], mul2(mul2(mul2(mul2(H, xx), gt.gx), mul2(dup2(-2.0f), gt.a)), rq));
+                dla2 = mul2(mul2(mul2(mul2(ab, nsp), gt.a), gt.ga), sub2(dup2(1.0f), gt.ga));
+                da = fma2(ab, mul2(mul2(mul2(dup2(-8.0f), gt.ga), sa), gt.a), da);
             }
             if (PL) {
-                bs.x += dlx0;
-                bs.y += dlx1;
-                bs.z += dla0;
-                bs.w += dla1;
+                bsx = add2(bsx, dlx2);
+                bsa = add2(bsa, dla2);
             }
+            float dx0, dx1, dlx0, dlx1, dla0, dla1;
+            up2(dx2, dx0, dx1);
+            up2(dlx2, dlx0, dlx1);
+            up2(dla2, dla0, dla1);
             if (PL && active) {
                 // token t, channels d, d+1 of block h at offset ob: parts p at gp + p * dk / 2
                 uint32_t* gp = a.gparts + ((((size_t)b * L + t0 + r0 + i) * D) * 6 + (size_t)(d / a.dk) * 6 * a.dk +
@@ -668,13 +699,20 @@ __global__ void __launch_bounds__(kRgThreads, 2)
                     __stcs(reinterpret_cast<uint32_t*>(a.dla) + o, f2_to_bf2(dla0, dla1));
                 }
             }
-            H0 *= g0.a;
-            H1 *= g1.a;
+            H = mul2(H, gt.a);
         }
     }
+    float H0, H1, da0, da1;
+    up2(H, H0, H1);
+    up2(da, da0, da1);
     if (c == 0 && warp == 0 && active) *reinterpret_cast<float2*>(a.dh0 + (size_t)b * D + d) = make_float2(H0, H1);
     s_acc[warp][lane] = make_float2(da0, da1);
-    if (PL) s_bacc[warp][lane] = bs;
+    if (PL) {
+        float x0, x1, y0, y1;
+        up2(bsx, x0, x1);
+        up2(bsa, y0, y1);
+        s_bacc[warp][lane] = make_float4(x0, x1, y0, y1);
+    }
     __syncthreads();
     if (warp == 0 && active) {
         float2 s = s_acc[0][lane];

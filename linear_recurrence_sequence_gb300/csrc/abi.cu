@@ -1,6 +1,7 @@
 // extern "C" entry points declared in include/samu.h: argument checks,
 // workspace carving and kernel launches.  No allocation, no synchronisation
-// (except lrs_device_status, which documents that it synchronises).
+// (except lrs_device_status, which documents that it synchronises, and the
+// projected RG-LRU's per-thread cuBLAS handle, created on first use).
 #include <cstdint>
 #include <cstring>
 #include <cublas_v2.h>

@@ -384,7 +384,7 @@ cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t
 // ---------------------------------------------------------------------------
 // RG-LRU
 // ---------------------------------------------------------------------------
-// With projected gates (the kernels' PL variant) l^x and l^a are FP32
+// With projected gates (logit modes 1 and 2, the "PL" variants) l^x and l^a are FP32
 // [B,L,D] (x W without the bias) and bx, ba the biases added on reading.
 struct RglruScanFwdArgs {
     ScanGeom g;

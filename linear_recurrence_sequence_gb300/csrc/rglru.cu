@@ -13,8 +13,13 @@
 //
 // Tiling as in the SAMU scan: a chain is (batch row, 64 channels), a CTA owns
 // a 128-token tile (x, l^x, l^a and, backward, dy staged by TMA), 8 warps of
-// 16-token sub-chunks, lane l owns channels 2l, 2l+1, decoupled look-back
-// between tiles.
+// 16-token sub-chunks, lane l owns channels 2l, 2l+1 (paired FP32 arithmetic),
+// decoupled look-back between tiles.
+//
+// The same kernels serve the mixer with its two 16-block block-diagonal gate
+// projections (logit modes 1 and 2 below; the "PL" variants): the logits are
+// x W (+ the biases, added on reading), from cuBLAS in FP32 or, in the
+// forward, formed per tile on the tensor cores.
 #include "kernels.cuh"
 #include "umma.cuh"
 

@@ -22,6 +22,9 @@
 //  1. maps:    every warp composes its segment's affine map, walking the
 //              segment in the opposite time direction to step 2, and a CTA
 //              (8 consecutive segments of one chain) composes its CTA map;
+//              a full 16-token item without a reset gets its transition in
+//              closed form from two per-item statistics (by default; see
+//              item_transition) and its affine part by Horner's rule;
 //  2. replay:  every CTA first folds the chain's earlier (later) CTA maps into
 //              its entry state (adjoint), every warp applies the earlier
 //              (later) segment maps of its CTA and replays its segment.

@@ -135,3 +135,30 @@ def test_chunk_transition_setting(lib):
     assert lib.samu_get_chunk_transition() == 0
     assert lib.samu_set_chunk_transition(1) == 0
     assert lib.samu_get_chunk_transition() == 1
+
+
+@pytest.mark.parametrize("B,L,D,expect", [
+    (8, 8192, 1024, 0), (1, 200, 2048, 0), (1, 16, 1536, 0), (1, 16, 128, 0),
+    (1, 16, 64, 2), (1, 16, 1000, 2), (1, 16, 1032, 2), (0, 16, 1024, 1),
+])
+def test_rglru_proj_shape_validation(lib, B, L, D, expect):
+    """Host-only: the projected RG-LRU needs D a multiple of 128 (16 diagonal
+    blocks whose width is a multiple of 8)."""
+    st, saved, scratch = _ws(lib, "rglru_proj_workspace_bytes", B, L, D)
+    assert st == expect
+    if st == 0:
+        # the FP32 logits of both gates and the six BF16 gradient parts per token at least
+        assert scratch >= B * L * D * (8 + 12)
+        st2, saved2, _ = _ws(lib, "rglru_workspace_bytes", B, L, D)
+        assert st2 == 0 and saved == saved2
+
+
+def test_projected_rglru_entry_points_reject_null_pointers(lib):
+    """Host-only argument checks return LRS_ERR_ARG before any CUDA call."""
+    null = ctypes.c_void_p(0)
+    st = lib.rglru_proj_forward(null, null, null, null, null, null, null, null, 1, 16, 128,
+                                null, null, null, null, null, null)
+    assert st == 1
+    st = lib.rglru_proj_backward(null, null, null, null, null, null, null, null, null, null, 1, 16, 128,
+                                 null, null, 0, null, null, null, null, null, null, null, null)
+    assert st == 1

@@ -81,6 +81,15 @@ int lrs_version(void);
  * misaligned and copied nothing).  Returns LRS_ERR_ARG / LRS_ERR_CUDA on failure. */
 int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
 
+/* Self-test of the failure path of the bounded device-side waits: launches
+ * one kernel whose wait on an mbarrier that nothing completes gives up at the
+ * same deadline as the library's own waits (about 0.2 s), clears and then
+ * sets the status word at the start of `scratch` (a buffer of at least 64
+ * bytes, 16-byte aligned), and returns.  lrs_device_status then reports
+ * LRS_ERR_TIMEOUT, and the context stays usable.  Asynchronous on `stream`.
+ * Errors: LRS_ERR_ARG (scratch NULL or misaligned), LRS_ERR_CUDA. */
+int lrs_selftest_wait_timeout(void* scratch, cudaStream_t stream);
+
 /* Opt-in per-kernel timing for benchmarks (not needed for computing).
  * lrs_profile_begin creates (once) `capacity` pairs of CUDA events and, until
  * lrs_profile_end, records one pair on the launching stream around every

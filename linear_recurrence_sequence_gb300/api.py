@@ -33,6 +33,7 @@ _SIGNATURES = {
     "lrs_status_string": ([_I], ctypes.c_char_p),
     "lrs_version": ([], _I),
     "lrs_device_status": ([_P, ctypes.POINTER(_I), _P], _I),
+    "lrs_selftest_wait_timeout": ([_P, _P], _I),
     "lrs_profile_begin": ([_I], _I),
     "lrs_profile_end": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
     "samu_set_chunk_transition": ([_I], _I),
@@ -434,6 +435,11 @@ def rglru_proj_backward(dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, saved,
     _check("rglru_proj_backward", st)
     o["scratch"] = scratch
     return o
+
+
+def selftest_wait_timeout(scratch) -> None:
+    """Launches the library's failure-path self-test on ``scratch`` (see lrs_selftest_wait_timeout)."""
+    _check("lrs_selftest_wait_timeout", _load().lrs_selftest_wait_timeout(_ptr(scratch), _stream(scratch.device)))
 
 
 def device_status(scratch, device=None) -> int:

@@ -171,6 +171,19 @@ int check_rglru_proj_shape(int B, int L, int D) {
     return LRS_OK;
 }
 
+// Failure-path self-test: one warp waits, bounded, on an mbarrier that nothing
+// completes; the wait gives up at its deadline and records the timeout in the
+// status word, exactly as a stalled copy would in the scan kernels.
+__global__ void lrs_selftest_wait_kernel(uint32_t* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        *status = 0u;
+        mbar_init(&bar, 1);
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded(&bar, 0) && threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+}
+
 template <typename T>
 T* at(void* base, size_t off) {
     return reinterpret_cast<T*>(static_cast<char*>(base) + off);
@@ -240,6 +253,12 @@ int lrs_profile_end(int* kernel_ids, float* ms, int capacity, int* count) {
     }
     *count = g_prof.n;
     return LRS_OK;
+}
+
+int lrs_selftest_wait_timeout(void* scratch, cudaStream_t stream) {
+    if (!req(scratch)) return LRS_ERR_ARG;
+    lrs_selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<uint32_t*>(scratch));
+    return cudaGetLastError() == cudaSuccess ? LRS_OK : LRS_ERR_CUDA;
 }
 
 int lrs_device_status(void* scratch, int* status, cudaStream_t stream) {

@@ -70,6 +70,9 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="time every workload family (one JSON line each) instead of the headline line")
     p.add_argument("--only", default=None, help="with --sweep: comma-separated workload names")
+    p.add_argument("--compare-pages", action="store_true",
+                   help="SAMU vs RG-LRU (with its gate projections) at B1 L8192 D1024 with the pages' timing "
+                        "protocol, one JSON line")
     p.add_argument("--transition", choices=["closed_form", "chained"], default="closed_form",
                    help="form of the SAMU maps kernels' 16-token item transitions")
     return p.parse_args(argv)
@@ -493,10 +496,11 @@ def run_ours(args, rank, world, local):
 SWEEP_BYTES_PER_BLD = {"samu": 16.0, "rglru": 22.0, "rglru_proj": 10.0}
 
 
-def sweep_one(name, dev, K, W, transition):
+def workload_step(wl, dev):
+    """One forward+backward of workload `wl` through the C ABI on resident
+    inputs and preallocated outputs (BF16 gradients); returns (step, scratch)."""
     import torch
-    from linear_recurrence_sequence_gb300 import api, synth
-    wl = synth.WORKLOADS[name]
+    from linear_recurrence_sequence_gb300 import api
     B, L, D = wl.B, wl.L, wl.D
     inp = wl.make()
     bf, f32 = torch.bfloat16, torch.float32
@@ -545,6 +549,16 @@ def sweep_one(name, dev, K, W, transition):
                               scratch=scratch)
             api.rglru_backward(t["dy"], t["dhT"], t["x"], t["lx"], t["la"], t["alpha"], t["h0"], t["reset"], saved,
                                out=go, scratch=scratch)
+
+    return step, scratch
+
+
+def sweep_one(name, dev, K, W, transition):
+    import torch
+    from linear_recurrence_sequence_gb300 import api, synth
+    wl = synth.WORKLOADS[name]
+    B, L, D = wl.B, wl.L, wl.D
+    step, scratch = workload_step(wl, dev)
 
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(W):
@@ -659,6 +673,55 @@ def sweep_decode(name, dev, K, W):
             "kernels_avg_ms": {"samu_decode_step_kernel": round(sum(kms) / max(1, len(kms)), 5)}}
 
 
+# ---------------------------------------------------------------------------
+# --compare-pages: the pages' headline pair, SAMU (1.801 ms) vs RG-LRU with its
+# 16-block gate projections (1.603 ms) F+B at B=1, L=8192, D=1024 on an H800,
+# timed the pages' way: two rounds (RG-LRU first, then SAMU first), each 3
+# warm-up and 5 timed samples per mixer; every sample is one eager F+B
+# between CUDA events on the stream, after an L2 flush; the median of the 10
+# samples with their range and the raw samples.
+PAGES_PAIR = {"samu": ("length_8k", 1.801), "rglru_proj": ("rglru_proj_b1_8k", 1.603)}
+
+
+def run_compare(args, local):
+    import statistics
+    import torch
+    from linear_recurrence_sequence_gb300 import synth
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    steps = {k: workload_step(synth.WORKLOADS[name], dev)[0] for k, (name, _) in PAGES_PAIR.items()}
+    samples = {k: [] for k in PAGES_PAIR}
+
+    def measure(kind):
+        for _ in range(3):
+            flush.zero_()
+            steps[kind]()
+        for _ in range(5):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            steps[kind]()
+            e1.record()
+            e1.synchronize()
+            samples[kind].append(e0.elapsed_time(e1))
+
+    for order in (("rglru_proj", "samu"), ("samu", "rglru_proj")):
+        for kind in order:
+            measure(kind)
+    line = {"compare": "pages_headline_pair", "B": 1, "L": 8192, "D": 1024,
+            "protocol": "2 rounds (RG-LRU first, then SAMU first) x (3 warm-up + 5 samples); eager F+B between "
+                        "CUDA events after an L2 flush; median of 10 [min, max]"}
+    for kind, (name, pages_ms) in PAGES_PAIR.items():
+        v = samples[kind]
+        line[kind] = {"workload": name, "median_ms": round(statistics.median(v), 5), "min_ms": round(min(v), 5),
+                      "max_ms": round(max(v), 5), "samples_ms": [round(x, 5) for x in v],
+                      "pages_h800_ms": pages_ms}
+    sm, rm = line["samu"]["median_ms"], line["rglru_proj"]["median_ms"]
+    line["samu_vs_rglru_percent"] = round(100.0 * (rm - sm) / rm, 1)   # positive: SAMU takes less time
+    print(json.dumps(line), flush=True)
+
+
 def run_sweep(args, local):
     import torch
     from linear_recurrence_sequence_gb300 import synth
@@ -685,6 +748,11 @@ def main(argv=None):
         if rank == 0:
             set_transition(args)
             run_sweep(args, local)
+        return 0
+    if args.compare_pages:
+        if rank == 0:
+            set_transition(args)
+            run_compare(args, local)
         return 0
     if world > 1:
         import torch.distributed as dist

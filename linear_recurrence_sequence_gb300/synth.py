@@ -200,5 +200,7 @@ WORKLOADS = {
     "rglru_16k": Workload("rglru_16k", "rglru", 8, 16384, 1024, (0,), h0=False),
     # the RG-LRU mixer with its 16-block gate projections (the pages' mixer scope)
     "rglru_proj_8k": Workload("rglru_proj_8k", "rglru_proj", 8, 8192, 1024, (0,), h0=False),
+    # the pages' headline comparison shape: B1 L8192 D1024, RG-LRU with its gate projections
+    "rglru_proj_b1_8k": Workload("rglru_proj_b1_8k", "rglru_proj", 1, 8192, 1024, (0,), h0=False),
     "rglru_proj_16k": Workload("rglru_proj_16k", "rglru_proj", 8, 16384, 1024, (0,), h0=False),
 }

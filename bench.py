@@ -71,8 +71,8 @@ def parse_args(argv=None):
                    help="time every workload family (one JSON line each) instead of the headline line")
     p.add_argument("--only", default=None, help="with --sweep: comma-separated workload names")
     p.add_argument("--compare-pages", action="store_true",
-                   help="SAMU vs RG-LRU (with its gate projections) at B1 L8192 D1024 with the pages' timing "
-                        "protocol, one JSON line")
+                   help="SAMU vs RG-LRU (with its gate projections) on the pages' comparison shapes with the "
+                        "pages' timing protocol, one JSON line per shape")
     p.add_argument("--transition", choices=["closed_form", "chained"], default="closed_form",
                    help="form of the SAMU maps kernels' 16-token item transitions")
     return p.parse_args(argv)
@@ -674,13 +674,21 @@ def sweep_decode(name, dev, K, W):
 
 
 # ---------------------------------------------------------------------------
-# --compare-pages: the pages' headline pair, SAMU (1.801 ms) vs RG-LRU with its
-# 16-block gate projections (1.603 ms) F+B at B=1, L=8192, D=1024 on an H800,
-# timed the pages' way: two rounds (RG-LRU first, then SAMU first), each 3
-# warm-up and 5 timed samples per mixer; every sample is one eager F+B
-# between CUDA events on the stream, after an L2 flush; the median of the 10
-# samples with their range and the raw samples.
-PAGES_PAIR = {"samu": ("length_8k", 1.801), "rglru_proj": ("rglru_proj_b1_8k", 1.603)}
+# --compare-pages: SAMU vs RG-LRU with its 16-block gate projections, F+B, on
+# the pages' comparison shapes, timed the pages' way: two rounds (RG-LRU
+# first, then SAMU first), each 3 warm-up and 5 timed samples per mixer;
+# every sample is one eager F+B between CUDA events on the stream, after an L2
+# flush; the median of the 10 samples with their range and the raw samples.
+# The pages' H800 figures: the absolute pair at B1 L8192 D1024 and, for their
+# four primary shapes, the time reduction (t_RG - t_SAMU) / t_RG.
+PAGES_SHAPES = [
+    # (B, L, D, pages SAMU ms, pages RG-LRU ms, pages reduction %)
+    (1, 8192, 1024, 1.801, 1.603, None),
+    (4, 2048, 2048, None, None, 24.6),
+    (1, 8192, 2560, None, None, 27.6),
+    (1, 32768, 1024, None, None, 37.3),
+    (1, 32768, 2048, None, None, 40.2),
+]
 
 
 def run_compare(args, local):
@@ -690,36 +698,43 @@ def run_compare(args, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    steps = {k: workload_step(synth.WORKLOADS[name], dev)[0] for k, (name, _) in PAGES_PAIR.items()}
-    samples = {k: [] for k in PAGES_PAIR}
+    for (B, L, D, p_samu, p_rg, p_red) in PAGES_SHAPES:
+        wls = {"samu": synth.Workload(f"samu_B{B}_L{L}_D{D}", "samu", B, L, D, (0,), h0=False),
+               "rglru_proj": synth.Workload(f"rglru_proj_B{B}_L{L}_D{D}", "rglru_proj", B, L, D, (0,), h0=False)}
+        steps = {k: workload_step(wl, dev)[0] for k, wl in wls.items()}
+        samples = {k: [] for k in wls}
 
-    def measure(kind):
-        for _ in range(3):
-            flush.zero_()
-            steps[kind]()
-        for _ in range(5):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            steps[kind]()
-            e1.record()
-            e1.synchronize()
-            samples[kind].append(e0.elapsed_time(e1))
+        def measure(kind):
+            for _ in range(3):
+                flush.zero_()
+                steps[kind]()
+            for _ in range(5):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                steps[kind]()
+                e1.record()
+                e1.synchronize()
+                samples[kind].append(e0.elapsed_time(e1))
 
-    for order in (("rglru_proj", "samu"), ("samu", "rglru_proj")):
-        for kind in order:
-            measure(kind)
-    line = {"compare": "pages_headline_pair", "B": 1, "L": 8192, "D": 1024,
-            "protocol": "2 rounds (RG-LRU first, then SAMU first) x (3 warm-up + 5 samples); eager F+B between "
-                        "CUDA events after an L2 flush; median of 10 [min, max]"}
-    for kind, (name, pages_ms) in PAGES_PAIR.items():
-        v = samples[kind]
-        line[kind] = {"workload": name, "median_ms": round(statistics.median(v), 5), "min_ms": round(min(v), 5),
-                      "max_ms": round(max(v), 5), "samples_ms": [round(x, 5) for x in v],
-                      "pages_h800_ms": pages_ms}
-    sm, rm = line["samu"]["median_ms"], line["rglru_proj"]["median_ms"]
-    line["samu_vs_rglru_percent"] = round(100.0 * (rm - sm) / rm, 1)   # positive: SAMU takes less time
-    print(json.dumps(line), flush=True)
+        for order in (("rglru_proj", "samu"), ("samu", "rglru_proj")):
+            for kind in order:
+                measure(kind)
+        line = {"compare": "pages_shapes", "B": B, "L": L, "D": D,
+                "protocol": "2 rounds (RG-LRU first, then SAMU first) x (3 warm-up + 5 samples); eager F+B "
+                            "between CUDA events after an L2 flush; median of 10 [min, max]"}
+        for kind, pages_ms in (("samu", p_samu), ("rglru_proj", p_rg)):
+            v = samples[kind]
+            line[kind] = {"median_ms": round(statistics.median(v), 5), "min_ms": round(min(v), 5),
+                          "max_ms": round(max(v), 5), "samples_ms": [round(x, 5) for x in v],
+                          "pages_h800_ms": pages_ms}
+        sm, rm = line["samu"]["median_ms"], line["rglru_proj"]["median_ms"]
+        line["samu_time_reduction_percent"] = round(100.0 * (rm - sm) / rm, 1)   # (t_RG - t_SAMU) / t_RG
+        line["pages_time_reduction_percent"] = (p_red if p_red is not None
+                                                else round(100.0 * (p_rg - p_samu) / p_rg, 1))
+        print(json.dumps(line), flush=True)
+        del steps
+        torch.cuda.empty_cache()
 
 
 def run_sweep(args, local):

@@ -188,6 +188,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // (kFlagAgg).  Each poll inspects 32 predecessors (one per lane, acquire
 // loads).  Returns the same value in every lane; -1 if a predecessor failed or
 // the deadline passed.
+//
+// Publishing side: the warp's lanes store the map or state, __syncwarp()
+// orders those stores before lane 0's, and lane 0's release store of the flag
+// (cumulative at gpu scope) makes them visible to any warp that acquires the
+// flag.  No separate fence per lane is needed.
 __device__ __forceinline__ int lookback_find_warp(const uint32_t* flags, int c, int C, int dir) {
     const int lane = threadIdx.x & 31;
     int base = c + dir;

@@ -325,6 +325,8 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         up2(SB, B0, B1);
         s_map[warp][lane] = make_float4(A0, B0, A1, B1);
     }
+    // the previous tile's flag, read while the other warps finish their maps
+    const uint32_t pflag = (warp == 0 && lane == 0 && c > 0) ? ld_acquire_gpu(fl + c - 1) : 0u;
     __syncthreads();
 
     if (warp == 0) {
@@ -345,12 +347,16 @@ __global__ void __launch_bounds__(kRgThreads, 2)
                 h1v = hv.y;
             }
         } else {
-            if (active)
-                *reinterpret_cast<float4*>(a.agg + ((size_t)b * CT + c) * D + d) = A;
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
-            const int j = lookback_find_warp(fl, c, CT, -1);
+            // the neighbouring tile already inclusive: its state
+            // is the entry and this tile's map need not be published
+            int j = __shfl_sync(0xffffffffu, pflag, 0) == kFlagIncl ? c - 1 : -2;
+            if (j == -2) {
+                if (active)
+                    *reinterpret_cast<float4*>(a.agg + ((size_t)b * CT + c) * D + d) = A;
+                __syncwarp();
+                if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
+                j = lookback_find_warp(fl, c, CT, -1);
+            }
             if (j < 0) {
                 err = true;
             } else if (active) {
@@ -388,9 +394,6 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             if (active)
                 *reinterpret_cast<float2*>(a.hsub + (hb + (size_t)(c + 1) * kRgWarps) * D + d) =
                     make_float2(rapply(make_float2(A.x, A.y), h0v), rapply(make_float2(A.z, A.w), h1v));
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
         } else if (lane == 0) {
             st_release_gpu(fl + c, kFlagErr);
             atomicOr(a.status, kStatusTimeout);
@@ -401,6 +404,10 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     if (s_err) {
         pend = it + 1;
         break;
+    }
+    if (warp == 0) {   // the state after the tile, published while the other warps replay
+        __syncwarp();
+        if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
     }
 
     const float2 e = s_ent[warp][lane];
@@ -570,6 +577,8 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         up2(q, q0, q1);
         s_map[warp][lane] = make_float4(P0, q0, P1, q1);
     }
+    // the next tile's flag, read while the other warps finish their maps
+    const uint32_t pflag = (warp == 0 && lane == 0 && c < CT - 1) ? ld_acquire_gpu(fl + c + 1) : 0u;
     __syncthreads();
 
     if (warp == 0) {
@@ -590,12 +599,16 @@ __global__ void __launch_bounds__(kRgThreads, 2)
                 R1 = v.y;
             }
         } else {
-            if (active)
-                *reinterpret_cast<float4*>(a.agg + ((size_t)b * CT + c) * D + d) = A;
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
-            const int j = lookback_find_warp(fl, c, CT, +1);
+            // the neighbouring tile already inclusive: its state
+            // is the entry and this tile's map need not be published
+            int j = __shfl_sync(0xffffffffu, pflag, 0) == kFlagIncl ? c + 1 : -2;
+            if (j == -2) {
+                if (active)
+                    *reinterpret_cast<float4*>(a.agg + ((size_t)b * CT + c) * D + d) = A;
+                __syncwarp();
+                if (lane == 0) st_release_gpu(fl + c, kFlagAgg);
+                j = lookback_find_warp(fl, c, CT, +1);
+            }
             if (j < 0) {
                 err = true;
             } else if (active) {
@@ -630,9 +643,6 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             if (active)
                 *reinterpret_cast<float2*>(a.rin + ((size_t)b * CT + c) * D + d) =
                     make_float2(rapply(make_float2(A.x, A.y), R0), rapply(make_float2(A.z, A.w), R1));
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
         } else if (lane == 0) {
             st_release_gpu(fl + c, kFlagErr);
             atomicOr(a.status, kStatusTimeout);
@@ -641,10 +651,14 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     }
     __syncthreads();
     if (s_err) return;
+    if (warp == 0) {   // the state after the tile, published while the other warps replay
+        __syncwarp();
+        if (lane == 0) st_release_gpu(fl + c, kFlagIncl);
+    }
 
     const float2 e = s_ent[warp][lane];
     f2x H = pk2(e.x, e.y), da = 0ull;
-    const f2x sa = pk2(sa0, sa1);
+    const f2x m8sa = mul2(dup2(-8.0f), pk2(sa0, sa1));   // -8 sigmoid(alpha)
     f2x bsx = 0ull, bsa = 0ull;   // PL: sums of dl^x, dl^a over the lane's tokens
     const size_t row = (((size_t)b * L + t0 + r0) * D + d) / 2;
 #pragma unroll
@@ -658,16 +672,18 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
             const f2x xx = pk2(xf.x, xf.y);
             H = add2(H, pk2(gg.x, gg.y));
+            const f2x Hxg = mul2(mul2(H, xx), gt.gx);
             const f2x dx2 = mul2(mul2(H, gt.gx), gt.n);
-            const f2x dlx2 = mul2(mul2(mul2(mul2(H, xx), gt.n), gt.gx), sub2(dup2(1.0f), gt.gx));
+            const f2x dlx2 = mul2(mul2(Hxg, gt.n), sub2(dup2(1.0f), gt.gx));
             f2x dla2 = 0ull;
             if (!rs) {
                 float u0, u1;
                 up2(mul2(dup2(4.0f), gt.u), u0, u1);
                 const f2x rq = pk2(rsqrt_approx(fmaxf(u0, 1e-6f)), rsqrt_approx(fmaxf(u1, 1e-6f)));
-                const f2x ab = fma2(H, hp[i], mul2(mul2(mul2(mul2(H, xx), gt.gx), mul2(dup2(-2.0f), gt.a)), rq));
-                dla2 = mul2(mul2(mul2(mul2(ab, nsp), gt.a), gt.ga), sub2(dup2(1.0f), gt.ga));
-                da = fma2(ab, mul2(mul2(mul2(dup2(-8.0f), gt.ga), sa), gt.a), da);
+                const f2x ab = fma2(H, hp[i], mul2(mul2(Hxg, mul2(dup2(-2.0f), gt.a)), rq));
+                const f2x aga = mul2(gt.a, gt.ga);
+                dla2 = mul2(mul2(ab, mul2(nsp, aga)), sub2(dup2(1.0f), gt.ga));
+                da = fma2(ab, mul2(aga, m8sa), da);
             }
             if (PL) {
                 bsx = add2(bsx, dlx2);

@@ -68,8 +68,10 @@ extern "C" {
 #define LRS_GRAD_BF16 0
 #define LRS_GRAD_FP32 1
 
-/* Human-readable text for a status code (static storage). */
+/* Human-readable text for a status code (static storage).  samu_status_string
+ * is the same function under the name the SAMU calls' documentation uses. */
 const char* lrs_status_string(int status);
+const char* samu_status_string(int status);
 
 /* ABI version (major * 100 + minor). */
 int lrs_version(void);
@@ -86,8 +88,11 @@ int lrs_device_status(void* scratch, int* status, cudaStream_t stream);
  * same deadline as the library's own waits (about 0.2 s), clears and then
  * sets the status word at the start of `scratch` (a buffer of at least 64
  * bytes, 16-byte aligned), and returns.  lrs_device_status then reports
- * LRS_ERR_TIMEOUT, and the context stays usable.  Asynchronous on `stream`.
- * Errors: LRS_ERR_ARG (scratch NULL or misaligned), LRS_ERR_CUDA. */
+ * LRS_ERR_TIMEOUT, and the context stays usable.  With scratch NULL the
+ * kernel uses the status word of samu_forward_noalloc's fixed array in the
+ * current context instead (samu_forward_noalloc_status then reports the
+ * timeout).  Asynchronous on `stream`.
+ * Errors: LRS_ERR_ARG (scratch misaligned), LRS_ERR_CUDA. */
 int lrs_selftest_wait_timeout(void* scratch, cudaStream_t stream);
 
 /* Opt-in per-kernel timing for benchmarks (not needed for computing).
@@ -122,7 +127,7 @@ int lrs_profile_end(int* kernel_ids, float* ms, int capacity, int* count);
  * within FP32 rounding.  The setting is process-wide.  It applies to the
  * samu_forward / samu_backward calls made after it, including CUDA graphs
  * captured after it (a captured graph keeps the form it was captured with).
- * Not synchronised with calls running on other host threads.
+ * Any host thread may call it; each SAMU call reads the setting once.
  * Errors: LRS_ERR_ARG for an unknown kind. */
 #define LRS_TRANSITION_CHAINED 0
 #define LRS_TRANSITION_CLOSED_FORM 1
@@ -317,10 +322,10 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
 /* SAMU forward without allocation                                           */
 /* ======================================================================== */
 
-/* Size of the fixed device workspace used by samu_forward_noalloc.  Every
- * GPU that loads this library holds this much device memory for it until the
- * process exits. */
-#define LRS_NOALLOC_BYTES (32u << 20)
+/* Size of the fixed device workspace used by samu_forward_noalloc (64 MiB).
+ * Every GPU that loads this library holds this much device memory for it
+ * until the process exits. */
+#define LRS_NOALLOC_BYTES (64u << 20)
 
 /* samu_forward for callers that cannot allocate device memory and have no
  * spare buffer to lend as `saved`/`scratch` (for example an application whose
@@ -336,20 +341,35 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
  * cudaFree or allocating library routine).  There is no matching backward:
  * the controller cache and entry states are overwritten by the next call.
  *
- * - The first call on each device looks up the array's device address (one
- *   cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture on the device.
+ * - The first call in each CUDA context (the device's primary context, or a
+ *   context of the caller's own) looks up the array's device address in that
+ *   context (one cudaGetSymbolAddress, with that context current) and keeps
+ *   it under the context's unique id; make that first call before any stream
+ *   capture in the context.
  * - Every call on a device shares the array and leaves its contents behind;
- *   each call clears what must start at zero.  Calls whose GPU work overlaps
- *   (other streams, other host threads) race on the array: serialise them.
+ *   each call clears what must start at zero (the status word).  Calls whose
+ *   GPU work overlaps (other streams, other host threads) race on the array:
+ *   serialise them.
  * - Problems whose intermediates exceed LRS_NOALLOC_BYTES are rejected with
- *   LRS_ERR_TOO_LARGE before anything is launched (B=1, L=32768, D=2048 uses
- *   about 22 MiB).
+ *   LRS_ERR_TOO_LARGE before anything is launched.  B=1, L=32768, D=2048 uses
+ *   about 52 MiB (the entry states every 8 tokens alone take 32 MiB there);
+ *   B=1, L=131072, D=1024 (87 MiB) is refused.
+ * - A bounded device-side wait that gives up is recorded in the array's
+ *   status word; samu_forward_noalloc_status reads it.
  * Errors: as samu_forward, plus LRS_ERR_TOO_LARGE. */
 int samu_forward_noalloc(const void* x_sel, const void* w, const float* h0, const uint8_t* reset,
                          const float* nu, const float* theta, const float* w_phi, const float* w_r,
                          const float* a_phi, const float* a_r, int B, int L, int D,
                          void* y, float* y32, float* hT, cudaStream_t stream);
+
+/* The device status word of the most recent samu_forward_noalloc in the
+ * current context (the same word samu_forward keeps in its scratch buffer):
+ * *status receives LRS_OK, or LRS_ERR_TIMEOUT if a bounded device-side wait
+ * of that call gave up (its outputs are then undefined).  SYNCHRONISES
+ * `stream`.  Allocates nothing; the first call in a context does the same
+ * address look-up as samu_forward_noalloc.  The paper has no counterpart.
+ * Errors: LRS_ERR_ARG (status NULL), LRS_ERR_CUDA. */
+int samu_forward_noalloc_status(int* status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

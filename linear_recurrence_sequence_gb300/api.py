@@ -31,6 +31,7 @@ _I = ctypes.c_int
 _SZP = ctypes.POINTER(ctypes.c_size_t)
 _SIGNATURES = {
     "lrs_status_string": ([_I], ctypes.c_char_p),
+    "samu_status_string": ([_I], ctypes.c_char_p),
     "lrs_version": ([], _I),
     "lrs_device_status": ([_P, ctypes.POINTER(_I), _P], _I),
     "lrs_selftest_wait_timeout": ([_P, _P], _I),
@@ -42,6 +43,7 @@ _SIGNATURES = {
     "samu_forward": ([_P] * 10 + [_I, _I, _I] + [_P] * 6, _I),
     "samu_backward": ([_P] * 12 + [_I, _I, _I] + [_P, _P, _P, _I] + [_P] * 9, _I),
     "samu_forward_noalloc": ([_P] * 10 + [_I, _I, _I] + [_P] * 4, _I),
+    "samu_forward_noalloc_status": ([ctypes.POINTER(_I), _P], _I),
     "samu_decode_params_floats": ([_I, _SZP], _I),
     "samu_decode_prepare": ([_P] * 6 + [_I, _P, _P], _I),
     "samu_decode_step": ([_P] * 6 + [_I, _I, _P, _P, _P], _I),
@@ -437,9 +439,21 @@ def rglru_proj_backward(dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, saved,
     return o
 
 
-def selftest_wait_timeout(scratch) -> None:
-    """Launches the library's failure-path self-test on ``scratch`` (see lrs_selftest_wait_timeout)."""
-    _check("lrs_selftest_wait_timeout", _load().lrs_selftest_wait_timeout(_ptr(scratch), _stream(scratch.device)))
+def selftest_wait_timeout(scratch, device=None) -> None:
+    """Launches the library's failure-path self-test on ``scratch`` (see
+    lrs_selftest_wait_timeout); with ``scratch=None``, on the status word of the
+    no-allocation forward's fixed array (on ``device``)."""
+    dev = scratch.device if scratch is not None else device
+    _check("lrs_selftest_wait_timeout", _load().lrs_selftest_wait_timeout(_ptr(scratch), _stream(dev)))
+
+
+def samu_forward_noalloc_status(device) -> int:
+    """Status word of the most recent ``samu_forward_noalloc`` on ``device``
+    (LRS_OK, or LRS_ERR_TIMEOUT; synchronises the current stream)."""
+    v = ctypes.c_int(0)
+    _check("samu_forward_noalloc_status",
+           _load().samu_forward_noalloc_status(ctypes.byref(v), _stream(device)))
+    return int(v.value)
 
 
 def device_status(scratch, device=None) -> int:

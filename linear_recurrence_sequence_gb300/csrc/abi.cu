@@ -2,6 +2,7 @@
 // workspace carving and kernel launches.  No allocation, no synchronisation
 // (except lrs_device_status, which documents that it synchronises, and the
 // projected RG-LRU's per-thread cuBLAS handle, created on first use).
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cublas_v2.h>
@@ -71,8 +72,8 @@ void prof_end(cudaStream_t s) {
 // on, so that every kernel's events bracket it alone.
 bool pdl_ok() { return !g_prof.on; }
 
-// samu_set_chunk_transition
-int g_transition = LRS_TRANSITION_CLOSED_FORM;
+// samu_set_chunk_transition (read once by each call, from any host thread)
+std::atomic<int> g_transition{LRS_TRANSITION_CLOSED_FORM};
 
 // Kernel ids reported by lrs_profile_end.
 enum {
@@ -209,15 +210,17 @@ const char* lrs_status_string(int status) {
     }
 }
 
-int lrs_version(void) { return 100; }
+const char* samu_status_string(int status) { return lrs_status_string(status); }
+
+int lrs_version(void) { return 101; }
 
 int samu_set_chunk_transition(int kind) {
     if (kind != LRS_TRANSITION_CHAINED && kind != LRS_TRANSITION_CLOSED_FORM) return LRS_ERR_ARG;
-    g_transition = kind;
+    g_transition.store(kind);
     return LRS_OK;
 }
 
-int samu_get_chunk_transition(void) { return g_transition; }
+int samu_get_chunk_transition(void) { return g_transition.load(); }
 
 int lrs_profile_begin(int capacity) {
     if (capacity < 1) return LRS_ERR_ARG;
@@ -256,8 +259,14 @@ int lrs_profile_end(int* kernel_ids, float* ms, int capacity, int* count) {
 }
 
 int lrs_selftest_wait_timeout(void* scratch, cudaStream_t stream) {
-    if (!req(scratch)) return LRS_ERR_ARG;
-    lrs_selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<uint32_t*>(scratch));
+    uint32_t* word = static_cast<uint32_t*>(scratch);
+    if (scratch == nullptr) {   // the no-allocation forward's fixed array
+        const int st = noalloc_status_word(&word);
+        if (st != LRS_OK) return st;
+    } else if (!req(scratch)) {
+        return LRS_ERR_ARG;
+    }
+    lrs_selftest_wait_kernel<<<1, 32, 0, stream>>>(word);
     return cudaGetLastError() == cudaSuccess ? LRS_OK : LRS_ERR_CUDA;
 }
 
@@ -333,7 +342,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     a.g = g;
     a.modes = modes;
     a.nu = nu;
-    a.closed_form = g_transition == LRS_TRANSITION_CLOSED_FORM;
+    a.closed_form = g_transition.load() == LRS_TRANSITION_CLOSED_FORM;
     a.h0 = h0;
     a.y = static_cast<uint32_t*>(y);
     a.y32 = y32;
@@ -385,7 +394,7 @@ int samu_backward(const void* dy, const float* dhT,
     s.g = g;
     s.modes = at<float4>(saved, sv.modes);
     s.nu = nu;
-    s.closed_form = g_transition == LRS_TRANSITION_CLOSED_FORM;
+    s.closed_form = g_transition.load() == LRS_TRANSITION_CLOSED_FORM;
     s.dhT = dhT;
     s.hsub = at<float2>(saved, sv.hsub);
     s.dw = dw;

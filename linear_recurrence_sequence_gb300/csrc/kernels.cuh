@@ -228,7 +228,7 @@ struct SamuScanFwdArgs {
     float2* hsub;           // [B][CS][M] the state every 8 tokens
     float4* smap;           // [B][NS][M] segment maps
     float4* cmap;           // [B][NC][M] CTA maps (four consecutive segments)
-    uint32_t* status;       // cleared by the maps kernel
+    uint32_t* status;       // cleared by the controller forward
 };
 
 // Backward scan over segments: adjoint segment maps, reverse chain prefix,
@@ -349,6 +349,9 @@ cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm
 // reductions of the unit-direction and amplitude gradients.
 cudaError_t launch_samu_ctrl_bwd(const SamuCtrlBwdArgs& args, cudaStream_t s, bool pdl);
 cudaError_t launch_samu_params(const SamuParamArgs& args, cudaStream_t s, bool pdl);
+// The status word of samu_forward_noalloc's fixed array in the current
+// context (its address looked up as that entry point does).
+int noalloc_status_word(uint32_t** out);
 
 // ---------------------------------------------------------------------------
 // SAMU single-token decode step

@@ -10,6 +10,8 @@
 // direction normalisation, using the cached p, r; the per-token partials are
 // reduced in a fixed order ("SAMU strengthened-baseline H800 report",
 // "Reverse complex backward": deterministic FP32 second stage).
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace lrs {
@@ -152,6 +154,10 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The call's status word starts at zero.  This kernel is the call's first
+    // and an ordinary launch; the scan kernels record failures only after
+    // their dependency wait, which ends once this kernel has completed.
+    if (blockIdx.x == 0 && tid == 0 && a.status != nullptr) *a.status = 0u;
     const int D = a.D, M = D / 2, n = D + 1, nch = D / 8;
     const long long BL = a.BL;
     const long long W = (long long)gridDim.x * kCfWarps;
@@ -718,11 +724,13 @@ struct CtrlOcc {
     int sms = 0;
 };
 CtrlOcc g_ctrl_occ[64];
+std::mutex g_ctrl_occ_mutex;   // calls may come from several host threads
 
 int ctrl_sms() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     CtrlOcc& o = g_ctrl_occ[dev];
+    std::lock_guard<std::mutex> lock(g_ctrl_occ_mutex);
     if (!o.done) {
         int v = 0;
         o.sms = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;

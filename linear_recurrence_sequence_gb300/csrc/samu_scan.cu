@@ -32,6 +32,7 @@
 // w (forward) or dy (backward) hit in L2.  Every composition runs in a fixed
 // order: results are bitwise reproducible from run to run.
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 
 #include "kernels.cuh"
@@ -506,7 +507,6 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue_data(R, k, &tm_w, x_re, x_im, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
     pdl_wait();
-    if (gw == 0 && lane == 0) *a.status = 0u;
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
@@ -1102,7 +1102,10 @@ struct EngineOccupancy {
     int bwd = 0;   // ... and for the backward pair (maps, main)
 };
 
+// Per device, filled once under g_occ_mutex (calls may come from several
+// host threads).
 EngineOccupancy g_occ[64];
+std::mutex g_occ_mutex;
 
 bool set_smem(const void* fn, int smem) {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
@@ -1118,6 +1121,7 @@ const EngineOccupancy& engine_occupancy() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     EngineOccupancy& o = g_occ[dev];
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
     if (!o.done) {
         int v = 0;
         o.sms = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;

@@ -162,3 +162,24 @@ def test_projected_rglru_entry_points_reject_null_pointers(lib):
     st = lib.rglru_proj_backward(null, null, null, null, null, null, null, null, null, null, 1, 16, 128,
                                  null, null, 0, null, null, null, null, null, null, null, null)
     assert st == 1
+
+
+def test_noalloc_size_limit_is_checked_before_any_device_call(lib):
+    """samu_forward_noalloc refuses shapes whose intermediates exceed
+    LRS_NOALLOC_BYTES before it touches the device.  Without a GPU, a shape
+    that fits gets past that check and fails at the device look-up instead
+    (LRS_ERR_CUDA); B=1, L=32768, D=2048 must fit, B=1, L=131072, D=1024 not."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: with a device the call would launch kernels")
+    text = open(HEADER).read()
+    assert re.search(r"#define LRS_NOALLOC_BYTES \(64u << 20\)", text)
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+    LRS_ERR_CUDA, LRS_ERR_TOO_LARGE = 3, 5
+    args = [p, p, None, None, p, p, p, p, p, p]
+    assert lib.samu_forward_noalloc(*args, 1, 32768, 2048, p, None, p, None) == LRS_ERR_CUDA
+    assert lib.samu_forward_noalloc(*args, 1, 32768, 2560, p, None, p, None) == LRS_ERR_CUDA
+    assert lib.samu_forward_noalloc(*args, 1, 131072, 1024, p, None, p, None) == LRS_ERR_TOO_LARGE
+    assert lib.samu_status_string(LRS_ERR_TOO_LARGE) == lib.lrs_status_string(LRS_ERR_TOO_LARGE)

@@ -4,7 +4,8 @@ import numpy as np
 import pytest
 
 from linear_recurrence_sequence_gb300 import synth
-from parity import check_samu, run_samu_gpu, run_samu_oracle
+from parity import (check_samu, check_samu_bench_variant, run_samu_gpu, run_samu_gpu_graph,
+                    run_samu_oracle, torch_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -148,3 +149,56 @@ def test_samu_workloads(name, dev):
         fwd, bwd = run_samu_gpu(inp, dev)
         check_samu(inp, fwd, bwd, ref_f, ref_b, label=f"{name}/seed{seed}")
         del ref_f, ref_b, fwd, bwd
+
+
+# ---------------------------------------------------------------------------
+# The kernel variants the benchmark times: the forward without the FP32
+# pre-cast output (replay kernel without y32), BF16 gradients (the reverse
+# replay writes dw through shared memory by TMA when M is a multiple of 64,
+# with plain stores otherwise), the step replayed as a CUDA graph.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["width_2048", "length_128k"])
+def test_samu_benchmarked_variants_full_size(name, dev):
+    """B1 L32K D2048 is the benchmark's own workload; B1 L128K D1024 the longest
+    chain.  BF16 y, dw and dx_sel are checked element by element against RNE
+    of the FP64 oracle; y must equal, bit for bit, the y of a run that also
+    writes the FP32 pre-cast output."""
+    import torch
+    wl = synth.WORKLOADS[name]
+    inp = wl.make(wl.seeds[0])
+    ref_f, ref_b = run_samu_oracle(inp)
+    fo, go = run_samu_gpu_graph(inp, dev)
+    check_samu_bench_variant(inp, fo, go, ref_f, ref_b, label=f"bench_variant/{name}")
+    f32run, _ = run_samu_gpu(inp, dev, grad_fp32=True, want_y32=True)
+    assert torch.equal(f32run["y"], fo["y"])
+    assert torch.equal(f32run["hT"], fo["hT"])
+
+
+BF16_PLAIN_STORE = {
+    # M % 64 != 0: dw leaves the reverse replay through plain BF16 stores
+    "bf16_partial_group_B2_L300_D1552": dict(B=2, L=300, D=1552, seed=14, h0=True, reset_p=0.01),
+    "bf16_B1_L8192_D400": dict(B=1, L=8192, D=400, seed=41, h0=True, reset_p=1 / 4096),
+    "bf16_ragged_B3_L77_D64": dict(B=3, L=77, D=64, seed=11, h0=True, reset_p=0.05),
+    # M % 64 == 0 with a ragged tail and resets: the TMA store path
+    "bf16_tma_B2_L1000_D256": dict(B=2, L=1000, D=256, seed=42, h0=True, reset_p=0.01),
+}
+
+
+@pytest.mark.parametrize("name", list(BF16_PLAIN_STORE))
+def test_samu_bf16_gradient_variants(name, dev):
+    inp = _case(**BF16_PLAIN_STORE[name])
+    ref_f, ref_b = run_samu_oracle(inp)
+    fo, go = run_samu_gpu_graph(inp, dev)
+    check_samu_bench_variant(inp, fo, go, ref_f, ref_b, label=f"bf16_variant/{name}")
+
+
+def test_samu_forward_without_y32_equals_with_y32(dev):
+    """The two replay variants write the same BF16 y and hT bit for bit."""
+    import torch
+    inp = _case(**SMALL["partial_group_B2_L300_D1552"])
+    a, _ = run_samu_gpu(inp, dev, want_y32=True)
+    b, _ = run_samu_gpu(inp, dev, want_y32=False)
+    assert b["y32"] is None
+    assert torch.equal(a["y"], b["y"])
+    assert torch.equal(a["hT"], b["hT"])
+    np.testing.assert_array_equal(torch_bits(a["y"]), torch_bits(b["y"]))

@@ -208,56 +208,133 @@ def gpu_selector(device):
 
 
 # ---------------------------------------------------------------------------
-def oracle_sample_time(B, L, D, seed=0):
-    """Seconds for one FP64 oracle forward+backward on a [B, L, D] SAMU sample."""
-    import oracle
+def _oracle_inputs(B, L, D, seed):
+    """Seeded SAMU sample widened for the oracle: (args, dy, dhT)."""
     from linear_recurrence_sequence_gb300 import synth
     inp = synth.samu_inputs(B, L, D, seed, h0=False)
     f64 = synth.bf16_bits_to_f64
     x, w, dy = f64(inp["x_sel"]), f64(inp["w"]), f64(inp["dy"])
     args = (x, w, inp["h0"], inp["reset"], inp["nu"], inp["theta"], inp["w_phi"], inp["w_r"],
             float(inp["a_phi"]), float(inp["a_r"]))
-    t0 = time.perf_counter()
+    return args, dy, inp["dhT"]
+
+
+def _oracle_fb(args, dy, dhT):
+    import oracle
     oracle.samu_forward(*args)
-    oracle.samu_backward(*args, dy, inp["dhT"])
+    oracle.samu_backward(*args, dy, dhT)
+
+
+def oracle_sample_time(B, L, D, seed=0):
+    """Seconds for one FP64 oracle forward+backward on a [B, L, D] SAMU sample."""
+    args, dy, dhT = _oracle_inputs(B, L, D, seed)
+    t0 = time.perf_counter()
+    _oracle_fb(args, dy, dhT)
     return time.perf_counter() - t0
 
 
+def host_cpu():
+    """Host core count available to this process and the CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return len(os.sched_getaffinity(0)), model or "unknown"
+
+
 def cpu_baseline(D, target_s=12.0):
-    """The oracle as it stands (single thread), on a bounded sample of the
-    workload: B=1, D of the workload, L sized for roughly target_s seconds."""
+    """The oracle as it stands, on bounded samples of the workload (B=1, the
+    workload's D): once on one thread, once on every host core with one
+    independent sample per thread (the oracle is plain C called through
+    ctypes, which releases the interpreter lock; the same kind of parallelism
+    as the method's independent batch rows).  The all-cores rate is the
+    reported value."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores, model = host_cpu()
     t_small = oracle_sample_time(1, 256, D)
     per_tok = t_small / 256
-    L = int(min(32768, max(512, target_s / max(per_tok, 1e-9))))
-    L = max(512, (L // 256) * 256)
-    t = oracle_sample_time(1, L, D, seed=1)
-    return {"value": L / t / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"one FP64 forward+backward at B=1, L={L}, D={D} (single thread), {t:.1f} s"}
+    L1 = int(min(32768, max(512, 0.4 * target_s / max(per_tok, 1e-9))))
+    L1 = max(512, (L1 // 256) * 256)
+    t1 = oracle_sample_time(1, L1, D, seed=1)
+    single = L1 / t1 / 1e6
+    # every core: per thread `reps` forward+backward passes over its own
+    # sample of Lp tokens, inputs drawn before the timed region
+    Lp = max(256, min(4096, (int(0.5 / max(per_tok, 1e-9)) // 256) * 256))
+    reps = max(1, int(0.6 * target_s / max(per_tok * Lp, 1e-9)))
+    samples = [_oracle_inputs(1, Lp, D, 100 + k) for k in range(cores)]
+
+    def work(k):
+        for _ in range(reps):
+            _oracle_fb(*samples[k])
+
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(work, range(cores)))
+        tp = time.perf_counter() - t0
+    par = cores * reps * Lp / tp / 1e6
+    del samples
+    return {"value": par, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": model,
+            "sample": f"{cores} threads, each {reps} FP64 forward+backward passes over its own B=1, L={Lp}, "
+                      f"D={D} sample, {tp:.1f} s wall",
+            "single_thread": {"value": single, "unit": UNIT, "cores": 1,
+                              "sample": f"one FP64 forward+backward at B=1, L={L1}, D={D}, {t1:.1f} s"}}
 
 
 def run_reference(args):
-    """Times the oracle itself: each step is one bounded sample of the workload."""
+    """Times the oracle itself on every host core: each step, every thread runs
+    one FP64 forward+backward over its own bounded sample of the workload
+    (B=1, the workload's D, a shorter L), inputs drawn before the timed steps."""
+    from concurrent.futures import ThreadPoolExecutor
     from linear_recurrence_sequence_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
     D = wl.D
+    cores, model = host_cpu()
     per_step_budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    t_small = oracle_sample_time(1, 128, D)
-    L = int(max(64, min(wl.L, per_step_budget / max(t_small / 128, 1e-9))))
-    L = max(64, (L // 64) * 64)
-    for _ in range(args.warmup):
-        oracle_sample_time(1, L, D)
-    times = [oracle_sample_time(1, L, D, seed=s) for s in range(args.steps)]
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        def one_step(samples):
+            t0 = time.perf_counter()
+            list(ex.map(lambda k: _oracle_fb(*samples[k]), range(cores)))
+            return time.perf_counter() - t0
+        # calibration: one all-threads step on 256-token samples (the threads
+        # share the host's memory system, so a thread runs slower than alone)
+        cal = [_oracle_inputs(1, 256, D, 300 + k) for k in range(cores)]
+        one_step(cal)
+        t_cal = one_step(cal)
+        del cal
+        L = int(max(64, min(wl.L, 8192, per_step_budget / max(t_cal / 256, 1e-9))))
+        L = max(64, (L // 64) * 64)
+        samples = [_oracle_inputs(1, L, D, 200 + k) for k in range(cores)]
+        for _ in range(args.warmup):
+            one_step(samples)
+        times = [one_step(samples) for _ in range(args.steps)]
     total = sum(times)
-    value = args.steps * L / total / 1e6
+    value = args.steps * cores * L / total / 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"samu_fb_B{wl.B}_L{wl.L}_D{wl.D}", "B": wl.B, "L": wl.L, "D": wl.D,
-                   "sample_per_step": f"B=1, L={L}, D={D}"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"each step one FP64 forward+backward at B=1, L={L}, D={D}"},
+                   "sample_per_step": f"{cores} x (B=1, L={L}, D={D})",
+                   "sample_note": f"the sample's L is shorter than the workload's L={wl.L} so that the run "
+                                  "ends within a few minutes: the oracle is one sequential pass over the "
+                                  "tokens, so its tokens per second do not depend on L"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": model,
+                         "sample": f"each step {cores} threads, each one FP64 forward+backward over its own "
+                                   f"B=1, L={L}, D={D} sample"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -408,22 +485,29 @@ def run_ours(args, rank, world, local):
             "din": [torch.empty_like(t["x_sel"]) for _ in range(3)],
             "fo": dfo, "go": dgo,
             "hout": [torch.empty((B, L, D), dtype=torch.bfloat16).pin_memory() for _ in range(3)],
-            "hsmall": {},
+            "hsmall": {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in dgo.items()
+                       if k in small_keys},
             "in_ready": torch.cuda.Event(), "done": torch.cuda.Event(), "out_read": torch.cuda.Event(),
         })
     h2d = 3 * BLD * 2
     d2h = 3 * BLD * 2 + 4 * (B * M * 2)
+    copy_ev = []   # per timed step: (H2D start, H2D end, D2H start, D2H end) events
     comp = torch.cuda.current_stream(dev)
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
 
-    def e2e_steps(n):
+    def e2e_steps(n, timed=False):
         for i in range(n):
             S = sets[i % 2]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
             with torch.cuda.stream(s_in):
                 s_in.wait_event(S["done"])            # step i-2 has finished with this set's inputs
+                if timed:
+                    ev[0].record(s_in)
                 for d_, h_ in zip(S["din"], hin):
                     d_.copy_(h_, non_blocking=True)
+                if timed:
+                    ev[1].record(s_in)
                 S["in_ready"].record(s_in)
             comp.wait_event(S["in_ready"])
             comp.wait_event(S["out_read"])           # step i-2's results have left this set
@@ -437,11 +521,17 @@ def run_ours(args, rank, world, local):
             S["done"].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(S["done"])
+                if timed:
+                    ev[2].record(s_out)
                 for h_, d_ in zip(S["hout"], (fo_i["y"], g["dx_sel"], g["dw"])):
                     h_.copy_(d_, non_blocking=True)
                 for k in small_keys:
-                    S["hsmall"][k] = g[k].to("cpu", non_blocking=True)
+                    S["hsmall"][k].copy_(g[k], non_blocking=True)
+                if timed:
+                    ev[3].record(s_out)
                 S["out_read"].record(s_out)
+            if timed:
+                copy_ev.append(ev)
 
     for S in sets:   # events start "recorded" so that the first waits pass
         S["done"].record(comp)
@@ -453,13 +543,24 @@ def run_ours(args, rank, world, local):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(comp)
-    e2e_steps(K2)
+    e2e_steps(K2, timed=True)
     comp.wait_stream(s_out)
     comp.wait_stream(s_in)
     e1.record(comp)
     e1.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     d2h += sum(v.numel() * 4 for k, v in sets[0]["hsmall"].items() if k != "dh0")
+    # copy rates inside the timed region: each step's H2D (resp. D2H) block
+    # between its own events on the copy stream
+    h2d_ms = statistics.median(ev[0].elapsed_time(ev[1]) for ev in copy_ev)
+    d2h_ms = statistics.median(ev[2].elapsed_time(ev[3]) for ev in copy_ev)
+    # step i's D2H block runs beside step i+1's H2D block
+    def _ov(a, b):
+        lo = max(e0.elapsed_time(a[0]), e0.elapsed_time(b[2]))
+        hi = min(e0.elapsed_time(a[1]), e0.elapsed_time(b[3]))
+        return max(0.0, hi - lo) / max(1e-9, min(a[0].elapsed_time(a[1]), b[2].elapsed_time(b[3])))
+    overlap = statistics.median(_ov(copy_ev[i + 1], copy_ev[i]) for i in range(len(copy_ev) - 1)) \
+        if len(copy_ev) > 1 else 0.0
     e2e_ms = reduce_max(e2e_ms, world, dev)
     e2e_value = world * B * L * K2 / (e2e_ms / 1e3) / 1e6
 
@@ -478,8 +579,13 @@ def run_ours(args, rank, world, local):
         "kernels_avg_ms": {k: round(v, 5) for k, v in sorted(avg.items())},
         "gpu_launches": launches,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": K2,
-                "overlap": "two buffer sets; H2D of step i+1 and D2H of step i-1 overlap step i"},
+                "d2h_bytes_per_step": d2h, "steps": K2, "ms_per_step": round(e2e_ms / K2, 4),
+                "h2d_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms / 1e3) / 1e9, 1),
+                "copy_overlap": round(overlap, 3),
+                "overlap": "two buffer sets; H2D of step i+1 and D2H of step i-1 overlap step i",
+                "rates": "median per-step H2D and D2H block durations between events on the copy streams; "
+                         "copy_overlap: median share of the shorter of step i's D2H and step i+1's H2D during which "
+                         "both ran"},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -392,6 +392,7 @@ int samu_backward(const void* dy, const float* dhT,
         return LRS_ERR_CUDA;
     SamuScanBwdArgs s;
     s.g = g;
+    s.ctrl = ctrl;
     s.modes = at<float4>(saved, sv.modes);
     s.nu = nu;
     s.closed_form = g_transition.load() == LRS_TRANSITION_CLOSED_FORM;

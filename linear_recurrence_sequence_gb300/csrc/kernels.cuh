@@ -236,6 +236,7 @@ struct SamuScanFwdArgs {
 // token from later tokens.
 struct SamuScanBwdArgs {
     SegGeom g;
+    const float4* ctrl;     // [B*L][2] the forward's control words (per-segment kind check)
     const float4* modes;    // [2][M] lbar, lbar^16 (hi/lo)
     const float* nu;
     int closed_form;        // full items without a reset: closed-form transition

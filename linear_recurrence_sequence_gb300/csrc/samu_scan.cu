@@ -58,14 +58,10 @@ struct alignas(128) WarpRingT {
     float4 ctrl[S][2 * R];           // [slot][token: two float4]
     uint64_t full[S];
 };
-// The maps and replay kernels stage kMapRows-token items, kMapSlots per warp;
-// the reverse replay 8-token units (a w item and a dy item each), 4 per warp.
+// The maps and replay kernels stage kMapRows-token items, kMapSlots per warp
+// (the reverse replay's ring, one slot per 8-token unit, is defined with it).
 using MapRing = WarpRingT<kMapRows, kMapSlots>;
-using RevRing = WarpRingT<kHalf, 4>;
-using RevRingTma = WarpRingT<kHalf, 6>;   // dw staged in the dy slots: two more slots cover the deferred refill
-constexpr int kRevTmaSmem = kEngineWarps * (int)sizeof(RevRingTma);
-static_assert(RevRingTma::kSlots % 2 == 0, "w and dy items alternate over the slots");
-constexpr int kWarpSmem = (int)(sizeof(MapRing) > sizeof(RevRing) ? sizeof(MapRing) : sizeof(RevRing));
+constexpr int kWarpSmem = (int)sizeof(MapRing);
 constexpr int kEngineSmem = kEngineWarps * kWarpSmem;
 
 template <class Ring>
@@ -826,37 +822,75 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
 
 // ---------------------------------------------------------------------------
 // Reverse replay.  It walks each segment backwards in units of 8 tokens, the
-// distance between the forward's state checkpoints, through a ring of 8-row
-// items: for every unit the w rows (forward sweep) and then the dy rows
-// (reverse sweep).  The forward sweep keeps lambda_t and u_t = lambda_t z_{t-1}
-// of all 8 tokens in registers, so lambda is evaluated once per token.
+// distance between the forward's state checkpoints.  One ring slot holds a
+// whole unit: its w rows, its dy rows (overwritten by its dw rows when dw
+// leaves by TMA) and its control words, so a unit costs one wait and one
+// refill.  The forward sweep rebuilds the unit's states from the checkpoint
+// with the forward replay's own step (the same bits) and keeps lambda_t and
+// the state z_{t-1} entering every token in registers; the reverse sweep
+// then runs the adjoint.
 // ---------------------------------------------------------------------------
-// Forward sweep of one unit from its entry state: lambda_t and
-// u_t = lambda_t z_{t-1} (kept for kappa), z_t = u_t + b_t.  A reset token
-// gets lambda_t = 0.
+template <int S>
+struct alignas(128) RevRingT {
+    static constexpr int kSlots = S;
+    static constexpr int kUnitBytes = 4 * kHalf * kRowBytes + kHalf * kCtlBytes;
+    uint32_t w[S][2][kHalf][kWords];   // [slot][re, im][token][pair]
+    uint32_t g[S][2][kHalf][kWords];   // dy rows, then (TMA variant) dw rows
+    float4 ctrl[S][2 * kHalf];         // [slot][token: two float4]
+    uint64_t full[S];
+};
+using RevRing = RevRingT<3>;
+constexpr int kRevSmem = kEngineWarps * (int)sizeof(RevRing);
+static_assert(sizeof(float4) * 2 * 32 <= sizeof(((RevRing*)nullptr)->w[0]),
+              "a slot's w rows hold the prologue's partial maps");
+
+__device__ __forceinline__ RevRing& rev_ring(uint8_t* smem_raw, int warp) {
+    return *reinterpret_cast<RevRing*>(smem_raw + (size_t)warp * sizeof(RevRing));
+}
+
+// Lane 0: the w and dy rows of the unit at token ts into `slot` (the slot's
+// expected bytes include the control words: it completes once
+// rev_issue_ctrl has been issued too).
+__device__ __forceinline__ void rev_issue_data(RevRing& R, int slot, const CUtensorMap* tm_w, const CUtensorMap* tm_dy,
+                                               int x_re, int x_im, int ts, int b) {
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&R.full[slot], RevRing::kUnitBytes);
+    tma_load_3d(&R.w[slot][0][0][0], tm_w, x_re, ts, b, &R.full[slot]);
+    tma_load_3d(&R.w[slot][1][0][0], tm_w, x_im, ts, b, &R.full[slot]);
+    tma_load_3d(&R.g[slot][0][0][0], tm_dy, x_re, ts, b, &R.full[slot]);
+    tma_load_3d(&R.g[slot][1][0][0], tm_dy, x_im, ts, b, &R.full[slot]);
+}
+__device__ __forceinline__ void rev_issue_ctrl(RevRing& R, int slot, const CUtensorMap* tm_ctrl, int ts, int b) {
+    tma_load_3d(&R.ctrl[slot][0], tm_ctrl, 0, ts, b, &R.full[slot]);
+}
+
+// Forward sweep of one unit from its entry state z: for every token lambda_t
+// and the state z_{t-1} entering it; z_t = lambda_t z_{t-1} + b_t with the
+// forward replay's expression.  A reset token gets lambda_t = 0 (z_t = b_t).
 template <bool FAST, bool SIMPLE>
-__device__ __forceinline__ void bwd_forward_unit(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nh,
-                                                 const ModePair& k, c2x z, c2x (&u)[kHalf], f2x (&lre)[kHalf],
-                                                 f2x (&lim)[kHalf]) {
+__device__ __forceinline__ void rev_forward_sweep(const float4* sc, const uint32_t* wre, const uint32_t* wim, int nh,
+                                                  const ModePair& k, c2x z, c2x (&zp)[kHalf], f2x (&lre)[kHalf],
+                                                  f2x (&lim)[kHalf]) {
 #pragma unroll
     for (int i = 0; i < kHalf; ++i) {
-        u[i] = czero();
+        zp[i] = z;
         lre[i] = 0ull;
         lim[i] = 0ull;
         if (SIMPLE || i < nh) {
             const Ctl2 ct = load_ctl(sc, i);
-            c2x bb;
-            bb.re = bf2x(wre[i * kWords]);
-            bb.im = bf2x(wim[i * kWords]);
+            const f2x bre = bf2x(wre[i * kWords]);
+            const f2x bim = bf2x(wim[i * kWords]);
             if (SIMPLE || !is_reset(ct)) {
                 const Lam2 l = samu_lambda2<FAST>(k, ct);
-                u[i] = cmul2(l, z);
-                z.re = add2(u[i].re, bb.re);
-                z.im = add2(u[i].im, bb.im);
+                const f2x zr = fma2(l.re, z.re, fma2(l.nim, z.im, bre));
+                const f2x zi = fma2(l.re, z.im, fma2(l.im, z.re, bim));
+                z.re = zr;
+                z.im = zi;
                 lre[i] = l.re;
                 lim[i] = l.im;
             } else {
-                z = bb;
+                z.re = bre;
+                z.im = bim;
             }
         }
     }
@@ -883,25 +917,26 @@ __device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane)
 enum DwStore { kDwBf16 = 0, kDwFp32 = 1, kDwBf16Tma = 2 };
 
 // Reverse sweep of one unit: A_t = dy_t + (adjoint from t+1); dw_t = A_t;
-// kappa_t = A_t conj(u_t); dtheta_m += Im kappa, dnu_m += -E_t Re kappa; per
-// token dbar += Im kappa and Ebar += -nu_m Re kappa summed over the 64 modes
-// of the warp (written to kp[token * kp_row + {0, 1}]); then
-// A <- conj(lambda_t) A.  DW == kDwBf16Tma: dw_t replaces dy_t in the staged
-// box (every lane active), stored by TMA afterwards.
+// A'_t = conj(lambda_t) A_t, the adjoint passed to t-1; then
+// kappa_t = A_t conj(lambda_t z_{t-1}) = A'_t conj(z_{t-1});
+// dtheta_m += Im kappa, dnu_m += -E_t Re kappa; per token dbar += Im kappa
+// and Ebar += -nu_m Re kappa summed over the 64 modes of the warp (written
+// to kp[token * kp_row + {0, 1}]).  DW == kDwBf16Tma: dw_t replaces dy_t in
+// the staged rows (every lane active), stored by TMA afterwards.
 template <bool SIMPLE, int DW>
-__device__ __forceinline__ void bwd_reverse_unit(const float4* sc, uint32_t* gre, uint32_t* gim, int nh,
-                                                 float nu0, float nu1, const c2x (&u)[kHalf],
-                                                 const f2x (&lre)[kHalf], const f2x (&lim)[kHalf], c2x& A,
-                                                 f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf,
-                                                 bool active, size_t row, int half, float* kp, size_t kp_row,
-                                                 int lane) {
+__device__ __forceinline__ void rev_reverse_sweep(const float4* sc, uint32_t* gre, uint32_t* gim, int nh,
+                                                  float nu0, float nu1, const c2x (&zp)[kHalf],
+                                                  const f2x (&lre)[kHalf], const f2x (&lim)[kHalf], c2x& A,
+                                                  f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf,
+                                                  bool active, size_t row, int half, float* kp, size_t kp_row,
+                                                  int lane) {
     float v[2 * kHalf];
 #pragma unroll
     for (int i = kHalf - 1; i >= 0; --i) {
         v[2 * i] = 0.f;
         v[2 * i + 1] = 0.f;
         if (SIMPLE || i < nh) {
-            const Ctl2 ct = load_ctl(sc, i);
+            const float rw = sc[2 * i + 1].z;   // -E, or +0 at a segment start
             A.re = add2(A.re, bf2x(gre[i * kWords]));
             A.im = add2(A.im, bf2x(gim[i * kWords]));
             if (DW == kDwBf16Tma) {
@@ -918,22 +953,22 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, uint32_t* gre
                     __stcs(p + half, x2bf(A.im));
                 }
             }
-            if (SIMPLE || !is_reset(ct)) {
-                // kappa = A conj(u)
-                const f2x kr = fma2(A.re, u[i].re, mul2(A.im, u[i].im));
-                const f2x ki = fma2(A.im, u[i].re, mul2(sub2(0ull, A.re), u[i].im));
-                acc_nu = fma2(ct.ne, kr, acc_nu);   // -E_t Re kappa
+            if (SIMPLE || !is_reset_word(rw)) {
+                // A' = conj(lambda) A
+                const f2x ar = fma2(lre[i], A.re, mul2(lim[i], A.im));
+                const f2x ai = fma2(lre[i], A.im, mul2(sub2(0ull, lim[i]), A.re));
+                // kappa = A' conj(z_{t-1})
+                const f2x kr = fma2(ar, zp[i].re, mul2(ai, zp[i].im));
+                const f2x ki = fma2(ai, zp[i].re, mul2(sub2(0ull, ar), zp[i].im));
+                acc_nu = fma2(dup2(rw), kr, acc_nu);   // -E_t Re kappa
                 acc_th = add2(acc_th, ki);
                 float ki0, ki1, kr0, kr1;
                 up2(ki, ki0, ki1);
                 up2(kr, kr0, kr1);
                 v[2 * i] = ki0 + ki1;
                 v[2 * i + 1] = -__fmaf_rn(nu0, kr0, __fmul_rn(nu1, kr1));
-                Lam2 l;
-                l.re = lre[i];
-                l.im = lim[i];
-                l.nim = sub2(0ull, lim[i]);
-                A = cmulc2(l, A);
+                A.re = ar;
+                A.im = ai;
             } else {   // segment start: no controller terms, the adjoint stops here
                 A = czero();
             }
@@ -941,6 +976,41 @@ __device__ __forceinline__ void bwd_reverse_unit(const float4* sc, uint32_t* gre
     }
     const float tot = warp_reduce_scatter16(v, lane);
     if (lane < 2 * kHalf && (lane >> 1) < nh) kp[(size_t)(lane >> 1) * kp_row + (lane & 1)] = tot;
+}
+
+// One unit (forward sweep, reverse sweep) of kind <FAST, SIMPLE>.
+template <bool FAST, bool SIMPLE, int DW>
+__device__ __forceinline__ void rev_unit(RevRing& R, int slot, int nh, const ModePair& k, float nu0, float nu1,
+                                         const c2x& z, c2x& A, f2x& acc_nu, f2x& acc_th, uint32_t* dwb, float* dwf,
+                                         bool active, size_t row, int half, float* kp, size_t kp_row, int lane) {
+    const float4* sc = R.ctrl[slot];
+    c2x zp[kHalf];
+    f2x lre[kHalf], lim[kHalf];
+    rev_forward_sweep<FAST, SIMPLE>(sc, &R.w[slot][0][0][lane], &R.w[slot][1][0][lane], nh, k, z, zp, lre, lim);
+    rev_reverse_sweep<SIMPLE, DW>(sc, &R.g[slot][0][0][lane], &R.g[slot][1][0][lane], nh, nu0, nu1, zp, lre, lim, A,
+                                  acc_nu, acc_th, dwb, dwf, active, row, half, kp, kp_row, lane);
+}
+
+// Warp-uniform facts about the whole segment [t_begin, t_end), read from the
+// control words in global memory: simple (no reset, whole units only) and
+// fast (|nu| max|E - 1| < kPolyBound for every lane's modes).  A segment that
+// is both runs every unit on the branch-free polynomial path; one that is not
+// decides per unit (sub_kind), as the forward replay does per item.
+__device__ __forceinline__ SubKind segment_kind(const float4* __restrict__ ctrl, long long row0, int n, int lane,
+                                                const ModePair& k) {
+    float emax = 0.f;
+    bool rst = false;
+    for (int i = lane; i < n; i += 32) {
+        emax = fmaxf(emax, fabsf(__ldg(&ctrl[2 * (row0 + i)].x)));
+        rst = rst || is_reset_word(__ldg(&ctrl[2 * (row0 + i) + 1].z));
+    }
+    emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(emax)));
+    float n0, n1;
+    up2(k.nu, n0, n1);
+    SubKind kd;
+    kd.fast = __all_sync(0xffffffffu, fabsf(n0) * emax < kPolyBound && fabsf(n1) * emax < kPolyBound);
+    kd.simple = !__any_sync(0xffffffffu, rst) && n % kHalf == 0;
+    return kd;
 }
 
 template <int DW>
@@ -951,9 +1021,8 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    using Ring = typename std::conditional<DW == kDwBf16Tma, RevRingTma, RevRing>::type;
-    Ring& R = *reinterpret_cast<Ring*>(smem_raw + (size_t)warp * sizeof(Ring));
-    constexpr int kRingH = Ring::kSlots;
+    RevRing& R = rev_ring(smem_raw, warp);
+    constexpr int kS = RevRing::kSlots;
     const SegGeom& g = a.g;
     const long long gw = (long long)blockIdx.x * kEngineWarps + warp;
     const SegTask T = seg_task(g, gw);
@@ -964,30 +1033,33 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     const bool active = m < M;
     const int x_re = T.grp * kGroup, x_im = M + T.grp * kGroup;
     const int n_units = T.t_end > T.t_begin ? (T.t_end - T.t_begin + kHalf - 1) / kHalf : 0;
-    const int n_items = 2 * n_units;
-    // item k: unit n_units-1-k/2 (the segment from its end backwards); even
-    // items carry w (forward sweep), odd items dy (reverse sweep)
-    auto item_ts = [&](int k) { return T.t_begin + (n_units - 1 - (k >> 1)) * kHalf; };
-    ring_init(R, lane);
+    // unit u: tokens from ts(u), the segment from its end backwards
+    auto unit_ts = [&](int u) { return T.t_begin + (n_units - 1 - u) * kHalf; };
+    if (lane == 0)
+        for (int s = 0; s < kS; ++s) mbar_init(&R.full[s], 1);
+    __syncwarp();
     pdl_trigger();
-    if (lane == 0)   // w and dy (inputs) before the wait for the maps kernel, control words after it
-        for (int k = 0; k < kRingH && k < n_items; ++k)
-            ring_issue_data(R, k, (k & 1) ? &tm_dy : &tm_w, x_re, x_im, item_ts(k), T.b);
-    pdl_wait();
-    // the adjoint arriving at the CTA from the later CTAs' maps (the rings'
-    // control-word areas, not yet filled, carry the warps' partial maps)
-    const int cc = T.s / kSegPerCta;
-    const c2x a0 = cta_entry_bwd(
-        a.cmap + (size_t)T.b * g.NC * M + m, cc, g.NC, M, a.dhT != nullptr ? a.dhT + ((size_t)T.b * M + m) * 2 : nullptr,
-        [&](int w) { return &reinterpret_cast<Ring*>(smem_raw + (size_t)w * sizeof(Ring))->ctrl[0][0]; }, warp, lane,
-        active);
-    if (lane == 0) {
-        fence_proxy_async();
-        for (int k = 0; k < kRingH && k < n_items; ++k) ring_issue_ctrl(R, k, &tm_ctrl, item_ts(k), T.b);
-    }
+    // w, dy (inputs) and the forward's control words and checkpoints (written
+    // before the previous, ordinary launch) are read before the dependency
+    // wait; slot kS - 1's w rows carry the prologue's partial maps, so its
+    // unit goes out after the fold.
+    if (lane == 0)
+        for (int u = 0; u < kS - 1 && u < n_units; ++u) rev_issue_data(R, u, &tm_w, &tm_dy, x_re, x_im, unit_ts(u), T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
+    const SubKind seg_kd = segment_kind(a.ctrl, (long long)T.b * L + T.t_begin, T.t_end - T.t_begin, lane, k);
+    pdl_wait();
+    // the adjoint arriving at the CTA from the later CTAs' maps
+    const int cc = T.s / kSegPerCta;
+    const c2x a0 = cta_entry_bwd(
+        a.cmap + (size_t)T.b * g.NC * M + m, cc, g.NC, M, a.dhT != nullptr ? a.dhT + ((size_t)T.b * M + m) * 2 : nullptr,
+        [&](int w) { return reinterpret_cast<float4*>(&rev_ring(smem_raw, w).w[kS - 1][0][0][0]); }, warp, lane,
+        active);
+    if (lane == 0) {
+        if (kS - 1 < n_units) rev_issue_data(R, kS - 1, &tm_w, &tm_dy, x_re, x_im, unit_ts(kS - 1), T.b);
+        for (int u = 0; u < kS && u < n_units; ++u) rev_issue_ctrl(R, u, &tm_ctrl, unit_ts(u), T.b);
+    }
     c2x A = czero();
     if (active) {   // the adjoint arriving at the CTA through the maps of the later segments of the CTA
         float2 r0, r1;
@@ -1015,70 +1087,82 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         A.im = pk2(r0.y, r1.y);
     }
     f2x acc_nu = 0ull, acc_th = 0ull;
-    for (int it = 0; it < n_items; it += 2) {
-        const int ts = item_ts(it);
+    const size_t kp_row = 2 * (size_t)g.n_groups;
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int u = 0; u < n_units; ++u) {
+        const int ts = unit_ts(u);
         const int nh = min(kHalf, T.t_end - ts);
-        c2x z = czero();
+        c2x z = czero();   // the forward's checkpoint: the state entering token ts
         if (active) {
             const f2x* hs = reinterpret_cast<const f2x*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m);
             z.re = hs[0];
             z.im = hs[1];
         }
-        // w item: forward sweep
-        int slot = it % kRingH;
-        if (!ring_wait(R, it, n_items, a.status, lane)) {
-            if (DW == kDwBf16Tma && lane == 0) bulk_wait_all();
-            return;
-        }
-        const float4* sc = R.ctrl[slot];
-        const SubKind kd = sub_kind<kHalf>(sc, nh, lane, k);
-        c2x u[kHalf];
-        f2x lre[kHalf], lim[kHalf];
-        LRS_SUB_DISPATCH(kd, bwd_forward_unit, sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, k, z, u,
-                         lre, lim);
-        __syncwarp();
-        if (lane == 0 && it + kRingH < n_items)
-            ring_issue(R, slot, ((it + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im, item_ts(it + kRingH),
-                        T.b);
-        // dy item: reverse sweep
-        slot = (it + 1) % kRingH;
-        if (!ring_wait(R, it + 1, n_items, a.status, lane)) {
-            if (DW == kDwBf16Tma && lane == 0) bulk_wait_all();
-            return;
-        }
-        sc = R.ctrl[slot];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
         float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
         float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
-        if (kd.simple)
-            bwd_reverse_unit<true, DW>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u, lre,
-                                       lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
-                                       2 * (size_t)g.n_groups, lane);
-        else
-            bwd_reverse_unit<false, DW>(sc, &R.box[slot][0][0][lane], &R.box[slot][1][0][lane], nh, nu0, nu1, u,
-                                        lre, lim, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2, kp,
-                                        2 * (size_t)g.n_groups, lane);
+        if (!mbar_wait_bounded(&R.full[slot], phase)) {
+            if (lane == 0) {
+                atomicOr(a.status, kStatusTimeout);
+                if (DW == kDwBf16Tma) bulk_wait_all();
+            }
+            // the copies still in flight: units up to u + kS - 1 (the TMA-store
+            // variant refills one unit later: up to max(kS - 1, u + 1))
+            const int last = DW == kDwBf16Tma ? max(kS - 1, u + 1) : u + kS - 1;
+            for (int j = u + 1; j <= last && j < n_units; ++j)
+                mbar_wait_bounded(&R.full[j % kS], (uint32_t)(j / kS) & 1u);
+            return;
+        }
+        if (seg_kd.fast && seg_kd.simple) {
+            rev_unit<true, true, DW>(R, slot, nh, k, nu0, nu1, z, A, acc_nu, acc_th, dwb, dwf, active, D / 2, M / 2,
+                                     kp, kp_row, lane);
+        } else {
+            const SubKind kd = sub_kind<kHalf>(R.ctrl[slot], nh, lane, k);
+            if (kd.fast) {
+                if (kd.simple)
+                    rev_unit<true, true, DW>(R, slot, nh, k, nu0, nu1, z, A, acc_nu, acc_th, dwb, dwf, active, D / 2,
+                                             M / 2, kp, kp_row, lane);
+                else
+                    rev_unit<true, false, DW>(R, slot, nh, k, nu0, nu1, z, A, acc_nu, acc_th, dwb, dwf, active, D / 2,
+                                              M / 2, kp, kp_row, lane);
+            } else {
+                if (kd.simple)
+                    rev_unit<false, true, DW>(R, slot, nh, k, nu0, nu1, z, A, acc_nu, acc_th, dwb, dwf, active,
+                                              D / 2, M / 2, kp, kp_row, lane);
+                else
+                    rev_unit<false, false, DW>(R, slot, nh, k, nu0, nu1, z, A, acc_nu, acc_th, dwb, dwf, active,
+                                               D / 2, M / 2, kp, kp_row, lane);
+            }
+        }
         if (DW == kDwBf16Tma) {
             // the unit's dw rows are in this slot: TMA-store them, then refill
-            // the previous unit's dy slot once its store has read it
+            // the previous unit's slot once its store has read it
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
-                tma_store_3d(&tm_dw, x_re, ts, T.b, &R.box[slot][0][0][0]);
-                tma_store_3d(&tm_dw, x_im, ts, T.b, &R.box[slot][1][0][0]);
+                tma_store_3d(&tm_dw, x_re, ts, T.b, &R.g[slot][0][0][0]);
+                tma_store_3d(&tm_dw, x_im, ts, T.b, &R.g[slot][1][0][0]);
                 bulk_commit();
-                const int j = it - 1 + kRingH;   // a dy item (kRingH is even)
-                if (it >= 2 && j < n_items) {
+                const int j = u - 1 + kS;
+                if (u >= 1 && j < n_units) {
                     bulk_wait_read<1>();
-                    ring_issue(R, (it - 1) % kRingH, &tm_dy, &tm_ctrl, x_re, x_im, item_ts(j), T.b);
+                    const int ps = slot == 0 ? kS - 1 : slot - 1;
+                    rev_issue_data(R, ps, &tm_w, &tm_dy, x_re, x_im, unit_ts(j), T.b);
+                    rev_issue_ctrl(R, ps, &tm_ctrl, unit_ts(j), T.b);
                 }
             }
         } else {
             __syncwarp();
-            if (lane == 0 && it + 1 + kRingH < n_items)
-                ring_issue(R, slot, ((it + 1 + kRingH) & 1) ? &tm_dy : &tm_w, &tm_ctrl, x_re, x_im,
-                            item_ts(it + 1 + kRingH), T.b);
+            if (lane == 0 && u + kS < n_units) {
+                rev_issue_data(R, slot, &tm_w, &tm_dy, x_re, x_im, unit_ts(u + kS), T.b);
+                rev_issue_ctrl(R, slot, &tm_ctrl, unit_ts(u + kS), T.b);
+            }
+        }
+        if (++slot == kS) {
+            slot = 0;
+            phase ^= 1u;
         }
     }
     if (DW == kDwBf16Tma && lane == 0) bulk_wait_all();
@@ -1132,7 +1216,7 @@ const EngineOccupancy& engine_occupancy() {
                              reinterpret_cast<const void*>(samu_bwd_main_kernel<kDwBf16>),
                              reinterpret_cast<const void*>(samu_bwd_main_kernel<kDwFp32>),
                              reinterpret_cast<const void*>(samu_bwd_main_kernel<kDwBf16Tma>)};
-        const int bwd_smem[] = {kEngineSmem, kEngineSmem, kEngineSmem, kRevTmaSmem};
+        const int bwd_smem[] = {kEngineSmem, kRevSmem, kRevSmem, kRevSmem};
         o.fwd = 1 << 30;
         for (const void* f : fwd) {
             set_smem(f, kEngineSmem);
@@ -1186,12 +1270,12 @@ cudaError_t launch_samu_bwd_main(const CUtensorMap& tm_dy, const CUtensorMap& tm
                                  const CUtensorMap& tm_dw, const SamuScanBwdArgs& args, cudaStream_t s, bool pdl) {
     const unsigned grid = engine_grid(args.g);
     if (args.grad_fp32)
-        return launch_ex(samu_bwd_main_kernel<kDwFp32>, grid, kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_w, tm_ctrl,
+        return launch_ex(samu_bwd_main_kernel<kDwFp32>, grid, kEngineThreads, kRevSmem, s, pdl, tm_dy, tm_w, tm_ctrl,
                          tm_dw, args);
     if (args.g.M % kGroup == 0)
-        return launch_ex(samu_bwd_main_kernel<kDwBf16Tma>, grid, kEngineThreads, kRevTmaSmem, s, pdl, tm_dy, tm_w,
+        return launch_ex(samu_bwd_main_kernel<kDwBf16Tma>, grid, kEngineThreads, kRevSmem, s, pdl, tm_dy, tm_w,
                          tm_ctrl, tm_dw, args);
-    return launch_ex(samu_bwd_main_kernel<kDwBf16>, grid, kEngineThreads, kEngineSmem, s, pdl, tm_dy, tm_w, tm_ctrl,
+    return launch_ex(samu_bwd_main_kernel<kDwBf16>, grid, kEngineThreads, kRevSmem, s, pdl, tm_dy, tm_w, tm_ctrl,
                      tm_dw, args);
 }
 

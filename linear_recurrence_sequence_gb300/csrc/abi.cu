@@ -313,10 +313,13 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     float* p = at<float>(saved, sv.p);
     float* r = at<float>(saved, sv.r);
     float4* ctrl = at<float4>(saved, sv.ctrl);
+    float4* items = at<float4>(saved, sv.items);
 
     float4* modes = at<float4>(saved, sv.modes);
     SamuCtrlFwdArgs cf;
     cf.BL = BL;
+    cf.B = B;
+    cf.L = L;
     cf.D = D;
     cf.x = static_cast<const uint4*>(x_sel);
     cf.reset = reset;
@@ -329,6 +332,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     cf.p = p;
     cf.r = r;
     cf.ctrl = ctrl;
+    cf.items = items;
     cf.wh = wh;
     cf.misc = misc;
     cf.modes = modes;
@@ -340,6 +344,7 @@ int samu_forward(const void* x_sel, const void* w, const float* h0, const uint8_
     if (!make_bf16_map(&tm_w, w, B, L, D, kMapRows) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kMapRows)) return LRS_ERR_CUDA;
     SamuScanFwdArgs a;
     a.g = g;
+    a.items = items;
     a.modes = modes;
     a.nu = nu;
     a.closed_form = g_transition.load() == LRS_TRANSITION_CLOSED_FORM;
@@ -392,7 +397,7 @@ int samu_backward(const void* dy, const float* dhT,
         return LRS_ERR_CUDA;
     SamuScanBwdArgs s;
     s.g = g;
-    s.ctrl = ctrl;
+    s.items = at<float4>(saved, sv.items);
     s.modes = at<float4>(saved, sv.modes);
     s.nu = nu;
     s.closed_form = g_transition.load() == LRS_TRANSITION_CLOSED_FORM;

@@ -218,6 +218,7 @@ __device__ __forceinline__ c2x cfma2(const c2x& P, const c2x& bb, f2x nb_im, con
 // boxes); everything indexed by segment is [B][NS][M] (per mode).
 struct SamuScanFwdArgs {
     SegGeom g;
+    const float4* items;    // [B][items per row] the controller's item records (per-item plan)
     const float4* modes;    // [2][M] lbar, lbar^16 (hi/lo)
     const float* nu;
     int closed_form;        // full items without a reset: closed-form transition
@@ -236,7 +237,7 @@ struct SamuScanFwdArgs {
 // token from later tokens.
 struct SamuScanBwdArgs {
     SegGeom g;
-    const float4* ctrl;     // [B*L][2] the forward's control words (per-segment kind check)
+    const float4* items;    // [B][items per row] the forward's item records (per-item plan, per-segment kind)
     const float4* modes;    // [2][M] lbar, lbar^16 (hi/lo)
     const float* nu;
     int closed_form;        // full items without a reset: closed-form transition
@@ -309,6 +310,7 @@ struct SamuParamArgs {
 
 struct SamuCtrlFwdArgs {
     long long BL;
+    int B, L;
     int D;
     const uint4* x;                // BF16 x_sel as 16-byte vectors
     const uint8_t* reset;
@@ -321,6 +323,7 @@ struct SamuCtrlFwdArgs {
     float* p;
     float* r;
     float4* ctrl;                  // [B*L][2] {E-1, E-1, C, C}, {S, S, R, d}
+    float4* items;                 // [B][items per row] item records (samu_items_per_row)
     float* wh;                     // [2][D+1]
     float* misc;
     float4* modes;                 // [2][M] lbar, lbar^16 hi/lo

@@ -127,8 +127,15 @@ inline SegGeom samu_seg_geom(int B, int L, int M, long long warps) {
 constexpr int kMiscFloats = 16;
 
 struct SamuSaved {
-    size_t p, r, ctrl, hsub, wh, misc, modes, total;
+    size_t p, r, ctrl, items, hsub, wh, misc, modes, total;
 };
+
+// Per-item records of the control words: one float4 per kMapRows-token item
+// of each batch row (items start at t = 0, 16, ... of the row):
+// {G = sum (E - 1), cos D, sin D with D = sum d, v}, v = max |E - 1| over the
+// item's tokens when the item is full and holds no reset, else
+// -(max |E - 1|) - 1.
+__host__ __device__ inline int samu_items_per_row(int L) { return (L + kMapRows - 1) / kMapRows; }
 
 inline SamuSaved samu_saved_layout(int B, int L, int D) {
     const int M = D / 2;
@@ -139,6 +146,7 @@ inline SamuSaved samu_saved_layout(int B, int L, int D) {
     s.p = o;      o = align_up(o + BL * 4);                          // p_t
     s.r = o;      o = align_up(o + BL * 4);                          // r_t
     s.ctrl = o;   o = align_up(o + BL * 32);                         // {E-1, E-1, C, C}, {S, S, R, d}, R = -E or +0 at a reset
+    s.items = o;  o = align_up(o + (size_t)B * samu_items_per_row(L) * 16);   // item records
     s.hsub = o;   o = align_up(o + (size_t)B * g.CS * M * 8);        // state every 8 tokens
     s.wh = o;     o = align_up(o + (size_t)2 * (D + 1) * 4);         // unit directions
     s.misc = o;   o = align_up(o + kMiscFloats * 4);

@@ -160,9 +160,12 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     float* p = reinterpret_cast<float*>(saved + sv.p);
     float* r = reinterpret_cast<float*>(saved + sv.r);
     float4* ctrl = reinterpret_cast<float4*>(saved + sv.ctrl);
+    float4* items = reinterpret_cast<float4*>(saved + sv.items);
 
     SamuCtrlFwdArgs cf;
     cf.BL = (long long)B * L;
+    cf.B = B;
+    cf.L = L;
     cf.D = D;
     cf.x = static_cast<const uint4*>(x_sel);
     cf.reset = reset;
@@ -175,6 +178,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     cf.p = p;
     cf.r = r;
     cf.ctrl = ctrl;
+    cf.items = items;
     cf.wh = wh;
     cf.misc = misc;
     cf.modes = modes;
@@ -185,6 +189,7 @@ extern "C" int samu_forward_noalloc(const void* x_sel, const void* w, const floa
     if (!make_bf16_map(&tm_w, w, B, L, D, kMapRows) || !make_ctrl_map(&tm_ctrl, ctrl, B, L, kMapRows)) return LRS_ERR_CUDA;
     SamuScanFwdArgs a;
     a.g = samu_scan_geom(B, L, M, false);
+    a.items = items;
     a.modes = modes;
     a.nu = nu;
     a.closed_form = samu_get_chunk_transition() == LRS_TRANSITION_CLOSED_FORM;

@@ -129,9 +129,11 @@ __device__ __forceinline__ void dot8(const uint4 q, const float4* __restrict__ w
 }
 
 // The per-token scalars from the two dot products (raw directions).
-__device__ __forceinline__ void ctrl_fwd_token(const SamuCtrlFwdArgs& a, long long t, float dp, float dr,
+// Returns E - 1 and d of the token in em1_out, d_out and whether it is a
+// segment start.
+__device__ __forceinline__ bool ctrl_fwd_token(const SamuCtrlFwdArgs& a, long long t, float dp, float dr,
                                                float inv_phi, float inv_r, float bias_p, float bias_r, float k_phi,
-                                               float k_r) {
+                                               float k_r, float& em1_out, float& d_out) {
     const float p = tanhf(fmaf(dp, inv_phi, bias_p));
     const float r = tanhf(fmaf(dr, inv_r, bias_r));
     const float qr = r / (1.0f + r * r);
@@ -143,9 +145,13 @@ __device__ __forceinline__ void ctrl_fwd_token(const SamuCtrlFwdArgs& a, long lo
     a.r[t] = r;
     const float em1 = expm1f(c);
     // R = -E, or +0 at a reset; d for the closed-form item transitions
-    const float rw = (a.reset != nullptr && a.reset[t] != 0) ? 0.0f : -(1.0f + em1);
+    const bool rst = a.reset != nullptr && a.reset[t] != 0;
+    const float rw = rst ? 0.0f : -(1.0f + em1);
     a.ctrl[2 * t] = make_float4(em1, em1, cs, cs);
     a.ctrl[2 * t + 1] = make_float4(sn, sn, rw, d);
+    em1_out = em1;
+    d_out = d;
+    return rst;
 }
 
 __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFwdArgs a) {
@@ -159,10 +165,9 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
     // their dependency wait, which ends once this kernel has completed.
     if (blockIdx.x == 0 && tid == 0 && a.status != nullptr) *a.status = 0u;
     const int D = a.D, M = D / 2, n = D + 1, nch = D / 8;
-    const long long BL = a.BL;
     const long long W = (long long)gridDim.x * kCfWarps;
     const long long gw = (long long)blockIdx.x * kCfWarps + warp;
-    const long long n_groups = (BL + kCfTok - 1) / kCfTok;
+    const long long n_items = (long long)a.B * samu_items_per_row(a.L);
     const int cpl = (nch + 31) / 32;   // chunks per lane
 
     // staged raw directions and the norms
@@ -223,62 +228,94 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
         }
     }
 
+    // Items of kMapRows tokens of each batch row (t = 0, 16, ... of the row),
+    // one per warp at a time, as kMapRows / kCfTok groups of kCfTok tokens;
+    // the item's record (G, cos D, sin D, max |E - 1| or not-simple) is
+    // formed from the per-token scalars.
     const uint4* x = a.x;
-    for (long long g = gw; g < n_groups; g += W) {
-        const long long t0 = g * kCfTok;
-        f2x pacc[2 * kCfTok];   // {token k: phi, r} as even/odd-channel pairs
+    const int ipr = samu_items_per_row(a.L);
+    for (long long it = gw; it < n_items; it += W) {
+        const long long b = it / ipr;
+        const int ii = (int)(it - b * ipr);
+        const long long tb = b * a.L + (long long)ii * kMapRows;
+        const long long te = b * a.L + min((long long)(ii + 1) * kMapRows, (long long)a.L);
+        float iG = 0.f, iD = 0.f, iemax = 0.f;
+        bool irst = false;
+        for (long long t0 = tb; t0 < te; t0 += kCfTok) {
+            f2x pacc[2 * kCfTok];   // {token k: phi, r} as even/odd-channel pairs
 #pragma unroll
-        for (int v = 0; v < 2 * kCfTok; ++v) pacc[v] = 0ull;
-        for (int i0 = 0; i0 < cpl; i0 += kCfBatch) {
-            uint4 xv[kCfBatch][kCfTok];
+            for (int v = 0; v < 2 * kCfTok; ++v) pacc[v] = 0ull;
+            for (int i0 = 0; i0 < cpl; i0 += kCfBatch) {
+                uint4 xv[kCfBatch][kCfTok];
 #pragma unroll
-            for (int b = 0; b < kCfBatch; ++b) {
-                const int c = lane + 32 * (i0 + b);
+                for (int b4 = 0; b4 < kCfBatch; ++b4) {
+                    const int c = lane + 32 * (i0 + b4);
 #pragma unroll
-                for (int k = 0; k < kCfTok; ++k) {
-                    const bool ok = i0 + b < cpl && c < nch && t0 + k < BL;
-                    xv[b][k] = ok ? __ldg(x + (size_t)(t0 + k) * nch + c) : make_uint4(0u, 0u, 0u, 0u);
+                    for (int k = 0; k < kCfTok; ++k) {
+                        const bool ok = i0 + b4 < cpl && c < nch && t0 + k < te;
+                        xv[b4][k] = ok ? __ldg(x + (size_t)(t0 + k) * nch + c) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+#pragma unroll
+                for (int b4 = 0; b4 < kCfBatch; ++b4) {
+                    const int c = lane + 32 * (i0 + b4);
+                    if (i0 + b4 < cpl && c < nch) {
+                        const float4* wb = wsm + (size_t)c * kCfBlock;
+#pragma unroll
+                        for (int k = 0; k < kCfTok; ++k) dot8(xv[b4][k], wb, pacc[2 * k], pacc[2 * k + 1]);
+                    }
                 }
             }
+            float acc[2 * kCfTok];
 #pragma unroll
-            for (int b = 0; b < kCfBatch; ++b) {
-                const int c = lane + 32 * (i0 + b);
-                if (i0 + b < cpl && c < nch) {
-                    const float4* wb = wsm + (size_t)c * kCfBlock;
+            for (int v = 0; v < 2 * kCfTok; ++v) {
+                float lo, hi;
+                up2(pacc[v], lo, hi);
+                acc[v] = lo + hi;
+            }
+            // reduce-scatter of the 8 sums {token k: phi, r} over the lanes:
+            // halving exchanges at distances 16, 8, 4 (lane bit b keeps the upper
+            // half), then full sums at distances 2, 1.  Lane L ends with value
+            // 4 bit4(L) + 2 bit3(L) + bit2(L): lanes 8k hold s_phi of token k,
+            // lanes 8k + 4 its s_r.
 #pragma unroll
-                    for (int k = 0; k < kCfTok; ++k) dot8(xv[b][k], wb, pacc[2 * k], pacc[2 * k + 1]);
+            for (int o = 16, h = kCfTok; o >= 4; o >>= 1, h >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int j = 0; j < h; ++j) {
+                    const float send = up ? acc[j] : acc[j + h];
+                    const float keep = up ? acc[j + h] : acc[j];
+                    acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                 }
             }
-        }
-        float acc[2 * kCfTok];
-#pragma unroll
-        for (int v = 0; v < 2 * kCfTok; ++v) {
-            float lo, hi;
-            up2(pacc[v], lo, hi);
-            acc[v] = lo + hi;
-        }
-        // reduce-scatter of the 8 sums {token k: phi, r} over the lanes:
-        // halving exchanges at distances 16, 8, 4 (lane bit b keeps the upper
-        // half), then full sums at distances 2, 1.  Lane L ends with value
-        // 4 bit4(L) + 2 bit3(L) + bit2(L): lanes 8k hold s_phi of token k,
-        // lanes 8k + 4 its s_r.
-#pragma unroll
-        for (int o = 16, h = kCfTok; o >= 4; o >>= 1, h >>= 1) {
-            const bool up = (lane & o) != 0;
-#pragma unroll
-            for (int j = 0; j < h; ++j) {
-                const float send = up ? acc[j] : acc[j + h];
-                const float keep = up ? acc[j + h] : acc[j];
-                acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            float sv = acc[0];
+            sv += __shfl_xor_sync(0xffffffffu, sv, 2);
+            sv += __shfl_xor_sync(0xffffffffu, sv, 1);
+            const float s_r = __shfl_down_sync(0xffffffffu, sv, 4);
+            const int k = lane >> 3;
+            if ((lane & 7) == 0 && t0 + k < te) {
+                float em1, d;
+                irst = ctrl_fwd_token(a, t0 + k, sv, s_r, inv_phi, inv_r, bias_p, bias_r, k_phi, k_r, em1, d) || irst;
+                iG += em1;
+                iD += d;
+                iemax = fmaxf(iemax, fabsf(em1));
             }
         }
-        float s = acc[0];
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        const float s_r = __shfl_down_sync(0xffffffffu, s, 4);
-        const int k = lane >> 3;
-        if ((lane & 7) == 0 && t0 + k < BL)
-            ctrl_fwd_token(a, t0 + k, s, s_r, inv_phi, inv_r, bias_p, bias_r, k_phi, k_r);
+        // lanes 0, 8, 16, 24 hold the sums over tokens k, k+4, ... of the
+        // item: combined in a fixed order, ((l0 + l8) + (l16 + l24)), in lane 0
+#pragma unroll
+        for (int o = 8; o <= 16; o <<= 1) {
+            iG += __shfl_xor_sync(0xffffffffu, iG, o);
+            iD += __shfl_xor_sync(0xffffffffu, iD, o);
+            iemax = fmaxf(iemax, __shfl_xor_sync(0xffffffffu, iemax, o));
+            irst = __shfl_xor_sync(0xffffffffu, (int)irst, o) != 0 || irst;
+        }
+        if (lane == 0) {
+            float sn, cs;
+            sincosf(iD, &sn, &cs);
+            const bool simple = !irst && te - tb == kMapRows;
+            a.items[it] = make_float4(iG, cs, sn, simple ? iemax : -iemax - 1.0f);
+        }
     }
 }
 
@@ -775,10 +812,11 @@ CtrlGeom samu_ctrl_geom(long long BL, int D) {
 }
 
 cudaError_t launch_samu_ctrl_fwd(const SamuCtrlFwdArgs& a, cudaStream_t s, bool pdl) {
-    // two CTAs per SM (one wave), fewer for short inputs
-    const long long groups = (a.BL + kCfTok - 1) / kCfTok;
+    // two CTAs per SM (one wave), fewer for short inputs; the warps past the
+    // items form the per-mode constants
+    const long long items = (long long)a.B * samu_items_per_row(a.L);
     long long ctas = (long long)ctrl_sms() * 2;
-    const long long need = (groups + kCfWarps - 1) / kCfWarps;
+    const long long need = (items + (a.D / 2 + 31) / 32 + kCfWarps - 1) / kCfWarps;
     if (ctas > need) ctas = need;
     if (ctas < 1) ctas = 1;
     const size_t smem = (size_t)(a.D / 8) * kCfBlock * sizeof(float4);

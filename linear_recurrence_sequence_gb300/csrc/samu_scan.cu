@@ -160,6 +160,54 @@ __device__ __forceinline__ SubKind sub_kind(const float4* sc, int nsub, int lane
         }                                              \
     } while (0)
 
+// Per-item plan of one warp's segment, 32 items at a time, from the
+// controller forward's item records (one float4 per 16-token item of a batch
+// row: G = sum (E - 1), cos D, sin D, and max |E - 1| with its sign marking
+// an item that is not simple): lane j describes item 32 q + j of the segment
+// (its tokens t_begin + 16 (32 q + j) ...):
+//  simple (bit j): all 16 tokens present and none a reset;
+//  fast (bit j):   numax max|E - 1| < kPolyBound, numax = max |nu| over the
+//                  warp's modes (the same test as sub_kind);
+//  G, c, s:        the closed-form transition's statistics.
+// One coalesced 16-byte load per lane and 32 items replaces the per-item
+// votes, sums and sincosf.
+struct ItemPlan {
+    unsigned fast, simple;
+    float G, c, s;
+    int q;   // batch held, -1 before the first
+};
+
+// max |nu| over the warp's modes
+__device__ __forceinline__ float warp_numax(const ModePair& k) {
+    float n0, n1;
+    up2(k.nu, n0, n1);
+    const float v = fmaxf(fabsf(n0), fabsf(n1));
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
+__device__ __forceinline__ float record_emax(float v) { return v >= 0.f ? v : -v - 1.f; }
+
+// Batch q of the plan of the segment T of a sequence of length L.  The
+// records are read through L2 (the controller forward may have run beside
+// this kernel before its dependency wait).
+template <bool STATS>
+__device__ __forceinline__ void plan_batch(ItemPlan& P, const float4* __restrict__ items, const SegTask& T, int L,
+                                           int q, const ModePair& k, int lane) {
+    const float numax = warp_numax(k);
+    const int idx = 32 * q + lane;
+    const bool ok = idx < T.nsc;
+    float4 r = make_float4(0.f, 1.f, 0.f, 0.f);
+    if (ok) r = __ldcg(items + (size_t)T.b * samu_items_per_row(L) + T.t_begin / kMapRows + idx);
+    P.fast = __ballot_sync(0xffffffffu, numax * record_emax(r.w) < kPolyBound);
+    P.simple = __ballot_sync(0xffffffffu, ok && r.w >= 0.f);
+    if (STATS) {
+        P.G = r.x;
+        P.c = r.y;
+        P.s = r.z;
+    }
+    P.q = q;
+}
+
 __device__ __forceinline__ float4 identity_map() { return make_float4(1.f, 0.f, 0.f, 0.f); }
 
 __device__ __forceinline__ c2x czero() {
@@ -283,22 +331,12 @@ __device__ __forceinline__ c2x cmulx(const c2x& a, const c2x& b) {   // a b
 }
 
 // The transition of one full item of N tokens, none a reset, for the lane's
-// two modes (zero for an inactive lane).  G and D are summed over the item's
-// tokens by a fixed xor tree within each half-warp (both halves hold the
-// same tokens, so every lane gets the same bits).
+// two modes (zero for an inactive lane), from the item's G and cos D, sin D
+// (ItemPlan).
 template <int N>
-__device__ __forceinline__ c2x item_transition(const float4* sc, const float4* __restrict__ modes_n,
-                                               const ModePair& k, int m, bool active, int lane) {
-    static_assert(N <= 16 && (N & (N - 1)) == 0, "an item fits a half-warp");
-    const int j = lane & (N - 1);
-    float G = sc[2 * j].x, Dsum = sc[2 * j + 1].w;
-#pragma unroll
-    for (int o = N / 2; o > 0; o >>= 1) {
-        G += __shfl_xor_sync(0xffffffffu, G, o);
-        Dsum += __shfl_xor_sync(0xffffffffu, Dsum, o);
-    }
-    float sn, cs;
-    sincosf(Dsum, &sn, &cs);
+__device__ __forceinline__ c2x item_transition(float G, float cs, float sn, const float4* __restrict__ modes_n,
+                                               const ModePair& k, int m, bool active) {
+    static_assert(N == kMapRows, "the plan's statistics cover kMapRows tokens");
     float n0, n1;
     up2(k.nu, n0, n1);
     const float x0 = n0 * G, x1 = n1 * G;   // nu G
@@ -329,7 +367,7 @@ __device__ __forceinline__ c2x item_transition(const float4* sc, const float4* _
 template <int N, bool FAST>
 __device__ __forceinline__ void fwd_maps_item_cf(const float4* sc, const uint32_t* wre, const uint32_t* wim,
                                                  const ModePair& k, const float4* __restrict__ modes_n, int m,
-                                                 bool active, int lane, c2x& P, c2x& be) {
+                                                 bool active, float G, float cs, float sn, c2x& P, c2x& be) {
     c2x h;
     h.re = bf2x(wre[0]);
     h.im = bf2x(wim[0]);
@@ -344,7 +382,7 @@ __device__ __forceinline__ void fwd_maps_item_cf(const float4* sc, const uint32_
         h.re = hr;
         h.im = hi;
     }
-    const c2x L = item_transition<N>(sc, modes_n, k, m, active, lane);
+    const c2x L = item_transition<N>(G, cs, sn, modes_n, k, m, active);
     const c2x Ph = cmulx(P, h);
     be.re = add2(be.re, Ph.re);
     be.im = add2(be.im, Ph.im);
@@ -507,24 +545,33 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         for (int k = 0; k < kRing && k < T.nsc; ++k)
             ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + (T.nsc - 1 - k) * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    ItemPlan plan;
+    plan.q = -1;
     c2x P;
     P.re = dup2(1.f);
     P.im = 0ull;
     c2x be = czero();
     for (int it = 0; it < T.nsc; ++it) {
         const int slot = it % kRing;
-        const int ts = T.t_begin + (T.nsc - 1 - it) * kN;
+        const int idx = T.nsc - 1 - it;   // the item's place in the segment
+        const int ts = T.t_begin + idx * kN;
         const int nsub = min(kN, T.t_end - ts);
+        if ((idx >> 5) != plan.q) plan_batch<true>(plan, a.items, T, g.L, idx >> 5, k, lane);
+        SubKind kd;
+        kd.fast = (plan.fast >> (idx & 31)) & 1u;
+        kd.simple = (plan.simple >> (idx & 31)) & 1u;
+        const float iG = __shfl_sync(0xffffffffu, plan.G, idx & 31);
+        const float ic = __shfl_sync(0xffffffffu, plan.c, idx & 31);
+        const float is = __shfl_sync(0xffffffffu, plan.s, idx & 31);
         if (!ring_wait(R, it, T.nsc, a.status, lane)) break;   // status set; the CTA still reaches its barriers
         const float4* sc = R.ctrl[slot];
         const uint32_t* wre = &R.box[slot][0][0][lane];
         const uint32_t* wim = &R.box[slot][1][0][lane];
-        const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
         if (a.closed_form && kd.simple) {
             if (kd.fast)
-                fwd_maps_item_cf<kN, true>(sc, wre, wim, k, a.modes + M, m, active, lane, P, be);
+                fwd_maps_item_cf<kN, true>(sc, wre, wim, k, a.modes + M, m, active, iG, ic, is, P, be);
             else
-                fwd_maps_item_cf<kN, false>(sc, wre, wim, k, a.modes + M, m, active, lane, P, be);
+                fwd_maps_item_cf<kN, false>(sc, wre, wim, k, a.modes + M, m, active, iG, ic, is, P, be);
         } else {
             LRS_SUB_DISPATCH_N(kd, fwd_maps_sub, kN, sc, wre, wim, nsub, k, P, be);
         }
@@ -590,6 +637,8 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + k * kN, T.b);
     }
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    ItemPlan plan;
+    plan.q = -1;
     c2x z = czero();
     if (active) {   // entry: the CTA's entry state through the maps of the earlier segments of the CTA
         float2 z0, z1;
@@ -634,7 +683,10 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         const uint32_t* wim = &R.box[slot][1][0][lane];
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         float* y32p = Y32 ? a.y32 + 2 * row0 : nullptr;
-        const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
+        if ((it >> 5) != plan.q) plan_batch<false>(plan, a.items, T, L, it >> 5, k, lane);
+        SubKind kd;
+        kd.fast = (plan.fast >> (it & 31)) & 1u;
+        kd.simple = (plan.simple >> (it & 31)) & 1u;
         LRS_SUB_DISPATCH_NX(kd, fwd_replay_sub, kN, Y32, sc, wre, wim, nsub, k, z, a.y + row0, y32p, active, D / 2,
                             M / 2, hs, M);
         __syncwarp();
@@ -680,7 +732,7 @@ __device__ __forceinline__ void bwd_maps_sub(const float4* sc, const uint32_t* g
 template <int N, bool FAST>
 __device__ __forceinline__ void bwd_maps_item_cf(const float4* sc, const uint32_t* gre, const uint32_t* gim,
                                                  const ModePair& k, const float4* __restrict__ modes_n, int m,
-                                                 bool active, int lane, c2x& Q, c2x& be) {
+                                                 bool active, float G, float cs, float sn, c2x& Q, c2x& be) {
     c2x y;
     y.re = bf2x(gre[(N - 1) * kWords]);
     y.im = bf2x(gim[(N - 1) * kWords]);
@@ -695,7 +747,7 @@ __device__ __forceinline__ void bwd_maps_item_cf(const float4* sc, const uint32_
         y.im = yi;
     }
     const c2x x = cmulc2(samu_lambda2<FAST>(k, load_ctl(sc, 0)), y);
-    c2x L = item_transition<N>(sc, modes_n, k, m, active, lane);
+    c2x L = item_transition<N>(G, cs, sn, modes_n, k, m, active);
     L.im = sub2(0ull, L.im);   // conj
     const c2x Qx = cmulx(Q, x);
     be.re = add2(be.re, Qx.re);
@@ -772,6 +824,8 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
     if (lane == 0)
         for (int k = 0; k < kRing && k < T.nsc; ++k) ring_issue_ctrl(R, k, &tm_ctrl, T.t_begin + k * kN, T.b);
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
+    ItemPlan plan;
+    plan.q = -1;
     c2x Q;
     Q.re = dup2(1.f);
     Q.im = 0ull;
@@ -780,16 +834,22 @@ __global__ void __launch_bounds__(kEngineThreads, 3)
         const int slot = it % kRing;
         const int ts = T.t_begin + it * kN;
         const int nsub = min(kN, T.t_end - ts);
+        if ((it >> 5) != plan.q) plan_batch<true>(plan, a.items, T, g.L, it >> 5, k, lane);
+        SubKind kd;
+        kd.fast = (plan.fast >> (it & 31)) & 1u;
+        kd.simple = (plan.simple >> (it & 31)) & 1u;
+        const float iG = __shfl_sync(0xffffffffu, plan.G, it & 31);
+        const float ic = __shfl_sync(0xffffffffu, plan.c, it & 31);
+        const float is = __shfl_sync(0xffffffffu, plan.s, it & 31);
         if (!ring_wait(R, it, T.nsc, a.status, lane)) break;   // status set; the CTA still reaches its barriers
         const float4* sc = R.ctrl[slot];
         const uint32_t* gre = &R.box[slot][0][0][lane];
         const uint32_t* gim = &R.box[slot][1][0][lane];
-        const SubKind kd = sub_kind<kN>(sc, nsub, lane, k);
         if (a.closed_form && kd.simple) {
             if (kd.fast)
-                bwd_maps_item_cf<kN, true>(sc, gre, gim, k, a.modes + M, m, active, lane, Q, be);
+                bwd_maps_item_cf<kN, true>(sc, gre, gim, k, a.modes + M, m, active, iG, ic, is, Q, be);
             else
-                bwd_maps_item_cf<kN, false>(sc, gre, gim, k, a.modes + M, m, active, lane, Q, be);
+                bwd_maps_item_cf<kN, false>(sc, gre, gim, k, a.modes + M, m, active, iG, ic, is, Q, be);
         } else {
             LRS_SUB_DISPATCH_N(kd, bwd_maps_sub, kN, sc, gre, gim, nsub, k, Q, be);
         }
@@ -991,25 +1051,24 @@ __device__ __forceinline__ void rev_unit(RevRing& R, int slot, int nh, const Mod
                                   acc_nu, acc_th, dwb, dwf, active, row, half, kp, kp_row, lane);
 }
 
-// Warp-uniform facts about the whole segment [t_begin, t_end), read from the
-// control words in global memory: simple (no reset, whole units only) and
-// fast (|nu| max|E - 1| < kPolyBound for every lane's modes).  A segment that
-// is both runs every unit on the branch-free polynomial path; one that is not
+// Warp-uniform facts about the whole segment, from the forward's item
+// records: simple (every item full and free of resets) and fast
+// (|nu| max|E - 1| < kPolyBound for every lane's modes).  A segment that is
+// both runs every unit on the branch-free polynomial path; one that is not
 // decides per unit (sub_kind), as the forward replay does per item.
-__device__ __forceinline__ SubKind segment_kind(const float4* __restrict__ ctrl, long long row0, int n, int lane,
+__device__ __forceinline__ SubKind segment_kind(const float4* __restrict__ items, const SegTask& T, int L, int lane,
                                                 const ModePair& k) {
+    const int n_it = (T.t_end - T.t_begin + kMapRows - 1) / kMapRows;
     float emax = 0.f;
-    bool rst = false;
-    for (int i = lane; i < n; i += 32) {
-        emax = fmaxf(emax, fabsf(__ldg(&ctrl[2 * (row0 + i)].x)));
-        rst = rst || is_reset_word(__ldg(&ctrl[2 * (row0 + i) + 1].z));
+    bool simple = true;
+    for (int i = lane; i < n_it; i += 32) {
+        const float v = __ldcg(&items[(size_t)T.b * samu_items_per_row(L) + T.t_begin / kMapRows + i].w);
+        emax = fmaxf(emax, record_emax(v));
+        simple = simple && v >= 0.f;
     }
-    emax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(emax)));
-    float n0, n1;
-    up2(k.nu, n0, n1);
     SubKind kd;
-    kd.fast = __all_sync(0xffffffffu, fabsf(n0) * emax < kPolyBound && fabsf(n1) * emax < kPolyBound);
-    kd.simple = !__any_sync(0xffffffffu, rst) && n % kHalf == 0;
+    kd.fast = warp_numax(k) * __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(emax))) < kPolyBound;
+    kd.simple = __all_sync(0xffffffffu, simple);
     return kd;
 }
 
@@ -1048,7 +1107,7 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     const ModePair k = active ? load_modes(a.modes, a.nu, m) : zero_modes();
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
-    const SubKind seg_kd = segment_kind(a.ctrl, (long long)T.b * L + T.t_begin, T.t_end - T.t_begin, lane, k);
+    const SubKind seg_kd = segment_kind(a.items, T, L, lane, k);
     pdl_wait();
     // the adjoint arriving at the CTA from the later CTAs' maps
     const int cc = T.s / kSegPerCta;

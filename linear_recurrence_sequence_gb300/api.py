@@ -469,8 +469,8 @@ KERNEL_NAMES = {
     4: "samu_bwd_main_kernel", 5: "samu_ctrl_bwd_kernel", 6: "samu_params_kernel",
     7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
     10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel", 12: "samu_decode_prepare_kernel",
-    13: "samu_decode_step_kernel", 14: "rglru_proj_gemms (cuBLAS)", 15: "rglru_proj_bwd_gemms (cuBLAS)",
-    16: "rglru_proj_pack_dw_kernels",
+    13: "samu_decode_step_kernel", 14: "proj_gemm_kernel<logits>", 15: "proj_gemm_kernel<dx, dW>",
+    16: "proj_pack_kernel",
 }
 
 

@@ -1,11 +1,9 @@
 // extern "C" entry points declared in include/samu.h: argument checks,
 // workspace carving and kernel launches.  No allocation, no synchronisation
-// (except lrs_device_status, which documents that it synchronises, and the
-// projected RG-LRU's per-thread cuBLAS handle, created on first use).
+// (except lrs_device_status, which documents that it synchronises).
 #include <atomic>
 #include <cstdint>
 #include <cstring>
-#include <cublas_v2.h>
 #include "kernels.cuh"
 #include "tmap.cuh"
 
@@ -90,79 +88,6 @@ enum {
         prof_end(stream);                       \
         if (e_ != cudaSuccess) return LRS_ERR_CUDA; \
     } while (0)
-
-// ---------------------------------------------------------------------------
-// Block-diagonal gate projections through cuBLAS (plain batched GEMMs, BF16
-// operands, FP32 accumulation and output): one handle per host thread,
-// created on first use (the library allocates its own small device state
-// then), with the caller's scratch as its workspace on every call.
-// Row-major [rows x D] activations are column-major [D x rows] matrices to
-// cuBLAS; block h is the D/16-wide column slice h, batched with stride D/16.
-// ---------------------------------------------------------------------------
-cublasHandle_t gemm_handle() {
-    thread_local cublasHandle_t h = nullptr;
-    if (h == nullptr && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
-    return h;
-}
-
-struct Gemm {
-    cublasHandle_t h;
-    int rows, D, dk;
-};
-
-cudaError_t gemm_begin(Gemm& gm, int rows, int D, void* ws, cudaStream_t s) {
-    gm.h = gemm_handle();
-    gm.rows = rows;
-    gm.D = D;
-    gm.dk = D / kProjBlocks;
-    if (gm.h == nullptr) return cudaErrorUnknown;
-    if (cublasSetStream(gm.h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-    if (cublasSetWorkspace(gm.h, ws, kGemmWorkspace) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-    return cudaSuccess;
-}
-
-// out[t][h dk + o] (+)= sum_i in[t][h dk + i] W[h][i][o]   (l = x W)
-cudaError_t gemm_xw(const Gemm& gm, const void* in, const void* w, float* out, float beta) {
-    const float one = 1.0f;
-    const cublasStatus_t st = cublasGemmStridedBatchedEx(
-        gm.h, CUBLAS_OP_N, CUBLAS_OP_N, gm.dk, gm.rows, gm.dk, &one, w, CUDA_R_16BF, gm.dk,
-        (long long)gm.dk * gm.dk, in, CUDA_R_16BF, gm.D, gm.dk, &beta, out, CUDA_R_32F, gm.D, gm.dk, kProjBlocks,
-        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-}
-
-// Both gates' products x W_x, x W_a (FP32, biases excluded) into scratch.
-cudaError_t proj_forward_gemms(int rows, int D, const void* x, const void* w_x, const void* w_a, float* lx, float* la,
-                               void* ws, cudaStream_t s) {
-    Gemm gm;
-    cudaError_t e = gemm_begin(gm, rows, D, ws, s);
-    if (e == cudaSuccess) e = gemm_xw(gm, x, w_x, lx, 0.0f);
-    if (e == cudaSuccess) e = gemm_xw(gm, x, w_a, la, 0.0f);
-    return e;
-}
-
-// The backward products from the six gradient parts G [rows][16][6][dk]
-// (dl^x hi, lo; dl^a hi, lo; dx-through-the-write-term hi, lo):
-//   dx[t][h dk + i] = sum_k Wcat[h](i, k) G[t][h][k]   (K = 6 dk, one GEMM, the
-//                     write-term parts through identity blocks; BF16 or FP32 out)
-//   Gx[h](k, i)     = sum_t G[t][h][k] x[t][h dk + i]  (k < 4 dk, K = rows)
-cudaError_t proj_backward_gemms(int rows, int D, const void* x, const void* gparts, const void* wcat, void* dx,
-                                bool dx_fp32, float* dwcat, void* ws, cudaStream_t s) {
-    Gemm gm;
-    cudaError_t e = gemm_begin(gm, rows, D, ws, s);
-    if (e != cudaSuccess) return e;
-    const int dk = gm.dk;
-    const float one = 1.0f, zero = 0.0f;
-    cublasStatus_t st = cublasGemmStridedBatchedEx(
-        gm.h, CUBLAS_OP_N, CUBLAS_OP_N, dk, rows, 6 * dk, &one, wcat, CUDA_R_16BF, dk, (long long)6 * dk * dk,
-        gparts, CUDA_R_16BF, 6 * D, 6 * dk, &zero, dx, dx_fp32 ? CUDA_R_32F : CUDA_R_16BF, D, dk, kProjBlocks,
-        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-    st = cublasGemmStridedBatchedEx(gm.h, CUBLAS_OP_N, CUBLAS_OP_T, 4 * dk, dk, rows, &one, gparts, CUDA_R_16BF,
-                                    6 * D, 6 * dk, x, CUDA_R_16BF, D, dk, &zero, dwcat, CUDA_R_32F, 4 * dk,
-                                    (long long)4 * dk * dk, kProjBlocks, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-}
 
 int check_rglru_proj_shape(int B, int L, int D) {
     const int st = check_rglru_shape(B, L, D);
@@ -629,8 +554,12 @@ int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const v
         tm_lx = tm_x;
         tm_la = tm_x;
     } else {
+        const ProjDims pd = proj_dims(B, L, D);
+        LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream,
+                   launch_proj_pack(w_x, w_a, at<void>(scratch, ps.wt), at<void>(scratch, ps.wc), pd, stream));
         LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
-                   proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, at<void>(scratch, ps.gemm_ws), stream));
+                   launch_proj_logits(x, at<void>(scratch, ps.wt), lx, la, D, pd, at<uint32_t>(scratch, sc.status),
+                                      stream, false));
         if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) ||
             !make_f32_map(&tm_la, la, B, L, D, kRgTile))
             return LRS_ERR_CUDA;
@@ -675,10 +604,14 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     float* lx = at<float>(scratch, ps.lx);
     float* la = at<float>(scratch, ps.la);
     const bool fp32 = grad_dtype == LRS_GRAD_FP32;
-    void* ws = at<void>(scratch, ps.gemm_ws);
-    const int dk = D / kProjBlocks;
+    const ProjDims pd = proj_dims(B, L, D);
+    const int dk = pd.dk;
+    uint32_t* status = at<uint32_t>(scratch, sc.status);
     if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
-    LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream, proj_forward_gemms(B * L, D, x, w_x, w_a, lx, la, ws, stream));
+    LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream,
+               launch_proj_pack(w_x, w_a, at<void>(scratch, ps.wt), at<void>(scratch, ps.wc), pd, stream));
+    LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
+               launch_proj_logits(x, at<void>(scratch, ps.wt), lx, la, D, pd, status, stream, false));
     CUtensorMap tm_dy, tm_x, tm_lx, tm_la;
     if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile) || !make_bf16_map(&tm_x, x, B, L, D, kRgTile) ||
         !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) || !make_f32_map(&tm_la, la, B, L, D, kRgTile))
@@ -711,12 +644,11 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.apart, apart2, dalpha, B * g.CT, D, stream));
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bxpart, apart2, db_x, B * g.CT, D, stream));
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bapart, apart2, db_a, B * g.CT, D, stream));
-    void* wcat = at<void>(scratch, ps.wcat);
-    float* dwcat = at<float>(scratch, ps.dwcat);
-    LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream, launch_rglru_proj_pack(w_x, w_a, wcat, dk, stream));
     LRS_LAUNCH(KID_RGLRU_PROJ_BWD, stream,
-               proj_backward_gemms(B * L, D, x, a.gparts, wcat, dx, fp32, dwcat, ws, stream));
-    LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream, launch_rglru_proj_dw(dwcat, dw_x, dw_a, dk, stream));
+               launch_proj_dx(a.gparts, at<void>(scratch, ps.wc), dx, fp32, D, pd, status, stream, false));
+    LRS_LAUNCH(KID_RGLRU_PROJ_BWD, stream,
+               launch_proj_dw(a.gparts, x, at<float>(scratch, ps.dwpart), dw_x, dw_a, D, pd, status, stream, false));
+    (void)dk;
     return LRS_OK;
 }
 

@@ -458,7 +458,18 @@ cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha,
 // Packed backward weights [16][6 dk][dk] (column-major dk x 6dk per block:
 // W_x, W_x, W_a, W_a transposed into (o, i), then two identity blocks) and
 // the combination dW_x = P0 + P1, dW_a = P2 + P3 of the [16][dk][4 dk] GEMM output.
-cudaError_t launch_rglru_proj_pack(const void* w_x, const void* w_a, void* wcat, int dk, cudaStream_t s);
-cudaError_t launch_rglru_proj_dw(const float* dwcat, float* dw_x, float* dw_a, int dk, cudaStream_t s);
+// The gate projections' contractions on the tensor cores (proj_gemm.cu):
+// operand images of W_x, W_a (logits) and of the packed Wcat (dx); the FP32
+// logits x W_q of both gates; dx from the gradient parts; dW_x, dW_a from the
+// gradient parts and x (token splits added in a fixed order).  status: the
+// call's device status word (bounded waits).
+cudaError_t launch_proj_pack(const void* w_x, const void* w_a, void* wt, void* wc, const ProjDims& d, cudaStream_t s);
+cudaError_t launch_proj_logits(const void* x, const void* wt, float* lx, float* la, int D, const ProjDims& d,
+                               uint32_t* status, cudaStream_t s, bool pdl);
+cudaError_t launch_proj_dx(const void* gparts, const void* wc, void* dx, bool dx_fp32, int D, const ProjDims& d,
+                           uint32_t* status, cudaStream_t s, bool pdl);
+int proj_dw_splits(const ProjDims& d);
+cudaError_t launch_proj_dw(const void* gparts, const void* x, float* part, float* dw_x, float* dw_a, int D,
+                           const ProjDims& d, uint32_t* status, cudaStream_t s, bool pdl);
 
 }  // namespace lrs

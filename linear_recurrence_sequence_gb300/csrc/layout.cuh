@@ -218,34 +218,54 @@ inline RglruScratch rglru_scratch_layout(int B, int L, int D) {
     return s;
 }
 
-// RG-LRU with the block-diagonal gate projections: the scan's scratch, then
-// the FP32 products x W of both gates, the six BF16 gradient parts per token
-// and block ([B*L][16][6][dk]), the packed backward weights, the dW product,
-// the bias-gradient partials and the GEMM library's workspace.
+// RG-LRU with the block-diagonal gate projections.  Sizes of the
+// tensor-core contractions: dk = D/16 channels per block, NP = dk rounded up
+// to 16 (the N tile), kp = dk and kp6 = 6 dk rounded up to 64 (the K slices),
+// dw_rows = 4 dk rounded up to 128 (the M tiles of the weight gradient).
 constexpr int kProjBlocks = 16;                      // diagonal blocks of each gate projection
-constexpr size_t kGemmWorkspace = 32u << 20;
+constexpr int kProjDwSplitsMax = 16;                 // token splits of the weight-gradient contraction
 
+struct ProjDims {
+    int BL, dk, NP, kp, kp6, dw_rows;
+};
+
+inline ProjDims proj_dims(int B, int L, int D) {
+    ProjDims d;
+    d.BL = B * L;
+    d.dk = D / kProjBlocks;
+    d.NP = (d.dk + 15) / 16 * 16;
+    d.kp = (d.dk + 63) / 64 * 64;
+    d.kp6 = (6 * d.dk + 63) / 64 * 64;
+    d.dw_rows = (4 * d.dk + 127) / 128 * 128;
+    return d;
+}
+
+// The scan's scratch, then the FP32 products x W of both gates, the six BF16
+// gradient parts per token and block ([B*L][16][6][dk]), the packed operand
+// images of the logits and dx contractions, the weight gradient's per-split
+// partial products, the bias-gradient partials and the weight images of the
+// in-kernel logits.
 struct RglruProjScratch {
     RglruScratch scan;
-    size_t lx, la, gparts, wcat, dwcat, wimg, bxpart, bapart, gemm_ws, total;
+    size_t lx, la, gparts, wt, wc, dwpart, wimg, bxpart, bapart, total;
 };
 
 inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
     const ScanGeom g = make_geom(B, L, D, kRgTile);
+    const ProjDims pd = proj_dims(B, L, D);
     RglruProjScratch s;
     s.scan = rglru_scratch_layout(B, L, D);
     const size_t bld = (size_t)B * L * D;
     size_t o = s.scan.total;
     s.lx = o;      o = align_up(o + bld * 4);
     s.la = o;      o = align_up(o + bld * 4);
-    const size_t dk = (size_t)D / kProjBlocks;
     s.gparts = o;  o = align_up(o + bld * 6 * 2);
-    s.wcat = o;    o = align_up(o + (size_t)kProjBlocks * 6 * dk * dk * 2);
-    s.dwcat = o;   o = align_up(o + (size_t)kProjBlocks * 4 * dk * dk * 4);
+    s.wt = o;      o = align_up(o + (size_t)kProjBlocks * 2 * pd.NP * pd.kp * 2);
+    s.wc = o;      o = align_up(o + (size_t)kProjBlocks * pd.NP * pd.kp6 * 2);
+    s.dwpart = o;  o = align_up(o + (size_t)kProjDwSplitsMax * kProjBlocks * pd.dw_rows * pd.NP * 4);
     s.wimg = o;    o = align_up(o + (size_t)(D / 64) * 2 * 64 * 64 * 2);   // in-kernel logits: weight images
     s.bxpart = o;  o = align_up(o + (size_t)B * g.CT * D * 4);
     s.bapart = o;  o = align_up(o + (size_t)B * g.CT * D * 4);
-    s.gemm_ws = o; o = align_up(o + kGemmWorkspace);
     s.total = o;
     return s;
 }

@@ -791,45 +791,6 @@ __global__ void __launch_bounds__(256) rglru_alpha_stage2_kernel(const float* __
     dalpha[d] = s;
 }
 
-// Packed backward weights: block h is the column-major [dk x 6 dk] matrix
-// A(i, p dk + o) = W_x[h][i][o] (p = 0, 1), W_a[h][i][o] (p = 2, 3), [i == o]
-// (p = 4, 5), so that dx = A . (parts of the token's gradients).
-__global__ void __launch_bounds__(256) rglru_proj_pack_kernel(const uint16_t* __restrict__ w_x,
-                                                              const uint16_t* __restrict__ w_a,
-                                                              uint16_t* __restrict__ wcat, int dk) {
-    const size_t n = (size_t)16 * 6 * dk * dk;
-    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
-        const int i = (int)(e % dk);
-        const size_t k = e / dk % ((size_t)6 * dk);
-        const int h = (int)(e / ((size_t)6 * dk * dk));
-        const int p = (int)(k / dk), o = (int)(k % dk);
-        const size_t wi = ((size_t)h * dk + i) * dk + o;
-        uint16_t v;
-        if (p < 2)
-            v = w_x[wi];
-        else if (p < 4)
-            v = w_a[wi];
-        else
-            v = i == o ? (uint16_t)0x3F80u : (uint16_t)0;   // BF16 1.0 and 0.0
-        wcat[e] = v;
-    }
-}
-
-// dW_x[h][i][o] = G(o, i) + G(dk + o, i), dW_a from rows 2 dk, 3 dk, where G is
-// block h's column-major [4 dk x dk] product of the gradient parts with x.
-__global__ void __launch_bounds__(256) rglru_proj_dw_kernel(const float* __restrict__ g, float* __restrict__ dw_x,
-                                                            float* __restrict__ dw_a, int dk) {
-    const size_t n = (size_t)16 * dk * dk;
-    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
-        const int o = (int)(e % dk);
-        const int i = (int)(e / dk % dk);
-        const size_t h = e / ((size_t)dk * dk);
-        const float* gb = g + h * 4 * dk * dk + (size_t)i * 4 * dk;
-        dw_x[e] = gb[o] + gb[dk + o];
-        dw_a[e] = gb[2 * dk + o] + gb[3 * dk + o];
-    }
-}
-
 // Weight images for the in-kernel logits: group g, gate q, output n, input k
 // (channels 64 g + n, 64 g + k) hold W_q[h][i][o] when both channels lie in
 // diagonal block h (i, o their offsets in it), else 0; stored K-major with the
@@ -859,20 +820,6 @@ cudaError_t launch_rglru_proj_wimg(const void* w_x, const void* w_a, void* wimg,
     const size_t n = (size_t)(D / kGroup) * 2 * kGroup * kGroup;
     rglru_proj_wimg_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(
         static_cast<const uint16_t*>(w_x), static_cast<const uint16_t*>(w_a), static_cast<uint16_t*>(wimg), D);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_rglru_proj_pack(const void* w_x, const void* w_a, void* wcat, int dk, cudaStream_t s) {
-    const size_t n = (size_t)16 * 6 * dk * dk;
-    rglru_proj_pack_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(
-        static_cast<const uint16_t*>(w_x), static_cast<const uint16_t*>(w_a), static_cast<uint16_t*>(wcat), dk);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_rglru_proj_dw(const float* dwcat, float* dw_x, float* dw_a, int dk, cudaStream_t s) {
-    const size_t n = (size_t)16 * dk * dk;
-    rglru_proj_dw_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, s>>>(dwcat, dw_x,
-                                                                                                      dw_a, dk);
     return cudaGetLastError();
 }
 

@@ -282,17 +282,16 @@ int rglru_backward(const void* dy, const float* dhT, const void* x, const void* 
  *   lx_t[h dk + o] = sum_i x_t[h dk + i] w_x[h][i][o] + b_x[h dk + o],
  *   la_t likewise with w_a, b_a;  h = 0..15, dk = D/16,
  * then the RG-LRU scan of rglru_forward on (x, lx, la).  The products are
- * formed from the BF16 x and BF16 weights with FP32 accumulation (cuBLAS
- * batched GEMMs) and stay in FP32 (no rounding of the logits).
+ * formed from the BF16 x and BF16 weights with FP32 accumulation on the
+ * tensor cores (inside the scan kernel when D/16 divides 64, else by a
+ * separate contraction kernel) and stay in FP32 (no rounding of the logits).
  *
  *   x           [B,L,D] BF16 (in)
  *   w_x, w_a    [16][dk][dk] BF16 (in), row i = input channel, column o = output
  *   b_x, b_a    [D] FP32 (in);  alpha [D] FP32 (in)
  *   h0, reset, y, y32, hT: as rglru_forward
  *   saved, scratch: rglru_proj_workspace_bytes() (scratch holds the FP32
- *               logits and the GEMM library's workspace)
- * The first call on a host thread creates that thread's cuBLAS handle (the
- * one place where this library allocates device memory itself).
+ *               logits, the gradient parts and the packed weight images)
  * Errors: as rglru_forward, plus LRS_ERR_UNSUPPORTED unless D is a multiple
  * of 128 (dk a multiple of 8). */
 int rglru_proj_workspace_bytes(int B, int L, int D, size_t* saved_bytes, size_t* scratch_bytes);
@@ -303,9 +302,10 @@ int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const v
 /* Backward of rglru_proj_forward: the scan backward with the logits
  * recomputed, then dx = dx_scan + dlx W_x^T + dla W_a^T per block,
  * dW_x = x^T dlx, dW_a = x^T dla, db = sum over tokens of dl.  The gate
- * gradients and dx_scan enter the two GEMMs (one for dx with K = 6 D/16, one
- * for dW with K = B L) as BF16 leading parts plus BF16 remainders (16
- * significant bits); the bias and alpha gradients are fixed-order sums.
+ * gradients and dx_scan enter the two tensor-core contractions (one for dx
+ * with K = 6 D/16, one for dW with K = B L, split over the tokens and added in
+ * a fixed order) as BF16 leading parts plus BF16 remainders (16 significant
+ * bits); the bias and alpha gradients are fixed-order sums.
  *
  *   dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, B, L, D, saved: as above
  *   dx          [B,L,D] BF16 or FP32 by grad_dtype (out)

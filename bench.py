@@ -554,13 +554,10 @@ def run_ours(args, rank, world, local):
     # between its own events on the copy stream
     h2d_ms = statistics.median(ev[0].elapsed_time(ev[1]) for ev in copy_ev)
     d2h_ms = statistics.median(ev[2].elapsed_time(ev[3]) for ev in copy_ev)
-    # step i's D2H block runs beside step i+1's H2D block
-    def _ov(a, b):
-        lo = max(e0.elapsed_time(a[0]), e0.elapsed_time(b[2]))
-        hi = min(e0.elapsed_time(a[1]), e0.elapsed_time(b[3]))
-        return max(0.0, hi - lo) / max(1e-9, min(a[0].elapsed_time(a[1]), b[2].elapsed_time(b[3])))
-    overlap = statistics.median(_ov(copy_ev[i + 1], copy_ev[i]) for i in range(len(copy_ev) - 1)) \
-        if len(copy_ev) > 1 else 0.0
+    # share of the timed region during which each copy direction was busy
+    # (both near 1: the two directions ran side by side the whole time)
+    h2d_busy = sum(ev[0].elapsed_time(ev[1]) for ev in copy_ev) / e2e_ms
+    d2h_busy = sum(ev[2].elapsed_time(ev[3]) for ev in copy_ev) / e2e_ms
     e2e_ms = reduce_max(e2e_ms, world, dev)
     e2e_value = world * B * L * K2 / (e2e_ms / 1e3) / 1e6
 
@@ -581,11 +578,10 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K2, "ms_per_step": round(e2e_ms / K2, 4),
                 "h2d_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms / 1e3) / 1e9, 1),
-                "copy_overlap": round(overlap, 3),
+                "h2d_busy": round(h2d_busy, 3), "d2h_busy": round(d2h_busy, 3),
                 "overlap": "two buffer sets; H2D of step i+1 and D2H of step i-1 overlap step i",
                 "rates": "median per-step H2D and D2H block durations between events on the copy streams; "
-                         "copy_overlap: median share of the shorter of step i's D2H and step i+1's H2D during which "
-                         "both ran"},
+                         "*_busy: their summed durations over the timed region"},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -18,8 +18,9 @@
 //
 // The same kernels serve the mixer with its two 16-block block-diagonal gate
 // projections (logit modes 1 and 2 below; the "PL" variants): the logits are
-// x W (+ the biases, added on reading), from cuBLAS in FP32 or, in the
-// forward, formed per tile on the tensor cores.
+// x W (+ the biases, added on reading), FP32 products of the library's
+// tensor-core contraction kernel or, in the forward, formed per tile on the
+// tensor cores inside the scan.
 #include "kernels.cuh"
 #include "umma.cuh"
 
@@ -30,7 +31,8 @@ constexpr int kRgBoxBytes = kRgTile * kRowBytes;   // one BF16 [128 x 64] box
 
 // Where the gate logits come from (the kernels' LM parameter):
 //   0  BF16 [128 x 64] boxes of the raw l^x, l^a inputs;
-//   1  FP32 [128 x 64] boxes of the products x W (cuBLAS), biases added on reading;
+//   1  FP32 [128 x 64] boxes of the products x W (tensor-core contraction
+//      kernel), biases added on reading;
 //   2  computed in the kernel on the tensor cores (forward): the tile's x box
 //      (TMA, 128-byte swizzle) times the group's packed weights (both gates),
 //      FP32 accumulators in tensor memory, staged to shared memory as

@@ -1,5 +1,5 @@
 """RG-LRU mixer with its two 16-block block-diagonal gate projections: CUDA
-path (cuBLAS batched GEMMs + the FP32-logit scan, through the C ABI) vs the
+path (tcgen05 contraction kernels + the FP32-logit scan, through the C ABI) vs the
 FP64 oracle (numpy projections + the oracle scan), element by element."""
 import pytest
 

@@ -105,8 +105,10 @@ int lrs_selftest_wait_timeout(void* scratch, cudaStream_t stream);
  * 7 RG-LRU scan forward, 8 RG-LRU scan backward, 9 RG-LRU alpha reduction,
  * 10 SAMU forward maps, 11 SAMU backward maps, 12 SAMU decode prepare,
  * 13 SAMU decode step, 14 RG-LRU gate-projection GEMMs, 15 RG-LRU projection
- * backward GEMMs, 16 RG-LRU weight packing and dW combination; 9 also covers
- * the bias-gradient reductions) and duration in milliseconds; *count receives the number of
+ * backward GEMMs, 16 RG-LRU weight packing and dW combination, 17 RecurrentBlock
+ * contractions, 18 RecurrentBlock norms, convolution, join and fixed-order
+ * gradient sums; 9 also covers the bias-gradient reductions) and duration in
+ * milliseconds; *count receives the number of
  * kernels launched while profiling was on.  Not thread-safe: one profiling
  * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),
  * LRS_ERR_CUDA. */
@@ -317,6 +319,98 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
                         const uint8_t* reset, int B, int L, int D, const void* saved, void* dx, int grad_dtype,
                         float* dw_x, float* db_x, float* dw_a, float* db_a, float* dalpha, float* dh0,
                         void* scratch, cudaStream_t stream);
+
+/* ======================================================================== */
+/* One RecurrentBlock around the SAMU mixer                                  */
+/* ======================================================================== */
+
+/* The mixer inside one complete block ([SAMU page] section 03, single-block
+ * table and the glossary entry on the complete block: normalisation, two
+ * input projections, per-channel convolution, the mixer, the join and output
+ * projection, a second normalisation and a gated MLP, with the input and
+ * parameter backward; the SAMU project page: the block's wide input branch,
+ * split into real and imaginary halves, is the mixer's write w).  Widths: Dm
+ * (the residual stream), D (the mixer, M = D/2 modes), F = 3 Dm (the MLP).
+ * The pages leave the layers' details open; this library reads them as:
+ *   h1 = RMSNorm(x; gamma1)          RMSNorm(x; g) = x / sqrt(mean(x^2) + 1e-6) * g
+ *   [g | v] = h1 w_in^T              g: gate branch, v: recurrent branch (D each)
+ *   u[t] = conv_b + sum_{j<4} conv_k[j] v[t-j]   causal, per channel; taps before
+ *                                    the start of t's segment (reset) are zero
+ *   (y_mix, hT) = SAMU(x_sel = u, w = u, h0, reset)   exactly samu_forward
+ *   r1 = x + (GeLU(g) y_mix) w_o^T   GeLU(x) = x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))
+ *   h2 = RMSNorm(r1; gamma2)
+ *   [a | b] = h2 w_mlp_in^T;  out = r1 + (GeLU(a) b) w_mlp_out^T
+ * Every activation between layers is stored in BF16 (round to nearest even)
+ * and every contraction accumulates in FP32 on the tensor cores.
+ *
+ * Parameters (device pointers in a host struct; BF16 matrices are row-major
+ * [out][in], FP32 vectors contiguous): */
+typedef struct {
+    const float* gamma1;     /* [Dm] */
+    const void* w_in;        /* [2D][Dm] BF16: rows 0..D-1 gate branch, D..2D-1 recurrent branch */
+    const float* conv_k;     /* [4][D]: tap j multiplies v[t-j] */
+    const float* conv_b;     /* [D] */
+    const float* nu;         /* [M]  the mixer's parameters, as samu_forward */
+    const float* theta;      /* [M] */
+    const float* w_phi;      /* [D+1] */
+    const float* w_r;        /* [D+1] */
+    const float* a_phi;      /* one FP32 */
+    const float* a_r;        /* one FP32 */
+    const void* w_o;         /* [Dm][D] BF16 */
+    const float* gamma2;     /* [Dm] */
+    const void* w_mlp_in;    /* [2F][Dm] BF16: rows 0..F-1 the GeLU branch a, F..2F-1 the linear branch b */
+    const void* w_mlp_out;   /* [Dm][F] BF16 */
+} samu_block_params;
+
+/* Parameter gradients (FP32, the parameters' shapes; every one overwritten). */
+typedef struct {
+    float* dgamma1; float* dw_in; float* dconv_k; float* dconv_b;
+    float* dnu; float* dtheta; float* dw_phi; float* dw_r; float* da_phi; float* da_r;
+    float* dw_o; float* dgamma2; float* dw_mlp_in; float* dw_mlp_out;
+} samu_block_grads;
+
+/* Bytes of `saved` (the mixer's saved buffer plus the block's BF16
+ * activations) and `scratch` for shape (B, L, Dm, D).  Pure host function.
+ * Errors: LRS_ERR_ARG / LRS_ERR_UNSUPPORTED as samu_block_forward. */
+int samu_block_workspace_bytes(int B, int L, int Dm, int D, size_t* saved_bytes, size_t* scratch_bytes);
+
+/* Block forward.
+ *   p          parameters (host struct of device pointers; every field required)
+ *   x          [B,L,Dm] BF16 (in)
+ *   h0         [B,M,2] FP32 (in) or NULL;  reset [B,L] uint8 (in) or NULL
+ *   out        [B,L,Dm] BF16 (out);  hT [B,M,2] FP32 (out)
+ *   saved, scratch: samu_block_workspace_bytes()
+ * lrs_device_status(scratch) reports the whole call (the mixer included).
+ * Errors: LRS_ERR_ARG (null or misaligned pointer, bad shape),
+ * LRS_ERR_UNSUPPORTED unless Dm and D are multiples of 256 with Dm <= 4096,
+ * D <= 4096 and B*L < 2^31, LRS_ERR_CUDA. */
+int samu_block_forward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                       int B, int L, int Dm, int D, void* out, float* hT, void* saved, void* scratch,
+                       cudaStream_t stream);
+
+/* Block backward for the cotangents dout [B,L,Dm] BF16 and dhT [B,M,2] FP32
+ * (or NULL): dx [B,L,Dm] BF16 (out), dh0 [B,M,2] FP32 (out) and every
+ * parameter gradient in g (out).  Gradients between layers are BF16; the
+ * weight gradients are FP32 contractions over the tokens (split over the
+ * tokens and added in a fixed order: deterministic).  The inputs must be the
+ * forward's and `saved` its saved buffer.  Errors: as samu_block_forward. */
+int samu_block_backward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                        const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved,
+                        void* dx, float* dh0, const samu_block_grads* g, void* scratch, cudaStream_t stream);
+
+/* The block's tensor-core contraction on its own (for tests), layouts:
+ *   LRS_GEMM_NT  C [M][N] BF16 = A [M][K] . B [N][K]^T
+ *   LRS_GEMM_NN  C [M][N] BF16 = A [M][K] . B [K][N]
+ *   LRS_GEMM_TN  C [M][N] FP32 = A [K][M]^T . B [K][N]   (one split)
+ * FP32 accumulation, BF16 results rounded to nearest even.  N must be a
+ * multiple of 256 and K of 64 (NT, NN); M a multiple of 128 (TN); other
+ * sizes return LRS_ERR_UNSUPPORTED.  scratch: 256 bytes (the status word).
+ * Errors: LRS_ERR_ARG, LRS_ERR_UNSUPPORTED, LRS_ERR_CUDA. */
+#define LRS_GEMM_NT 0
+#define LRS_GEMM_NN 1
+#define LRS_GEMM_TN 2
+int lrs_dense_gemm(int layout, const void* A, const void* Bm, void* C, int M, int N, int K, void* scratch,
+                   cudaStream_t stream);
 
 /* ======================================================================== */
 /* SAMU forward without allocation                                           */

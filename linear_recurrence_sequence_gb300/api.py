@@ -53,7 +53,23 @@ _SIGNATURES = {
     "rglru_proj_workspace_bytes": ([_I, _I, _I, _SZP, _SZP], _I),
     "rglru_proj_forward": ([_P] * 8 + [_I, _I, _I] + [_P] * 6, _I),
     "rglru_proj_backward": ([_P] * 10 + [_I, _I, _I] + [_P] * 2 + [_I] + [_P] * 8, _I),
+    "samu_block_workspace_bytes": ([_I] * 4 + [_SZP, _SZP], _I),
+    "samu_block_forward": ([_P] * 4 + [_I] * 4 + [_P] * 5, _I),
+    "samu_block_backward": ([_P] * 6 + [_I] * 4 + [_P] * 6, _I),
+    "lrs_dense_gemm": ([_I, _P, _P, _P, _I, _I, _I, _P, _P], _I),
 }
+
+# samu_block_params / samu_block_grads (include/samu.h): one pointer per field, in order
+BLOCK_PARAMS = ("gamma1", "w_in", "conv_k", "conv_b", "nu", "theta", "w_phi", "w_r", "a_phi", "a_r",
+                "w_o", "gamma2", "w_mlp_in", "w_mlp_out")
+
+
+class _BlockParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in BLOCK_PARAMS]
+
+
+class _BlockGrads(ctypes.Structure):
+    _fields_ = [("d" + n, ctypes.c_void_p) for n in BLOCK_PARAMS]
 
 
 def library_path() -> str:
@@ -439,6 +455,127 @@ def rglru_proj_backward(dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, saved,
     return o
 
 
+# ---------------------------------------------------------------------------
+# One RecurrentBlock around the SAMU mixer
+# ---------------------------------------------------------------------------
+def samu_block_workspace_bytes(B: int, L: int, Dm: int, D: int):
+    lib = _load()
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    _check("samu_block_workspace_bytes",
+           lib.samu_block_workspace_bytes(B, L, Dm, D, ctypes.byref(s), ctypes.byref(c)))
+    return int(s.value), int(c.value)
+
+
+def _block_shapes(Dm: int, D: int) -> dict:
+    M, F = D // 2, 3 * Dm
+    return {"gamma1": (Dm,), "w_in": (2 * D, Dm), "conv_k": (4, D), "conv_b": (D,), "nu": (M,), "theta": (M,),
+            "w_phi": (D + 1,), "w_r": (D + 1,), "a_phi": (1,), "a_r": (1,), "w_o": (Dm, D), "gamma2": (Dm,),
+            "w_mlp_in": (2 * F, Dm), "w_mlp_out": (Dm, F)}
+
+
+_BLOCK_BF16 = ("w_in", "w_o", "w_mlp_in", "w_mlp_out")
+
+
+def _block_params(params: dict, Dm: int, dev) -> _BlockParams:
+    D = 2 * params["nu"].numel()
+    shapes = _block_shapes(Dm, D)
+    st = _BlockParams()
+    for n in BLOCK_PARAMS:
+        dt = torch.bfloat16 if n in _BLOCK_BF16 else torch.float32
+        setattr(st, n, _need(params.get(n), n, dt, dev, shapes[n]).data_ptr())
+    return st
+
+
+def samu_block_forward(x, params: dict, h0=None, reset=None, *, out=None, saved=None, scratch=None):
+    """One RecurrentBlock forward through ``samu_block_forward``.  x: [B,L,Dm] BF16;
+    params: dict of the block's parameters (``BLOCK_PARAMS``).  Returns dict(out, hT, saved, scratch)."""
+    dev = x.device
+    B, L, Dm = x.shape
+    _need(x, "x", torch.bfloat16, dev)
+    D = 2 * params["nu"].numel()
+    M = D // 2
+    _opt(h0, "h0", torch.float32, dev, (B, M, 2))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    ps = _block_params(params, Dm, dev)
+    nsaved, nscratch = samu_block_workspace_bytes(B, L, Dm, D)
+    y = _empty((B, L, Dm), torch.bfloat16, dev, out, "out")
+    hT = _empty((B, M, 2), torch.float32, dev, out, "hT")
+    if saved is None:
+        saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    if saved.numel() < nsaved or scratch.numel() < nscratch:
+        raise ValueError("saved/scratch buffers are too small")
+    st = _load().samu_block_forward(ctypes.cast(ctypes.pointer(ps), _P), _ptr(x), _ptr(h0), _ptr(reset), B, L, Dm,
+                                    D, _ptr(y), _ptr(hT), _ptr(saved), _ptr(scratch), _stream(dev))
+    _check("samu_block_forward", st)
+    return {"out": y, "hT": hT, "saved": saved, "scratch": scratch}
+
+
+def samu_block_backward(dout, dhT, x, params: dict, h0, reset, saved, *, out=None, scratch=None):
+    """Backward of samu_block_forward.  Returns dict(dx, dh0, d<param> for every
+    parameter (FP32, the parameter's shape), scratch)."""
+    dev = x.device
+    B, L, Dm = x.shape
+    D = 2 * params["nu"].numel()
+    M = D // 2
+    _need(dout, "dout", torch.bfloat16, dev, (B, L, Dm))
+    _opt(dhT, "dhT", torch.float32, dev, (B, M, 2))
+    _opt(reset, "reset", torch.uint8, dev, (B, L))
+    ps = _block_params(params, Dm, dev)
+    nsaved, nscratch = samu_block_workspace_bytes(B, L, Dm, D)
+    if saved is None or saved.numel() < nsaved:
+        raise ValueError("saved must be the forward's saved buffer")
+    if scratch is None:
+        scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    shapes = _block_shapes(Dm, D)
+    o = {"dx": _empty((B, L, Dm), torch.bfloat16, dev, out, "dx"),
+         "dh0": _empty((B, M, 2), torch.float32, dev, out, "dh0")}
+    gs = _BlockGrads()
+    for n in BLOCK_PARAMS:
+        o["d" + n] = _empty(shapes[n], torch.float32, dev, out, "d" + n)
+        setattr(gs, "d" + n, o["d" + n].data_ptr())
+    st = _load().samu_block_backward(ctypes.cast(ctypes.pointer(ps), _P), _ptr(x), _ptr(h0), _ptr(reset),
+                                     _ptr(dout), _ptr(dhT), B, L, Dm, D, _ptr(saved), _ptr(o["dx"]),
+                                     _ptr(o["dh0"]), ctypes.cast(ctypes.pointer(gs), _P), _ptr(scratch),
+                                     _stream(dev))
+    _check("samu_block_backward", st)
+    o["scratch"] = scratch
+    return o
+
+
+LRS_GEMM_NT, LRS_GEMM_NN, LRS_GEMM_TN = 0, 1, 2
+
+
+def dense_gemm(layout: int, A, B, M: int, N: int, K: int, *, out=None, scratch=None):
+    """The block's tensor-core contraction on its own (``lrs_dense_gemm``):
+    NT: C[M,N] = A[M,K] B[N,K]^T (BF16); NN: C = A[M,K] B[K,N] (BF16);
+    TN: C[M,N] = A[K,M]^T B[K,N] (FP32)."""
+    dev = A.device
+    _need(A, "A", torch.bfloat16, dev, (K, M) if layout == LRS_GEMM_TN else (M, K))
+    _need(B, "B", torch.bfloat16, dev, (N, K) if layout == LRS_GEMM_NT else (K, N))
+    dt = torch.float32 if layout == LRS_GEMM_TN else torch.bfloat16
+    C = out if out is not None else torch.empty((M, N), dtype=dt, device=dev)
+    _need(C, "C", dt, dev, (M, N))
+    if scratch is None:
+        scratch = torch.empty(256, dtype=torch.uint8, device=dev)
+    _check("lrs_dense_gemm", _load().lrs_dense_gemm(layout, _ptr(A), _ptr(B), _ptr(C), M, N, K, _ptr(scratch),
+                                                    _stream(dev)))
+    return C
+
+
+def block_tensors_from_numpy(inp: dict, device) -> dict:
+    """Device tensors of synth.block_inputs: {"x", "dout", "h0", "dhT", "reset", "params": {...}}."""
+    params = {}
+    for n in BLOCK_PARAMS:
+        params[n] = _bf16(inp[n], device) if n in _BLOCK_BF16 else _f32(inp[n], device)
+    out = {"x": _bf16(inp["x"], device), "dout": _bf16(inp["dout"], device), "h0": _f32(inp["h0"], device),
+           "dhT": _f32(inp["dhT"], device), "params": params}
+    out["reset"] = None if inp["reset"] is None else torch.from_numpy(inp["reset"]).to(device)
+    return out
+
+
 def selftest_wait_timeout(scratch, device=None) -> None:
     """Launches the library's failure-path self-test on ``scratch`` (see
     lrs_selftest_wait_timeout); with ``scratch=None``, on the status word of the
@@ -470,7 +607,7 @@ KERNEL_NAMES = {
     7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
     10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel", 12: "samu_decode_prepare_kernel",
     13: "samu_decode_step_kernel", 14: "proj_gemm_kernel<logits>", 15: "proj_gemm_kernel<dx, dW>",
-    16: "proj_pack_kernel",
+    16: "proj_pack_kernel", 17: "block_gemm_kernel", 18: "block_elementwise_kernels",
 }
 
 

@@ -1,6 +1,7 @@
 // extern "C" entry points declared in include/samu.h: argument checks,
 // workspace carving and kernel launches.  No allocation, no synchronisation
 // (except lrs_device_status, which documents that it synchronises).
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -78,7 +79,7 @@ enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
     KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
     KID_SAMU_BWD_MAPS, KID_SAMU_DECODE_PREP, KID_SAMU_DECODE_STEP, KID_RGLRU_PROJ_FWD, KID_RGLRU_PROJ_BWD,
-    KID_RGLRU_PROJ_PACK
+    KID_RGLRU_PROJ_PACK, KID_BLOCK_GEMM, KID_BLOCK_ELEM
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -649,6 +650,282 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     LRS_LAUNCH(KID_RGLRU_PROJ_BWD, stream,
                launch_proj_dw(a.gparts, x, at<float>(scratch, ps.dwpart), dw_x, dw_a, D, pd, status, stream, false));
     (void)dk;
+    return LRS_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// RecurrentBlock around the SAMU mixer
+// ---------------------------------------------------------------------------
+namespace {
+
+int check_block_shape(int B, int L, int Dm, int D) {
+    if (Dm < 1) return LRS_ERR_ARG;
+    const int st = check_samu_shape(B, L, D);
+    if (st != LRS_OK) return st;
+    if (Dm % 256 != 0 || D % 256 != 0 || Dm > 4096) return LRS_ERR_UNSUPPORTED;
+    if ((long long)B * L >= (1LL << 31)) return LRS_ERR_UNSUPPORTED;
+    return LRS_OK;
+}
+
+// The four weight-gradient contractions (rows M x columns N of the gradient).
+struct BlockDw {
+    int M, N;
+};
+void block_dws(int Dm, int D, BlockDw (&w)[4]) {
+    const int F = kBlockMlpRatio * Dm;
+    w[0] = {Dm, F};        // w_mlp_out
+    w[1] = {2 * F, Dm};    // w_mlp_in
+    w[2] = {Dm, D};        // w_o
+    w[3] = {2 * D, Dm};    // w_in
+}
+
+BlockScratch block_scratch(int B, int L, int Dm, int D) {
+    BlockDw w[4];
+    block_dws(Dm, D, w);
+    size_t wp = 0;
+    for (const BlockDw& d : w) {
+        const int sp = block_gemm_splits(d.M, d.N, (long long)B * L, kBlockSmsBound);
+        if (sp > 1) wp = std::max(wp, (size_t)sp * d.M * d.N);
+    }
+    const size_t np = (size_t)block_norm_bwd_ctas((long long)B * L) * Dm;
+    const size_t cp = (size_t)block_conv_parts(B, L) * 5 * D;
+    return block_scratch_layout(B, L, Dm, D, wp, np, cp);
+}
+
+bool block_params_ok(const samu_block_params* p) {
+    return p != nullptr && req(p->gamma1) && req(p->w_in) && req(p->conv_k) && req(p->conv_b) && req(p->nu) &&
+           req(p->theta) && req(p->w_phi) && req(p->w_r) && p->a_phi != nullptr && p->a_r != nullptr &&
+           req(p->w_o) && req(p->gamma2) && req(p->w_mlp_in) && req(p->w_mlp_out);
+}
+
+bool block_grads_ok(const samu_block_grads* g) {
+    return g != nullptr && req(g->dgamma1) && req(g->dw_in) && req(g->dconv_k) && req(g->dconv_b) && req(g->dnu) &&
+           req(g->dtheta) && req(g->dw_phi) && req(g->dw_r) && g->da_phi != nullptr && g->da_r != nullptr &&
+           req(g->dw_o) && req(g->dgamma2) && req(g->dw_mlp_in) && req(g->dw_mlp_out);
+}
+
+BlockGemmArgs gemm_args(int layout, int epi, int M, int N, int K, uint32_t* status) {
+    BlockGemmArgs g{};
+    g.layout = layout;
+    g.epi = epi;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.splits = 1;
+    g.status = status;
+    return g;
+}
+
+// dW [M][N] = A^T B over the tokens: split partials into wpart and a fixed-order
+// sum, or straight into dw with one split.
+int block_weight_grad(const void* A, const void* Bm, int M, int N, long long BL, float* dw, float* wpart,
+                      uint32_t* status, cudaStream_t stream) {
+    BlockGemmArgs g = gemm_args(kBgTN, kEpiF32, M, N, (int)BL, status);
+    g.splits = block_gemm_splits(M, N, BL, block_gemm_sms());
+    g.part = g.splits > 1 ? wpart : dw;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, A, Bm, stream, pdl_ok()));
+    if (g.splits > 1)
+        LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+                   launch_sum_parts(wpart, (long long)M * N, g.splits, (long long)M * N, dw, stream, pdl_ok()));
+    return LRS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int samu_block_workspace_bytes(int B, int L, int Dm, int D, size_t* saved_bytes, size_t* scratch_bytes) {
+    const int st = check_block_shape(B, L, Dm, D);
+    if (st != LRS_OK) return st;
+    if (saved_bytes != nullptr) *saved_bytes = block_saved_layout(B, L, Dm, D).total;
+    if (scratch_bytes != nullptr) *scratch_bytes = block_scratch(B, L, Dm, D).total;
+    return LRS_OK;
+}
+
+int samu_block_forward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset, int B,
+                       int L, int Dm, int D, void* out, float* hT, void* saved, void* scratch, cudaStream_t stream) {
+    const int st0 = check_block_shape(B, L, Dm, D);
+    if (st0 != LRS_OK) return st0;
+    if (!block_params_ok(p) || !req(x) || !opt(h0) || !req(out) || !req(hT) || !req(saved) || !req(scratch))
+        return LRS_ERR_ARG;
+    const long long BL = (long long)B * L;
+    const int F = kBlockMlpRatio * Dm;
+    const BlockSaved sv = block_saved_layout(B, L, Dm, D);
+    const BlockScratch sc = block_scratch(B, L, Dm, D);
+    uint32_t* status = at<uint32_t>(scratch, 0);
+    void* msaved = at<void>(saved, sv.mixer);
+    void* mscratch = at<void>(scratch, sc.mixer);
+    const uint32_t* mstatus = at<uint32_t>(mscratch, samu_scratch_layout(B, L, D).status);
+    void* h1 = at<void>(saved, sv.h1);
+    float* rstd1 = at<float>(saved, sv.rstd1);
+    void* gv = at<void>(saved, sv.gv);
+    void* u = at<void>(saved, sv.u);
+    void* ym = at<void>(saved, sv.ym);
+    void* j = at<void>(saved, sv.j);
+    void* r1 = at<void>(saved, sv.r1);
+    float* rstd2 = at<float>(saved, sv.rstd2);
+    void* h2 = at<void>(saved, sv.h2);
+    void* ab = at<void>(saved, sv.ab);
+    void* q = at<void>(saved, sv.q);
+
+    // h1 = RMSNorm(x); [g | v] = h1 w_in^T; u = conv(v)
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_rmsnorm_fwd(x, p->gamma1, h1, rstd1, BL, Dm, status, stream, false));
+    BlockGemmArgs g = gemm_args(kBgNT, kEpiStore, (int)BL, 2 * D, Dm, status);
+    g.out = static_cast<uint16_t*>(gv);
+    g.ldo = 2 * D;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h1, p->w_in, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+               launch_conv_fwd(gv, p->conv_k, p->conv_b, reset, u, B, L, D, stream, pdl_ok()));
+    // the mixer on x_sel = w = u
+    const int st = samu_forward(u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L, D, ym,
+                                nullptr, hT, msaved, mscratch, stream);
+    if (st != LRS_OK) return st;
+    // j = GeLU(g) y_mix; r1 = x + j w_o^T
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_join_fwd(gv, ym, j, BL, D, status, mstatus, stream, pdl_ok()));
+    g = gemm_args(kBgNT, kEpiResid, (int)BL, Dm, D, status);
+    g.out = static_cast<uint16_t*>(r1);
+    g.ldo = Dm;
+    g.r = static_cast<const uint16_t*>(x);
+    g.ldr = Dm;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, j, p->w_o, stream, pdl_ok()));
+    // h2 = RMSNorm(r1); [a | b] = h2 w_mlp_in^T, q = GeLU(a) b; out = r1 + q w_mlp_out^T
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_rmsnorm_fwd(r1, p->gamma2, h2, rstd2, BL, Dm, nullptr, stream, pdl_ok()));
+    g = gemm_args(kBgNT, kEpiGlu, (int)BL, F, Dm, status);
+    g.out = static_cast<uint16_t*>(q);
+    g.ldo = F;
+    g.out2 = static_cast<uint16_t*>(ab);
+    g.ld2 = 2 * F;
+    g.F = F;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h2, p->w_mlp_in, stream, pdl_ok()));
+    g = gemm_args(kBgNT, kEpiResid, (int)BL, Dm, F, status);
+    g.out = static_cast<uint16_t*>(out);
+    g.ldo = Dm;
+    g.r = static_cast<const uint16_t*>(r1);
+    g.ldr = Dm;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, q, p->w_mlp_out, stream, pdl_ok()));
+    return LRS_OK;
+}
+
+int samu_block_backward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                        const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved, void* dx,
+                        float* dh0, const samu_block_grads* gr, void* scratch, cudaStream_t stream) {
+    const int st0 = check_block_shape(B, L, Dm, D);
+    if (st0 != LRS_OK) return st0;
+    if (!block_params_ok(p) || !block_grads_ok(gr) || !req(x) || !opt(h0) || !req(dout) || !opt(dhT) ||
+        !req(saved) || !req(dx) || !req(dh0) || !req(scratch))
+        return LRS_ERR_ARG;
+    const long long BL = (long long)B * L;
+    const int F = kBlockMlpRatio * Dm;
+    const BlockSaved sv = block_saved_layout(B, L, Dm, D);
+    const BlockScratch sc = block_scratch(B, L, Dm, D);
+    uint32_t* status = at<uint32_t>(scratch, 0);
+    const void* msaved = at<void>(saved, sv.mixer);
+    void* mscratch = at<void>(scratch, sc.mixer);
+    const uint32_t* mstatus = at<uint32_t>(mscratch, samu_scratch_layout(B, L, D).status);
+    const void* h1 = at<void>(saved, sv.h1);
+    const float* rstd1 = at<float>(saved, sv.rstd1);
+    const void* gv = at<void>(saved, sv.gv);
+    const void* u = at<void>(saved, sv.u);
+    const void* ym = at<void>(saved, sv.ym);
+    const void* j = at<void>(saved, sv.j);
+    const void* r1 = at<void>(saved, sv.r1);
+    const float* rstd2 = at<float>(saved, sv.rstd2);
+    const void* h2 = at<void>(saved, sv.h2);
+    const void* ab = at<void>(saved, sv.ab);
+    const void* q = at<void>(saved, sv.q);
+    void* dab = at<void>(scratch, sc.dab);
+    void* dh2 = at<void>(scratch, sc.dh2);
+    void* dr1 = at<void>(scratch, sc.dr1);
+    void* dym = at<void>(scratch, sc.dym);
+    void* dgv = at<void>(scratch, sc.dgv);
+    void* dxs = at<void>(scratch, sc.dxs);
+    void* dwm = at<void>(scratch, sc.dwm);
+    void* dh1 = at<void>(scratch, sc.dh1);
+    float* wpart = at<float>(scratch, sc.wpart);
+    float* npart = at<float>(scratch, sc.npart);
+    float* cpart = at<float>(scratch, sc.cpart);
+    const int ncta = block_norm_bwd_ctas(BL);
+    int st;
+
+    if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    // gated MLP: dq = dout w_mlp_out -> [da | db]; dW_mlp_out = dout^T q
+    BlockGemmArgs g = gemm_args(kBgNN, kEpiGluBwd, (int)BL, F, Dm, status);
+    g.out = static_cast<uint16_t*>(dab);
+    g.ldo = 2 * F;
+    g.e0 = static_cast<const uint16_t*>(ab);
+    g.lde0 = 2 * F;
+    g.F = F;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dout, p->w_mlp_out, stream, false));
+    if ((st = block_weight_grad(dout, q, Dm, F, BL, gr->dw_mlp_out, wpart, status, stream)) != LRS_OK) return st;
+    // dh2 = [da | db] w_mlp_in; dW_mlp_in = [da | db]^T h2
+    g = gemm_args(kBgNN, kEpiStore, (int)BL, Dm, 2 * F, status);
+    g.out = static_cast<uint16_t*>(dh2);
+    g.ldo = Dm;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dab, p->w_mlp_in, stream, pdl_ok()));
+    if ((st = block_weight_grad(dab, h2, 2 * F, Dm, BL, gr->dw_mlp_in, wpart, status, stream)) != LRS_OK) return st;
+    // dr1 = dout + RMSNorm'(dh2)
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+               launch_rmsnorm_bwd(r1, p->gamma2, rstd2, dh2, dout, dr1, npart, BL, Dm, nullptr, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma2, stream, pdl_ok()));
+    // join: dj = dr1 w_o -> dy_mix, dg; dW_o = dr1^T j
+    g = gemm_args(kBgNN, kEpiJoinBwd, (int)BL, D, Dm, status);
+    g.out = static_cast<uint16_t*>(dym);
+    g.ldo = D;
+    g.out2 = static_cast<uint16_t*>(dgv);
+    g.ld2 = 2 * D;
+    g.e0 = static_cast<const uint16_t*>(gv);
+    g.lde0 = 2 * D;
+    g.e1 = static_cast<const uint16_t*>(ym);
+    g.lde1 = D;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dr1, p->w_o, stream, pdl_ok()));
+    if ((st = block_weight_grad(dr1, j, Dm, D, BL, gr->dw_o, wpart, status, stream)) != LRS_OK) return st;
+    // the mixer (x_sel = w = u): both of its input gradients reach u
+    st = samu_backward(dym, dhT, u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L, D,
+                       msaved, dxs, dwm, LRS_GRAD_BF16, dh0, gr->dnu, gr->dtheta, gr->dw_phi, gr->dw_r, gr->da_phi,
+                       gr->da_r, mscratch, stream);
+    if (st != LRS_OK) return st;
+    // convolution: dv (the recurrent half of [dg | dv]), dconv_k, dconv_b
+    const int cparts = block_conv_parts(B, L);
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+               launch_conv_bwd(gv, p->conv_k, reset, dxs, dwm, dgv, cpart, B, L, D, status, mstatus, stream,
+                               pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+               launch_sum_parts(cpart, 5LL * D, cparts, 4LL * D, gr->dconv_k, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+               launch_sum_parts(cpart + 4 * (size_t)D, 5LL * D, cparts, D, gr->dconv_b, stream, pdl_ok()));
+    // dh1 = [dg | dv] w_in; dW_in = [dg | dv]^T h1
+    g = gemm_args(kBgNN, kEpiStore, (int)BL, Dm, 2 * D, status);
+    g.out = static_cast<uint16_t*>(dh1);
+    g.ldo = Dm;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dgv, p->w_in, stream, pdl_ok()));
+    if ((st = block_weight_grad(dgv, h1, 2 * D, Dm, BL, gr->dw_in, wpart, status, stream)) != LRS_OK) return st;
+    // dx = dr1 + RMSNorm'(dh1)
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+               launch_rmsnorm_bwd(x, p->gamma1, rstd1, dh1, dr1, dx, npart, BL, Dm, nullptr, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma1, stream, pdl_ok()));
+    return LRS_OK;
+}
+
+int lrs_dense_gemm(int layout, const void* A, const void* Bm, void* C, int M, int N, int K, void* scratch,
+                   cudaStream_t stream) {
+    if (!req(A) || !req(Bm) || !req(C) || !req(scratch) || M < 1 || N < 1 || K < 1) return LRS_ERR_ARG;
+    if (layout != LRS_GEMM_NT && layout != LRS_GEMM_NN && layout != LRS_GEMM_TN) return LRS_ERR_ARG;
+    if (N % 256 != 0) return LRS_ERR_UNSUPPORTED;
+    if (layout != LRS_GEMM_TN && K % 64 != 0) return LRS_ERR_UNSUPPORTED;
+    if (layout == LRS_GEMM_TN && M % 128 != 0) return LRS_ERR_UNSUPPORTED;
+    uint32_t* status = at<uint32_t>(scratch, 0);
+    if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return LRS_ERR_CUDA;
+    BlockGemmArgs g = gemm_args(layout == LRS_GEMM_NT ? kBgNT : layout == LRS_GEMM_NN ? kBgNN : kBgTN,
+                                layout == LRS_GEMM_TN ? kEpiF32 : kEpiStore, M, N, K, status);
+    if (layout == LRS_GEMM_TN) {
+        g.part = static_cast<float*>(C);
+    } else {
+        g.out = static_cast<uint16_t*>(C);
+        g.ldo = N;
+    }
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, A, Bm, stream, false));
     return LRS_OK;
 }
 

@@ -1,0 +1,480 @@
+// Dense BF16 contractions of the RecurrentBlock on the fifth-generation tensor
+// cores (sm_103a).
+//
+// The block around the mixer ("SAMU 与 RG-LRU 的 H800 训练性能对比", section
+// 03, single-block table: normalisation, two input projections, per-channel
+// convolution, mixer, join and output projection, second normalisation,
+// gated MLP, with the input and parameter backward) is made of dense linear
+// layers.  One kernel template computes every one of their contractions,
+//   C(m, n) = sum_k A(m, k) B(n, k),
+// on 128 x 256 tiles with BF16 operands and FP32 accumulators in tensor
+// memory, in three operand layouts:
+//   NT  forward   y = x W^T:   A = x [rows][K] and B = W [N][K], both K-major;
+//   NN  dX        dx = dy W:   A = dy [rows][K] K-major, B(n, k) = W[k][n]
+//                              (MN-major: the weight's rows are the K index);
+//   TN  dW        dW = dy^T x: A(m, k) = dy[k][m], B(n, k) = x[k][n], both
+//                              MN-major (the token index is the row index of
+//                              both), split over the tokens with FP32 partials
+//                              added in a fixed order by a second kernel.
+// Roles: warp 4 streams 64-wide K slices of both operands by TMA (128-byte
+// swizzle) into a ring of stages; one thread of warp 5 issues tcgen05.mma
+// (M 128, N 256, K 16) and frees each stage with tcgen05.commit; warps 0-3
+// drain the accumulator (tcgen05.ld, one row per thread) through the layer's
+// fused epilogue.  Two accumulators (512 tensor-memory columns) let the
+// epilogue of one tile run under the MMAs of the next.  CTAs are persistent
+// over the tiles; every wait is bounded and an abort flag ends the other
+// roles after a failure.
+//
+// Fused epilogues (row t of the tile, columns n):
+//   store     C in BF16;
+//   resid     C + R in BF16 (the residual stream);
+//   glu       the tile's columns 0..127 are a = h W_1^T, 128..255 b = h W_2^T
+//             for the same 128 hidden units: a, b (BF16) and
+//             q = GeLU(a) b (BF16, from the rounded a and b);
+//   glu_bwd   C = dq: da = dq b GeLU'(a), db = dq GeLU(a) (BF16);
+//   join_bwd  C = dj: dy_mixer = dj GeLU(g), dg = dj y_mixer GeLU'(g) (BF16);
+//   f32       C in FP32 (dW partials).
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "tmap.cuh"
+#include "umma.cuh"
+
+namespace lrs {
+
+namespace {
+
+constexpr int kBgThreads = 192;   // warps 0-3 epilogue, 4 producer, 5 MMA
+constexpr int kBgK = 64;          // K per stage (one 128-byte swizzle row of BF16)
+constexpr int kBgM = 128;         // tile rows
+constexpr int kBgN = 256;         // tile columns (accumulator columns)
+constexpr int kBgStages = 4;
+constexpr uint32_t kBgABytes = kBgM * 128;            // 16 KB
+constexpr uint32_t kBgBBytes = kBgN * 128;            // 32 KB
+constexpr uint32_t kBgStageBytes = kBgABytes + kBgBBytes;
+constexpr size_t kBgSmem = (size_t)kBgStages * kBgStageBytes + 1024 + 16 * 1024;   // + alignment and slack
+constexpr uint32_t kBgTmemCols = 2 * kBgN;           // two accumulators
+
+constexpr float kGeluC = 0.7978845608028654f;   // sqrt(2 / pi)
+constexpr float kGeluA = 0.044715f;
+
+// GeLU (tanh form) and its derivative.
+__device__ __forceinline__ void gelu_fwd_grad(float x, float& g, float& dg) {
+    const float u = kGeluC * (x + kGeluA * x * x * x);
+    const float th = tanhf(u);
+    g = 0.5f * x * (1.f + th);
+    dg = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * kGeluC * (1.f + 3.f * kGeluA * x * x);
+}
+__device__ __forceinline__ float gelu_fwd(float x) {
+    const float u = kGeluC * (x + kGeluA * x * x * x);
+    return 0.5f * x * (1.f + tanhf(u));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf_round(float x) {   // value of RNE(x) in BF16, as FP32
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// 8 BF16 values from 16 bytes.
+__device__ __forceinline__ void unpack8(const uint4 q, float (&v)[8]) {
+    v[0] = bf_lo(q.x); v[1] = bf_hi(q.x); v[2] = bf_lo(q.y); v[3] = bf_hi(q.y);
+    v[4] = bf_lo(q.z); v[5] = bf_hi(q.z); v[6] = bf_lo(q.w); v[7] = bf_hi(q.w);
+}
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    uint4 q;
+    q.x = f2_to_bf2(v[0], v[1]);
+    q.y = f2_to_bf2(v[2], v[3]);
+    q.z = f2_to_bf2(v[4], v[5]);
+    q.w = f2_to_bf2(v[6], v[7]);
+    return q;
+}
+
+struct BgItem {
+    int mt, nt, s, k0, k1;
+};
+
+__device__ __forceinline__ BgItem bg_item(const BlockGemmArgs& a, int w) {
+    BgItem it;
+    if (a.layout == kBgTN) {
+        it.s = w % a.splits;
+        const int r = w / a.splits;
+        it.nt = r % a.n_tiles;
+        it.mt = r / a.n_tiles;
+        it.k0 = (int)((long long)a.ksteps * it.s / a.splits);
+        it.k1 = (int)((long long)a.ksteps * (it.s + 1) / a.splits);
+    } else {
+        it.mt = w / a.n_tiles;
+        it.nt = w % a.n_tiles;
+        it.s = 0;
+        it.k0 = 0;
+        it.k1 = a.ksteps;
+    }
+    return it;
+}
+
+// Epilogue of one accumulator row (row `m` of tile `it`, accumulator columns
+// at taddr).
+template <int EPI>
+__device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem& it, int m, uint32_t taddr) {
+    const long long t = (long long)it.mt * kBgM + m;
+    if (EPI == kEpiF32) {
+        float* o = a.part + ((size_t)it.s * a.M + (size_t)t) * a.N + (size_t)it.nt * kBgN;
+        for (int c = 0; c < kBgN; c += 16) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)c, v);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(o + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+        return;
+    }
+    const bool ok = t < a.M;
+    if (EPI == kEpiGlu) {
+        const int f0 = it.nt * (kBgN / 2);
+        for (int c = 0; c < kBgN / 2; c += 16) {
+            float va[16], vb[16];
+            tmem_ld16(taddr + (uint32_t)c, va);
+            tmem_ld16(taddr + (uint32_t)(kBgN / 2 + c), vb);
+            if (!ok) continue;
+            float q[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                va[j] = bf_round(va[j]);
+                vb[j] = bf_round(vb[j]);
+                q[j] = gelu_fwd(va[j]) * vb[j];
+            }
+            uint16_t* ab = a.out2 + (size_t)t * a.ld2 + f0 + c;
+            uint16_t* qo = a.out + (size_t)t * a.ldo + f0 + c;
+#pragma unroll
+            for (int j = 0; j < 16; j += 8) {
+                *reinterpret_cast<uint4*>(ab + j) = pack8(va + j);
+                *reinterpret_cast<uint4*>(ab + a.F + j) = pack8(vb + j);
+                *reinterpret_cast<uint4*>(qo + j) = pack8(q + j);
+            }
+        }
+        return;
+    }
+    const int n0 = it.nt * kBgN;
+    for (int c = 0; c < kBgN; c += 16) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+        if (!ok) continue;
+        const int n = n0 + c;
+        if (EPI == kEpiStore) {
+            uint16_t* o = a.out + (size_t)t * a.ldo + n;
+#pragma unroll
+            for (int j = 0; j < 16; j += 8) *reinterpret_cast<uint4*>(o + j) = pack8(v + j);
+        } else if (EPI == kEpiResid) {
+            const uint16_t* r = a.r + (size_t)t * a.ldr + n;
+            uint16_t* o = a.out + (size_t)t * a.ldo + n;
+#pragma unroll
+            for (int j = 0; j < 16; j += 8) {
+                float rv[8];
+                unpack8(*reinterpret_cast<const uint4*>(r + j), rv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[j + i] += rv[i];
+                *reinterpret_cast<uint4*>(o + j) = pack8(v + j);
+            }
+        } else if (EPI == kEpiGluBwd) {
+            const uint16_t* ap = a.e0 + (size_t)t * a.lde0 + n;   // a at column f, b at F + f
+            uint16_t* o = a.out + (size_t)t * a.ldo + n;          // da at f, db at F + f
+#pragma unroll
+            for (int j = 0; j < 16; j += 8) {
+                float av[8], bv[8], da[8], db[8];
+                unpack8(*reinterpret_cast<const uint4*>(ap + j), av);
+                unpack8(*reinterpret_cast<const uint4*>(ap + a.F + j), bv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float g, dg;
+                    gelu_fwd_grad(av[i], g, dg);
+                    da[i] = v[j + i] * bv[i] * dg;
+                    db[i] = v[j + i] * g;
+                }
+                *reinterpret_cast<uint4*>(o + j) = pack8(da);
+                *reinterpret_cast<uint4*>(o + a.F + j) = pack8(db);
+            }
+        } else if (EPI == kEpiJoinBwd) {
+            const uint16_t* gp = a.e0 + (size_t)t * a.lde0 + n;   // gate branch g
+            const uint16_t* yp = a.e1 + (size_t)t * a.lde1 + n;   // mixer output
+            uint16_t* o = a.out + (size_t)t * a.ldo + n;          // d y_mixer
+            uint16_t* o2 = a.out2 + (size_t)t * a.ld2 + n;        // d g
+#pragma unroll
+            for (int j = 0; j < 16; j += 8) {
+                float gv[8], yv[8], dym[8], dgo[8];
+                unpack8(*reinterpret_cast<const uint4*>(gp + j), gv);
+                unpack8(*reinterpret_cast<const uint4*>(yp + j), yv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float g, dg;
+                    gelu_fwd_grad(gv[i], g, dg);
+                    dym[i] = v[j + i] * g;
+                    dgo[i] = v[j + i] * yv[i] * dg;
+                }
+                *reinterpret_cast<uint4*>(o + j) = pack8(dym);
+                *reinterpret_cast<uint4*>(o2 + j) = pack8(dgo);
+            }
+        }
+    }
+}
+
+template <int LAYOUT, int EPI>
+__global__ void __launch_bounds__(kBgThreads, 1)
+    block_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      BlockGemmArgs a) {
+    extern __shared__ uint8_t bg_raw[];
+    __shared__ __align__(8) uint64_t s_full[kBgStages], s_empty[kBgStages], s_acc[2], s_free[2], s_fin;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bg_raw) + 1023u) & ~uintptr_t(1023));
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kBgStages; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_acc[i], 1);
+            mbar_init(&s_free[i], 4);   // the four epilogue warps
+        }
+        mbar_init(&s_fin, 1);
+        s_abort = 0;
+    }
+    if (warp == 5) {
+        tmem_alloc(&s_tmem, kBgTmemCols);
+        tmem_fence_before_sync();
+    }
+    pdl_trigger();
+    pdl_wait();
+    __syncthreads();
+    tmem_fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicOr(a.status, kStatusTimeout);
+    };
+
+    if (warp == 4) {
+        // producer: every K step of every tile of this CTA, in order
+        if (lane == 0) {
+            uint32_t n = 0;   // stages issued
+            for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x) {
+                const BgItem it = bg_item(a, w);
+                for (int ks = it.k0; ks < it.k1; ++ks, ++n) {
+                    const int slot = (int)(n % kBgStages);
+                    if (n >= (uint32_t)kBgStages &&
+                        !mbar_wait_bounded(&s_empty[slot], ((n / kBgStages) - 1) & 1u)) {
+                        fail();
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    uint8_t* sa = ring + (size_t)slot * kBgStageBytes;
+                    uint8_t* sb = sa + kBgABytes;
+                    const int k0 = kBgK * ks;
+                    mbar_arrive_expect_tx(&s_full[slot], kBgStageBytes);
+                    if (LAYOUT == kBgNT) {
+                        tma_load_2d(sa, &tm_a, k0, it.mt * kBgM, &s_full[slot]);
+                        const int r0 = EPI == kEpiGlu ? it.nt * (kBgN / 2) : it.nt * kBgN;
+                        const int r1 = EPI == kEpiGlu ? a.F + r0 : r0 + kBgN / 2;
+                        tma_load_2d(sb, &tm_b, k0, r0, &s_full[slot]);
+                        tma_load_2d(sb + kBgBBytes / 2, &tm_b, k0, r1, &s_full[slot]);
+                    } else if (LAYOUT == kBgNN) {
+                        tma_load_2d(sa, &tm_a, k0, it.mt * kBgM, &s_full[slot]);
+#pragma unroll
+                        for (int j = 0; j < kBgN / 64; ++j)
+                            tma_load_2d(sb + (size_t)j * 8192, &tm_b, it.nt * kBgN + 64 * j, k0, &s_full[slot]);
+                    } else {
+                        tma_load_2d(sa, &tm_a, it.mt * kBgM, k0, &s_full[slot]);
+                        tma_load_2d(sa + 8192, &tm_a, it.mt * kBgM + 64, k0, &s_full[slot]);
+#pragma unroll
+                        for (int j = 0; j < kBgN / 64; ++j)
+                            tma_load_2d(sb + (size_t)j * 8192, &tm_b, it.nt * kBgN + 64 * j, k0, &s_full[slot]);
+                    }
+                }
+            }
+            // copies still in flight land before the CTA may exit
+            const uint32_t lo = n > (uint32_t)kBgStages ? n - kBgStages : 0;
+            for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_full[j % kBgStages], (j / kBgStages) & 1u);
+        }
+    } else if (warp == 5) {
+        // MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(kBgM, kBgN) | (LAYOUT == kBgTN ? (1u << 15) : 0u) |
+                                       (LAYOUT != kBgNT ? (1u << 16) : 0u);
+            uint32_t n = 0, item = 0;
+            for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x, ++item) {
+                const BgItem it = bg_item(a, w);
+                const uint32_t buf = item & 1u;
+                // the epilogue has drained this accumulator's previous tile
+                if (item >= 2 && !mbar_wait_bounded(&s_free[buf], ((item >> 1) - 1) & 1u)) {
+                    fail();
+                    break;
+                }
+                tmem_fence_after_sync();
+                const uint32_t acc_t = tmem + buf * (uint32_t)kBgN;
+                bool ok = true;
+                for (int ks = it.k0; ks < it.k1; ++ks, ++n) {
+                    const int slot = (int)(n % kBgStages);
+                    if (!mbar_wait_bounded(&s_full[slot], (n / kBgStages) & 1u)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    tmem_fence_after_sync();
+                    const uint32_t sa = smem_u32(ring + (size_t)slot * kBgStageBytes);
+                    const uint32_t sb = sa + kBgABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBgK / 16; ++kk) {
+                        const bool accum = ks > it.k0 || kk > 0;
+                        const uint64_t da = LAYOUT == kBgTN ? umma_desc_sw128_mn(sa + 2048u * kk, 8192u)
+                                                            : umma_desc_sw128(sa + 32u * kk);
+                        const uint64_t db = LAYOUT == kBgNT ? umma_desc_sw128(sb + 32u * kk)
+                                                            : umma_desc_sw128_mn(sb + 2048u * kk, 8192u);
+                        umma_bf16(acc_t, da, db, idesc, accum);
+                    }
+                    umma_commit(&s_empty[slot]);   // the stage is free once these MMAs have read it
+                }
+                if (!ok) break;
+                umma_commit(&s_acc[buf]);
+            }
+            // every MMA issued by this thread has completed before the columns are released
+            umma_commit(&s_fin);
+            mbar_wait_bounded(&s_fin, 0);
+        }
+    } else {
+        // epilogue warps 0-3: accumulator rows 32 warp .. 32 warp + 31
+        uint32_t item = 0;
+        for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x, ++item) {
+            const BgItem it = bg_item(a, w);
+            const uint32_t buf = item & 1u;
+            if (!mbar_wait_bounded(&s_acc[buf], (item >> 1) & 1u)) {
+                if (lane == 0) fail();
+                break;
+            }
+            tmem_fence_after_sync();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + buf * (uint32_t)kBgN;
+            bg_epilogue<EPI>(a, it, 32 * warp + lane, taddr);
+            tmem_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[buf]);
+        }
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tmem_fence_after_sync();
+        tmem_dealloc(tmem, kBgTmemCols);
+    }
+}
+
+// Out[i] (i < n) = sum over p < parts, in order, of part[p * stride + i].
+__global__ void __launch_bounds__(256) sum_parts_kernel(const float* __restrict__ part, long long stride, int parts,
+                                                        long long n, float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int p = 0; p < parts; ++p) s += part[(size_t)p * stride + i];
+        out[i] = s;
+    }
+}
+
+// 2-D tensor map over a row-major [rows][cols] BF16 matrix, box {64, box_rows},
+// 128-byte swizzle (rows past the matrix and columns past cols read as zero).
+bool bg_map(CUtensorMap* map, const void* ptr, long long cols, long long rows, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBgK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int bg_sms() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    return (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;
+}
+
+template <int LAYOUT, int EPI>
+cudaError_t bg_launch(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(block_gemm_kernel<LAYOUT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBgSmem);
+    if (e != cudaSuccess) return e;
+    int grid = bg_sms();
+    if (grid > a.n_items) grid = a.n_items;
+    return launch_ex(block_gemm_kernel<LAYOUT, EPI>, (unsigned)grid, kBgThreads, kBgSmem, s, pdl, ta, tb, a);
+}
+
+}  // namespace
+
+int block_gemm_sms() {
+    const int n = bg_sms();
+    return n < kBlockSmsBound ? n : kBlockSmsBound;
+}
+
+int block_gemm_splits(int M, int N, long long K, int sms) {
+    const int tiles = (M / kBgM) * (N / kBgN);
+    if (tiles < 1) return 1;
+    int s = (sms + tiles - 1) / tiles;
+    const long long steps = (K + kBgK - 1) / kBgK;
+    if (s > kBlockGemmSplitsMax) s = kBlockGemmSplitsMax;
+    if (s > steps) s = (int)steps;
+    return s < 1 ? 1 : s;
+}
+
+cudaError_t launch_block_gemm(const BlockGemmArgs& args_in, const void* A, const void* Bm, cudaStream_t s, bool pdl) {
+    BlockGemmArgs a = args_in;
+    CUtensorMap ta, tb;
+    const long long M = a.M, N = a.N, K = a.K;
+    if (a.layout == kBgNT) {
+        // A [M][K]; B [N][K] (glu: [2F][K], tile columns pair rows f and F + f)
+        const long long brows = a.epi == kEpiGlu ? 2LL * a.F : N;
+        if (!bg_map(&ta, A, K, M, kBgM) || !bg_map(&tb, Bm, K, brows, kBgN / 2)) return cudaErrorInvalidValue;
+        a.n_tiles = a.epi == kEpiGlu ? (int)(N / (kBgN / 2)) : (int)(N / kBgN);
+        a.m_tiles = (int)((M + kBgM - 1) / kBgM);
+        a.splits = 1;
+        a.ksteps = (int)(K / kBgK);
+    } else if (a.layout == kBgNN) {
+        // A [M][K]; B = W [K][N]
+        if (!bg_map(&ta, A, K, M, kBgM) || !bg_map(&tb, Bm, N, K, 64)) return cudaErrorInvalidValue;
+        a.n_tiles = (int)(N / kBgN);
+        a.m_tiles = (int)((M + kBgM - 1) / kBgM);
+        a.splits = 1;
+        a.ksteps = (int)(K / kBgK);
+    } else {
+        // A = dy [K][M]; B = x [K][N]; K = tokens (a ragged last step reads zeros)
+        if (!bg_map(&ta, A, M, K, 64) || !bg_map(&tb, Bm, N, K, 64)) return cudaErrorInvalidValue;
+        a.n_tiles = (int)(N / kBgN);
+        a.m_tiles = (int)(M / kBgM);
+        a.ksteps = (int)((K + kBgK - 1) / kBgK);
+        if (a.splits < 1) a.splits = 1;
+    }
+    a.n_items = a.m_tiles * a.n_tiles * a.splits;
+    if (a.n_items < 1) return cudaSuccess;
+    switch (a.layout * 16 + a.epi) {
+        case kBgNT * 16 + kEpiStore: return bg_launch<kBgNT, kEpiStore>(ta, tb, a, s, pdl);
+        case kBgNT * 16 + kEpiResid: return bg_launch<kBgNT, kEpiResid>(ta, tb, a, s, pdl);
+        case kBgNT * 16 + kEpiGlu: return bg_launch<kBgNT, kEpiGlu>(ta, tb, a, s, pdl);
+        case kBgNN * 16 + kEpiStore: return bg_launch<kBgNN, kEpiStore>(ta, tb, a, s, pdl);
+        case kBgNN * 16 + kEpiGluBwd: return bg_launch<kBgNN, kEpiGluBwd>(ta, tb, a, s, pdl);
+        case kBgNN * 16 + kEpiJoinBwd: return bg_launch<kBgNN, kEpiJoinBwd>(ta, tb, a, s, pdl);
+        case kBgTN * 16 + kEpiF32: return bg_launch<kBgTN, kEpiF32>(ta, tb, a, s, pdl);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_sum_parts(const float* part, long long stride, int parts, long long n, float* out, cudaStream_t s,
+                             bool pdl) {
+    long long blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    return launch_ex(sum_parts_kernel, (unsigned)blocks, 256, 0, s, pdl, part, stride, parts, n, out);
+}
+
+}  // namespace lrs

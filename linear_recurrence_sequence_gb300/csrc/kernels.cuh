@@ -455,9 +455,6 @@ cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& t
                                   bool projected = false);
 cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,
                                cudaStream_t s);
-// Packed backward weights [16][6 dk][dk] (column-major dk x 6dk per block:
-// W_x, W_x, W_a, W_a transposed into (o, i), then two identity blocks) and
-// the combination dW_x = P0 + P1, dW_a = P2 + P3 of the [16][dk][4 dk] GEMM output.
 // The gate projections' contractions on the tensor cores (proj_gemm.cu):
 // operand images of W_x, W_a (logits) and of the packed Wcat (dx); the FP32
 // logits x W_q of both gates; dx from the gradient parts; dW_x, dW_a from the
@@ -471,5 +468,55 @@ cudaError_t launch_proj_dx(const void* gparts, const void* wc, void* dx, bool dx
 int proj_dw_splits(const ProjDims& d);
 cudaError_t launch_proj_dw(const void* gparts, const void* x, float* part, float* dw_x, float* dw_a, int D,
                            const ProjDims& d, uint32_t* status, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------------------
+// RecurrentBlock around the SAMU mixer (block_gemm.cu, block_elem.cu).
+// ---------------------------------------------------------------------------
+// Operand layouts of the dense contraction C(m, n) = sum_k A(m, k) B(n, k):
+//   NT: A [M][K], B [N][K] (forward, y = x W^T);
+//   NN: A [M][K], B [K][N] (dX, dx = dy W);
+//   TN: A [K][M], B [K][N] (dW = dy^T x, K = tokens, split into FP32 partials).
+enum BgLayoutKind { kBgNT = 0, kBgNN = 1, kBgTN = 2 };
+// Fused epilogues (see block_gemm.cu).
+enum BgEpiKind { kEpiStore = 0, kEpiResid = 1, kEpiGlu = 2, kEpiGluBwd = 3, kEpiJoinBwd = 4, kEpiF32 = 5 };
+constexpr int kBlockGemmSplitsMax = 16;
+constexpr int kBlockSmsBound = 256;   // SMs assumed when sizing the split partials (GB300: 152)
+
+struct BlockGemmArgs {
+    int layout, epi;
+    int M, N, K;                 // glu: N = F hidden units (the B rows f and F + f pair up)
+    int m_tiles, n_tiles, splits, ksteps, n_items;   // filled by launch_block_gemm (splits: TN only, in)
+    uint16_t* out;  int ldo;     // BF16 output (store, resid: C; glu: q; glu_bwd: [da | db]; join_bwd: dy_mixer)
+    const uint16_t* r; int ldr;  // resid: the residual added to C
+    uint16_t* out2; int ld2;     // glu: [a | b]; join_bwd: dg (the gate half of [dg | dv])
+    const uint16_t* e0; int lde0;   // glu_bwd: [a | b]; join_bwd: [g | v]
+    const uint16_t* e1; int lde1;   // join_bwd: y_mixer
+    int F;                       // glu, glu_bwd: offset of the b (db) half
+    float* part;                 // f32: [splits][M][N]
+    uint32_t* status;
+};
+
+// Token splits of a TN contraction of an M x N weight gradient over K tokens
+// on `sms` SMs (block_gemm_sms(): this device's, capped at kBlockSmsBound).
+int block_gemm_sms();
+int block_gemm_splits(int M, int N, long long K, int sms);
+cudaError_t launch_block_gemm(const BlockGemmArgs& a, const void* A, const void* B, cudaStream_t s, bool pdl);
+// out[i] = sum_{p < parts} part[p * stride + i] in order, i < n.
+cudaError_t launch_sum_parts(const float* part, long long stride, int parts, long long n, float* out, cudaStream_t s,
+                             bool pdl);
+int block_norm_bwd_ctas(long long rows);
+int block_conv_parts(int B, int L);
+cudaError_t launch_rmsnorm_fwd(const void* x, const float* gamma, void* h, float* rstd, long long rows, int W,
+                               uint32_t* status_clear, cudaStream_t s, bool pdl);
+cudaError_t launch_rmsnorm_bwd(const void* x, const float* gamma, const float* rstd, const void* dh, const void* dres,
+                               void* dx, float* dgamma_part, long long rows, int W, uint32_t* status_clear,
+                               cudaStream_t s, bool pdl);
+cudaError_t launch_conv_fwd(const void* gv, const float* k, const float* kb, const uint8_t* reset, void* u, int B,
+                            int L, int D, cudaStream_t s, bool pdl);
+cudaError_t launch_conv_bwd(const void* gv, const float* k, const uint8_t* reset, const void* dxs, const void* dwm,
+                            void* dgv, float* part, int B, int L, int D, uint32_t* status,
+                            const uint32_t* mixer_status, cudaStream_t s, bool pdl);
+cudaError_t launch_join_fwd(const void* gv, const void* ym, void* j, long long BL, int D, uint32_t* status,
+                            const uint32_t* mixer_status, cudaStream_t s, bool pdl);
 
 }  // namespace lrs

@@ -270,4 +270,64 @@ inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
     return s;
 }
 
+// ---------------------------------------------------------------------------
+// RecurrentBlock around the SAMU mixer: widths Dm (residual stream), D (the
+// mixer), F = 3 Dm (MLP hidden units).
+// ---------------------------------------------------------------------------
+constexpr int kBlockMlpRatio = 3;
+
+// Forward -> backward: the mixer's own saved buffer, then the block's BF16
+// activations and the two norms' FP32 reciprocal RMS per token.
+struct BlockSaved {
+    size_t mixer, h1, rstd1, gv, u, ym, j, r1, rstd2, h2, ab, q, total;
+};
+
+inline BlockSaved block_saved_layout(int B, int L, int Dm, int D) {
+    const size_t BL = (size_t)B * L, F = (size_t)kBlockMlpRatio * Dm;
+    BlockSaved s;
+    size_t o = 0;
+    s.mixer = o;  o = align_up(o + samu_saved_layout(B, L, D).total);
+    s.h1 = o;     o = align_up(o + BL * Dm * 2);
+    s.rstd1 = o;  o = align_up(o + BL * 4);
+    s.gv = o;     o = align_up(o + BL * 2 * D * 2);     // [g | v]
+    s.u = o;      o = align_up(o + BL * D * 2);
+    s.ym = o;     o = align_up(o + BL * D * 2);
+    s.j = o;      o = align_up(o + BL * D * 2);
+    s.r1 = o;     o = align_up(o + BL * Dm * 2);
+    s.rstd2 = o;  o = align_up(o + BL * 4);
+    s.h2 = o;     o = align_up(o + BL * Dm * 2);
+    s.ab = o;     o = align_up(o + BL * 2 * F * 2);     // [a | b]
+    s.q = o;      o = align_up(o + BL * F * 2);
+    s.total = o;
+    return s;
+}
+
+// Scratch: the block's status word, the mixer's scratch, the BF16 gradients
+// between layers, the weight-gradient split partials (shared by the four
+// weight contractions, one after another), the norm and convolution partials.
+struct BlockScratch {
+    size_t mixer, dab, dh2, dr1, dym, dgv, dxs, dwm, dh1, wpart, npart, cpart, total;
+};
+
+inline BlockScratch block_scratch_layout(int B, int L, int Dm, int D, size_t wpart_floats, size_t npart_floats,
+                                         size_t cpart_floats) {
+    const size_t BL = (size_t)B * L, F = (size_t)kBlockMlpRatio * Dm;
+    BlockScratch s;
+    size_t o = kAlign;   // [0, kAlign): the block's status word
+    s.mixer = o;  o = align_up(o + samu_scratch_layout(B, L, D).total);
+    s.dab = o;    o = align_up(o + BL * 2 * F * 2);
+    s.dh2 = o;    o = align_up(o + BL * Dm * 2);
+    s.dr1 = o;    o = align_up(o + BL * Dm * 2);
+    s.dym = o;    o = align_up(o + BL * D * 2);
+    s.dgv = o;    o = align_up(o + BL * 2 * D * 2);
+    s.dxs = o;    o = align_up(o + BL * D * 2);
+    s.dwm = o;    o = align_up(o + BL * D * 2);
+    s.dh1 = o;    o = align_up(o + BL * Dm * 2);
+    s.wpart = o;  o = align_up(o + wpart_floats * 4);
+    s.npart = o;  o = align_up(o + npart_floats * 4);
+    s.cpart = o;  o = align_up(o + cpart_floats * 4);
+    s.total = o;
+    return s;
+}
+
 }  // namespace lrs

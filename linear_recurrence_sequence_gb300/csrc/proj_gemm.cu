@@ -45,34 +45,6 @@ constexpr size_t kPgSmemBudget = 200 * 1024;
 
 enum { kModeLogit = 0, kModeDx = 1, kModeDw = 2 };
 
-// Shared-memory descriptor, MN-major with the 128-byte swizzle: rows of 128
-// bytes run along M (or N), eight consecutive rows are eight K values (one
-// 1024-byte atom); lbo = byte distance between successive 64-element M (or N)
-// chunks, the stride byte offset = 1024 between successive 8-row K groups.
-__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_addr, uint32_t lbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1u << 46;
-    d |= (uint64_t)2u << 61;
-    return d;
-}
-
-// kind::f16 instruction descriptor with both operands MN-major (the
-// transpose bits of A and B set).
-__host__ __device__ constexpr uint32_t umma_idesc_bf16_mn(int M, int N) {
-    return umma_idesc_bf16(M, N) | (1u << 15) | (1u << 16);
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 }  // namespace
 
 struct ProjGemmArgs {

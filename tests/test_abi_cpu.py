@@ -183,3 +183,43 @@ def test_noalloc_size_limit_is_checked_before_any_device_call(lib):
     assert lib.samu_forward_noalloc(*args, 1, 32768, 2560, p, None, p, None) == LRS_ERR_CUDA
     assert lib.samu_forward_noalloc(*args, 1, 131072, 1024, p, None, p, None) == LRS_ERR_TOO_LARGE
     assert lib.samu_status_string(LRS_ERR_TOO_LARGE) == lib.lrs_status_string(LRS_ERR_TOO_LARGE)
+
+
+def _block_ws(lib, B, L, Dm, D):
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    st = lib.samu_block_workspace_bytes(B, L, Dm, D, ctypes.byref(s), ctypes.byref(c))
+    return st, s.value, c.value
+
+
+@pytest.mark.parametrize("B,L,Dm,D,expect", [
+    (4, 4096, 1024, 1024, 0), (1, 8192, 2048, 2560, 0), (2, 100, 256, 256, 0), (1, 16, 4096, 256, 0),
+    (1, 16, 384, 256, 2), (1, 16, 256, 384, 2), (1, 16, 8192, 256, 2), (1, 16, 256, 4352, 2),
+    (0, 16, 256, 256, 1), (1, 16, 0, 256, 1), (1, 16, 256, 255, 1),
+])
+def test_block_shape_validation(lib, B, L, Dm, D, expect):
+    """Host-only: the block needs Dm and D multiples of 256 (the contraction
+    tiles' 256 columns), Dm <= 4096 and D within the mixer's limits; its saved
+    buffer holds the mixer's plus the BF16 activations of every layer."""
+    st, saved, scratch = _block_ws(lib, B, L, Dm, D)
+    assert st == expect
+    if st == 0:
+        mixer_saved = _ws(lib, "samu_workspace_bytes", B, L, D)[1]
+        F = 3 * Dm
+        # h1, r1, h2 (Dm each), [g|v] (2D), u, y, j (D each), [a|b] (2F), q (F): BF16
+        assert saved >= mixer_saved + B * L * 2 * (3 * Dm + 5 * D + 3 * F)
+        assert scratch > _ws(lib, "samu_workspace_bytes", B, L, D)[2]
+
+
+def test_block_entry_points_reject_null_pointers(lib):
+    """Host-only argument checks return LRS_ERR_ARG before any CUDA call."""
+    null = ctypes.c_void_p(0)
+    assert lib.samu_block_forward(null, null, null, null, 1, 16, 256, 256, null, null, null, null, null) == 1
+    assert lib.samu_block_backward(null, null, null, null, null, null, 1, 16, 256, 256, null, null, null, null,
+                                   null, null) == 1
+    assert lib.lrs_dense_gemm(0, null, null, null, 128, 256, 64, null, null) == 1
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) // 256 * 256)
+    assert lib.lrs_dense_gemm(3, p, p, p, 128, 256, 64, p, null) == 1          # unknown layout
+    assert lib.lrs_dense_gemm(0, p, p, p, 128, 192, 64, p, null) == 2          # N not a multiple of 256
+    assert lib.lrs_dense_gemm(2, p, p, p, 100, 256, 64, p, null) == 2          # TN: M not a multiple of 128

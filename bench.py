@@ -784,6 +784,110 @@ def sweep_decode(name, dev, K, W):
             "kernels_avg_ms": {"samu_decode_step_kernel": round(sum(kms) / max(1, len(kms)), 5)}}
 
 
+# One RecurrentBlock around the SAMU mixer (widths Dm, D, F = 3 Dm), F+B as a
+# CUDA graph after an L2 flush, like the mixer workloads.  The block is
+# dominated by its dense contractions: 18 B L Dm (D + F) flops per F+B (the
+# forward's 2 B L Dm (3 D + 3 F), and the same again for dX and for dW), so the
+# roofline line is the contraction kernel's achieved TFLOP/s (all its launches
+# of a step, eager events) against the measured BF16 tensor-core peak.
+# Shapes: the mixer's short shape (B4 L4K, both widths 1024); the pages'
+# 400M-width block (Dm 1024, recurrent width D 1536) at their ablation batch
+# B4 L2K; the 1.3B widths (Dm 2048, D 2560) at the mixer's medium length.
+BLOCK_WORKLOADS = {"block_short": (4, 4096, 1024, 1024), "block_400m": (4, 2048, 1024, 1536),
+                   "block_medium": (1, 8192, 2048, 2560)}
+MIXER_KERNELS = ("samu_ctrl_fwd_kernel", "samu_fwd_maps_kernel", "samu_fwd_replay_kernel", "samu_bwd_maps_kernel",
+                 "samu_bwd_main_kernel", "samu_ctrl_bwd_kernel", "samu_params_kernel")
+
+
+def block_step(B, L, Dm, D, dev, seed=0):
+    """One block forward+backward through the C ABI on resident inputs and
+    preallocated outputs; returns (step, scratch_fwd, scratch_bwd)."""
+    import torch
+    from linear_recurrence_sequence_gb300 import api, synth
+    inp = synth.block_inputs(B, L, Dm, D, seed, h0=False, reset_p=0.0)
+    t = api.block_tensors_from_numpy(inp, dev)
+    nsaved, nscratch = api.samu_block_workspace_bytes(B, L, Dm, D)
+    saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    M = D // 2
+    fo = {"out": torch.empty((B, L, Dm), dtype=torch.bfloat16, device=dev),
+          "hT": torch.empty((B, M, 2), dtype=torch.float32, device=dev)}
+    go = None
+
+    def step():
+        nonlocal go
+        api.samu_block_forward(t["x"], t["params"], t["h0"], t["reset"], out=fo, saved=saved, scratch=scratch)
+        go = api.samu_block_backward(t["dout"], t["dhT"], t["x"], t["params"], t["h0"], t["reset"], saved,
+                                     out=go, scratch=scratch)
+
+    return step, scratch
+
+
+def sweep_block(name, dev, K, W):
+    import torch
+    from linear_recurrence_sequence_gb300 import api
+    B, L, Dm, D = BLOCK_WORKLOADS[name]
+    F = 3 * Dm
+    step, scratch = block_step(B, L, Dm, D, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(cs)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        step()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record()
+        graph.replay()
+        ev1[i].record()
+    torch.cuda.synchronize(dev)
+    if api.device_status(scratch) != 0:
+        raise RuntimeError(f"device-side wait timed out ({name})")
+    ms = sorted(ev0[i].elapsed_time(ev1[i]) for i in range(K))
+    ms_mean = sum(ms) / K
+    KP = max(3, min(K, 10))
+    cap = KP * 64
+    api.profile_begin(cap)
+    for _ in range(KP):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    records, n = api.profile_end(cap)
+    per = {}
+    for kname, kms in records:
+        per[kname] = per.get(kname, 0.0) + kms / KP    # per step: all launches of the kernel
+    flops = 18.0 * B * L * Dm * (D + F)
+    gemm_ms = per.get("block_gemm_kernel", float("nan"))
+    tflops = flops / (gemm_ms / 1e3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak, peak_src = float(pk["bf16_tflops"]), "measured (bf16_tflops, burst)"
+    except Exception:
+        peak, peak_src = 1900.0, "fallback"
+    mixer_ms = sum(per.get(k, 0.0) for k in MIXER_KERNELS)
+    eager_ms = sum(per.values())
+    return {"workload": name, "kind": "samu_block", "B": B, "L": L, "Dm": Dm, "D": D, "F": F, "steps": K,
+            "ms_per_step": round(ms_mean, 5), "ms_min": round(ms[0], 5), "ms_max": round(ms[-1], 5),
+            "Mtok_per_s": round(B * L / (ms_mean / 1e3) / 1e6, 3),
+            "roofline": {"bound": "tensor", "kernel": "block_gemm_kernel", "flops_per_step": flops,
+                         "kernel_ms_per_step": round(gemm_ms, 5), "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "peak_source": peak_src},
+            "mixer_share_of_eager_step": round(mixer_ms / eager_ms, 4) if eager_ms > 0 else None,
+            "launches_per_step": n // KP,
+            "kernels_ms_per_step": {k: round(v, 5) for k, v in sorted(per.items())}}
+
+
 # ---------------------------------------------------------------------------
 # --compare-pages: SAMU vs RG-LRU with its 16-block gate projections, F+B, on
 # the pages' comparison shapes, timed the pages' way: two rounds (RG-LRU
@@ -855,9 +959,15 @@ def run_sweep(args, local):
     torch.cuda.set_device(dev)
     K = max(5, min(args.steps, 50))
     W = max(3, args.warmup)
-    names = args.only.split(",") if args.only else list(synth.WORKLOADS) + list(DECODE_WORKLOADS)
+    names = (args.only.split(",") if args.only
+             else list(synth.WORKLOADS) + list(DECODE_WORKLOADS) + list(BLOCK_WORKLOADS))
     for name in names:
-        line = sweep_decode(name, dev, K, W) if name in DECODE_WORKLOADS else sweep_one(name, dev, K, W, args.transition)
+        if name in DECODE_WORKLOADS:
+            line = sweep_decode(name, dev, K, W)
+        elif name in BLOCK_WORKLOADS:
+            line = sweep_block(name, dev, K, W)
+        else:
+            line = sweep_one(name, dev, K, W, args.transition)
         print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
 

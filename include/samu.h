@@ -106,8 +106,9 @@ int lrs_selftest_wait_timeout(void* scratch, cudaStream_t stream);
  * 10 SAMU forward maps, 11 SAMU backward maps, 12 SAMU decode prepare,
  * 13 SAMU decode step, 14 RG-LRU gate-projection GEMMs, 15 RG-LRU projection
  * backward GEMMs, 16 RG-LRU weight packing and dW combination, 17 RecurrentBlock
- * contractions, 18 RecurrentBlock norms, convolution, join and fixed-order
- * gradient sums; 9 also covers the bias-gradient reductions) and duration in
+ * contractions, 18 RecurrentBlock RMSNorm (forward and backward), 19 its
+ * convolution, 20 its join, 21 its fixed-order gradient sums; 9 also covers
+ * the bias-gradient reductions) and duration in
  * milliseconds; *count receives the number of
  * kernels launched while profiling was on.  Not thread-safe: one profiling
  * session per process.  Errors: LRS_ERR_ARG (capacity < 1 or count NULL),

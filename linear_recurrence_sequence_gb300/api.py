@@ -607,7 +607,8 @@ KERNEL_NAMES = {
     7: "rglru_scan_fwd_kernel", 8: "rglru_scan_bwd_kernel", 9: "rglru_alpha_kernels",
     10: "samu_fwd_maps_kernel", 11: "samu_bwd_maps_kernel", 12: "samu_decode_prepare_kernel",
     13: "samu_decode_step_kernel", 14: "proj_gemm_kernel<logits>", 15: "proj_gemm_kernel<dx, dW>",
-    16: "proj_pack_kernel", 17: "block_gemm_kernel", 18: "block_elementwise_kernels",
+    16: "proj_pack_kernel", 17: "block_gemm_kernel", 18: "rmsnorm_kernels", 19: "conv_kernels",
+    20: "join_fwd_kernel", 21: "sum_parts_kernel",
 }
 
 

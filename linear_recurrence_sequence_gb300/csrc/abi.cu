@@ -79,7 +79,7 @@ enum {
     KID_SAMU_CTRL_FWD = 2, KID_SAMU_SCAN_FWD, KID_SAMU_SCAN_BWD, KID_SAMU_CTRL_BWD,
     KID_SAMU_PARAMS, KID_RGLRU_SCAN_FWD, KID_RGLRU_SCAN_BWD, KID_RGLRU_ALPHA, KID_SAMU_FWD_MAPS,
     KID_SAMU_BWD_MAPS, KID_SAMU_DECODE_PREP, KID_SAMU_DECODE_STEP, KID_RGLRU_PROJ_FWD, KID_RGLRU_PROJ_BWD,
-    KID_RGLRU_PROJ_PACK, KID_BLOCK_GEMM, KID_BLOCK_ELEM
+    KID_RGLRU_PROJ_PACK, KID_BLOCK_GEMM, KID_BLOCK_NORM, KID_BLOCK_CONV, KID_BLOCK_JOIN, KID_BLOCK_SUM
 };
 
 #define LRS_LAUNCH(id, stream, expr)            \
@@ -727,7 +727,7 @@ int block_weight_grad(const void* A, const void* Bm, int M, int N, long long BL,
     g.part = g.splits > 1 ? wpart : dw;
     LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, A, Bm, stream, pdl_ok()));
     if (g.splits > 1)
-        LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+        LRS_LAUNCH(KID_BLOCK_SUM, stream,
                    launch_sum_parts(wpart, (long long)M * N, g.splits, (long long)M * N, dw, stream, pdl_ok()));
     return LRS_OK;
 }
@@ -771,19 +771,19 @@ int samu_block_forward(const samu_block_params* p, const void* x, const float* h
     void* q = at<void>(saved, sv.q);
 
     // h1 = RMSNorm(x); [g | v] = h1 w_in^T; u = conv(v)
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_rmsnorm_fwd(x, p->gamma1, h1, rstd1, BL, Dm, status, stream, false));
+    LRS_LAUNCH(KID_BLOCK_NORM, stream, launch_rmsnorm_fwd(x, p->gamma1, h1, rstd1, BL, Dm, status, stream, false));
     BlockGemmArgs g = gemm_args(kBgNT, kEpiStore, (int)BL, 2 * D, Dm, status);
     g.out = static_cast<uint16_t*>(gv);
     g.ldo = 2 * D;
     LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h1, p->w_in, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+    LRS_LAUNCH(KID_BLOCK_CONV, stream,
                launch_conv_fwd(gv, p->conv_k, p->conv_b, reset, u, B, L, D, stream, pdl_ok()));
     // the mixer on x_sel = w = u
     const int st = samu_forward(u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L, D, ym,
                                 nullptr, hT, msaved, mscratch, stream);
     if (st != LRS_OK) return st;
     // j = GeLU(g) y_mix; r1 = x + j w_o^T
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_join_fwd(gv, ym, j, BL, D, status, mstatus, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_JOIN, stream, launch_join_fwd(gv, ym, j, BL, D, status, mstatus, stream, pdl_ok()));
     g = gemm_args(kBgNT, kEpiResid, (int)BL, Dm, D, status);
     g.out = static_cast<uint16_t*>(r1);
     g.ldo = Dm;
@@ -791,7 +791,7 @@ int samu_block_forward(const samu_block_params* p, const void* x, const float* h
     g.ldr = Dm;
     LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, j, p->w_o, stream, pdl_ok()));
     // h2 = RMSNorm(r1); [a | b] = h2 w_mlp_in^T, q = GeLU(a) b; out = r1 + q w_mlp_out^T
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_rmsnorm_fwd(r1, p->gamma2, h2, rstd2, BL, Dm, nullptr, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_NORM, stream, launch_rmsnorm_fwd(r1, p->gamma2, h2, rstd2, BL, Dm, nullptr, stream, pdl_ok()));
     g = gemm_args(kBgNT, kEpiGlu, (int)BL, F, Dm, status);
     g.out = static_cast<uint16_t*>(q);
     g.ldo = F;
@@ -866,9 +866,9 @@ int samu_block_backward(const samu_block_params* p, const void* x, const float* 
     LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dab, p->w_mlp_in, stream, pdl_ok()));
     if ((st = block_weight_grad(dab, h2, 2 * F, Dm, BL, gr->dw_mlp_in, wpart, status, stream)) != LRS_OK) return st;
     // dr1 = dout + RMSNorm'(dh2)
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+    LRS_LAUNCH(KID_BLOCK_NORM, stream,
                launch_rmsnorm_bwd(r1, p->gamma2, rstd2, dh2, dout, dr1, npart, BL, Dm, nullptr, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma2, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_SUM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma2, stream, pdl_ok()));
     // join: dj = dr1 w_o -> dy_mix, dg; dW_o = dr1^T j
     g = gemm_args(kBgNN, kEpiJoinBwd, (int)BL, D, Dm, status);
     g.out = static_cast<uint16_t*>(dym);
@@ -888,12 +888,12 @@ int samu_block_backward(const samu_block_params* p, const void* x, const float* 
     if (st != LRS_OK) return st;
     // convolution: dv (the recurrent half of [dg | dv]), dconv_k, dconv_b
     const int cparts = block_conv_parts(B, L);
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+    LRS_LAUNCH(KID_BLOCK_CONV, stream,
                launch_conv_bwd(gv, p->conv_k, reset, dxs, dwm, dgv, cpart, B, L, D, status, mstatus, stream,
                                pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+    LRS_LAUNCH(KID_BLOCK_SUM, stream,
                launch_sum_parts(cpart, 5LL * D, cparts, 4LL * D, gr->dconv_k, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+    LRS_LAUNCH(KID_BLOCK_SUM, stream,
                launch_sum_parts(cpart + 4 * (size_t)D, 5LL * D, cparts, D, gr->dconv_b, stream, pdl_ok()));
     // dh1 = [dg | dv] w_in; dW_in = [dg | dv]^T h1
     g = gemm_args(kBgNN, kEpiStore, (int)BL, Dm, 2 * D, status);
@@ -902,9 +902,9 @@ int samu_block_backward(const samu_block_params* p, const void* x, const float* 
     LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dgv, p->w_in, stream, pdl_ok()));
     if ((st = block_weight_grad(dgv, h1, 2 * D, Dm, BL, gr->dw_in, wpart, status, stream)) != LRS_OK) return st;
     // dx = dr1 + RMSNorm'(dh1)
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream,
+    LRS_LAUNCH(KID_BLOCK_NORM, stream,
                launch_rmsnorm_bwd(x, p->gamma1, rstd1, dh1, dr1, dx, npart, BL, Dm, nullptr, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_ELEM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma1, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_SUM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma1, stream, pdl_ok()));
     return LRS_OK;
 }
 

@@ -8,20 +8,13 @@
 // are multiples of 256, so a thread works on 8 consecutive channels (one
 // 16-byte load).
 #include "kernels.cuh"
+#include "block_math.cuh"
 
 namespace lrs {
 
 namespace {
 
 constexpr float kNormEps = 1e-6f;
-constexpr float kGeluC = 0.7978845608028654f;   // sqrt(2 / pi)
-constexpr float kGeluA = 0.044715f;
-
-__device__ __forceinline__ float gelu_fwd(float x) {
-    const float u = kGeluC * (x + kGeluA * x * x * x);
-    return 0.5f * x * (1.f + tanhf(u));
-}
-
 __device__ __forceinline__ void unpack8(const uint4 q, float (&v)[8]) {
     float2 f;
     f = bf2_to_f2(q.x); v[0] = f.x; v[1] = f.y;
@@ -162,137 +155,282 @@ __global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(const uint4* __restric
     dp[1] = make_float4(dg[4], dg[5], dg[6], dg[7]);
 }
 
-// Causal depthwise convolution of width 4 (reading): u[t] = kb + sum_{j<4}
-// k[j] v[t - j] over the taps that stay inside t's segment (a reset at t' > t
-// - j, t' <= t cuts the taps before it; t = 0 starts every row).  v is the
-// recurrent half (columns D .. 2D - 1) of the input projection's [B L][2 D]
-// output.  One thread per (token, 8 channels).
-__global__ void __launch_bounds__(256) conv_fwd_kernel(const uint16_t* __restrict__ gv, const float* __restrict__ k,
-                                                       const float* __restrict__ kb, const uint8_t* __restrict__ reset,
-                                                       uint4* __restrict__ u, int B, int L, int D) {
+// The same for W <= 1024 (more channels per lane would spill), one warp per row: lane l owns the 8-channel groups
+// l + 32 k (k < NK = W / 256) and keeps the row's x, dh and dres in registers
+// (3 NK independent 16-byte loads), the row mean is a warp sum, dgamma
+// accumulates per lane over the warp's rows.  The CTA's 8192 / W warps share
+// its contiguous row range; their dgamma rows are added in warp order through
+// shared memory into the CTA's partial row.
+template <int NK>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_warp_kernel(const uint4* __restrict__ x,
+                                                               const float* __restrict__ gamma,
+                                                               const float* __restrict__ rstd,
+                                                               const uint4* __restrict__ dh,
+                                                               const uint4* __restrict__ dres, uint4* __restrict__ dx,
+                                                               float* __restrict__ dgamma_part, long long rows) {
+    constexpr int W = 256 * NK, nv = W / 8, WPC = 8192 / W > 8 ? 8 : 8192 / W;
+    __shared__ float red[WPC][W];
     pdl_trigger();
     pdl_wait();
-    const int nv = D / 8;
-    const long long n = (long long)B * L * nv;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
-        const int v = (int)(e % nv);
-        const long long bt = e / nv;
-        const int t = (int)(bt % L);
-        float acc[8];
-        {
-            const float4 b0 = __ldg(reinterpret_cast<const float4*>(kb) + 2 * v);
-            const float4 b1 = __ldg(reinterpret_cast<const float4*>(kb) + 2 * v + 1);
-            acc[0] = b0.x; acc[1] = b0.y; acc[2] = b0.z; acc[3] = b0.w;
-            acc[4] = b1.x; acc[5] = b1.y; acc[6] = b1.z; acc[7] = b1.w;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long r0 = rows * blockIdx.x / gridDim.x, r1 = rows * (blockIdx.x + 1) / gridDim.x;
+    float gm[NK][8], dg[NK][8];
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+        const int v = lane + 32 * k;
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v);
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v + 1);
+        gm[k][0] = g0.x; gm[k][1] = g0.y; gm[k][2] = g0.z; gm[k][3] = g0.w;
+        gm[k][4] = g1.x; gm[k][5] = g1.y; gm[k][6] = g1.z; gm[k][7] = g1.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dg[k][i] = 0.f;
+    }
+    for (long long row = r0 + warp; row < r1; row += WPC) {
+        uint4 qx[NK], qh[NK], qr[NK];
+#pragma unroll
+        for (int k = 0; k < NK; ++k) {
+            const size_t o = (size_t)row * nv + lane + 32 * k;
+            qx[k] = __ldg(x + o);
+            qh[k] = __ldg(dh + o);
+            qr[k] = __ldg(dres + o);
         }
-        bool live = true;   // tap j still inside t's segment
+        const float rs = __ldg(rstd + row);
+        float part = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j > 0) live = live && t - j >= 0 && !(reset != nullptr && reset[bt - j + 1]);
-            if (live) {
-                float f[8];
-                unpack8(__ldg(reinterpret_cast<const uint4*>(gv + (size_t)(bt - j) * 2 * D + D) + v), f);
-                const float4 k0 = __ldg(reinterpret_cast<const float4*>(k + (size_t)j * D) + 2 * v);
-                const float4 k1 = __ldg(reinterpret_cast<const float4*>(k + (size_t)j * D) + 2 * v + 1);
-                const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        for (int k = 0; k < NK; ++k) {
+            float xv[8], hv[8];
+            unpack8(qx[k], xv);
+            unpack8(qh[k], hv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(kk[i], f[i], acc[i]);
+            for (int i = 0; i < 8; ++i) {
+                const float n = xv[i] * rs;
+                part = fmaf(hv[i] * gm[k][i], n, part);
+                dg[k][i] = fmaf(hv[i], n, dg[k][i]);
             }
         }
-        u[(size_t)bt * nv + v] = pack8(acc);
+        const float mean = warp_sum(part) / (float)W;
+#pragma unroll
+        for (int k = 0; k < NK; ++k) {
+            float xv[8], hv[8], rv[8], o[8];
+            unpack8(qx[k], xv);
+            unpack8(qh[k], hv);
+            unpack8(qr[k], rv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float n = xv[i] * rs;
+                o[i] = rv[i] + rs * (hv[i] * gm[k][i] - n * mean);
+            }
+            dx[(size_t)row * nv + lane + 32 * k] = pack8(o);
+        }
+    }
+    if (warp < WPC) {
+#pragma unroll
+        for (int k = 0; k < NK; ++k)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) red[warp][8 * (lane + 32 * k) + i] = dg[k][i];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < W; c += blockDim.x) {
+        float sum = 0.f;
+        for (int w = 0; w < WPC; ++w) sum += red[w][c];
+        dgamma_part[(size_t)blockIdx.x * W + c] = sum;
+    }
+}
+
+// Causal depthwise convolution of width 4 (reading): u[t] = kb + sum_{j<4}
+// k[j] v[t - j] over the taps that stay inside t's segment (a segment start
+// at t - j + 1 .. t cuts tap j; t = 0 starts every row).  v is the recurrent
+// half (columns D .. 2D - 1) of the input projection's [B L][2 D] output.
+// Thread: 4 channels of kConvRun consecutive tokens; it loads every row its
+// window needs first (kConvRun + 3 independent 8-byte loads), then forms the
+// outputs.  A warp covers 128 channels of one run (256 contiguous bytes per
+// row).
+constexpr int kConvRun = 16;
+
+__device__ __forceinline__ void unpack4(const uint2 q, float (&v)[4]) {
+    float2 f;
+    f = bf2_to_f2(q.x); v[0] = f.x; v[1] = f.y;
+    f = bf2_to_f2(q.y); v[2] = f.x; v[3] = f.y;
+}
+__device__ __forceinline__ uint2 pack4(const float (&v)[4]) {
+    uint2 q;
+    q.x = f2_to_bf2(v[0], v[1]);
+    q.y = f2_to_bf2(v[2], v[3]);
+    return q;
+}
+__device__ __forceinline__ void load_k4(const float* __restrict__ k, const float* __restrict__ kb, int D, int q,
+                                        float (&kk)[4][4], float (&bb)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float4 kv = __ldg(reinterpret_cast<const float4*>(k + (size_t)j * D) + q);
+        kk[j][0] = kv.x; kk[j][1] = kv.y; kk[j][2] = kv.z; kk[j][3] = kv.w;
+    }
+    if (kb != nullptr) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(kb) + q);
+        bb[0] = b.x; bb[1] = b.y; bb[2] = b.z; bb[3] = b.w;
+    }
+}
+
+__global__ void __launch_bounds__(256) conv_fwd_kernel(const uint16_t* __restrict__ gv, const float* __restrict__ k,
+                                                       const float* __restrict__ kb, const uint8_t* __restrict__ reset,
+                                                       uint16_t* __restrict__ u, int B, int L, int D) {
+    pdl_trigger();
+    pdl_wait();
+    const int nq = D / 4;
+    const int runs = (L + kConvRun - 1) / kConvRun;
+    const long long n = (long long)B * runs * nq;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+        const int q = (int)(e % nq);
+        const long long br = e / nq;
+        const int b = (int)(br / runs), t0 = (int)(br % runs) * kConvRun;
+        const size_t row0 = (size_t)b * L;
+        uint2 rows[kConvRun + 3];   // v[t0 - 3 + i]
+#pragma unroll
+        for (int i = 0; i < kConvRun + 3; ++i) {
+            const int t = t0 - 3 + i;
+            rows[i] = (t >= 0 && t < L) ? __ldg(reinterpret_cast<const uint2*>(gv + (row0 + t) * 2 * D + D) + q)
+                                        : make_uint2(0u, 0u);
+        }
+        float kk[4][4], bb[4];
+        load_k4(k, kb, D, q, kk, bb);
+        // st[i]: a segment starts at t0 - 3 + i
+        bool st[kConvRun + 3];
+#pragma unroll
+        for (int i = 0; i < kConvRun + 3; ++i) {
+            const int t = t0 - 3 + i;
+            st[i] = t >= 0 && t < L && reset != nullptr && reset[row0 + t] != 0;
+        }
+#pragma unroll
+        for (int r = 0; r < kConvRun; ++r) {
+            const int t = t0 + r;
+            if (t >= L) break;
+            float acc[4] = {bb[0], bb[1], bb[2], bb[3]};
+            bool live = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j > 0) live = live && t - j >= 0 && !st[r + 3 - j + 1];
+                if (live) {
+                    float f[4];
+                    unpack4(rows[r + 3 - j], f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(kk[j][i], f[i], acc[i]);
+                }
+            }
+            *reinterpret_cast<uint2*>(u + (row0 + t) * D + 4 * q) = pack4(acc);
+        }
     }
 }
 
 // Adjoint of conv_fwd_kernel with du = dx_sel + dw (the mixer reads x_sel =
 // w = u, so both gradients reach u):
-//   dv[t] = sum_j k[j] du[t + j] over the taps of t + j that reach t,
-//   dk[j] += du[t] v[t - j], dkb += du[t] (per-chunk partials, reduced in a
-//   fixed order by sum_parts).
-// Thread: 8 channels of one chunk of kConvChunk tokens of one row.  The
-// mixer's status word is OR-ed into the block's (thread 0 of CTA 0).
-constexpr int kConvChunk = 64;
+//   dv[t] = sum_j k[j] du[t + j] over the outputs t + j whose tap j reaches t
+//           (no segment start at t + 1 .. t + j),
+//   dk[j] += du[t] v[t - j] over t's live taps, dkb += du[t].
+// CTA: a tile of kConvTile = 4 kConvRun tokens of one row and 256 channels;
+// thread (run r, channel group g): channels 4 g .. 4 g + 3 of the span and
+// the run's tokens, with every row it needs loaded first (du rows t .. t + 3
+// and v rows t - 3 .. t of the run: 2 (kConvRun + 3) independent 8-byte
+// loads).  The k and bias contributions of the four runs are added in run
+// order through shared memory: one partial row per tile, reduced in a fixed
+// order by sum_parts.  The mixer's status word is OR-ed into the block's
+// (thread 0 of CTA 0).
+constexpr int kConvTile = 4 * kConvRun;
+
 __global__ void __launch_bounds__(256) conv_bwd_kernel(const uint16_t* __restrict__ gv, const float* __restrict__ k,
                                                        const uint8_t* __restrict__ reset,
                                                        const uint16_t* __restrict__ dxs, const uint16_t* __restrict__ dwm,
                                                        uint16_t* __restrict__ dgv, float* __restrict__ part, int B,
                                                        int L, int D, uint32_t* status, const uint32_t* mixer_status) {
+    __shared__ float red[4][5][256];
     pdl_trigger();
     pdl_wait();
-    if (blockIdx.x == 0 && threadIdx.x == 0 && mixer_status != nullptr) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && mixer_status != nullptr) {
         const uint32_t m = *mixer_status;
         if (m != 0u) atomicOr(status, m);
     }
-    const int nv = D / 8;
-    const int chunks = (L + kConvChunk - 1) / kConvChunk;
-    const long long n = (long long)B * chunks * nv;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
-        const int v = (int)(e % nv);
-        const long long bc = e / nv;   // row b, chunk c: partial slot
-        const int c = (int)(bc % chunks);
-        const int b = (int)(bc / chunks);
-        float kk[4][8];
+    const int g = threadIdx.x & 63, run = threadIdx.x >> 6;
+    const int tiles = (L + kConvTile - 1) / kConvTile;
+    const int b = blockIdx.x / tiles, tile = blockIdx.x % tiles;
+    const int q = blockIdx.y * 64 + g;   // channels 4 q .. 4 q + 3
+    const int t0 = tile * kConvTile + run * kConvRun;
+    const size_t row0 = (size_t)b * L;
+    float du[kConvRun + 3][4];   // du[t0 + i]
+    uint2 vr[kConvRun + 3];      // v[t0 - 3 + i]
+    {
+        uint2 ra[kConvRun + 3], rw[kConvRun + 3];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 k0 = __ldg(reinterpret_cast<const float4*>(k + (size_t)j * D) + 2 * v);
-            const float4 k1 = __ldg(reinterpret_cast<const float4*>(k + (size_t)j * D) + 2 * v + 1);
-            kk[j][0] = k0.x; kk[j][1] = k0.y; kk[j][2] = k0.z; kk[j][3] = k0.w;
-            kk[j][4] = k1.x; kk[j][5] = k1.y; kk[j][6] = k1.z; kk[j][7] = k1.w;
+        for (int i = 0; i < kConvRun + 3; ++i) {
+            const int t = t0 + i;
+            const bool ok = t < L;
+            ra[i] = ok ? __ldg(reinterpret_cast<const uint2*>(dxs + (row0 + t) * D) + q) : make_uint2(0u, 0u);
+            rw[i] = ok ? __ldg(reinterpret_cast<const uint2*>(dwm + (row0 + t) * D) + q) : make_uint2(0u, 0u);
+            const int tv = t0 - 3 + i;
+            vr[i] = (tv >= 0 && tv < L) ? __ldg(reinterpret_cast<const uint2*>(gv + (row0 + tv) * 2 * D + D) + q)
+                                        : make_uint2(0u, 0u);
         }
-        float dk[5][8];
 #pragma unroll
-        for (int j = 0; j < 5; ++j)
+        for (int i = 0; i < kConvRun + 3; ++i) {
+            float a[4], w[4];
+            unpack4(ra[i], a);
+            unpack4(rw[i], w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dk[j][i] = 0.f;
-        const int t0 = c * kConvChunk, t1 = min(L, t0 + kConvChunk);
-        const size_t row0 = (size_t)b * L;
-        auto du_at = [&](int t, float (&o)[8]) {
-            float a[8], w[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(dxs + (row0 + t) * D) + v), a);
-            unpack8(__ldg(reinterpret_cast<const uint4*>(dwm + (row0 + t) * D) + v), w);
+            for (int c = 0; c < 4; ++c) du[i][c] = a[c] + w[c];
+        }
+    }
+    float kk[4][4], unused[4];
+    load_k4(k, nullptr, D, q, kk, unused);
+    // st[i]: a segment starts at t0 - 3 + i (i < kConvRun + 6)
+    bool st[kConvRun + 6];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = a[i] + w[i];
-        };
-        for (int t = t0; t < t1; ++t) {
-            float dut[8];
-            du_at(t, dut);
-            // parameter partials: du[t] v[t - j] over t's live taps
-            bool live = true;
+    for (int i = 0; i < kConvRun + 6; ++i) {
+        const int t = t0 - 3 + i;
+        st[i] = t >= 0 && t < L && reset != nullptr && reset[row0 + t] != 0;
+    }
+    float c[5][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j > 0) live = live && t - j >= 0 && !(reset != nullptr && reset[row0 + t - j + 1]);
-                if (live) {
-                    float f[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(gv + (row0 + t - j) * 2 * D + D) + v), f);
+    for (int j = 0; j < 5; ++j)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) dk[j][i] = fmaf(dut[i], f[i], dk[j][i]);
-                }
-            }
+        for (int i = 0; i < 4; ++i) c[j][i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dk[4][i] += dut[i];
-            // dv[t] = sum_j k[j] du[t + j] over the outputs t + j whose tap j reaches t
-            float acc[8];
+    for (int r = 0; r < kConvRun; ++r) {
+        const int t = t0 + r;
+        if (t < L) {
+            float acc[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = kk[0][i] * dut[i];
+            for (int i = 0; i < 4; ++i) acc[i] = kk[0][i] * du[r][i];
             bool reach = true;
 #pragma unroll
             for (int j = 1; j < 4; ++j) {
-                reach = reach && t + j < L && !(reset != nullptr && reset[row0 + t + j]);
-                if (reach) {
-                    float d2[8];
-                    du_at(t + j, d2);
+                reach = reach && t + j < L && !st[r + 3 + j];
+                if (reach)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(kk[j][i], d2[i], acc[i]);
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(kk[j][i], du[r + j][i], acc[i]);
+            }
+            *reinterpret_cast<uint2*>(dgv + (row0 + t) * 2 * D + D + 4 * q) = pack4(acc);
+            bool live = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j > 0) live = live && t - j >= 0 && !st[r + 3 - j + 1];
+                if (live) {
+                    float f[4];
+                    unpack4(vr[r + 3 - j], f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c[j][i] = fmaf(du[r][i], f[i], c[j][i]);
                 }
             }
-            *reinterpret_cast<uint4*>(dgv + (row0 + t) * 2 * D + D + 8 * v) = pack8(acc);
-        }
-        float* p = part + (size_t)bc * 5 * D;
 #pragma unroll
-        for (int j = 0; j < 5; ++j) {
-            float4* q = reinterpret_cast<float4*>(p + (size_t)j * D + 8 * v);
-            q[0] = make_float4(dk[j][0], dk[j][1], dk[j][2], dk[j][3]);
-            q[1] = make_float4(dk[j][4], dk[j][5], dk[j][6], dk[j][7]);
+            for (int i = 0; i < 4; ++i) c[4][i] += du[r][i];
         }
+    }
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[run][j][4 * g + i] = c[j][i];
+    __syncthreads();
+    float* p = part + (size_t)blockIdx.x * 5 * D + (size_t)blockIdx.y * 256;
+    for (int e = threadIdx.x; e < 5 * 256; e += blockDim.x) {
+        const int j = e / 256, ch = e % 256;
+        p[(size_t)j * D + ch] = ((red[0][j][ch] + red[1][j][ch]) + red[2][j][ch]) + red[3][j][ch];
     }
 }
 
@@ -331,12 +469,12 @@ unsigned grid_for(long long n, int threads) {
 }  // namespace
 
 int block_norm_bwd_ctas(long long rows) {
-    long long c = 2LL * 152;
+    long long c = 8LL * 152;
     if (c > rows) c = rows;
     return (int)(c < 1 ? 1 : c);
 }
 
-int block_conv_parts(int B, int L) { return B * ((L + kConvChunk - 1) / kConvChunk); }
+int block_conv_parts(int B, int L) { return B * ((L + kConvTile - 1) / kConvTile); }
 
 cudaError_t launch_rmsnorm_fwd(const void* x, const float* gamma, void* h, float* rstd, long long rows, int W,
                                uint32_t* status_clear, cudaStream_t s, bool pdl) {
@@ -347,24 +485,41 @@ cudaError_t launch_rmsnorm_fwd(const void* x, const float* gamma, void* h, float
 cudaError_t launch_rmsnorm_bwd(const void* x, const float* gamma, const float* rstd, const void* dh, const void* dres,
                                void* dx, float* dgamma_part, long long rows, int W, uint32_t* status_clear,
                                cudaStream_t s, bool pdl) {
-    return launch_ex(rmsnorm_bwd_kernel, (unsigned)block_norm_bwd_ctas(rows), (unsigned)(W / 8), 0, s, pdl,
-                     static_cast<const uint4*>(x), gamma, rstd, static_cast<const uint4*>(dh),
-                     static_cast<const uint4*>(dres), static_cast<uint4*>(dx), dgamma_part, rows, W, status_clear);
+    const unsigned ctas = (unsigned)block_norm_bwd_ctas(rows);
+    const uint4* xx = static_cast<const uint4*>(x);
+    const uint4* hh = static_cast<const uint4*>(dh);
+    const uint4* rr = static_cast<const uint4*>(dres);
+    uint4* oo = static_cast<uint4*>(dx);
+    if (status_clear == nullptr && W <= 1024) {
+        const unsigned threads = 32u * (unsigned)(8192 / W > 8 ? 8 : 8192 / W);
+        switch (W / 256) {
+            case 1: return launch_ex(rmsnorm_bwd_warp_kernel<1>, ctas, threads, 0, s, pdl, xx, gamma, rstd, hh, rr, oo,
+                                     dgamma_part, rows);
+            case 2: return launch_ex(rmsnorm_bwd_warp_kernel<2>, ctas, threads, 0, s, pdl, xx, gamma, rstd, hh, rr, oo,
+                                     dgamma_part, rows);
+            case 4: return launch_ex(rmsnorm_bwd_warp_kernel<4>, ctas, threads, 0, s, pdl, xx, gamma, rstd, hh, rr, oo,
+                                     dgamma_part, rows);
+            default: break;
+        }
+    }
+    return launch_ex(rmsnorm_bwd_kernel, ctas, (unsigned)(W / 8), 0, s, pdl, xx, gamma, rstd, hh, rr, oo, dgamma_part,
+                     rows, W, status_clear);
 }
 
 cudaError_t launch_conv_fwd(const void* gv, const float* k, const float* kb, const uint8_t* reset, void* u, int B,
                             int L, int D, cudaStream_t s, bool pdl) {
-    return launch_ex(conv_fwd_kernel, grid_for((long long)B * L * (D / 8), 256), 256, 0, s, pdl,
-                     static_cast<const uint16_t*>(gv), k, kb, reset, static_cast<uint4*>(u), B, L, D);
+    const long long n = (long long)B * ((L + kConvRun - 1) / kConvRun) * (D / 4);
+    return launch_ex(conv_fwd_kernel, grid_for(n, 256), 256, 0, s, pdl, static_cast<const uint16_t*>(gv), k, kb, reset,
+                     static_cast<uint16_t*>(u), B, L, D);
 }
 
 cudaError_t launch_conv_bwd(const void* gv, const float* k, const uint8_t* reset, const void* dxs, const void* dwm,
                             void* dgv, float* part, int B, int L, int D, uint32_t* status,
                             const uint32_t* mixer_status, cudaStream_t s, bool pdl) {
-    return launch_ex(conv_bwd_kernel, grid_for((long long)block_conv_parts(B, L) * (D / 8), 256), 256, 0, s, pdl,
-                     static_cast<const uint16_t*>(gv), k, reset, static_cast<const uint16_t*>(dxs),
-                     static_cast<const uint16_t*>(dwm), static_cast<uint16_t*>(dgv), part, B, L, D, status,
-                     mixer_status);
+    const dim3 grid((unsigned)block_conv_parts(B, L), (unsigned)(D / 256));
+    return launch_ex(conv_bwd_kernel, grid, 256, 0, s, pdl, static_cast<const uint16_t*>(gv), k, reset,
+                     static_cast<const uint16_t*>(dxs), static_cast<const uint16_t*>(dwm), static_cast<uint16_t*>(dgv),
+                     part, B, L, D, status, mixer_status);
 }
 
 cudaError_t launch_join_fwd(const void* gv, const void* ym, void* j, long long BL, int D, uint32_t* status,

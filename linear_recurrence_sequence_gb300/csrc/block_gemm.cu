@@ -16,11 +16,12 @@
 //                              MN-major (the token index is the row index of
 //                              both), split over the tokens with FP32 partials
 //                              added in a fixed order by a second kernel.
-// Roles: warp 4 streams 64-wide K slices of both operands by TMA (128-byte
-// swizzle) into a ring of stages; one thread of warp 5 issues tcgen05.mma
-// (M 128, N 256, K 16) and frees each stage with tcgen05.commit; warps 0-3
-// drain the accumulator (tcgen05.ld, one row per thread) through the layer's
-// fused epilogue.  Two accumulators (512 tensor-memory columns) let the
+// Roles: warp 8 streams 64-wide K slices of both operands by TMA (128-byte
+// swizzle) into a ring of stages; one thread of warp 9 issues tcgen05.mma
+// (M 128, N 256, K 16) and frees each stage with tcgen05.commit; warps 0-7
+// drain the accumulator (tcgen05.ld, one row per thread; warp w reads the
+// rows of tensor-memory lane quarter w % 4 and column half w / 4) through the
+// layer's fused epilogue.  Two accumulators (512 tensor-memory columns) let the
 // epilogue of one tile run under the MMAs of the next.  CTAs are persistent
 // over the tiles; every wait is bounded and an abort flag ends the other
 // roles after a failure.
@@ -39,12 +40,15 @@
 #include "kernels.cuh"
 #include "tmap.cuh"
 #include "umma.cuh"
+#include "block_math.cuh"
 
 namespace lrs {
 
 namespace {
 
-constexpr int kBgThreads = 192;   // warps 0-3 epilogue, 4 producer, 5 MMA
+constexpr int kBgEpiWarps = 8;
+constexpr int kBgThreads = 32 * (kBgEpiWarps + 2);   // warps 0-7 epilogue, 8 producer, 9 MMA
+constexpr int kBgProducer = kBgEpiWarps, kBgIssuer = kBgEpiWarps + 1;
 constexpr int kBgK = 64;          // K per stage (one 128-byte swizzle row of BF16)
 constexpr int kBgM = 128;         // tile rows
 constexpr int kBgN = 256;         // tile columns (accumulator columns)
@@ -54,21 +58,6 @@ constexpr uint32_t kBgBBytes = kBgN * 128;            // 32 KB
 constexpr uint32_t kBgStageBytes = kBgABytes + kBgBBytes;
 constexpr size_t kBgSmem = (size_t)kBgStages * kBgStageBytes + 1024 + 16 * 1024;   // + alignment and slack
 constexpr uint32_t kBgTmemCols = 2 * kBgN;           // two accumulators
-
-constexpr float kGeluC = 0.7978845608028654f;   // sqrt(2 / pi)
-constexpr float kGeluA = 0.044715f;
-
-// GeLU (tanh form) and its derivative.
-__device__ __forceinline__ void gelu_fwd_grad(float x, float& g, float& dg) {
-    const float u = kGeluC * (x + kGeluA * x * x * x);
-    const float th = tanhf(u);
-    g = 0.5f * x * (1.f + th);
-    dg = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * kGeluC * (1.f + 3.f * kGeluA * x * x);
-}
-__device__ __forceinline__ float gelu_fwd(float x) {
-    const float u = kGeluC * (x + kGeluA * x * x * x);
-    return 0.5f * x * (1.f + tanhf(u));
-}
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -114,13 +103,14 @@ __device__ __forceinline__ BgItem bg_item(const BlockGemmArgs& a, int w) {
 }
 
 // Epilogue of one accumulator row (row `m` of tile `it`, accumulator columns
-// at taddr).
+// at taddr), column half `half` of the tile (of its 128 hidden units for glu).
 template <int EPI>
-__device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem& it, int m, uint32_t taddr) {
+__device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem& it, int m, uint32_t taddr, int half) {
     const long long t = (long long)it.mt * kBgM + m;
+    const int c0 = half * (kBgN / 2), c1 = c0 + kBgN / 2;
     if (EPI == kEpiF32) {
         float* o = a.part + ((size_t)it.s * a.M + (size_t)t) * a.N + (size_t)it.nt * kBgN;
-        for (int c = 0; c < kBgN; c += 16) {
+        for (int c = c0; c < c1; c += 16) {
             float v[16];
             tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
@@ -132,7 +122,7 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
     const bool ok = t < a.M;
     if (EPI == kEpiGlu) {
         const int f0 = it.nt * (kBgN / 2);
-        for (int c = 0; c < kBgN / 2; c += 16) {
+        for (int c = half * (kBgN / 4); c < (half + 1) * (kBgN / 4); c += 16) {
             float va[16], vb[16];
             tmem_ld16(taddr + (uint32_t)c, va);
             tmem_ld16(taddr + (uint32_t)(kBgN / 2 + c), vb);
@@ -156,63 +146,71 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
         return;
     }
     const int n0 = it.nt * kBgN;
-    for (int c = 0; c < kBgN; c += 16) {
-        float v[16];
-        tmem_ld16(taddr + (uint32_t)c, v);
-        if (!ok) continue;
-        const int n = n0 + c;
-        if (EPI == kEpiStore) {
-            uint16_t* o = a.out + (size_t)t * a.ldo + n;
+    if (EPI == kEpiStore) {
+        for (int c = c0; c < c1; c += 16) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)c, v);
+            if (!ok) continue;
+            uint16_t* o = a.out + (size_t)t * a.ldo + n0 + c;
 #pragma unroll
             for (int j = 0; j < 16; j += 8) *reinterpret_cast<uint4*>(o + j) = pack8(v + j);
-        } else if (EPI == kEpiResid) {
-            const uint16_t* r = a.r + (size_t)t * a.ldr + n;
-            uint16_t* o = a.out + (size_t)t * a.ldo + n;
+        }
+        return;
+    }
+    // Epilogues that read operands of their own: the row's operands of 64
+    // columns are loaded first (up to 16 independent 16-byte loads in flight
+    // per thread), then the accumulator is drained 16 columns at a time.
+    constexpr int kChunk = 64;
+    for (int cc = c0; cc < c1; cc += kChunk) {
+        const int n = n0 + cc;
+        uint4 p0[kChunk / 8], p1[kChunk / 8];
+        if (ok) {
+            const uint16_t* s0 = EPI == kEpiResid ? a.r + (size_t)t * a.ldr + n : a.e0 + (size_t)t * a.lde0 + n;
+            const uint16_t* s1 = EPI == kEpiGluBwd ? s0 + a.F : EPI == kEpiJoinBwd ? a.e1 + (size_t)t * a.lde1 + n : s0;
 #pragma unroll
-            for (int j = 0; j < 16; j += 8) {
-                float rv[8];
-                unpack8(*reinterpret_cast<const uint4*>(r + j), rv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[j + i] += rv[i];
-                *reinterpret_cast<uint4*>(o + j) = pack8(v + j);
+            for (int j = 0; j < kChunk / 8; ++j) {
+                p0[j] = __ldg(reinterpret_cast<const uint4*>(s0) + j);
+                if (EPI != kEpiResid) p1[j] = __ldg(reinterpret_cast<const uint4*>(s1) + j);
             }
-        } else if (EPI == kEpiGluBwd) {
-            const uint16_t* ap = a.e0 + (size_t)t * a.lde0 + n;   // a at column f, b at F + f
-            uint16_t* o = a.out + (size_t)t * a.ldo + n;          // da at f, db at F + f
+        }
 #pragma unroll
-            for (int j = 0; j < 16; j += 8) {
-                float av[8], bv[8], da[8], db[8];
-                unpack8(*reinterpret_cast<const uint4*>(ap + j), av);
-                unpack8(*reinterpret_cast<const uint4*>(ap + a.F + j), bv);
+        for (int q = 0; q < kChunk / 16; ++q) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)(cc + 16 * q), v);
+            if (!ok) continue;
+            const size_t col = (size_t)n + 16 * q;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float x0[8], x1[8], r0[8], r1[8];
+                unpack8(p0[2 * q + h], x0);
+                if (EPI != kEpiResid) unpack8(p1[2 * q + h], x1);
+                float* vv = v + 8 * h;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    float g, dg;
-                    gelu_fwd_grad(av[i], g, dg);
-                    da[i] = v[j + i] * bv[i] * dg;
-                    db[i] = v[j + i] * g;
+                    if (EPI == kEpiResid) {
+                        r0[i] = vv[i] + x0[i];
+                    } else if (EPI == kEpiGluBwd) {   // x0 = a, x1 = b: da, db
+                        float g, dg;
+                        gelu_fwd_grad(x0[i], g, dg);
+                        r0[i] = vv[i] * x1[i] * dg;
+                        r1[i] = vv[i] * g;
+                    } else {                          // x0 = g, x1 = y_mixer: d y_mixer, dg
+                        float g, dg;
+                        gelu_fwd_grad(x0[i], g, dg);
+                        r0[i] = vv[i] * g;
+                        r1[i] = vv[i] * x1[i] * dg;
+                    }
                 }
-                *reinterpret_cast<uint4*>(o + j) = pack8(da);
-                *reinterpret_cast<uint4*>(o + a.F + j) = pack8(db);
-            }
-        } else if (EPI == kEpiJoinBwd) {
-            const uint16_t* gp = a.e0 + (size_t)t * a.lde0 + n;   // gate branch g
-            const uint16_t* yp = a.e1 + (size_t)t * a.lde1 + n;   // mixer output
-            uint16_t* o = a.out + (size_t)t * a.ldo + n;          // d y_mixer
-            uint16_t* o2 = a.out2 + (size_t)t * a.ld2 + n;        // d g
-#pragma unroll
-            for (int j = 0; j < 16; j += 8) {
-                float gv[8], yv[8], dym[8], dgo[8];
-                unpack8(*reinterpret_cast<const uint4*>(gp + j), gv);
-                unpack8(*reinterpret_cast<const uint4*>(yp + j), yv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float g, dg;
-                    gelu_fwd_grad(gv[i], g, dg);
-                    dym[i] = v[j + i] * g;
-                    dgo[i] = v[j + i] * yv[i] * dg;
+                if (EPI == kEpiResid) {
+                    *reinterpret_cast<uint4*>(a.out + (size_t)t * a.ldo + col + 8 * h) = pack8(r0);
+                } else if (EPI == kEpiGluBwd) {
+                    uint16_t* o = a.out + (size_t)t * a.ldo + col + 8 * h;   // da at f, db at F + f
+                    *reinterpret_cast<uint4*>(o) = pack8(r0);
+                    *reinterpret_cast<uint4*>(o + a.F) = pack8(r1);
+                } else {
+                    *reinterpret_cast<uint4*>(a.out + (size_t)t * a.ldo + col + 8 * h) = pack8(r0);
+                    *reinterpret_cast<uint4*>(a.out2 + (size_t)t * a.ld2 + col + 8 * h) = pack8(r1);
                 }
-                *reinterpret_cast<uint4*>(o + j) = pack8(dym);
-                *reinterpret_cast<uint4*>(o2 + j) = pack8(dgo);
             }
         }
     }
@@ -236,12 +234,12 @@ __global__ void __launch_bounds__(kBgThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_acc[i], 1);
-            mbar_init(&s_free[i], 4);   // the four epilogue warps
+            mbar_init(&s_free[i], kBgEpiWarps);
         }
         mbar_init(&s_fin, 1);
         s_abort = 0;
     }
-    if (warp == 5) {
+    if (warp == kBgIssuer) {
         tmem_alloc(&s_tmem, kBgTmemCols);
         tmem_fence_before_sync();
     }
@@ -256,7 +254,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
         atomicOr(a.status, kStatusTimeout);
     };
 
-    if (warp == 4) {
+    if (warp == kBgProducer) {
         // producer: every K step of every tile of this CTA, in order
         if (lane == 0) {
             uint32_t n = 0;   // stages issued
@@ -298,7 +296,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             const uint32_t lo = n > (uint32_t)kBgStages ? n - kBgStages : 0;
             for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_full[j % kBgStages], (j / kBgStages) & 1u);
         }
-    } else if (warp == 5) {
+    } else if (warp == kBgIssuer) {
         // MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_bf16(kBgM, kBgN) | (LAYOUT == kBgTN ? (1u << 15) : 0u) |
@@ -344,7 +342,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             mbar_wait_bounded(&s_fin, 0);
         }
     } else {
-        // epilogue warps 0-3: accumulator rows 32 warp .. 32 warp + 31
+        // epilogue warps 0-7: accumulator rows 32 (warp % 4) .. + 31, column half warp / 4
         uint32_t item = 0;
         for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x, ++item) {
             const BgItem it = bg_item(a, w);
@@ -354,21 +352,25 @@ __global__ void __launch_bounds__(kBgThreads, 1)
                 break;
             }
             tmem_fence_after_sync();
-            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + buf * (uint32_t)kBgN;
-            bg_epilogue<EPI>(a, it, 32 * warp + lane, taddr);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + buf * (uint32_t)kBgN;
+            bg_epilogue<EPI>(a, it, 32 * (warp & 3) + lane, taddr, warp >> 2);
             tmem_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[buf]);
         }
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kBgIssuer) {
         tmem_fence_after_sync();
         tmem_dealloc(tmem, kBgTmemCols);
     }
 }
 
-// Out[i] (i < n) = sum over p < parts, in order, of part[p * stride + i].
+// Out[i] (i < n) = sum over p < parts of part[p * stride + i], in a fixed
+// order.  Few parts: one thread per output, p = 0, 1, ... .  Many parts: 32
+// outputs per CTA (one per lane) and 32 groups of parts (one per warp, group g
+// taking p = g, g + 32, ... in order), the group sums then added g = 0..31.
+constexpr int kSumGroups = 32;
 __global__ void __launch_bounds__(256) sum_parts_kernel(const float* __restrict__ part, long long stride, int parts,
                                                         long long n, float* __restrict__ out) {
     pdl_trigger();
@@ -379,7 +381,28 @@ __global__ void __launch_bounds__(256) sum_parts_kernel(const float* __restrict_
         out[i] = s;
     }
 }
-
+__global__ void __launch_bounds__(32 * kSumGroups) sum_parts_grouped_kernel(const float* __restrict__ part,
+                                                                           long long stride, int parts, long long n,
+                                                                           float* __restrict__ out) {
+    __shared__ float acc[kSumGroups][33];
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    for (long long i0 = (long long)blockIdx.x * 32; i0 < n; i0 += (long long)gridDim.x * 32) {
+        const long long i = i0 + lane;
+        float s = 0.f;
+        if (i < n)
+            for (int p = g; p < parts; p += kSumGroups) s += part[(size_t)p * stride + i];
+        acc[g][lane] = s;
+        __syncthreads();
+        if (g == 0 && i < n) {
+            float t = 0.f;
+            for (int k = 0; k < kSumGroups; ++k) t += acc[k][lane];
+            out[i] = t;
+        }
+        __syncthreads();
+    }
+}
 // 2-D tensor map over a row-major [rows][cols] BF16 matrix, box {64, box_rows},
 // 128-byte swizzle (rows past the matrix and columns past cols read as zero).
 bool bg_map(CUtensorMap* map, const void* ptr, long long cols, long long rows, int box_rows) {
@@ -471,8 +494,14 @@ cudaError_t launch_block_gemm(const BlockGemmArgs& args_in, const void* A, const
 
 cudaError_t launch_sum_parts(const float* part, long long stride, int parts, long long n, float* out, cudaStream_t s,
                              bool pdl) {
+    if (parts > 16) {
+        long long blocks = (n + 31) / 32;
+        if (blocks > 8192) blocks = 8192;
+        return launch_ex(sum_parts_grouped_kernel, (unsigned)blocks, 32 * kSumGroups, 0, s, pdl, part, stride, parts,
+                         n, out);
+    }
     long long blocks = (n + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
+    if (blocks > 8192) blocks = 8192;
     if (blocks < 1) blocks = 1;
     return launch_ex(sum_parts_kernel, (unsigned)blocks, 256, 0, s, pdl, part, stride, parts, n, out);
 }

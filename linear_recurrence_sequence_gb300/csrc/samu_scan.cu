@@ -897,6 +897,7 @@ struct alignas(128) RevRingT {
     uint32_t w[S][2][kHalf][kWords];   // [slot][re, im][token][pair]
     uint32_t g[S][2][kHalf][kWords];   // dy rows, then (TMA variant) dw rows
     float4 ctrl[S][2 * kHalf];         // [slot][token: two float4]
+    float4 ck[2][32];                  // two units' checkpoints, {re, re, im, im} per lane (per-lane async copies)
     uint64_t full[S];
 };
 using RevRing = RevRingT<3>;
@@ -907,6 +908,14 @@ static_assert(sizeof(float4) * 2 * 32 <= sizeof(((RevRing*)nullptr)->w[0]),
 __device__ __forceinline__ RevRing& rev_ring(uint8_t* smem_raw, int warp) {
     return *reinterpret_cast<RevRing*>(smem_raw + (size_t)warp * sizeof(RevRing));
 }
+
+// Per-lane asynchronous 16-byte copy global -> shared (cp.async, no register
+// staging); each lane waits for its own copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Lane 0: the w and dy rows of the unit at token ts into `slot` (the slot's
 // expected bytes include the control words: it completes once
@@ -1094,6 +1103,11 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     const int n_units = T.t_end > T.t_begin ? (T.t_end - T.t_begin + kHalf - 1) / kHalf : 0;
     // unit u: tokens from ts(u), the segment from its end backwards
     auto unit_ts = [&](int u) { return T.t_begin + (n_units - 1 - u) * kHalf; };
+    // the forward's checkpoint of unit u (the state entering its first token),
+    // fetched one unit ahead by per-lane asynchronous copies
+    auto ckpt_src = [&](int u) {
+        return reinterpret_cast<const float4*>(a.hsub + ((size_t)T.b * g.CS + unit_ts(u) / kHalf) * M + m);
+    };
     if (lane == 0)
         for (int s = 0; s < kS; ++s) mbar_init(&R.full[s], 1);
     __syncwarp();
@@ -1108,6 +1122,8 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
     float nu0, nu1;
     up2(k.nu, nu0, nu1);
     const SubKind seg_kd = segment_kind(a.items, T, L, lane, k);
+    if (active && n_units > 0) cp_async16(&R.ck[0][lane], ckpt_src(0));
+    cp_async_commit();
     pdl_wait();
     // the adjoint arriving at the CTA from the later CTAs' maps
     const int cc = T.s / kSegPerCta;
@@ -1153,16 +1169,20 @@ __global__ void __launch_bounds__(kEngineThreads, 2)
         const int ts = unit_ts(u);
         const int nh = min(kHalf, T.t_end - ts);
         c2x z = czero();   // the forward's checkpoint: the state entering token ts
+        cp_async_wait_all();
         if (active) {
-            const f2x* hs = reinterpret_cast<const f2x*>(a.hsub + ((size_t)T.b * g.CS + ts / kHalf) * M + m);
-            z.re = hs[0];
-            z.im = hs[1];
+            const float4 c4 = R.ck[u & 1][lane];
+            z.re = pk2(c4.x, c4.y);
+            z.im = pk2(c4.z, c4.w);
         }
+        if (active && u + 1 < n_units) cp_async16(&R.ck[(u + 1) & 1][lane], ckpt_src(u + 1));
+        cp_async_commit();
         const size_t row0 = (((size_t)T.b * L + ts) * D + m) / 2;
         uint32_t* dwb = reinterpret_cast<uint32_t*>(a.dw) + row0;
         float* dwf = reinterpret_cast<float*>(a.dw) + 2 * row0;
         float* kp = reinterpret_cast<float*>(a.kpart + ((size_t)T.b * L + ts) * g.n_groups + T.grp);
         if (!mbar_wait_bounded(&R.full[slot], phase)) {
+            cp_async_wait_all();   // this lane's checkpoint copy lands before the CTA may exit
             if (lane == 0) {
                 atomicOr(a.status, kStatusTimeout);
                 if (DW == kDwBf16Tma) bulk_wait_all();

@@ -241,6 +241,22 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
         const long long te = b * a.L + min((long long)(ii + 1) * kMapRows, (long long)a.L);
         float iG = 0.f, iD = 0.f, iemax = 0.f;
         bool irst = false;
+        // The scalars of a group (tanh, sincos, expm1 in one lane per token)
+        // are formed after the next group's loads have been issued, so that
+        // their latency overlaps the loads; the item's last group follows
+        // the loop.
+        float pend_p = 0.f, pend_r = 0.f;
+        long long pend_t = -1;
+        auto scalars = [&](float s_p, float s_r, long long tg) {
+            const int k = lane >> 3;
+            if ((lane & 7) == 0 && tg + k < te) {
+                float em1, d;
+                irst = ctrl_fwd_token(a, tg + k, s_p, s_r, inv_phi, inv_r, bias_p, bias_r, k_phi, k_r, em1, d) || irst;
+                iG += em1;
+                iD += d;
+                iemax = fmaxf(iemax, fabsf(em1));
+            }
+        };
         for (long long t0 = tb; t0 < te; t0 += kCfTok) {
             f2x pacc[2 * kCfTok];   // {token k: phi, r} as even/odd-channel pairs
 #pragma unroll
@@ -255,6 +271,10 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
                         const bool ok = i0 + b4 < cpl && c < nch && t0 + k < te;
                         xv[b4][k] = ok ? __ldg(x + (size_t)(t0 + k) * nch + c) : make_uint4(0u, 0u, 0u, 0u);
                     }
+                }
+                if (i0 == 0 && pend_t >= 0) {   // the previous group's scalars under this group's first loads
+                    scalars(pend_p, pend_r, pend_t);
+                    pend_t = -1;
                 }
 #pragma unroll
                 for (int b4 = 0; b4 < kCfBatch; ++b4) {
@@ -291,16 +311,11 @@ __global__ void __launch_bounds__(kCfThreads, 2) samu_ctrl_fwd_kernel(SamuCtrlFw
             float sv = acc[0];
             sv += __shfl_xor_sync(0xffffffffu, sv, 2);
             sv += __shfl_xor_sync(0xffffffffu, sv, 1);
-            const float s_r = __shfl_down_sync(0xffffffffu, sv, 4);
-            const int k = lane >> 3;
-            if ((lane & 7) == 0 && t0 + k < te) {
-                float em1, d;
-                irst = ctrl_fwd_token(a, t0 + k, sv, s_r, inv_phi, inv_r, bias_p, bias_r, k_phi, k_r, em1, d) || irst;
-                iG += em1;
-                iD += d;
-                iemax = fmaxf(iemax, fabsf(em1));
-            }
+            pend_p = sv;
+            pend_r = __shfl_down_sync(0xffffffffu, sv, 4);
+            pend_t = t0;
         }
+        if (pend_t >= 0) scalars(pend_p, pend_r, pend_t);
         // lanes 0, 8, 16, 24 hold the sums over tokens k, k+4, ... of the
         // item: combined in a fixed order, ((l0 + l8) + (l16 + l24)), in lane 0
 #pragma unroll

@@ -801,25 +801,30 @@ def sweep_decode(name, dev, K, W):
 # Shapes: the mixer's short shape (B4 L4K, both widths 1024); the pages'
 # 400M-width block (Dm 1024, recurrent width D 1536) at their ablation batch
 # B4 L2K; the 1.3B widths (Dm 2048, D 2560) at the mixer's medium length.
-BLOCK_WORKLOADS = {"block_short": (4, 4096, 1024, 1024), "block_400m": (4, 2048, 1024, 1536),
-                   "block_medium": (1, 8192, 2048, 2560)}
-MIXER_KERNELS = ("samu_ctrl_fwd_kernel", "samu_fwd_maps_kernel", "samu_fwd_replay_kernel", "samu_bwd_maps_kernel",
-                 "samu_bwd_main_kernel", "samu_ctrl_bwd_kernel", "samu_params_kernel")
+# The RG-LRU block (rglru_block_*: the same layers around the RG-LRU with its
+# gate projections) at the same shapes: the pages' single-block comparison.
+BLOCK_SHAPES = {"short": (4, 4096, 1024, 1024), "400m": (4, 2048, 1024, 1536), "medium": (1, 8192, 2048, 2560)}
+BLOCK_WORKLOADS = {f"{pre}block_{k}": v + (mix,) for pre, mix in (("", "samu"), ("rglru_", "rglru"))
+                   for k, v in BLOCK_SHAPES.items()}
+MIXER_KERNELS = {"samu": ("samu_ctrl_fwd_kernel", "samu_fwd_maps_kernel", "samu_fwd_replay_kernel",
+                          "samu_bwd_maps_kernel", "samu_bwd_main_kernel", "samu_ctrl_bwd_kernel", "samu_params_kernel"),
+                 "rglru": ("rglru_scan_fwd_kernel", "rglru_scan_bwd_kernel", "rglru_alpha_kernels",
+                           "proj_gemm_kernel<logits>", "proj_gemm_kernel<dx, dW>", "proj_pack_kernel")}
 
 
-def block_step(B, L, Dm, D, dev, seed=0):
+def block_step(B, L, Dm, D, dev, seed=0, mixer="samu"):
     """One block forward+backward through the C ABI on resident inputs and
-    preallocated outputs; returns (step, scratch_fwd, scratch_bwd)."""
+    preallocated outputs; returns (step, scratch)."""
     import torch
     from linear_recurrence_sequence_gb300 import api, synth
-    inp = synth.block_inputs(B, L, Dm, D, seed, h0=False, reset_p=0.0)
+    inp = synth.block_inputs(B, L, Dm, D, seed, h0=False, reset_p=0.0, mixer=mixer)
     t = api.block_tensors_from_numpy(inp, dev)
-    nsaved, nscratch = api.samu_block_workspace_bytes(B, L, Dm, D)
+    nsaved, nscratch = api.samu_block_workspace_bytes(B, L, Dm, D, mixer)
     saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
     scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
-    M = D // 2
+    sshape = (B, D // 2, 2) if mixer == "samu" else (B, D)
     fo = {"out": torch.empty((B, L, Dm), dtype=torch.bfloat16, device=dev),
-          "hT": torch.empty((B, M, 2), dtype=torch.float32, device=dev)}
+          "hT": torch.empty(sshape, dtype=torch.float32, device=dev)}
     go = None
 
     def step():
@@ -834,9 +839,9 @@ def block_step(B, L, Dm, D, dev, seed=0):
 def sweep_block(name, dev, K, W):
     import torch
     from linear_recurrence_sequence_gb300 import api
-    B, L, Dm, D = BLOCK_WORKLOADS[name]
+    B, L, Dm, D, mixer = BLOCK_WORKLOADS[name]
     F = 3 * Dm
-    step, scratch = block_step(B, L, Dm, D, dev)
+    step, scratch = block_step(B, L, Dm, D, dev, mixer=mixer)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(W):
         flush.zero_()
@@ -883,9 +888,9 @@ def sweep_block(name, dev, K, W):
         peak, peak_src = float(pk["bf16_tflops"]), "measured (bf16_tflops, burst)"
     except Exception:
         peak, peak_src = 1900.0, "fallback"
-    mixer_ms = sum(per.get(k, 0.0) for k in MIXER_KERNELS)
+    mixer_ms = sum(per.get(k, 0.0) for k in MIXER_KERNELS[mixer])
     eager_ms = sum(per.values())
-    return {"workload": name, "kind": "samu_block", "B": B, "L": L, "Dm": Dm, "D": D, "F": F, "steps": K,
+    return {"workload": name, "kind": f"{mixer}_block", "B": B, "L": L, "Dm": Dm, "D": D, "F": F, "steps": K,
             "ms_per_step": round(ms_mean, 5), "ms_min": round(ms[0], 5), "ms_max": round(ms[-1], 5),
             "Mtok_per_s": round(B * L / (ms_mean / 1e3) / 1e6, 3),
             "roofline": {"bound": "tensor", "kernel": "block_gemm_kernel", "flops_per_step": flops,
@@ -912,6 +917,12 @@ PAGES_SHAPES = [
     (1, 32768, 1024, None, None, 37.3),
     (1, 32768, 2048, None, None, 40.2),
 ]
+
+
+# The pages' single-block table: one complete RecurrentBlock, F+B, SAMU
+# 5.8-7.6 % faster than RG-LRU over its three block shapes (the per-shape
+# values are not printed).
+PAGES_BLOCK_REDUCTION = "5.8-7.6"
 
 
 def run_compare(args, local):
@@ -955,6 +966,40 @@ def run_compare(args, local):
         line["samu_time_reduction_percent"] = round(100.0 * (rm - sm) / rm, 1)   # (t_RG - t_SAMU) / t_RG
         line["pages_time_reduction_percent"] = (p_red if p_red is not None
                                                 else round(100.0 * (p_rg - p_samu) / p_rg, 1))
+        print(json.dumps(line), flush=True)
+        del steps
+        torch.cuda.empty_cache()
+    # the single-block table: the same block around each mixer, same protocol
+    for name, (B, L, Dm, D) in BLOCK_SHAPES.items():
+        steps = {k: block_step(B, L, Dm, D, dev, mixer=k)[0] for k in ("samu", "rglru")}
+        samples = {k: [] for k in steps}
+
+        def measure_block(kind):
+            for _ in range(3):
+                flush.zero_()
+                steps[kind]()
+            for _ in range(5):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                steps[kind]()
+                e1.record()
+                e1.synchronize()
+                samples[kind].append(e0.elapsed_time(e1))
+
+        for order in (("rglru", "samu"), ("samu", "rglru")):
+            for kind in order:
+                measure_block(kind)
+        line = {"compare": "pages_block", "block": name, "B": B, "L": L, "Dm": Dm, "D": D, "F": 3 * Dm,
+                "protocol": "as the mixer rows: 2 rounds x (3 warm-up + 5 samples), eager F+B of one block "
+                            "between CUDA events after an L2 flush; median of 10 [min, max]"}
+        for kind in ("samu", "rglru"):
+            v = samples[kind]
+            line[kind + "_block"] = {"median_ms": round(statistics.median(v), 5), "min_ms": round(min(v), 5),
+                                     "max_ms": round(max(v), 5), "samples_ms": [round(x, 5) for x in v]}
+        sm, rm = line["samu_block"]["median_ms"], line["rglru_block"]["median_ms"]
+        line["samu_time_reduction_percent"] = round(100.0 * (rm - sm) / rm, 1)
+        line["pages_time_reduction_percent"] = PAGES_BLOCK_REDUCTION
         print(json.dumps(line), flush=True)
         del steps
         torch.cuda.empty_cache()

@@ -399,6 +399,37 @@ int samu_block_backward(const samu_block_params* p, const void* x, const float* 
                         const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved,
                         void* dx, float* dh0, const samu_block_grads* g, void* scratch, cudaStream_t stream);
 
+/* The same block around the RG-LRU mixer with its two 16-block gate
+ * projections, the comparison the [SAMU page] section 03 single-block table
+ * makes: identical layers, with (y_mix, hT) = rglru_proj_forward(x = u, ...)
+ * in place of the SAMU mixer (h0, hT, dhT, dh0 are [B,D] FP32).  Parameters:
+ * the block's own as in samu_block_params, then the mixer's as
+ * rglru_proj_forward takes them.  Errors: as samu_block_forward, with the
+ * mixer's width rules of rglru_proj_forward in place of samu_forward's. */
+typedef struct {
+    const float* gamma1; const void* w_in; const float* conv_k; const float* conv_b;
+    const void* w_x;         /* [16][D/16][D/16] BF16 */
+    const float* b_x;        /* [D] */
+    const void* w_a;         /* [16][D/16][D/16] BF16 */
+    const float* b_a;        /* [D] */
+    const float* alpha;      /* [D] */
+    const void* w_o; const float* gamma2; const void* w_mlp_in; const void* w_mlp_out;
+} rglru_block_params;
+
+typedef struct {
+    float* dgamma1; float* dw_in; float* dconv_k; float* dconv_b;
+    float* dw_x; float* db_x; float* dw_a; float* db_a; float* dalpha;
+    float* dw_o; float* dgamma2; float* dw_mlp_in; float* dw_mlp_out;
+} rglru_block_grads;
+
+int rglru_block_workspace_bytes(int B, int L, int Dm, int D, size_t* saved_bytes, size_t* scratch_bytes);
+int rglru_block_forward(const rglru_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                        int B, int L, int Dm, int D, void* out, float* hT, void* saved, void* scratch,
+                        cudaStream_t stream);
+int rglru_block_backward(const rglru_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                         const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved,
+                         void* dx, float* dh0, const rglru_block_grads* g, void* scratch, cudaStream_t stream);
+
 /* The block's tensor-core contraction on its own (for tests), layouts:
  *   LRS_GEMM_NT  C [M][N] BF16 = A [M][K] . B [N][K]^T
  *   LRS_GEMM_NN  C [M][N] BF16 = A [M][K] . B [K][N]

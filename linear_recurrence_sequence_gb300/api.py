@@ -57,6 +57,9 @@ _SIGNATURES = {
     "samu_block_forward": ([_P] * 4 + [_I] * 4 + [_P] * 5, _I),
     "samu_block_backward": ([_P] * 6 + [_I] * 4 + [_P] * 6, _I),
     "lrs_dense_gemm": ([_I, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "rglru_block_workspace_bytes": ([_I] * 4 + [_SZP, _SZP], _I),
+    "rglru_block_forward": ([_P] * 4 + [_I] * 4 + [_P] * 5, _I),
+    "rglru_block_backward": ([_P] * 6 + [_I] * 4 + [_P] * 6, _I),
 }
 
 # samu_block_params / samu_block_grads (include/samu.h): one pointer per field, in order
@@ -70,6 +73,19 @@ class _BlockParams(ctypes.Structure):
 
 class _BlockGrads(ctypes.Structure):
     _fields_ = [("d" + n, ctypes.c_void_p) for n in BLOCK_PARAMS]
+
+
+# rglru_block_params / rglru_block_grads: the block around the RG-LRU mixer
+RGLRU_BLOCK_PARAMS = ("gamma1", "w_in", "conv_k", "conv_b", "w_x", "b_x", "w_a", "b_a", "alpha",
+                      "w_o", "gamma2", "w_mlp_in", "w_mlp_out")
+
+
+class _RgBlockParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in RGLRU_BLOCK_PARAMS]
+
+
+class _RgBlockGrads(ctypes.Structure):
+    _fields_ = [("d" + n, ctypes.c_void_p) for n in RGLRU_BLOCK_PARAMS]
 
 
 def library_path() -> str:
@@ -458,89 +474,104 @@ def rglru_proj_backward(dy, dhT, x, w_x, b_x, w_a, b_a, alpha, h0, reset, saved,
 # ---------------------------------------------------------------------------
 # One RecurrentBlock around the SAMU mixer
 # ---------------------------------------------------------------------------
-def samu_block_workspace_bytes(B: int, L: int, Dm: int, D: int):
+def samu_block_workspace_bytes(B: int, L: int, Dm: int, D: int, mixer: str = "samu"):
     lib = _load()
     s = ctypes.c_size_t(0)
     c = ctypes.c_size_t(0)
-    _check("samu_block_workspace_bytes",
-           lib.samu_block_workspace_bytes(B, L, Dm, D, ctypes.byref(s), ctypes.byref(c)))
+    fn = "samu_block_workspace_bytes" if mixer == "samu" else "rglru_block_workspace_bytes"
+    _check(fn, getattr(lib, fn)(B, L, Dm, D, ctypes.byref(s), ctypes.byref(c)))
     return int(s.value), int(c.value)
 
 
 def _block_shapes(Dm: int, D: int) -> dict:
-    M, F = D // 2, 3 * Dm
+    M, F, dk = D // 2, 3 * Dm, D // PROJ_BLOCKS
     return {"gamma1": (Dm,), "w_in": (2 * D, Dm), "conv_k": (4, D), "conv_b": (D,), "nu": (M,), "theta": (M,),
             "w_phi": (D + 1,), "w_r": (D + 1,), "a_phi": (1,), "a_r": (1,), "w_o": (Dm, D), "gamma2": (Dm,),
-            "w_mlp_in": (2 * F, Dm), "w_mlp_out": (Dm, F)}
+            "w_mlp_in": (2 * F, Dm), "w_mlp_out": (Dm, F), "w_x": (PROJ_BLOCKS, dk, dk), "b_x": (D,),
+            "w_a": (PROJ_BLOCKS, dk, dk), "b_a": (D,), "alpha": (D,)}
 
 
-_BLOCK_BF16 = ("w_in", "w_o", "w_mlp_in", "w_mlp_out")
+_BLOCK_BF16 = ("w_in", "w_o", "w_mlp_in", "w_mlp_out", "w_x", "w_a")
 
 
-def _block_params(params: dict, Dm: int, dev) -> _BlockParams:
-    D = 2 * params["nu"].numel()
+def _block_kind(params: dict):
+    """(mixer, names, params struct, grads struct, D) of a parameter dict."""
+    if "nu" in params:
+        return "samu", BLOCK_PARAMS, _BlockParams, _BlockGrads, 2 * params["nu"].numel()
+    return "rglru", RGLRU_BLOCK_PARAMS, _RgBlockParams, _RgBlockGrads, params["alpha"].numel()
+
+
+def _block_params(params: dict, Dm: int, dev):
+    mixer, names, Struct, _, D = _block_kind(params)
     shapes = _block_shapes(Dm, D)
-    st = _BlockParams()
-    for n in BLOCK_PARAMS:
+    st = Struct()
+    for n in names:
         dt = torch.bfloat16 if n in _BLOCK_BF16 else torch.float32
         setattr(st, n, _need(params.get(n), n, dt, dev, shapes[n]).data_ptr())
     return st
 
 
+def _state_shape(mixer, B, D):
+    return (B, D // 2, 2) if mixer == "samu" else (B, D)
+
+
 def samu_block_forward(x, params: dict, h0=None, reset=None, *, out=None, saved=None, scratch=None):
-    """One RecurrentBlock forward through ``samu_block_forward``.  x: [B,L,Dm] BF16;
-    params: dict of the block's parameters (``BLOCK_PARAMS``).  Returns dict(out, hT, saved, scratch)."""
+    """One RecurrentBlock forward through ``samu_block_forward`` (params with
+    the SAMU mixer's nu, theta, ...) or ``rglru_block_forward`` (params with
+    the RG-LRU mixer's w_x, b_x, w_a, b_a, alpha).  x: [B,L,Dm] BF16.
+    Returns dict(out, hT, saved, scratch)."""
     dev = x.device
     B, L, Dm = x.shape
     _need(x, "x", torch.bfloat16, dev)
-    D = 2 * params["nu"].numel()
-    M = D // 2
-    _opt(h0, "h0", torch.float32, dev, (B, M, 2))
+    mixer, _, _, _, D = _block_kind(params)
+    sshape = _state_shape(mixer, B, D)
+    _opt(h0, "h0", torch.float32, dev, sshape)
     _opt(reset, "reset", torch.uint8, dev, (B, L))
     ps = _block_params(params, Dm, dev)
-    nsaved, nscratch = samu_block_workspace_bytes(B, L, Dm, D)
+    nsaved, nscratch = samu_block_workspace_bytes(B, L, Dm, D, mixer)
     y = _empty((B, L, Dm), torch.bfloat16, dev, out, "out")
-    hT = _empty((B, M, 2), torch.float32, dev, out, "hT")
+    hT = _empty(sshape, torch.float32, dev, out, "hT")
     if saved is None:
         saved = torch.empty(nsaved, dtype=torch.uint8, device=dev)
     if scratch is None:
         scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
     if saved.numel() < nsaved or scratch.numel() < nscratch:
         raise ValueError("saved/scratch buffers are too small")
-    st = _load().samu_block_forward(ctypes.cast(ctypes.pointer(ps), _P), _ptr(x), _ptr(h0), _ptr(reset), B, L, Dm,
-                                    D, _ptr(y), _ptr(hT), _ptr(saved), _ptr(scratch), _stream(dev))
-    _check("samu_block_forward", st)
+    fn = "samu_block_forward" if mixer == "samu" else "rglru_block_forward"
+    st = getattr(_load(), fn)(ctypes.cast(ctypes.pointer(ps), _P), _ptr(x), _ptr(h0), _ptr(reset), B, L, Dm, D,
+                              _ptr(y), _ptr(hT), _ptr(saved), _ptr(scratch), _stream(dev))
+    _check(fn, st)
     return {"out": y, "hT": hT, "saved": saved, "scratch": scratch}
 
 
 def samu_block_backward(dout, dhT, x, params: dict, h0, reset, saved, *, out=None, scratch=None):
-    """Backward of samu_block_forward.  Returns dict(dx, dh0, d<param> for every
-    parameter (FP32, the parameter's shape), scratch)."""
+    """Backward of samu_block_forward (either mixer).  Returns dict(dx, dh0,
+    d<param> for every parameter (FP32, the parameter's shape), scratch)."""
     dev = x.device
     B, L, Dm = x.shape
-    D = 2 * params["nu"].numel()
-    M = D // 2
+    mixer, names, _, Grads, D = _block_kind(params)
+    sshape = _state_shape(mixer, B, D)
     _need(dout, "dout", torch.bfloat16, dev, (B, L, Dm))
-    _opt(dhT, "dhT", torch.float32, dev, (B, M, 2))
+    _opt(dhT, "dhT", torch.float32, dev, sshape)
     _opt(reset, "reset", torch.uint8, dev, (B, L))
     ps = _block_params(params, Dm, dev)
-    nsaved, nscratch = samu_block_workspace_bytes(B, L, Dm, D)
+    nsaved, nscratch = samu_block_workspace_bytes(B, L, Dm, D, mixer)
     if saved is None or saved.numel() < nsaved:
         raise ValueError("saved must be the forward's saved buffer")
     if scratch is None:
         scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
     shapes = _block_shapes(Dm, D)
     o = {"dx": _empty((B, L, Dm), torch.bfloat16, dev, out, "dx"),
-         "dh0": _empty((B, M, 2), torch.float32, dev, out, "dh0")}
-    gs = _BlockGrads()
-    for n in BLOCK_PARAMS:
+         "dh0": _empty(sshape, torch.float32, dev, out, "dh0")}
+    gs = Grads()
+    for n in names:
         o["d" + n] = _empty(shapes[n], torch.float32, dev, out, "d" + n)
         setattr(gs, "d" + n, o["d" + n].data_ptr())
-    st = _load().samu_block_backward(ctypes.cast(ctypes.pointer(ps), _P), _ptr(x), _ptr(h0), _ptr(reset),
-                                     _ptr(dout), _ptr(dhT), B, L, Dm, D, _ptr(saved), _ptr(o["dx"]),
-                                     _ptr(o["dh0"]), ctypes.cast(ctypes.pointer(gs), _P), _ptr(scratch),
-                                     _stream(dev))
-    _check("samu_block_backward", st)
+    fn = "samu_block_backward" if mixer == "samu" else "rglru_block_backward"
+    st = getattr(_load(), fn)(ctypes.cast(ctypes.pointer(ps), _P), _ptr(x), _ptr(h0), _ptr(reset), _ptr(dout),
+                              _ptr(dhT), B, L, Dm, D, _ptr(saved), _ptr(o["dx"]), _ptr(o["dh0"]),
+                              ctypes.cast(ctypes.pointer(gs), _P), _ptr(scratch), _stream(dev))
+    _check(fn, st)
     o["scratch"] = scratch
     return o
 
@@ -568,7 +599,7 @@ def dense_gemm(layout: int, A, B, M: int, N: int, K: int, *, out=None, scratch=N
 def block_tensors_from_numpy(inp: dict, device) -> dict:
     """Device tensors of synth.block_inputs: {"x", "dout", "h0", "dhT", "reset", "params": {...}}."""
     params = {}
-    for n in BLOCK_PARAMS:
+    for n in (BLOCK_PARAMS if inp.get("mixer", "samu") == "samu" else RGLRU_BLOCK_PARAMS):
         params[n] = _bf16(inp[n], device) if n in _BLOCK_BF16 else _f32(inp[n], device)
     out = {"x": _bf16(inp["x"], device), "dout": _bf16(inp["dout"], device), "h0": _f32(inp["h0"], device),
            "dhT": _f32(inp["dhT"], device), "params": params}

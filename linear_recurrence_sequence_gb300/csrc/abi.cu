@@ -656,17 +656,65 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// RecurrentBlock around the SAMU mixer
+// RecurrentBlock around a mixer: SAMU (samu_block_*) or, for the pages'
+// comparison, the RG-LRU with its gate projections (rglru_block_*).  The
+// block's own layers are the same; only the mixer calls differ.
 // ---------------------------------------------------------------------------
 namespace {
+
+int check_block_widths(int B, int L, int Dm, int D) {
+    if (Dm % 256 != 0 || D % 256 != 0 || Dm > 4096) return LRS_ERR_UNSUPPORTED;
+    if ((long long)B * L >= (1LL << 31)) return LRS_ERR_UNSUPPORTED;
+    return LRS_OK;
+}
 
 int check_block_shape(int B, int L, int Dm, int D) {
     if (Dm < 1) return LRS_ERR_ARG;
     const int st = check_samu_shape(B, L, D);
-    if (st != LRS_OK) return st;
-    if (Dm % 256 != 0 || D % 256 != 0 || Dm > 4096) return LRS_ERR_UNSUPPORTED;
-    if ((long long)B * L >= (1LL << 31)) return LRS_ERR_UNSUPPORTED;
-    return LRS_OK;
+    return st != LRS_OK ? st : check_block_widths(B, L, Dm, D);
+}
+
+int check_rglru_block_shape(int B, int L, int Dm, int D) {
+    if (Dm < 1) return LRS_ERR_ARG;
+    const int st = check_rglru_proj_shape(B, L, D);
+    return st != LRS_OK ? st : check_block_widths(B, L, Dm, D);
+}
+
+// The block's own parameters and their gradients (both block kinds).
+struct BlockCore {
+    const float* gamma1;
+    const void* w_in;
+    const float* conv_k;
+    const float* conv_b;
+    const void* w_o;
+    const float* gamma2;
+    const void* w_mlp_in;
+    const void* w_mlp_out;
+};
+struct BlockCoreGrads {
+    float *dgamma1, *dw_in, *dconv_k, *dconv_b, *dw_o, *dgamma2, *dw_mlp_in, *dw_mlp_out;
+};
+
+bool core_ok(const BlockCore& p) {
+    return req(p.gamma1) && req(p.w_in) && req(p.conv_k) && req(p.conv_b) && req(p.w_o) && req(p.gamma2) &&
+           req(p.w_mlp_in) && req(p.w_mlp_out);
+}
+bool core_grads_ok(const BlockCoreGrads& g) {
+    return req(g.dgamma1) && req(g.dw_in) && req(g.dconv_k) && req(g.dconv_b) && req(g.dw_o) && req(g.dgamma2) &&
+           req(g.dw_mlp_in) && req(g.dw_mlp_out);
+}
+
+// The mixer's buffers inside the block's: its saved and scratch bytes and
+// the offset of its status word in its scratch.
+struct MixerSizes {
+    size_t saved, scratch, status;
+};
+MixerSizes samu_mixer_sizes(int B, int L, int D) {
+    return {samu_saved_layout(B, L, D).total, samu_scratch_layout(B, L, D).total, samu_scratch_layout(B, L, D).status};
+}
+MixerSizes rglru_mixer_sizes(int B, int L, int D) {
+    const RglruProjScratch ps = rglru_proj_scratch_layout(B, L, D);
+    return {rglru_saved_layout(B, L, D).total, ps.total, ps.scan.status};
 }
 
 // The four weight-gradient contractions (rows M x columns N of the gradient).
@@ -681,7 +729,7 @@ void block_dws(int Dm, int D, BlockDw (&w)[4]) {
     w[3] = {2 * D, Dm};    // w_in
 }
 
-BlockScratch block_scratch(int B, int L, int Dm, int D) {
+BlockScratch block_scratch(int B, int L, int Dm, int D, size_t mixer_scratch) {
     BlockDw w[4];
     block_dws(Dm, D, w);
     size_t wp = 0;
@@ -691,19 +739,7 @@ BlockScratch block_scratch(int B, int L, int Dm, int D) {
     }
     const size_t np = (size_t)block_norm_bwd_ctas((long long)B * L) * Dm;
     const size_t cp = (size_t)block_conv_parts(B, L) * 5 * D;
-    return block_scratch_layout(B, L, Dm, D, wp, np, cp);
-}
-
-bool block_params_ok(const samu_block_params* p) {
-    return p != nullptr && req(p->gamma1) && req(p->w_in) && req(p->conv_k) && req(p->conv_b) && req(p->nu) &&
-           req(p->theta) && req(p->w_phi) && req(p->w_r) && p->a_phi != nullptr && p->a_r != nullptr &&
-           req(p->w_o) && req(p->gamma2) && req(p->w_mlp_in) && req(p->w_mlp_out);
-}
-
-bool block_grads_ok(const samu_block_grads* g) {
-    return g != nullptr && req(g->dgamma1) && req(g->dw_in) && req(g->dconv_k) && req(g->dconv_b) && req(g->dnu) &&
-           req(g->dtheta) && req(g->dw_phi) && req(g->dw_r) && g->da_phi != nullptr && g->da_r != nullptr &&
-           req(g->dw_o) && req(g->dgamma2) && req(g->dw_mlp_in) && req(g->dw_mlp_out);
+    return block_scratch_layout(B, L, Dm, D, mixer_scratch, wp, np, cp);
 }
 
 BlockGemmArgs gemm_args(int layout, int epi, int M, int N, int K, uint32_t* status) {
@@ -732,32 +768,18 @@ int block_weight_grad(const void* A, const void* Bm, int M, int N, long long BL,
     return LRS_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int samu_block_workspace_bytes(int B, int L, int Dm, int D, size_t* saved_bytes, size_t* scratch_bytes) {
-    const int st = check_block_shape(B, L, Dm, D);
-    if (st != LRS_OK) return st;
-    if (saved_bytes != nullptr) *saved_bytes = block_saved_layout(B, L, Dm, D).total;
-    if (scratch_bytes != nullptr) *scratch_bytes = block_scratch(B, L, Dm, D).total;
-    return LRS_OK;
-}
-
-int samu_block_forward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset, int B,
-                       int L, int Dm, int D, void* out, float* hT, void* saved, void* scratch, cudaStream_t stream) {
-    const int st0 = check_block_shape(B, L, Dm, D);
-    if (st0 != LRS_OK) return st0;
-    if (!block_params_ok(p) || !req(x) || !opt(h0) || !req(out) || !req(hT) || !req(saved) || !req(scratch))
-        return LRS_ERR_ARG;
+// Block forward around mix(u, y_mixer, mixer saved, mixer scratch) -> status.
+template <class Mix>
+int block_forward_impl(const BlockCore& p, const void* x, const uint8_t* reset, int B, int L, int Dm, int D,
+                       void* out, void* saved, void* scratch, const MixerSizes& ms, Mix mix, cudaStream_t stream) {
     const long long BL = (long long)B * L;
     const int F = kBlockMlpRatio * Dm;
-    const BlockSaved sv = block_saved_layout(B, L, Dm, D);
-    const BlockScratch sc = block_scratch(B, L, Dm, D);
+    const BlockSaved sv = block_saved_layout(B, L, Dm, D, ms.saved);
+    const BlockScratch sc = block_scratch(B, L, Dm, D, ms.scratch);
     uint32_t* status = at<uint32_t>(scratch, 0);
     void* msaved = at<void>(saved, sv.mixer);
     void* mscratch = at<void>(scratch, sc.mixer);
-    const uint32_t* mstatus = at<uint32_t>(mscratch, samu_scratch_layout(B, L, D).status);
+    const uint32_t* mstatus = at<uint32_t>(mscratch, ms.status);
     void* h1 = at<void>(saved, sv.h1);
     float* rstd1 = at<float>(saved, sv.rstd1);
     void* gv = at<void>(saved, sv.gv);
@@ -771,16 +793,13 @@ int samu_block_forward(const samu_block_params* p, const void* x, const float* h
     void* q = at<void>(saved, sv.q);
 
     // h1 = RMSNorm(x); [g | v] = h1 w_in^T; u = conv(v)
-    LRS_LAUNCH(KID_BLOCK_NORM, stream, launch_rmsnorm_fwd(x, p->gamma1, h1, rstd1, BL, Dm, status, stream, false));
+    LRS_LAUNCH(KID_BLOCK_NORM, stream, launch_rmsnorm_fwd(x, p.gamma1, h1, rstd1, BL, Dm, status, stream, false));
     BlockGemmArgs g = gemm_args(kBgNT, kEpiStore, (int)BL, 2 * D, Dm, status);
     g.out = static_cast<uint16_t*>(gv);
     g.ldo = 2 * D;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h1, p->w_in, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_CONV, stream,
-               launch_conv_fwd(gv, p->conv_k, p->conv_b, reset, u, B, L, D, stream, pdl_ok()));
-    // the mixer on x_sel = w = u
-    const int st = samu_forward(u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L, D, ym,
-                                nullptr, hT, msaved, mscratch, stream);
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h1, p.w_in, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_CONV, stream, launch_conv_fwd(gv, p.conv_k, p.conv_b, reset, u, B, L, D, stream, pdl_ok()));
+    const int st = mix(u, ym, msaved, mscratch);
     if (st != LRS_OK) return st;
     // j = GeLU(g) y_mix; r1 = x + j w_o^T
     LRS_LAUNCH(KID_BLOCK_JOIN, stream, launch_join_fwd(gv, ym, j, BL, D, status, mstatus, stream, pdl_ok()));
@@ -789,41 +808,40 @@ int samu_block_forward(const samu_block_params* p, const void* x, const float* h
     g.ldo = Dm;
     g.r = static_cast<const uint16_t*>(x);
     g.ldr = Dm;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, j, p->w_o, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, j, p.w_o, stream, pdl_ok()));
     // h2 = RMSNorm(r1); [a | b] = h2 w_mlp_in^T, q = GeLU(a) b; out = r1 + q w_mlp_out^T
-    LRS_LAUNCH(KID_BLOCK_NORM, stream, launch_rmsnorm_fwd(r1, p->gamma2, h2, rstd2, BL, Dm, nullptr, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_NORM, stream, launch_rmsnorm_fwd(r1, p.gamma2, h2, rstd2, BL, Dm, nullptr, stream, pdl_ok()));
     g = gemm_args(kBgNT, kEpiGlu, (int)BL, F, Dm, status);
     g.out = static_cast<uint16_t*>(q);
     g.ldo = F;
     g.out2 = static_cast<uint16_t*>(ab);
     g.ld2 = 2 * F;
     g.F = F;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h2, p->w_mlp_in, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, h2, p.w_mlp_in, stream, pdl_ok()));
     g = gemm_args(kBgNT, kEpiResid, (int)BL, Dm, F, status);
     g.out = static_cast<uint16_t*>(out);
     g.ldo = Dm;
     g.r = static_cast<const uint16_t*>(r1);
     g.ldr = Dm;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, q, p->w_mlp_out, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, q, p.w_mlp_out, stream, pdl_ok()));
     return LRS_OK;
 }
 
-int samu_block_backward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset,
-                        const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved, void* dx,
-                        float* dh0, const samu_block_grads* gr, void* scratch, cudaStream_t stream) {
-    const int st0 = check_block_shape(B, L, Dm, D);
-    if (st0 != LRS_OK) return st0;
-    if (!block_params_ok(p) || !block_grads_ok(gr) || !req(x) || !opt(h0) || !req(dout) || !opt(dhT) ||
-        !req(saved) || !req(dx) || !req(dh0) || !req(scratch))
-        return LRS_ERR_ARG;
+// Block backward around mixb(dy_mixer, u, mixer saved, dxs, dwm, mixer
+// scratch) -> status, which writes the mixer's input gradient(s) w.r.t. u:
+// dxs, and dwm when two_grads (SAMU: x_sel = w = u).
+template <class MixB>
+int block_backward_impl(const BlockCore& p, const BlockCoreGrads& gr, const void* x, const uint8_t* reset,
+                        const void* dout, int B, int L, int Dm, int D, const void* saved, void* dx, void* scratch,
+                        const MixerSizes& ms, bool two_grads, MixB mixb, cudaStream_t stream) {
     const long long BL = (long long)B * L;
     const int F = kBlockMlpRatio * Dm;
-    const BlockSaved sv = block_saved_layout(B, L, Dm, D);
-    const BlockScratch sc = block_scratch(B, L, Dm, D);
+    const BlockSaved sv = block_saved_layout(B, L, Dm, D, ms.saved);
+    const BlockScratch sc = block_scratch(B, L, Dm, D, ms.scratch);
     uint32_t* status = at<uint32_t>(scratch, 0);
     const void* msaved = at<void>(saved, sv.mixer);
     void* mscratch = at<void>(scratch, sc.mixer);
-    const uint32_t* mstatus = at<uint32_t>(mscratch, samu_scratch_layout(B, L, D).status);
+    const uint32_t* mstatus = at<uint32_t>(mscratch, ms.status);
     const void* h1 = at<void>(saved, sv.h1);
     const float* rstd1 = at<float>(saved, sv.rstd1);
     const void* gv = at<void>(saved, sv.gv);
@@ -857,18 +875,18 @@ int samu_block_backward(const samu_block_params* p, const void* x, const float* 
     g.e0 = static_cast<const uint16_t*>(ab);
     g.lde0 = 2 * F;
     g.F = F;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dout, p->w_mlp_out, stream, false));
-    if ((st = block_weight_grad(dout, q, Dm, F, BL, gr->dw_mlp_out, wpart, status, stream)) != LRS_OK) return st;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dout, p.w_mlp_out, stream, false));
+    if ((st = block_weight_grad(dout, q, Dm, F, BL, gr.dw_mlp_out, wpart, status, stream)) != LRS_OK) return st;
     // dh2 = [da | db] w_mlp_in; dW_mlp_in = [da | db]^T h2
     g = gemm_args(kBgNN, kEpiStore, (int)BL, Dm, 2 * F, status);
     g.out = static_cast<uint16_t*>(dh2);
     g.ldo = Dm;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dab, p->w_mlp_in, stream, pdl_ok()));
-    if ((st = block_weight_grad(dab, h2, 2 * F, Dm, BL, gr->dw_mlp_in, wpart, status, stream)) != LRS_OK) return st;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dab, p.w_mlp_in, stream, pdl_ok()));
+    if ((st = block_weight_grad(dab, h2, 2 * F, Dm, BL, gr.dw_mlp_in, wpart, status, stream)) != LRS_OK) return st;
     // dr1 = dout + RMSNorm'(dh2)
     LRS_LAUNCH(KID_BLOCK_NORM, stream,
-               launch_rmsnorm_bwd(r1, p->gamma2, rstd2, dh2, dout, dr1, npart, BL, Dm, nullptr, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_SUM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma2, stream, pdl_ok()));
+               launch_rmsnorm_bwd(r1, p.gamma2, rstd2, dh2, dout, dr1, npart, BL, Dm, nullptr, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_SUM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr.dgamma2, stream, pdl_ok()));
     // join: dj = dr1 w_o -> dy_mix, dg; dW_o = dr1^T j
     g = gemm_args(kBgNN, kEpiJoinBwd, (int)BL, D, Dm, status);
     g.out = static_cast<uint16_t*>(dym);
@@ -879,33 +897,138 @@ int samu_block_backward(const samu_block_params* p, const void* x, const float* 
     g.lde0 = 2 * D;
     g.e1 = static_cast<const uint16_t*>(ym);
     g.lde1 = D;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dr1, p->w_o, stream, pdl_ok()));
-    if ((st = block_weight_grad(dr1, j, Dm, D, BL, gr->dw_o, wpart, status, stream)) != LRS_OK) return st;
-    // the mixer (x_sel = w = u): both of its input gradients reach u
-    st = samu_backward(dym, dhT, u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L, D,
-                       msaved, dxs, dwm, LRS_GRAD_BF16, dh0, gr->dnu, gr->dtheta, gr->dw_phi, gr->dw_r, gr->da_phi,
-                       gr->da_r, mscratch, stream);
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dr1, p.w_o, stream, pdl_ok()));
+    if ((st = block_weight_grad(dr1, j, Dm, D, BL, gr.dw_o, wpart, status, stream)) != LRS_OK) return st;
+    // the mixer: its input gradient(s) w.r.t. u
+    st = mixb(dym, u, msaved, dxs, dwm, mscratch);
     if (st != LRS_OK) return st;
     // convolution: dv (the recurrent half of [dg | dv]), dconv_k, dconv_b
     const int cparts = block_conv_parts(B, L);
     LRS_LAUNCH(KID_BLOCK_CONV, stream,
-               launch_conv_bwd(gv, p->conv_k, reset, dxs, dwm, dgv, cpart, B, L, D, status, mstatus, stream,
-                               pdl_ok()));
+               launch_conv_bwd(gv, p.conv_k, reset, dxs, two_grads ? dwm : nullptr, dgv, cpart, B, L, D, status,
+                               mstatus, stream, pdl_ok()));
     LRS_LAUNCH(KID_BLOCK_SUM, stream,
-               launch_sum_parts(cpart, 5LL * D, cparts, 4LL * D, gr->dconv_k, stream, pdl_ok()));
+               launch_sum_parts(cpart, 5LL * D, cparts, 4LL * D, gr.dconv_k, stream, pdl_ok()));
     LRS_LAUNCH(KID_BLOCK_SUM, stream,
-               launch_sum_parts(cpart + 4 * (size_t)D, 5LL * D, cparts, D, gr->dconv_b, stream, pdl_ok()));
+               launch_sum_parts(cpart + 4 * (size_t)D, 5LL * D, cparts, D, gr.dconv_b, stream, pdl_ok()));
     // dh1 = [dg | dv] w_in; dW_in = [dg | dv]^T h1
     g = gemm_args(kBgNN, kEpiStore, (int)BL, Dm, 2 * D, status);
     g.out = static_cast<uint16_t*>(dh1);
     g.ldo = Dm;
-    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dgv, p->w_in, stream, pdl_ok()));
-    if ((st = block_weight_grad(dgv, h1, 2 * D, Dm, BL, gr->dw_in, wpart, status, stream)) != LRS_OK) return st;
+    LRS_LAUNCH(KID_BLOCK_GEMM, stream, launch_block_gemm(g, dgv, p.w_in, stream, pdl_ok()));
+    if ((st = block_weight_grad(dgv, h1, 2 * D, Dm, BL, gr.dw_in, wpart, status, stream)) != LRS_OK) return st;
     // dx = dr1 + RMSNorm'(dh1)
     LRS_LAUNCH(KID_BLOCK_NORM, stream,
-               launch_rmsnorm_bwd(x, p->gamma1, rstd1, dh1, dr1, dx, npart, BL, Dm, nullptr, stream, pdl_ok()));
-    LRS_LAUNCH(KID_BLOCK_SUM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr->dgamma1, stream, pdl_ok()));
+               launch_rmsnorm_bwd(x, p.gamma1, rstd1, dh1, dr1, dx, npart, BL, Dm, nullptr, stream, pdl_ok()));
+    LRS_LAUNCH(KID_BLOCK_SUM, stream, launch_sum_parts(npart, Dm, ncta, Dm, gr.dgamma1, stream, pdl_ok()));
     return LRS_OK;
+}
+
+BlockCore core_of(const samu_block_params* p) {
+    return {p->gamma1, p->w_in, p->conv_k, p->conv_b, p->w_o, p->gamma2, p->w_mlp_in, p->w_mlp_out};
+}
+BlockCore core_of(const rglru_block_params* p) {
+    return {p->gamma1, p->w_in, p->conv_k, p->conv_b, p->w_o, p->gamma2, p->w_mlp_in, p->w_mlp_out};
+}
+BlockCoreGrads core_of(const samu_block_grads* g) {
+    return {g->dgamma1, g->dw_in, g->dconv_k, g->dconv_b, g->dw_o, g->dgamma2, g->dw_mlp_in, g->dw_mlp_out};
+}
+BlockCoreGrads core_of(const rglru_block_grads* g) {
+    return {g->dgamma1, g->dw_in, g->dconv_k, g->dconv_b, g->dw_o, g->dgamma2, g->dw_mlp_in, g->dw_mlp_out};
+}
+
+}  // namespace
+
+extern "C" {
+
+int samu_block_workspace_bytes(int B, int L, int Dm, int D, size_t* saved_bytes, size_t* scratch_bytes) {
+    const int st = check_block_shape(B, L, Dm, D);
+    if (st != LRS_OK) return st;
+    const MixerSizes ms = samu_mixer_sizes(B, L, D);
+    if (saved_bytes != nullptr) *saved_bytes = block_saved_layout(B, L, Dm, D, ms.saved).total;
+    if (scratch_bytes != nullptr) *scratch_bytes = block_scratch(B, L, Dm, D, ms.scratch).total;
+    return LRS_OK;
+}
+
+int samu_block_forward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset, int B,
+                       int L, int Dm, int D, void* out, float* hT, void* saved, void* scratch, cudaStream_t stream) {
+    const int st0 = check_block_shape(B, L, Dm, D);
+    if (st0 != LRS_OK) return st0;
+    if (p == nullptr || !core_ok(core_of(p)) || !req(p->nu) || !req(p->theta) || !req(p->w_phi) || !req(p->w_r) ||
+        p->a_phi == nullptr || p->a_r == nullptr || !req(x) || !opt(h0) || !req(out) || !req(hT) || !req(saved) ||
+        !req(scratch))
+        return LRS_ERR_ARG;
+    // the mixer on x_sel = w = u
+    auto mix = [&](const void* u, void* ym, void* msaved, void* mscratch) {
+        return samu_forward(u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L, D, ym,
+                            nullptr, hT, msaved, mscratch, stream);
+    };
+    return block_forward_impl(core_of(p), x, reset, B, L, Dm, D, out, saved, scratch, samu_mixer_sizes(B, L, D), mix,
+                              stream);
+}
+
+int samu_block_backward(const samu_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                        const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved, void* dx,
+                        float* dh0, const samu_block_grads* gr, void* scratch, cudaStream_t stream) {
+    const int st0 = check_block_shape(B, L, Dm, D);
+    if (st0 != LRS_OK) return st0;
+    if (p == nullptr || gr == nullptr || !core_ok(core_of(p)) || !core_grads_ok(core_of(gr)) || !req(p->nu) ||
+        !req(p->theta) || !req(p->w_phi) || !req(p->w_r) || p->a_phi == nullptr || p->a_r == nullptr ||
+        !req(gr->dnu) || !req(gr->dtheta) || !req(gr->dw_phi) || !req(gr->dw_r) || gr->da_phi == nullptr ||
+        gr->da_r == nullptr || !req(x) || !opt(h0) || !req(dout) || !opt(dhT) || !req(saved) || !req(dx) ||
+        !req(dh0) || !req(scratch))
+        return LRS_ERR_ARG;
+    // the mixer (x_sel = w = u): both of its input gradients reach u
+    auto mixb = [&](const void* dym, const void* u, const void* msaved, void* dxs, void* dwm, void* mscratch) {
+        return samu_backward(dym, dhT, u, u, h0, reset, p->nu, p->theta, p->w_phi, p->w_r, p->a_phi, p->a_r, B, L,
+                             D, msaved, dxs, dwm, LRS_GRAD_BF16, dh0, gr->dnu, gr->dtheta, gr->dw_phi, gr->dw_r,
+                             gr->da_phi, gr->da_r, mscratch, stream);
+    };
+    return block_backward_impl(core_of(p), core_of(gr), x, reset, dout, B, L, Dm, D, saved, dx, scratch,
+                               samu_mixer_sizes(B, L, D), true, mixb, stream);
+}
+
+int rglru_block_workspace_bytes(int B, int L, int Dm, int D, size_t* saved_bytes, size_t* scratch_bytes) {
+    const int st = check_rglru_block_shape(B, L, Dm, D);
+    if (st != LRS_OK) return st;
+    const MixerSizes ms = rglru_mixer_sizes(B, L, D);
+    if (saved_bytes != nullptr) *saved_bytes = block_saved_layout(B, L, Dm, D, ms.saved).total;
+    if (scratch_bytes != nullptr) *scratch_bytes = block_scratch(B, L, Dm, D, ms.scratch).total;
+    return LRS_OK;
+}
+
+int rglru_block_forward(const rglru_block_params* p, const void* x, const float* h0, const uint8_t* reset, int B,
+                        int L, int Dm, int D, void* out, float* hT, void* saved, void* scratch, cudaStream_t stream) {
+    const int st0 = check_rglru_block_shape(B, L, Dm, D);
+    if (st0 != LRS_OK) return st0;
+    if (p == nullptr || !core_ok(core_of(p)) || !req(p->w_x) || !req(p->b_x) || !req(p->w_a) || !req(p->b_a) ||
+        !req(p->alpha) || !req(x) || !opt(h0) || !req(out) || !req(hT) || !req(saved) || !req(scratch))
+        return LRS_ERR_ARG;
+    auto mix = [&](const void* u, void* ym, void* msaved, void* mscratch) {
+        return rglru_proj_forward(u, p->w_x, p->b_x, p->w_a, p->b_a, p->alpha, h0, reset, B, L, D, ym, nullptr, hT,
+                                  msaved, mscratch, stream);
+    };
+    return block_forward_impl(core_of(p), x, reset, B, L, Dm, D, out, saved, scratch, rglru_mixer_sizes(B, L, D), mix,
+                              stream);
+}
+
+int rglru_block_backward(const rglru_block_params* p, const void* x, const float* h0, const uint8_t* reset,
+                         const void* dout, const float* dhT, int B, int L, int Dm, int D, const void* saved, void* dx,
+                         float* dh0, const rglru_block_grads* gr, void* scratch, cudaStream_t stream) {
+    const int st0 = check_rglru_block_shape(B, L, Dm, D);
+    if (st0 != LRS_OK) return st0;
+    if (p == nullptr || gr == nullptr || !core_ok(core_of(p)) || !core_grads_ok(core_of(gr)) || !req(p->w_x) ||
+        !req(p->b_x) || !req(p->w_a) || !req(p->b_a) || !req(p->alpha) || !req(gr->dw_x) || !req(gr->db_x) ||
+        !req(gr->dw_a) || !req(gr->db_a) || !req(gr->dalpha) || !req(x) || !opt(h0) || !req(dout) || !opt(dhT) ||
+        !req(saved) || !req(dx) || !req(dh0) || !req(scratch))
+        return LRS_ERR_ARG;
+    auto mixb = [&](const void* dym, const void* u, const void* msaved, void* dxs, void*, void* mscratch) {
+        return rglru_proj_backward(dym, dhT, u, p->w_x, p->b_x, p->w_a, p->b_a, p->alpha, h0, reset, B, L, D,
+                                   msaved, dxs, LRS_GRAD_BF16, gr->dw_x, gr->db_x, gr->dw_a, gr->db_a, gr->dalpha,
+                                   dh0, mscratch, stream);
+    };
+    return block_backward_impl(core_of(p), core_of(gr), x, reset, dout, B, L, Dm, D, saved, dx, scratch,
+                               rglru_mixer_sizes(B, L, D), false, mixb, stream);
 }
 
 int lrs_dense_gemm(int layout, const void* A, const void* Bm, void* C, int M, int N, int K, void* scratch,

@@ -321,8 +321,9 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const uint16_t* __restric
     }
 }
 
-// Adjoint of conv_fwd_kernel with du = dx_sel + dw (the mixer reads x_sel =
-// w = u, so both gradients reach u):
+// Adjoint of conv_fwd_kernel with du = dx_sel + dw (the SAMU mixer reads
+// x_sel = w = u, so both gradients reach u; dwm == nullptr: du = dx_sel, the
+// RG-LRU mixer's single input gradient):
 //   dv[t] = sum_j k[j] du[t + j] over the outputs t + j whose tap j reaches t
 //           (no segment start at t + 1 .. t + j),
 //   dk[j] += du[t] v[t - j] over t's live taps, dkb += du[t].
@@ -363,7 +364,8 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const uint16_t* __restric
             const int t = t0 + i;
             const bool ok = t < L;
             ra[i] = ok ? __ldg(reinterpret_cast<const uint2*>(dxs + (row0 + t) * D) + q) : make_uint2(0u, 0u);
-            rw[i] = ok ? __ldg(reinterpret_cast<const uint2*>(dwm + (row0 + t) * D) + q) : make_uint2(0u, 0u);
+            rw[i] = (ok && dwm != nullptr) ? __ldg(reinterpret_cast<const uint2*>(dwm + (row0 + t) * D) + q)
+                                           : make_uint2(0u, 0u);
             const int tv = t0 - 3 + i;
             vr[i] = (tv >= 0 && tv < L) ? __ldg(reinterpret_cast<const uint2*>(gv + (row0 + tv) * 2 * D + D) + q)
                                         : make_uint2(0u, 0u);

@@ -276,17 +276,18 @@ inline RglruProjScratch rglru_proj_scratch_layout(int B, int L, int D) {
 // ---------------------------------------------------------------------------
 constexpr int kBlockMlpRatio = 3;
 
-// Forward -> backward: the mixer's own saved buffer, then the block's BF16
+// Forward -> backward: the mixer's own saved buffer (SAMU or the RG-LRU with
+// its gate projections: mixer_saved bytes), then the block's BF16
 // activations and the two norms' FP32 reciprocal RMS per token.
 struct BlockSaved {
     size_t mixer, h1, rstd1, gv, u, ym, j, r1, rstd2, h2, ab, q, total;
 };
 
-inline BlockSaved block_saved_layout(int B, int L, int Dm, int D) {
+inline BlockSaved block_saved_layout(int B, int L, int Dm, int D, size_t mixer_saved) {
     const size_t BL = (size_t)B * L, F = (size_t)kBlockMlpRatio * Dm;
     BlockSaved s;
     size_t o = 0;
-    s.mixer = o;  o = align_up(o + samu_saved_layout(B, L, D).total);
+    s.mixer = o;  o = align_up(o + mixer_saved);
     s.h1 = o;     o = align_up(o + BL * Dm * 2);
     s.rstd1 = o;  o = align_up(o + BL * 4);
     s.gv = o;     o = align_up(o + BL * 2 * D * 2);     // [g | v]
@@ -309,12 +310,12 @@ struct BlockScratch {
     size_t mixer, dab, dh2, dr1, dym, dgv, dxs, dwm, dh1, wpart, npart, cpart, total;
 };
 
-inline BlockScratch block_scratch_layout(int B, int L, int Dm, int D, size_t wpart_floats, size_t npart_floats,
-                                         size_t cpart_floats) {
+inline BlockScratch block_scratch_layout(int B, int L, int Dm, int D, size_t mixer_scratch, size_t wpart_floats,
+                                         size_t npart_floats, size_t cpart_floats) {
     const size_t BL = (size_t)B * L, F = (size_t)kBlockMlpRatio * Dm;
     BlockScratch s;
     size_t o = kAlign;   // [0, kAlign): the block's status word
-    s.mixer = o;  o = align_up(o + samu_scratch_layout(B, L, D).total);
+    s.mixer = o;  o = align_up(o + mixer_scratch);
     s.dab = o;    o = align_up(o + BL * 2 * F * 2);
     s.dh2 = o;    o = align_up(o + BL * Dm * 2);
     s.dr1 = o;    o = align_up(o + BL * Dm * 2);

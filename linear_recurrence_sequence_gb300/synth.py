@@ -7,8 +7,8 @@ same bits: BF16 tensors as uint16 bit patterns, FP32 parameters as float32.
 Draw order (one numpy PCG64 stream per seed):
     SAMU  : x_sel, w, nu, theta, w_phi, w_r, a_phi, a_r, h0, reset, dy, dhT
     RG-LRU: x, lx, la, alpha, h0, reset, dy, dhT
-    Block : x, then the block's own parameters, the mixer's (as SAMU), h0,
-            reset, dout, dhT (see block_inputs)
+    Block : x, then the block's own parameters, the mixer's (as SAMU, or the
+            projected RG-LRU's), h0, reset, dout, dhT (see block_inputs)
 
 Value distributions follow the workloads of the SAMU GPU page's measurements:
 BF16 N(0,1) activations and cotangents; nu_m = -ln U[0.9, 0.999];
@@ -92,17 +92,23 @@ def samu_inputs(B: int, L: int, D: int, seed: int, *, h0: bool = True,
 # Parameters of one RecurrentBlock, in the order of the C struct samu_block_params.
 BLOCK_PARAMS = ("gamma1", "w_in", "conv_k", "conv_b", "nu", "theta", "w_phi", "w_r", "a_phi", "a_r",
                 "w_o", "gamma2", "w_mlp_in", "w_mlp_out")
-BLOCK_BF16_PARAMS = ("w_in", "w_o", "w_mlp_in", "w_mlp_out")
+BLOCK_BF16_PARAMS = ("w_in", "w_o", "w_mlp_in", "w_mlp_out", "w_x", "w_a")
+# The same block around the RG-LRU mixer with its gate projections (the
+# pages' comparison), in the order of the C struct rglru_block_params.
+RGLRU_BLOCK_PARAMS = ("gamma1", "w_in", "conv_k", "conv_b", "w_x", "b_x", "w_a", "b_a", "alpha",
+                      "w_o", "gamma2", "w_mlp_in", "w_mlp_out")
 
 
 def block_inputs(B: int, L: int, Dm: int, D: int, seed: int, *, h0: bool = True,
-                 reset_p: float = 0.0) -> dict:
-    """Seeded inputs of one RecurrentBlock around the SAMU mixer (widths Dm,
-    D, F = 3 Dm).  BF16 tensors as uint16 bits: x, dout [B,L,Dm] ~ N(0,1);
+                 reset_p: float = 0.0, mixer: str = "samu") -> dict:
+    """Seeded inputs of one RecurrentBlock (widths Dm, D, F = 3 Dm) around
+    the SAMU mixer, or with mixer="rglru" around the RG-LRU with its gate
+    projections.  BF16 tensors as uint16 bits: x, dout [B,L,Dm] ~ N(0,1);
     the dense weights ~ N(0, 1/fan_in): w_in [2D,Dm], w_o [Dm,D],
     w_mlp_in [2F,Dm], w_mlp_out [Dm,F].  FP32: gamma1, gamma2 ~ 1 + 0.1 N(0,1);
     conv_k [4,D] ~ N(0, 1/4), conv_b [D] ~ 0.1 N(0,1); the mixer's parameters
-    drawn as samu_inputs draws them; h0, dhT [B,M,2]; Bernoulli resets."""
+    drawn as samu_inputs (or rglru_proj_inputs) draws them; h0, dhT [B,M,2]
+    (RG-LRU: [B,D]); Bernoulli resets."""
     if D % 2:
         raise ValueError("D must be even")
     M, F = D // 2, 3 * Dm
@@ -117,22 +123,32 @@ def block_inputs(B: int, L: int, Dm: int, D: int, seed: int, *, h0: bool = True,
     out["w_in"] = dense(2 * D, Dm)
     out["conv_k"] = (0.5 * rng.standard_normal((4, D))).astype(np.float32)
     out["conv_b"] = (0.1 * rng.standard_normal(D)).astype(np.float32)
-    out["nu"] = (-np.log(rng.uniform(0.9, 0.999, size=M))).astype(np.float32)
-    out["theta"] = rng.uniform(0.0, 2.0 * math.pi, size=M).astype(np.float32)
-    out["w_phi"] = rng.standard_normal(D + 1).astype(np.float32)
-    out["w_r"] = rng.standard_normal(D + 1).astype(np.float32)
-    out["a_phi"] = np.float32(rng.uniform(-1.0, 1.0))
-    out["a_r"] = np.float32(rng.uniform(-1.0, 1.0))
+    if mixer == "samu":
+        out["nu"] = (-np.log(rng.uniform(0.9, 0.999, size=M))).astype(np.float32)
+        out["theta"] = rng.uniform(0.0, 2.0 * math.pi, size=M).astype(np.float32)
+        out["w_phi"] = rng.standard_normal(D + 1).astype(np.float32)
+        out["w_r"] = rng.standard_normal(D + 1).astype(np.float32)
+        out["a_phi"] = np.float32(rng.uniform(-1.0, 1.0))
+        out["a_r"] = np.float32(rng.uniform(-1.0, 1.0))
+    else:
+        dk = D // PROJ_BLOCKS
+        out["w_x"] = f32_to_bf16_bits(rng.standard_normal((PROJ_BLOCKS, dk, dk)) / math.sqrt(dk))
+        out["w_a"] = f32_to_bf16_bits(rng.standard_normal((PROJ_BLOCKS, dk, dk)) / math.sqrt(dk))
+        out["b_x"] = (0.1 * rng.standard_normal(D)).astype(np.float32)
+        out["b_a"] = (0.1 * rng.standard_normal(D)).astype(np.float32)
+        sp = -np.log(rng.uniform(0.9, 0.999, size=D)) / 8.0          # softplus(alpha)
+        out["alpha"] = np.log(np.expm1(sp)).astype(np.float32)
     out["w_o"] = dense(Dm, D)
     out["gamma2"] = (1.0 + 0.1 * rng.standard_normal(Dm)).astype(np.float32)
     out["w_mlp_in"] = dense(2 * F, Dm)
     out["w_mlp_out"] = dense(Dm, F)
-    h0_arr = (0.1 * rng.standard_normal((B, M, 2))).astype(np.float32)
+    state = (B, M, 2) if mixer == "samu" else (B, D)
+    h0_arr = (0.1 * rng.standard_normal(state)).astype(np.float32)
     out["h0"] = h0_arr if h0 else None
     out["reset"] = (rng.random((B, L)) < reset_p).astype(np.uint8) if reset_p > 0 else None
     out["dout"] = _normal_bf16(rng, (B, L, Dm))
-    out["dhT"] = rng.standard_normal((B, M, 2)).astype(np.float32)
-    out.update({"B": B, "L": L, "Dm": Dm, "D": D})
+    out["dhT"] = rng.standard_normal(state).astype(np.float32)
+    out.update({"B": B, "L": L, "Dm": Dm, "D": D, "mixer": mixer})
     return out
 
 

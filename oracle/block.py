@@ -23,7 +23,9 @@ listed in the design notes) are:
     u[t, c] = kb[c] + sum_{j<4} k[j, c] v[t - j, c], taps before the start of
     t's segment (the last reset at or before t; t = 0 always starts one) are
     zero, so nothing leaks across a packed-sequence boundary;
-  - the mixer reads x_sel = w = u;
+  - the mixer reads x_sel = w = u (SAMU); the RG-LRU block, the pages'
+    comparison, puts the RG-LRU mixer with its two 16-block gate projections
+    (oracle.rglru_proj_forward) in the same place, on x = u;
   - the join is j = GeLU(g) * y_mixer, then r1 = x + j W_o^T (W_o: [Dm, D]);
   - the gated MLP has hidden width F = 3 Dm: q = GeLU(h2 W_1^T) * (h2 W_2^T),
     out = r1 + q W_3^T (W_1, W_2: [F, Dm]; W_3: [Dm, F]).
@@ -36,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import bf16_rne, samu_backward, samu_forward
+from . import bf16_rne, rglru_proj_backward, rglru_proj_forward, samu_backward, samu_forward
 
 EPS = 1e-6
 GELU_C = np.sqrt(2.0 / np.pi)
@@ -118,11 +120,34 @@ def conv_backward(v, k, start, du):
     return dv, dk, du.sum(axis=(0, 1))
 
 
-def samu_block_forward(x, p, h0=None, reset=None, bf16=True):
+def _mixer_forward(mixer, u, p, h0, reset):
+    if mixer == "samu":
+        return samu_forward(u, u, h0, reset, p["nu"], p["theta"], p["w_phi"], p["w_r"], p["a_phi"], p["a_r"])
+    return rglru_proj_forward(u, p["w_x"], p["b_x"], p["w_a"], p["b_a"], p["alpha"], h0, reset)
+
+
+def _mixer_backward(mixer, u, p, h0, reset, dym, dhT, r):
+    """The mixer's input gradient (BF16 points as the CUDA path stores them)
+    and its parameter gradients."""
+    if mixer == "samu":
+        gm = samu_backward(u, u, h0, reset, p["nu"], p["theta"], p["w_phi"], p["w_r"], p["a_phi"], p["a_r"],
+                           dym, dhT)
+        du = r(gm["dx_sel"]) + r(gm["dw"])          # x_sel = w = u: both gradients reach u
+        keys = ("dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r", "dh0")
+    else:
+        gm = rglru_proj_backward(u, p["w_x"], p["b_x"], p["w_a"], p["b_a"], p["alpha"], h0, reset, dym, dhT)
+        du = r(gm["dx"])
+        keys = ("dw_x", "db_x", "dw_a", "db_a", "dalpha", "dh0")
+    return du, {k: gm[k] for k in keys}
+
+
+def samu_block_forward(x, p, h0=None, reset=None, bf16=True, mixer="samu"):
     """x: [B, L, Dm]; p: dict of parameters (gamma1, w_g, w_v, conv_k, conv_b,
-    nu, theta, w_phi, w_r, a_phi, a_r, w_o, gamma2, w_1, w_2, w_3), all float64
+    the mixer's: nu, theta, w_phi, w_r, a_phi, a_r for SAMU, w_x, b_x, w_a,
+    b_a, alpha for mixer="rglru"; w_o, gamma2, w_1, w_2, w_3), all float64
     (BF16 values where the CUDA path keeps them in BF16).  Returns a dict with
-    out [B, L, Dm], hT [B, M, 2] and every saved intermediate."""
+    out [B, L, Dm], hT (the mixer's final state) and every saved
+    intermediate."""
     x = np.asarray(x, dtype=np.float64)
     B, L, _ = x.shape
     r = lambda a: _bf(a, bf16)
@@ -132,7 +157,7 @@ def samu_block_forward(x, p, h0=None, reset=None, bf16=True):
     v = r(h1 @ p["w_v"].T)
     start = segment_starts(reset, B, L)
     u = r(conv_forward(v, p["conv_k"], p["conv_b"], start))
-    mix = samu_forward(u, u, h0, reset, p["nu"], p["theta"], p["w_phi"], p["w_r"], p["a_phi"], p["a_r"])
+    mix = _mixer_forward(mixer, u, p, h0, reset)
     ym = r(mix["y"])
     j = r(gelu(g) * ym)
     r1 = r(x + j @ p["w_o"].T)
@@ -146,13 +171,13 @@ def samu_block_forward(x, p, h0=None, reset=None, bf16=True):
             "j": j, "r1": r1, "h2": h2, "rstd2": rstd2, "a": a, "b": b, "q": q, "start": start}
 
 
-def samu_block_backward(x, p, dout, h0=None, reset=None, dhT=None, bf16=True):
+def samu_block_backward(x, p, dout, h0=None, reset=None, dhT=None, bf16=True, mixer="samu"):
     """Backward of samu_block_forward for the cotangents dout [B, L, Dm] and
-    dhT [B, M, 2] (None: zero).  Returns dx and the gradient of every
-    parameter (keys d<name>), plus dh0."""
+    dhT (the mixer's final state; None: zero).  Returns dx and the gradient of
+    every parameter (keys d<name>), plus dh0."""
     x = np.asarray(x, dtype=np.float64)
     dout = np.asarray(dout, dtype=np.float64)
-    f = samu_block_forward(x, p, h0, reset, bf16)
+    f = samu_block_forward(x, p, h0, reset, bf16, mixer)
     r = lambda a: _bf(a, bf16)
     flat = lambda a: a.reshape(-1, a.shape[-1])
     # gated MLP: out = r1 + q W_3^T, q = GeLU(a) b
@@ -170,10 +195,8 @@ def samu_block_backward(x, p, dout, h0=None, reset=None, dhT=None, bf16=True):
     dw_o = flat(dr1).T @ flat(f["j"])
     dym = r(dj * gelu(f["g"]))
     dg = r(dj * f["ym"] * gelu_grad(f["g"]))
-    # mixer (x_sel = w = u): the oracle's own adjoint, BF16 outputs as the CUDA path stores them
-    gm = samu_backward(f["u"], f["u"], h0, reset, p["nu"], p["theta"], p["w_phi"], p["w_r"], p["a_phi"],
-                       p["a_r"], dym, dhT)
-    du = r(gm["dx_sel"]) + r(gm["dw"])
+    # the mixer: the oracle's own adjoint, BF16 outputs as the CUDA path stores them
+    du, gm = _mixer_backward(mixer, f["u"], p, h0, reset, dym, dhT, r)
     dv, dconv_k, dconv_b = conv_backward(f["v"], p["conv_k"], f["start"], du)
     dv = r(dv)
     # input projections and the first norm
@@ -182,7 +205,7 @@ def samu_block_backward(x, p, dout, h0=None, reset=None, dhT=None, bf16=True):
     dw_v = flat(dv).T @ flat(f["h1"])
     dxn, dgamma1 = rmsnorm_backward(x, p["gamma1"], f["rstd1"], dh1)
     dx = r(dr1 + dxn)
-    return {"dx": dx, "dgamma1": dgamma1, "dw_g": dw_g, "dw_v": dw_v, "dconv_k": dconv_k, "dconv_b": dconv_b,
-            "dnu": gm["dnu"], "dtheta": gm["dtheta"], "dw_phi": gm["dw_phi"], "dw_r": gm["dw_r"],
-            "da_phi": gm["da_phi"], "da_r": gm["da_r"], "dh0": gm["dh0"], "dw_o": dw_o, "dgamma2": dgamma2,
-            "dw_1": dw_1, "dw_2": dw_2, "dw_3": dw_3}
+    out = {"dx": dx, "dgamma1": dgamma1, "dw_g": dw_g, "dw_v": dw_v, "dconv_k": dconv_k, "dconv_b": dconv_b,
+           "dw_o": dw_o, "dgamma2": dgamma2, "dw_1": dw_1, "dw_2": dw_2, "dw_3": dw_3}
+    out.update(gm)
+    return out

@@ -223,3 +223,26 @@ def test_block_entry_points_reject_null_pointers(lib):
     assert lib.lrs_dense_gemm(3, p, p, p, 128, 256, 64, p, null) == 1          # unknown layout
     assert lib.lrs_dense_gemm(0, p, p, p, 128, 192, 64, p, null) == 2          # N not a multiple of 256
     assert lib.lrs_dense_gemm(2, p, p, p, 100, 256, 64, p, null) == 2          # TN: M not a multiple of 128
+
+
+@pytest.mark.parametrize("B,L,Dm,D,expect", [
+    (4, 4096, 1024, 1024, 0), (1, 8192, 2048, 2560, 0), (2, 100, 256, 256, 0), (1, 16, 256, 8192, 0),
+    (1, 16, 384, 256, 2), (1, 16, 256, 384, 2), (0, 16, 256, 256, 1), (1, 16, 0, 256, 1),
+])
+def test_rglru_block_shape_validation(lib, B, L, Dm, D, expect):
+    """Host-only: the RG-LRU block follows the block's width rules and the
+    projected RG-LRU's (no SAMU width limit: D = 8192 is accepted)."""
+    s = ctypes.c_size_t(0)
+    c = ctypes.c_size_t(0)
+    st = lib.rglru_block_workspace_bytes(B, L, Dm, D, ctypes.byref(s), ctypes.byref(c))
+    assert st == expect
+    if st == 0:
+        st2, msaved, _ = _ws(lib, "rglru_proj_workspace_bytes", B, L, D)
+        assert st2 == 0 and s.value >= msaved + B * L * 2 * (3 * Dm + 5 * D + 9 * Dm)
+
+
+def test_rglru_block_entry_points_reject_null_pointers(lib):
+    null = ctypes.c_void_p(0)
+    assert lib.rglru_block_forward(null, null, null, null, 1, 16, 256, 256, null, null, null, null, null) == 1
+    assert lib.rglru_block_backward(null, null, null, null, null, null, 1, 16, 256, 256, null, null, null, null,
+                                    null, null) == 1

@@ -72,15 +72,16 @@ def _oracle_params(inp):
     """The oracle's per-layer parameters from the library's stacked ones:
     w_in = [W_g; W_v], w_mlp_in = [W_1; W_2], w_mlp_out = W_3."""
     p = {}
-    for n in synth.BLOCK_PARAMS:
+    for n in (synth.BLOCK_PARAMS if inp["mixer"] == "samu" else synth.RGLRU_BLOCK_PARAMS):
         v = inp[n]
         p[n] = synth.bf16_bits_to_f64(v) if n in synth.BLOCK_BF16_PARAMS else np.asarray(v, dtype=np.float64)
     D, F = inp["D"], 3 * inp["Dm"]
     p["w_g"], p["w_v"] = p["w_in"][:D], p["w_in"][D:]
     p["w_1"], p["w_2"] = p["w_mlp_in"][:F], p["w_mlp_in"][F:]
     p["w_3"] = p["w_mlp_out"]
-    p["a_phi"] = float(inp["a_phi"])
-    p["a_r"] = float(inp["a_r"])
+    if inp["mixer"] == "samu":
+        p["a_phi"] = float(inp["a_phi"])
+        p["a_r"] = float(inp["a_r"])
     return p
 
 
@@ -110,31 +111,37 @@ CASES = {
     "two_tiles": dict(B=1, L=640, Dm=512, D=512, seed=22, reset_p=0.0),
     # mixer wider than the residual stream
     "wide_mixer": dict(B=1, L=256, Dm=256, D=768, seed=23, reset_p=0.02),
+    # the same block around the RG-LRU mixer with its gate projections (the pages' comparison)
+    "rglru_small_ragged": dict(B=2, L=300, Dm=256, D=256, seed=31, reset_p=0.01, mixer="rglru"),
+    "rglru_two_tiles": dict(B=1, L=640, Dm=512, D=512, seed=32, reset_p=0.0, mixer="rglru"),
 }
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_block_forward_backward_matches_oracle(case):
     c = CASES[case]
-    inp = synth.block_inputs(c["B"], c["L"], c["Dm"], c["D"], c["seed"], h0=True, reset_p=c["reset_p"])
+    mixer = c.get("mixer", "samu")
+    inp = synth.block_inputs(c["B"], c["L"], c["Dm"], c["D"], c["seed"], h0=True, reset_p=c["reset_p"], mixer=mixer)
     f, g = _run_block(inp)
     p = _oracle_params(inp)
     x = synth.bf16_bits_to_f64(inp["x"])
     dout = synth.bf16_bits_to_f64(inp["dout"])
     h0 = inp["h0"].astype(np.float64)
     dhT = inp["dhT"].astype(np.float64)
-    ref = ob.samu_block_forward(x, p, h0, inp["reset"], bf16=True)
-    exact = ob.samu_block_forward(x, p, h0, inp["reset"], bf16=False)
+    ref = ob.samu_block_forward(x, p, h0, inp["reset"], bf16=True, mixer=mixer)
+    exact = ob.samu_block_forward(x, p, h0, inp["reset"], bf16=False, mixer=mixer)
     _check_bf16("out", _f64(f["out"]), ref["out"], exact["out"], 2.0 ** -8)
     rel_hT = _rel(_f64(f["hT"]), ref["hT"])
     print(f"hT: rel {rel_hT:.2e}")
     assert rel_hT <= 2.0 ** -8
-    gr = _stacked_grads(ob.samu_block_backward(x, p, dout, h0, inp["reset"], dhT, bf16=True))
-    gx = ob.samu_block_backward(x, p, dout, h0, inp["reset"], dhT, bf16=False)
+    gr = _stacked_grads(ob.samu_block_backward(x, p, dout, h0, inp["reset"], dhT, bf16=True, mixer=mixer))
+    gx = ob.samu_block_backward(x, p, dout, h0, inp["reset"], dhT, bf16=False, mixer=mixer)
     _check_bf16("dx", _f64(g["dx"]), gr["dx"], gx["dx"], 2.0 ** -7)
-    mixer_group = ["dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r"]
+    mixer_group = (["dnu", "dtheta", "dw_phi", "dw_r", "da_phi", "da_r"] if mixer == "samu"
+                   else ["dw_x", "db_x", "dw_a", "db_a", "dalpha"])
     group_rms = np.sqrt(np.mean(np.concatenate([np.ravel(gr[k]) for k in mixer_group]) ** 2))
-    for k in ["dh0"] + ["d" + n for n in synth.BLOCK_PARAMS]:
+    names = synth.BLOCK_PARAMS if mixer == "samu" else synth.RGLRU_BLOCK_PARAMS
+    for k in ["dh0"] + ["d" + n for n in names]:
         ref_k = np.asarray(gr[k], dtype=np.float64)
         got = _f64(g[k]).reshape(np.shape(ref_k))
         if ref_k.size == 1:

@@ -24,20 +24,35 @@ def _params(rng, Dm, D, F, active=True):
     }
 
 
-def _case(seed=3, B=2, L=11, Dm=6, D=8):
+def _rglru_params(rng, Dm, D, F):
+    """The block's own parameters with the RG-LRU mixer's (16 gate-projection
+    blocks of width D/16)."""
+    p = _params(rng, Dm, D, F)
+    for k in ("nu", "theta", "w_phi", "w_r", "a_phi", "a_r"):
+        del p[k]
+    dk = D // 16
+    p["w_x"] = rng.standard_normal((16, dk, dk)) / np.sqrt(dk)
+    p["w_a"] = rng.standard_normal((16, dk, dk)) / np.sqrt(dk)
+    p["b_x"] = 0.1 * rng.standard_normal(D)
+    p["b_a"] = 0.1 * rng.standard_normal(D)
+    p["alpha"] = rng.uniform(-4.0, -1.0, D)
+    return p
+
+
+def _case(seed=3, B=2, L=11, Dm=6, D=8, mixer="samu"):
     rng = np.random.default_rng(seed)
     F = 3 * Dm
-    p = _params(rng, Dm, D, F)
+    p = _params(rng, Dm, D, F) if mixer == "samu" else _rglru_params(rng, Dm, D, F)
     x = rng.standard_normal((B, L, Dm))
-    h0 = 0.3 * rng.standard_normal((B, D // 2, 2))
+    h0 = 0.3 * rng.standard_normal((B, D // 2, 2) if mixer == "samu" else (B, D))
     reset = np.zeros((B, L), dtype=np.uint8)
     reset[1, 5] = 1
     reset[0, 9] = 1
     return rng, p, x, h0, reset
 
 
-def _loss(x, p, h0, reset, R, S):
-    f = ob.samu_block_forward(x, p, h0, reset, bf16=False)
+def _loss(x, p, h0, reset, R, S, mixer="samu"):
+    f = ob.samu_block_forward(x, p, h0, reset, bf16=False, mixer=mixer)
     return float(np.sum(f["out"] * R) + np.sum(f["hT"] * S))
 
 
@@ -65,6 +80,39 @@ def test_block_gradients_match_central_differences():
         def perturb(delta, key=key):
             q = dict(p)
             q[key] = p[key] + (delta if np.ndim(p[key]) else float(delta))
+            return x, q, h0, reset
+        check(key, g[gk], perturb)
+    check("x", g["dx"], lambda delta: (x + delta, p, h0, reset))
+    check("h0", g["dh0"], lambda delta: (x, p, h0 + delta, reset))
+
+
+RGLRU_GRAD_OF = {"gamma1": "dgamma1", "w_g": "dw_g", "w_v": "dw_v", "conv_k": "dconv_k", "conv_b": "dconv_b",
+                 "w_x": "dw_x", "b_x": "db_x", "w_a": "dw_a", "b_a": "db_a", "alpha": "dalpha",
+                 "w_o": "dw_o", "gamma2": "dgamma2", "w_1": "dw_1", "w_2": "dw_2", "w_3": "dw_3"}
+
+
+def test_rglru_block_gradients_match_central_differences():
+    """The same pins for the block with the RG-LRU mixer (the pages' comparison),
+    D = 32 (16 gate-projection blocks of width 2); the gates stay inside the
+    square-root clip's unclipped branch on these inputs."""
+    rng, p, x, h0, reset = _case(seed=4, D=32, mixer="rglru")
+    R = rng.standard_normal(x.shape)
+    S = rng.standard_normal(h0.shape)
+    g = ob.samu_block_backward(x, p, R, h0, reset, dhT=S, bf16=False, mixer="rglru")
+    eps = 1e-5
+
+    def check(name, grad, perturb):
+        d = rng.standard_normal(np.shape(grad))
+        lp = _loss(*perturb(+eps * d), R, S, mixer="rglru")
+        lm = _loss(*perturb(-eps * d), R, S, mixer="rglru")
+        fd = (lp - lm) / (2 * eps)
+        an = float(np.sum(np.asarray(grad) * d))
+        assert abs(fd - an) <= 2e-6 * max(1.0, abs(an)), (name, fd, an)
+
+    for key, gk in RGLRU_GRAD_OF.items():
+        def perturb(delta, key=key):
+            q = dict(p)
+            q[key] = p[key] + delta
             return x, q, h0, reset
         check(key, g[gk], perturb)
     check("x", g["dx"], lambda delta: (x + delta, p, h0, reset))

@@ -734,7 +734,7 @@ BlockScratch block_scratch(int B, int L, int Dm, int D, size_t mixer_scratch) {
     block_dws(Dm, D, w);
     size_t wp = 0;
     for (const BlockDw& d : w) {
-        const int sp = block_gemm_splits(d.M, d.N, (long long)B * L, kBlockSmsBound);
+        const int sp = block_gemm_splits_bound(d.M, d.N, (long long)B * L);
         if (sp > 1) wp = std::max(wp, (size_t)sp * d.M * d.N);
     }
     const size_t np = (size_t)block_norm_bwd_ctas((long long)B * L) * Dm;

@@ -35,6 +35,8 @@
 //   glu_bwd   C = dq: da = dq b GeLU'(a), db = dq GeLU(a) (BF16);
 //   join_bwd  C = dj: dy_mixer = dj GeLU(g), dg = dj y_mixer GeLU'(g) (BF16);
 //   f32       C in FP32 (dW partials).
+#include <algorithm>
+
 #include <cudaTypedefs.h>
 
 #include "kernels.cuh"
@@ -441,14 +443,37 @@ int block_gemm_sms() {
     return n < kBlockSmsBound ? n : kBlockSmsBound;
 }
 
+// Token splits of a TN (dW) contraction: the count that minimises the
+// estimated time, waves x K steps per item x the time of one K step of a
+// 128 x 256 tile (0.48 us, measured at B4 L4K Dm = D = 1024), plus the split
+// partials' extra traffic (written, read back, the sum written) at 6 TB/s.
+// A count that only fills one wave can leave most of a second wave idle
+// (192 items on 152 SMs run as two waves at 63%).
+constexpr double kBgStepUs = 0.48;
+constexpr double kBgBytesPerUs = 6.0e6;
+
 int block_gemm_splits(int M, int N, long long K, int sms) {
-    const int tiles = (M / kBgM) * (N / kBgN);
-    if (tiles < 1) return 1;
-    int s = (sms + tiles - 1) / tiles;
+    const long long tiles = (long long)(M / kBgM) * (N / kBgN);
+    if (tiles < 1 || sms < 1) return 1;
     const long long steps = (K + kBgK - 1) / kBgK;
-    if (s > kBlockGemmSplitsMax) s = kBlockGemmSplitsMax;
-    if (s > steps) s = (int)steps;
-    return s < 1 ? 1 : s;
+    double best = 0.0;
+    int best_s = 1;
+    for (int sp = 1; sp <= kBlockGemmSplitsMax && sp <= steps; ++sp) {
+        const long long waves = (tiles * sp + sms - 1) / sms;
+        const double t = (double)waves * (double)((steps + sp - 1) / sp) * kBgStepUs +
+                         (sp > 1 ? ((double)sp * 8.0 + 4.0) * (double)M * (double)N / kBgBytesPerUs : 0.0);
+        if (sp == 1 || t < best) {
+            best = t;
+            best_s = sp;
+        }
+    }
+    return best_s;
+}
+
+int block_gemm_splits_bound(int M, int N, long long K) {
+    int s = 1;
+    for (int sms = 1; sms <= kBlockSmsBound; ++sms) s = std::max(s, block_gemm_splits(M, N, K, sms));
+    return s;
 }
 
 cudaError_t launch_block_gemm(const BlockGemmArgs& args_in, const void* A, const void* Bm, cudaStream_t s, bool pdl) {

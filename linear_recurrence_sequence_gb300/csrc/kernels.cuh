@@ -497,9 +497,12 @@ struct BlockGemmArgs {
 };
 
 // Token splits of a TN contraction of an M x N weight gradient over K tokens
-// on `sms` SMs (block_gemm_sms(): this device's, capped at kBlockSmsBound).
+// on `sms` SMs (block_gemm_sms(): this device's, capped at kBlockSmsBound),
+// and the largest count any SM count up to kBlockSmsBound can choose (the
+// split partials' workspace is sized for it).
 int block_gemm_sms();
 int block_gemm_splits(int M, int N, long long K, int sms);
+int block_gemm_splits_bound(int M, int N, long long K);
 cudaError_t launch_block_gemm(const BlockGemmArgs& a, const void* A, const void* B, cudaStream_t s, bool pdl);
 // out[i] = sum_{p < parts} part[p * stride + i] in order, i < n.
 cudaError_t launch_sum_parts(const float* part, long long stride, int parts, long long n, float* out, cudaStream_t s,

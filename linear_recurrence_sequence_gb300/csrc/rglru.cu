@@ -21,6 +21,8 @@
 // x W (+ the biases, added on reading), FP32 products of the library's
 // tensor-core contraction kernel or, in the forward, formed per tile on the
 // tensor cores inside the scan.
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "umma.cuh"
 
@@ -35,10 +37,11 @@ constexpr int kRgBoxBytes = kRgTile * kRowBytes;   // one BF16 [128 x 64] box
 //      kernel), biases added on reading;
 //   2  computed in the kernel on the tensor cores (forward): the tile's x box
 //      (TMA, 128-byte swizzle) times the group's packed weights (both gates),
-//      FP32 accumulators in tensor memory, staged to shared memory as
-//      [128 tokens][kStageRow] FP32 per gate; biases added on reading.
+//      FP32 accumulators in tensor memory, staged to shared memory one gate
+//      at a time as [128 tokens][kStageRow] FP32; biases added on reading.
+//      (One gate's staging area keeps the CTA at two per SM.)
 constexpr int kStageRow = 68;                              // padded row: conflict-free staging stores
-constexpr int kStageBytes = 2 * kRgTile * kStageRow * 4;   // both gates
+constexpr int kStageBytes = kRgTile * kStageRow * 4;       // one gate
 constexpr int kWimgBytes = 2 * kGroup * kGroup * 2;        // both gates' [64 x 64] BF16 weight images
 
 template <int LM>
@@ -130,6 +133,22 @@ __device__ __forceinline__ RgGate2 rg_gate2(f2x lx, f2x la, f2x nsp, bool is_res
     return gt;
 }
 
+// The retention part of rg_gate2 alone (the same operations in the same
+// order): from the keep-gate logit, a and the write normaliser n.
+__device__ __forceinline__ void rg_retention2(f2x la, f2x nsp, bool is_reset, f2x& a, f2x& n) {
+    const f2x ga = sigmoid2(la);
+    const f2x lg = mul2(ga, nsp);   // log a
+    a = sfu_ex2(mul2(lg, dup2(kLog2e)));
+    const f2x u = sub2(0ull, expm1_2(mul2(dup2(2.0f), lg)));
+    float u0, u1;
+    up2(u, u0, u1);
+    n = pk2(sqrt_approx(fmaxf(u0, 0.0f)), sqrt_approx(fmaxf(u1, 0.0f)));
+    if (is_reset) {
+        a = 0ull;
+        n = dup2(1.0f);
+    }
+}
+
 __device__ __forceinline__ float softplus_f(float v) {
     return v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v));
 }
@@ -219,7 +238,7 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     uint8_t* sb = s_dyn + (size_t)slot * SB;
     const uint8_t* s_x = sb;
     const uint8_t* s_lx = LM == 2 ? s_stage : sb + kRgBoxBytes;
-    const uint8_t* s_la = LM == 2 ? s_stage + kRgTile * kStageRow * 4 : sb + kRgBoxBytes + LB;
+    const uint8_t* s_la = LM == 2 ? s_stage : sb + kRgBoxBytes + LB;   // LM 2: the same area, one gate at a time
     const long long tile = tile_u;
     const int chain = (int)(tile % g.n_chains);
     const int c = (int)(tile / g.n_chains);
@@ -284,41 +303,71 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             break;
         }
         tmem_fence_after_sync();
-        {   // warp w: tokens 32 (w % 4) .. + 31 (its tensor-memory lanes) of gate w / 4
-            const int q = warp & 3, gt = warp >> 2;
-            float* st = reinterpret_cast<float*>(s_stage) + (size_t)gt * kRgTile * kStageRow +
-                        (size_t)(32 * q + lane) * kStageRow;
-#pragma unroll
-            for (int col = 0; col < kGroup; col += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gt * kGroup + col), v);
-#pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4*>(st + col + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            }
-        }
-        tmem_fence_before_sync();
-        __syncthreads();
     }
 
     // the lane's two channels as pairs: a_t, b_t per token; the sub-chunk map (SA, SB)
     f2x av[kSub], bv[kSub];
     f2x SA = dup2(1.0f), SB = 0ull;
     const f2x nsp = pk2(nsp0, nsp1);
+    if (LM == 2) {
+        // gate 0 (write gate) staged: x g^x per token; then gate 1 (keep gate) into
+        // the same area: a, the normaliser n and b = (x g^x) n
 #pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        av[i] = dup2(1.0f);
-        bv[i] = 0ull;
-        if (i < nsub) {
-            const bool rs = s_rst[r0 + i] != 0;
-            const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
-            const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
-            const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
-            const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
-            av[i] = gt.a;
-            bv[i] = mul2(mul2(pk2(xx.x, xx.y), gt.gx), gt.n);
-            SA = mul2(av[i], SA);                // (a, b) o (A, B) = (a A, a B + b)
-            SB = fma2(av[i], SB, bv[i]);
+        for (int gt = 0; gt < 2; ++gt) {
+            {   // warp w: tokens 32 (w % 4) .. + 31 (its tensor-memory lanes), columns 32 (w / 4) .. + 31
+                const int q = warp & 3, ch = 32 * (warp >> 2);
+                float* st = reinterpret_cast<float*>(s_stage) + (size_t)(32 * q + lane) * kStageRow;
+#pragma unroll
+                for (int col = 0; col < 32; col += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gt * kGroup + ch + col), v);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4*>(st + ch + col + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < kSub; ++i) {
+                if (gt == 0) {
+                    av[i] = dup2(1.0f);
+                    bv[i] = 0ull;
+                }
+                if (i < nsub) {
+                    if (gt == 0) {
+                        const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
+                        const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
+                        bv[i] = mul2(pk2(xx.x, xx.y), sigmoid2(pk2(gl.x, gl.y)));
+                    } else {
+                        const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
+                        f2x a, n;
+                        rg_retention2(pk2(al.x, al.y), nsp, s_rst[r0 + i] != 0, a, n);
+                        av[i] = a;
+                        bv[i] = mul2(bv[i], n);
+                        SA = mul2(av[i], SA);                // (a, b) o (A, B) = (a A, a B + b)
+                        SB = fma2(av[i], SB, bv[i]);
+                    }
+                }
+            }
+            if (gt == 0) __syncthreads();   // every warp has read gate 0 before gate 1 overwrites it
+        }
+        tmem_fence_before_sync();
+    } else {
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+            av[i] = dup2(1.0f);
+            bv[i] = 0ull;
+            if (i < nsub) {
+                const bool rs = s_rst[r0 + i] != 0;
+                const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
+                const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
+                const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
+                const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+                av[i] = gt.a;
+                bv[i] = mul2(mul2(pk2(xx.x, xx.y), gt.gx), gt.n);
+                SA = mul2(av[i], SA);                // (a, b) o (A, B) = (a A, a B + b)
+                SB = fma2(av[i], SB, bv[i]);
+            }
         }
     }
     {
@@ -826,6 +875,12 @@ cudaError_t launch_rglru_proj_wimg(const void* w_x, const void* w_a, void* wimg,
 }
 
 // Persistent grid: as many CTAs as are resident at once, at most one per tile.
+// Residency is counted from the kernel's registers and shared memory against
+// the SM's (the occupancy query answers one CTA per SM for a kernel that
+// allocates tensor memory whatever its size, while two of the forward's fit).
+// Tickets go out in the order CTAs start, so a CTA only ever waits on tiles
+// held by CTAs already running: a grid larger than what is resident is slower,
+// never stuck.
 template <typename K>
 unsigned rg_grid(K kernel, int smem, long long n_tiles) {
     int dev = 0, sms = 1, per = 1;
@@ -833,6 +888,21 @@ unsigned rg_grid(K kernel, int smem, long long n_tiles) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kRgThreads, smem) != cudaSuccess || per < 1)
         per = 1;
+    cudaFuncAttributes fa{};
+    int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0;
+    if (cudaFuncGetAttributes(&fa, kernel) == cudaSuccess &&
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) == cudaSuccess) {
+        const long long cta_smem = (long long)fa.sharedSizeBytes + smem + reserved;
+        const long long warp_regs = ((long long)fa.numRegs * 32 + 255) / 256 * 256;   // 256-register units
+        const long long cta_regs = warp_regs * (kRgThreads / 32);
+        long long fit = threads_sm / kRgThreads;
+        if (cta_smem > 0) fit = std::min(fit, (long long)smem_sm / cta_smem);
+        if (cta_regs > 0) fit = std::min(fit, (long long)regs_sm / cta_regs);
+        if (fit > per) per = (int)fit;
+    }
     const long long n = (long long)sms * per;
     return (unsigned)(n < n_tiles ? n : (n_tiles > 0 ? n_tiles : 1));
 }

@@ -608,15 +608,27 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     const ProjDims pd = proj_dims(B, L, D);
     const int dk = pd.dk;
     uint32_t* status = at<uint32_t>(scratch, sc.status);
+    // the logits formed again in the scan kernel on the tensor cores when the
+    // diagonal blocks tile the 64-channel groups, as in the forward; otherwise
+    // by the logits contraction
+    const bool fused = 64 % dk == 0;
     if (cudaMemsetAsync(scratch, 0, sc.memset_bytes, stream) != cudaSuccess) return LRS_ERR_CUDA;
     LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream,
                launch_proj_pack(w_x, w_a, at<void>(scratch, ps.wt), at<void>(scratch, ps.wc), pd, stream));
-    LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
-               launch_proj_logits(x, at<void>(scratch, ps.wt), lx, la, D, pd, status, stream, false));
     CUtensorMap tm_dy, tm_x, tm_lx, tm_la;
-    if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile) || !make_bf16_map(&tm_x, x, B, L, D, kRgTile) ||
-        !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) || !make_f32_map(&tm_la, la, B, L, D, kRgTile))
-        return LRS_ERR_CUDA;
+    if (!make_bf16_map(&tm_dy, dy, B, L, D, kRgTile)) return LRS_ERR_CUDA;
+    if (fused) {
+        LRS_LAUNCH(KID_RGLRU_PROJ_PACK, stream, launch_rglru_proj_wimg(w_x, w_a, at<void>(scratch, ps.wimg), D, stream));
+        if (!make_bf16_map_sw128(&tm_x, x, B, L, D, kRgTile)) return LRS_ERR_CUDA;
+        tm_lx = tm_x;
+        tm_la = tm_x;
+    } else {
+        LRS_LAUNCH(KID_RGLRU_PROJ_FWD, stream,
+                   launch_proj_logits(x, at<void>(scratch, ps.wt), lx, la, D, pd, status, stream, false));
+        if (!make_bf16_map(&tm_x, x, B, L, D, kRgTile) || !make_f32_map(&tm_lx, lx, B, L, D, kRgTile) ||
+            !make_f32_map(&tm_la, la, B, L, D, kRgTile))
+            return LRS_ERR_CUDA;
+    }
     RglruScanBwdArgs a{};
     a.g = g;
     a.alpha = alpha;
@@ -630,6 +642,7 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     a.dla = nullptr;
     a.gparts = at<uint32_t>(scratch, ps.gparts);
     a.dk = dk;
+    a.wimg = at<uint8_t>(scratch, ps.wimg);
     a.bxpart = at<float>(scratch, ps.bxpart);
     a.bapart = at<float>(scratch, ps.bapart);
     a.grad_fp32 = 1;
@@ -640,7 +653,7 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
     a.flags = at<uint32_t>(scratch, sc.flags);
     a.counter = at<uint32_t>(scratch, sc.status + 4);
     a.status = at<uint32_t>(scratch, sc.status);
-    LRS_LAUNCH(KID_RGLRU_SCAN_BWD, stream, launch_rglru_scan_bwd(tm_dy, tm_x, tm_lx, tm_la, a, stream, true));
+    LRS_LAUNCH(KID_RGLRU_SCAN_BWD, stream, launch_rglru_scan_bwd(tm_dy, tm_x, tm_lx, tm_la, a, stream, fused ? 2 : 1));
     float* apart2 = at<float>(scratch, sc.apart2);
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.apart, apart2, dalpha, B * g.CT, D, stream));
     LRS_LAUNCH(KID_RGLRU_ALPHA, stream, launch_rglru_alpha(a.bxpart, apart2, db_x, B * g.CT, D, stream));
@@ -649,7 +662,6 @@ int rglru_proj_backward(const void* dy, const float* dhT, const void* x, const v
                launch_proj_dx(a.gparts, at<void>(scratch, ps.wc), dx, fp32, D, pd, status, stream, false));
     LRS_LAUNCH(KID_RGLRU_PROJ_BWD, stream,
                launch_proj_dw(a.gparts, x, at<float>(scratch, ps.dwpart), dw_x, dw_a, D, pd, status, stream, false));
-    (void)dk;
     return LRS_OK;
 }
 

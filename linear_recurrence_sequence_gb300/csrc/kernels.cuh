@@ -429,6 +429,7 @@ struct RglruScanBwdArgs {
     void* dla;
     uint32_t* gparts;       // PL only
     int dk;                 // PL only: D / 16
+    const uint8_t* wimg;    // logits mode 2: the groups' weight images
     float* bxpart;          // [B*CT][D]
     float* bapart;
     int grad_fp32;
@@ -450,9 +451,13 @@ cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm
 // [64 outputs][64 inputs] BF16 matrix (zero outside the diagonal blocks;
 // dk = D/16 must divide 64) in the K-major 128-byte-swizzled layout.
 cudaError_t launch_rglru_proj_wimg(const void* w_x, const void* w_a, void* wimg, int D, cudaStream_t s);
+// logits as for the forward: 0 raw BF16 l^x, l^a (dx, dl^x, dl^a out); 1 FP32
+// products x W, 2 products formed in the kernel from args.wimg (both: the
+// projected gradient parts out; for 2, tm_x is the 128-byte-swizzled map of x
+// and tm_lx, tm_la are unused).
 cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
                                   const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s,
-                                  bool projected = false);
+                                  int logits = 0);
 cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,
                                cudaStream_t s);
 // The gate projections' contractions on the tensor cores (proj_gemm.cu):

@@ -50,6 +50,22 @@ struct RgLogits {
     static constexpr int kSlotBytes = LM == 2 ? kRgBoxBytes + kWimgBytes : kRgBoxBytes + 2 * kBoxBytes;
 };
 
+// Logits mode 2: one gate's [128 tokens x 64] FP32 products from tensor memory
+// to the staging area [128][kStageRow]; warp w drains tokens 32 (w % 4) .. + 31
+// (the tensor-memory lanes it may read), columns 32 (w / 4) .. + 31.
+__device__ __forceinline__ void rg_stage_gate(uint32_t tmem, uint8_t* s_stage, int gt, int warp, int lane) {
+    const int q = warp & 3, ch = 32 * (warp >> 2);
+    float* st = reinterpret_cast<float*>(s_stage) + (size_t)(32 * q + lane) * kStageRow;
+#pragma unroll
+    for (int col = 0; col < 32; col += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gt * kGroup + ch + col), v);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(st + ch + col + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+}
+
 // The lane's two logits of token row r (biases added for LM >= 1).
 template <int LM>
 __device__ __forceinline__ float2 rg_logit(const uint8_t* box, int r, int lane, float2 bias) {
@@ -116,9 +132,10 @@ __device__ __forceinline__ f2x expm1_2(f2x v) {
                fabsf(v1) < 0.25f ? s1 : ex2_approx(v1 * kLog2e) - 1.0f);
 }
 
-__device__ __forceinline__ RgGate2 rg_gate2(f2x lx, f2x la, f2x nsp, bool is_reset) {
+// The keep gate's part (everything but g^x) from l^a.
+__device__ __forceinline__ RgGate2 rg_keep_gate2(f2x la, f2x nsp, bool is_reset) {
     RgGate2 gt;
-    gt.gx = sigmoid2(lx);
+    gt.gx = 0ull;
     gt.ga = sigmoid2(la);
     const f2x lg = mul2(gt.ga, nsp);   // log a
     gt.a = sfu_ex2(mul2(lg, dup2(kLog2e)));
@@ -133,20 +150,10 @@ __device__ __forceinline__ RgGate2 rg_gate2(f2x lx, f2x la, f2x nsp, bool is_res
     return gt;
 }
 
-// The retention part of rg_gate2 alone (the same operations in the same
-// order): from the keep-gate logit, a and the write normaliser n.
-__device__ __forceinline__ void rg_retention2(f2x la, f2x nsp, bool is_reset, f2x& a, f2x& n) {
-    const f2x ga = sigmoid2(la);
-    const f2x lg = mul2(ga, nsp);   // log a
-    a = sfu_ex2(mul2(lg, dup2(kLog2e)));
-    const f2x u = sub2(0ull, expm1_2(mul2(dup2(2.0f), lg)));
-    float u0, u1;
-    up2(u, u0, u1);
-    n = pk2(sqrt_approx(fmaxf(u0, 0.0f)), sqrt_approx(fmaxf(u1, 0.0f)));
-    if (is_reset) {
-        a = 0ull;
-        n = dup2(1.0f);
-    }
+__device__ __forceinline__ RgGate2 rg_gate2(f2x lx, f2x la, f2x nsp, bool is_reset) {
+    RgGate2 gt = rg_keep_gate2(la, nsp, is_reset);
+    gt.gx = sigmoid2(lx);
+    return gt;
 }
 
 __device__ __forceinline__ float softplus_f(float v) {
@@ -314,18 +321,7 @@ __global__ void __launch_bounds__(kRgThreads, 2)
         // the same area: a, the normaliser n and b = (x g^x) n
 #pragma unroll
         for (int gt = 0; gt < 2; ++gt) {
-            {   // warp w: tokens 32 (w % 4) .. + 31 (its tensor-memory lanes), columns 32 (w / 4) .. + 31
-                const int q = warp & 3, ch = 32 * (warp >> 2);
-                float* st = reinterpret_cast<float*>(s_stage) + (size_t)(32 * q + lane) * kStageRow;
-#pragma unroll
-                for (int col = 0; col < 32; col += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gt * kGroup + ch + col), v);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4*>(st + ch + col + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                }
-            }
+            rg_stage_gate(tmem, s_stage, gt, warp, lane);
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < kSub; ++i) {
@@ -340,10 +336,9 @@ __global__ void __launch_bounds__(kRgThreads, 2)
                         bv[i] = mul2(pk2(xx.x, xx.y), sigmoid2(pk2(gl.x, gl.y)));
                     } else {
                         const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
-                        f2x a, n;
-                        rg_retention2(pk2(al.x, al.y), nsp, s_rst[r0 + i] != 0, a, n);
-                        av[i] = a;
-                        bv[i] = mul2(bv[i], n);
+                        const RgGate2 kg = rg_keep_gate2(pk2(al.x, al.y), nsp, s_rst[r0 + i] != 0);
+                        av[i] = kg.a;
+                        bv[i] = mul2(bv[i], kg.n);
                         SA = mul2(av[i], SA);                // (a, b) o (A, B) = (a A, a B + b)
                         SB = fma2(av[i], SB, bv[i]);
                     }
@@ -516,34 +511,62 @@ __device__ __forceinline__ void split_bf2(float v0, float v1, uint32_t& hi, uint
     lo = f2_to_bf2(v0 - h.x, v1 - h.y);
 }
 
-template <bool PL>
+// Logits mode 2 (gate logits formed in the kernel): dynamic shared memory is
+// [x box, 128-byte swizzle][weight images, then g^x per token][dy box][staging];
+// the write gate's products are staged first and turned into g^x (kept in
+// shared memory for the reverse sweep), then the keep gate's, which stay in the
+// staging area for both sweeps.
+constexpr int kBwdGxOff = kRgBoxBytes;                       // the weight images' slot, reused
+constexpr int kBwdGxBytes = kRgTile * kGroup * 4;            // g^x [128][64] FP32
+constexpr int kBwdDyOff = kBwdGxOff + kBwdGxBytes;
+constexpr int kBwdStageOff = kBwdDyOff + kRgBoxBytes;
+constexpr int kBwdFusedBytes = kBwdStageOff + kStageBytes;
+static_assert(kWimgBytes <= kBwdGxBytes, "the weight images fit the g^x area");
+
+template <int LM>
 __global__ void __launch_bounds__(kRgThreads, 2)
     rglru_scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_lx, const __grid_constant__ CUtensorMap tm_la,
                           RglruScanBwdArgs a) {
-    constexpr int LB = RgLogits<PL>::kBoxBytes;
-    extern __shared__ __align__(128) uint8_t s_dyn[];   // boxes: dy, x, l^x, l^a
-    uint32_t (*s_g)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn);
-    uint32_t (*s_x)[kGroup / 2] = reinterpret_cast<uint32_t (*)[kGroup / 2]>(s_dyn + kRgBoxBytes);
-    const uint8_t* s_lx = s_dyn + 2 * kRgBoxBytes;
-    const uint8_t* s_la = s_dyn + 2 * kRgBoxBytes + LB;
+    constexpr bool PL = LM >= 1;
+    constexpr int LB = RgLogits<LM>::kBoxBytes;
+    constexpr uint32_t kIdesc = umma_idesc_bf16(kRgTile, kGroup);
+    // LM 0/1 boxes: dy, x, l^x, l^a; LM 2: see above (1024-byte aligned for the swizzle)
+    extern __shared__ __align__(1024) uint8_t s_raw[];
+    uint8_t* s_dyn = LM == 2 ? s_raw + ((1024u - (smem_u32(s_raw) & 1023u)) & 1023u) : s_raw;
+    uint32_t (*s_g)[kGroup / 2] =
+        reinterpret_cast<uint32_t (*)[kGroup / 2]>(LM == 2 ? s_dyn + kBwdDyOff : s_dyn);
+    const uint8_t* s_x = LM == 2 ? s_dyn : s_dyn + kRgBoxBytes;
+    uint8_t* s_stage = s_dyn + kBwdStageOff;
+    float2* s_gx = reinterpret_cast<float2*>(s_dyn + kBwdGxOff);   // LM 2: [128][32] pairs
+    const uint8_t* s_lx = LM == 2 ? s_stage : s_dyn + 2 * kRgBoxBytes;
+    const uint8_t* s_la = LM == 2 ? s_stage : s_dyn + 2 * kRgBoxBytes + LB;
     __shared__ uint8_t s_rst[kRgTile];
     __shared__ float4 s_map[kRgWarps][32];
     __shared__ float2 s_ent[kRgWarps][32];
     __shared__ float2 s_acc[kRgWarps][32];
     __shared__ float4 s_bacc[PL ? kRgWarps : 1][32];
     __shared__ __align__(8) uint64_t s_bar;
+    __shared__ __align__(8) uint64_t s_mma_bar;
+    __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_tile;
     __shared__ int s_err;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    if (LM == 2 && warp == 0) {   // two gates x 64 FP32 columns of tensor memory
+        tmem_alloc(&s_tmem, 2 * kGroup);
+        tmem_fence_before_sync();
+    }
     if (tid == 0) {
         s_tile = atomicAdd(a.counter, 1u);
         mbar_init(&s_bar, 1);
+        if (LM == 2) mbar_init(&s_mma_bar, 1);
     }
     __syncthreads();
+    if (LM == 2) tmem_fence_after_sync();
+    const uint32_t tmem = LM == 2 ? s_tmem : 0u;
     const ScanGeom& g = a.g;
     const long long tile = s_tile;
     const int chain = (int)(tile % g.n_chains);
@@ -560,11 +583,18 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     const size_t hb = (size_t)b * g.CS;
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(&s_bar, 2 * kRgBoxBytes + 2 * LB);
-        tma_load_3d(&s_g[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(&s_x[0][0], &tm_x, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(s_dyn + 2 * kRgBoxBytes, &tm_lx, grp * kGroup, t0, b, &s_bar);
-        tma_load_3d(s_dyn + 2 * kRgBoxBytes + LB, &tm_la, grp * kGroup, t0, b, &s_bar);
+        if (LM == 2) {
+            mbar_arrive_expect_tx(&s_bar, 2 * kRgBoxBytes + kWimgBytes);
+            tma_load_3d(s_dyn, &tm_x, grp * kGroup, t0, b, &s_bar);
+            bulk_load(s_dyn + kBwdGxOff, a.wimg + (size_t)grp * kWimgBytes, kWimgBytes, &s_bar);
+            tma_load_3d(&s_g[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
+        } else {
+            mbar_arrive_expect_tx(&s_bar, 2 * kRgBoxBytes + 2 * LB);
+            tma_load_3d(&s_g[0][0], &tm_dy, grp * kGroup, t0, b, &s_bar);
+            tma_load_3d(s_dyn + kRgBoxBytes, &tm_x, grp * kGroup, t0, b, &s_bar);
+            tma_load_3d(s_dyn + 2 * kRgBoxBytes, &tm_lx, grp * kGroup, t0, b, &s_bar);
+            tma_load_3d(s_dyn + 2 * kRgBoxBytes + LB, &tm_la, grp * kGroup, t0, b, &s_bar);
+        }
     }
     if (tid < kRgTile) {
         const int t = t0 + tid;
@@ -592,34 +622,103 @@ __global__ void __launch_bounds__(kRgThreads, 2)
             h1v = hv.y;
         }
     }
-    const bool landed = mbar_wait_bounded(&s_bar, 0);
-    if (!__syncthreads_and(landed)) {
+    bool ok = mbar_wait_bounded(&s_bar, 0);
+    if (!__syncthreads_and(ok)) {
         if (tid == 0) {
             st_release_gpu(fl + c, kFlagErr);
             atomicOr(a.status, kStatusTimeout);
+            mbar_wait_bounded(&s_bar, 0);
         }
-        mbar_wait_bounded(&s_bar, 0);
+        if (LM == 2) {
+            __syncthreads();
+            if (warp == 0) tmem_dealloc(tmem, 2 * kGroup);
+        }
         return;
+    }
+    if (LM == 2) {
+        // logits of the tile: D_gate[128 x 64] = x[128 x 64] . Wimg_gate[64 x 64]^T
+        if (tid == 0) {
+            tmem_fence_after_sync();
+            const uint32_t xa = smem_u32(s_dyn), wa = smem_u32(s_dyn + kBwdGxOff);
+#pragma unroll
+            for (int gt = 0; gt < 2; ++gt)
+#pragma unroll
+                for (int ks = 0; ks < kGroup / 16; ++ks)
+                    umma_bf16(tmem + (uint32_t)(gt * kGroup), umma_desc_sw128(xa + 32u * ks),
+                              umma_desc_sw128(wa + (uint32_t)(gt * kGroup * kGroup * 2) + 32u * ks), kIdesc, ks > 0);
+            umma_commit(&s_mma_bar);
+        }
+        ok = mbar_wait_bounded(&s_mma_bar, 0);
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) {
+                st_release_gpu(fl + c, kFlagErr);
+                atomicOr(a.status, kStatusTimeout);
+                mbar_wait_bounded(&s_mma_bar, 0);
+            }
+            __syncthreads();
+            if (warp == 0) {
+                tmem_fence_after_sync();
+                tmem_dealloc(tmem, 2 * kGroup);
+            }
+            return;
+        }
+        tmem_fence_after_sync();
     }
 
     // the lane's two channels as pairs (the same IEEE operations per element)
     const f2x nsp = pk2(nsp0, nsp1);
     f2x hp[kSub];   // h_{t-1} per token
     f2x hv = pk2(h0v, h1v), P = dup2(1.0f), q = 0ull;
+    if (LM == 2) {
+        // write gate: g^x kept for the reverse sweep, x g^x in hp[] until the keep gate is staged
+        rg_stage_gate(tmem, s_stage, 0, warp, lane);
+        __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kSub; ++i) {
-        hp[i] = 0ull;
-        if (i < nsub) {
-            const bool rs = s_rst[r0 + i] != 0;
-            const float2 xx = bf2_to_f2(s_x[r0 + i][lane]);
-            const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
-            const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
-            const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
-            const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
-            hp[i] = hv;
-            hv = fma2(gt.a, hv, mul2(mul2(pk2(xx.x, xx.y), gt.gx), gt.n));
-            P = mul2(P, gt.a);
-            q = fma2(P, pk2(gg.x, gg.y), q);
+        for (int i = 0; i < kSub; ++i) {
+            hp[i] = 0ull;
+            if (i < nsub) {
+                const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
+                const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
+                const f2x gx = sigmoid2(pk2(gl.x, gl.y));
+                float g0, g1;
+                up2(gx, g0, g1);
+                s_gx[(r0 + i) * 32 + lane] = make_float2(g0, g1);
+                hp[i] = mul2(pk2(xx.x, xx.y), gx);
+            }
+        }
+        __syncthreads();   // every warp has read the write gate before the keep gate replaces it
+        rg_stage_gate(tmem, s_stage, 1, warp, lane);
+        tmem_fence_before_sync();
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+            if (i < nsub) {
+                const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
+                const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
+                const RgGate2 kg = rg_keep_gate2(pk2(al.x, al.y), nsp, s_rst[r0 + i] != 0);
+                const f2x bt = mul2(hp[i], kg.n);
+                hp[i] = hv;
+                hv = fma2(kg.a, hv, bt);
+                P = mul2(P, kg.a);
+                q = fma2(P, pk2(gg.x, gg.y), q);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+            hp[i] = 0ull;
+            if (i < nsub) {
+                const bool rs = s_rst[r0 + i] != 0;
+                const float2 xx = rg_x<LM>(s_x, r0 + i, lane);
+                const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
+                const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
+                const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
+                const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+                hp[i] = hv;
+                hv = fma2(gt.a, hv, mul2(mul2(pk2(xx.x, xx.y), gt.gx), gt.n));
+                P = mul2(P, gt.a);
+                q = fma2(P, pk2(gg.x, gg.y), q);
+            }
         }
     }
     {
@@ -631,6 +730,10 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     // the next tile's flag, read while the other warps finish their maps
     const uint32_t pflag = (warp == 0 && lane == 0 && c < CT - 1) ? ld_acquire_gpu(fl + c + 1) : 0u;
     __syncthreads();
+    if (LM == 2 && warp == 0) {   // the tile's tensor memory is no longer read
+        tmem_fence_after_sync();
+        tmem_dealloc(tmem, 2 * kGroup);
+    }
 
     if (warp == 0) {
         float4 A = s_map[kRgWarps - 1][lane];
@@ -716,11 +819,18 @@ __global__ void __launch_bounds__(kRgThreads, 2)
     for (int i = kSub - 1; i >= 0; --i) {
         if (i < nsub) {
             const bool rs = s_rst[r0 + i] != 0;
-            const float2 xf = bf2_to_f2(s_x[r0 + i][lane]);
-            const float2 gl = rg_logit<PL>(s_lx, r0 + i, lane, bxv);
-            const float2 al = rg_logit<PL>(s_la, r0 + i, lane, bav);
+            const float2 xf = rg_x<LM>(s_x, r0 + i, lane);
+            const float2 al = rg_logit<LM>(s_la, r0 + i, lane, bav);
             const float2 gg = bf2_to_f2(s_g[r0 + i][lane]);
-            const RgGate2 gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+            RgGate2 gt;
+            if (LM == 2) {
+                gt = rg_keep_gate2(pk2(al.x, al.y), nsp, rs);
+                const float2 gx = s_gx[(r0 + i) * 32 + lane];
+                gt.gx = pk2(gx.x, gx.y);
+            } else {
+                const float2 gl = rg_logit<LM>(s_lx, r0 + i, lane, bxv);
+                gt = rg_gate2(pk2(gl.x, gl.y), pk2(al.x, al.y), nsp, rs);
+            }
             const f2x xx = pk2(xf.x, xf.y);
             H = add2(H, pk2(gg.x, gg.y));
             const f2x Hxg = mul2(mul2(H, xx), gt.gx);
@@ -926,21 +1036,23 @@ cudaError_t launch_rglru_scan_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm
     return launch_fwd<0>(tm_x, tm_lx, tm_la, args, s);
 }
 
-template <bool PL>
+template <int LM>
 cudaError_t launch_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
                        const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s) {
-    const int smem = 2 * kRgBoxBytes + 2 * RgLogits<PL>::kBoxBytes;
-    cudaError_t e = cudaFuncSetAttribute(rglru_scan_bwd_kernel<PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // LM 2: a spare kilobyte for the 1024-byte alignment of the swizzled boxes
+    const int smem = LM == 2 ? kBwdFusedBytes + 1024 : 2 * kRgBoxBytes + 2 * RgLogits<LM>::kBoxBytes;
+    cudaError_t e = cudaFuncSetAttribute(rglru_scan_bwd_kernel<LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_bwd_kernel<PL><<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
+    rglru_scan_bwd_kernel<LM><<<(unsigned)args.g.n_tiles, kRgThreads, smem, s>>>(tm_dy, tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rglru_scan_bwd(const CUtensorMap& tm_dy, const CUtensorMap& tm_x, const CUtensorMap& tm_lx,
                                   const CUtensorMap& tm_la, const RglruScanBwdArgs& args, cudaStream_t s,
-                                  bool projected) {
-    return projected ? launch_bwd<true>(tm_dy, tm_x, tm_lx, tm_la, args, s)
-                     : launch_bwd<false>(tm_dy, tm_x, tm_lx, tm_la, args, s);
+                                  int logits) {
+    if (logits == 2) return launch_bwd<2>(tm_dy, tm_x, tm_lx, tm_la, args, s);
+    if (logits == 1) return launch_bwd<1>(tm_dy, tm_x, tm_lx, tm_la, args, s);
+    return launch_bwd<0>(tm_dy, tm_x, tm_lx, tm_la, args, s);
 }
 
 cudaError_t launch_rglru_alpha(const float* apart, float* apart2, float* dalpha, int rows, int D,

@@ -117,12 +117,23 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
+# The sources the SAMU step's kernels and their launches are built from: the
+# committed DRAM figures stay valid while these are unchanged.
+STEP_SOURCES = ("linear_recurrence_sequence_gb300/csrc/samu_scan.cu",
+                "linear_recurrence_sequence_gb300/csrc/samu_ctrl.cu",
+                "linear_recurrence_sequence_gb300/csrc/abi.cu",
+                "linear_recurrence_sequence_gb300/csrc/common.cuh",
+                "linear_recurrence_sequence_gb300/csrc/kernels.cuh",
+                "linear_recurrence_sequence_gb300/csrc/layout.cuh",
+                "linear_recurrence_sequence_gb300/csrc/tmap.cuh",
+                "include/samu.h")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "linear_recurrence_sequence_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), encoding="utf-8") as f:
-            h.update(name.encode())
+    for rel in STEP_SOURCES:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(os.path.basename(rel).encode())
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 

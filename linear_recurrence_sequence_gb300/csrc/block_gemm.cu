@@ -25,6 +25,13 @@
 // epilogue of one tile run under the MMAs of the next.  CTAs are persistent
 // over the tiles; every wait is bounded and an abort flag ends the other
 // roles after a failure.
+// Two-CTA clusters (MC): the two CTAs take the tiles of two consecutive row
+// blocks with the same columns (and token split) in lockstep; each loads its
+// own A slice and one half of the shared B slice, multicast into both CTAs'
+// stages, so the L2 delivers B once per pair.  A stage is refilled only after
+// the MMAs of both CTAs have read it (each issuer's commit arrives on both
+// CTAs' empty barriers).  A row block past the matrix (odd row-block count)
+// runs on zero-filled A and stores nothing.
 //
 // Fused epilogues (row t of the tile, columns n):
 //   store     C in BF16;
@@ -85,17 +92,18 @@ struct BgItem {
     int mt, nt, s, k0, k1;
 };
 
-__device__ __forceinline__ BgItem bg_item(const BlockGemmArgs& a, int w) {
+// Work item w of a CTA (MC: pair item w, row block 2 (w's row pair) + rank).
+__device__ __forceinline__ BgItem bg_item(const BlockGemmArgs& a, int w, bool mc, int rank) {
     BgItem it;
     if (a.layout == kBgTN) {
         it.s = w % a.splits;
         const int r = w / a.splits;
         it.nt = r % a.n_tiles;
-        it.mt = r / a.n_tiles;
+        it.mt = mc ? 2 * (r / a.n_tiles) + rank : r / a.n_tiles;
         it.k0 = (int)((long long)a.ksteps * it.s / a.splits);
         it.k1 = (int)((long long)a.ksteps * (it.s + 1) / a.splits);
     } else {
-        it.mt = w / a.n_tiles;
+        it.mt = mc ? 2 * (w / a.n_tiles) + rank : w / a.n_tiles;
         it.nt = w % a.n_tiles;
         it.s = 0;
         it.k0 = 0;
@@ -218,7 +226,7 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
     }
 }
 
-template <int LAYOUT, int EPI>
+template <int LAYOUT, int EPI, bool MC>
 __global__ void __launch_bounds__(kBgThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       BlockGemmArgs a) {
@@ -229,10 +237,16 @@ __global__ void __launch_bounds__(kBgThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bg_raw) + 1023u) & ~uintptr_t(1023));
 
+    const int rank = MC ? (int)cluster_ctarank() : 0;
+    constexpr uint16_t kPair = 0x3;
+    // MC: the CTA's pair items, the same sequence in both CTAs of the cluster
+    const int w0 = MC ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int wstep = MC ? (int)gridDim.x / 2 : (int)gridDim.x;
+    const int n_work = MC ? a.n_pairs : a.n_items;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kBgStages; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 1);
+            mbar_init(&s_empty[i], MC ? 2 : 1);   // MC: both CTAs' MMAs free a stage
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_acc[i], 1);
@@ -248,6 +262,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
     pdl_trigger();
     pdl_wait();
     __syncthreads();
+    if (MC) cluster_sync();   // both CTAs' barriers exist before either reaches the other's
     tmem_fence_after_sync();
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
@@ -260,8 +275,8 @@ __global__ void __launch_bounds__(kBgThreads, 1)
         // producer: every K step of every tile of this CTA, in order
         if (lane == 0) {
             uint32_t n = 0;   // stages issued
-            for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x) {
-                const BgItem it = bg_item(a, w);
+            for (int w = w0; w < n_work && !*abort_flag; w += wstep) {
+                const BgItem it = bg_item(a, w, MC, rank);
                 for (int ks = it.k0; ks < it.k1; ++ks, ++n) {
                     const int slot = (int)(n % kBgStages);
                     if (n >= (uint32_t)kBgStages &&
@@ -274,29 +289,39 @@ __global__ void __launch_bounds__(kBgThreads, 1)
                     uint8_t* sb = sa + kBgABytes;
                     const int k0 = kBgK * ks;
                     mbar_arrive_expect_tx(&s_full[slot], kBgStageBytes);
+                    // B: MC loads half of the slice (rank 0 the first, rank 1 the second) into both CTAs
+                    auto load_b = [&](int part, uint8_t* dst, int x, int y) {
+                        if (!MC)
+                            tma_load_2d(dst, &tm_b, x, y, &s_full[slot]);
+                        else if (part == rank)
+                            tma_load_2d_mc(dst, &tm_b, x, y, &s_full[slot], kPair);
+                    };
                     if (LAYOUT == kBgNT) {
                         tma_load_2d(sa, &tm_a, k0, it.mt * kBgM, &s_full[slot]);
                         const int r0 = EPI == kEpiGlu ? it.nt * (kBgN / 2) : it.nt * kBgN;
                         const int r1 = EPI == kEpiGlu ? a.F + r0 : r0 + kBgN / 2;
-                        tma_load_2d(sb, &tm_b, k0, r0, &s_full[slot]);
-                        tma_load_2d(sb + kBgBBytes / 2, &tm_b, k0, r1, &s_full[slot]);
+                        load_b(0, sb, k0, r0);
+                        load_b(1, sb + kBgBBytes / 2, k0, r1);
                     } else if (LAYOUT == kBgNN) {
                         tma_load_2d(sa, &tm_a, k0, it.mt * kBgM, &s_full[slot]);
 #pragma unroll
                         for (int j = 0; j < kBgN / 64; ++j)
-                            tma_load_2d(sb + (size_t)j * 8192, &tm_b, it.nt * kBgN + 64 * j, k0, &s_full[slot]);
+                            load_b(j / 2, sb + (size_t)j * 8192, it.nt * kBgN + 64 * j, k0);
                     } else {
                         tma_load_2d(sa, &tm_a, it.mt * kBgM, k0, &s_full[slot]);
                         tma_load_2d(sa + 8192, &tm_a, it.mt * kBgM + 64, k0, &s_full[slot]);
 #pragma unroll
                         for (int j = 0; j < kBgN / 64; ++j)
-                            tma_load_2d(sb + (size_t)j * 8192, &tm_b, it.nt * kBgN + 64 * j, k0, &s_full[slot]);
+                            load_b(j / 2, sb + (size_t)j * 8192, it.nt * kBgN + 64 * j, k0);
                     }
                 }
             }
-            // copies still in flight land before the CTA may exit
+            // copies still in flight land before the CTA may exit (MC: and the
+            // other CTA's MMAs have read this CTA's halves of the last stages)
             const uint32_t lo = n > (uint32_t)kBgStages ? n - kBgStages : 0;
             for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_full[j % kBgStages], (j / kBgStages) & 1u);
+            if (MC)
+                for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_empty[j % kBgStages], (j / kBgStages) & 1u);
         }
     } else if (warp == kBgIssuer) {
         // MMA issuer
@@ -304,8 +329,8 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             constexpr uint32_t idesc = umma_idesc_bf16(kBgM, kBgN) | (LAYOUT == kBgTN ? (1u << 15) : 0u) |
                                        (LAYOUT != kBgNT ? (1u << 16) : 0u);
             uint32_t n = 0, item = 0;
-            for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x, ++item) {
-                const BgItem it = bg_item(a, w);
+            for (int w = w0; w < n_work && !*abort_flag; w += wstep, ++item) {
+                const BgItem it = bg_item(a, w, MC, rank);
                 const uint32_t buf = item & 1u;
                 // the epilogue has drained this accumulator's previous tile
                 if (item >= 2 && !mbar_wait_bounded(&s_free[buf], ((item >> 1) - 1) & 1u)) {
@@ -334,7 +359,11 @@ __global__ void __launch_bounds__(kBgThreads, 1)
                                                             : umma_desc_sw128_mn(sb + 2048u * kk, 8192u);
                         umma_bf16(acc_t, da, db, idesc, accum);
                     }
-                    umma_commit(&s_empty[slot]);   // the stage is free once these MMAs have read it
+                    // the stage is free once these MMAs have read it (MC: in both CTAs)
+                    if (MC)
+                        umma_commit_mc(&s_empty[slot], kPair);
+                    else
+                        umma_commit(&s_empty[slot]);
                 }
                 if (!ok) break;
                 umma_commit(&s_acc[buf]);
@@ -346,8 +375,8 @@ __global__ void __launch_bounds__(kBgThreads, 1)
     } else {
         // epilogue warps 0-7: accumulator rows 32 (warp % 4) .. + 31, column half warp / 4
         uint32_t item = 0;
-        for (int w = blockIdx.x; w < a.n_items && !*abort_flag; w += gridDim.x, ++item) {
-            const BgItem it = bg_item(a, w);
+        for (int w = w0; w < n_work && !*abort_flag; w += wstep, ++item) {
+            const BgItem it = bg_item(a, w, MC, rank);
             const uint32_t buf = item & 1u;
             if (!mbar_wait_bounded(&s_acc[buf], (item >> 1) & 1u)) {
                 if (lane == 0) fail();
@@ -355,7 +384,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             }
             tmem_fence_after_sync();
             const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + buf * (uint32_t)kBgN;
-            bg_epilogue<EPI>(a, it, 32 * (warp & 3) + lane, taddr, warp >> 2);
+            if (it.mt < a.m_tiles) bg_epilogue<EPI>(a, it, 32 * (warp & 3) + lane, taddr, warp >> 2);
             tmem_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[buf]);
@@ -366,6 +395,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
         tmem_fence_after_sync();
         tmem_dealloc(tmem, kBgTmemCols);
     }
+    if (MC) cluster_sync();   // neither CTA leaves while the other may still use its stages
 }
 
 // Out[i] (i < n) = sum over p < parts of part[p * stride + i], in a fixed
@@ -426,14 +456,53 @@ int bg_sms() {
     return (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 1;
 }
 
+// Two-CTA clusters sharing the B slice, when there are row blocks to pair.
+template <int LAYOUT, int EPI, bool MC>
+cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s,
+                         bool pdl) {
+    auto* fn = block_gemm_kernel<LAYOUT, EPI, MC>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBgSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kBgThreads);
+    cfg.dynamicSmemBytes = kBgSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (MC) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    long long grid = bg_sms();
+    if (MC) {
+        // one cluster per pair item at most, as many as fit at once
+        cfg.gridDim = dim3(2);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess || clusters < 1) clusters = (int)(grid / 2);
+        if (clusters < 1) clusters = 1;
+        grid = 2LL * std::min<long long>(clusters, a.n_pairs);
+    } else if (grid > a.n_items) {
+        grid = a.n_items;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.numAttrs = na;
+    cfg.gridDim = dim3((unsigned)grid);
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, a);
+}
+
 template <int LAYOUT, int EPI>
 cudaError_t bg_launch(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(block_gemm_kernel<LAYOUT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBgSmem);
-    if (e != cudaSuccess) return e;
-    int grid = bg_sms();
-    if (grid > a.n_items) grid = a.n_items;
-    return launch_ex(block_gemm_kernel<LAYOUT, EPI>, (unsigned)grid, kBgThreads, kBgSmem, s, pdl, ta, tb, a);
+    if (a.m_tiles >= 2) return bg_launch_as<LAYOUT, EPI, true>(ta, tb, a, s, pdl);
+    return bg_launch_as<LAYOUT, EPI, false>(ta, tb, a, s, pdl);
 }
 
 }  // namespace
@@ -504,6 +573,7 @@ cudaError_t launch_block_gemm(const BlockGemmArgs& args_in, const void* A, const
         if (a.splits < 1) a.splits = 1;
     }
     a.n_items = a.m_tiles * a.n_tiles * a.splits;
+    a.n_pairs = (a.m_tiles + 1) / 2 * a.n_tiles * a.splits;
     if (a.n_items < 1) return cudaSuccess;
     switch (a.layout * 16 + a.epi) {
         case kBgNT * 16 + kEpiStore: return bg_launch<kBgNT, kEpiStore>(ta, tb, a, s, pdl);

@@ -491,6 +491,7 @@ struct BlockGemmArgs {
     int layout, epi;
     int M, N, K;                 // glu: N = F hidden units (the B rows f and F + f pair up)
     int m_tiles, n_tiles, splits, ksteps, n_items;   // filled by launch_block_gemm (splits: TN only, in)
+    int n_pairs;                 // filled: items of the two-CTA clusters (row-block pairs)
     uint16_t* out;  int ldo;     // BF16 output (store, resid: C; glu: q; glu_bwd: [da | db]; join_bwd: dy_mixer)
     const uint16_t* r; int ldr;  // resid: the residual added to C
     uint16_t* out2; int ld2;     // glu: [a | b]; join_bwd: dg (the gate half of [dg | dv])

@@ -120,12 +120,13 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
     const int c0 = half * (kBgN / 2), c1 = c0 + kBgN / 2;
     if (EPI == kEpiF32) {
         float* o = a.part + ((size_t)it.s * a.M + (size_t)t) * a.N + (size_t)it.nt * kBgN;
-        for (int c = c0; c < c1; c += 16) {
-            float v[16];
-            tmem_ld16(taddr + (uint32_t)c, v);
+        for (int c = c0; c < c1; c += 32) {
+            float v[2][16];
+            tmem_ld16x2(taddr + (uint32_t)c, taddr + (uint32_t)(c + 16), v[0], v[1]);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(o + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(o + c + j) =
+                    make_float4(v[j / 16][j % 16], v[j / 16][j % 16 + 1], v[j / 16][j % 16 + 2], v[j / 16][j % 16 + 3]);
         }
         return;
     }
@@ -134,8 +135,7 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
         const int f0 = it.nt * (kBgN / 2);
         for (int c = half * (kBgN / 4); c < (half + 1) * (kBgN / 4); c += 16) {
             float va[16], vb[16];
-            tmem_ld16(taddr + (uint32_t)c, va);
-            tmem_ld16(taddr + (uint32_t)(kBgN / 2 + c), vb);
+            tmem_ld16x2(taddr + (uint32_t)c, taddr + (uint32_t)(kBgN / 2 + c), va, vb);
             if (!ok) continue;
             float q[16];
 #pragma unroll
@@ -157,13 +157,13 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
     }
     const int n0 = it.nt * kBgN;
     if (EPI == kEpiStore) {
-        for (int c = c0; c < c1; c += 16) {
-            float v[16];
-            tmem_ld16(taddr + (uint32_t)c, v);
+        for (int c = c0; c < c1; c += 32) {
+            float v[2][16];
+            tmem_ld16x2(taddr + (uint32_t)c, taddr + (uint32_t)(c + 16), v[0], v[1]);
             if (!ok) continue;
             uint16_t* o = a.out + (size_t)t * a.ldo + n0 + c;
 #pragma unroll
-            for (int j = 0; j < 16; j += 8) *reinterpret_cast<uint4*>(o + j) = pack8(v + j);
+            for (int j = 0; j < 32; j += 8) *reinterpret_cast<uint4*>(o + j) = pack8(v[j / 16] + j % 16);
         }
         return;
     }
@@ -183,10 +183,12 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
                 if (EPI != kEpiResid) p1[j] = __ldg(reinterpret_cast<const uint4*>(s1) + j);
             }
         }
+        float vq[2][16];   // two groups of 16 accumulator columns per tensor-memory round trip
 #pragma unroll
         for (int q = 0; q < kChunk / 16; ++q) {
-            float v[16];
-            tmem_ld16(taddr + (uint32_t)(cc + 16 * q), v);
+            if ((q & 1) == 0)
+                tmem_ld16x2(taddr + (uint32_t)(cc + 16 * q), taddr + (uint32_t)(cc + 16 * q + 16), vq[0], vq[1]);
+            float* v = vq[q & 1];
             if (!ok) continue;
             const size_t col = (size_t)n + 16 * q;
 #pragma unroll
@@ -375,6 +377,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
     } else {
         // epilogue warps 0-7: accumulator rows 32 (warp % 4) .. + 31, column half warp / 4
         uint32_t item = 0;
+        const int row = 32 * (warp & 3) + lane;
         for (int w = w0; w < n_work && !*abort_flag; w += wstep, ++item) {
             const BgItem it = bg_item(a, w, MC, rank);
             const uint32_t buf = item & 1u;
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             }
             tmem_fence_after_sync();
             const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + buf * (uint32_t)kBgN;
-            if (it.mt < a.m_tiles) bg_epilogue<EPI>(a, it, 32 * (warp & 3) + lane, taddr, warp >> 2);
+            if (it.mt < a.m_tiles) bg_epilogue<EPI>(a, it, row, taddr, warp >> 2);
             tmem_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[buf]);

@@ -43,6 +43,7 @@
 //   join_bwd  C = dj: dy_mixer = dj GeLU(g), dg = dj y_mixer GeLU'(g) (BF16);
 //   f32       C in FP32 (dW partials).
 #include <algorithm>
+#include <atomic>
 
 #include <cudaTypedefs.h>
 
@@ -483,11 +484,19 @@ cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const Blo
     cfg.numAttrs = na;
     long long grid = bg_sms();
     if (MC) {
-        // one cluster per pair item at most, as many as fit at once
-        cfg.gridDim = dim3(2);
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess || clusters < 1) clusters = (int)(grid / 2);
-        if (clusters < 1) clusters = 1;
+        // one cluster per pair item at most, as many as fit at once (the
+        // occupancy query is slow next to a launch: asked once per device)
+        static std::atomic<int> cached[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+        int clusters = cached[dev].load(std::memory_order_relaxed);
+        if (clusters < 1) {
+            cfg.gridDim = dim3(2);
+            if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess || clusters < 1)
+                clusters = (int)(grid / 2);
+            if (clusters < 1) clusters = 1;
+            cached[dev].store(clusters, std::memory_order_relaxed);
+        }
         grid = 2LL * std::min<long long>(clusters, a.n_pairs);
     } else if (grid > a.n_items) {
         grid = a.n_items;

@@ -62,12 +62,27 @@ constexpr int kBgProducer = kBgEpiWarps, kBgIssuer = kBgEpiWarps + 1;
 constexpr int kBgK = 64;          // K per stage (one 128-byte swizzle row of BF16)
 constexpr int kBgM = 128;         // tile rows
 constexpr int kBgN = 256;         // tile columns (accumulator columns)
-constexpr int kBgStages = 4;
+constexpr int kBgStages = 4;      // ring stages (3 for the epilogues with operands)
 constexpr uint32_t kBgABytes = kBgM * 128;            // 16 KB
 constexpr uint32_t kBgBBytes = kBgN * 128;            // 32 KB
 constexpr uint32_t kBgStageBytes = kBgABytes + kBgBBytes;
-constexpr size_t kBgSmem = (size_t)kBgStages * kBgStageBytes + 1024 + 16 * 1024;   // + alignment and slack
 constexpr uint32_t kBgTmemCols = 2 * kBgN;           // two accumulators
+// Epilogues that read operands of their own (residual, GLU backward, join
+// backward) take them by TMA into shared memory: per epilogue warp two slots,
+// each one 32-column group of its 32 rows per operand ([32][32] BF16 boxes,
+// 64-byte swizzle), filled two groups ahead.  With two operands the ring gives
+// up a stage for them; the residual's one operand fits beside four stages.
+__host__ __device__ constexpr bool bg_op_epi(int epi) {
+    return epi == kEpiResid || epi == kEpiGluBwd || epi == kEpiJoinBwd;
+}
+__host__ __device__ constexpr int bg_op_count(int epi) { return !bg_op_epi(epi) ? 0 : epi == kEpiResid ? 1 : 2; }
+__host__ __device__ constexpr int bg_stages(int epi) { return bg_op_count(epi) == 2 ? kBgStages - 1 : kBgStages; }
+constexpr int kBgOpCols = 32;
+constexpr uint32_t kBgOpBox = 32 * kBgOpCols * 2;     // 2 KB
+__host__ __device__ constexpr uint32_t bg_op_slot(int epi) { return (uint32_t)bg_op_count(epi) * kBgOpBox; }
+constexpr size_t bg_smem(int epi) {   // + 1 KB for the 1024-byte alignment
+    return (size_t)bg_stages(epi) * kBgStageBytes + (size_t)kBgEpiWarps * 2 * bg_op_slot(epi) + 1024;
+}
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -232,9 +247,13 @@ __device__ __forceinline__ void bg_epilogue(const BlockGemmArgs& a, const BgItem
 template <int LAYOUT, int EPI, bool MC>
 __global__ void __launch_bounds__(kBgThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_e0, const __grid_constant__ CUtensorMap tm_e1,
                       BlockGemmArgs a) {
+    constexpr int S = bg_stages(EPI);
+    constexpr bool OP = bg_op_epi(EPI);
     extern __shared__ uint8_t bg_raw[];
     __shared__ __align__(8) uint64_t s_full[kBgStages], s_empty[kBgStages], s_acc[2], s_free[2], s_fin;
+    __shared__ __align__(8) uint64_t s_op[kBgEpiWarps][2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -247,10 +266,15 @@ __global__ void __launch_bounds__(kBgThreads, 1)
     const int wstep = MC ? (int)gridDim.x / 2 : (int)gridDim.x;
     const int n_work = MC ? a.n_pairs : a.n_items;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kBgStages; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], MC ? 2 : 1);   // MC: both CTAs' MMAs free a stage
         }
+        if (OP)
+            for (int i = 0; i < kBgEpiWarps; ++i) {
+                mbar_init(&s_op[i][0], 1);
+                mbar_init(&s_op[i][1], 1);
+            }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_acc[i], 1);
             mbar_init(&s_free[i], kBgEpiWarps);
@@ -281,9 +305,8 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             for (int w = w0; w < n_work && !*abort_flag; w += wstep) {
                 const BgItem it = bg_item(a, w, MC, rank);
                 for (int ks = it.k0; ks < it.k1; ++ks, ++n) {
-                    const int slot = (int)(n % kBgStages);
-                    if (n >= (uint32_t)kBgStages &&
-                        !mbar_wait_bounded(&s_empty[slot], ((n / kBgStages) - 1) & 1u)) {
+                    const int slot = (int)(n % S);
+                    if (n >= (uint32_t)S && !mbar_wait_bounded(&s_empty[slot], ((n / S) - 1) & 1u)) {
                         fail();
                         break;
                     }
@@ -321,10 +344,10 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             }
             // copies still in flight land before the CTA may exit (MC: and the
             // other CTA's MMAs have read this CTA's halves of the last stages)
-            const uint32_t lo = n > (uint32_t)kBgStages ? n - kBgStages : 0;
-            for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_full[j % kBgStages], (j / kBgStages) & 1u);
+            const uint32_t lo = n > (uint32_t)S ? n - S : 0;
+            for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_full[j % S], (j / S) & 1u);
             if (MC)
-                for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_empty[j % kBgStages], (j / kBgStages) & 1u);
+                for (uint32_t j = lo; j < n; ++j) mbar_wait_bounded(&s_empty[j % S], (j / S) & 1u);
         }
     } else if (warp == kBgIssuer) {
         // MMA issuer
@@ -344,8 +367,8 @@ __global__ void __launch_bounds__(kBgThreads, 1)
                 const uint32_t acc_t = tmem + buf * (uint32_t)kBgN;
                 bool ok = true;
                 for (int ks = it.k0; ks < it.k1; ++ks, ++n) {
-                    const int slot = (int)(n % kBgStages);
-                    if (!mbar_wait_bounded(&s_full[slot], (n / kBgStages) & 1u)) {
+                    const int slot = (int)(n % S);
+                    if (!mbar_wait_bounded(&s_full[slot], (n / S) & 1u)) {
                         fail();
                         ok = false;
                         break;
@@ -375,6 +398,112 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             umma_commit(&s_fin);
             mbar_wait_bounded(&s_fin, 0);
         }
+    } else if (OP) {
+        // epilogue warps 0-7 with operands: rows 32 (warp % 4) .. + 31, column half warp / 4,
+        // in groups of 32 columns whose operand rows arrive by TMA two groups ahead
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int row = 32 * q4 + lane;
+        constexpr uint32_t kSlot = bg_op_slot(EPI);
+        uint8_t* ops = ring + (size_t)S * kBgStageBytes + (size_t)warp * 2 * kSlot;
+        constexpr int kG = (kBgN / 2) / kBgOpCols;   // groups per tile
+        const uint32_t n_groups = w0 < n_work ? (uint32_t)((n_work - 1 - w0) / wstep + 1) * kG : 0u;
+        uint32_t issued = 0;   // lane 0: groups asked for
+        auto issue = [&]() {
+            const uint32_t gi = issued++;
+            const int slot = (int)(gi & 1u);
+            const BgItem ig = bg_item(a, w0 + (int)(gi / kG) * wstep, MC, rank);
+            const int x = ig.nt * kBgN + hf * (kBgN / 2) + (int)(gi % kG) * kBgOpCols;
+            const int y = ig.mt * kBgM + 32 * q4;
+            uint8_t* dst = ops + (size_t)slot * kSlot;
+            fence_proxy_async();   // the slot's earlier reads (the warp's, before __syncwarp) come first
+            mbar_arrive_expect_tx(&s_op[warp][slot], kSlot);
+            tma_load_2d(dst, &tm_e0, x, y, &s_op[warp][slot]);
+            if (EPI == kEpiGluBwd) tma_load_2d(dst + kBgOpBox, &tm_e0, a.F + x, y, &s_op[warp][slot]);
+            if (EPI == kEpiJoinBwd) tma_load_2d(dst + kBgOpBox, &tm_e1, x, y, &s_op[warp][slot]);
+        };
+        if (lane == 0)
+            while (issued < n_groups && issued < 2u) issue();
+        uint32_t item = 0, g = 0;   // g: groups consumed
+        for (int w = w0; w < n_work && !*abort_flag; w += wstep, ++item) {
+            const BgItem it = bg_item(a, w, MC, rank);
+            const uint32_t buf = item & 1u;
+            if (!mbar_wait_bounded(&s_acc[buf], (item >> 1) & 1u)) {
+                if (lane == 0) fail();
+                break;
+            }
+            tmem_fence_after_sync();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + buf * (uint32_t)kBgN;
+            const long long t = (long long)it.mt * kBgM + row;
+            const bool ok = it.mt < a.m_tiles && t < a.M;
+            bool lost = false;
+            for (int k = 0; k < kG; ++k, ++g) {
+                const int slot = (int)(g & 1u);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_op[warp][slot], (g >> 1) & 1u))) {
+                    lost = true;
+                    break;
+                }
+                const int c = hf * (kBgN / 2) + k * kBgOpCols;   // the group's first column in the tile
+                float v[2][16];
+                tmem_ld16x2(taddr + (uint32_t)c, taddr + (uint32_t)(c + 16), v[0], v[1]);
+                // this row's operands: four 16-byte units of 64 bytes, the unit index
+                // XOR-ed with bits 1-2 of the row (the 64-byte swizzle)
+                const uint8_t* src = ops + (size_t)slot * kSlot + (size_t)lane * 64;
+                uint4 o0[4], o1[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int pu = u ^ ((lane >> 1) & 3);
+                    o0[u] = *reinterpret_cast<const uint4*>(src + 16 * pu);
+                    if (EPI != kEpiResid) o1[u] = *reinterpret_cast<const uint4*>(src + kBgOpBox + 16 * pu);
+                }
+                __syncwarp();
+                if (lane == 0 && issued < n_groups) issue();
+                if (!ok) continue;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const size_t col = (size_t)it.nt * kBgN + c + 8 * u;
+                    float x0[8], x1[8], r0[8], r1[8];
+                    unpack8(o0[u], x0);
+                    if (EPI != kEpiResid) unpack8(o1[u], x1);
+                    const float* vv = v[u >> 1] + 8 * (u & 1);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (EPI == kEpiResid) {
+                            r0[i] = vv[i] + x0[i];
+                        } else if (EPI == kEpiGluBwd) {   // x0 = a, x1 = b: da, db
+                            float gg, dg;
+                            gelu_fwd_grad(x0[i], gg, dg);
+                            r0[i] = vv[i] * x1[i] * dg;
+                            r1[i] = vv[i] * gg;
+                        } else {                          // x0 = g, x1 = y_mixer: d y_mixer, dg
+                            float gg, dg;
+                            gelu_fwd_grad(x0[i], gg, dg);
+                            r0[i] = vv[i] * gg;
+                            r1[i] = vv[i] * x1[i] * dg;
+                        }
+                    }
+                    if (EPI == kEpiResid) {
+                        *reinterpret_cast<uint4*>(a.out + (size_t)t * a.ldo + col) = pack8(r0);
+                    } else if (EPI == kEpiGluBwd) {
+                        uint16_t* o = a.out + (size_t)t * a.ldo + col;   // da at f, db at F + f
+                        *reinterpret_cast<uint4*>(o) = pack8(r0);
+                        *reinterpret_cast<uint4*>(o + a.F) = pack8(r1);
+                    } else {
+                        *reinterpret_cast<uint4*>(a.out + (size_t)t * a.ldo + col) = pack8(r0);
+                        *reinterpret_cast<uint4*>(a.out2 + (size_t)t * a.ld2 + col) = pack8(r1);
+                    }
+                }
+            }
+            if (lost) {
+                if (lane == 0) fail();
+                break;
+            }
+            tmem_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[buf]);
+        }
+        // operand groups still in flight land before the CTA may exit
+        if (lane == 0)
+            for (uint32_t j = g; j < issued; ++j) mbar_wait_bounded(&s_op[warp][j & 1u], (j >> 1) & 1u);
     } else {
         // epilogue warps 0-7: accumulator rows 32 (warp % 4) .. + 31, column half warp / 4
         uint32_t item = 0;
@@ -462,14 +591,15 @@ int bg_sms() {
 
 // Two-CTA clusters sharing the B slice, when there are row blocks to pair.
 template <int LAYOUT, int EPI, bool MC>
-cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s,
-                         bool pdl) {
+cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& te0, const CUtensorMap& te1,
+                         const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
     auto* fn = block_gemm_kernel<LAYOUT, EPI, MC>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBgSmem);
+    constexpr size_t smem = bg_smem(EPI);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kBgThreads);
-    cfg.dynamicSmemBytes = kBgSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -508,13 +638,37 @@ cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const Blo
     }
     cfg.numAttrs = na;
     cfg.gridDim = dim3((unsigned)grid);
-    return cudaLaunchKernelEx(&cfg, fn, ta, tb, a);
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, te0, te1, a);
+}
+
+// The epilogue operands' tensor maps: [rows][cols] BF16 with row stride ld,
+// box 32 x 32, 64-byte swizzle (rows past the matrix read as zero).
+bool bg_op_map(CUtensorMap* map, const void* ptr, long long cols, long long rows, long long ld) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBgOpCols, 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 template <int LAYOUT, int EPI>
 cudaError_t bg_launch(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
-    if (a.m_tiles >= 2) return bg_launch_as<LAYOUT, EPI, true>(ta, tb, a, s, pdl);
-    return bg_launch_as<LAYOUT, EPI, false>(ta, tb, a, s, pdl);
+    CUtensorMap te0 = ta, te1 = ta;
+    if (EPI == kEpiResid) {
+        if (!bg_op_map(&te0, a.r, a.N, a.M, a.ldr)) return cudaErrorInvalidValue;
+    } else if (EPI == kEpiGluBwd) {   // [a | b]: a at column f, b at F + f
+        if (!bg_op_map(&te0, a.e0, 2LL * a.F, a.M, a.lde0)) return cudaErrorInvalidValue;
+    } else if (EPI == kEpiJoinBwd) {  // g: the first N columns of [g | v]; y_mixer
+        if (!bg_op_map(&te0, a.e0, a.N, a.M, a.lde0) || !bg_op_map(&te1, a.e1, a.N, a.M, a.lde1))
+            return cudaErrorInvalidValue;
+    }
+    if (a.m_tiles >= 2) return bg_launch_as<LAYOUT, EPI, true>(ta, tb, te0, te1, a, s, pdl);
+    return bg_launch_as<LAYOUT, EPI, false>(ta, tb, te0, te1, a, s, pdl);
 }
 
 }  // namespace

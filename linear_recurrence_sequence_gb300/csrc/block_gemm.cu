@@ -80,8 +80,13 @@ __host__ __device__ constexpr int bg_stages(int epi) { return bg_op_count(epi) =
 constexpr int kBgOpCols = 32;
 constexpr uint32_t kBgOpBox = 32 * kBgOpCols * 2;     // 2 KB
 __host__ __device__ constexpr uint32_t bg_op_slot(int epi) { return (uint32_t)bg_op_count(epi) * kBgOpBox; }
+// The GLU epilogue writes a, b and q by TMA stores from per-warp staging:
+// [32 rows][16 columns] BF16 boxes (32-byte swizzle), one of each.
+constexpr uint32_t kBgStBox = 32 * 16 * 2;            // 1 KB
+__host__ __device__ constexpr uint32_t bg_st_warp(int epi) { return epi == kEpiGlu ? 3 * kBgStBox : 0u; }
 constexpr size_t bg_smem(int epi) {   // + 1 KB for the 1024-byte alignment
-    return (size_t)bg_stages(epi) * kBgStageBytes + (size_t)kBgEpiWarps * 2 * bg_op_slot(epi) + 1024;
+    return (size_t)bg_stages(epi) * kBgStageBytes + (size_t)kBgEpiWarps * (2 * bg_op_slot(epi) + bg_st_warp(epi)) +
+           1024;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -504,6 +509,61 @@ __global__ void __launch_bounds__(kBgThreads, 1)
         // operand groups still in flight land before the CTA may exit
         if (lane == 0)
             for (uint32_t j = g; j < issued; ++j) mbar_wait_bounded(&s_op[warp][j & 1u], (j >> 1) & 1u);
+    } else if (EPI == kEpiGlu) {
+        // epilogue warps 0-7 of the GLU: rows 32 (warp % 4) .. + 31, hidden units of column
+        // half warp / 4, 16 at a time; a, b and q leave by TMA stores (tm_e0: [a | b], tm_e1: q)
+        const int q4 = warp & 3, hf = warp >> 2;
+        uint8_t* stg = ring + (size_t)S * kBgStageBytes + (size_t)warp * bg_st_warp(EPI);
+        bool pending = false;   // lane 0: stores committed whose staging reads may be in flight
+        uint32_t item = 0;
+        for (int w = w0; w < n_work && !*abort_flag; w += wstep, ++item) {
+            const BgItem it = bg_item(a, w, MC, rank);
+            const uint32_t buf = item & 1u;
+            if (!mbar_wait_bounded(&s_acc[buf], (item >> 1) & 1u)) {
+                if (lane == 0) fail();
+                break;
+            }
+            tmem_fence_after_sync();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + buf * (uint32_t)kBgN;
+            const int f0 = it.nt * (kBgN / 2);
+            const int y = it.mt * kBgM + 32 * q4;
+            const bool store = it.mt < a.m_tiles && y < a.M;   // rows past M are clipped by the TMA
+#pragma unroll 1
+            for (int c = hf * (kBgN / 4); c < (hf + 1) * (kBgN / 4); c += 16) {
+                float va[16], vb[16];
+                tmem_ld16x2(taddr + (uint32_t)c, taddr + (uint32_t)(kBgN / 2 + c), va, vb);
+                float q[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    va[j] = bf_round(va[j]);
+                    vb[j] = bf_round(vb[j]);
+                    q[j] = gelu_fwd(va[j]) * vb[j];
+                }
+                if (lane == 0 && pending) bulk_wait_read<0>();   // the staging is free again
+                __syncwarp();
+                // row `lane` of each box: 32 bytes, the 16-byte unit u at u ^ bit 2 of the row
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t off = (uint32_t)lane * 32u + 16u * (uint32_t)(u ^ ((lane >> 2) & 1));
+                    *reinterpret_cast<uint4*>(stg + off) = pack8(va + 8 * u);
+                    *reinterpret_cast<uint4*>(stg + kBgStBox + off) = pack8(vb + 8 * u);
+                    *reinterpret_cast<uint4*>(stg + 2 * kBgStBox + off) = pack8(q + 8 * u);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0 && store) {
+                    tma_store_2d(&tm_e0, f0 + c, y, stg);
+                    tma_store_2d(&tm_e0, a.F + f0 + c, y, stg + kBgStBox);
+                    tma_store_2d(&tm_e1, f0 + c, y, stg + 2 * kBgStBox);
+                    bulk_commit();
+                    pending = true;
+                }
+            }
+            tmem_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[buf]);
+        }
+        if (lane == 0) bulk_wait_all();   // every store has completed before the CTA may exit
     } else {
         // epilogue warps 0-7: accumulator rows 32 (warp % 4) .. + 31, column half warp / 4
         uint32_t item = 0;
@@ -656,10 +716,28 @@ bool bg_op_map(CUtensorMap* map, const void* ptr, long long cols, long long rows
     return r == CUDA_SUCCESS;
 }
 
+// The GLU's output maps: [rows][cols] BF16 with row stride ld, box 16 x 32,
+// 32-byte swizzle (rows past the matrix are not written).
+bool bg_st_map(CUtensorMap* map, const void* ptr, long long cols, long long rows, long long ld) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int LAYOUT, int EPI>
 cudaError_t bg_launch(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
     CUtensorMap te0 = ta, te1 = ta;
-    if (EPI == kEpiResid) {
+    if (EPI == kEpiGlu) {   // stores: [a | b] and q, box 16 x 32, 32-byte swizzle
+        if (!bg_st_map(&te0, a.out2, 2LL * a.F, a.M, a.ld2) || !bg_st_map(&te1, a.out, a.F, a.M, a.ldo))
+            return cudaErrorInvalidValue;
+    } else if (EPI == kEpiResid) {
         if (!bg_op_map(&te0, a.r, a.N, a.M, a.ldr)) return cudaErrorInvalidValue;
     } else if (EPI == kEpiGluBwd) {   // [a | b]: a at column f, b at F + f
         if (!bg_op_map(&te0, a.e0, 2LL * a.F, a.M, a.lde0)) return cudaErrorInvalidValue;

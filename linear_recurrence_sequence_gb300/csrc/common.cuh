@@ -163,6 +163,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int 
                  "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
                  : "memory");
 }
+// 2-D tiled tensor store of one box from shared memory, the same rules.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until at most N committed bulk groups still read shared memory.
 template <int N>

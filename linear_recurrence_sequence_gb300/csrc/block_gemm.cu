@@ -83,7 +83,11 @@ __host__ __device__ constexpr uint32_t bg_op_slot(int epi) { return (uint32_t)bg
 // The GLU epilogue writes a, b and q by TMA stores from per-warp staging:
 // [32 rows][16 columns] BF16 boxes (32-byte swizzle), one of each.
 constexpr uint32_t kBgStBox = 32 * 16 * 2;            // 1 KB
-__host__ __device__ constexpr uint32_t bg_st_warp(int epi) { return epi == kEpiGlu ? 3 * kBgStBox : 0u; }
+// The plain store's staging: two [32 rows][32 columns] BF16 boxes (64-byte
+// swizzle) per warp, alternating.
+__host__ __device__ constexpr uint32_t bg_st_warp(int epi) {
+    return epi == kEpiGlu ? 3 * kBgStBox : epi == kEpiStore ? 2 * kBgOpBox : 0u;
+}
 constexpr size_t bg_smem(int epi) {   // + 1 KB for the 1024-byte alignment
     return (size_t)bg_stages(epi) * kBgStageBytes + (size_t)kBgEpiWarps * (2 * bg_op_slot(epi) + bg_st_warp(epi)) +
            1024;
@@ -253,6 +257,7 @@ template <int LAYOUT, int EPI, bool MC>
 __global__ void __launch_bounds__(kBgThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_e0, const __grid_constant__ CUtensorMap tm_e1,
+                      const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
                       BlockGemmArgs a) {
     constexpr int S = bg_stages(EPI);
     constexpr bool OP = bg_op_epi(EPI);
@@ -407,7 +412,6 @@ __global__ void __launch_bounds__(kBgThreads, 1)
         // epilogue warps 0-7 with operands: rows 32 (warp % 4) .. + 31, column half warp / 4,
         // in groups of 32 columns whose operand rows arrive by TMA two groups ahead
         const int q4 = warp & 3, hf = warp >> 2;
-        const int row = 32 * q4 + lane;
         constexpr uint32_t kSlot = bg_op_slot(EPI);
         uint8_t* ops = ring + (size_t)S * kBgStageBytes + (size_t)warp * 2 * kSlot;
         constexpr int kG = (kBgN / 2) / kBgOpCols;   // groups per tile
@@ -438,8 +442,6 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             }
             tmem_fence_after_sync();
             const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + buf * (uint32_t)kBgN;
-            const long long t = (long long)it.mt * kBgM + row;
-            const bool ok = it.mt < a.m_tiles && t < a.M;
             bool lost = false;
             for (int k = 0; k < kG; ++k, ++g) {
                 const int slot = (int)(g & 1u);
@@ -460,12 +462,12 @@ __global__ void __launch_bounds__(kBgThreads, 1)
                     o0[u] = *reinterpret_cast<const uint4*>(src + 16 * pu);
                     if (EPI != kEpiResid) o1[u] = *reinterpret_cast<const uint4*>(src + kBgOpBox + 16 * pu);
                 }
-                __syncwarp();
-                if (lane == 0 && issued < n_groups) issue();
-                if (!ok) continue;
+                // the group's results, staged in the slot its operands came in and
+                // stored by TMA (rows past M are clipped; a row block past the matrix
+                // stores nothing), before the slot takes group g + 2
+                uint4 w0[4], w1[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const size_t col = (size_t)it.nt * kBgN + c + 8 * u;
                     float x0[8], x1[8], r0[8], r1[8];
                     unpack8(o0[u], x0);
                     if (EPI != kEpiResid) unpack8(o1[u], x1);
@@ -486,16 +488,30 @@ __global__ void __launch_bounds__(kBgThreads, 1)
                             r1[i] = vv[i] * x1[i] * dg;
                         }
                     }
-                    if (EPI == kEpiResid) {
-                        *reinterpret_cast<uint4*>(a.out + (size_t)t * a.ldo + col) = pack8(r0);
-                    } else if (EPI == kEpiGluBwd) {
-                        uint16_t* o = a.out + (size_t)t * a.ldo + col;   // da at f, db at F + f
-                        *reinterpret_cast<uint4*>(o) = pack8(r0);
-                        *reinterpret_cast<uint4*>(o + a.F) = pack8(r1);
-                    } else {
-                        *reinterpret_cast<uint4*>(a.out + (size_t)t * a.ldo + col) = pack8(r0);
-                        *reinterpret_cast<uint4*>(a.out2 + (size_t)t * a.ld2 + col) = pack8(r1);
+                    w0[u] = pack8(r0);
+                    if (EPI != kEpiResid) w1[u] = pack8(r1);
+                }
+                __syncwarp();   // every lane has read its operands from the slot
+                uint8_t* box = ops + (size_t)slot * kSlot;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int pu = u ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4*>(box + (size_t)lane * 64 + 16 * pu) = w0[u];
+                    if (EPI != kEpiResid) *reinterpret_cast<uint4*>(box + kBgOpBox + (size_t)lane * 64 + 16 * pu) = w1[u];
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    if (it.mt < a.m_tiles && it.mt * kBgM + 32 * q4 < a.M) {
+                        const int x = it.nt * kBgN + c;
+                        // resid: out; glu_bwd: da at f, db at F + f of [da | db]; join_bwd: d y_mixer, dg
+                        tma_store_2d(&tm_s0, x, it.mt * kBgM + 32 * q4, box);
+                        if (EPI == kEpiGluBwd) tma_store_2d(&tm_s0, a.F + x, it.mt * kBgM + 32 * q4, box + kBgOpBox);
+                        if (EPI == kEpiJoinBwd) tma_store_2d(&tm_s1, x, it.mt * kBgM + 32 * q4, box + kBgOpBox);
+                        bulk_commit();
+                        bulk_wait_read<0>();   // the slot is read out before it takes the next group
                     }
+                    if (issued < n_groups) issue();
                 }
             }
             if (lost) {
@@ -506,9 +522,52 @@ __global__ void __launch_bounds__(kBgThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[buf]);
         }
-        // operand groups still in flight land before the CTA may exit
-        if (lane == 0)
+        // operand groups still in flight land, and the stores complete, before the CTA may exit
+        if (lane == 0) {
             for (uint32_t j = g; j < issued; ++j) mbar_wait_bounded(&s_op[warp][j & 1u], (j >> 1) & 1u);
+            bulk_wait_all();
+        }
+    } else if (EPI == kEpiStore) {
+        // epilogue warps 0-7 of the plain store: rows 32 (warp % 4) .. + 31, column half
+        // warp / 4, 32 columns at a time staged in two alternating boxes and stored by TMA
+        const int q4 = warp & 3, hf = warp >> 2;
+        uint8_t* stg = ring + (size_t)S * kBgStageBytes + (size_t)warp * bg_st_warp(EPI);
+        uint32_t chunk = 0, item = 0;   // every chunk commits one bulk group (empty when nothing is stored)
+        for (int w = w0; w < n_work && !*abort_flag; w += wstep, ++item) {
+            const BgItem it = bg_item(a, w, MC, rank);
+            const uint32_t buf = item & 1u;
+            if (!mbar_wait_bounded(&s_acc[buf], (item >> 1) & 1u)) {
+                if (lane == 0) fail();
+                break;
+            }
+            tmem_fence_after_sync();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + buf * (uint32_t)kBgN;
+            const int y = it.mt * kBgM + 32 * q4;
+            const bool store = it.mt < a.m_tiles && y < a.M;   // rows past M are clipped by the TMA
+#pragma unroll 1
+            for (int c = hf * (kBgN / 2); c < (hf + 1) * (kBgN / 2); c += 32, ++chunk) {
+                float v[2][16];
+                tmem_ld16x2(taddr + (uint32_t)c, taddr + (uint32_t)(c + 16), v[0], v[1]);
+                uint8_t* box = stg + (size_t)(chunk & 1u) * kBgOpBox;
+                if (lane == 0 && chunk >= 2) bulk_wait_read<1>();   // the box of two chunks ago is read out
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int pu = u ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4*>(box + (size_t)lane * 64 + 16 * pu) = pack8(v[u >> 1] + 8 * (u & 1));
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    if (store) tma_store_2d(&tm_s0, it.nt * kBgN + c, y, box);
+                    bulk_commit();
+                }
+            }
+            tmem_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[buf]);
+        }
+        if (lane == 0) bulk_wait_all();   // every store has completed before the CTA may exit
     } else if (EPI == kEpiGlu) {
         // epilogue warps 0-7 of the GLU: rows 32 (warp % 4) .. + 31, hidden units of column
         // half warp / 4, 16 at a time; a, b and q leave by TMA stores (tm_e0: [a | b], tm_e1: q)
@@ -684,7 +743,8 @@ int bg_sms() {
 // Two-CTA clusters sharing the B slice, when there are row blocks to pair.
 template <int LAYOUT, int EPI, bool MC>
 cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& te0, const CUtensorMap& te1,
-                         const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
+                         const CUtensorMap& ts0, const CUtensorMap& ts1, const BlockGemmArgs& a, cudaStream_t s,
+                         bool pdl) {
     auto* fn = block_gemm_kernel<LAYOUT, EPI, MC>;
     constexpr size_t smem = bg_smem(EPI);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -730,7 +790,7 @@ cudaError_t bg_launch_as(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
     }
     cfg.numAttrs = na;
     cfg.gridDim = dim3((unsigned)grid);
-    return cudaLaunchKernelEx(&cfg, fn, ta, tb, te0, te1, a);
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, te0, te1, ts0, ts1, a);
 }
 
 // The epilogue operands' tensor maps: [rows][cols] BF16 with row stride ld,
@@ -765,7 +825,15 @@ bool bg_st_map(CUtensorMap* map, const void* ptr, long long cols, long long rows
 
 template <int LAYOUT, int EPI>
 cudaError_t bg_launch(const CUtensorMap& ta, const CUtensorMap& tb, const BlockGemmArgs& a, cudaStream_t s, bool pdl) {
-    CUtensorMap te0 = ta, te1 = ta;
+    CUtensorMap te0 = ta, te1 = ta, ts0 = ta, ts1 = ta;
+    // stores of the plain, residual, GLU backward and join backward epilogues:
+    // box 32 x 32, 64-byte swizzle (rows past the matrix are not written)
+    if (EPI == kEpiStore || EPI == kEpiResid || EPI == kEpiJoinBwd) {
+        if (!bg_op_map(&ts0, a.out, a.N, a.M, a.ldo)) return cudaErrorInvalidValue;
+    } else if (EPI == kEpiGluBwd) {   // [da | db]
+        if (!bg_op_map(&ts0, a.out, 2LL * a.F, a.M, a.ldo)) return cudaErrorInvalidValue;
+    }
+    if (EPI == kEpiJoinBwd && !bg_op_map(&ts1, a.out2, a.N, a.M, a.ld2)) return cudaErrorInvalidValue;
     if (EPI == kEpiGlu) {   // stores: [a | b] and q, box 16 x 32, 32-byte swizzle
         if (!bg_st_map(&te0, a.out2, 2LL * a.F, a.M, a.ld2) || !bg_st_map(&te1, a.out, a.F, a.M, a.ldo))
             return cudaErrorInvalidValue;
@@ -777,8 +845,8 @@ cudaError_t bg_launch(const CUtensorMap& ta, const CUtensorMap& tb, const BlockG
         if (!bg_op_map(&te0, a.e0, a.N, a.M, a.lde0) || !bg_op_map(&te1, a.e1, a.N, a.M, a.lde1))
             return cudaErrorInvalidValue;
     }
-    if (a.m_tiles >= 2) return bg_launch_as<LAYOUT, EPI, true>(ta, tb, te0, te1, a, s, pdl);
-    return bg_launch_as<LAYOUT, EPI, false>(ta, tb, te0, te1, a, s, pdl);
+    if (a.m_tiles >= 2) return bg_launch_as<LAYOUT, EPI, true>(ta, tb, te0, te1, ts0, ts1, a, s, pdl);
+    return bg_launch_as<LAYOUT, EPI, false>(ta, tb, te0, te1, ts0, ts1, a, s, pdl);
 }
 
 }  // namespace

@@ -382,6 +382,7 @@ struct SamuDecodeStepArgs {
     const float* params;
     uint16_t* y;            // [B][D] BF16
     float* y32;             // [B][D] or null
+    int parts;              // CTAs per sequence (set by the launcher)
 };
 
 size_t samu_decode_params_floats(int D);

@@ -12,7 +12,11 @@
 //
 // GB300 organisation: one CTA of T threads per sequence (T = 128 for
 // D <= 1024, else 256, so that every thread owns one to four mode pairs; at
-// most 64 registers, so that 32 warps of it are resident per SM).
+// most 64 registers, so that 32 warps of it are resident per SM).  When the
+// batch alone would leave most SMs idle, P CTAs per sequence (a separate
+// instantiation): each forms the token's dot products and scalars in full
+// (the same operations, so the same bits) and updates every P-th group of T
+// mode pairs.
 // Thread t owns the 8-channel chunks t, t+T, ... of the token's x_sel row for
 // the two dot products (16-byte loads, paired FP32 arithmetic), reduced over
 // the CTA in a fixed order behind a CTA barrier; lane 0 of every warp then
@@ -23,6 +27,8 @@
 // move as 16-byte (state) and 4-byte (BF16 pairs) accesses, coalesced across
 // the CTA.  Bandwidth-bound: per sequence 2D (x_sel) + 2D (w) + 2D (y) + 8D
 // (state read and written) bytes.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace lrs {
@@ -93,14 +99,18 @@ __global__ void __launch_bounds__(kDecThreads) samu_decode_prepare_kernel(SamuDe
     }
 }
 
-// One token of sequence blockIdx.x, T threads.
-template <int T>
+// One token of sequence blockIdx.x, T threads (SPLIT: of sequence
+// blockIdx.x / P, part blockIdx.x % P of its modes).
+template <int T, bool SPLIT>
 __global__ void __launch_bounds__(T, 1024 / T) samu_decode_step_kernel(SamuDecodeStepArgs a) {
     constexpr int W = T / 32;
     __shared__ float2 s_red[W];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int D = a.D, M = D / 2, nch = D / 8;
-    const size_t b = blockIdx.x;
+    const size_t b = SPLIT ? blockIdx.x / (unsigned)a.parts : blockIdx.x;
+    // the first mode of the thread's pairs and the distance between them
+    const int m0 = SPLIT ? 2 * ((int)(blockIdx.x % (unsigned)a.parts) * T + tid) : 2 * tid;
+    const int mstep = SPLIT ? 2 * T * a.parts : 2 * T;
     const float* wh = a.params;
     const float* misc = a.params + dec_off_misc(D);
     const float* nu = a.params + dec_off_nu(D);
@@ -114,7 +124,7 @@ __global__ void __launch_bounds__(T, 1024 / T) samu_decode_step_kernel(SamuDecod
     uint32_t wre[kDecPairs], wim[kDecPairs];
 #pragma unroll
     for (int j = 0; j < kDecPairs; ++j) {
-        const int m = 2 * tid + j * 2 * T;
+        const int m = m0 + j * mstep;
         if (m < M) {
             zs[j] = __ldcs(reinterpret_cast<const float4*>(a.state_in + (b * M + m) * 2));   // re0, im0, re1, im1
             wre[j] = __ldcs(wrow + m / 2);
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(T, 1024 / T) samu_decode_step_kernel(SamuDecod
 
 #pragma unroll
     for (int j = 0; j < kDecPairs; ++j) {
-        const int m = 2 * tid + j * 2 * T;
+        const int m = m0 + j * mstep;
         if (m >= M) continue;
         const float4 z4 = zs[j];
         const f2x bre = bf2x(wre[j]), bim = bf2x(wim[j]);
@@ -228,12 +238,31 @@ cudaError_t launch_samu_decode_prepare(const SamuDecodePrepArgs& args, cudaStrea
     return cudaGetLastError();
 }
 
-cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t s) {
-    if (args.D <= 1024)
-        samu_decode_step_kernel<128><<<(unsigned)args.B, 128, 0, s>>>(args);
-    else
-        samu_decode_step_kernel<kDecThreads><<<(unsigned)args.B, kDecThreads, 0, s>>>(args);
+// CTAs per sequence: P >= 2 when B P still fits the CTAs resident at once
+// (at most the mode-pair groups of T, and 8); otherwise one.
+template <int T>
+cudaError_t launch_step(SamuDecodeStepArgs a, cudaStream_t s) {
+    int dev = 0, sms = 1, per = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, samu_decode_step_kernel<T, true>, T, 0) != cudaSuccess ||
+        per < 1)
+        per = 1;
+    const long long groups = (a.D / 4 + T - 1) / T;   // groups of T mode pairs
+    const long long P = std::min<long long>({a.B > 0 ? (long long)sms * per / a.B : 1LL, groups, 8LL});
+    if (P >= 2) {
+        a.parts = (int)P;
+        samu_decode_step_kernel<T, true><<<(unsigned)(a.B * P), T, 0, s>>>(a);
+    } else {
+        a.parts = 1;
+        samu_decode_step_kernel<T, false><<<(unsigned)a.B, T, 0, s>>>(a);
+    }
     return cudaGetLastError();
+}
+
+cudaError_t launch_samu_decode_step(const SamuDecodeStepArgs& args, cudaStream_t s) {
+    if (args.D <= 1024) return launch_step<128>(args, s);
+    return launch_step<kDecThreads>(args, s);
 }
 
 }  // namespace lrs

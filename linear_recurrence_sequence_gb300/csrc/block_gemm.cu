@@ -42,6 +42,10 @@
 //   glu_bwd   C = dq: da = dq b GeLU'(a), db = dq GeLU(a) (BF16);
 //   join_bwd  C = dj: dy_mixer = dj GeLU(g), dg = dj y_mixer GeLU'(g) (BF16);
 //   f32       C in FP32 (dW partials).
+// The BF16 results leave by TMA stores from swizzled per-warp staging; the
+// operands that resid, glu_bwd and join_bwd read come by TMA into per-warp
+// slots two 32-column groups ahead (their results are staged in the slot the
+// group's operands came in).  The f32 partials are stored by the threads.
 #include <algorithm>
 #include <atomic>
 

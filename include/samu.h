@@ -303,7 +303,9 @@ int rglru_proj_forward(const void* x, const void* w_x, const float* b_x, const v
                        void* y, float* y32, float* hT, void* saved, void* scratch, cudaStream_t stream);
 
 /* Backward of rglru_proj_forward: the scan backward with the logits
- * recomputed, then dx = dx_scan + dlx W_x^T + dla W_a^T per block,
+ * recomputed (inside the scan kernel on the tensor cores when D/16 divides
+ * 64, else by the contraction kernel), then dx = dx_scan + dlx W_x^T +
+ * dla W_a^T per block,
  * dW_x = x^T dlx, dW_a = x^T dla, db = sum over tokens of dl.  The gate
  * gradients and dx_scan enter the two tensor-core contractions (one for dx
  * with K = 6 D/16, one for dW with K = B L, split over the tokens and added in

@@ -381,13 +381,14 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const uint16_t* __restric
     }
     float kk[4][4], unused[4];
     load_k4(k, nullptr, D, q, kk, unused);
-    // st[i]: a segment starts at t0 - 3 + i (i < kConvRun + 6)
-    bool st[kConvRun + 6];
+    // bit i: a segment starts at t0 - 3 + i (i < kConvRun + 6)
+    uint32_t st = 0u;
+    if (reset != nullptr)
 #pragma unroll
-    for (int i = 0; i < kConvRun + 6; ++i) {
-        const int t = t0 - 3 + i;
-        st[i] = t >= 0 && t < L && reset != nullptr && reset[row0 + t] != 0;
-    }
+        for (int i = 0; i < kConvRun + 6; ++i) {
+            const int t = t0 - 3 + i;
+            if (t >= 0 && t < L && reset[row0 + t] != 0) st |= 1u << i;
+        }
     float c[5][4];
 #pragma unroll
     for (int j = 0; j < 5; ++j)
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const uint16_t* __restric
             bool reach = true;
 #pragma unroll
             for (int j = 1; j < 4; ++j) {
-                reach = reach && t + j < L && !st[r + 3 + j];
+                reach = reach && t + j < L && !((st >> (r + 3 + j)) & 1u);
                 if (reach)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[i] = fmaf(kk[j][i], du[r + j][i], acc[i]);
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const uint16_t* __restric
             bool live = true;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (j > 0) live = live && t - j >= 0 && !st[r + 3 - j + 1];
+                if (j > 0) live = live && t - j >= 0 && !((st >> (r + 4 - j)) & 1u);
                 if (live) {
                     float f[4];
                     unpack4(vr[r + 3 - j], f);

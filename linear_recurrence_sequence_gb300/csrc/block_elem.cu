@@ -157,34 +157,32 @@ __global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(const uint4* __restric
 
 // The same for W <= 1024 (more channels per lane would spill), one warp per row: lane l owns the 8-channel groups
 // l + 32 k (k < NK = W / 256) and keeps the row's x, dh and dres in registers
-// (3 NK independent 16-byte loads), the row mean is a warp sum, dgamma
-// accumulates per lane over the warp's rows.  The CTA's 8192 / W warps share
-// its contiguous row range; their dgamma rows are added in warp order through
-// shared memory into the CTA's partial row.
+// (3 NK independent 16-byte loads), the row mean is a warp sum.  gamma and
+// the per-warp dgamma rows live in shared memory (dgamma accumulates per
+// lane over the warp's rows there), which keeps two CTAs per SM; the CTA's
+// 8192 / W warps share its contiguous row range and their dgamma rows are
+// added in warp order into the CTA's partial row.
 template <int NK>
-__global__ void __launch_bounds__(256) rmsnorm_bwd_warp_kernel(const uint4* __restrict__ x,
-                                                               const float* __restrict__ gamma,
-                                                               const float* __restrict__ rstd,
-                                                               const uint4* __restrict__ dh,
-                                                               const uint4* __restrict__ dres, uint4* __restrict__ dx,
-                                                               float* __restrict__ dgamma_part, long long rows) {
+__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_warp_kernel(const uint4* __restrict__ x,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ rstd,
+                                                                  const uint4* __restrict__ dh,
+                                                                  const uint4* __restrict__ dres,
+                                                                  uint4* __restrict__ dx,
+                                                                  float* __restrict__ dgamma_part, long long rows) {
     constexpr int W = 256 * NK, nv = W / 8, WPC = 8192 / W > 8 ? 8 : 8192 / W;
-    __shared__ float red[WPC][W];
+    __shared__ __align__(16) float red[WPC][W];
+    __shared__ __align__(16) float s_g[W];
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long r0 = rows * blockIdx.x / gridDim.x, r1 = rows * (blockIdx.x + 1) / gridDim.x;
-    float gm[NK][8], dg[NK][8];
-#pragma unroll
-    for (int k = 0; k < NK; ++k) {
-        const int v = lane + 32 * k;
-        const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v);
-        const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v + 1);
-        gm[k][0] = g0.x; gm[k][1] = g0.y; gm[k][2] = g0.z; gm[k][3] = g0.w;
-        gm[k][4] = g1.x; gm[k][5] = g1.y; gm[k][6] = g1.z; gm[k][7] = g1.w;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dg[k][i] = 0.f;
-    }
+    for (int c = threadIdx.x; c < W; c += blockDim.x) s_g[c] = __ldg(gamma + c);
+    if (warp < WPC)
+        for (int c = lane; c < W; c += 32) red[warp][c] = 0.f;
+    __syncthreads();
+    float4* dgw = reinterpret_cast<float4*>(red[warp < WPC ? warp : 0]);
+    const float4* gw = reinterpret_cast<const float4*>(s_g);
     for (long long row = r0 + warp; row < r1; row += WPC) {
         uint4 qx[NK], qh[NK], qr[NK];
 #pragma unroll
@@ -198,36 +196,40 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_warp_kernel(const uint4* __re
         float part = 0.f;
 #pragma unroll
         for (int k = 0; k < NK; ++k) {
+            const int v = lane + 32 * k;
             float xv[8], hv[8];
             unpack8(qx[k], xv);
             unpack8(qh[k], hv);
+            const float4 g0 = gw[2 * v], g1 = gw[2 * v + 1];
+            const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float4 d0 = dgw[2 * v], d1 = dgw[2 * v + 1];
+            float dg[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float n = xv[i] * rs;
-                part = fmaf(hv[i] * gm[k][i], n, part);
-                dg[k][i] = fmaf(hv[i], n, dg[k][i]);
+                part = fmaf(hv[i] * gm[i], n, part);
+                dg[i] = fmaf(hv[i], n, dg[i]);
             }
+            dgw[2 * v] = make_float4(dg[0], dg[1], dg[2], dg[3]);
+            dgw[2 * v + 1] = make_float4(dg[4], dg[5], dg[6], dg[7]);
         }
         const float mean = warp_sum(part) / (float)W;
 #pragma unroll
         for (int k = 0; k < NK; ++k) {
+            const int v = lane + 32 * k;
             float xv[8], hv[8], rv[8], o[8];
             unpack8(qx[k], xv);
             unpack8(qh[k], hv);
             unpack8(qr[k], rv);
+            const float4 g0 = gw[2 * v], g1 = gw[2 * v + 1];
+            const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float n = xv[i] * rs;
-                o[i] = rv[i] + rs * (hv[i] * gm[k][i] - n * mean);
+                o[i] = rv[i] + rs * (hv[i] * gm[i] - n * mean);
             }
             dx[(size_t)row * nv + lane + 32 * k] = pack8(o);
         }
-    }
-    if (warp < WPC) {
-#pragma unroll
-        for (int k = 0; k < NK; ++k)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) red[warp][8 * (lane + 32 * k) + i] = dg[k][i];
     }
     __syncthreads();
     for (int c = threadIdx.x; c < W; c += blockDim.x) {
@@ -293,13 +295,14 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const uint16_t* __restric
         }
         float kk[4][4], bb[4];
         load_k4(k, kb, D, q, kk, bb);
-        // st[i]: a segment starts at t0 - 3 + i
-        bool st[kConvRun + 3];
+        // bit i: a segment starts at t0 - 3 + i
+        uint32_t st = 0u;
+        if (reset != nullptr)
 #pragma unroll
-        for (int i = 0; i < kConvRun + 3; ++i) {
-            const int t = t0 - 3 + i;
-            st[i] = t >= 0 && t < L && reset != nullptr && reset[row0 + t] != 0;
-        }
+            for (int i = 0; i < kConvRun + 3; ++i) {
+                const int t = t0 - 3 + i;
+                if (t >= 0 && t < L && reset[row0 + t] != 0) st |= 1u << i;
+            }
 #pragma unroll
         for (int r = 0; r < kConvRun; ++r) {
             const int t = t0 + r;
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const uint16_t* __restric
             bool live = true;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (j > 0) live = live && t - j >= 0 && !st[r + 3 - j + 1];
+                if (j > 0) live = live && t - j >= 0 && !((st >> (r + 4 - j)) & 1u);
                 if (live) {
                     float f[4];
                     unpack4(rows[r + 3 - j], f);
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const uint16_t* __restric
 // thread (run r, channel group g): channels 4 g .. 4 g + 3 of the span and
 // the run's tokens, with every row it needs loaded first (du rows t .. t + 3
 // and v rows t - 3 .. t of the run: 2 (kConvRun + 3) independent 8-byte
-// loads).  The k and bias contributions of the four runs are added in run
+// loads) and the run's segment starts as bits of one word.  The k and bias contributions of the four runs are added in run
 // order through shared memory: one partial row per tile, reduced in a fixed
 // order by sum_parts.  The mixer's status word is OR-ed into the block's
 // (thread 0 of CTA 0).

@@ -22,6 +22,7 @@
 // tensor-core contraction kernel or, in the forward, formed per tile on the
 // tensor cores inside the scan.
 #include <algorithm>
+#include <atomic>
 
 #include "kernels.cuh"
 #include "umma.cuh"
@@ -991,10 +992,15 @@ cudaError_t launch_rglru_proj_wimg(const void* w_x, const void* w_a, void* wimg,
 // Tickets go out in the order CTAs start, so a CTA only ever waits on tiles
 // held by CTAs already running: a grid larger than what is resident is slower,
 // never stuck.
-template <typename K>
+// (The count is asked once per device and logits mode.)
+template <int LM, typename K>
 unsigned rg_grid(K kernel, int smem, long long n_tiles) {
-    int dev = 0, sms = 1, per = 1;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    static std::atomic<long long> resident_cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    const long long cached = resident_cache[dev].load(std::memory_order_relaxed);
+    if (cached > 0) return (unsigned)(cached < n_tiles ? cached : (n_tiles > 0 ? n_tiles : 1));
+    int sms = 1, per = 1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kRgThreads, smem) != cudaSuccess || per < 1)
         per = 1;
@@ -1014,6 +1020,7 @@ unsigned rg_grid(K kernel, int smem, long long n_tiles) {
         if (fit > per) per = (int)fit;
     }
     const long long n = (long long)sms * per;
+    resident_cache[dev].store(n, std::memory_order_relaxed);
     return (unsigned)(n < n_tiles ? n : (n_tiles > 0 ? n_tiles : 1));
 }
 
@@ -1024,7 +1031,7 @@ cudaError_t launch_fwd(const CUtensorMap& tm_x, const CUtensorMap& tm_lx, const 
     const int smem = 2 * RgLogits<LM>::kSlotBytes + (LM == 2 ? kStageBytes : 0) + 1024;
     cudaError_t e = cudaFuncSetAttribute(rglru_scan_fwd_kernel<LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    rglru_scan_fwd_kernel<LM><<<rg_grid(rglru_scan_fwd_kernel<LM>, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
+    rglru_scan_fwd_kernel<LM><<<rg_grid<LM>(rglru_scan_fwd_kernel<LM>, smem, args.g.n_tiles), kRgThreads, smem, s>>>(
         tm_x, tm_lx, tm_la, args);
     return cudaGetLastError();
 }

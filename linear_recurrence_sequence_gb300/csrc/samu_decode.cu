@@ -28,6 +28,7 @@
 // the CTA.  Bandwidth-bound: per sequence 2D (x_sel) + 2D (w) + 2D (y) + 8D
 // (state read and written) bytes.
 #include <algorithm>
+#include <atomic>
 
 #include "kernels.cuh"
 
@@ -242,14 +243,24 @@ cudaError_t launch_samu_decode_prepare(const SamuDecodePrepArgs& args, cudaStrea
 // (at most the mode-pair groups of T, and 8); otherwise one.
 template <int T>
 cudaError_t launch_step(SamuDecodeStepArgs a, cudaStream_t s) {
-    int dev = 0, sms = 1, per = 1;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, samu_decode_step_kernel<T, true>, T, 0) != cudaSuccess ||
-        per < 1)
-        per = 1;
+    // resident CTAs per device, asked once per device (a decode step is one
+    // launch per token: no per-call queries)
+    static std::atomic<long long> resident_cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    long long resident = resident_cache[dev].load(std::memory_order_relaxed);
+    if (resident < 1) {
+        int sms = 1, per = 1;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, samu_decode_step_kernel<T, true>, T, 0) !=
+                cudaSuccess ||
+            per < 1)
+            per = 1;
+        resident = (long long)sms * per;
+        resident_cache[dev].store(resident, std::memory_order_relaxed);
+    }
     const long long groups = (a.D / 4 + T - 1) / T;   // groups of T mode pairs
-    const long long P = std::min<long long>({a.B > 0 ? (long long)sms * per / a.B : 1LL, groups, 8LL});
+    const long long P = std::min<long long>({a.B > 0 ? resident / a.B : 1LL, groups, 8LL});
     if (P >= 2) {
         a.parts = (int)P;
         samu_decode_step_kernel<T, true><<<(unsigned)(a.B * P), T, 0, s>>>(a);

@@ -397,8 +397,34 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const uint16_t* __restric
     for (int j = 0; j < 5; ++j)
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[j][i] = 0.f;
+    // a run whose window holds no segment start and no row edge: every tap
+    // counts (the same operations in the same order, without the tests)
+    const bool clean = st == 0u && t0 >= 3 && t0 + kConvRun + 3 <= L;
+    if (clean) {
 #pragma unroll
-    for (int r = 0; r < kConvRun; ++r) {
+        for (int r = 0; r < kConvRun; ++r) {
+            const int t = t0 + r;
+            float acc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = kk[0][i] * du[r][i];
+#pragma unroll
+            for (int j = 1; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = fmaf(kk[j][i], du[r + j][i], acc[i]);
+            *reinterpret_cast<uint2*>(dgv + (row0 + t) * 2 * D + D + 4 * q) = pack4(acc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float f[4];
+                unpack4(vr[r + 3 - j], f);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[j][i] = fmaf(du[r][i], f[i], c[j][i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[4][i] += du[r][i];
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kConvRun && !clean; ++r) {
         const int t = t0 + r;
         if (t < L) {
             float acc[4];
